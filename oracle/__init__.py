@@ -1,0 +1,256 @@
+"""CPU oracle for tile-based Gaussian splatting -- TEST INFRASTRUCTURE ONLY.
+
+Thin ctypes loader over `liboracle.so`, the plain single-threaded C++ statement of the
+method in `oracle.cpp`.  Only the test suite, the smoke check and the benchmark's
+CPU-baseline leg may import this package; the CUDA library never does, and this package
+never touches the CUDA library.  All arrays are numpy; inputs are passed as float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_HDR = os.path.join(_HERE, "oracle.h")
+_SO = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+AMB_NEAR, AMB_DET, AMB_RADIUS, AMB_SPAN, AMB_CLAMP = 1, 2, 4, 8, 16
+AMB_ALPHA_MIN, AMB_T_STOP, AMB_ALPHA_MAX = 1, 2, 4
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with g++ (no fast-math, no FMA contraction) if it is missing or stale."""
+    stale = (not os.path.exists(_SO) or
+             os.path.getmtime(_SO) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+    if force or stale:
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-Wall", "-o", tmp, _SRC])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class CCamera(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_double * 9), ("t", ctypes.c_double * 3),
+                ("fx", ctypes.c_double), ("fy", ctypes.c_double),
+                ("cx", ctypes.c_double), ("cy", ctypes.c_double),
+                ("width", ctypes.c_int32), ("height", ctypes.c_int32)]
+
+
+def _cam(cam) -> CCamera:
+    c = CCamera()
+    R = np.asarray(cam.R, np.float64).reshape(9)
+    t = np.asarray(cam.t, np.float64).reshape(3)
+    for i in range(9):
+        c.R[i] = float(R[i])
+    for i in range(3):
+        c.t[i] = float(t[i])
+    c.fx, c.fy, c.cx, c.cy = float(cam.fx), float(cam.fy), float(cam.cx), float(cam.cy)
+    c.width, c.height = int(cam.width), int(cam.height)
+    return c
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = ctypes.CDLL(_SO)
+        _lib.orc_exclusive_scan_u32.restype = ctypes.c_uint64
+        _lib.orc_bin_count.restype = ctypes.c_int64
+        _lib.orc_bin.restype = ctypes.c_int64
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _d(a):
+    return None if a is None else np.ascontiguousarray(a, np.float64)
+
+
+def project(cam, g, prec: int = 64, margin: float = 0.0):
+    """c1 + c6.  Returns dict of means2d [2,N], depth, conic [3,N], color [3,N], radius (int32),
+    rect [4,N] (x_lo, x_hi, y_lo, y_hi), tiles_touched (uint32), ambig (uint8)."""
+    n = g.n
+    out = dict(means2d=np.zeros((2, n)), depth=np.zeros(n), conic=np.zeros((3, n)),
+               color=np.zeros((3, n)), radius=np.zeros(n, np.int32), rect=np.zeros((4, n), np.int32),
+               tiles_touched=np.zeros(n, np.uint32), ambig=np.zeros(n, np.uint8))
+    c = _cam(cam)
+    ins = [_d(g.means), _d(g.scales), _d(g.quats), _d(g.opacity), _d(g.sh), _d(g.colors)]
+    rc = lib().orc_project(ctypes.c_int(prec), ctypes.byref(c), ctypes.c_int32(n),
+                           _p(ins[0]), _p(ins[1]), _p(ins[2]), _p(ins[3]), _p(ins[4]),
+                           ctypes.c_int32(g.sh_degree), _p(ins[5]),
+                           _p(out["means2d"]), _p(out["depth"]), _p(out["conic"]), _p(out["color"]),
+                           _p(out["radius"]), _p(out["rect"]), _p(out["tiles_touched"]),
+                           ctypes.c_double(margin), _p(out["ambig"]))
+    if rc != 0:
+        raise ValueError(f"orc_project returned {rc}")
+    return out
+
+
+def project_intermediates(cam, g):
+    n = g.n
+    cov3d, cov2d = np.zeros((6, n)), np.zeros((3, n))
+    jac, pcam = np.zeros((6, n)), np.zeros((3, n))
+    c = _cam(cam)
+    m, s, q = _d(g.means), _d(g.scales), _d(g.quats)
+    lib().orc_project_intermediates(ctypes.byref(c), ctypes.c_int32(n), _p(m), _p(s), _p(q),
+                                    _p(cov3d), _p(cov2d), _p(jac), _p(pcam))
+    return dict(cov3d=cov3d, cov2d=cov2d, jac=jac, pcam=pcam)
+
+
+def sh_basis(dirs):
+    dirs = _d(dirs)
+    m = dirs.shape[1]
+    Y = np.zeros((16, m))
+    lib().orc_sh_basis(_p(dirs), ctypes.c_int32(m), _p(Y))
+    return Y
+
+
+def exclusive_scan(values):
+    v = np.ascontiguousarray(values, np.uint32)
+    out = np.zeros(v.shape[0], np.uint64)
+    total = lib().orc_exclusive_scan_u32(_p(v), ctypes.c_int64(v.shape[0]), _p(out))
+    return out, int(total)
+
+
+def tile_ranges(keys_sorted, n_tiles):
+    k = np.ascontiguousarray(keys_sorted, np.uint64)
+    r = np.zeros((n_tiles, 2), np.uint32)
+    lib().orc_tile_ranges(_p(k), ctypes.c_int64(k.shape[0]), ctypes.c_int32(n_tiles), _p(r))
+    return r
+
+
+def bin(cam, means2d, depth, radius):
+    """c2 from float32 projected data.  Returns keys_sorted (uint64), point_list (uint32),
+    ranges [n_tiles,2] (uint32), tiles_touched (uint32)."""
+    m2 = np.ascontiguousarray(means2d, np.float32)
+    dp = np.ascontiguousarray(depth, np.float32)
+    rd = np.ascontiguousarray(radius, np.int32)
+    n = rd.shape[0]
+    c = _cam(cam)
+    E = lib().orc_bin_count(ctypes.byref(c), ctypes.c_int32(n), _p(m2), _p(rd))
+    keys = np.zeros(max(E, 1), np.uint64)
+    pl = np.zeros(max(E, 1), np.uint32)
+    n_tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
+    ranges = np.zeros((n_tiles, 2), np.uint32)
+    tt = np.zeros(n, np.uint32)
+    E2 = lib().orc_bin(ctypes.byref(c), ctypes.c_int32(n), _p(m2), _p(dp), _p(rd),
+                       ctypes.c_int64(E), _p(keys), _p(pl), _p(ranges), _p(tt))
+    assert E2 == E
+    return dict(keys_sorted=keys[:E], point_list=pl[:E], ranges=ranges, tiles_touched=tt,
+                n_entries=int(E))
+
+
+def raster_fwd(cam, means2d, conic, opacity, color, ranges, point_list, bg=(0.0, 0.0, 0.0),
+               prec: int = 64, margin: float = 0.0, tile_mask=None):
+    """c3.  Returns image [3,H,W], final_T [H,W], n_contrib [H,W] (uint32), ambig [H,W] (uint8)."""
+    n = int(np.asarray(opacity).shape[0])
+    H, W = cam.height, cam.width
+    image, final_T = np.zeros((3, H, W)), np.zeros((H, W))
+    n_contrib, ambig = np.zeros((H, W), np.uint32), np.zeros((H, W), np.uint8)
+    c = _cam(cam)
+    a = [_d(means2d), _d(conic), _d(opacity), _d(color)]
+    rg = np.ascontiguousarray(ranges, np.uint32)
+    pl = np.ascontiguousarray(point_list, np.uint32)
+    if pl.size == 0:
+        pl = np.zeros(1, np.uint32)
+    b = np.asarray(bg, np.float64)
+    tm = None if tile_mask is None else np.ascontiguousarray(tile_mask, np.uint8)
+    rc = lib().orc_raster_fwd(ctypes.c_int(prec), ctypes.byref(c), ctypes.c_int32(n), _p(a[0]),
+                              _p(a[1]), _p(a[2]), _p(a[3]), _p(rg), _p(pl), _p(b), _p(tm),
+                              _p(image), _p(final_T), _p(n_contrib), ctypes.c_double(margin),
+                              _p(ambig))
+    if rc != 0:
+        raise ValueError(f"orc_raster_fwd returned {rc}")
+    return dict(image=image, final_T=final_T, n_contrib=n_contrib, ambig=ambig)
+
+
+def raster_bwd(cam, means2d, conic, opacity, color, ranges, point_list, n_contrib, dL_dimage,
+               bg=(0.0, 0.0, 0.0), tile_mask=None):
+    """c4 in double.  Returns dmeans2d [2,N], dconic [3,N], dopacity [N], dcolor [3,N]."""
+    n = int(np.asarray(opacity).shape[0])
+    out = dict(dmeans2d=np.zeros((2, n)), dconic=np.zeros((3, n)), dopacity=np.zeros(n),
+               dcolor=np.zeros((3, n)))
+    c = _cam(cam)
+    a = [_d(means2d), _d(conic), _d(opacity), _d(color)]
+    rg = np.ascontiguousarray(ranges, np.uint32)
+    pl = np.ascontiguousarray(point_list, np.uint32)
+    if pl.size == 0:
+        pl = np.zeros(1, np.uint32)
+    nc = np.ascontiguousarray(n_contrib, np.uint32)
+    gi = _d(dL_dimage)
+    b = np.asarray(bg, np.float64)
+    tm = None if tile_mask is None else np.ascontiguousarray(tile_mask, np.uint8)
+    rc = lib().orc_raster_bwd(ctypes.byref(c), ctypes.c_int32(n), _p(a[0]), _p(a[1]), _p(a[2]),
+                              _p(a[3]), _p(rg), _p(pl), _p(b), _p(nc), _p(gi), _p(tm),
+                              _p(out["dmeans2d"]), _p(out["dconic"]), _p(out["dopacity"]),
+                              _p(out["dcolor"]))
+    if rc != 0:
+        raise ValueError(f"orc_raster_bwd returned {rc}")
+    return out
+
+
+def project_bwd(cam, g, radius, dmeans2d, dconic, dcolor):
+    """c5 in double.  Returns dmeans [3,N], dscales [3,N], dquats [4,N], dsh [3K,N] or None."""
+    n = g.n
+    K = (g.sh_degree + 1) ** 2 if g.sh_degree >= 0 else 0
+    out = dict(dmeans=np.zeros((3, n)), dscales=np.zeros((3, n)), dquats=np.zeros((4, n)),
+               dsh=np.zeros((3 * K, n)) if K else None)
+    c = _cam(cam)
+    m, s, q, sh = _d(g.means), _d(g.scales), _d(g.quats), _d(g.sh)
+    rd = None if radius is None else np.ascontiguousarray(radius, np.int32)
+    d2, dc, dcol = _d(dmeans2d), _d(dconic), _d(dcolor)
+    rc = lib().orc_project_bwd(ctypes.byref(c), ctypes.c_int32(n), _p(m), _p(s), _p(q), _p(sh),
+                               ctypes.c_int32(g.sh_degree), _p(rd), _p(d2), _p(dc), _p(dcol),
+                               _p(out["dmeans"]), _p(out["dscales"]), _p(out["dquats"]),
+                               _p(out["dsh"]))
+    if rc != 0:
+        raise ValueError(f"orc_project_bwd returned {rc}")
+    return out
+
+
+def appearance_fwd(cam, means, latents, W1, b1, W2, b2):
+    lat = _d(latents)
+    L, n = lat.shape
+    H = int(np.asarray(W1).shape[0])
+    colors = np.zeros((3, n))
+    c = _cam(cam)
+    args = [_d(means), lat, _d(W1), _d(b1), _d(W2), _d(b2)]
+    rc = lib().orc_appearance_fwd(ctypes.byref(c), ctypes.c_int32(n), ctypes.c_int32(L),
+                                  ctypes.c_int32(H), *[_p(a) for a in args], _p(colors))
+    if rc != 0:
+        raise ValueError(f"orc_appearance_fwd returned {rc}")
+    return colors
+
+
+def appearance_bwd(cam, means, latents, W1, b1, W2, b2, dcolors):
+    lat = _d(latents)
+    L, n = lat.shape
+    H = int(np.asarray(W1).shape[0])
+    out = dict(dlatents=np.zeros((L, n)), dW1=np.zeros((H, L + 3)), db1=np.zeros(H),
+               dW2=np.zeros((3, H)), db2=np.zeros(3))
+    c = _cam(cam)
+    args = [_d(means), lat, _d(W1), _d(b1), _d(W2), _d(b2), _d(dcolors)]
+    rc = lib().orc_appearance_bwd(ctypes.byref(c), ctypes.c_int32(n), ctypes.c_int32(L),
+                                  ctypes.c_int32(H), *[_p(a) for a in args],
+                                  _p(out["dlatents"]), _p(out["dW1"]), _p(out["db1"]),
+                                  _p(out["dW2"]), _p(out["db2"]))
+    if rc != 0:
+        raise ValueError(f"orc_appearance_bwd returned {rc}")
+    return out
+
+
+def render(cam, g, bg=(0.0, 0.0, 0.0), prec: int = 64):
+    """Convenience: oracle project (decisions in `prec`) -> bin -> forward compositing."""
+    P = project(cam, g, prec=prec)
+    B = bin(cam, P["means2d"].astype(np.float32), P["depth"].astype(np.float32), P["radius"])
+    F = raster_fwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"],
+                   B["point_list"], bg=bg, prec=prec)
+    return P, B, F

@@ -1,0 +1,123 @@
+/*
+ * Oracle for tile-based 3D Gaussian Splatting rasterisation -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU statement of what the GPU path computes, written from
+ * the method's description on the source pages (rigel README; "3D Gaussian Splatting
+ * ビューワを作る"; learn-gs notebook "11 - Tiles: the actual 3DGS design").  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it.  It shares no
+ * source, header, constant or helper with the CUDA library, and never calls it.
+ *
+ * Conventions (all arrays planar, one row per component, row stride n):
+ *   means [3][n], scales [3][n] (linear, already activated), quats [4][n] as (w,x,y,z), any norm,
+ *   opacity [n] (already activated), sh [3K][n] with row k*3+ch, K = (degree+1)^2,
+ *   colors [3][n] when sh_degree < 0.  Camera: p_cam = R * m + t, R row-major; pinhole fx,fy,cx,cy.
+ * Inputs are passed as double; the 32-bit variants round every input to float first and
+ * carry out every step in float, so that integer decisions (cull, radius, tile span,
+ * contributor counts) are taken in the precision of the GPU kernels.
+ *
+ * Parity status: every function here is pinned by the CPU test suite (closed forms, worked
+ * examples printed on the pages, invariants, brute force, library routines, finite
+ * differences).  None is "parity unpinned".
+ */
+#ifndef GS_ORACLE_H
+#define GS_ORACLE_H
+#include <stdint.h>
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct orc_camera {
+    double R[9];
+    double t[3];
+    double fx, fy, cx, cy;
+    int32_t width, height;
+} orc_camera;
+
+/* Projection flags (per Gaussian) for decisions that sit within `margin` of their threshold. */
+enum {
+    ORC_AMB_NEAR = 1,     /* camera-space z close to the near plane            */
+    ORC_AMB_DET = 2,      /* determinant of the dilated 2D covariance near 0    */
+    ORC_AMB_RADIUS = 4,   /* 3*sqrt(lambda_max) close to an integer              */
+    ORC_AMB_SPAN = 8,     /* (u +- r)/16 or (v +- r)/16 close to an integer      */
+    ORC_AMB_CLAMP = 16    /* |x/z| or |y/z| close to the 1.3x frustum limit      */
+};
+/* Rasterisation flags (per pixel). */
+enum {
+    ORC_AMB_ALPHA_MIN = 1, /* some alpha within margin of the 1/255 skip threshold */
+    ORC_AMB_T_STOP = 2,    /* transmittance within margin of the 1e-4 stop test    */
+    ORC_AMB_ALPHA_MAX = 4  /* opacity*G within margin of the 0.99 clamp            */
+};
+
+/* c1 + c6: projection and colour.  prec = 32 or 64.  Culled Gaussians get radius 0,
+ * tiles_touched 0 and zeros everywhere else.  rect = [x_lo, x_hi, y_lo, y_hi][n] in tiles.
+ * ambig may be NULL.  Returns 0, or -1 on a bad argument. */
+int orc_project(int prec, const orc_camera* cam, int32_t n, const double* means,
+                const double* scales, const double* quats, const double* opacity,
+                const double* sh, int32_t sh_degree, const double* colors,
+                double* means2d, double* depth, double* conic, double* color,
+                int32_t* radius, int32_t* rect, uint32_t* tiles_touched,
+                double margin, uint8_t* ambig);
+
+/* Intermediates of the projection in double, for the pins: cov3d [6][n] (xx,xy,xz,yy,yz,zz),
+ * cov2d [3][n] (a,b,c after the +0.3 dilation), jac [6][n] (J row-major 2x3, clamped),
+ * pcam [3][n]. */
+void orc_project_intermediates(const orc_camera* cam, int32_t n, const double* means,
+                               const double* scales, const double* quats, double* cov3d,
+                               double* cov2d, double* jac, double* pcam);
+
+/* c6: the 16 real SH basis functions at unit directions dirs [3][m] -> Y [16][m]. */
+void orc_sh_basis(const double* dirs, int32_t m, double* Y);
+
+/* c2 pieces. */
+uint64_t orc_exclusive_scan_u32(const uint32_t* in, int64_t n, uint64_t* out);
+void orc_tile_ranges(const uint64_t* keys_sorted, int64_t n_entries, int32_t n_tiles,
+                     uint32_t* ranges);
+/* Count the (Gaussian, tile) entries from projected float data (decisions in float). */
+int64_t orc_bin_count(const orc_camera* cam, int32_t n, const float* means2d,
+                      const int32_t* radius);
+/* Full binning: entries, stable sort, ranges.  keys_sorted/point_list hold `capacity`
+ * entries; returns the entry count, or -2 when it exceeds capacity (nothing written). */
+int64_t orc_bin(const orc_camera* cam, int32_t n, const float* means2d, const float* depth,
+                const int32_t* radius, int64_t capacity, uint64_t* keys_sorted,
+                uint32_t* point_list, uint32_t* ranges, uint32_t* tiles_touched);
+
+/* c3: forward compositing of every pixel in the tiles selected by tile_mask (NULL = all).
+ * Pixels of unselected tiles are left untouched. */
+int orc_raster_fwd(int prec, const orc_camera* cam, int32_t n, const double* means2d,
+                   const double* conic, const double* opacity, const double* color,
+                   const uint32_t* ranges, const uint32_t* point_list, const double* bg,
+                   const uint8_t* tile_mask, double* image, double* final_T,
+                   uint32_t* n_contrib, double margin, uint8_t* ambig);
+
+/* c4: backward of the compositing, in double.  Walk length per pixel is n_contrib (as given).
+ * Gradients are accumulated into zero-initialised outputs by this call. */
+int orc_raster_bwd(const orc_camera* cam, int32_t n, const double* means2d,
+                   const double* conic, const double* opacity, const double* color,
+                   const uint32_t* ranges, const uint32_t* point_list, const double* bg,
+                   const uint32_t* n_contrib, const double* dL_dimage,
+                   const uint8_t* tile_mask, double* dmeans2d, double* dconic,
+                   double* dopacity, double* dcolor);
+
+/* c5: backward of the projection and colour, in double.  Culled Gaussians (radius 0) get zero
+ * gradients.  dsh may be NULL when sh_degree < 0 (then dcolor is the colours' gradient). */
+int orc_project_bwd(const orc_camera* cam, int32_t n, const double* means,
+                    const double* scales, const double* quats, const double* sh,
+                    int32_t sh_degree, const int32_t* radius, const double* dmeans2d,
+                    const double* dconic, const double* dcolor, double* dmeans,
+                    double* dscales, double* dquats, double* dsh);
+
+/* c7: appearance MLP. x = [latent (L) ; unit view dir (3)], h = relu(W1 x + b1) (H wide),
+ * rgb = sigmoid(W2 h + b2).  latents [L][n]; W1 [H][L+3] row-major; W2 [3][H]. */
+int orc_appearance_fwd(const orc_camera* cam, int32_t n, int32_t L, int32_t H,
+                       const double* means, const double* latents, const double* W1,
+                       const double* b1, const double* W2, const double* b2, double* colors);
+int orc_appearance_bwd(const orc_camera* cam, int32_t n, int32_t L, int32_t H,
+                       const double* means, const double* latents, const double* W1,
+                       const double* b1, const double* W2, const double* b2,
+                       const double* dcolors, double* dlatents, double* dW1, double* db1,
+                       double* dW2, double* db2);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
