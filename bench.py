@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark of the tile-based Gaussian splatting path on GB300.
+
+One step = one forward + backward of one view through the five C-ABI calls (project, bin,
+rasterize fwd, rasterize bwd, project bwd) of the 160,000-Gaussian procedural scene at
+1920x1080, SH degree 3, cycling through a 60-view orbit (the rigel README's gallery scene and
+its 1920x1080 timing row).  Metric: fwd+bwd ms per frame and (Gaussian, tile) entries per
+second; the JSON line also carries the roofline fraction of the dominant kernel and of the
+whole step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) each rank renders its own views (view = rank + N*k mod 60) with no
+collective on the data path; timing is the max over ranks, `value` the entries of all ranks
+divided by that time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd ms/frame & entries/s, 160k Gaussians @1920x1080; % of roofline"
+UNIT = "entries/s"
+# rigel README header table, Tesla T4, 1920x1080: 2,154,540 entries, 4.60 + 34.12 ms
+T4_ENTRIES_PER_S = 2_154_540 / (4.60e-3 + 34.12e-3)
+WIDTH, HEIGHT, VIEWS = 1920, 1080, 60
+
+# GB300: 152 SMs, 128 FP32 lanes and 16 MUFU lanes per SM, 2070 MHz maximum SM clock.
+SMS, FP32_LANES, MUFU_LANES, MAX_MHZ = 152, 128, 16, 2070.0
+
+# Algorithmic work per unit (counted from the method's formulas, rigel README "Rasterization"
+# and "Backward"; one FP32 instruction = one op, FMA included):
+#   forward, per examined entry: dx, dy (2), quadratic form (5), o*G (1), min (1), skip test (1)
+#            = 10 ops + 1 ex2; per composited entry: a*T (1), colour (3), T update (1), stop test (1)
+#   backward, per examined entry: the same 10 ops + 1 ex2; per composited entry: 1-a (1),
+#            T/(1-a) (1 + 1 rcp), a*T (1), colour grads (3), dL/da (7), colour behind (6),
+#            clamp test (1), dL/do (1), dL/dpower (1), conic (6), mean (6), per-pixel sums (9)
+#            = 43 ops + 1 rcp.
+OPS_FWD_EXAMINED, OPS_FWD_BLEND = 10, 6
+OPS_BWD_EXAMINED, OPS_BWD_BLEND = 10, 43
+# bytes (algorithmic, moved once): see DESIGN.md "Roofline"
+B_PROJECT_PER_G = 236 + 44          # SH degree 3 inputs + means2d/depth/conic/colour/radius/tiles
+B_PROJECT_BWD_PER_G = 504
+B_FWD_PER_ENTRY, B_FWD_PER_PIXEL = 40, 20
+B_BWD_PER_ENTRY, B_BWD_PER_PIXEL, B_BWD_PER_G = 40 + 36, 20, 36
+OPS_PROJECT_PER_G, OPS_PROJECT_BWD_PER_G = 400, 1000
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed host logic
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def assign_views(rank: int, world: int, count: int, views: int = VIEWS, offset: int = 0):
+    """Views a rank renders, in order: rank + world * k (mod views)."""
+    return [(rank + world * (offset + k)) % views for k in range(count)]
+
+
+def reduce_timing(local_ms: float, local_entries: int, device=None):
+    """Max of the timed wall over ranks and the sum of entries (identity at world size 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_ms, local_entries
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    e = torch.tensor([float(local_entries)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(e, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(e.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return out
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        out.update(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                   reasons=reasons, samples=len(rows))
+        return out
+
+
+# ------------------------------------------------------------------ launches per step
+
+def scan_launches(n: int) -> int:
+    if n <= 0:
+        return 0
+    blocks = math.ceil(n / 2048)
+    return 1 if blocks == 1 else 2 + scan_launches(blocks)
+
+
+def launches_per_step(n: int, E: int, n_tiles: int) -> int:
+    """Kernels of this library one forward + backward launches (the D2H read is a copy)."""
+    tile_bits = max(0, math.ceil(math.log2(n_tiles))) if n_tiles > 1 else 0
+    passes = math.ceil((32 + tile_bits) / 8)
+    sort_blocks = math.ceil(E / 4096)
+    project = 1
+    binning = 1 + scan_launches(n) + (1 + passes * (2 + scan_launches(256 * sort_blocks)) + 1 if E else 0)
+    fwd = 1
+    bwd = 2 + 1
+    return project + binning + fwd + bwd
+
+
+# ------------------------------------------------------------------ our implementation
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from gaussian_splatting_tile_gb300 import pipeline, rs, scenes
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=device)
+
+    g = scenes.procedural_scene(seed=0)
+    cams = scenes.orbit_cameras(WIDTH, HEIGHT, VIEWS)
+    dg = rs.DeviceGaussians.from_numpy(g, device)
+    R = pipeline.Renderer(cams[0], g.n, device, capacity=4_000_000, keep_keys=False)
+    dL = torch.from_numpy(scenes.image_grad(cams[0])).to(device)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)  # > 126 MB L2
+    stream = torch.cuda.current_stream(device)
+
+    def step(view):
+        R.set_camera(cams[view])
+        R.forward(dg)
+        R.backward(dg, dL)
+
+    warm = assign_views(rank, world, args.warmup)
+    for v in warm:
+        step(v)
+    torch.cuda.synchronize(device)
+
+    views = assign_views(rank, world, args.steps, offset=args.warmup)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in views]
+    entries = []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for i, v in enumerate(views):
+        flush.fill_(float(i))  # evict the previous step's working set from L2 (not timed)
+        e = ev[i]
+        R.set_camera(cams[v])
+        e[0].record(stream)
+        R.project(dg)
+        e[1].record(stream)
+        E = R.bin()
+        e[2].record(stream)
+        R.rasterize()
+        e[3].record(stream)
+        R._grads(dg.sh_degree)
+        R.rasterize_backward(dL)
+        e[4].record(stream)
+        R.project_backward(dg)
+        e[5].record(stream)
+        entries.append(E)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    wall_ms = (time.perf_counter() - t_wall0) * 1e3
+    clk = clocks.stop()
+
+    stage = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(5)] for e in ev])  # ms
+    step_ms = stage.sum(axis=1)
+    local_ms = float(step_ms.sum())
+    tot_ms, tot_entries = reduce_timing(local_ms, int(sum(entries)), device)
+    ms_per_step = tot_ms / len(views)
+    fwd_ms = float(stage[:, 0:3].sum(axis=1).mean())
+    bwd_ms = float(stage[:, 3:5].sum(axis=1).mean())
+    value = tot_entries / (tot_ms * 1e-3)
+
+    # work counts of the timed views, measured after the timed region
+    Qs = []
+    for v in sorted(set(views)):
+        R.set_camera(cams[v])
+        R.forward(dg)
+        Qs.append(float(R.n_contrib.to(torch.int64).sum().item()))
+    Q = statistics.mean(Qs)
+    E_mean = statistics.mean(entries)
+
+    result = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=len(views),
+                  warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True,
+                  scaling="weak", vs_baseline=value / T4_ENTRIES_PER_S, dtype="f32",
+                  data="synthetic (seeded procedural scene; no dataset)",
+                  config=dict(workload="160k Gaussians (sphere shell 100k + helix 30k + checkered plane "
+                                       "30k), SH degree 3, 1920x1080, 60-view orbit at radius 4.3, "
+                                       "50-degree vertical FOV; fwd+bwd per view",
+                              n_gaussians=g.n, width=WIDTH, height=HEIGHT, views=VIEWS,
+                              l2="256 MB buffer written before every timed step (not timed)",
+                              timing="CUDA events around each stage on the launching stream"),
+                  fwd_ms=fwd_ms, bwd_ms=bwd_ms, wall_ms_timed_region=wall_ms,
+                  stage_ms=dict(zip(["project", "bin", "rasterize_fwd", "rasterize_bwd", "project_bwd"],
+                                    [float(x) for x in stage.mean(axis=0)])),
+                  entries_per_frame=E_mean, examined_per_frame=Q,
+                  clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"]),
+                  gpu_launches=sum(launches_per_step(g.n, E, cams[0].n_tiles) for E in entries))
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(g, cams[views[0]])
+        result["cpu_baseline"] = cpu
+    blend_ratio = result.get("cpu_baseline", {}).get("blend_ratio")
+    result["roofline"], result["roofline_step"] = roofline(result, Q, E_mean, g.n, cams[0], blend_ratio)
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(g, cams, rank, world, args, device)
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def roofline(res, Q, E, n, cam, blend_ratio):
+    """Dominant kernel (compositing backward) against the FP32 pipe, and the whole step against
+    the sum of per-stage roofline times."""
+    hbm_gbs, src = measured_peaks()
+    fp32 = SMS * FP32_LANES * MAX_MHZ * 1e6   # lane ops/s
+    mufu = SMS * MUFU_LANES * MAX_MHZ * 1e6
+    bw = hbm_gbs * 1e9
+    r = blend_ratio if blend_ratio is not None else 0.0
+    Qb = Q * r
+    HW = cam.width * cam.height
+    ops_bwd = Q * OPS_BWD_EXAMINED + Qb * OPS_BWD_BLEND
+    t_bwd = res["stage_ms"]["rasterize_bwd"] * 1e-3
+    dominant = dict(kernel="rasterize_bwd (k_zero4 + k_raster_bwd)", bound="alu",
+                    achieved=ops_bwd / t_bwd / 1e12, peak=fp32 / 1e12, unit="Tops/s",
+                    frac=(ops_bwd / t_bwd) / fp32, traffic=None,
+                    peak_source=f"152 SMs x 128 FP32 lanes x {MAX_MHZ:.0f} MHz (max SM clock)",
+                    ops_per_launch=ops_bwd, composited_fraction=r,
+                    composited_fraction_source="oracle on the timed view" if blend_ratio is not None else "unknown: counted as 0")
+    t = {}
+    t["project"] = max(n * B_PROJECT_PER_G / bw, n * OPS_PROJECT_PER_G / fp32)
+    p = math.ceil((32 + math.ceil(math.log2(cam.n_tiles))) / 8)
+    t["bin"] = (n * 28 + E * (12 + 24 * p + 8) + cam.n_tiles * 8) / bw
+    t["rasterize_fwd"] = max((E * B_FWD_PER_ENTRY + HW * B_FWD_PER_PIXEL) / bw,
+                             (Q * OPS_FWD_EXAMINED + Qb * OPS_FWD_BLEND) / fp32, Q / mufu)
+    t["rasterize_bwd"] = max((E * B_BWD_PER_ENTRY + HW * B_BWD_PER_PIXEL + n * B_BWD_PER_G) / bw,
+                             ops_bwd / fp32, (Q + Qb) / mufu)
+    t["project_bwd"] = max(n * B_PROJECT_BWD_PER_G / bw, n * OPS_PROJECT_BWD_PER_G / fp32)
+    t_roof = sum(t.values())
+    measured = res["ms_per_step"] * 1e-3
+    step = dict(roofline_ms=t_roof * 1e3, measured_ms=res["ms_per_step"], frac=t_roof / measured,
+                per_stage_roofline_ms={k: v * 1e3 for k, v in t.items()},
+                hbm_gbs=hbm_gbs, hbm_source=src, fp32_tops=fp32 / 1e12, mufu_tops=mufu / 1e12)
+    return dominant, step
+
+
+def run_e2e(g, cams, rank, world, args, device):
+    """Same metric through the public API with host buffers: every step copies the Gaussian
+    parameters and dL/dimage from pinned host memory to the device and reads the per-Gaussian
+    gradients back into pinned host memory."""
+    import numpy as np
+    import torch
+
+    from gaussian_splatting_tile_gb300 import pipeline, rs, scenes
+
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).pin_memory()
+    host = dict(means=pin(g.means), scales=pin(g.scales), quats=pin(g.quats), opacity=pin(g.opacity),
+                sh=pin(g.sh))
+    hdL = pin(scenes.image_grad(cams[0]))
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    ddL = torch.empty_like(hdL, device=device)
+    dg = rs.DeviceGaussians(dev["means"], dev["scales"], dev["quats"], dev["opacity"], dev["sh"], g.sh_degree)
+    R = pipeline.Renderer(cams[0], g.n, device, capacity=4_000_000, keep_keys=False)
+    R._grads(g.sh_degree)
+    out_names = ("dmeans", "dscales", "dquats", "dopacity", "dsh")
+    hout = {k: torch.empty(tuple(getattr(R.grads, k).shape), dtype=torch.float32).pin_memory() for k in out_names}
+    h2d = sum(v.numel() * 4 for v in host.values()) + hdL.numel() * 4
+    d2h = sum(v.numel() * 4 for v in hout.values())
+
+    def step(view):
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        ddL.copy_(hdL, non_blocking=True)
+        R.set_camera(cams[view])
+        R.forward(dg)
+        B = R.backward(dg, ddL)
+        for k in out_names:
+            hout[k].copy_(getattr(B, k), non_blocking=True)
+        torch.cuda.current_stream(device).synchronize()
+        return R.n_entries
+
+    for v in assign_views(rank, world, args.warmup):
+        step(v)
+    views = assign_views(rank, world, args.steps, offset=args.warmup)
+    t0 = time.perf_counter()
+    ents = sum(step(v) for v in views)
+    local_ms = (time.perf_counter() - t0) * 1e3
+    tot_ms, tot_e = reduce_timing(local_ms, ents, device)
+    return dict(value=tot_e / (tot_ms * 1e-3), unit=UNIT, h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                ms_per_step=tot_ms / len(views))
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline)
+
+def oracle_frame(g, cam, tile_fraction: float = 1.0, seed: int = 0):
+    """The oracle as it stands (single-threaded C++), one view: projection, binning, then
+    compositing forward and backward over a fraction of the tiles, projection backward.
+    Returns (seconds scaled to a full frame, entries, composited/examined ratio, detail)."""
+    import numpy as np
+
+    import oracle
+    from gaussian_splatting_tile_gb300 import scenes
+
+    t0 = time.perf_counter()
+    P = oracle.project(cam, g, prec=64)
+    t1 = time.perf_counter()
+    B = oracle.bin(cam, P["means2d"].astype(np.float32), P["depth"].astype(np.float32), P["radius"])
+    t2 = time.perf_counter()
+    tm = None
+    sample_entries = B["n_entries"]
+    if tile_fraction < 1.0:
+        rng = np.random.default_rng(seed)
+        tm = np.zeros(cam.n_tiles, np.uint8)
+        tm[rng.choice(cam.n_tiles, max(1, int(tile_fraction * cam.n_tiles)), replace=False)] = 1
+        r = B["ranges"].astype(np.int64)
+        sample_entries = int((r[:, 1] - r[:, 0])[tm.astype(bool)].sum())
+    F = oracle.raster_fwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"],
+                          B["point_list"], tile_mask=tm)
+    t3 = time.perf_counter()
+    O = oracle.raster_bwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"],
+                          B["point_list"], F["n_contrib"], scenes.image_grad(cam), tile_mask=tm)
+    t4 = time.perf_counter()
+    oracle.project_bwd(cam, g, P["radius"], O["dmeans2d"], O["dconic"], O["dcolor"])
+    t5 = time.perf_counter()
+    scale = B["n_entries"] / max(sample_entries, 1)
+    frame_s = (t1 - t0) + (t2 - t1) + (t3 - t2 + t4 - t3) * scale + (t5 - t4)
+    ratio = float(F["n_blend"].sum()) / max(float(F["n_contrib"].sum()), 1.0)
+    return frame_s, B["n_entries"], ratio, dict(project=t1 - t0, bin=t2 - t1, rasterize_fwd=t3 - t2,
+                                                rasterize_bwd=t4 - t3, project_bwd=t5 - t4,
+                                                sampled_entries=sample_entries)
+
+
+def cpu_baseline(g, cam):
+    frame_s, E, ratio, d = oracle_frame(g, cam, 1.0)
+    return dict(value=E / frame_s, unit=UNIT, cores=1, kind="oracle",
+                sample="one full 1920x1080 view (all tiles) of the 160k scene: projection, binning, "
+                       "compositing forward and backward, projection backward, single thread, float64",
+                ms_per_frame=frame_s * 1e3, blend_ratio=ratio,
+                stage_s={k: v for k, v in d.items() if k != "sampled_entries"},
+                host_cpus=os.cpu_count())
+
+
+def run_reference(args):
+    """The oracle as the reference arm: every step is one view at a bounded sample (a quarter of
+    the tiles for the compositing passes, the whole view for projection and binning)."""
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    from gaussian_splatting_tile_gb300 import scenes
+    g = scenes.procedural_scene(seed=0)
+    cams = scenes.orbit_cameras(WIDTH, HEIGHT, VIEWS)
+    for v in assign_views(0, 1, args.warmup):
+        oracle_frame(g, cams[v], 0.25, seed=v)
+    tot_s, tot_e = 0.0, 0
+    t0 = time.perf_counter()
+    for v in assign_views(0, 1, args.steps, offset=args.warmup):
+        s, E, _, _ = oracle_frame(g, cams[v], 0.25, seed=v)
+        tot_s += s
+        tot_e += E
+    wall = time.perf_counter() - t0
+    value = tot_e / tot_s
+    res = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+               warmup=args.warmup, ms_per_step=tot_s / args.steps * 1e3, higher_is_better=True,
+               scaling="weak", vs_baseline=value / T4_ENTRIES_PER_S, dtype="f64",
+               data="synthetic (seeded procedural scene; no dataset)", impl="reference",
+               config=dict(workload="160k Gaussians, SH degree 3, 1920x1080, 60-view orbit; fwd+bwd per view",
+                           n_gaussians=g.n, width=WIDTH, height=HEIGHT, views=VIEWS),
+               cpu_baseline=dict(value=value, unit=UNIT, cores=1, kind="oracle",
+                                 sample="per step one view: projection and binning in full, compositing "
+                                        "forward/backward on 25% of the tiles scaled by entries"),
+               e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+               wall_s=wall)
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+// The C ABI of include/rs.h: argument validation, then the kernel launchers.  No device memory
+// is allocated here; rs_bin performs the path's single device-to-host read (the entry count).
+#include <stdint.h>
+
+#include "rs_internal.cuh"
+
+namespace {
+
+using rs::CameraF;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool camera_ok(const rs_camera* c) {
+    if (!c) return false;
+    if (c->width < 1 || c->height < 1 || c->width > 32768 || c->height > 32768) return false;
+    if (!(c->fx > 0.f) || !(c->fy > 0.f)) return false;
+    const float v[] = {c->fx, c->fy, c->cx, c->cy};
+    for (float x : v)
+        if (!isfinite(x)) return false;
+    for (int i = 0; i < 9; ++i)
+        if (!isfinite(c->R[i])) return false;
+    for (int i = 0; i < 3; ++i)
+        if (!isfinite(c->t[i])) return false;
+    return true;
+}
+
+bool n_ok(int32_t n) { return n >= 0 && n <= RS_MAX_GAUSSIANS; }
+
+bool dev_f(const void* p) { return p && aligned(p, 4); }
+
+bool gaussians_ok(const rs_gaussians* g) {
+    if (!g || !n_ok(g->n)) return false;
+    if (g->sh_degree < -1 || g->sh_degree > 3) return false;
+    if (g->n == 0) return true;
+    if (!dev_f(g->d_means) || !dev_f(g->d_scales) || !dev_f(g->d_quats) || !dev_f(g->d_opacity))
+        return false;
+    if (g->sh_degree >= 0 ? !dev_f(g->d_sh) : !dev_f(g->d_colors)) return false;
+    return true;
+}
+
+bool projected_ok(const rs_projected* p, bool need_records) {
+    if (!p) return false;
+    if (!dev_f(p->d_means2d) || !dev_f(p->d_depth) || !dev_f(p->d_conic) || !dev_f(p->d_color) ||
+        !dev_f(p->d_radius) || !dev_f(p->d_tiles_touched))
+        return false;
+    if (need_records && !(p->d_records && aligned(p->d_records, 16))) return false;
+    return true;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RS_OK : RS_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* rs_error_string(int code) {
+    switch (code) {
+        case RS_OK: return "success";
+        case RS_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size or parameter)";
+        case RS_ERR_CAPACITY: return "entry count exceeds capacity; *n_entries holds the required count";
+        case RS_ERR_WORKSPACE: return "workspace smaller than rs_bin_workspace_size reports";
+        case RS_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown error code";
+    }
+}
+
+int rs_project(const rs_camera* camera, const rs_gaussians* gaussians, const rs_projected* out,
+               void* stream) {
+    if (!camera_ok(camera) || !gaussians_ok(gaussians)) return RS_ERR_INVALID_ARG;
+    if (gaussians->n == 0) return RS_OK;
+    if (!projected_ok(out, true)) return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    return cuda_rc(rs::launch_project(cam, *gaussians, *out, static_cast<cudaStream_t>(stream)));
+}
+
+int rs_bin_workspace_size(int32_t n, const rs_camera* camera, size_t capacity, size_t* bytes) {
+    if (!camera_ok(camera) || !n_ok(n) || !bytes || capacity > size_t(UINT32_MAX))
+        return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    *bytes = rs::plan_bin(n, cam, capacity).total_bytes;
+    return RS_OK;
+}
+
+int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
+           size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
+           uint32_t* d_point_list, uint32_t* d_tile_ranges, size_t* n_entries, void* stream) {
+    if (!camera_ok(camera) || !n_ok(n) || !n_entries || capacity > size_t(UINT32_MAX))
+        return RS_ERR_INVALID_ARG;
+    if (!d_tile_ranges || !aligned(d_tile_ranges, 8)) return RS_ERR_INVALID_ARG;
+    if (!d_workspace || !aligned(d_workspace, 256)) return RS_ERR_INVALID_ARG;
+    if (n > 0 && !projected_ok(proj, false)) return RS_ERR_INVALID_ARG;
+    if (capacity > 0 && (!d_point_list || !aligned(d_point_list, 4))) return RS_ERR_INVALID_ARG;
+    if (d_keys_sorted && !aligned(d_keys_sorted, 8)) return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    const rs::BinPlan plan = rs::plan_bin(n, cam, capacity);
+    if (workspace_bytes < plan.total_bytes) return RS_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    rs_projected empty{};
+    const rs_projected& p = proj ? *proj : empty;
+    cudaError_t e = rs::launch_bin_scan(plan, cam, p, ws, d_tile_ranges, s);
+    if (e != cudaSuccess) return RS_ERR_CUDA;
+    // the path's one device-to-host read: the number of entries
+    uint64_t E = 0;
+    e = cudaMemcpyAsync(&E, ws + plan.off_total, sizeof(E), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return RS_ERR_CUDA;
+    *n_entries = size_t(E);
+    if (E > uint64_t(capacity)) return RS_ERR_CAPACITY;
+    return cuda_rc(rs::launch_bin_sort(plan, cam, p, ws, E, d_keys_sorted, d_point_list,
+                                       d_tile_ranges, s));
+}
+
+int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
+                     float* d_image, float* d_final_T, uint32_t* d_n_contrib, void* stream) {
+    if (!camera_ok(camera) || !n_ok(n) || !bg) return RS_ERR_INVALID_ARG;
+    if (!dev_f(d_image) || !dev_f(d_final_T) || !dev_f(d_n_contrib)) return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    const float3 b = make_float3(bg[0], bg[1], bg[2]);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n == 0) return cuda_rc(rs::launch_fill_background(cam, b, d_image, d_final_T, d_n_contrib, s));
+    if (!proj || !proj->d_records || !aligned(proj->d_records, 16)) return RS_ERR_INVALID_ARG;
+    if (!d_tile_ranges || !aligned(d_tile_ranges, 8) || !dev_f(d_point_list)) return RS_ERR_INVALID_ARG;
+    return cuda_rc(rs::launch_raster_fwd(cam, static_cast<const rs::Record*>(proj->d_records),
+                                         d_tile_ranges, d_point_list, b, d_image, d_final_T,
+                                         d_n_contrib, s));
+}
+
+int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
+                     const float* d_final_T, const uint32_t* d_n_contrib,
+                     const float* d_dL_dimage, float* d_dL_dmeans2d, float* d_dL_dconic,
+                     float* d_dL_dopacity, float* d_dL_dcolor, void* stream) {
+    if (!camera_ok(camera) || !n_ok(n) || !bg) return RS_ERR_INVALID_ARG;
+    if (n == 0) return RS_OK;
+    if (!proj || !proj->d_records || !aligned(proj->d_records, 16)) return RS_ERR_INVALID_ARG;
+    if (!d_tile_ranges || !aligned(d_tile_ranges, 8) || !dev_f(d_point_list)) return RS_ERR_INVALID_ARG;
+    if (!dev_f(d_final_T) || !dev_f(d_n_contrib) || !dev_f(d_dL_dimage)) return RS_ERR_INVALID_ARG;
+    if (!dev_f(d_dL_dmeans2d) || !dev_f(d_dL_dconic) || !dev_f(d_dL_dopacity) || !dev_f(d_dL_dcolor))
+        return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (rs::launch_zero_grads(d_dL_dmeans2d, d_dL_dconic, d_dL_dopacity, d_dL_dcolor, size_t(n), s) !=
+        cudaSuccess)
+        return RS_ERR_CUDA;
+    const float3 b = make_float3(bg[0], bg[1], bg[2]);
+    return cuda_rc(rs::launch_raster_bwd(cam, n, static_cast<const rs::Record*>(proj->d_records),
+                                         d_tile_ranges, d_point_list, b, d_final_T, d_n_contrib,
+                                         d_dL_dimage, d_dL_dmeans2d, d_dL_dconic, d_dL_dopacity,
+                                         d_dL_dcolor, s));
+}
+
+int rs_project_bwd(const rs_camera* camera, const rs_gaussians* gaussians,
+                   const rs_projected* proj, const float* d_dL_dmeans2d,
+                   const float* d_dL_dconic, const float* d_dL_dcolor, float* d_dL_dmeans,
+                   float* d_dL_dscales, float* d_dL_dquats, float* d_dL_dsh, void* stream) {
+    if (!camera_ok(camera) || !gaussians_ok(gaussians)) return RS_ERR_INVALID_ARG;
+    if (gaussians->n == 0) return RS_OK;
+    if (!proj || !dev_f(proj->d_radius)) return RS_ERR_INVALID_ARG;
+    if (!dev_f(d_dL_dmeans2d) || !dev_f(d_dL_dconic) || !dev_f(d_dL_dcolor)) return RS_ERR_INVALID_ARG;
+    if (!dev_f(d_dL_dmeans) || !dev_f(d_dL_dscales) || !dev_f(d_dL_dquats)) return RS_ERR_INVALID_ARG;
+    if (gaussians->sh_degree >= 0 && !dev_f(d_dL_dsh)) return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    return cuda_rc(rs::launch_project_bwd(cam, *gaussians, *proj, d_dL_dmeans2d, d_dL_dconic,
+                                          d_dL_dcolor, d_dL_dmeans, d_dL_dscales, d_dL_dquats,
+                                          d_dL_dsh, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// Internal declarations of the sm_103a rasteriser library: constants of the method, the packed
+// per-Gaussian record and the kernel launchers behind the C ABI in include/rs.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "rs.h"
+
+namespace rs {
+
+// Constants of the method (rigel README "Projection", "Rasterization"; learn-gs "11 - Tiles",
+// constants cell).
+constexpr int kTile = RS_TILE;
+constexpr int kTilePixels = kTile * kTile;
+constexpr float kDilation = 0.3f;      // EWA low-pass added to the 2D covariance diagonal
+constexpr float kZNear = 0.05f;        // near-plane cull
+constexpr float kClampFrac = 1.3f;     // x/z, y/z clamp, in units of the frustum half-width
+constexpr float kLambdaFloor = 0.1f;   // floor on the eigenvalue discriminant
+constexpr float kAlphaMax = 0.99f;
+constexpr float kAlphaMin = 1.0f / 255.0f;
+constexpr float kTStop = 1e-4f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Packed record the projection writes once per Gaussian and both rasterisers gather per list
+// entry.  Three 16-byte words:
+//   p = (u, v, opacity, A)        position, opacity, raw conic A
+//   q = (qa, qb, qc, B)           power in log2 units: power2 = qa dx^2 + qb dx dy + qc dy^2
+//                                 with qa = -A/2 log2(e), qb = -B log2(e), qc = -C/2 log2(e)
+//   c = (r, g, b, C)              colour, raw conic C
+// Storing the log2-scaled quadratic lets the rasterisers evaluate exp(power) as one ex2 on the
+// multi-function unit; forward and backward read the same words, so both evaluate alpha with
+// bit-identical arithmetic.
+struct __align__(16) Record {
+    float4 p;
+    float4 q;
+    float4 c;
+};
+static_assert(sizeof(Record) == RS_RECORD_BYTES, "record size");
+
+struct CameraF {
+    float R[9];
+    float t[3];
+    float fx, fy, cx, cy;
+    int W, H;
+    int TX, TY;
+};
+
+inline CameraF make_camera(const rs_camera& c) {
+    CameraF o;
+    for (int i = 0; i < 9; ++i) o.R[i] = c.R[i];
+    for (int i = 0; i < 3; ++i) o.t[i] = c.t[i];
+    o.fx = c.fx; o.fy = c.fy; o.cx = c.cx; o.cy = c.cy;
+    o.W = c.width; o.H = c.height;
+    o.TX = (c.width + kTile - 1) / kTile;
+    o.TY = (c.height + kTile - 1) / kTile;
+    return o;
+}
+
+// ex2.approx.ftz: the multi-function unit's base-2 exponential (PTX ISA), relative error about
+// 2^-22; arguments below -126 give 0, which the alpha threshold then skips.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// alpha of one list entry at pixel (px, py), shared by the forward and the backward so both
+// take identical skip, clamp and stop decisions (rigel README "Rasterization":
+// alpha = min(0.99, opacity exp(power)), power = -1/2 (A dx^2 + C dy^2) - B dx dy, here in log2
+// units).  Returns alpha; `G` = exp(power), `raw` = opacity * G before the clamp.
+__device__ __forceinline__ float entry_alpha(const float4& p, const float4& q, float px, float py,
+                                             float& dx, float& dy, float& G, float& raw) {
+    dx = px - p.x;
+    dy = py - p.y;
+    const float power2 = fmaf(dx, fmaf(q.x, dx, q.y * dy), (q.z * dy) * dy);
+    G = ex2_approx(power2);
+    raw = p.z * G;
+    return fminf(kAlphaMax, raw);
+}
+
+// Tile span bound of a splat's bounding square (learn-gs "11 - Tiles", tile_spans):
+// floor((p - r) / 16) for the lower bound, floor((p + r) / 16) + 1 for the upper, clamped to
+// [0, n_tiles] in float before the conversion so any finite or infinite p is safe.  The
+// projection (tiles_touched) and the expansion (keys) both call this, so they always agree.
+__device__ __forceinline__ int span_bound(float p, float r, int n_tiles, bool upper) {
+    float f = floorf((upper ? p + r : p - r) * (1.0f / kTile));
+    if (upper) f += 1.0f;
+    f = fminf(fmaxf(f, 0.0f), float(n_tiles));
+    return int(f);
+}
+
+// Launchers (each returns the cudaError_t of its launches).
+cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_projected& out,
+                           cudaStream_t s);
+cudaError_t launch_project_bwd(const CameraF& cam, const rs_gaussians& g, const rs_projected& p,
+                               const float* dm2, const float* dcon, const float* dcol,
+                               float* dmeans, float* dscales, float* dquats, float* dsh,
+                               cudaStream_t s);
+
+struct BinPlan {
+    int32_t n;
+    int n_tiles;
+    int key_bits;          // 32 + ceil(log2(n_tiles))
+    int passes;            // ceil(key_bits / 8)
+    size_t capacity;
+    // workspace layout (byte offsets)
+    size_t off_offsets, off_scan_tmp, off_keys, off_vals, off_keys2, off_vals2, off_hist,
+        off_hist_tmp, off_total, total_bytes;
+    size_t scan_tmp_elems, hist_tmp_elems;
+};
+BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity);
+// Scan tiles_touched into offsets and leave the total on the device at ws + off_total.
+cudaError_t launch_bin_scan(const BinPlan& plan, const CameraF& cam, const rs_projected& p,
+                            uint8_t* ws, uint32_t* tile_ranges, cudaStream_t s);
+// Expand, sort and extract ranges for `E` entries.
+cudaError_t launch_bin_sort(const BinPlan& plan, const CameraF& cam, const rs_projected& p,
+                            uint8_t* ws, uint64_t E, uint64_t* keys_out, uint32_t* point_list,
+                            uint32_t* tile_ranges, cudaStream_t s);
+
+cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
+                              const uint32_t* list, float3 bg, float* image, float* final_T,
+                              uint32_t* n_contrib, cudaStream_t s);
+cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
+                              const uint32_t* ranges, const uint32_t* list, float3 bg,
+                              const float* final_T, const uint32_t* n_contrib,
+                              const float* dL_dimage, float* dm2, float* dcon, float* dop,
+                              float* dcol, cudaStream_t s);
+// Fill a background image (n = 0 or no entries): image = bg, final_T = 1, n_contrib = 0.
+cudaError_t launch_fill_background(const CameraF& cam, float3 bg, float* image, float* final_T,
+                                   uint32_t* n_contrib, cudaStream_t s);
+cudaError_t launch_zero_grads(float* dm2, float* dcon, float* dop, float* dcol, size_t n,
+                              cudaStream_t s);
+
+}  // namespace rs

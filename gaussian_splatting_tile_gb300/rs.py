@@ -1,0 +1,285 @@
+"""Thin Python binding of the C ABI in include/rs.h (librs.so), with the same names.
+
+Argument marshalling only: torch tensors are checked (device, dtype, contiguity, shape) and
+their device pointers and the current CUDA stream are handed to the library; every step of the
+rasteriser runs in the library's kernels.  There is no fallback: if librs.so is missing or the
+GPU is unavailable, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import re
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "librs.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "rs.h")
+
+RS_OK, RS_ERR_INVALID_ARG, RS_ERR_CAPACITY, RS_ERR_WORKSPACE, RS_ERR_CUDA = 0, -1, -2, -3, -4
+RECORD_BYTES = 48
+TILE = 16
+
+
+class RsError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed with {code}: {msg}")
+        self.code = code
+
+
+class rs_camera(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_float * 9), ("t", ctypes.c_float * 3),
+                ("fx", ctypes.c_float), ("fy", ctypes.c_float),
+                ("cx", ctypes.c_float), ("cy", ctypes.c_float),
+                ("width", ctypes.c_int32), ("height", ctypes.c_int32)]
+
+
+class rs_gaussians(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("d_means", ctypes.c_void_p), ("d_scales", ctypes.c_void_p),
+                ("d_quats", ctypes.c_void_p), ("d_opacity", ctypes.c_void_p),
+                ("d_sh", ctypes.c_void_p), ("sh_degree", ctypes.c_int32),
+                ("d_colors", ctypes.c_void_p)]
+
+
+class rs_projected(ctypes.Structure):
+    _fields_ = [("d_means2d", ctypes.c_void_p), ("d_depth", ctypes.c_void_p),
+                ("d_conic", ctypes.c_void_p), ("d_color", ctypes.c_void_p),
+                ("d_radius", ctypes.c_void_p), ("d_tiles_touched", ctypes.c_void_p),
+                ("d_records", ctypes.c_void_p)]
+
+
+_lib = None
+_VP = ctypes.c_void_p
+
+
+def declared_symbols(header: str = HEADER):
+    """Names of the entry points include/rs.h declares."""
+    text = open(header).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*|size_t)\s+(rs_\w+)\s*\(", text, re.M)))
+
+
+def lib():
+    """Load librs.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m gaussian_splatting_tile_gb300.build_lib`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.rs_error_string.restype = ctypes.c_char_p
+        L.rs_error_string.argtypes = [ctypes.c_int]
+        L.rs_project.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_gaussians),
+                                 ctypes.POINTER(rs_projected), _VP]
+        L.rs_bin_workspace_size.argtypes = [ctypes.c_int32, ctypes.POINTER(rs_camera), ctypes.c_size_t,
+                                            ctypes.POINTER(ctypes.c_size_t)]
+        L.rs_bin.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
+                             _VP, ctypes.c_size_t, ctypes.c_size_t, _VP, _VP, _VP,
+                             ctypes.POINTER(ctypes.c_size_t), _VP]
+        L.rs_rasterize_fwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected),
+                                       ctypes.c_int32, _VP, _VP, ctypes.POINTER(ctypes.c_float),
+                                       _VP, _VP, _VP, _VP]
+        L.rs_rasterize_bwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected),
+                                       ctypes.c_int32, _VP, _VP, ctypes.POINTER(ctypes.c_float),
+                                       _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
+        L.rs_project_bwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_gaussians),
+                                     ctypes.POINTER(rs_projected), _VP, _VP, _VP, _VP, _VP, _VP,
+                                     _VP, _VP]
+        for name in declared_symbols():
+            getattr(L, name).restype = ctypes.c_char_p if name == "rs_error_string" else ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def error_string(code: int) -> str:
+    return lib().rs_error_string(code).decode()
+
+
+def _check(fn: str, code: int):
+    if code != RS_OK:
+        raise RsError(fn, code, error_string(code))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtype=None, numel=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def camera_struct(cam) -> rs_camera:
+    c = rs_camera()
+    R = np.asarray(cam.R, np.float32).reshape(9)
+    t = np.asarray(cam.t, np.float32).reshape(3)
+    for i in range(9):
+        c.R[i] = float(R[i])
+    for i in range(3):
+        c.t[i] = float(t[i])
+    c.fx, c.fy, c.cx, c.cy = float(cam.fx), float(cam.fy), float(cam.cx), float(cam.cy)
+    c.width, c.height = int(cam.width), int(cam.height)
+    return c
+
+
+@dataclasses.dataclass
+class DeviceGaussians:
+    """Planar float32 CUDA tensors: means [3,N], scales [3,N], quats [4,N], opacity [N],
+    sh [3K,N] (sh_degree 0..3) or colors [3,N] (sh_degree -1)."""
+    means: torch.Tensor
+    scales: torch.Tensor
+    quats: torch.Tensor
+    opacity: torch.Tensor
+    sh: torch.Tensor | None
+    sh_degree: int
+    colors: torch.Tensor | None = None
+
+    @property
+    def n(self) -> int:
+        return int(self.opacity.shape[0])
+
+    @staticmethod
+    def from_numpy(g, device="cuda"):
+        f = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+        return DeviceGaussians(f(g.means), f(g.scales), f(g.quats), f(g.opacity), f(g.sh),
+                               int(g.sh_degree), f(g.colors))
+
+    def struct(self) -> rs_gaussians:
+        n = self.n
+        s = rs_gaussians()
+        s.n = n
+        s.d_means = _ptr(self.means, torch.float32, 3 * n, "means")
+        s.d_scales = _ptr(self.scales, torch.float32, 3 * n, "scales")
+        s.d_quats = _ptr(self.quats, torch.float32, 4 * n, "quats")
+        s.d_opacity = _ptr(self.opacity, torch.float32, n, "opacity")
+        s.sh_degree = int(self.sh_degree)
+        if self.sh_degree >= 0:
+            s.d_sh = _ptr(self.sh, torch.float32, 3 * (self.sh_degree + 1) ** 2 * n, "sh")
+        else:
+            s.d_colors = _ptr(self.colors, torch.float32, 3 * n, "colors")
+        return s
+
+
+@dataclasses.dataclass
+class DeviceProjected:
+    means2d: torch.Tensor
+    depth: torch.Tensor
+    conic: torch.Tensor
+    color: torch.Tensor
+    radius: torch.Tensor
+    tiles_touched: torch.Tensor
+    records: torch.Tensor  # uint8 [N*48]
+
+    @staticmethod
+    def empty(n: int, device="cuda"):
+        f = lambda *s: torch.empty(*s, dtype=torch.float32, device=device)
+        return DeviceProjected(f(2, n), f(n), f(3, n), f(3, n),
+                               torch.empty(n, dtype=torch.int32, device=device),
+                               torch.empty(n, dtype=torch.int32, device=device),
+                               torch.empty(max(n, 1) * RECORD_BYTES, dtype=torch.uint8, device=device))
+
+    def struct(self) -> rs_projected:
+        n = int(self.depth.shape[0])
+        s = rs_projected()
+        s.d_means2d = _ptr(self.means2d, torch.float32, 2 * n, "means2d")
+        s.d_depth = _ptr(self.depth, torch.float32, n, "depth")
+        s.d_conic = _ptr(self.conic, torch.float32, 3 * n, "conic")
+        s.d_color = _ptr(self.color, torch.float32, 3 * n, "color")
+        s.d_radius = _ptr(self.radius, torch.int32, n, "radius")
+        s.d_tiles_touched = _ptr(self.tiles_touched, None, n, "tiles_touched")
+        s.d_records = _ptr(self.records, torch.uint8, n * RECORD_BYTES, "records")
+        return s
+
+
+# ------------------------------------------------------------------ the five calls
+
+def rs_project(camera, gaussians: DeviceGaussians, out: DeviceProjected, stream=None):
+    c, g, o = camera_struct(camera), gaussians.struct(), out.struct()
+    _check("rs_project", lib().rs_project(ctypes.byref(c), ctypes.byref(g), ctypes.byref(o), _stream(stream)))
+
+
+def rs_bin_workspace_size(n: int, camera, capacity: int) -> int:
+    c = camera_struct(camera)
+    b = ctypes.c_size_t(0)
+    _check("rs_bin_workspace_size", lib().rs_bin_workspace_size(int(n), ctypes.byref(c), int(capacity), ctypes.byref(b)))
+    return int(b.value)
+
+
+def rs_bin(camera, proj: DeviceProjected, n: int, workspace: torch.Tensor, capacity: int,
+           keys_sorted, point_list: torch.Tensor, tile_ranges: torch.Tensor, stream=None) -> int:
+    """Returns the entry count E; raises RsError (code RS_ERR_CAPACITY, .n_entries set) when
+    E exceeds `capacity`."""
+    c = camera_struct(camera)
+    p = proj.struct()
+    E = ctypes.c_size_t(0)
+    rc = lib().rs_bin(ctypes.byref(c), ctypes.byref(p), int(n), _ptr(workspace, torch.uint8, None, "workspace"),
+                      int(workspace.numel()), int(capacity), _ptr(keys_sorted, torch.int64, capacity, "keys_sorted"),
+                      _ptr(point_list, torch.int32, capacity, "point_list"),
+                      _ptr(tile_ranges, torch.int32, 2 * ((camera.width + 15) // 16) * ((camera.height + 15) // 16),
+                           "tile_ranges"),
+                      ctypes.byref(E), _stream(stream))
+    if rc == RS_ERR_CAPACITY:
+        err = RsError("rs_bin", rc, error_string(rc))
+        err.n_entries = int(E.value)
+        raise err
+    _check("rs_bin", rc)
+    return int(E.value)
+
+
+def _bg(bg):
+    arr = (ctypes.c_float * 3)(*[float(x) for x in bg])
+    return arr
+
+
+def rs_rasterize_fwd(camera, proj: DeviceProjected, n: int, tile_ranges, point_list, bg, image,
+                     final_T, n_contrib, stream=None):
+    c = camera_struct(camera)
+    p = proj.struct()
+    HW = camera.width * camera.height
+    _check("rs_rasterize_fwd", lib().rs_rasterize_fwd(
+        ctypes.byref(c), ctypes.byref(p), int(n), _ptr(tile_ranges, torch.int32, None, "tile_ranges"),
+        _ptr(point_list, torch.int32, None, "point_list"), _bg(bg), _ptr(image, torch.float32, 3 * HW, "image"),
+        _ptr(final_T, torch.float32, HW, "final_T"), _ptr(n_contrib, torch.int32, HW, "n_contrib"),
+        _stream(stream)))
+
+
+def rs_rasterize_bwd(camera, proj: DeviceProjected, n: int, tile_ranges, point_list, bg, final_T,
+                     n_contrib, dL_dimage, dL_dmeans2d, dL_dconic, dL_dopacity, dL_dcolor, stream=None):
+    c = camera_struct(camera)
+    p = proj.struct()
+    HW = camera.width * camera.height
+    _check("rs_rasterize_bwd", lib().rs_rasterize_bwd(
+        ctypes.byref(c), ctypes.byref(p), int(n), _ptr(tile_ranges, torch.int32, None, "tile_ranges"),
+        _ptr(point_list, torch.int32, None, "point_list"), _bg(bg), _ptr(final_T, torch.float32, HW, "final_T"),
+        _ptr(n_contrib, torch.int32, HW, "n_contrib"), _ptr(dL_dimage, torch.float32, 3 * HW, "dL_dimage"),
+        _ptr(dL_dmeans2d, torch.float32, 2 * n, "dL_dmeans2d"), _ptr(dL_dconic, torch.float32, 3 * n, "dL_dconic"),
+        _ptr(dL_dopacity, torch.float32, n, "dL_dopacity"), _ptr(dL_dcolor, torch.float32, 3 * n, "dL_dcolor"),
+        _stream(stream)))
+
+
+def rs_project_bwd(camera, gaussians: DeviceGaussians, proj: DeviceProjected, dL_dmeans2d, dL_dconic,
+                   dL_dcolor, dL_dmeans, dL_dscales, dL_dquats, dL_dsh, stream=None):
+    c = camera_struct(camera)
+    g = gaussians.struct()
+    p = proj.struct()
+    n = gaussians.n
+    K = (gaussians.sh_degree + 1) ** 2 if gaussians.sh_degree >= 0 else 0
+    _check("rs_project_bwd", lib().rs_project_bwd(
+        ctypes.byref(c), ctypes.byref(g), ctypes.byref(p), _ptr(dL_dmeans2d, torch.float32, 2 * n, "dL_dmeans2d"),
+        _ptr(dL_dconic, torch.float32, 3 * n, "dL_dconic"), _ptr(dL_dcolor, torch.float32, 3 * n, "dL_dcolor"),
+        _ptr(dL_dmeans, torch.float32, 3 * n, "dL_dmeans"), _ptr(dL_dscales, torch.float32, 3 * n, "dL_dscales"),
+        _ptr(dL_dquats, torch.float32, 4 * n, "dL_dquats"),
+        _ptr(dL_dsh, torch.float32, 3 * K * n, "dL_dsh") if K else None, _stream(stream)))

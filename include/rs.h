@@ -1,0 +1,181 @@
+/*
+ * rs.h -- C ABI of the GB300 (sm_103a) tile-based 3D Gaussian Splatting rasteriser.
+ *
+ * Five calls carry the data-parallel path, in the order the rigel README's "How it works"
+ * diagram runs them: rs_project [1], rs_bin [2], rs_rasterize_fwd [3] (forward), then
+ * rs_rasterize_bwd [4] and rs_project_bwd [5] (backward).
+ *
+ * Conventions shared by every call
+ *  - Ownership: the caller allocates and owns every buffer, device and host, including the
+ *    binning workspace.  The library allocates no device memory, keeps no state between calls
+ *    and may be called from several host threads on distinct buffers.
+ *  - Pointers named d_* are device pointers; everything else is host memory.
+ *  - Layout: planar (structure of arrays) float32, one row per component, row stride n:
+ *    element (k, i) of a [K][n] array sits at base[k*n + i].  Images are [3][H][W]; per-pixel
+ *    buffers are [H][W].  Device arrays need their natural alignment (4 bytes; 8 bytes for
+ *    64-bit keys); the packed records need 16 bytes.
+ *  - Streams: every call takes `stream` (a cudaStream_t; NULL = the legacy default stream) and
+ *    only enqueues work on it, except rs_bin, which reads the entry count back to the host once
+ *    (a stream-ordered copy followed by a synchronisation of that stream).
+ *  - Outputs are overwritten, never accumulated into; gradient outputs are zeroed by the callee.
+ *  - Arguments are validated before anything is enqueued; a failed check returns
+ *    RS_ERR_INVALID_ARG and leaves every buffer untouched.
+ *  - n = 0 is valid: no Gaussian work is launched; the image is the background, final_T is 1
+ *    and n_contrib is 0.
+ *  - Limits: 0 <= n <= RS_MAX_GAUSSIANS; 1 <= width, height <= 32768; the number of
+ *    (Gaussian, tile) entries is below 2^32.
+ */
+#ifndef RS_H
+#define RS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define RS_OK 0
+#define RS_ERR_INVALID_ARG (-1)     /* null or misaligned pointer, bad size or parameter      */
+#define RS_ERR_CAPACITY (-2)        /* more entries than `capacity`; *n_entries holds the count */
+#define RS_ERR_WORKSPACE (-3)       /* workspace smaller than rs_bin_workspace_size reports   */
+#define RS_ERR_CUDA (-4)            /* a CUDA runtime call or launch failed                   */
+
+#define RS_TILE 16                  /* tile edge in pixels (rigel "Binning")                    */
+#define RS_RECORD_BYTES 48          /* packed per-Gaussian record written by rs_project         */
+#define RS_MAX_GAUSSIANS 67108864   /* 2^26                                                     */
+
+/* Pinhole camera: a world point m maps to p = R m + t (R row-major, world to camera), then to
+ * pixel (fx p.x/p.z + cx, fy p.y/p.z + cy).  Pixel (x, y) is sampled at integer coordinates.
+ * rigel README, "Deliberate differences from the reference implementation" (row-major
+ * world-to-camera matrices and explicit pinhole intrinsics). */
+typedef struct rs_camera {
+    float R[9];
+    float t[3];
+    float fx, fy, cx, cy;
+    int32_t width, height;
+} rs_camera;
+
+/* Gaussian parameters, already activated (scales linear, opacity in [0, 1]).
+ *   d_means [3][n], d_scales [3][n], d_quats [4][n] as (w, x, y, z) of any non-zero norm,
+ *   d_opacity [n];
+ *   sh_degree 0..3: d_sh [3K][n] with K = (sh_degree+1)^2, row k*3+ch holds the coefficient of
+ *   basis function k for channel ch (the f_dc / f_rest order of "3D Gaussian Splatting
+ *   ビューワを作る", 2.2.3);
+ *   sh_degree -1: d_colors [3][n] are the colours and d_sh is ignored. */
+typedef struct rs_gaussians {
+    int32_t n;
+    const float* d_means;
+    const float* d_scales;
+    const float* d_quats;
+    const float* d_opacity;
+    const float* d_sh;
+    int32_t sh_degree;
+    const float* d_colors;
+} rs_gaussians;
+
+/* Per-Gaussian results of rs_project (all [n] or [C][n]):
+ *   d_means2d [2][n] pixel position (u, v); d_depth [n] camera-space z;
+ *   d_conic [3][n] (A, B, C) of the inverse 2D covariance [[A, B], [B, C]];
+ *   d_color [3][n]; d_radius [n] int32 bounding radius in pixels, 0 = culled;
+ *   d_tiles_touched [n] uint32 number of 16x16 tiles of the radius square;
+ *   d_records: n * RS_RECORD_BYTES bytes, 16-byte aligned, the rasterisers' packed copy
+ *   (opaque: written by rs_project, read by the two rasterisers).
+ * A culled Gaussian has radius 0, tiles_touched 0 and zeros in every other field. */
+typedef struct rs_projected {
+    float* d_means2d;
+    float* d_depth;
+    float* d_conic;
+    float* d_color;
+    int32_t* d_radius;
+    uint32_t* d_tiles_touched;
+    void* d_records;
+} rs_projected;
+
+/* Human-readable text for a return code; never NULL. */
+const char* rs_error_string(int code);
+
+/* [1] Projection, rigel README "Projection"; covariance, conic and radius as in "3D Gaussian
+ * Splatting ビューワを作る" 2.1-2.3; tile span as tile_spans in the learn-gs notebook
+ * "11 - Tiles".  Per Gaussian: p = R m + t, culled unless p.z > 0.05; Sigma_3d = (R(q) S)(R(q) S)^T
+ * with q normalised; J at x/z, y/z clamped to 1.3x the half-widths W/(2 fx), H/(2 fy);
+ * Sigma_2d = J R Sigma_3d R^T J^T + 0.3 I; culled unless det > 0; conic = Sigma_2d^-1;
+ * (u, v) = (fx x/z + cx, fy y/z + cy); radius = ceil(3 sqrt(lambda_max)) with
+ * lambda_max = mid + sqrt(max(0.1, mid^2 - det)); span = [floor((u-r)/16), floor((u+r)/16)+1)
+ * clamped to the tile grid (same in y); culled when the span is empty.  Colour: degree-K real
+ * SH (viewer 2.2.3) at the unit direction from the camera centre -R^T t to the mean, no offset
+ * or clamp; or the given colours.  Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_project(const rs_camera* camera, const rs_gaussians* gaussians, const rs_projected* out,
+               void* stream);
+
+/* Workspace bytes rs_bin needs for n Gaussians on this camera with room for `capacity`
+ * entries.  Writes *bytes; returns RS_OK or RS_ERR_INVALID_ARG. */
+int rs_bin_workspace_size(int32_t n, const rs_camera* camera, size_t capacity, size_t* bytes);
+
+/* [2] Binning, rigel README "Binning": one entry per (visible Gaussian, covered tile) with
+ * key = (tile_id << 32) | float_bits(depth), tile_id = ty * ceil(W/16) + tx; entries are
+ * produced in Gaussian index order (tile rows outer, columns inner) at the offsets of an
+ * exclusive scan of tiles_touched, then sorted stably by key on the device (an LSD radix sort
+ * over the low 32 + ceil(log2(n_tiles)) bits, "3D Gaussian Splatting ビューワを作る" 4.3), and
+ * each tile's [start, end) range is extracted (viewer 4.4; empty tiles get (0, 0)).
+ * Inputs: `proj` from rs_project (means2d, depth, radius, tiles_touched are read).
+ * Outputs: d_point_list [capacity] uint32 Gaussian index per sorted entry; d_tile_ranges
+ * [n_tiles][2] uint32; d_keys_sorted [capacity] uint64 (may be NULL); *n_entries (host) = E.
+ * The entry count is read back to the host once.  If E > capacity the call returns
+ * RS_ERR_CAPACITY after setting *n_entries, so the caller can grow the buffers and call again.
+ * d_workspace: at least rs_bin_workspace_size bytes, 256-byte aligned, contents undefined on
+ * entry and exit.  Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CAPACITY, RS_ERR_CUDA. */
+int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
+           size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
+           uint32_t* d_point_list, uint32_t* d_tile_ranges, size_t* n_entries, void* stream);
+
+/* [3] Forward compositing, rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel".
+ * One thread block per 16x16 tile; each pixel walks its tile's list front to back:
+ * power = -1/2 (A dx^2 + C dy^2) - B dx dy with (dx, dy) = (x - u, y - v),
+ * alpha = min(0.99, opacity exp(power)); entries with alpha < 1/255 are skipped;
+ * C += colour alpha T, T *= 1 - alpha; the pixel stops after the entry that brings T below 1e-4.
+ * image = C + T bg.  n_contrib counts every entry the pixel examined (skipped ones and the one
+ * that stopped it included).  bg: host float[3].
+ * Outputs: d_image [3][H][W], d_final_T [H][W], d_n_contrib [H][W] uint32.
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
+                     float* d_image, float* d_final_T, uint32_t* d_n_contrib, void* stream);
+
+/* [4] Backward of the compositing, rigel README "Backward": each tile's list is walked back to
+ * front from final_T, undoing the transmittance one step at a time (T_i = T_{i+1} / (1 - a_i))
+ * and carrying the colour behind the current entry; entries past a pixel's n_contrib and
+ * skipped entries (alpha < 1/255) give nothing; an entry whose opacity * exp(power) exceeds
+ * 0.99 (clamped) passes no gradient to opacity, conic or mean ("Deliberate differences").
+ * Per-pixel contributions are reduced across each warp and tile before they reach global memory.
+ * Inputs: the forward's tile_ranges, point_list, final_T, n_contrib, bg (host float[3]) and
+ * d_dL_dimage [3][H][W].  Outputs (zeroed, then accumulated by the call):
+ * d_dL_dmeans2d [2][n], d_dL_dconic [3][n], d_dL_dopacity [n], d_dL_dcolor [3][n].
+ * The accumulation order is not fixed, so results may differ in the last bits between runs.
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
+                     const float* d_final_T, const uint32_t* d_n_contrib,
+                     const float* d_dL_dimage, float* d_dL_dmeans2d, float* d_dL_dconic,
+                     float* d_dL_dopacity, float* d_dL_dcolor, void* stream);
+
+/* [5] Backward of the projection and colour, rigel README "Backward" (second paragraph): through
+ * the 2x2 inverse, Sigma_2d = T Sigma_3d T^T with T = J R, the Jacobian's dependence on p_cam
+ * (a clamped x/z or y/z sends its gradient to z), the pinhole, the camera transform and
+ * Sigma_3d = M M^T with M = R(q) S, including the normalisation of q (the quaternion gradient
+ * has no component along q); and through the SH basis, including the view direction's
+ * dependence on the mean.  Culled Gaussians (radius 0) get zero gradients.
+ * Inputs: the forward's gaussians and proj (radius is read), and the gradients of means2d,
+ * conic and colour.  Outputs (overwritten): d_dL_dmeans [3][n], d_dL_dscales [3][n],
+ * d_dL_dquats [4][n], d_dL_dsh [3K][n] (ignored and may be NULL when sh_degree is -1; then
+ * d_dL_dcolor already is the colours' gradient).  Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_project_bwd(const rs_camera* camera, const rs_gaussians* gaussians,
+                   const rs_projected* proj, const float* d_dL_dmeans2d,
+                   const float* d_dL_dconic, const float* d_dL_dcolor, float* d_dL_dmeans,
+                   float* d_dL_dscales, float* d_dL_dquats, float* d_dL_dsh, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RS_H */

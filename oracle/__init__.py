@@ -150,11 +150,13 @@ def bin(cam, means2d, depth, radius):
 
 def raster_fwd(cam, means2d, conic, opacity, color, ranges, point_list, bg=(0.0, 0.0, 0.0),
                prec: int = 64, margin: float = 0.0, tile_mask=None):
-    """c3.  Returns image [3,H,W], final_T [H,W], n_contrib [H,W] (uint32), ambig [H,W] (uint8)."""
+    """c3.  Returns image [3,H,W], final_T [H,W], n_contrib [H,W] (uint32), ambig [H,W] (uint8),
+    n_blend [H,W] (uint32, composited entries per pixel)."""
     n = int(np.asarray(opacity).shape[0])
     H, W = cam.height, cam.width
     image, final_T = np.zeros((3, H, W)), np.zeros((H, W))
     n_contrib, ambig = np.zeros((H, W), np.uint32), np.zeros((H, W), np.uint8)
+    n_blend = np.zeros((H, W), np.uint32)
     c = _cam(cam)
     a = [_d(means2d), _d(conic), _d(opacity), _d(color)]
     rg = np.ascontiguousarray(ranges, np.uint32)
@@ -166,10 +168,10 @@ def raster_fwd(cam, means2d, conic, opacity, color, ranges, point_list, bg=(0.0,
     rc = lib().orc_raster_fwd(ctypes.c_int(prec), ctypes.byref(c), ctypes.c_int32(n), _p(a[0]),
                               _p(a[1]), _p(a[2]), _p(a[3]), _p(rg), _p(pl), _p(b), _p(tm),
                               _p(image), _p(final_T), _p(n_contrib), ctypes.c_double(margin),
-                              _p(ambig))
+                              _p(ambig), _p(n_blend))
     if rc != 0:
         raise ValueError(f"orc_raster_fwd returned {rc}")
-    return dict(image=image, final_T=final_T, n_contrib=n_contrib, ambig=ambig)
+    return dict(image=image, final_T=final_T, n_contrib=n_contrib, ambig=ambig, n_blend=n_blend)
 
 
 def raster_bwd(cam, means2d, conic, opacity, color, ranges, point_list, n_contrib, dL_dimage,

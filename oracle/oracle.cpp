@@ -355,10 +355,10 @@ void composite_pixel(int px, int py, const uint32_t* list, uint32_t start, uint3
                      int32_t n, const double* means2d, const double* conic,
                      const double* opacity, const double* color, const double* bg,
                      double margin, double* out_rgb, double* out_T, uint32_t* out_n,
-                     uint8_t* out_amb) {
+                     uint8_t* out_amb, uint32_t* out_blend) {
     Real T = 1;
     Real C[3] = {0, 0, 0};
-    uint32_t cnt = 0;
+    uint32_t cnt = 0, blended = 0;
     uint8_t amb = 0;
     for (uint32_t j = start; j < end; ++j) {
         const uint32_t g = list[j];
@@ -374,6 +374,7 @@ void composite_pixel(int px, int py, const uint32_t* list, uint32_t start, uint3
             if (near_rel(double(raw), 0.99, margin)) amb |= ORC_AMB_ALPHA_MAX;
         }
         if (alpha < K<Real>::alpha_min()) continue;
+        ++blended;
         for (int ch = 0; ch < 3; ++ch) C[ch] += Real(color[size_t(ch) * n + g]) * alpha * T;
         T = T * (Real(1) - alpha);
         if (margin > 0 && near_rel(double(T), 1e-4, margin)) amb |= ORC_AMB_T_STOP;
@@ -383,13 +384,15 @@ void composite_pixel(int px, int py, const uint32_t* list, uint32_t start, uint3
     *out_T = double(T);
     *out_n = cnt;
     *out_amb = amb;
+    *out_blend = blended;
 }
 
 template <typename Real>
 int raster_fwd(const orc_camera* cam, int32_t n, const double* means2d, const double* conic,
                const double* opacity, const double* color, const uint32_t* ranges,
                const uint32_t* list, const double* bg, const uint8_t* tile_mask, double* image,
-               double* final_T, uint32_t* n_contrib, double margin, uint8_t* ambig) {
+               double* final_T, uint32_t* n_contrib, double margin, uint8_t* ambig,
+               uint32_t* n_blend) {
     const int W = cam->width, H = cam->height;
     const int TX = (W + TILE - 1) / TILE, TY = (H + TILE - 1) / TILE;
     const size_t HW = size_t(W) * size_t(H);
@@ -402,10 +405,11 @@ int raster_fwd(const orc_camera* cam, int32_t n, const double* means2d, const do
                 for (int px = tx * TILE; px < std::min(W, (tx + 1) * TILE); ++px) {
                     const size_t pix = size_t(py) * W + px;
                     double rgb[3], Tf;
-                    uint32_t cnt;
+                    uint32_t cnt, blended;
                     uint8_t amb;
                     composite_pixel<Real>(px, py, list, start, end, n, means2d, conic, opacity,
-                                          color, bg, margin, rgb, &Tf, &cnt, &amb);
+                                          color, bg, margin, rgb, &Tf, &cnt, &amb, &blended);
+                    if (n_blend) n_blend[pix] = blended;
                     for (int ch = 0; ch < 3; ++ch) image[size_t(ch) * HW + pix] = rgb[ch];
                     final_T[pix] = Tf;
                     n_contrib[pix] = cnt;
@@ -754,14 +758,14 @@ int orc_raster_fwd(int prec, const orc_camera* cam, int32_t n, const double* mea
                    const double* conic, const double* opacity, const double* color,
                    const uint32_t* ranges, const uint32_t* point_list, const double* bg,
                    const uint8_t* tile_mask, double* image, double* final_T,
-                   uint32_t* n_contrib, double margin, uint8_t* ambig) {
+                   uint32_t* n_contrib, double margin, uint8_t* ambig, uint32_t* n_blend) {
     if (!cam || n < 0) return -1;
     if (prec == 32)
         return raster_fwd<float>(cam, n, means2d, conic, opacity, color, ranges, point_list, bg,
-                                 tile_mask, image, final_T, n_contrib, margin, ambig);
+                                 tile_mask, image, final_T, n_contrib, margin, ambig, n_blend);
     if (prec == 64)
         return raster_fwd<double>(cam, n, means2d, conic, opacity, color, ranges, point_list, bg,
-                                  tile_mask, image, final_T, n_contrib, margin, ambig);
+                                  tile_mask, image, final_T, n_contrib, margin, ambig, n_blend);
     return -1;
 }
 

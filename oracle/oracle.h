@@ -82,12 +82,13 @@ int64_t orc_bin(const orc_camera* cam, int32_t n, const float* means2d, const fl
                 uint32_t* point_list, uint32_t* ranges, uint32_t* tiles_touched);
 
 /* c3: forward compositing of every pixel in the tiles selected by tile_mask (NULL = all).
- * Pixels of unselected tiles are left untouched. */
+ * Pixels of unselected tiles are left untouched.  n_blend (may be NULL) receives, per pixel,
+ * how many of the examined entries were composited (not skipped). */
 int orc_raster_fwd(int prec, const orc_camera* cam, int32_t n, const double* means2d,
                    const double* conic, const double* opacity, const double* color,
                    const uint32_t* ranges, const uint32_t* point_list, const double* bg,
                    const uint8_t* tile_mask, double* image, double* final_T,
-                   uint32_t* n_contrib, double margin, uint8_t* ambig);
+                   uint32_t* n_contrib, double margin, uint8_t* ambig, uint32_t* n_blend);
 
 /* c4: backward of the compositing, in double.  Walk length per pixel is n_contrib (as given).
  * Gradients are accumulated into zero-initialised outputs by this call. */

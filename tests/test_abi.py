@@ -1,0 +1,82 @@
+"""The C-ABI library loads and exports every entry point include/rs.h declares; host-only calls
+and argument validation behave as documented.  No GPU work is issued (CPU only)."""
+import ctypes
+
+import pytest
+
+from gaussian_splatting_tile_gb300 import build_lib, rs, scenes
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return rs.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = rs.declared_symbols()
+    assert {"rs_project", "rs_bin", "rs_rasterize_fwd", "rs_rasterize_bwd", "rs_project_bwd",
+            "rs_bin_workspace_size", "rs_error_string"} <= set(names)
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_error_strings(L):
+    for code in (0, -1, -2, -3, -4, 7):
+        assert rs.error_string(code)
+    assert "capacity" in rs.error_string(rs.RS_ERR_CAPACITY)
+
+
+def test_workspace_size_grows_with_capacity(L):
+    cam = scenes.procedural_camera(1920, 1080)
+    a = rs.rs_bin_workspace_size(160_000, cam, 1_000_000)
+    b = rs.rs_bin_workspace_size(160_000, cam, 4_000_000)
+    assert 0 < a < b
+    # 8 + 8 + 4 bytes of sort buffers per entry at least
+    assert b - a >= 3_000_000 * 20
+    assert rs.rs_bin_workspace_size(0, cam, 0) > 0
+
+
+def test_invalid_arguments_rejected_before_any_launch(L):
+    cam = rs.camera_struct(scenes.procedural_camera(64, 48))
+    nbytes = ctypes.c_size_t(0)
+    assert L.rs_bin_workspace_size(-1, ctypes.byref(cam), 10, ctypes.byref(nbytes)) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_bin_workspace_size(10, None, 10, ctypes.byref(nbytes)) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_bin_workspace_size(10, ctypes.byref(cam), 10, None) == rs.RS_ERR_INVALID_ARG
+    bad = rs.camera_struct(scenes.procedural_camera(64, 48))
+    bad.fx = 0.0
+    assert L.rs_bin_workspace_size(10, ctypes.byref(bad), 10, ctypes.byref(nbytes)) == rs.RS_ERR_INVALID_ARG
+    bad = rs.camera_struct(scenes.procedural_camera(64, 48))
+    bad.width = 0
+    assert L.rs_bin_workspace_size(10, ctypes.byref(bad), 10, ctypes.byref(nbytes)) == rs.RS_ERR_INVALID_ARG
+    # null pointers / bad degree are caught by validation, which runs before any CUDA call
+    g = rs.rs_gaussians()
+    g.n = 10
+    g.sh_degree = 0
+    assert L.rs_project(ctypes.byref(cam), ctypes.byref(g), None, None) == rs.RS_ERR_INVALID_ARG
+    g.sh_degree = 4
+    assert L.rs_project(ctypes.byref(cam), ctypes.byref(g), None, None) == rs.RS_ERR_INVALID_ARG
+    g.n = -3
+    g.sh_degree = 0
+    assert L.rs_project(ctypes.byref(cam), ctypes.byref(g), None, None) == rs.RS_ERR_INVALID_ARG
+    bgv = (ctypes.c_float * 3)(0, 0, 0)
+    assert L.rs_rasterize_fwd(ctypes.byref(cam), None, 5, None, None, bgv, None, None, None, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_rasterize_bwd(ctypes.byref(cam), None, 5, None, None, bgv, None, None, None, None, None, None,
+                              None, None) == rs.RS_ERR_INVALID_ARG
+    E = ctypes.c_size_t(0)
+    assert L.rs_bin(ctypes.byref(cam), None, 5, None, 0, 0, None, None, None, ctypes.byref(E), None) == rs.RS_ERR_INVALID_ARG
+    # misaligned workspace
+    assert L.rs_bin(ctypes.byref(cam), None, 0, ctypes.c_void_p(0x1001), 1 << 20, 0, None, None,
+                    ctypes.c_void_p(0x2000), ctypes.byref(E), None) == rs.RS_ERR_INVALID_ARG
+    # workspace too small (validated on the host, before launches)
+    assert L.rs_bin(ctypes.byref(cam), None, 0, ctypes.c_void_p(0x1000), 16, 0, None, None,
+                    ctypes.c_void_p(0x2000), ctypes.byref(E), None) == rs.RS_ERR_WORKSPACE
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+    cam = scenes.procedural_camera(64, 48)
+    g = rs.DeviceGaussians(torch.zeros(3, 4), torch.zeros(3, 4), torch.zeros(4, 4), torch.zeros(4),
+                           torch.zeros(3, 4), 0)
+    with pytest.raises(TypeError):
+        g.struct()
