@@ -78,6 +78,8 @@ def lib():
         L.rs_bin.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
                              _VP, ctypes.c_size_t, ctypes.c_size_t, _VP, _VP, _VP,
                              ctypes.POINTER(ctypes.c_size_t), _VP]
+        L.rs_bin_noalloc.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
+                                     ctypes.c_size_t, _VP, _VP, _VP, ctypes.POINTER(ctypes.c_size_t), _VP]
         L.rs_rasterize_fwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected),
                                        ctypes.c_int32, _VP, _VP, ctypes.POINTER(ctypes.c_float),
                                        _VP, _VP, _VP, _VP]
@@ -236,6 +238,28 @@ def rs_bin(camera, proj: DeviceProjected, n: int, workspace: torch.Tensor, capac
         err.n_entries = int(E.value)
         raise err
     _check("rs_bin", rc)
+    return int(E.value)
+
+
+def rs_bin_noalloc(camera, proj: DeviceProjected, n: int, capacity: int, keys_sorted,
+                   point_list: torch.Tensor, tile_ranges: torch.Tensor, stream=None) -> int:
+    """rs_bin without a workspace (the library's fixed scratch array is used).  Returns E; raises
+    RsError (RS_ERR_CAPACITY with .n_entries, or RS_ERR_WORKSPACE when the sizes exceed the
+    fixed scratch)."""
+    c = camera_struct(camera)
+    p = proj.struct()
+    E = ctypes.c_size_t(0)
+    rc = lib().rs_bin_noalloc(ctypes.byref(c), ctypes.byref(p), int(n), int(capacity),
+                              _ptr(keys_sorted, torch.int64, capacity, "keys_sorted"),
+                              _ptr(point_list, torch.int32, capacity, "point_list"),
+                              _ptr(tile_ranges, torch.int32,
+                                   2 * ((camera.width + 15) // 16) * ((camera.height + 15) // 16), "tile_ranges"),
+                              ctypes.byref(E), _stream(stream))
+    if rc == RS_ERR_CAPACITY:
+        err = RsError("rs_bin_noalloc", rc, error_string(rc))
+        err.n_entries = int(E.value)
+        raise err
+    _check("rs_bin_noalloc", rc)
     return int(E.value)
 
 

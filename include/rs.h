@@ -175,6 +175,28 @@ int rs_project_bwd(const rs_camera* camera, const rs_gaussians* gaussians,
                    const float* d_dL_dconic, const float* d_dL_dcolor, float* d_dL_dmeans,
                    float* d_dL_dscales, float* d_dL_dquats, float* d_dL_dsh, void* stream);
 
+/* Allocation-free variant of rs_bin.  The source pages have no counterpart: this entry point
+ * exists for callers of this library that cannot allocate device memory -- for example a plug-in
+ * whose host application owns and budgets all device memory, or a per-frame loop that must not
+ * call cudaMalloc because an allocation synchronises the device and has unbounded latency.
+ * Arguments, outputs and errors are those of rs_bin, except that there is no workspace: the
+ * scratch is a fixed array of RS_BIN_NOALLOC_SCRATCH_BYTES bytes that is part of the library's
+ * device image.  Every GPU that loads the library holds that array until the process exits.
+ *  - Limit: the call returns RS_ERR_WORKSPACE, before any work, when
+ *    rs_bin_workspace_size(n, camera, capacity) exceeds RS_BIN_NOALLOC_SCRATCH_BYTES
+ *    (48 MiB: about 2.2 million entries for 160,000 Gaussians at 1920x1080).
+ *  - Set-up: the first call on a device, with that device current, looks up the array's device
+ *    address (cudaGetSymbolAddress) and keeps it for later calls; make that first call before
+ *    any stream capture.  RS_ERR_CUDA if the lookup fails.
+ *  - Sharing: all calls use the same array and it keeps the last call's contents; nothing in it
+ *    needs to start at zero.  Calls whose work overlaps on the GPU (other streams, other host
+ *    threads on the same device) race on the array: serialise them.
+ * The call itself allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. */
+#define RS_BIN_NOALLOC_SCRATCH_BYTES (48u << 20)
+int rs_bin_noalloc(const rs_camera* camera, const rs_projected* proj, int32_t n, size_t capacity,
+                   uint64_t* d_keys_sorted, uint32_t* d_point_list, uint32_t* d_tile_ranges,
+                   size_t* n_entries, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
