@@ -92,14 +92,24 @@ __device__ __forceinline__ void sh_basis_grad(float x, float y, float z, float (
     }
 }
 
+// a*b - c*d with one rounding error (Kahan's algorithm with a fused multiply-add).
+__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
+    const float w = c * d;
+    const float e = fmaf(-c, d, w);
+    const float f = fmaf(a, b, -w);
+    return f + e;
+}
+
 // Forward geometry of one Gaussian (everything but colour).
 struct Geo {
     float p[3];       // camera-space mean
     float qn;         // |q|
     float qh[4];      // q / |q|
     float Rq[9];      // rotation of qh
-    float S3[6];      // 3D covariance xx xy xz yy yz zz
+    float s2[3];      // squared scales
     float T[6];       // J R (2x3)
+    float U[6];       // T Rq (2x3): Sigma_2d = U diag(s^2) U^T + 0.3 I
+    float m01, m02, m12;  // 2x2 minors of U: m_jk = U0j U1k - U0k U1j
     float tx, ty;
     bool cx, cy;      // clamp active
     float a, b, c;    // dilated 2D covariance
@@ -136,18 +146,9 @@ __device__ __forceinline__ void geometry(const CameraF& cam, const float m[3], c
     G.Rq[6] = 2.f * (qx * qz - w * qy);
     G.Rq[7] = 2.f * (qy * qz + w * qx);
     G.Rq[8] = 1.f - 2.f * (qx * qx + qy * qy);
-    float M[9];
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-#pragma unroll
-        for (int j = 0; j < 3; ++j) M[i * 3 + j] = G.Rq[i * 3 + j] * s[j];
-    // Sigma_3d = M M^T (symmetric: xx xy xz yy yz zz)
-    G.S3[0] = M[0] * M[0] + M[1] * M[1] + M[2] * M[2];
-    G.S3[1] = M[0] * M[3] + M[1] * M[4] + M[2] * M[5];
-    G.S3[2] = M[0] * M[6] + M[1] * M[7] + M[2] * M[8];
-    G.S3[3] = M[3] * M[3] + M[4] * M[4] + M[5] * M[5];
-    G.S3[4] = M[3] * M[6] + M[4] * M[7] + M[5] * M[8];
-    G.S3[5] = M[6] * M[6] + M[7] * M[7] + M[8] * M[8];
+    G.s2[0] = s[0] * s[0];
+    G.s2[1] = s[1] * s[1];
+    G.s2[2] = s[2] * s[2];
     // J at the clamped centre
     const float lim_x = kClampFrac * (0.5f * float(cam.W)) / cam.fx;
     const float lim_y = kClampFrac * (0.5f * float(cam.H)) / cam.fy;
@@ -165,20 +166,27 @@ __device__ __forceinline__ void geometry(const CameraF& cam, const float m[3], c
         G.T[j] = j00 * cam.R[0 * 3 + j] + j02 * cam.R[2 * 3 + j];
         G.T[3 + j] = j11 * cam.R[1 * 3 + j] + j12 * cam.R[2 * 3 + j];
     }
-    // Sigma_2d = T Sigma_3d T^T
-    const float* S = G.S3;
-    float TS[6];
+    // Sigma_2d = T (Rq S^2 Rq^T) T^T = U S^2 U^T with U = T Rq: the same matrix as
+    // J W Sigma_3d W^T J^T, evaluated through the 2x3 factor (fewer products, less cancellation)
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float* t = &G.T[i * 3];
-        TS[i * 3 + 0] = t[0] * S[0] + t[1] * S[1] + t[2] * S[2];
-        TS[i * 3 + 1] = t[0] * S[1] + t[1] * S[3] + t[2] * S[4];
-        TS[i * 3 + 2] = t[0] * S[2] + t[1] * S[4] + t[2] * S[5];
-    }
-    G.a = TS[0] * G.T[0] + TS[1] * G.T[1] + TS[2] * G.T[2] + kDilation;
-    G.b = TS[0] * G.T[3] + TS[1] * G.T[4] + TS[2] * G.T[5];
-    G.c = TS[3] * G.T[3] + TS[4] * G.T[4] + TS[5] * G.T[5] + kDilation;
-    G.det = G.a * G.c - G.b * G.b;
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            G.U[k * 3 + j] = G.T[k * 3 + 0] * G.Rq[0 * 3 + j] + G.T[k * 3 + 1] * G.Rq[1 * 3 + j] +
+                             G.T[k * 3 + 2] * G.Rq[2 * 3 + j];
+    const float ap = G.s2[0] * G.U[0] * G.U[0] + G.s2[1] * G.U[1] * G.U[1] + G.s2[2] * G.U[2] * G.U[2];
+    const float cp = G.s2[0] * G.U[3] * G.U[3] + G.s2[1] * G.U[4] * G.U[4] + G.s2[2] * G.U[5] * G.U[5];
+    G.a = ap + kDilation;
+    G.b = G.s2[0] * G.U[0] * G.U[3] + G.s2[1] * G.U[1] * G.U[4] + G.s2[2] * G.U[2] * G.U[5];
+    G.c = cp + kDilation;
+    // det = ac - b^2 without its cancellation: by Cauchy-Binet,
+    // det(0.3 I + V V^T) = 0.09 + 0.3 tr(V V^T) + sum_{j<k} (s_j s_k m_jk)^2 with V = U diag(s),
+    // a sum of non-negative terms (for a needle seen end-on ac and b^2 agree to many digits)
+    G.m01 = diff_of_products(G.U[0], G.U[4], G.U[1], G.U[3]);
+    G.m02 = diff_of_products(G.U[0], G.U[5], G.U[2], G.U[3]);
+    G.m12 = diff_of_products(G.U[1], G.U[5], G.U[2], G.U[4]);
+    const float t01 = s[0] * s[1] * G.m01, t02 = s[0] * s[2] * G.m02, t12 = s[1] * s[2] * G.m12;
+    G.det = kDilation * kDilation + kDilation * (ap + cp) + (t01 * t01 + t02 * t02 + t12 * t12);
     if (!(G.det > 0.f) || !isfinite(G.det)) return;
     const float inv = 1.0f / G.det;
     G.A = G.c * inv;
@@ -262,10 +270,22 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
     color[i] = rgb[0]; color[N + i] = rgb[1]; color[2 * N + i] = rgb[2];
     radius[i] = G.radius;
     tiles[i] = uint32_t(G.rect[1] - G.rect[0]) * uint32_t(G.rect[3] - G.rect[2]);
+    // Half-extents of the region where opacity * exp(power) >= 1/255, i.e. d^T Q d <= k with
+    // k = 2 ln(255 o): the ellipse's bounding box is sqrt(k a) by sqrt(k c) (a, c the diagonal of
+    // Sigma_2d = Q^-1).  Inflated by 0.1% in k and 0.01 px so that float rounding in the
+    // rasterisers' alpha can never reach 1/255 outside it; negative when o < 1/255 (the Gaussian
+    // can never pass the alpha threshold).
+    float ext_x = -1.f, ext_y = -1.f;
+    const float o255 = 255.f * o;
+    if (o255 > 1.f) {
+        const float k = 2.002f * logf(o255);
+        ext_x = sqrtf(k * G.a) + 0.01f;
+        ext_y = sqrtf(k * G.c) + 0.01f;
+    }
     Record r;
-    r.p = make_float4(G.u, G.v, o, G.A);
-    r.q = make_float4(-0.5f * kLog2e * G.A, -kLog2e * G.B, -0.5f * kLog2e * G.C, G.B);
-    r.c = make_float4(rgb[0], rgb[1], rgb[2], G.C);
+    r.p = make_float4(G.u, G.v, o, ext_x);
+    r.q = make_float4(-0.5f * kLog2e * G.A, -kLog2e * G.B, -0.5f * kLog2e * G.C, ext_y);
+    r.c = make_float4(rgb[0], rgb[1], rgb[2], 0.f);
     rec[i] = r;
 }
 
@@ -306,33 +326,60 @@ __global__ void __launch_bounds__(256) k_project_bwd(
     const float g00 = -(qg00 * A + qg01 * B);
     const float g01 = -(qg00 * B + qg01 * C);
     const float g11 = -(qg10 * B + qg11 * C);
-    // Sigma_2d = T S T^T: dT = 2 G2 T S, dS = T^T G2 T (G2 symmetric [[g00, g01], [g01, g11]])
-    const float* S = G.S3;
-    float TS[6];
+    // Sigma_2d = U S^2 U^T + 0.3 I with U = T Rq and G2 = [[g00, g01], [g01, g11]]:
+    //   dU = 2 G2 U S^2 (feeds dT = dU Rq^T, the mean's path through J);
+    //   scales and rotation go through W = Q U = Sigma_2d^-1 U instead, since
+    //   dRq = T^T dU = -2 Rq Z S^2 and ds_j = -2 s_j Z_jj with Z = W^T Gq W (T = U Rq^T).
+    //   Column j of adj(Sigma_2d) U is 0.3 u_j + sum_{k != j} s_k^2 m_jk (U1k, -U0k): the
+    //   s_j^2 u_j u_j^T part of Sigma_2d cancels out exactly and is never formed.
+    float dU[6];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const float* t = &G.T[r * 3];
-        TS[r * 3 + 0] = t[0] * S[0] + t[1] * S[1] + t[2] * S[2];
-        TS[r * 3 + 1] = t[0] * S[1] + t[1] * S[3] + t[2] * S[4];
-        TS[r * 3 + 2] = t[0] * S[2] + t[1] * S[4] + t[2] * S[5];
+    for (int j = 0; j < 3; ++j) {
+        dU[j] = 2.f * G.s2[j] * (g00 * G.U[j] + g01 * G.U[3 + j]);
+        dU[3 + j] = 2.f * G.s2[j] * (g01 * G.U[j] + g11 * G.U[3 + j]);
     }
     float dT[6];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        dT[j] = 2.f * (g00 * TS[j] + g01 * TS[3 + j]);
-        dT[3 + j] = 2.f * (g01 * TS[j] + g11 * TS[3 + j]);
-    }
-    float GT[6];  // G2 T
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+            dT[k * 3 + r] = dU[k * 3 + 0] * G.Rq[r * 3 + 0] + dU[k * 3 + 1] * G.Rq[r * 3 + 1] +
+                            dU[k * 3 + 2] * G.Rq[r * 3 + 2];
+    const float mn[3][3] = {{0.f, G.m01, G.m02}, {-G.m01, 0.f, G.m12}, {-G.m02, -G.m12, 0.f}};
+    const float inv_det = 1.0f / G.det;
+    float Wx[3], Wy[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
-        GT[j] = g00 * G.T[j] + g01 * G.T[3 + j];
-        GT[3 + j] = g01 * G.T[j] + g11 * G.T[3 + j];
+        float wx = kDilation * G.U[j], wy = kDilation * G.U[3 + j];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            if (k == j) continue;
+            const float mm = G.s2[k] * mn[j][k];
+            wx = fmaf(mm, G.U[3 + k], wx);
+            wy = fmaf(-mm, G.U[k], wy);
+        }
+        Wx[j] = wx * inv_det;
+        Wy[j] = wy * inv_det;
     }
-    float dS[9];  // T^T G2 T, full 3x3
+    // Z = W^T Gq W with Gq = [[gA, gB], [gB, gC]] (gB already halved)
+    float Z[3][3];
 #pragma unroll
-    for (int a = 0; a < 3; ++a)
+    for (int j = 0; j < 3; ++j)
 #pragma unroll
-        for (int b = 0; b < 3; ++b) dS[a * 3 + b] = G.T[a] * GT[b] + G.T[3 + a] * GT[3 + b];
+        for (int k = j; k < 3; ++k) {
+            Z[j][k] = gA * Wx[j] * Wx[k] + gB * (Wx[j] * Wy[k] + Wy[j] * Wx[k]) + gC * Wy[j] * Wy[k];
+            Z[k][j] = Z[j][k];
+        }
+    float ds[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) ds[j] = -2.f * s[j] * Z[j][j];
+    float dR[9];
+#pragma unroll
+    for (int r = 0; r < 3; ++r)
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            dR[r * 3 + j] = -2.f * G.s2[j] *
+                            (G.Rq[r * 3 + 0] * Z[0][j] + G.Rq[r * 3 + 1] * Z[1][j] + G.Rq[r * 3 + 2] * Z[2][j]);
     // T = J R -> dJ = dT R^T; only J00, J02, J11, J12 are variables
     float dJ[6];
 #pragma unroll
@@ -357,23 +404,6 @@ __global__ void __launch_bounds__(256) k_project_bwd(
     float dm[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) dm[j] = cam.R[j] * dp[0] + cam.R[3 + j] * dp[1] + cam.R[6 + j] * dp[2];
-    // Sigma_3d = M M^T, M = Rq diag(s): dM = 2 dS M
-    float M[9];
-#pragma unroll
-    for (int a = 0; a < 3; ++a)
-#pragma unroll
-        for (int b = 0; b < 3; ++b) M[a * 3 + b] = G.Rq[a * 3 + b] * s[b];
-    float ds[3] = {0.f, 0.f, 0.f};
-    float dR[9];
-#pragma unroll
-    for (int a = 0; a < 3; ++a)
-#pragma unroll
-        for (int b = 0; b < 3; ++b) {
-            const float dMab = 2.f * (dS[a * 3 + 0] * M[0 * 3 + b] + dS[a * 3 + 1] * M[1 * 3 + b] +
-                                      dS[a * 3 + 2] * M[2 * 3 + b]);
-            dR[a * 3 + b] = dMab * s[b];
-            ds[b] += dMab * G.Rq[a * 3 + b];
-        }
     const float w = G.qh[0], qx = G.qh[1], qy = G.qh[2], qz = G.qh[3];
     float dqh[4];
     dqh[0] = 2.f * (-qz * dR[1] + qy * dR[2] + qz * dR[3] - qx * dR[5] - qy * dR[6] + qx * dR[7]);

@@ -5,20 +5,71 @@
 // fetch, __syncthreads_count vote: the block leaves once all 256 pixels are saturated).
 // Backward: rigel README "Backward": walk each tile back to front from final_T and n_contrib,
 // T_i = T_{i+1} / (1 - a_i), the colour behind carried as a running blend; per-pixel
-// contributions are summed over the warp (shuffles) and over the tile (shared-memory
-// accumulators, one slot per staged entry) before one global atomic per entry, component and
-// tile -- the reduction rigel's README names as missing from its rasteriser backward.
+// contributions are summed over the warp (a shuffle reduce-scatter) and over the tile
+// (shared-memory accumulators, one slot per staged entry) before one global atomic per entry,
+// component and tile -- the reduction rigel's README names as missing from its backward.
+//
+// Both kernels give each warp an 8x4 pixel rectangle and, after a batch is staged, let each warp
+// compact the entries whose alpha >= 1/255 box (from the record) meets its rectangle: the other
+// entries would be examined and skipped at every pixel of the warp, so they are skipped without
+// being evaluated.  n_contrib is kept as a position in the list (one past the entry that stopped
+// the pixel, or the list length), which is exactly the count of examined entries.
 #include "rs_internal.cuh"
 
 namespace rs {
 namespace {
 
 constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per thread
+constexpr int kWarps = kTilePixels / 32;
+constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int& px, int& py) {
-    const int tx = tile % cam.TX, ty = tile / cam.TX;
-    px = tx * kTile + (threadIdx.x & (kTile - 1));
-    py = ty * kTile + (threadIdx.x / kTile);
+// Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
+// (w >> 1) * 4 of the tile; lane l is pixel (l & 7, l >> 3) inside it.
+__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int& tx0, int& ty0, int& px,
+                                           int& py) {
+    tx0 = (tile % cam.TX) * kTile;
+    ty0 = (tile / cam.TX) * kTile;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    px = tx0 + (warp & 1) * 8 + (lane & 7);
+    py = ty0 + (warp >> 1) * 4 + (lane >> 3);
+}
+
+// Bit w is set when warp w's 8x4 pixel rectangle meets the entry's alpha >= 1/255 box
+// [u - ext_x, u + ext_x] x [v - ext_y, v + ext_y]; pixels outside the box cannot pass the alpha
+// threshold, so a warp whose bit is clear would skip the entry at every one of its pixels.
+__device__ __forceinline__ uint32_t warp_mask(const float4& p, const float4& q, int tx0, int ty0) {
+    if (!(p.w >= 0.f)) return 0u;
+    const float xl = p.x - p.w - float(tx0), xh = p.x + p.w - float(tx0);
+    const float yl = p.y - q.w - float(ty0), yh = p.y + q.w - float(ty0);
+    const bool c0 = xl <= 7.f && xh >= 0.f;
+    const bool c1 = xl <= 15.f && xh >= 8.f;
+    uint32_t m = 0u;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const bool row = yl <= float(4 * r + 3) && yh >= float(4 * r);
+        m |= (row && c0 ? 1u : 0u) << (2 * r);
+        m |= (row && c1 ? 1u : 0u) << (2 * r + 1);
+    }
+    return m;
+}
+
+// Compacts, in order, the staged entries j (< 256) for which `hit` holds into `list`; returns
+// the count.  Warp-cooperative: every lane of the warp must call it.
+template <typename Hit>
+__device__ __forceinline__ int compact_warp(uint8_t* list, Hit hit) {
+    const unsigned lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    int n = 0;
+#pragma unroll
+    for (int c = 0; c < kBatch / 32; ++c) {
+        const int j = c * 32 + int(lane);
+        const bool h = hit(j);
+        const uint32_t b = __ballot_sync(kFull, h);
+        if (h) list[n + __popc(b & lt)] = uint8_t(j);
+        n += __popc(b);
+    }
+    __syncwarp();
+    return n;
 }
 
 __global__ void __launch_bounds__(kTilePixels) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
@@ -28,43 +79,52 @@ __global__ void __launch_bounds__(kTilePixels) k_raster_fwd(CameraF cam, const R
                                                            float* __restrict__ final_T,
                                                            uint32_t* __restrict__ n_contrib) {
     __shared__ float4 s_p[kBatch], s_q[kBatch], s_c[kBatch];
+    __shared__ uint32_t s_mask[kBatch];
+    __shared__ uint8_t s_list[kWarps][kBatch];
     const int tile = blockIdx.x;
-    int px, py;
-    tile_pixel(cam, tile, px, py);
+    const int warp = threadIdx.x >> 5;
+    int tx0, ty0, px, py;
+    tile_pixel(cam, tile, tx0, ty0, px, py);
     const bool inside = px < cam.W && py < cam.H;
     const uint2 range = ranges[tile];
     const float fx = float(px), fy = float(py);
     float T = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
-    uint32_t count = 0;
+    uint32_t stop = range.y;  // one past the last entry this pixel examined
     bool done = !inside;
+    const uint32_t wbit = 1u << warp;
+    uint8_t* my_list = s_list[warp];
     for (uint32_t base = range.x; base < range.y; base += kBatch) {
         // every thread reaches this barrier; the block leaves once all 256 pixels are done
         if (__syncthreads_count(done) == kBatch) break;
         const uint32_t e = base + threadIdx.x;
+        uint32_t m = 0u;
         if (e < range.y) {
             const Record& r = rec[list[e]];
             s_p[threadIdx.x] = r.p;
             s_q[threadIdx.x] = r.q;
             s_c[threadIdx.x] = r.c;
+            m = warp_mask(r.p, r.q, tx0, ty0);
         }
+        s_mask[threadIdx.x] = m;
         __syncthreads();
-        if (!done) {
-            const int cnt = int(min(uint32_t(kBatch), range.y - base));
-            for (int j = 0; j < cnt; ++j) {
-                ++count;
-                float dx, dy, G, raw;
-                const float alpha = entry_alpha(s_p[j], s_q[j], fx, fy, dx, dy, G, raw);
-                if (alpha < kAlphaMin) continue;
-                const float4 c = s_c[j];
-                const float w = alpha * T;
-                C0 = fmaf(c.x, w, C0);
-                C1 = fmaf(c.y, w, C1);
-                C2 = fmaf(c.z, w, C2);
-                T = fmaf(-T, alpha, T);
-                if (T < kTStop) {
-                    done = true;
-                    break;
-                }
+        if (__all_sync(kFull, done)) continue;
+        const int nl = compact_warp(my_list, [&](int j) { return (s_mask[j] & wbit) != 0u; });
+        if (done) continue;
+        for (int k = 0; k < nl; ++k) {
+            const int j = my_list[k];
+            float dx, dy, G, raw;
+            const float alpha = entry_alpha(s_p[j], s_q[j], fx, fy, dx, dy, G, raw);
+            if (alpha < kAlphaMin) continue;
+            const float4 c = s_c[j];
+            const float w = alpha * T;
+            C0 = fmaf(c.x, w, C0);
+            C1 = fmaf(c.y, w, C1);
+            C2 = fmaf(c.z, w, C2);
+            T = fmaf(-T, alpha, T);
+            if (T < kTStop) {
+                done = true;
+                stop = base + uint32_t(j) + 1u;
+                break;
             }
         }
     }
@@ -74,17 +134,48 @@ __global__ void __launch_bounds__(kTilePixels) k_raster_fwd(CameraF cam, const R
         image[HW + pix] = fmaf(T, bg.y, C1);
         image[2 * HW + pix] = fmaf(T, bg.z, C2);
         final_T[pix] = T;
-        n_contrib[pix] = count;
+        n_contrib[pix] = stop - range.x;
     }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Reduce-scatter of nine per-lane values over the warp in five xor-shuffle steps (9 -> 5 -> 3
+// -> 2 -> 1 -> 1), each lane sending the half of its vector that its partner keeps.  Afterwards
+// lane L holds the warp's sum of value sum_slot(L) (lanes L and L^1 hold the same sum): 46
+// instructions instead of 9 x 5 shuffle-add pairs.
+__device__ __forceinline__ float butterfly9(const float (&v)[9], unsigned lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+    float a[5];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    for (int k = 0; k < 5; ++k) {
+        const float lo = v[k], hi = k + 5 < 9 ? v[k + 5] : 0.f;
+        a[k] = (b4 ? hi : lo) + __shfl_xor_sync(kFull, b4 ? lo : hi, 16);
+    }
+    float b[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const float lo = a[k], hi = k + 3 < 5 ? a[k + 3] : 0.f;
+        b[k] = (b3 ? hi : lo) + __shfl_xor_sync(kFull, b3 ? lo : hi, 8);
+    }
+    float c[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float lo = b[k], hi = k + 2 < 3 ? b[k + 2] : 0.f;
+        c[k] = (b2 ? hi : lo) + __shfl_xor_sync(kFull, b2 ? lo : hi, 4);
+    }
+    float d = (b1 ? c[1] : c[0]) + __shfl_xor_sync(kFull, b1 ? c[0] : c[1], 2);
+    return d + __shfl_xor_sync(kFull, d, 1);
 }
 
-constexpr int kGrads = 9;  // du, dv, dA, dB, dC, dopacity, dr, dg, db
+// Which of the nine sums lane L holds after butterfly9 (-1: padding or the odd twin).
+__device__ __forceinline__ int sum_slot(unsigned lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+    if ((lane & 1) || (b2 && b1) || (b3 && b2) || (b4 && b3 && b1)) return -1;
+    const int v = 5 * b4 + 3 * b3 + 2 * b2 + b1;
+    return v < 9 ? v : -1;
+}
+
+constexpr int kSums = 9;          // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2, gp, w G_rgb
+constexpr int kAccStride = kBatch + 1;  // padding keeps the nine slots of one entry in nine banks
 
 __global__ void __launch_bounds__(kTilePixels) k_raster_bwd(
     CameraF cam, int n, const Record* __restrict__ rec, const uint2* __restrict__ ranges,
@@ -94,35 +185,45 @@ __global__ void __launch_bounds__(kTilePixels) k_raster_bwd(
     float* __restrict__ dcol) {
     __shared__ float4 s_p[kBatch], s_q[kBatch], s_c[kBatch];
     __shared__ uint32_t s_g[kBatch];
-    __shared__ float s_acc[kGrads][kBatch];
+    __shared__ uint32_t s_mask[kBatch];
+    __shared__ uint8_t s_list[kWarps][kBatch];
+    __shared__ float s_acc[kSums * kAccStride];
     __shared__ uint32_t s_max;
     const int tile = blockIdx.x;
-    int px, py;
-    tile_pixel(cam, tile, px, py);
+    const int warp = threadIdx.x >> 5;
+    const unsigned lane = threadIdx.x & 31;
+    int tx0, ty0, px, py;
+    tile_pixel(cam, tile, tx0, ty0, px, py);
     const bool inside = px < cam.W && py < cam.H;
     const uint2 range = ranges[tile];
+    const uint32_t len = range.y - range.x;
     const size_t HW = size_t(cam.W) * cam.H, pix = inside ? size_t(py) * cam.W + px : 0;
-    const uint32_t my_n = inside ? n_contrib[pix] : 0u;
+    // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the min()
+    // keeps inconsistent caller data inside the tile's list
+    const uint32_t my_n = inside ? min(n_contrib[pix], len) : 0u;
     float T = inside ? final_T[pix] : 1.f;
     const float G0 = inside ? dL_dimage[pix] : 0.f;
     const float G1 = inside ? dL_dimage[HW + pix] : 0.f;
     const float G2 = inside ? dL_dimage[2 * HW + pix] : 0.f;
     float S0 = bg.x, S1 = bg.y, S2 = bg.z;  // colour behind the current entry, per unit T
     if (threadIdx.x == 0) s_max = 0;
+#pragma unroll
+    for (int k = 0; k < kSums; ++k) s_acc[k * kAccStride + threadIdx.x] = 0.f;
     __syncthreads();
-    const uint32_t wmax = __reduce_max_sync(0xffffffffu, my_n);
-    if ((threadIdx.x & 31) == 0) atomicMax(&s_max, wmax);
+    const uint32_t wmax = __reduce_max_sync(kFull, my_n);
+    if (lane == 0) atomicMax(&s_max, wmax);
     __syncthreads();
-    // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the min()
-    // keeps inconsistent caller data inside the tile's list
-    const uint32_t len = range.y - range.x;
-    const uint32_t my_end = range.x + min(my_n, len);
-    const uint32_t walk_end = range.x + min(s_max, len);
+    const uint32_t my_end = range.x + my_n;
+    const uint32_t warp_end = range.x + wmax;
+    const uint32_t walk_end = range.x + s_max;
     const float fx = float(px), fy = float(py);
-    const unsigned lane = threadIdx.x & 31;
+    const uint32_t wbit = 1u << warp;
+    const int slot = sum_slot(lane);
+    uint8_t* my_list = s_list[warp];
     for (uint32_t batch_end = walk_end; batch_end > range.x;) {
         const uint32_t batch_start = batch_end - range.x > uint32_t(kBatch) ? batch_end - kBatch : range.x;
         const int cnt = int(batch_end - batch_start);
+        uint32_t m = 0u;
         if (int(threadIdx.x) < cnt) {
             const uint32_t g = list[batch_start + threadIdx.x];
             const Record& r = rec[g];
@@ -130,66 +231,83 @@ __global__ void __launch_bounds__(kTilePixels) k_raster_bwd(
             s_p[threadIdx.x] = r.p;
             s_q[threadIdx.x] = r.q;
             s_c[threadIdx.x] = r.c;
+            m = warp_mask(r.p, r.q, tx0, ty0);
         }
-#pragma unroll
-        for (int k = 0; k < kGrads; ++k) s_acc[k][threadIdx.x] = 0.f;
+        s_mask[threadIdx.x] = m;
         __syncthreads();
-        for (int j = cnt - 1; j >= 0; --j) {
-            float gr[kGrads];
+        const int nl = compact_warp(my_list, [&](int j) {
+            return (s_mask[j] & wbit) != 0u && batch_start + uint32_t(j) < warp_end;
+        });
+        for (int k = nl - 1; k >= 0; --k) {
+            const int j = my_list[k];
+            float v[kSums];
 #pragma unroll
-            for (int k = 0; k < kGrads; ++k) gr[k] = 0.f;
+            for (int t = 0; t < kSums; ++t) v[t] = 0.f;
             bool act = false;
             if (batch_start + uint32_t(j) < my_end) {
-                const float4 p = s_p[j], q = s_q[j];
                 float dx, dy, G, raw;
-                const float alpha = entry_alpha(p, q, fx, fy, dx, dy, G, raw);
+                const float alpha = entry_alpha(s_p[j], s_q[j], fx, fy, dx, dy, G, raw);
                 if (alpha >= kAlphaMin) {
                     act = true;
                     const float4 c = s_c[j];
                     const float one_m = 1.f - alpha;
                     const float Tj = __fdividef(T, one_m);
                     const float w = alpha * Tj;
-                    gr[6] = w * G0;
-                    gr[7] = w * G1;
-                    gr[8] = w * G2;
+                    v[6] = w * G0;
+                    v[7] = w * G1;
+                    v[8] = w * G2;
                     const float dalpha = Tj * ((c.x - S0) * G0 + (c.y - S1) * G1 + (c.z - S2) * G2);
                     S0 = fmaf(alpha, c.x, one_m * S0);
                     S1 = fmaf(alpha, c.y, one_m * S1);
                     S2 = fmaf(alpha, c.z, one_m * S2);
                     T = Tj;
                     if (raw <= kAlphaMax) {  // not clamped: alpha = opacity * exp(power)
-                        gr[5] = G * dalpha;
-                        const float gp = alpha * dalpha;  // dL/dpower
-                        gr[2] = -0.5f * dx * dx * gp;
-                        gr[3] = -dx * dy * gp;
-                        gr[4] = -0.5f * dy * dy * gp;
-                        gr[0] = gp * fmaf(p.w, dx, q.w * dy);  // A dx + B dy
-                        gr[1] = gp * fmaf(c.w, dy, q.w * dx);  // C dy + B dx
+                        const float gp = alpha * dalpha;  // dL/dpower at this pixel
+                        v[0] = gp * dx;
+                        v[1] = gp * dy;
+                        v[2] = v[0] * dx;
+                        v[3] = v[0] * dy;
+                        v[4] = v[1] * dy;
+                        v[5] = gp;
                     }
                 }
             }
-            if (__any_sync(0xffffffffu, act)) {
-#pragma unroll
-                for (int k = 0; k < kGrads; ++k) {
-                    const float v = warp_sum(gr[k]);
-                    if (lane == 0 && v != 0.f) atomicAdd(&s_acc[k][j], v);
-                }
+            if (__any_sync(kFull, act)) {
+                const float sum = butterfly9(v, lane);
+                if (slot >= 0) atomicAdd(&s_acc[slot * kAccStride + j], sum);
             }
         }
         __syncthreads();
         if (int(threadIdx.x) < cnt) {
-            const uint32_t g = s_g[threadIdx.x];
-            const size_t N = size_t(n);
-            float v;
-            if ((v = s_acc[0][threadIdx.x]) != 0.f) atomicAdd(dm2 + g, v);
-            if ((v = s_acc[1][threadIdx.x]) != 0.f) atomicAdd(dm2 + N + g, v);
-            if ((v = s_acc[2][threadIdx.x]) != 0.f) atomicAdd(dcon + g, v);
-            if ((v = s_acc[3][threadIdx.x]) != 0.f) atomicAdd(dcon + N + g, v);
-            if ((v = s_acc[4][threadIdx.x]) != 0.f) atomicAdd(dcon + 2 * N + g, v);
-            if ((v = s_acc[5][threadIdx.x]) != 0.f) atomicAdd(dop + g, v);
-            if ((v = s_acc[6][threadIdx.x]) != 0.f) atomicAdd(dcol + g, v);
-            if ((v = s_acc[7][threadIdx.x]) != 0.f) atomicAdd(dcol + N + g, v);
-            if ((v = s_acc[8][threadIdx.x]) != 0.f) atomicAdd(dcol + 2 * N + g, v);
+            // per-entry tile sums -> gradients of the entry's Gaussian:
+            //   du = A sum(gp dx) + B sum(gp dy), dv = B sum(gp dx) + C sum(gp dy),
+            //   dA = -sum(gp dx^2)/2, dB = -sum(gp dx dy), dC = -sum(gp dy^2)/2,
+            //   dopacity = sum(gp)/opacity (gp = opacity exp(power) dL/dalpha), dcolour = sum(w G)
+            const int t = threadIdx.x;
+            float a[kSums];
+            bool any = false;
+#pragma unroll
+            for (int k = 0; k < kSums; ++k) {
+                a[k] = s_acc[k * kAccStride + t];
+                s_acc[k * kAccStride + t] = 0.f;
+                any |= a[k] != 0.f;
+            }
+            if (any) {
+                const uint32_t g = s_g[t];
+                const size_t N = size_t(n);
+                const float4 p = s_p[t], q = s_q[t];
+                constexpr float kLn2 = 0.6931471805599453f;
+                const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
+                atomicAdd(dm2 + g, fmaf(A, a[0], B * a[1]));
+                atomicAdd(dm2 + N + g, fmaf(B, a[0], C * a[1]));
+                atomicAdd(dcon + g, -0.5f * a[2]);
+                atomicAdd(dcon + N + g, -a[3]);
+                atomicAdd(dcon + 2 * N + g, -0.5f * a[4]);
+                atomicAdd(dop + g, a[5] / p.z);
+                atomicAdd(dcol + g, a[6]);
+                atomicAdd(dcol + N + g, a[7]);
+                atomicAdd(dcol + 2 * N + g, a[8]);
+            }
         }
         __syncthreads();
         batch_end = batch_start;

@@ -26,13 +26,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Packed record the projection writes once per Gaussian and both rasterisers gather per list
 // entry.  Three 16-byte words:
-//   p = (u, v, opacity, A)        position, opacity, raw conic A
-//   q = (qa, qb, qc, B)           power in log2 units: power2 = qa dx^2 + qb dx dy + qc dy^2
-//                                 with qa = -A/2 log2(e), qb = -B log2(e), qc = -C/2 log2(e)
-//   c = (r, g, b, C)              colour, raw conic C
+//   p = (u, v, opacity, ext_x)    position, opacity, half-width of the alpha >= 1/255 region
+//   q = (qa, qb, qc, ext_y)       power in log2 units: power2 = qa dx^2 + qb dx dy + qc dy^2
+//                                 with qa = -A/2 log2(e), qb = -B log2(e), qc = -C/2 log2(e);
+//                                 half-height of the alpha >= 1/255 region
+//   c = (r, g, b, 0)              colour
 // Storing the log2-scaled quadratic lets the rasterisers evaluate exp(power) as one ex2 on the
 // multi-function unit; forward and backward read the same words, so both evaluate alpha with
-// bit-identical arithmetic.
+// bit-identical arithmetic.  The extents (negative: never reaches 1/255) let a warp skip entries
+// that cannot pass the alpha threshold anywhere in its pixels; skipping such an entry is exactly
+// what evaluating it and failing the threshold would do.
 struct __align__(16) Record {
     float4 p;
     float4 q;
