@@ -318,33 +318,14 @@ __global__ void __launch_bounds__(256) k_project_bwd(
             for (int k = 0; k < 3 * K; ++k) dsh[size_t(k) * N + i] = 0.f;
         return;
     }
-    // conic = Q = Sigma_2d^-1: dL/dSigma_2d = -Q Gq Q, Gq = [[gA, gB/2], [gB/2, gC]]
+    // conic = Q = Sigma_2d^-1 with Sigma_2d = U S^2 U^T + 0.3 I, U = T Rq; the conic's gradient
+    // Gq = [[gA, gB/2], [gB/2, gC]] gives dL/dSigma_2d = -Q Gq Q.  Everything below goes through
+    // W = Q U and Q y = adj(Sigma_2d) y / det with
+    //   adj(Sigma_2d) y = 0.3 y + sum_k s_k^2 u_k_perp (u_k_perp . y),  u_perp = (-u1, u0),
+    // so the large s_j^2 u_j u_j^T part of a needle-like Gaussian is never subtracted from itself:
+    //   Z = W^T Gq W,  ds_j = -2 s_j Z_jj,  dRq = -2 Rq Z S^2  (T^T dU with T = U Rq^T),
+    //   dU_j = -2 s_j^2 Q (Gq w_j),  dT = dU Rq^T.
     const float gA = __ldg(dcon + i), gB = 0.5f * __ldg(dcon + N + i), gC = __ldg(dcon + 2 * N + i);
-    const float A = G.A, B = G.B, C = G.C;
-    const float qg00 = A * gA + B * gB, qg01 = A * gB + B * gC;
-    const float qg10 = B * gA + C * gB, qg11 = B * gB + C * gC;
-    const float g00 = -(qg00 * A + qg01 * B);
-    const float g01 = -(qg00 * B + qg01 * C);
-    const float g11 = -(qg10 * B + qg11 * C);
-    // Sigma_2d = U S^2 U^T + 0.3 I with U = T Rq and G2 = [[g00, g01], [g01, g11]]:
-    //   dU = 2 G2 U S^2 (feeds dT = dU Rq^T, the mean's path through J);
-    //   scales and rotation go through W = Q U = Sigma_2d^-1 U instead, since
-    //   dRq = T^T dU = -2 Rq Z S^2 and ds_j = -2 s_j Z_jj with Z = W^T Gq W (T = U Rq^T).
-    //   Column j of adj(Sigma_2d) U is 0.3 u_j + sum_{k != j} s_k^2 m_jk (U1k, -U0k): the
-    //   s_j^2 u_j u_j^T part of Sigma_2d cancels out exactly and is never formed.
-    float dU[6];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        dU[j] = 2.f * G.s2[j] * (g00 * G.U[j] + g01 * G.U[3 + j]);
-        dU[3 + j] = 2.f * G.s2[j] * (g01 * G.U[j] + g11 * G.U[3 + j]);
-    }
-    float dT[6];
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-#pragma unroll
-        for (int r = 0; r < 3; ++r)
-            dT[k * 3 + r] = dU[k * 3 + 0] * G.Rq[r * 3 + 0] + dU[k * 3 + 1] * G.Rq[r * 3 + 1] +
-                            dU[k * 3 + 2] * G.Rq[r * 3 + 2];
     const float mn[3][3] = {{0.f, G.m01, G.m02}, {-G.m01, 0.f, G.m12}, {-G.m02, -G.m12, 0.f}};
     const float inv_det = 1.0f / G.det;
     float Wx[3], Wy[3];
@@ -354,14 +335,36 @@ __global__ void __launch_bounds__(256) k_project_bwd(
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
             if (k == j) continue;
-            const float mm = G.s2[k] * mn[j][k];
+            const float mm = G.s2[k] * mn[j][k];  // s_k^2 m_jk = -s_k^2 (u_k_perp . u_j)
             wx = fmaf(mm, G.U[3 + k], wx);
             wy = fmaf(-mm, G.U[k], wy);
         }
         Wx[j] = wx * inv_det;
         Wy[j] = wy * inv_det;
     }
-    // Z = W^T Gq W with Gq = [[gA, gB], [gB, gC]] (gB already halved)
+    float dU[6];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const float yx = gA * Wx[j] + gB * Wy[j];  // y = Gq w_j
+        const float yy = gB * Wx[j] + gC * Wy[j];
+        float ax = kDilation * yx, ay = kDilation * yy;  // adj(Sigma_2d) y
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const float ux = G.U[k], uy = G.U[3 + k];
+            const float d = G.s2[k] * fmaf(-uy, yx, ux * yy);  // s_k^2 (u_k_perp . y)
+            ax = fmaf(-uy, d, ax);
+            ay = fmaf(ux, d, ay);
+        }
+        dU[j] = -2.f * G.s2[j] * ax * inv_det;
+        dU[3 + j] = -2.f * G.s2[j] * ay * inv_det;
+    }
+    float dT[6];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+            dT[k * 3 + r] = dU[k * 3 + 0] * G.Rq[r * 3 + 0] + dU[k * 3 + 1] * G.Rq[r * 3 + 1] +
+                            dU[k * 3 + 2] * G.Rq[r * 3 + 2];
     float Z[3][3];
 #pragma unroll
     for (int j = 0; j < 3; ++j)

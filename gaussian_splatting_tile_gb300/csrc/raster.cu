@@ -205,7 +205,9 @@ __global__ void __launch_bounds__(kTilePixels) k_raster_bwd(
     const float G0 = inside ? dL_dimage[pix] : 0.f;
     const float G1 = inside ? dL_dimage[HW + pix] : 0.f;
     const float G2 = inside ? dL_dimage[2 * HW + pix] : 0.f;
-    float S0 = bg.x, S1 = bg.y, S2 = bg.z;  // colour behind the current entry, per unit T
+    // the colour behind an entry (per unit T) only enters the gradient through its dot product
+    // with dL/dC, so that scalar is carried instead of the colour
+    float SG = bg.x * G0 + bg.y * G1 + bg.z * G2;
     if (threadIdx.x == 0) s_max = 0;
 #pragma unroll
     for (int k = 0; k < kSums; ++k) s_acc[k * kAccStride + threadIdx.x] = 0.f;
@@ -256,10 +258,9 @@ __global__ void __launch_bounds__(kTilePixels) k_raster_bwd(
                     v[6] = w * G0;
                     v[7] = w * G1;
                     v[8] = w * G2;
-                    const float dalpha = Tj * ((c.x - S0) * G0 + (c.y - S1) * G1 + (c.z - S2) * G2);
-                    S0 = fmaf(alpha, c.x, one_m * S0);
-                    S1 = fmaf(alpha, c.y, one_m * S1);
-                    S2 = fmaf(alpha, c.z, one_m * S2);
+                    const float cG = fmaf(c.x, G0, fmaf(c.y, G1, c.z * G2));
+                    const float dalpha = Tj * (cG - SG);
+                    SG = fmaf(alpha, cG, one_m * SG);
                     T = Tj;
                     if (raw <= kAlphaMax) {  // not clamped: alpha = opacity * exp(power)
                         const float gp = alpha * dalpha;  // dL/dpower at this pixel

@@ -60,6 +60,7 @@ const char* rs_error_string(int code) {
         case RS_ERR_CAPACITY: return "entry count exceeds capacity; *n_entries holds the required count";
         case RS_ERR_WORKSPACE: return "workspace smaller than rs_bin_workspace_size reports";
         case RS_ERR_CUDA: return "CUDA runtime error";
+        case RS_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up; the outputs are not valid";
         default: return "unknown error code";
     }
 }
@@ -74,7 +75,7 @@ int rs_project(const rs_camera* camera, const rs_gaussians* gaussians, const rs_
 }
 
 int rs_bin_workspace_size(int32_t n, const rs_camera* camera, size_t capacity, size_t* bytes) {
-    if (!camera_ok(camera) || !n_ok(n) || !bytes || capacity > size_t(UINT32_MAX))
+    if (!camera_ok(camera) || !n_ok(n) || !bytes || capacity > size_t(RS_MAX_ENTRIES))
         return RS_ERR_INVALID_ARG;
     const CameraF cam = rs::make_camera(*camera);
     *bytes = rs::plan_bin(n, cam, capacity).total_bytes;
@@ -84,7 +85,7 @@ int rs_bin_workspace_size(int32_t n, const rs_camera* camera, size_t capacity, s
 int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
            size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
            uint32_t* d_point_list, uint32_t* d_tile_ranges, size_t* n_entries, void* stream) {
-    if (!camera_ok(camera) || !n_ok(n) || !n_entries || capacity > size_t(UINT32_MAX))
+    if (!camera_ok(camera) || !n_ok(n) || !n_entries || capacity > size_t(RS_MAX_ENTRIES))
         return RS_ERR_INVALID_ARG;
     if (!d_tile_ranges || !aligned(d_tile_ranges, 8)) return RS_ERR_INVALID_ARG;
     if (!d_workspace || !aligned(d_workspace, 256)) return RS_ERR_INVALID_ARG;
@@ -98,17 +99,20 @@ int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     rs_projected empty{};
     const rs_projected& p = proj ? *proj : empty;
-    cudaError_t e = rs::launch_bin_scan(plan, cam, p, ws, d_tile_ranges, s);
+    cudaError_t e = rs::launch_bin(plan, cam, p, ws, d_keys_sorted, d_point_list, d_tile_ranges, s);
     if (e != cudaSuccess) return RS_ERR_CUDA;
-    // the path's one device-to-host read: the number of entries
-    uint64_t E = 0;
-    e = cudaMemcpyAsync(&E, ws + plan.off_total, sizeof(E), cudaMemcpyDeviceToHost, s);
+    // the path's one device-to-host read: the entry count (and the sort's wait flag)
+    struct {
+        uint64_t E;
+        uint32_t error, pad;
+    } result{};
+    e = cudaMemcpyAsync(&result, ws + plan.off_result, sizeof(result), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return RS_ERR_CUDA;
-    *n_entries = size_t(E);
-    if (E > uint64_t(capacity)) return RS_ERR_CAPACITY;
-    return cuda_rc(rs::launch_bin_sort(plan, cam, p, ws, E, d_keys_sorted, d_point_list,
-                                       d_tile_ranges, s));
+    *n_entries = size_t(result.E);
+    if (result.E > uint64_t(capacity)) return RS_ERR_CAPACITY;
+    if (result.error != 0) return RS_ERR_DEVICE_TIMEOUT;
+    return RS_OK;
 }
 
 int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,

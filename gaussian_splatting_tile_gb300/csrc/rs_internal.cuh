@@ -106,22 +106,23 @@ cudaError_t launch_project_bwd(const CameraF& cam, const rs_gaussians& g, const 
 struct BinPlan {
     int32_t n;
     int n_tiles;
-    int key_bits;          // 32 + ceil(log2(n_tiles))
-    int passes;            // ceil(key_bits / 8)
+    int tile_bits;         // ceil(log2(n_tiles)), at least 1
+    int tile_passes;       // ceil(tile_bits / 8)
     size_t capacity;
+    size_t depth_tiles, tile_tiles;  // sort tiles of the depth sort and of the tile sort
     // workspace layout (byte offsets)
-    size_t off_offsets, off_scan_tmp, off_keys, off_vals, off_keys2, off_vals2, off_hist,
-        off_hist_tmp, off_total, total_bytes;
-    size_t scan_tmp_elems, hist_tmp_elems;
+    size_t off_dkeys, off_dvals, off_tiles_sorted, off_offsets, off_scan_tmp, off_tkeys, off_tvals;
+    size_t off_ctl, off_result, off_counters, off_ghist_depth, off_ghist_tile, off_status_depth,
+        off_status_tile, ctl_bytes, total_bytes;
+    size_t scan_tmp_elems;
 };
 BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity);
-// Scan tiles_touched into offsets and leave the total on the device at ws + off_total.
-cudaError_t launch_bin_scan(const BinPlan& plan, const CameraF& cam, const rs_projected& p,
-                            uint8_t* ws, uint32_t* tile_ranges, cudaStream_t s);
-// Expand, sort and extract ranges for `E` entries.
-cudaError_t launch_bin_sort(const BinPlan& plan, const CameraF& cam, const rs_projected& p,
-                            uint8_t* ws, uint64_t E, uint64_t* keys_out, uint32_t* point_list,
-                            uint32_t* tile_ranges, cudaStream_t s);
+// Enqueues the whole binning: depth sort of the Gaussians, scan of their tile counts, expansion
+// in depth order, stable sort by tile, ranges.  Afterwards ws + off_result holds
+// {E (uint64), error (uint32)}: E is the entry count (nothing past the capacity is written when
+// E > capacity) and error is nonzero when a bounded wait of the sort gave up.
+cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_projected& p, uint8_t* ws,
+                       uint64_t* keys_out, uint32_t* point_list, uint32_t* tile_ranges, cudaStream_t s);
 
 cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
                               const uint32_t* list, float3 bg, float* image, float* final_T,

@@ -48,6 +48,8 @@ class Renderer:
         self.device = torch.device(device)
         self.n_tiles = ((camera.width + 15) // 16) * ((camera.height + 15) // 16)
         self.keep_keys = keep_keys
+        self.cam_struct = rs.camera_struct(camera)
+        self._bound = None
         self.proj = rs.DeviceProjected.empty(self.n, self.device)
         H, W = camera.height, camera.width
         self.image = torch.empty(3, H, W, dtype=torch.float32, device=self.device)
@@ -68,29 +70,67 @@ class Renderer:
     def set_camera(self, camera):
         assert camera.width == self.camera.width and camera.height == self.camera.height
         self.camera = camera
+        rs.set_camera_struct(self.cam_struct, camera)
+
+    # ---- prepared calls: the ctypes arguments of this renderer's buffers, built once
+    def _prepare(self, g: rs.DeviceGaussians, bg):
+        ptrs = tuple(0 if t is None else t.data_ptr() for t in (g.means, g.scales, g.quats, g.opacity, g.sh, g.colors))
+        key = (ptrs, g.n, g.sh_degree, tuple(float(x) for x in bg), self.capacity, self.grads is not None)
+        if self._bound is not None and self._bound[0] == key:
+            return self._bound[1]
+        import ctypes
+        cam = ctypes.byref(self.cam_struct)
+        gs = g.struct()
+        ps = self.proj.struct()
+        self._keep = (gs, ps)
+        self._E = ctypes.c_size_t(0)
+        bgv = (ctypes.c_float * 3)(*[float(x) for x in bg])
+        self._bgv = bgv
+        vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+        calls = dict(
+            project=rs.PreparedCall("rs_project", (cam, ctypes.byref(gs), ctypes.byref(ps))),
+            bin=rs.PreparedCall("rs_bin", (cam, ctypes.byref(ps), self.n, vp(self.workspace),
+                                           self.workspace.numel(), self.capacity, vp(self.keys_sorted),
+                                           vp(self.point_list), vp(self.tile_ranges), ctypes.byref(self._E))),
+            fwd=rs.PreparedCall("rs_rasterize_fwd", (cam, ctypes.byref(ps), self.n, vp(self.tile_ranges),
+                                                     vp(self.point_list), bgv, vp(self.image),
+                                                     vp(self.final_T), vp(self.n_contrib))))
+        if self.grads is not None:
+            gr = self.grads
+            calls["rbwd_args"] = (cam, ctypes.byref(ps), self.n, vp(self.tile_ranges), vp(self.point_list),
+                                  bgv, vp(self.final_T), vp(self.n_contrib))
+            calls["rbwd_out"] = (vp(gr.dmeans2d), vp(gr.dconic), vp(gr.dopacity), vp(gr.dcolor))
+            calls["pbwd"] = rs.PreparedCall("rs_project_bwd", (
+                cam, ctypes.byref(gs), ctypes.byref(ps), vp(gr.dmeans2d), vp(gr.dconic), vp(gr.dcolor),
+                vp(gr.dmeans), vp(gr.dscales), vp(gr.dquats), vp(gr.dsh)))
+        self._bound = (key, calls)
+        return calls
 
     def project(self, g: rs.DeviceGaussians, stream=None):
-        rs.rs_project(self.camera, g, self.proj, stream)
+        self._g = g
+        self._prepare(g, getattr(self, "bg", (0.0, 0.0, 0.0)))["project"].run(rs.stream_handle(stream))
 
     def bin(self, stream=None) -> int:
+        h = rs.stream_handle(stream)
         while True:
             try:
-                return rs.rs_bin(self.camera, self.proj, self.n, self.workspace, self.capacity,
-                                 self.keys_sorted, self.point_list, self.tile_ranges, stream)
+                self._prepare(self._g, getattr(self, "bg", (0.0, 0.0, 0.0)))["bin"].run(h)
+                return int(self._E.value)
             except rs.RsError as e:
                 if e.code != rs.RS_ERR_CAPACITY:
                     raise
-                self._alloc(int(e.n_entries * 1.25) + 1024)
+                self._alloc(int(self._E.value * 1.25) + 1024)
+                self._bound = None
 
     def rasterize(self, bg=(0.0, 0.0, 0.0), stream=None):
-        rs.rs_rasterize_fwd(self.camera, self.proj, self.n, self.tile_ranges, self.point_list, bg,
-                            self.image, self.final_T, self.n_contrib, stream)
+        self.bg = tuple(bg)
+        self._prepare(self._g, self.bg)["fwd"].run(rs.stream_handle(stream))
 
     def forward(self, g: rs.DeviceGaussians, bg=(0.0, 0.0, 0.0), stream=None) -> Forward:
+        self.bg = tuple(bg)
         self.project(g, stream)
         E = self.bin(stream)
         self.rasterize(bg, stream)
-        self.bg = tuple(bg)
         self.n_entries = E
         return Forward(self.proj, E, self.point_list, self.keys_sorted, self.tile_ranges,
                        self.image, self.final_T, self.n_contrib, self.bg)
@@ -102,20 +142,24 @@ class Renderer:
             f = lambda *s: torch.empty(*s, dtype=torch.float32, device=d)
             self.grads = Backward(f(2, n), f(3, n), f(n), f(3, n), f(3, n), f(3, n), f(4, n),
                                   f(3 * K, n) if K else None)
-        return self.grads
+            self._bound = None  # prepared calls must point at the new gradient buffers
+            return True
+        return False
 
     def rasterize_backward(self, dL_dimage, stream=None) -> Backward:
-        g = self.grads
-        rs.rs_rasterize_bwd(self.camera, self.proj, self.n, self.tile_ranges, self.point_list,
-                            self.bg, self.final_T, self.n_contrib, dL_dimage, g.dmeans2d, g.dconic,
-                            g.dopacity, g.dcolor, stream)
-        return g
+        import ctypes
+        if not (dL_dimage.is_cuda and dL_dimage.dtype == torch.float32 and dL_dimage.is_contiguous()
+                and dL_dimage.numel() >= 3 * self.camera.width * self.camera.height):
+            raise ValueError("dL_dimage must be a contiguous float32 CUDA tensor [3, H, W]")
+        calls = self._prepare(self._g, self.bg)
+        fn = rs.PreparedCall("rs_rasterize_bwd", calls["rbwd_args"] + (ctypes.c_void_p(dL_dimage.data_ptr()),)
+                             + calls["rbwd_out"])
+        fn.run(rs.stream_handle(stream))
+        return self.grads
 
     def project_backward(self, gs: rs.DeviceGaussians, stream=None) -> Backward:
-        g = self.grads
-        rs.rs_project_bwd(self.camera, gs, self.proj, g.dmeans2d, g.dconic, g.dcolor, g.dmeans,
-                          g.dscales, g.dquats, g.dsh, stream)
-        return g
+        self._prepare(gs, self.bg)["pbwd"].run(rs.stream_handle(stream))
+        return self.grads
 
     def backward(self, gs: rs.DeviceGaussians, dL_dimage, stream=None) -> Backward:
         self._grads(gs.sh_degree)

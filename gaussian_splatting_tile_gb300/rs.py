@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "librs.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "rs.h")
 
 RS_OK, RS_ERR_INVALID_ARG, RS_ERR_CAPACITY, RS_ERR_WORKSPACE, RS_ERR_CUDA = 0, -1, -2, -3, -4
+RS_ERR_DEVICE_TIMEOUT = -5
 RECORD_BYTES = 48
 TILE = 16
 
@@ -204,6 +205,40 @@ class DeviceProjected:
         s.d_tiles_touched = _ptr(self.tiles_touched, None, n, "tiles_touched")
         s.d_records = _ptr(self.records, torch.uint8, n * RECORD_BYTES, "records")
         return s
+
+
+# ------------------------------------------------------------------ prepared calls
+class PreparedCall:
+    """One C-ABI call with its arguments marshalled once: the pointer arguments of a fixed set of
+    buffers are built a single time and the camera struct is shared (and updated in place when the
+    view changes), so a frame loop pays only the foreign call.  `run(stream_handle)` returns the
+    library's return code after raising on errors."""
+
+    def __init__(self, name: str, args):
+        self.name = name
+        self.fn = getattr(lib(), name)
+        self.args = tuple(args)
+
+    def run(self, stream_handle) -> int:
+        rc = self.fn(*self.args, stream_handle)
+        if rc != RS_OK:
+            raise RsError(self.name, rc, error_string(rc))
+        return rc
+
+
+def set_camera_struct(c: rs_camera, cam) -> rs_camera:
+    """Overwrite an existing rs_camera with `cam` (prepared calls keep pointing at it)."""
+    R = np.asarray(cam.R, np.float32).reshape(9)
+    t = np.asarray(cam.t, np.float32).reshape(3)
+    c.R[:] = [float(x) for x in R]
+    c.t[:] = [float(x) for x in t]
+    c.fx, c.fy, c.cx, c.cy = float(cam.fx), float(cam.fy), float(cam.cx), float(cam.cy)
+    c.width, c.height = int(cam.width), int(cam.height)
+    return c
+
+
+def stream_handle(stream=None):
+    return _stream(stream)
 
 
 # ------------------------------------------------------------------ the five calls

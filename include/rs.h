@@ -23,7 +23,7 @@
  *  - n = 0 is valid: no Gaussian work is launched; the image is the background, final_T is 1
  *    and n_contrib is 0.
  *  - Limits: 0 <= n <= RS_MAX_GAUSSIANS; 1 <= width, height <= 32768; the number of
- *    (Gaussian, tile) entries is below 2^32.
+ *    (Gaussian, tile) entries is at most RS_MAX_ENTRIES.
  */
 #ifndef RS_H
 #define RS_H
@@ -41,10 +41,12 @@ extern "C" {
 #define RS_ERR_CAPACITY (-2)        /* more entries than `capacity`; *n_entries holds the count */
 #define RS_ERR_WORKSPACE (-3)       /* workspace smaller than rs_bin_workspace_size reports   */
 #define RS_ERR_CUDA (-4)            /* a CUDA runtime call or launch failed                   */
+#define RS_ERR_DEVICE_TIMEOUT (-5)  /* a bounded wait inside a kernel gave up (outputs invalid) */
 
 #define RS_TILE 16                  /* tile edge in pixels (rigel "Binning")                    */
 #define RS_RECORD_BYTES 48          /* packed per-Gaussian record written by rs_project         */
 #define RS_MAX_GAUSSIANS 67108864   /* 2^26                                                     */
+#define RS_MAX_ENTRIES 1073741823   /* 2^30 - 1: largest `capacity` of rs_bin                   */
 
 /* Pinhole camera: a world point m maps to p = R m + t (R row-major, world to camera), then to
  * pixel (fx p.x/p.z + cx, fy p.y/p.z + cy).  Pixel (x, y) is sampled at integer coordinates.
@@ -114,18 +116,22 @@ int rs_project(const rs_camera* camera, const rs_gaussians* gaussians, const rs_
 int rs_bin_workspace_size(int32_t n, const rs_camera* camera, size_t capacity, size_t* bytes);
 
 /* [2] Binning, rigel README "Binning": one entry per (visible Gaussian, covered tile) with
- * key = (tile_id << 32) | float_bits(depth), tile_id = ty * ceil(W/16) + tx; entries are
- * produced in Gaussian index order (tile rows outer, columns inner) at the offsets of an
- * exclusive scan of tiles_touched, then sorted stably by key on the device (an LSD radix sort
- * over the low 32 + ceil(log2(n_tiles)) bits, "3D Gaussian Splatting ビューワを作る" 4.3), and
- * each tile's [start, end) range is extracted (viewer 4.4; empty tiles get (0, 0)).
+ * key = (tile_id << 32) | float_bits(depth), tile_id = ty * ceil(W/16) + tx, sorted stably by key
+ * on the device -- equal keys keep Gaussian index order, the order in which the entries are
+ * produced (tile rows outer, columns inner) -- and each tile's [start, end) range extracted
+ * (viewer 4.4; empty tiles get (0, 0)).  The 64-bit stable sort runs as an LSD radix sort
+ * ("3D Gaussian Splatting ビューワを作る" 4.3) of the Gaussians by depth followed by one of the
+ * entries, produced in that depth order, by tile id: the same order, in fewer passes.
  * Inputs: `proj` from rs_project (means2d, depth, radius, tiles_touched are read).
  * Outputs: d_point_list [capacity] uint32 Gaussian index per sorted entry; d_tile_ranges
- * [n_tiles][2] uint32; d_keys_sorted [capacity] uint64 (may be NULL); *n_entries (host) = E.
- * The entry count is read back to the host once.  If E > capacity the call returns
- * RS_ERR_CAPACITY after setting *n_entries, so the caller can grow the buffers and call again.
+ * [n_tiles][2] uint32 (8-byte aligned); d_keys_sorted [capacity] uint64 (may be NULL);
+ * *n_entries (host) = E.  The entry count is read back to the host once, at the end.  If
+ * E > capacity the call writes no entry, returns RS_ERR_CAPACITY and sets *n_entries, so the
+ * caller can grow the buffers and call again.
  * d_workspace: at least rs_bin_workspace_size bytes, 256-byte aligned, contents undefined on
- * entry and exit.  Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CAPACITY, RS_ERR_CUDA. */
+ * entry and exit.  Errors: RS_ERR_INVALID_ARG (also capacity > RS_MAX_ENTRIES),
+ * RS_ERR_WORKSPACE, RS_ERR_CAPACITY, RS_ERR_CUDA, RS_ERR_DEVICE_TIMEOUT (a bounded wait of the
+ * sort's look-back gave up; cannot happen while the GPU runs the call's blocks normally). */
 int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
            size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
            uint32_t* d_point_list, uint32_t* d_tile_ranges, size_t* n_entries, void* stream);
@@ -184,7 +190,7 @@ int rs_project_bwd(const rs_camera* camera, const rs_gaussians* gaussians,
  * device image.  Every GPU that loads the library holds that array until the process exits.
  *  - Limit: the call returns RS_ERR_WORKSPACE, before any work, when
  *    rs_bin_workspace_size(n, camera, capacity) exceeds RS_BIN_NOALLOC_SCRATCH_BYTES
- *    (48 MiB: about 2.2 million entries for 160,000 Gaussians at 1920x1080).
+ *    (48 MiB: about 3.3 million entries for 160,000 Gaussians at 1920x1080).
  *  - Set-up: the first call on a device, with that device current, looks up the array's device
  *    address (cudaGetSymbolAddress) and keeps it for later calls; make that first call before
  *    any stream capture.  RS_ERR_CUDA if the lookup fails.
