@@ -29,10 +29,6 @@
 namespace rs {
 namespace {
 
-constexpr int kScanThreads = 256;
-constexpr int kScanItems = 8;
-constexpr int kScanChunk = kScanThreads * kScanItems;  // 2048 elements per block
-
 constexpr int kRsThreads = 256;
 constexpr int kRsWarps = kRsThreads / 32;
 constexpr int kDepthItems = 8;                          // depth sort: 2048 keys per block
@@ -41,120 +37,6 @@ constexpr unsigned kFull = 0xffffffffu;
 
 size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// ---------------------------------------------------------------- device-wide exclusive scan
-// Three phases per level: per-chunk sums, a scan of those sums (recursively), then a per-chunk
-// scan seeded with its chunk's offset.
-
-__device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t v, uint64_t* s_warp, uint64_t& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint64_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        uint64_t w = lane < (kScanThreads / 32) ? s_warp[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint64_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        if (lane < (kScanThreads / 32)) s_warp[lane] = w;
-    }
-    __syncthreads();
-    total = s_warp[kScanThreads / 32 - 1];
-    const uint64_t before = warp > 0 ? s_warp[warp - 1] : 0;
-    __syncthreads();
-    return before + x - v;
-}
-
-template <typename In>
-__global__ void __launch_bounds__(kScanThreads) k_scan_reduce(const In* __restrict__ in, size_t n,
-                                                              uint64_t* __restrict__ sums) {
-    __shared__ uint64_t s_warp[kScanThreads / 32];
-    const size_t base = size_t(blockIdx.x) * kScanChunk;
-    uint64_t acc = 0;
-#pragma unroll
-    for (int k = 0; k < kScanItems; ++k) {
-        const size_t i = base + size_t(k) * kScanThreads + threadIdx.x;
-        if (i < n) acc += uint64_t(in[i]);
-    }
-    uint64_t total;
-    block_exclusive_scan(acc, s_warp, total);
-    if (threadIdx.x == 0) sums[blockIdx.x] = total;
-}
-
-// Scans [0, n) of `in` into `out` (exclusive), adding offsets[blockIdx.x] (if given); if
-// `total_out` is given, the grand total is written there by the last block.
-template <typename In, typename Out>
-__global__ void __launch_bounds__(kScanThreads) k_scan_down(const In* __restrict__ in, size_t n,
-                                                            const uint64_t* __restrict__ offsets,
-                                                            Out* __restrict__ out,
-                                                            uint64_t* __restrict__ total_out) {
-    __shared__ uint64_t s_data[kScanChunk];
-    __shared__ uint64_t s_warp[kScanThreads / 32];
-    const size_t base = size_t(blockIdx.x) * kScanChunk;
-#pragma unroll
-    for (int k = 0; k < kScanItems; ++k) {
-        const int j = k * kScanThreads + threadIdx.x;
-        const size_t i = base + j;
-        s_data[j] = i < n ? uint64_t(in[i]) : 0;
-    }
-    __syncthreads();
-    uint64_t local[kScanItems];
-    uint64_t acc = 0;
-#pragma unroll
-    for (int k = 0; k < kScanItems; ++k) {
-        local[k] = acc;
-        acc += s_data[threadIdx.x * kScanItems + k];
-    }
-    uint64_t total;
-    const uint64_t pre = block_exclusive_scan(acc, s_warp, total);
-    const uint64_t off = offsets ? offsets[blockIdx.x] : 0;
-#pragma unroll
-    for (int k = 0; k < kScanItems; ++k) s_data[threadIdx.x * kScanItems + k] = off + pre + local[k];
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kScanItems; ++k) {
-        const int j = k * kScanThreads + threadIdx.x;
-        const size_t i = base + j;
-        if (i < n) out[i] = Out(s_data[j]);
-    }
-    if (total_out && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) *total_out = off + total;
-}
-
-size_t scan_tmp_elems(size_t n) {
-    size_t t = 0;
-    while (n > size_t(kScanChunk)) {
-        n = ceil_div(n, kScanChunk);
-        t += n;
-    }
-    return t;
-}
-
-// Exclusive scan of n elements into out; `tmp` holds scan_tmp_elems(n) uint64_t.
-template <typename In, typename Out>
-cudaError_t device_exclusive_scan(const In* in, size_t n, Out* out, uint64_t* total,
-                                  uint64_t* tmp, cudaStream_t s) {
-    if (n == 0) return cudaSuccess;
-    const size_t blocks = ceil_div(n, kScanChunk);
-    if (blocks == 1) {
-        k_scan_down<In, Out><<<1, kScanThreads, 0, s>>>(in, n, nullptr, out, total);
-        return cudaGetLastError();
-    }
-    uint64_t* sums = tmp;
-    k_scan_reduce<In><<<unsigned(blocks), kScanThreads, 0, s>>>(in, n, sums);
-    // scan the block sums in place (exclusive), recursively
-    cudaError_t e = device_exclusive_scan<uint64_t, uint64_t>(sums, blocks, sums, nullptr,
-                                                              tmp + blocks, s);
-    if (e != cudaSuccess) return e;
-    k_scan_down<In, Out><<<unsigned(blocks), kScanThreads, 0, s>>>(in, n, sums, out, total);
-    return cudaGetLastError();
-}
 
 // ---------------------------------------------------------------- one-sweep LSD radix sort
 constexpr uint32_t kFlagAgg = 1u << 30;    // status word: this tile's own digit count
@@ -244,20 +126,32 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_hist(const uint32_t* __res
     }
 }
 
-// Exclusive scan of one value per thread over the first 256 threads (others pass 0).
-__device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t v, uint32_t* s_w) {
+// Exclusive scans of two values per thread over the block's 256 threads: returns that of a,
+// stores that of b in eb.
+__device__ __forceinline__ uint32_t block_exclusive_scan2_256(uint32_t a, uint32_t b, uint32_t (*s_w)[kRsWarps],
+                                                              uint32_t& eb) {
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t x = v;
+    uint32_t x = a, y = b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, x, o);
-        if (lane >= uint32_t(o)) x += y;
+        const uint32_t xa = __shfl_up_sync(kFull, x, o), yb = __shfl_up_sync(kFull, y, o);
+        if (lane >= uint32_t(o)) {
+            x += xa;
+            y += yb;
+        }
     }
-    if (lane == 31) s_w[warp] = x;
+    if (lane == 31) {
+        s_w[0][warp] = x;
+        s_w[1][warp] = y;
+    }
     __syncthreads();
-    uint32_t before = 0u;
-    for (uint32_t w = 0; w < warp; ++w) before += s_w[w];
-    return before + x - v;
+    uint32_t ba = 0u, bb = 0u;
+    for (uint32_t w = 0; w < warp; ++w) {
+        ba += s_w[0][w];
+        bb += s_w[1][w];
+    }
+    eb = bb + y - b;
+    return ba + x - a;
 }
 
 // One stable pass over the digit at `shift`.  A block owns ITEMS x 256 consecutive keys of its
@@ -274,8 +168,10 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
     constexpr int R = 1 << RBITS;
     constexpr uint32_t TILE = kRsThreads * ITEMS;
     __shared__ uint32_t s_cnt[kRsWarps][R];
-    __shared__ uint32_t s_off[R];
-    __shared__ uint32_t s_w[kRsWarps];
+    __shared__ uint32_t s_lstart[R];  // first slot of each digit in the tile's reordered keys
+    __shared__ uint32_t s_delta[R];   // global position - slot, per digit
+    __shared__ uint32_t s_w[2][kRsWarps];
+    __shared__ uint32_t s_k[TILE], s_v[TILE];
     __shared__ uint32_t s_tile;
     if (threadIdx.x == 0) s_tile = atomicAdd(ctl.counter + pass, 1u);
     for (int i = threadIdx.x; i < kRsWarps * R; i += kRsThreads) (&s_cnt[0][0])[i] = 0u;
@@ -309,7 +205,7 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
     __syncthreads();
     uint32_t* status = ctl.status + size_t(pass) * ctl.max_tiles * 256;
     const uint32_t t = threadIdx.x;
-    uint32_t excl = 0u, gtotal = 0u;
+    uint32_t excl = 0u, gtotal = 0u, run_out = 0u;
     if (t < uint32_t(R)) {
         uint32_t run = 0u;  // per-warp offsets inside the tile; run ends as the tile's count
 #pragma unroll
@@ -357,17 +253,38 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
             st_relaxed(mine, kFlagIncl | (excl + run));
         }
         gtotal = ctl.ghist[pass * 256 + t];
+        run_out = run;
     }
-    const uint32_t dbase = block_exclusive_scan_256(t < uint32_t(R) ? gtotal : 0u, s_w);
-    if (t < uint32_t(R)) s_off[t] = dbase + excl;
+    // digit d of this tile goes to [dbase(d) + excl(d), ...) globally and to [lstart(d), ...) in
+    // shared memory; keys are first reordered by digit in shared memory so that the global
+    // writes of one digit are consecutive
+    uint32_t lstart;
+    const uint32_t dbase = block_exclusive_scan2_256(t < uint32_t(R) ? gtotal : 0u, t < uint32_t(R) ? run_out : 0u,
+                                                     s_w, lstart);
+    if (t < uint32_t(R)) {
+        s_lstart[t] = lstart;
+        s_delta[t] = dbase + excl - lstart;
+    }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
         if (d[k] < uint32_t(R)) {
-            const uint32_t pos = s_off[d[k]] + s_cnt[warp][d[k]] + rank[k];
-            keys_out[pos] = key[k];
-            vals_out[pos] = val[k];
-            if (GATHER_TILES) tiles_out[pos] = tiles_in[val[k]];
+            const uint32_t slot = s_lstart[d[k]] + s_cnt[warp][d[k]] + rank[k];
+            s_k[slot] = key[k];
+            s_v[slot] = val[k];
+        }
+    }
+    __syncthreads();
+    const uint32_t in_tile = min(TILE, n - tile * TILE);
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+        const uint32_t j = uint32_t(k) * kRsThreads + t;
+        if (j < in_tile) {
+            const uint32_t kk = s_k[j], vv = s_v[j];
+            const uint32_t pos = s_delta[(kk >> shift) & uint32_t(R - 1)] + j;
+            keys_out[pos] = kk;
+            vals_out[pos] = vv;
+            if (GATHER_TILES) tiles_out[pos] = tiles_in[vv];
         }
     }
 }
@@ -387,78 +304,207 @@ __global__ void k_ranges(const uint32_t* __restrict__ tiles, const uint32_t* __r
                          const float* __restrict__ depth, Count count, uint32_t n_tiles,
                          uint32_t* __restrict__ ranges, uint64_t* __restrict__ keys_out) {
     const uint32_t E = count.get();
-    const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
-    const uint32_t tile = tiles[e];
-    if (keys_out) keys_out[e] = (uint64_t(tile) << 32) | uint64_t(__float_as_uint(depth[vals[e]]));
-    if (tile >= n_tiles) return;  // unreachable for ids made by k_expand; keeps writes in bounds
-    if (e == 0 || tiles[e - 1] != tile) ranges[2 * size_t(tile)] = e;
-    if (e == E - 1 || tiles[e + 1] != tile) ranges[2 * size_t(tile) + 1] = e + 1;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride) {
+        const uint32_t tile = tiles[e];
+        if (keys_out) keys_out[e] = (uint64_t(tile) << 32) | uint64_t(__float_as_uint(depth[vals[e]]));
+        if (tile >= n_tiles) continue;  // unreachable for ids made by the expansion; keeps writes in bounds
+        if (e == 0 || tiles[e - 1] != tile) ranges[2 * size_t(tile)] = e;
+        if (e == E - 1 || tiles[e + 1] != tile) ranges[2 * size_t(tile) + 1] = e + 1;
+    }
 }
 
-// ---------------------------------------------------------------- expansion in depth order
-// Block b produces entries [1024 b, 1024 b + 1024).  offsets[i] (i in depth order; E past the
-// end) starts Gaussian perm[i]'s slice.  Every Gaussian before the culled tail of the depth order
-// has at least one entry, so the owners of 1024 consecutive entries are at most 1024 consecutive
-// depth positions: the block finds the first owner with a warp-parallel search, stages the
-// 1025 offsets after it in shared memory and searches there per entry.  Tiles of a Gaussian are
-// taken row by row (tile rows outer, columns inner).
+// ---------------------------------------------------------------- slices and expansion in depth order
+// k_slices gives every Gaussian its slice of the entry list: block b (ids taken from an atomic
+// counter, as in the sort passes) owns Gaussians [1024 b, 1024 b + 1024) of the depth order,
+// scans their tile counts locally and gets the entries of all earlier blocks with a decoupled
+// look-back over 64-bit status words.  It stores each slice start, the Gaussian's tile rectangle
+// (first column | first row << 16, columns) and, for every 1024-entry chunk of the list, the
+// Gaussian owning the chunk's first entry; the last block stores the total E.
+// k_expand then writes 1024 entries per block (tiles of a Gaussian row by row: rows outer,
+// columns inner) and counts the digits of the tile ids for every pass of the tile sort.
+constexpr int kSlThreads = 256;
+constexpr int kSlItems = 4;                          // Gaussians per thread
+constexpr int kSlGauss = kSlThreads * kSlItems;      // Gaussians per block
 constexpr int kExpThreads = 256;
-constexpr int kExpTile = 1024;
+constexpr int kExpChunk = 1024;                      // entries per expansion block
+constexpr unsigned long long kSlAgg = 1ull << 62;    // status: this block's entry count
+constexpr unsigned long long kSlIncl = 2ull << 62;   // status: entries of this and earlier blocks
+constexpr unsigned long long kSlFlags = 3ull << 62;
 
-__global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, int n, Count count,
-                                                       const uint64_t* __restrict__ offsets,
-                                                       const uint32_t* __restrict__ perm,
-                                                       const float* __restrict__ means2d,
-                                                       const int* __restrict__ radius,
-                                                       uint32_t* __restrict__ tile_keys,
-                                                       uint32_t* __restrict__ vals) {
-    __shared__ uint64_t s_off[kExpTile + 1];
-    __shared__ int s_i0;
-    const uint32_t E = count.get();
-    const uint32_t e0 = blockIdx.x * kExpTile;
-    if (e0 >= E) return;
-    if (threadIdx.x < 32) {
-        // last i with offsets[i] <= e0; invariant offsets[lo] <= e0 < offsets[hi] (offsets[n] = E)
-        const unsigned lane = threadIdx.x;
-        int lo = 0, hi = n;
-        while (hi - lo > 1) {
-            const int step = (hi - lo + 31) / 32;
-            const int p = lo + int(lane + 1) * step;
-            const bool le = p < hi && offsets[p] <= e0;
-            const int c = __popc(__ballot_sync(kFull, le));
-            lo += c * step;
-            hi = min(hi, lo + step);
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+struct SliceOut {
+    uint64_t* start;      // [n] first entry of each Gaussian's slice (depth order)
+    uint2* rect;          // [n] tile rectangle of each Gaussian (depth order)
+    uint32_t* owner;      // [chunks] depth position owning entry 1024 c
+    uint32_t chunks;      // ceil(capacity / 1024)
+};
+
+__global__ void __launch_bounds__(kSlThreads) k_slices(CameraF cam, uint32_t n, const uint32_t* __restrict__ perm,
+                                                      const uint32_t* __restrict__ tiles_sorted,
+                                                      const float* __restrict__ means2d,
+                                                      const int* __restrict__ radius, uint32_t* counter,
+                                                      unsigned long long* status, uint32_t* error,
+                                                      uint64_t* total_out, SliceOut out) {
+    __shared__ uint64_t s_w[kSlThreads / 32];
+    __shared__ uint64_t s_prefix;
+    __shared__ uint32_t s_blk;
+    if (threadIdx.x == 0) s_blk = atomicAdd(counter, 1u);
+    __syncthreads();
+    const uint32_t blk = s_blk;
+    const uint32_t nblk = (n + kSlGauss - 1) / kSlGauss;
+    if (blk >= nblk) return;  // uniform; the grid has exactly nblk blocks, so never taken
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t i0 = blk * kSlGauss + threadIdx.x * kSlItems;
+    uint32_t cnt[kSlItems];
+    uint64_t run = 0;
+#pragma unroll
+    for (int k = 0; k < kSlItems; ++k) {
+        cnt[k] = i0 + k < n ? tiles_sorted[i0 + k] : 0u;
+        run += cnt[k];
+    }
+    uint64_t x = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= uint32_t(o)) x += y;
+    }
+    if (lane == 31) s_w[warp] = x;
+    __syncthreads();
+    uint64_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kSlThreads / 32; ++w) {
+        const uint64_t c = s_w[w];
+        before += uint32_t(w) < warp ? c : 0;
+        total += c;
+    }
+    if (warp == 0) {
+        // publish, then look back over 32 predecessors at a time (one per lane)
+        if (lane == 0) st_relaxed64(status + blk, (blk == 0 ? kSlIncl : kSlAgg) | total);
+        uint64_t excl = 0;
+        int pt = int(blk) - 1;
+        bool found = blk == 0;
+        while (!found) {
+            const int q = pt - int(lane);
+            unsigned long long w = q >= 0 ? ld_relaxed64(status + q) : kSlIncl;
+            int spins = 0;
+            while ((w & kSlFlags) == 0ull) {
+                ++spins;
+                if ((spins & 255) == 0 && (spins >= kMaxSpins || ld_relaxed(error) != 0u)) {
+                    atomicOr(error, 1u);
+                    w = kSlIncl;  // give up: the binning is reported as failed
+                    break;
+                }
+                __nanosleep(32);
+                w = ld_relaxed64(status + q);
+            }
+            const uint32_t incl = __ballot_sync(kFull, (w & kSlFlags) == kSlIncl);
+            // nearest inclusive word at lane f: sum lanes 0..f; otherwise all 32 and go on
+            const int f = incl ? __ffs(incl) - 1 : 31;
+            uint64_t c = uint32_t(lane) <= uint32_t(f) ? uint64_t(w & ~kSlFlags) : 0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+            excl += c;
+            found = incl != 0u;
+            pt -= 32;
         }
-        if (lane == 0) s_i0 = lo;
+        if (lane == 0) {
+            if (blk != 0) st_relaxed64(status + blk, kSlIncl | (excl + total));
+            if (blk == nblk - 1) *total_out = excl + total;
+            s_prefix = excl;
+        }
     }
     __syncthreads();
-    const int i0 = s_i0;
-    const int window = min(kExpTile + 1, n + 1 - i0);
-    for (int j = threadIdx.x; j < window; j += kExpThreads)
-        s_off[j] = i0 + j < n ? offsets[i0 + j] : uint64_t(E);
-    __syncthreads();
+    uint64_t start = s_prefix + before + x - run;
 #pragma unroll
-    for (int k = 0; k < kExpTile / kExpThreads; ++k) {
-        const uint32_t e = e0 + k * kExpThreads + threadIdx.x;
-        if (e >= E) break;
-        int lo = 0, hi = window - 1;  // s_off[lo] <= e < s_off[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_off[mid] <= e) lo = mid; else hi = mid;
+    for (int k = 0; k < kSlItems; ++k) {
+        const uint32_t i = i0 + k;
+        if (i < n) {
+            out.start[i] = start;
+            uint2 r = make_uint2(0u, 1u);
+            if (cnt[k]) {
+                const uint32_t g = perm[i];
+                const float u = means2d[g], v = means2d[size_t(n) + g];
+                const float rad = float(radius[g]);
+                const int xl = span_bound(u, rad, cam.TX, false), xh = span_bound(u, rad, cam.TX, true);
+                const int yl = span_bound(v, rad, cam.TY, false);
+                // >= 1 whenever tiles_touched > 0 came from the projection (same span arithmetic)
+                r = make_uint2(uint32_t(xl) | (uint32_t(yl) << 16), uint32_t(max(xh - xl, 1)));
+                // chunks whose first entry falls in this slice
+                const uint64_t end = start + cnt[k];
+                for (uint64_t c = (start + kExpChunk - 1) / kExpChunk; c * kExpChunk < end && c < out.chunks; ++c)
+                    out.owner[c] = i;
+            }
+            out.rect[i] = r;
         }
-        const uint32_t g = perm[i0 + lo];
-        const uint32_t kk = e - uint32_t(s_off[lo]);
-        const float u = means2d[g], v = means2d[size_t(n) + g];
-        const float r = float(radius[g]);
-        const int xl = span_bound(u, r, cam.TX, false), xh = span_bound(u, r, cam.TX, true);
-        const int yl = span_bound(v, r, cam.TY, false);
-        // sx >= 1 whenever tiles_touched[g] > 0 came from rs_project (same span arithmetic); the
-        // max() only keeps inconsistent caller data from dividing by zero
-        const uint32_t sx = uint32_t(max(xh - xl, 1));
-        const uint32_t tx = uint32_t(xl) + kk % sx, ty = uint32_t(yl) + kk / sx;
-        tile_keys[e] = ty * uint32_t(cam.TX) + tx;
-        vals[e] = g;
+        start += cnt[k];
+    }
+}
+
+template <int RBITS>
+__global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n, Count count,
+                                                       const uint32_t* __restrict__ perm, SliceOut sl,
+                                                       int digit_bits, int passes, uint32_t* __restrict__ ghist,
+                                                       uint32_t* __restrict__ tile_keys,
+                                                       uint32_t* __restrict__ vals) {
+    constexpr int R = 1 << RBITS;
+    __shared__ uint64_t s_start[kExpChunk + 1];
+    __shared__ uint2 s_rect[kExpChunk];
+    __shared__ uint32_t s_g[kExpChunk];
+    __shared__ uint32_t s_h[3][R];
+    const uint32_t E = count.get();
+    const uint32_t e0 = blockIdx.x * kExpChunk;
+    if (e0 >= E) return;
+    for (int i = threadIdx.x; i < 3 * R; i += kExpThreads) (&s_h[0][0])[i] = 0u;
+    // every Gaussian before the culled tail of the depth order has at least one entry, so the
+    // owners of 1024 consecutive entries are at most 1024 consecutive depth positions
+    const uint32_t i0 = sl.owner[blockIdx.x];
+    for (int j = threadIdx.x; j <= kExpChunk; j += kExpThreads) {
+        const uint32_t i = i0 + uint32_t(j);
+        s_start[j] = i < n ? sl.start[i] : uint64_t(0xffffffffffffffffull);
+        if (j < kExpChunk && i < n) {
+            s_rect[j] = sl.rect[i];
+            s_g[j] = perm[i];
+        }
+    }
+    __syncthreads();
+    const uint32_t lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < kExpChunk / kExpThreads; ++k) {
+        const uint32_t e = e0 + k * kExpThreads + threadIdx.x;
+        const bool valid = e < E;
+        uint32_t tile = 0u;
+        if (valid) {
+            int lo = 0, hi = kExpChunk;  // s_start[lo] <= e < s_start[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_start[mid] <= e) lo = mid; else hi = mid;
+            }
+            const uint2 r = s_rect[lo];
+            const uint32_t kk = uint32_t(uint64_t(e) - s_start[lo]);
+            const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
+            tile = ty * uint32_t(cam.TX) + tx;
+            tile_keys[e] = tile;
+            vals[e] = s_g[lo];
+        }
+        for (int p = 0; p < passes; ++p) {
+            const uint32_t d = valid ? (tile >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
+            const uint32_t peers = __match_any_sync(kFull, d);
+            if (d < uint32_t(R) && lane == uint32_t(__ffs(peers) - 1)) atomicAdd(&s_h[p][d], uint32_t(__popc(peers)));
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < passes * R; i += kExpThreads) {
+        const uint32_t c = (&s_h[0][0])[i];
+        if (c) atomicAdd(ghist + (i / R) * 256 + (i % R), c);
     }
 }
 
@@ -467,15 +513,6 @@ void tile_sort_launch(const uint32_t* kin, const uint32_t* vin, Count count, int
                       const SortCtl& ctl, unsigned blocks, uint32_t* kout, uint32_t* vout, cudaStream_t s) {
     k_sweep_pass<RBITS, kTileItems, false, false><<<blocks, kRsThreads, 0, s>>>(
         kin, vin, DepthKeySource{}, count, pass * digit, pass, ctl, kout, vout, nullptr, nullptr);
-}
-
-template <int RBITS>
-void tile_hist_launch(const uint32_t* keys, Count count, int digit, int passes, unsigned blocks,
-                      uint32_t* ghist, cudaStream_t s) {
-    if (passes == 1)
-        k_sweep_hist<RBITS, kTileItems, 1, false><<<blocks, kRsThreads, 0, s>>>(keys, DepthKeySource{}, count, digit, ghist);
-    else
-        k_sweep_hist<RBITS, kTileItems, 2, false><<<blocks, kRsThreads, 0, s>>>(keys, DepthKeySource{}, count, digit, ghist);
 }
 
 }  // namespace
@@ -492,13 +529,15 @@ BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity) {
     const size_t N = size_t(n);
     p.depth_tiles = ceil_div(std::max<size_t>(N, 1), size_t(kRsThreads) * kDepthItems);
     p.tile_tiles = ceil_div(std::max<size_t>(capacity, 1), size_t(kRsThreads) * kTileItems);
-    p.scan_tmp_elems = scan_tmp_elems(N);
+    p.slice_blocks = ceil_div(std::max<size_t>(N, 1), size_t(kSlGauss));
+    p.chunks = ceil_div(std::max<size_t>(capacity, 1), size_t(kExpChunk));
     size_t o = 0;
     p.off_dkeys = o;      o = align256(o + 2 * N * sizeof(uint32_t));   // depth keys, 2 buffers
     p.off_dvals = o;      o = align256(o + 2 * N * sizeof(uint32_t));   // Gaussian ids, 2 buffers
     p.off_tiles_sorted = o; o = align256(o + N * sizeof(uint32_t));     // tiles_touched, depth order
-    p.off_offsets = o;    o = align256(o + std::max<size_t>(N, 1) * sizeof(uint64_t));
-    p.off_scan_tmp = o;   o = align256(o + std::max<size_t>(p.scan_tmp_elems, 1) * sizeof(uint64_t));
+    p.off_start = o;      o = align256(o + N * sizeof(uint64_t));     // slice starts, depth order
+    p.off_rect = o;       o = align256(o + N * sizeof(uint2));        // tile rectangles, depth order
+    p.off_owner = o;      o = align256(o + p.chunks * sizeof(uint32_t));  // owner of each chunk
     p.off_tkeys = o;      o = align256(o + 2 * capacity * sizeof(uint32_t));  // tile ids, 2 buffers
     p.off_tvals = o;      o = align256(o + capacity * sizeof(uint32_t));      // + the caller's list
     // control words, zeroed by one kernel at the start of every call:
@@ -507,13 +546,21 @@ BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity) {
     p.off_result = o;               o += 16;
     p.off_counters = o;             o += 8 * sizeof(uint32_t);
     p.off_ghist_depth = o;          o += 4 * 256 * sizeof(uint32_t);
-    p.off_ghist_tile = o;           o += 2 * 256 * sizeof(uint32_t);
+    p.off_ghist_tile = o;           o += 3 * 256 * sizeof(uint32_t);
+    p.off_status_slices = o;        o += p.slice_blocks * sizeof(uint64_t);
     p.off_status_depth = o;         o += 4 * p.depth_tiles * 256 * sizeof(uint32_t);
     p.off_status_tile = o;          o += size_t(p.tile_passes) * p.tile_tiles * 256 * sizeof(uint32_t);
     p.ctl_bytes = o - p.off_ctl;
     o = align256(o);
     p.total_bytes = o;
     return p;
+}
+
+template <int RBITS>
+void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* perm, const SliceOut& sl, int digit,
+                   int passes, uint32_t* ghist, uint32_t* tk, uint32_t* tv, cudaStream_t s) {
+    const unsigned blocks = sl.chunks;
+    k_expand<RBITS><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
 }
 
 cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_projected& p, uint8_t* ws,
@@ -556,32 +603,37 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
     if (e != cudaSuccess) return e;
     const uint32_t* perm = DV[1];
 
-    // 2. offsets of each Gaussian's entries, in depth order; E lands in result[0]
-    uint64_t* offsets = reinterpret_cast<uint64_t*>(ws + plan.off_offsets);
-    uint64_t* tmp = reinterpret_cast<uint64_t*>(ws + plan.off_scan_tmp);
-    e = device_exclusive_scan<uint32_t, uint64_t>(tiles_sorted, size_t(n), offsets, result, tmp, s);
-    if (e != cudaSuccess || plan.capacity == 0) return e;
-
-    // 3. entries in depth order, then a stable sort by tile id
-    const Count ce{0u, result, uint32_t(plan.capacity)};
+    // 2. slices (E lands in result[0]), then the entries in depth order and the digit totals of
+    //    their tile ids
+    const int digit = (plan.tile_bits + plan.tile_passes - 1) / plan.tile_passes;  // <= 8
+    const int rbits = digit <= 4 ? 4 : digit <= 6 ? 6 : digit == 7 ? 7 : 8;
     uint32_t* tk = reinterpret_cast<uint32_t*>(ws + plan.off_tkeys);
     uint32_t* TK[2] = {tk, tk + plan.capacity};
     uint32_t* TV[2] = {point_list, reinterpret_cast<uint32_t*>(ws + plan.off_tvals)};
     int cur = plan.tile_passes % 2;  // the last pass lands in buffer 0 (the caller's list)
-    k_expand<<<unsigned(ceil_div(plan.capacity, kExpTile)), kExpThreads, 0, s>>>(
-        cam, plan.n, ce, offsets, perm, p.d_means2d, p.d_radius, TK[cur], TV[cur]);
-    const int digit = (plan.tile_bits + plan.tile_passes - 1) / plan.tile_passes;  // <= 8
+    const SliceOut sl{reinterpret_cast<uint64_t*>(ws + plan.off_start), reinterpret_cast<uint2*>(ws + plan.off_rect),
+                      reinterpret_cast<uint32_t*>(ws + plan.off_owner), uint32_t(plan.chunks)};
+    k_slices<<<unsigned(plan.slice_blocks), kSlThreads, 0, s>>>(
+        cam, n, perm, tiles_sorted, p.d_means2d, p.d_radius, counters + 7,
+        reinterpret_cast<unsigned long long*>(ws + plan.off_status_slices), error, result, sl);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || plan.capacity == 0) return e;
+    const Count ce{0u, result, uint32_t(plan.capacity)};
+    uint32_t* ghist_tile = reinterpret_cast<uint32_t*>(ws + plan.off_ghist_tile);
+    switch (rbits) {
+        case 4: expand_launch<4>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
+        case 6: expand_launch<6>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
+        case 7: expand_launch<7>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
+        default: expand_launch<8>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // 3. stable sort of the entries by tile id, then the ranges
     const SortCtl tctl{counters + 4, reinterpret_cast<uint32_t*>(ws + plan.off_ghist_tile),
                        reinterpret_cast<uint32_t*>(ws + plan.off_status_tile), error,
                        uint32_t(plan.tile_tiles)};
     const unsigned tblocks = unsigned(plan.tile_tiles);
-    const int rbits = digit <= 4 ? 4 : digit <= 6 ? 6 : digit == 7 ? 7 : 8;
-    switch (rbits) {
-        case 4: tile_hist_launch<4>(TK[cur], ce, digit, plan.tile_passes, tblocks, tctl.ghist, s); break;
-        case 6: tile_hist_launch<6>(TK[cur], ce, digit, plan.tile_passes, tblocks, tctl.ghist, s); break;
-        case 7: tile_hist_launch<7>(TK[cur], ce, digit, plan.tile_passes, tblocks, tctl.ghist, s); break;
-        default: tile_hist_launch<8>(TK[cur], ce, digit, plan.tile_passes, tblocks, tctl.ghist, s); break;
-    }
     for (int pass = 0; pass < plan.tile_passes; ++pass) {
         switch (rbits) {
             case 4: tile_sort_launch<4>(TK[cur], TV[cur], ce, digit, pass, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
@@ -591,8 +643,10 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
         }
         cur ^= 1;
     }
-    k_ranges<<<unsigned(ceil_div(plan.capacity, 256)), 256, 0, s>>>(TK[0], TV[0], p.d_depth, ce,
-                                                                   uint32_t(plan.n_tiles), tile_ranges, keys_out);
+    {
+        const unsigned rb = unsigned(std::min<size_t>(ceil_div(plan.capacity, 256), 152 * 16));
+        k_ranges<<<rb, 256, 0, s>>>(TK[0], TV[0], p.d_depth, ce, uint32_t(plan.n_tiles), tile_ranges, keys_out);
+    }
     return cudaGetLastError();
 }
 

@@ -110,11 +110,12 @@ struct BinPlan {
     int tile_passes;       // ceil(tile_bits / 8)
     size_t capacity;
     size_t depth_tiles, tile_tiles;  // sort tiles of the depth sort and of the tile sort
+    size_t slice_blocks;             // blocks of the slice scan (1024 Gaussians each)
+    size_t chunks;                   // 1024-entry chunks of the capacity (expansion blocks)
     // workspace layout (byte offsets)
-    size_t off_dkeys, off_dvals, off_tiles_sorted, off_offsets, off_scan_tmp, off_tkeys, off_tvals;
-    size_t off_ctl, off_result, off_counters, off_ghist_depth, off_ghist_tile, off_status_depth,
-        off_status_tile, ctl_bytes, total_bytes;
-    size_t scan_tmp_elems;
+    size_t off_dkeys, off_dvals, off_tiles_sorted, off_start, off_rect, off_owner, off_tkeys, off_tvals;
+    size_t off_ctl, off_result, off_counters, off_ghist_depth, off_ghist_tile, off_status_slices,
+        off_status_depth, off_status_tile, ctl_bytes, total_bytes;
 };
 BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity);
 // Enqueues the whole binning: depth sort of the Gaussians, scan of their tile counts, expansion
