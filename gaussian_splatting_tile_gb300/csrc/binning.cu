@@ -33,6 +33,7 @@ constexpr int kRsThreads = 256;
 constexpr int kRsWarps = kRsThreads / 32;
 constexpr int kDepthItems = 8;                          // depth sort: 2048 keys per block
 constexpr int kTileItems = 16;                          // tile sort: 4096 keys per block
+constexpr int kDepthHistItems = 2;                      // depth digit counts: 512 keys per block
 constexpr unsigned kFull = 0xffffffffu;
 
 size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
@@ -44,7 +45,7 @@ constexpr uint32_t kFlagIncl = 2u << 30;   // status word: count of this and eve
 constexpr uint32_t kFlagMask = 3u << 30;
 constexpr uint32_t kCountMask = (1u << 30) - 1u;
 constexpr int kMaxSpins = 1 << 20;         // bound on one look-back wait (then give up, flag it)
-constexpr int kWindow = 8;                 // predecessors whose status words are read together
+constexpr int kWindow = 32;                // predecessors whose status words are read together
 
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
     uint32_t v;
@@ -126,51 +127,42 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_hist(const uint32_t* __res
     }
 }
 
-// Exclusive scans of two values per thread over the block's 256 threads: returns that of a,
-// stores that of b in eb.
-__device__ __forceinline__ uint32_t block_exclusive_scan2_256(uint32_t a, uint32_t b, uint32_t (*s_w)[kRsWarps],
-                                                              uint32_t& eb) {
+// Exclusive scan of one value per thread over the block's 256 threads.
+__device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t a, uint32_t* s_w) {
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t x = a, y = b;
+    uint32_t x = a;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t xa = __shfl_up_sync(kFull, x, o), yb = __shfl_up_sync(kFull, y, o);
-        if (lane >= uint32_t(o)) {
-            x += xa;
-            y += yb;
-        }
+        const uint32_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= uint32_t(o)) x += y;
     }
-    if (lane == 31) {
-        s_w[0][warp] = x;
-        s_w[1][warp] = y;
-    }
+    if (lane == 31) s_w[warp] = x;
     __syncthreads();
-    uint32_t ba = 0u, bb = 0u;
-    for (uint32_t w = 0; w < warp; ++w) {
-        ba += s_w[0][w];
-        bb += s_w[1][w];
-    }
-    eb = bb + y - b;
-    return ba + x - a;
+    uint32_t before = 0u;
+    for (uint32_t w = 0; w < warp; ++w) before += s_w[w];
+    return before + x - a;
 }
 
 // One stable pass over the digit at `shift`.  A block owns ITEMS x 256 consecutive keys of its
 // tile; warp w owns the w-th contiguous 32 x ITEMS of them and walks them 32 at a time in index
 // order, ranking equal digits with match masks and per-warp running counts.  A key goes to
 // (keys of smaller digits) + (same digit in earlier tiles, from the look-back)
-// + (same digit in earlier warps of the tile) + (its rank in its warp).
-template <int RBITS, int ITEMS, bool FROM_DEPTH, bool GATHER_TILES>
+// + (same digit in earlier warps of the tile) + (its rank in its warp).  The tile's keys are
+// first put in that order in shared memory, so the global writes of one digit are consecutive.
+// With KEYS64 (last pass of the tile sort) the 64-bit keys (tile << 32) | float_bits(depth) are
+// written as well when `keys64` is given.
+template <int RBITS, int ITEMS, bool FROM_DEPTH, bool GATHER_TILES, bool KEYS64 = false>
 __global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
     const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, DepthKeySource src,
     Count count, int shift, int pass, SortCtl ctl, uint32_t* __restrict__ keys_out,
     uint32_t* __restrict__ vals_out, const uint32_t* __restrict__ tiles_in,
-    uint32_t* __restrict__ tiles_out) {
+    uint32_t* __restrict__ tiles_out, uint64_t* __restrict__ keys64) {
     constexpr int R = 1 << RBITS;
     constexpr uint32_t TILE = kRsThreads * ITEMS;
     __shared__ uint32_t s_cnt[kRsWarps][R];
     __shared__ uint32_t s_lstart[R];  // first slot of each digit in the tile's reordered keys
     __shared__ uint32_t s_delta[R];   // global position - slot, per digit
-    __shared__ uint32_t s_w[2][kRsWarps];
+    __shared__ uint32_t s_w[kRsWarps];
     __shared__ uint32_t s_k[TILE], s_v[TILE];
     __shared__ uint32_t s_tile;
     if (threadIdx.x == 0) s_tile = atomicAdd(ctl.counter + pass, 1u);
@@ -181,44 +173,58 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
     if (tile >= (n + TILE - 1) / TILE) return;  // uniform: nothing to do (and nobody waits on it)
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt = (1u << lane) - 1u;
-    const uint32_t base = tile * TILE + warp * (32 * ITEMS);
-    uint32_t key[ITEMS], val[ITEMS], d[ITEMS], rank[ITEMS];
-#pragma unroll
-    for (int k = 0; k < ITEMS; ++k) {
-        const uint32_t i = base + k * 32 + lane;
-        key[k] = 0u;
-        val[k] = 0u;
-        if (i < n) rs_load<FROM_DEPTH>(keys_in, vals_in, src, i, key[k], val[k]);
-        d[k] = i < n ? (key[k] >> shift) & uint32_t(R - 1) : uint32_t(R);
-    }
-#pragma unroll
-    for (int k = 0; k < ITEMS; ++k) {
-        const uint32_t peers = __match_any_sync(kFull, d[k]);
-        const uint32_t leader = uint32_t(__ffs(peers) - 1);
-        const bool lead = lane == leader && d[k] < uint32_t(R);
-        uint32_t before = lead ? s_cnt[warp][d[k]] : 0u;
-        before = __shfl_sync(kFull, before, leader);
-        rank[k] = before + uint32_t(__popc(peers & lt));
-        if (lead) s_cnt[warp][d[k]] = before + uint32_t(__popc(peers));
-        __syncwarp();
-    }
-    __syncthreads();
-    uint32_t* status = ctl.status + size_t(pass) * ctl.max_tiles * 256;
     const uint32_t t = threadIdx.x;
-    uint32_t excl = 0u, gtotal = 0u, run_out = 0u;
-    if (t < uint32_t(R)) {
-        uint32_t run = 0u;  // per-warp offsets inside the tile; run ends as the tile's count
+    uint32_t* status = ctl.status + size_t(pass) * ctl.max_tiles * 256;
+    uint32_t run = 0u, lstart;
+    {
+        const uint32_t base = tile * TILE + warp * (32 * ITEMS);
+        uint32_t key[ITEMS], val[ITEMS], d[ITEMS], rank[ITEMS];
 #pragma unroll
-        for (int w = 0; w < kRsWarps; ++w) {
-            const uint32_t c = s_cnt[w][t];
-            s_cnt[w][t] = run;
-            run += c;
+        for (int k = 0; k < ITEMS; ++k) {
+            const uint32_t i = base + k * 32 + lane;
+            key[k] = 0u;
+            val[k] = 0u;
+            if (i < n) rs_load<FROM_DEPTH>(keys_in, vals_in, src, i, key[k], val[k]);
+            d[k] = i < n ? (key[k] >> shift) & uint32_t(R - 1) : uint32_t(R);
         }
-        uint32_t* mine = status + size_t(tile) * 256 + t;
-        if (tile == 0) {
-            st_relaxed(mine, kFlagIncl | run);
-        } else {
-            st_relaxed(mine, kFlagAgg | run);
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            const uint32_t peers = __match_any_sync(kFull, d[k]);
+            const uint32_t leader = uint32_t(__ffs(peers) - 1);
+            const bool lead = lane == leader && d[k] < uint32_t(R);
+            uint32_t before = lead ? s_cnt[warp][d[k]] : 0u;
+            before = __shfl_sync(kFull, before, leader);
+            rank[k] = before + uint32_t(__popc(peers & lt));
+            if (lead) s_cnt[warp][d[k]] = before + uint32_t(__popc(peers));
+            __syncwarp();
+        }
+        __syncthreads();
+        if (t < uint32_t(R)) {
+            // per-warp offsets inside the tile; run ends as the tile's count of digit t, which is
+            // published at once so that later tiles can go on looking back
+#pragma unroll
+            for (int w = 0; w < kRsWarps; ++w) {
+                const uint32_t c = s_cnt[w][t];
+                s_cnt[w][t] = run;
+                run += c;
+            }
+            st_relaxed(status + size_t(tile) * 256 + t, (tile == 0 ? kFlagIncl : kFlagAgg) | run);
+        }
+        lstart = block_exclusive_scan_256(t < uint32_t(R) ? run : 0u, s_w);
+        if (t < uint32_t(R)) s_lstart[t] = lstart;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < ITEMS; ++k) {
+            if (d[k] < uint32_t(R)) {
+                const uint32_t slot = s_lstart[d[k]] + s_cnt[warp][d[k]] + rank[k];
+                s_k[slot] = key[k];
+                s_v[slot] = val[k];
+            }
+        }
+    }
+    uint32_t excl = 0u, gtotal = 0u;
+    if (t < uint32_t(R)) {
+        if (tile != 0) {
             // look back over up to kWindow predecessors at a time: the window's status words are
             // loaded together, then consumed nearest first; only a word not yet published is
             // re-read (bounded)
@@ -250,30 +256,12 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
                 }
                 pt -= nwin;
             }
-            st_relaxed(mine, kFlagIncl | (excl + run));
+            st_relaxed(status + size_t(tile) * 256 + t, kFlagIncl | (excl + run));
         }
         gtotal = ctl.ghist[pass * 256 + t];
-        run_out = run;
     }
-    // digit d of this tile goes to [dbase(d) + excl(d), ...) globally and to [lstart(d), ...) in
-    // shared memory; keys are first reordered by digit in shared memory so that the global
-    // writes of one digit are consecutive
-    uint32_t lstart;
-    const uint32_t dbase = block_exclusive_scan2_256(t < uint32_t(R) ? gtotal : 0u, t < uint32_t(R) ? run_out : 0u,
-                                                     s_w, lstart);
-    if (t < uint32_t(R)) {
-        s_lstart[t] = lstart;
-        s_delta[t] = dbase + excl - lstart;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < ITEMS; ++k) {
-        if (d[k] < uint32_t(R)) {
-            const uint32_t slot = s_lstart[d[k]] + s_cnt[warp][d[k]] + rank[k];
-            s_k[slot] = key[k];
-            s_v[slot] = val[k];
-        }
-    }
+    const uint32_t dbase = block_exclusive_scan_256(t < uint32_t(R) ? gtotal : 0u, s_w);
+    if (t < uint32_t(R)) s_delta[t] = dbase + excl - lstart;
     __syncthreads();
     const uint32_t in_tile = min(TILE, n - tile * TILE);
 #pragma unroll
@@ -285,6 +273,7 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
             keys_out[pos] = kk;
             vals_out[pos] = vv;
             if (GATHER_TILES) tiles_out[pos] = tiles_in[vv];
+            if (KEYS64 && keys64) keys64[pos] = (uint64_t(kk) << 32) | uint64_t(__float_as_uint(src.depth[vv]));
         }
     }
 }
@@ -299,15 +288,13 @@ __global__ void k_clear(uint32_t* __restrict__ ranges, uint32_t range_words, uin
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < ctl_words; i += stride) ctl[i] = 0u;
 }
 
-// Ranges from the sorted tile ids; also writes the 64-bit keys when asked.
-__global__ void k_ranges(const uint32_t* __restrict__ tiles, const uint32_t* __restrict__ vals,
-                         const float* __restrict__ depth, Count count, uint32_t n_tiles,
-                         uint32_t* __restrict__ ranges, uint64_t* __restrict__ keys_out) {
+// Ranges from the sorted tile ids.
+__global__ void k_ranges(const uint32_t* __restrict__ tiles, Count count, uint32_t n_tiles,
+                         uint32_t* __restrict__ ranges) {
     const uint32_t E = count.get();
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride) {
         const uint32_t tile = tiles[e];
-        if (keys_out) keys_out[e] = (uint64_t(tile) << 32) | uint64_t(__float_as_uint(depth[vals[e]]));
         if (tile >= n_tiles) continue;  // unreachable for ids made by the expansion; keeps writes in bounds
         if (e == 0 || tiles[e - 1] != tile) ranges[2 * size_t(tile)] = e;
         if (e == E - 1 || tiles[e + 1] != tile) ranges[2 * size_t(tile) + 1] = e + 1;
@@ -461,58 +448,71 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
     __shared__ uint32_t s_g[kExpChunk];
     __shared__ uint32_t s_h[3][R];
     const uint32_t E = count.get();
-    const uint32_t e0 = blockIdx.x * kExpChunk;
-    if (e0 >= E) return;
+    const uint32_t chunks = (E + kExpChunk - 1) / kExpChunk;
+    if (blockIdx.x >= chunks) return;
     for (int i = threadIdx.x; i < 3 * R; i += kExpThreads) (&s_h[0][0])[i] = 0u;
-    // every Gaussian before the culled tail of the depth order has at least one entry, so the
-    // owners of 1024 consecutive entries are at most 1024 consecutive depth positions
-    const uint32_t i0 = sl.owner[blockIdx.x];
-    for (int j = threadIdx.x; j <= kExpChunk; j += kExpThreads) {
-        const uint32_t i = i0 + uint32_t(j);
-        s_start[j] = i < n ? sl.start[i] : uint64_t(0xffffffffffffffffull);
-        if (j < kExpChunk && i < n) {
-            s_rect[j] = sl.rect[i];
-            s_g[j] = perm[i];
-        }
-    }
-    __syncthreads();
     const uint32_t lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 0; k < kExpChunk / kExpThreads; ++k) {
-        const uint32_t e = e0 + k * kExpThreads + threadIdx.x;
-        const bool valid = e < E;
-        uint32_t tile = 0u;
-        if (valid) {
-            int lo = 0, hi = kExpChunk;  // s_start[lo] <= e < s_start[hi]
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (s_start[mid] <= e) lo = mid; else hi = mid;
+    for (uint32_t c = blockIdx.x; c < chunks; c += gridDim.x) {
+        const uint32_t e0 = c * kExpChunk;
+        // owners of the chunk's entries: depth positions i0 ..= i1.  Every Gaussian before the
+        // culled tail of the depth order has at least one entry, so there are at most 1024 of
+        // them; the slice after i1 starts past the chunk.
+        const uint32_t i0 = sl.owner[c];
+        const uint32_t i1 = c + 1 < chunks ? sl.owner[c + 1] : min(i0 + uint32_t(kExpChunk) - 1u, n - 1u);
+        const int w = int(min(i1 - i0 + 1u, uint32_t(kExpChunk)));
+        __syncthreads();  // the previous chunk is done with the window
+        for (int j = threadIdx.x; j <= w; j += kExpThreads) {
+            const uint32_t i = i0 + uint32_t(j);
+            s_start[j] = i < n ? sl.start[i] : uint64_t(0xffffffffffffffffull);
+            if (j < w) {
+                s_rect[j] = sl.rect[i];
+                s_g[j] = perm[i];
             }
-            const uint2 r = s_rect[lo];
-            const uint32_t kk = uint32_t(uint64_t(e) - s_start[lo]);
-            const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
-            tile = ty * uint32_t(cam.TX) + tx;
-            tile_keys[e] = tile;
-            vals[e] = s_g[lo];
         }
-        for (int p = 0; p < passes; ++p) {
-            const uint32_t d = valid ? (tile >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
-            const uint32_t peers = __match_any_sync(kFull, d);
-            if (d < uint32_t(R) && lane == uint32_t(__ffs(peers) - 1)) atomicAdd(&s_h[p][d], uint32_t(__popc(peers)));
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kExpChunk / kExpThreads; ++k) {
+            const uint32_t e = e0 + k * kExpThreads + threadIdx.x;
+            const bool valid = e < E;
+            uint32_t tile = 0u;
+            if (valid) {
+                int lo = 0, hi = w;  // s_start[lo] <= e < s_start[hi]
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_start[mid] <= e) lo = mid; else hi = mid;
+                }
+                const uint2 r = s_rect[lo];
+                const uint32_t kk = uint32_t(uint64_t(e) - s_start[lo]);
+                const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
+                tile = ty * uint32_t(cam.TX) + tx;
+                tile_keys[e] = tile;
+                vals[e] = s_g[lo];
+            }
+            for (int p = 0; p < passes; ++p) {
+                const uint32_t d = valid ? (tile >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
+                const uint32_t peers = __match_any_sync(kFull, d);
+                if (d < uint32_t(R) && lane == uint32_t(__ffs(peers) - 1)) atomicAdd(&s_h[p][d], uint32_t(__popc(peers)));
+            }
         }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < passes * R; i += kExpThreads) {
-        const uint32_t c = (&s_h[0][0])[i];
-        if (c) atomicAdd(ghist + (i / R) * 256 + (i % R), c);
+        const uint32_t cnt = (&s_h[0][0])[i];
+        if (cnt) atomicAdd(ghist + (i / R) * 256 + (i % R), cnt);
     }
 }
 
 template <int RBITS>
-void tile_sort_launch(const uint32_t* kin, const uint32_t* vin, Count count, int digit, int pass,
-                      const SortCtl& ctl, unsigned blocks, uint32_t* kout, uint32_t* vout, cudaStream_t s) {
-    k_sweep_pass<RBITS, kTileItems, false, false><<<blocks, kRsThreads, 0, s>>>(
-        kin, vin, DepthKeySource{}, count, pass * digit, pass, ctl, kout, vout, nullptr, nullptr);
+void tile_sort_launch(const uint32_t* kin, const uint32_t* vin, Count count, int digit, int pass, bool last,
+                      const float* depth, uint64_t* keys64, const SortCtl& ctl, unsigned blocks, uint32_t* kout,
+                      uint32_t* vout, cudaStream_t s) {
+    if (last && keys64)
+        k_sweep_pass<RBITS, kTileItems, false, false, true><<<blocks, kRsThreads, 0, s>>>(
+            kin, vin, DepthKeySource{depth, nullptr}, count, pass * digit, pass, ctl, kout, vout, nullptr,
+            nullptr, keys64);
+    else
+        k_sweep_pass<RBITS, kTileItems, false, false><<<blocks, kRsThreads, 0, s>>>(
+            kin, vin, DepthKeySource{}, count, pass * digit, pass, ctl, kout, vout, nullptr, nullptr, nullptr);
 }
 
 }  // namespace
@@ -559,7 +559,7 @@ BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity) {
 template <int RBITS>
 void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* perm, const SliceOut& sl, int digit,
                    int passes, uint32_t* ghist, uint32_t* tk, uint32_t* tv, cudaStream_t s) {
-    const unsigned blocks = sl.chunks;
+    const unsigned blocks = unsigned(std::min<size_t>(sl.chunks, 152 * 8));
     k_expand<RBITS><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
 }
 
@@ -590,15 +590,16 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
                        reinterpret_cast<uint32_t*>(ws + plan.off_status_depth), error,
                        uint32_t(plan.depth_tiles)};
     const unsigned dblocks = unsigned(plan.depth_tiles);
-    k_sweep_hist<8, kDepthItems, 4, true><<<dblocks, kRsThreads, 0, s>>>(nullptr, src, cn, 8, dctl.ghist);
+    k_sweep_hist<8, kDepthHistItems, 4, true><<<unsigned(ceil_div(n, kRsThreads * kDepthHistItems)), kRsThreads, 0, s>>>(
+        nullptr, src, cn, 8, dctl.ghist);
     k_sweep_pass<8, kDepthItems, true, false><<<dblocks, kRsThreads, 0, s>>>(
-        nullptr, nullptr, src, cn, 0, 0, dctl, DK[0], DV[0], nullptr, nullptr);
+        nullptr, nullptr, src, cn, 0, 0, dctl, DK[0], DV[0], nullptr, nullptr, nullptr);
     k_sweep_pass<8, kDepthItems, false, false><<<dblocks, kRsThreads, 0, s>>>(
-        DK[0], DV[0], src, cn, 8, 1, dctl, DK[1], DV[1], nullptr, nullptr);
+        DK[0], DV[0], src, cn, 8, 1, dctl, DK[1], DV[1], nullptr, nullptr, nullptr);
     k_sweep_pass<8, kDepthItems, false, false><<<dblocks, kRsThreads, 0, s>>>(
-        DK[1], DV[1], src, cn, 16, 2, dctl, DK[0], DV[0], nullptr, nullptr);
+        DK[1], DV[1], src, cn, 16, 2, dctl, DK[0], DV[0], nullptr, nullptr, nullptr);
     k_sweep_pass<8, kDepthItems, false, true><<<dblocks, kRsThreads, 0, s>>>(
-        DK[0], DV[0], src, cn, 24, 3, dctl, DK[1], DV[1], p.d_tiles_touched, tiles_sorted);
+        DK[0], DV[0], src, cn, 24, 3, dctl, DK[1], DV[1], p.d_tiles_touched, tiles_sorted, nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const uint32_t* perm = DV[1];
@@ -636,16 +637,16 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
     const unsigned tblocks = unsigned(plan.tile_tiles);
     for (int pass = 0; pass < plan.tile_passes; ++pass) {
         switch (rbits) {
-            case 4: tile_sort_launch<4>(TK[cur], TV[cur], ce, digit, pass, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
-            case 6: tile_sort_launch<6>(TK[cur], TV[cur], ce, digit, pass, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
-            case 7: tile_sort_launch<7>(TK[cur], TV[cur], ce, digit, pass, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
-            default: tile_sort_launch<8>(TK[cur], TV[cur], ce, digit, pass, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
+            case 4: tile_sort_launch<4>(TK[cur], TV[cur], ce, digit, pass, pass == plan.tile_passes - 1, p.d_depth, keys_out, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
+            case 6: tile_sort_launch<6>(TK[cur], TV[cur], ce, digit, pass, pass == plan.tile_passes - 1, p.d_depth, keys_out, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
+            case 7: tile_sort_launch<7>(TK[cur], TV[cur], ce, digit, pass, pass == plan.tile_passes - 1, p.d_depth, keys_out, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
+            default: tile_sort_launch<8>(TK[cur], TV[cur], ce, digit, pass, pass == plan.tile_passes - 1, p.d_depth, keys_out, tctl, tblocks, TK[cur ^ 1], TV[cur ^ 1], s); break;
         }
         cur ^= 1;
     }
     {
         const unsigned rb = unsigned(std::min<size_t>(ceil_div(plan.capacity, 256), 152 * 16));
-        k_ranges<<<rb, 256, 0, s>>>(TK[0], TV[0], p.d_depth, ce, uint32_t(plan.n_tiles), tile_ranges, keys_out);
+        k_ranges<<<rb, 256, 0, s>>>(TK[0], ce, uint32_t(plan.n_tiles), tile_ranges);
     }
     return cudaGetLastError();
 }
