@@ -55,6 +55,16 @@ B_PROJECT_BWD_PER_G = 504
 B_FWD_PER_ENTRY, B_FWD_PER_PIXEL = 40, 20
 B_BWD_PER_ENTRY, B_BWD_PER_PIXEL, B_BWD_PER_G = 40 + 36, 20, 36
 OPS_PROJECT_PER_G, OPS_PROJECT_BWD_PER_G = 400, 1000
+# binning: per Gaussian, digit counts (8 B) + 4 depth passes (16 B each) + the tiles_touched gather
+# (8 B) + slices (24 B read, 16 B written); per entry, the expansion's writes (8 B) and the ranges'
+# read (4 B), plus 16 B (key and value read and written) per tile-id pass
+B_BIN_PER_G = 8 + 4 * 16 + 8 + 40
+B_BIN_PER_ENTRY_FIXED, B_BIN_PER_ENTRY_PASS = 12, 16
+# DRAM bytes (read + write) of one k_raster_bwd launch on orbit view 1, from an ncu --set full
+# capture of the current kernel; must be re-taken (or set to None) whenever the kernel changes
+TRAFFIC_RASTER_BWD_BYTES = 58.290944e6 + 0.580352e6
+TRAFFIC_RASTER_BWD_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of k_raster_bwd, "
+                             "160k scene, 1920x1080 orbit view 1")
 
 
 def measured_peaks():
@@ -299,14 +309,16 @@ def roofline(res, Q, E, n, cam, blend_ratio):
     t_bwd = res["stage_ms"]["rasterize_bwd"] * 1e-3
     dominant = dict(kernel="rasterize_bwd (k_zero4 + k_raster_bwd)", bound="alu",
                     achieved=ops_bwd / t_bwd / 1e12, peak=fp32 / 1e12, unit="Tops/s",
-                    frac=(ops_bwd / t_bwd) / fp32, traffic=None,
+                    frac=(ops_bwd / t_bwd) / fp32, traffic=TRAFFIC_RASTER_BWD_BYTES,
+                    traffic_source=TRAFFIC_RASTER_BWD_SOURCE,
                     peak_source=f"152 SMs x 128 FP32 lanes x {MAX_MHZ:.0f} MHz (max SM clock)",
                     ops_per_launch=ops_bwd, composited_fraction=r,
                     composited_fraction_source="oracle on the timed view" if blend_ratio is not None else "unknown: counted as 0")
     t = {}
     t["project"] = max(n * B_PROJECT_PER_G / bw, n * OPS_PROJECT_PER_G / fp32)
-    p = math.ceil((32 + math.ceil(math.log2(cam.n_tiles))) / 8)
-    t["bin"] = (n * 28 + E * (12 + 24 * p + 8) + cam.n_tiles * 8) / bw
+    tile_passes = math.ceil(max(1, math.ceil(math.log2(cam.n_tiles))) / 8)
+    t["bin"] = (n * B_BIN_PER_G + E * (B_BIN_PER_ENTRY_FIXED + B_BIN_PER_ENTRY_PASS * tile_passes)
+                + cam.n_tiles * 8) / bw
     t["rasterize_fwd"] = max((E * B_FWD_PER_ENTRY + HW * B_FWD_PER_PIXEL) / bw,
                              (Q * OPS_FWD_EXAMINED + Qb * OPS_FWD_BLEND) / fp32, Q / mufu)
     t["rasterize_bwd"] = max((E * B_BWD_PER_ENTRY + HW * B_BWD_PER_PIXEL + n * B_BWD_PER_G) / bw,
