@@ -1,0 +1,484 @@
+// Appearance MLP (rigel README "Appearance MLP") and the L1 loss gradient of the training step.
+//
+// Per Gaussian and view: x = [latent ; unit view direction], h = relu(W1 x + b1),
+// colour = sigmoid(W2 h + b2).  The page runs one thread per Gaussian with the weights in shared
+// memory.  Here a warp takes 16 Gaussians at a time and runs both layers as mma.sync m16n8k8
+// TF32 products on the tensor cores with split operands: a = a_hi + a_lo with both parts TF32,
+// and a.b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi, which keeps float32 accuracy.  The first layer's
+// accumulator fragment is the second layer's A operand without any data movement: in k-chunk kc
+// of the second product, fragment columns t and t + 4 stand for hidden units kc*8 + 2t and
+// kc*8 + 2t + 1, which are the two accumulator columns lane (g, t) already holds.
+//
+// The backward recomputes both layers, forms dL/dz2 and dL/dz1 in registers, gets dL/dx with a
+// third product (same renumbering), and accumulates the weight gradients from per-warp
+// shared-memory copies of dL/dz1, h and x, each lane owning whole hidden units; a block adds its
+// warps' sums in shared memory and flushes them with one global atomic per weight per block (the
+// reduction pattern the page describes for its MLP backward).  View directions are constants:
+// no gradient reaches the means.
+#include "rs_internal.cuh"
+
+namespace rs {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMlpWarps = 4;
+constexpr int kMlpThreads = kMlpWarps * 32;
+constexpr int kRows = 16;              // Gaussians per warp tile (the mma M dimension)
+constexpr int kInMax = 32;             // padded input width: latent_dim + 3 <= 32
+constexpr int kXStride = kInMax + 4;   // row stride of x and W1 copies: conflict-free fragments
+
+__device__ __forceinline__ uint32_t tf32_of(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// head and tail of x, both TF32 (the tail is the rounding error of the head, rounded again)
+__device__ __forceinline__ void split(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32_of(x);
+    lo = tf32_of(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d += a.b in split TF32 (three products)
+__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                     uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+    mma8(d, ah, bh0, bh1);
+    mma8(d, ah, bl0, bl1);
+    mma8(d, al, bh0, bh1);
+}
+
+struct MlpArgs {
+    CameraF cam;
+    int n, L, D;                       // Gaussians, latent width, input width L + 3
+    const float* means;
+    const float* latents;
+    const float* W1;
+    const float* b1;
+    const float* W2;
+    const float* b2;
+};
+
+// Weights in shared memory: W1 [HID][kXStride] (columns past D zero) and W2 [3][HID + 8] as TF32
+// heads and tails, W2 in float32 for the backward's dL/dh, and the biases.
+template <int HID>
+struct WeightSmem {
+    uint32_t w1h[HID * kXStride], w1l[HID * kXStride];
+    uint32_t w2h[3 * (HID + 8)], w2l[3 * (HID + 8)];
+    float w2f[3 * HID];
+    float b1[HID];
+    float b2[4];
+};
+
+template <int HID>
+__device__ void load_weights(const MlpArgs& a, WeightSmem<HID>& w) {
+    for (int i = threadIdx.x; i < HID * kInMax; i += blockDim.x) {
+        const int h = i / kInMax, k = i % kInMax;
+        const float v = k < a.D ? a.W1[h * a.D + k] : 0.f;
+        split(v, w.w1h[h * kXStride + k], w.w1l[h * kXStride + k]);
+    }
+    for (int i = threadIdx.x; i < 3 * HID; i += blockDim.x) {
+        const int c = i / HID, h = i % HID;
+        const float v = a.W2[i];
+        split(v, w.w2h[c * (HID + 8) + h], w.w2l[c * (HID + 8) + h]);
+        w.w2f[i] = v;
+    }
+    for (int i = threadIdx.x; i < HID; i += blockDim.x) w.b1[i] = a.b1[i];
+    if (threadIdx.x < 3) w.b2[threadIdx.x] = a.b2[threadIdx.x];
+}
+
+// x of Gaussians i0 .. i0 + 15 into s_x [16][kXStride]; rows past n and columns past D are zero.
+template <int KS>
+__device__ __forceinline__ void stage_x(const MlpArgs& a, int i0, float* s_x) {
+    const int lane = threadIdx.x & 31;
+    if (lane < kRows) {
+        const int i = i0 + lane;
+        float* row = s_x + lane * kXStride;
+        if (i < a.n) {
+            for (int k = 0; k < a.L; ++k) row[k] = a.latents[size_t(k) * a.n + i];
+            const CameraF& cam = a.cam;
+            // camera centre C = -R^T t
+            const float C0 = -(cam.R[0] * cam.t[0] + cam.R[3] * cam.t[1] + cam.R[6] * cam.t[2]);
+            const float C1 = -(cam.R[1] * cam.t[0] + cam.R[4] * cam.t[1] + cam.R[7] * cam.t[2]);
+            const float C2 = -(cam.R[2] * cam.t[0] + cam.R[5] * cam.t[1] + cam.R[8] * cam.t[2]);
+            const float d0 = a.means[i] - C0, d1 = a.means[size_t(a.n) + i] - C1,
+                        d2 = a.means[2 * size_t(a.n) + i] - C2;
+            const float len = sqrtf(d0 * d0 + d1 * d1 + d2 * d2);
+            const float il = len > 0.f ? 1.0f / len : 0.f;
+            row[a.L] = d0 * il;
+            row[a.L + 1] = d1 * il;
+            row[a.L + 2] = d2 * il;
+            for (int k = a.D; k < KS * 8; ++k) row[k] = 0.f;
+        } else {
+            for (int k = 0; k < KS * 8; ++k) row[k] = 0.f;
+        }
+    }
+    __syncwarp();
+}
+
+// First layer: acc[nt] = W1 x + b1 for hidden units nt*8 + (2t, 2t + 1) of rows g, g + 8,
+// then relu (h > 0 exactly where z > 0).
+template <int HID, int KS>
+__device__ __forceinline__ void layer1(const WeightSmem<HID>& w, const float* s_x, float (&acc)[HID / 8][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < HID / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        uint32_t ah[4], al[4];
+        split(s_x[g * kXStride + ks * 8 + t], ah[0], al[0]);
+        split(s_x[(g + 8) * kXStride + ks * 8 + t], ah[1], al[1]);
+        split(s_x[g * kXStride + ks * 8 + t + 4], ah[2], al[2]);
+        split(s_x[(g + 8) * kXStride + ks * 8 + t + 4], ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < HID / 8; ++nt) {
+            const int o = (nt * 8 + g) * kXStride + ks * 8 + t;
+            mma3(acc[nt], ah, al, w.w1h[o], w.w1h[o + 4], w.w1l[o], w.w1l[o + 4]);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < HID / 8; ++nt) {
+        const float c0 = w.b1[nt * 8 + 2 * t], c1 = w.b1[nt * 8 + 2 * t + 1];
+        acc[nt][0] = fmaxf(acc[nt][0] + c0, 0.f);
+        acc[nt][1] = fmaxf(acc[nt][1] + c1, 0.f);
+        acc[nt][2] = fmaxf(acc[nt][2] + c0, 0.f);
+        acc[nt][3] = fmaxf(acc[nt][3] + c1, 0.f);
+    }
+}
+
+// Second layer without bias: out = (rows g, g + 8) x (columns 2t, 2t + 1) of W2 h; columns 0..2
+// are the colour channels.
+template <int HID>
+__device__ __forceinline__ void layer2(const WeightSmem<HID>& w, const float (&h)[HID / 8][4], float (&out)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    out[0] = out[1] = out[2] = out[3] = 0.f;
+    const int gc = g < 3 ? g : 0;
+#pragma unroll
+    for (int kc = 0; kc < HID / 8; ++kc) {
+        uint32_t ah[4], al[4];
+        split(h[kc][0], ah[0], al[0]);
+        split(h[kc][2], ah[1], al[1]);
+        split(h[kc][1], ah[2], al[2]);
+        split(h[kc][3], ah[3], al[3]);
+        const int o = gc * (HID + 8) + kc * 8 + 2 * t;
+        const uint32_t bh0 = g < 3 ? w.w2h[o] : 0u, bh1 = g < 3 ? w.w2h[o + 1] : 0u;
+        const uint32_t bl0 = g < 3 ? w.w2l[o] : 0u, bl1 = g < 3 ? w.w2l[o + 1] : 0u;
+        mma3(out, ah, al, bh0, bh1, bl0, bl1);
+    }
+}
+
+__device__ __forceinline__ float sigmoidf(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+template <int HID, int KS>
+__global__ void __launch_bounds__(kMlpThreads) k_mlp_fwd(MlpArgs a, float* __restrict__ colors) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    WeightSmem<HID>& w = *reinterpret_cast<WeightSmem<HID>*>(smem);
+    float* s_x = reinterpret_cast<float*>(smem + sizeof(WeightSmem<HID>)) +
+                 (threadIdx.x >> 5) * (kRows * kXStride);
+    load_weights<HID>(a, w);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int tiles = (a.n + kRows - 1) / kRows;
+    for (int tile = blockIdx.x * kMlpWarps + (threadIdx.x >> 5); tile < tiles; tile += gridDim.x * kMlpWarps) {
+        const int i0 = tile * kRows;
+        stage_x<KS>(a, i0, s_x);
+        float h[HID / 8][4];
+        layer1<HID, KS>(w, s_x, h);
+        float z[4];
+        layer2<HID>(w, h, z);
+        // lane t = 0 holds channels 0, 1 and lane t = 1 channel 2, for rows g and g + 8
+        if (t < 2) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int i = i0 + g + 8 * half;
+                if (i < a.n) {
+                    const int c0 = 2 * t;
+                    colors[size_t(c0) * a.n + i] = sigmoidf(z[2 * half] + w.b2[c0]);
+                    if (t == 0) colors[size_t(1) * a.n + i] = sigmoidf(z[2 * half + 1] + w.b2[1]);
+                }
+            }
+        }
+        __syncwarp();  // s_x is rewritten by the next tile
+    }
+}
+
+// Per-warp staging of the backward and the block's gradient sums.
+template <int HID>
+struct BwdWarpSmem {
+    float x[kRows * kXStride];
+    float dz1[kRows * (HID + 8)];
+    float h[kRows * (HID + 8)];
+    float dz2[kRows * 4];
+};
+template <int HID>
+struct BwdSums {
+    float dW1[HID * kInMax];
+    float db1[HID];
+    float dW2[3 * HID];
+    float db2[4];
+};
+
+template <int HID, int KS>
+__global__ void __launch_bounds__(kMlpThreads) k_mlp_bwd(MlpArgs a, const float* __restrict__ dcolors,
+                                                        float* __restrict__ dlatents, float* __restrict__ dW1,
+                                                        float* __restrict__ db1, float* __restrict__ dW2,
+                                                        float* __restrict__ db2) {
+    constexpr int HS = HID + 8;   // row stride of dz1 and h copies
+    constexpr int Q = HID / 32;   // hidden units owned per lane: lane + 32 q
+    extern __shared__ __align__(16) unsigned char smem[];
+    WeightSmem<HID>& w = *reinterpret_cast<WeightSmem<HID>*>(smem);
+    BwdSums<HID>& sums = *reinterpret_cast<BwdSums<HID>*>(smem + sizeof(WeightSmem<HID>));
+    BwdWarpSmem<HID>& st = reinterpret_cast<BwdWarpSmem<HID>*>(
+        smem + sizeof(WeightSmem<HID>) + sizeof(BwdSums<HID>))[threadIdx.x >> 5];
+    load_weights<HID>(a, w);
+    for (int i = threadIdx.x; i < int(sizeof(BwdSums<HID>) / 4); i += blockDim.x)
+        reinterpret_cast<float*>(&sums)[i] = 0.f;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    float gw1[Q][KS * 8], gb1[Q], gw2[Q][3], gb2 = 0.f;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+#pragma unroll
+        for (int j = 0; j < KS * 8; ++j) gw1[q][j] = 0.f;
+        gb1[q] = 0.f;
+        gw2[q][0] = gw2[q][1] = gw2[q][2] = 0.f;
+    }
+    const int tiles = (a.n + kRows - 1) / kRows;
+    for (int tile = blockIdx.x * kMlpWarps + (threadIdx.x >> 5); tile < tiles; tile += gridDim.x * kMlpWarps) {
+        const int i0 = tile * kRows;
+        stage_x<KS>(a, i0, st.x);
+        float h[HID / 8][4];
+        layer1<HID, KS>(w, st.x, h);
+        float z[4];
+        layer2<HID>(w, h, z);
+        // dL/dz2 = dL/dcolour * s (1 - s), s = sigmoid(z2 + b2): lane t = 0 holds channels 0, 1
+        // and lane t = 1 channel 2 (slots 0, 2 for rows g, g + 8)
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < 2) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = 2 * t + (k & 1), i = i0 + g + 8 * (k >> 1);
+                if (c < 3 && i < a.n) {
+                    const float s = sigmoidf(z[k] + w.b2[c]);
+                    p[k] = dcolors[size_t(c) * a.n + i] * s * (1.f - s);
+                }
+            }
+        }
+        // every lane needs dL/dz2 of rows g and g + 8
+        const float d00 = __shfl_sync(kFull, p[0], 4 * g), d01 = __shfl_sync(kFull, p[1], 4 * g);
+        const float d10 = __shfl_sync(kFull, p[2], 4 * g), d11 = __shfl_sync(kFull, p[3], 4 * g);
+        const float d02 = __shfl_sync(kFull, p[0], 4 * g + 1), d12 = __shfl_sync(kFull, p[2], 4 * g + 1);
+        // dL/dz1 = (W2^T dL/dz2) where z1 > 0, in the accumulator layout of h
+        float dz[HID / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < HID / 8; ++nt) {
+            const int u0 = nt * 8 + 2 * t, u1 = u0 + 1;
+            const float w00 = w.w2f[u0], w10 = w.w2f[HID + u0], w20 = w.w2f[2 * HID + u0];
+            const float w01 = w.w2f[u1], w11 = w.w2f[HID + u1], w21 = w.w2f[2 * HID + u1];
+            dz[nt][0] = h[nt][0] > 0.f ? fmaf(d00, w00, fmaf(d01, w10, d02 * w20)) : 0.f;
+            dz[nt][1] = h[nt][1] > 0.f ? fmaf(d00, w01, fmaf(d01, w11, d02 * w21)) : 0.f;
+            dz[nt][2] = h[nt][2] > 0.f ? fmaf(d10, w00, fmaf(d11, w10, d12 * w20)) : 0.f;
+            dz[nt][3] = h[nt][3] > 0.f ? fmaf(d10, w01, fmaf(d11, w11, d12 * w21)) : 0.f;
+        }
+        // dL/dx = W1^T dL/dz1: A = dz1 (hidden units renumbered as in layer 2), B = W1
+        float dx[KS][4];
+#pragma unroll
+        for (int nt = 0; nt < KS; ++nt) dx[nt][0] = dx[nt][1] = dx[nt][2] = dx[nt][3] = 0.f;
+#pragma unroll
+        for (int kc = 0; kc < HID / 8; ++kc) {
+            uint32_t ah[4], al[4];
+            split(dz[kc][0], ah[0], al[0]);
+            split(dz[kc][2], ah[1], al[1]);
+            split(dz[kc][1], ah[2], al[2]);
+            split(dz[kc][3], ah[3], al[3]);
+#pragma unroll
+            for (int nt = 0; nt < KS; ++nt) {
+                const int o = (kc * 8 + 2 * t) * kXStride + nt * 8 + g;
+                mma3(dx[nt], ah, al, w.w1h[o], w.w1h[o + kXStride], w.w1l[o], w.w1l[o + kXStride]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < KS; ++nt) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int j = nt * 8 + 2 * t + (k & 1), i = i0 + g + 8 * (k >> 1);
+                if (j < a.L && i < a.n) dlatents[size_t(j) * a.n + i] = dx[nt][k];
+            }
+        }
+        // stage dz1, h, dz2 for the weight gradients
+#pragma unroll
+        for (int nt = 0; nt < HID / 8; ++nt) {
+            const int u0 = nt * 8 + 2 * t;
+            *reinterpret_cast<float2*>(&st.dz1[g * HS + u0]) = make_float2(dz[nt][0], dz[nt][1]);
+            *reinterpret_cast<float2*>(&st.dz1[(g + 8) * HS + u0]) = make_float2(dz[nt][2], dz[nt][3]);
+            *reinterpret_cast<float2*>(&st.h[g * HS + u0]) = make_float2(h[nt][0], h[nt][1]);
+            *reinterpret_cast<float2*>(&st.h[(g + 8) * HS + u0]) = make_float2(h[nt][2], h[nt][3]);
+        }
+        if (t == 0) {
+            st.dz2[g * 4] = d00;
+            st.dz2[g * 4 + 1] = d01;
+            st.dz2[g * 4 + 2] = d02;
+            st.dz2[(g + 8) * 4] = d10;
+            st.dz2[(g + 8) * 4 + 1] = d11;
+            st.dz2[(g + 8) * 4 + 2] = d12;
+        }
+        __syncwarp();
+        // lane owns hidden units lane + 32 q: dW1 rows, db1, dW2 columns; lanes 0..2 db2
+#pragma unroll 4
+        for (int r = 0; r < kRows; ++r) {
+            const float* xr = st.x + r * kXStride;
+            const float e0 = st.dz2[r * 4], e1 = st.dz2[r * 4 + 1], e2 = st.dz2[r * 4 + 2];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int u = lane + 32 * q;
+                const float dzv = st.dz1[r * HS + u], hv = st.h[r * HS + u];
+                gb1[q] += dzv;
+#pragma unroll
+                for (int j = 0; j < KS * 8; ++j) gw1[q][j] = fmaf(dzv, xr[j], gw1[q][j]);
+                gw2[q][0] = fmaf(e0, hv, gw2[q][0]);
+                gw2[q][1] = fmaf(e1, hv, gw2[q][1]);
+                gw2[q][2] = fmaf(e2, hv, gw2[q][2]);
+            }
+            gb2 += lane == 0 ? e0 : lane == 1 ? e1 : lane == 2 ? e2 : 0.f;
+        }
+        __syncwarp();  // the staging is rewritten by the next tile
+    }
+    // block sums, then one global atomic per weight per block
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        const int u = lane + 32 * q;
+#pragma unroll
+        for (int j = 0; j < KS * 8; ++j)
+            if (j < a.D) atomicAdd(&sums.dW1[u * kInMax + j], gw1[q][j]);
+        atomicAdd(&sums.db1[u], gb1[q]);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) atomicAdd(&sums.dW2[c * HID + u], gw2[q][c]);
+    }
+    if (lane < 3) atomicAdd(&sums.db2[lane], gb2);
+    __syncthreads();
+    for (int i = threadIdx.x; i < HID * a.D; i += blockDim.x) {
+        const int u = i / a.D, j = i % a.D;
+        const float v = sums.dW1[u * kInMax + j];
+        if (v != 0.f) atomicAdd(dW1 + i, v);
+    }
+    for (int i = threadIdx.x; i < HID; i += blockDim.x)
+        if (sums.db1[i] != 0.f) atomicAdd(db1 + i, sums.db1[i]);
+    for (int i = threadIdx.x; i < 3 * HID; i += blockDim.x)
+        if (sums.dW2[i] != 0.f) atomicAdd(dW2 + i, sums.dW2[i]);
+    if (threadIdx.x < 3 && sums.db2[threadIdx.x] != 0.f) atomicAdd(db2 + threadIdx.x, sums.db2[threadIdx.x]);
+}
+
+__global__ void k_zero_mlp_grads(float* dW1, int nW1, float* db1, int nb1, float* dW2, int nW2, float* db2) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nW1; i += gridDim.x * blockDim.x) dW1[i] = 0.f;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nb1; i += gridDim.x * blockDim.x) db1[i] = 0.f;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nW2; i += gridDim.x * blockDim.x) dW2[i] = 0.f;
+    if (blockIdx.x == 0 && threadIdx.x < 3) db2[threadIdx.x] = 0.f;
+}
+
+// L1 loss and its gradient; the block sums of |d| go to *loss with one atomic per block.
+__global__ void __launch_bounds__(256) k_l1(size_t count, const float* __restrict__ img,
+                                            const float* __restrict__ tgt, float scale,
+                                            float* __restrict__ dimg, float* __restrict__ loss) {
+    __shared__ float s_w[8];
+    float acc = 0.f;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += size_t(gridDim.x) * blockDim.x) {
+        const float d = img[i] - tgt[i];
+        dimg[i] = d > 0.f ? scale : (d < 0.f ? -scale : 0.f);
+        acc += fabsf(d);
+    }
+    if (!loss) return;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+    if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = 0.f;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) b += s_w[w];
+        atomicAdd(loss, b * scale);
+    }
+}
+
+template <int HID, int KS>
+cudaError_t launch_fwd_t(const MlpArgs& a, float* colors, cudaStream_t s) {
+    const size_t smem = sizeof(WeightSmem<HID>) + size_t(kMlpWarps) * kRows * kXStride * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_mlp_fwd<HID, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    const int tiles = (a.n + kRows - 1) / kRows;
+    const int blocks = std::min((tiles + kMlpWarps - 1) / kMlpWarps, 152 * 4);
+    k_mlp_fwd<HID, KS><<<blocks, kMlpThreads, smem, s>>>(a, colors);
+    return cudaGetLastError();
+}
+
+template <int HID, int KS>
+cudaError_t launch_bwd_t(const MlpArgs& a, const float* dcol, float* dlat, const rs_mlp_grads& gr, cudaStream_t s) {
+    const size_t smem = sizeof(WeightSmem<HID>) + sizeof(BwdSums<HID>) + size_t(kMlpWarps) * sizeof(BwdWarpSmem<HID>);
+    cudaError_t e = cudaFuncSetAttribute(k_mlp_bwd<HID, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    k_zero_mlp_grads<<<8, 256, 0, s>>>(gr.d_dW1, HID * a.D, gr.d_db1, HID, gr.d_dW2, 3 * HID, gr.d_db2);
+    if (a.n == 0) return cudaGetLastError();
+    const int tiles = (a.n + kRows - 1) / kRows;
+    const int blocks = std::min((tiles + kMlpWarps - 1) / kMlpWarps, 152 * 2);
+    k_mlp_bwd<HID, KS><<<blocks, kMlpThreads, smem, s>>>(a, dcol, dlat, gr.d_dW1, gr.d_db1, gr.d_dW2, gr.d_db2);
+    return cudaGetLastError();
+}
+
+MlpArgs make_args(const CameraF& cam, int n, const float* means, const float* latents, const rs_mlp& m) {
+    return MlpArgs{cam, n, m.latent_dim, m.latent_dim + 3, means, latents, m.d_W1, m.d_b1, m.d_W2, m.d_b2};
+}
+
+template <int HID>
+cudaError_t fwd_ks(const MlpArgs& a, float* colors, cudaStream_t s) {
+    switch ((a.D + 7) / 8) {
+        case 1: return launch_fwd_t<HID, 1>(a, colors, s);
+        case 2: return launch_fwd_t<HID, 2>(a, colors, s);
+        case 3: return launch_fwd_t<HID, 3>(a, colors, s);
+        default: return launch_fwd_t<HID, 4>(a, colors, s);
+    }
+}
+
+template <int HID>
+cudaError_t bwd_ks(const MlpArgs& a, const float* dcol, float* dlat, const rs_mlp_grads& gr, cudaStream_t s) {
+    switch ((a.D + 7) / 8) {
+        case 1: return launch_bwd_t<HID, 1>(a, dcol, dlat, gr, s);
+        case 2: return launch_bwd_t<HID, 2>(a, dcol, dlat, gr, s);
+        case 3: return launch_bwd_t<HID, 3>(a, dcol, dlat, gr, s);
+        default: return launch_bwd_t<HID, 4>(a, dcol, dlat, gr, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_appearance_fwd(const CameraF& cam, int n, const float* means, const float* latents,
+                                  const rs_mlp& m, float* colors, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const MlpArgs a = make_args(cam, n, means, latents, m);
+    return m.hidden == 32 ? fwd_ks<32>(a, colors, s) : fwd_ks<64>(a, colors, s);
+}
+
+cudaError_t launch_appearance_bwd(const CameraF& cam, int n, const float* means, const float* latents,
+                                  const rs_mlp& m, const float* dcolors, float* dlatents,
+                                  const rs_mlp_grads& gr, cudaStream_t s) {
+    const MlpArgs a = make_args(cam, n, means, latents, m);
+    return m.hidden == 32 ? bwd_ks<32>(a, dcolors, dlatents, gr, s) : bwd_ks<64>(a, dcolors, dlatents, gr, s);
+}
+
+cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float scale, float* dimg,
+                      float* loss, cudaStream_t s) {
+    if (loss) {
+        cudaError_t e = cudaMemsetAsync(loss, 0, sizeof(float), s);
+        if (e != cudaSuccess) return e;
+    }
+    if (count == 0) return cudaSuccess;
+    const unsigned blocks = unsigned(std::min<size_t>((count + 255) / 256, 152 * 8));
+    k_l1<<<blocks, 256, 0, s>>>(count, img, tgt, scale, dimg, loss);
+    return cudaGetLastError();
+}
+
+}  // namespace rs

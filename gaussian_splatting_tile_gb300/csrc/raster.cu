@@ -23,6 +23,15 @@ constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per th
 constexpr int kWarps = kTilePixels / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
+// Resident blocks per SM the compositing kernels are compiled for (register budget per thread =
+// 65536 / (256 x blocks)).
+#ifndef RS_FWD_MIN_BLOCKS
+#define RS_FWD_MIN_BLOCKS 6
+#endif
+#ifndef RS_BWD_MIN_BLOCKS
+#define RS_BWD_MIN_BLOCKS 6
+#endif
+
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
 // (w >> 1) * 4 of the tile; lane l is pixel (l & 7, l >> 3) inside it.
 __device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int& tx0, int& ty0, int& px,
@@ -72,7 +81,7 @@ __device__ __forceinline__ int compact_warp(uint8_t* list, Hit hit) {
     return n;
 }
 
-__global__ void __launch_bounds__(kTilePixels) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
+__global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
                                                            const uint2* __restrict__ ranges,
                                                            const uint32_t* __restrict__ list,
                                                            float3 bg, float* __restrict__ image,
@@ -177,7 +186,7 @@ __device__ __forceinline__ int sum_slot(unsigned lane) {
 constexpr int kSums = 9;          // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2, gp, w G_rgb
 constexpr int kAccStride = kBatch + 1;  // padding keeps the nine slots of one entry in nine banks
 
-__global__ void __launch_bounds__(kTilePixels) k_raster_bwd(
+__global__ void __launch_bounds__(kTilePixels, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     CameraF cam, int n, const Record* __restrict__ rec, const uint2* __restrict__ ranges,
     const uint32_t* __restrict__ list, float3 bg, const float* __restrict__ final_T,
     const uint32_t* __restrict__ n_contrib, const float* __restrict__ dL_dimage,

@@ -49,6 +49,13 @@ bool projected_ok(const rs_projected* p, bool need_records) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RS_OK : RS_ERR_CUDA; }
 
+bool mlp_ok(const rs_mlp* m) {
+    if (!m) return false;
+    if (m->hidden != 32 && m->hidden != 64) return false;
+    if (m->latent_dim < 1 || m->latent_dim > 29) return false;
+    return dev_f(m->d_W1) && dev_f(m->d_b1) && dev_f(m->d_W2) && dev_f(m->d_b2);
+}
+
 }  // namespace
 
 extern "C" {
@@ -169,6 +176,38 @@ int rs_project_bwd(const rs_camera* camera, const rs_gaussians* gaussians,
     return cuda_rc(rs::launch_project_bwd(cam, *gaussians, *proj, d_dL_dmeans2d, d_dL_dconic,
                                           d_dL_dcolor, d_dL_dmeans, d_dL_dscales, d_dL_dquats,
                                           d_dL_dsh, static_cast<cudaStream_t>(stream)));
+}
+
+int rs_appearance_fwd(const rs_camera* camera, int32_t n, const float* d_means,
+                      const float* d_latents, const rs_mlp* mlp, float* d_colors, void* stream) {
+    if (!camera_ok(camera) || !n_ok(n) || !mlp_ok(mlp)) return RS_ERR_INVALID_ARG;
+    if (n == 0) return RS_OK;
+    if (!dev_f(d_means) || !dev_f(d_latents) || !dev_f(d_colors)) return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    return cuda_rc(rs::launch_appearance_fwd(cam, n, d_means, d_latents, *mlp, d_colors,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int rs_appearance_bwd(const rs_camera* camera, int32_t n, const float* d_means,
+                      const float* d_latents, const rs_mlp* mlp, const float* d_dL_dcolors,
+                      float* d_dL_dlatents, const rs_mlp_grads* grads, void* stream) {
+    if (!camera_ok(camera) || !n_ok(n) || !mlp_ok(mlp) || !grads) return RS_ERR_INVALID_ARG;
+    if (!dev_f(grads->d_dW1) || !dev_f(grads->d_db1) || !dev_f(grads->d_dW2) || !dev_f(grads->d_db2))
+        return RS_ERR_INVALID_ARG;
+    if (n > 0 && (!dev_f(d_means) || !dev_f(d_latents) || !dev_f(d_dL_dcolors) || !dev_f(d_dL_dlatents)))
+        return RS_ERR_INVALID_ARG;
+    const CameraF cam = rs::make_camera(*camera);
+    return cuda_rc(rs::launch_appearance_bwd(cam, n, d_means, d_latents, *mlp, d_dL_dcolors,
+                                             d_dL_dlatents, *grads, static_cast<cudaStream_t>(stream)));
+}
+
+int rs_l1_loss_grad(size_t count, const float* d_image, const float* d_target, float scale,
+                    float* d_dL_dimage, float* d_loss, void* stream) {
+    if (!isfinite(scale)) return RS_ERR_INVALID_ARG;
+    if (d_loss && !aligned(d_loss, 4)) return RS_ERR_INVALID_ARG;
+    if (count > 0 && (!dev_f(d_image) || !dev_f(d_target) || !dev_f(d_dL_dimage))) return RS_ERR_INVALID_ARG;
+    return cuda_rc(rs::launch_l1(count, d_image, d_target, scale, d_dL_dimage, d_loss,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

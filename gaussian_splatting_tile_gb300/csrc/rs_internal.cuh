@@ -139,4 +139,13 @@ cudaError_t launch_fill_background(const CameraF& cam, float3 bg, float* image, 
 cudaError_t launch_zero_grads(float* dm2, float* dcon, float* dop, float* dcol, size_t n,
                               cudaStream_t s);
 
+// Appearance MLP (hidden 32 or 64, latent_dim + 3 <= 32) and the L1 loss gradient.
+cudaError_t launch_appearance_fwd(const CameraF& cam, int n, const float* means, const float* latents,
+                                  const rs_mlp& m, float* colors, cudaStream_t s);
+cudaError_t launch_appearance_bwd(const CameraF& cam, int n, const float* means, const float* latents,
+                                  const rs_mlp& m, const float* dcolors, float* dlatents,
+                                  const rs_mlp_grads& gr, cudaStream_t s);
+cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float scale, float* dimg,
+                      float* loss, cudaStream_t s);
+
 }  // namespace rs

@@ -165,3 +165,51 @@ class Renderer:
         self._grads(gs.sh_degree)
         self.rasterize_backward(dL_dimage, stream)
         return self.project_backward(gs, stream)
+
+
+class AppearanceStep:
+    """The training-shaped step of rigel's appearance-MLP model ("Appearance MLP" and its training
+    loop): per view, the MLP gives every Gaussian its colour, the rasteriser renders it, the L1
+    loss against the view's target gives dL/dimage, and the backward runs through compositing,
+    projection and the MLP.  Every stage is a call of the C ABI; this class only owns buffers.
+
+    `forward` and `backward` are separate so that a caller can inspect or change dL/dimage in
+    between; `view` runs both."""
+
+    def __init__(self, camera, g: rs.DeviceGaussians, mlp: rs.DeviceMLP, latents: torch.Tensor,
+                 device="cuda", capacity: int | None = None):
+        self.device = torch.device(device)
+        self.g, self.mlp, self.latents = g, mlp, latents
+        n = g.n
+        self.R = Renderer(camera, n, self.device, capacity)
+        self.colors = torch.empty(3, n, dtype=torch.float32, device=self.device)
+        # geometry of g with the MLP's colours as the colour source
+        self.gc = rs.DeviceGaussians(g.means, g.scales, g.quats, g.opacity, None, -1, self.colors)
+        H, W = camera.height, camera.width
+        self.dL_dimage = torch.empty(3, H, W, dtype=torch.float32, device=self.device)
+        self.loss = torch.zeros(1, dtype=torch.float32, device=self.device)
+        self.dL_dlatents = torch.empty_like(latents)
+        self.mlp_grads = rs.DeviceMLPGrads.like(mlp)
+
+    def forward(self, camera, target: torch.Tensor, scale: float, bg=(0.0, 0.0, 0.0), stream=None) -> Forward:
+        """MLP colours, render, L1 loss and its gradient (into self.dL_dimage, self.loss)."""
+        self.R.set_camera(camera)
+        rs.rs_appearance_fwd(camera, self.g.means, self.latents, self.mlp, self.colors, stream)
+        F = self.R.forward(self.gc, bg=bg, stream=stream)
+        rs.rs_l1_loss_grad(F.image, target, scale, self.dL_dimage, self.loss, stream)
+        return F
+
+    def backward(self, dL_dimage: torch.Tensor | None = None, stream=None) -> Backward:
+        """Compositing and projection backward from dL/dimage (default: the L1 gradient), then
+        the MLP backward (into self.dL_dlatents and self.mlp_grads)."""
+        B = self.R.backward(self.gc, self.dL_dimage if dL_dimage is None else dL_dimage, stream)
+        self.mlp_backward(B.dcolor, stream)
+        return B
+
+    def mlp_backward(self, dL_dcolor: torch.Tensor, stream=None):
+        rs.rs_appearance_bwd(self.R.camera, self.g.means, self.latents, self.mlp, dL_dcolor,
+                             self.dL_dlatents, self.mlp_grads, stream)
+
+    def view(self, camera, target, scale, bg=(0.0, 0.0, 0.0), stream=None):
+        F = self.forward(camera, target, scale, bg, stream)
+        return F, self.backward(stream=stream)

@@ -52,6 +52,17 @@ class rs_projected(ctypes.Structure):
                 ("d_records", ctypes.c_void_p)]
 
 
+class rs_mlp(ctypes.Structure):
+    _fields_ = [("latent_dim", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("d_W1", ctypes.c_void_p), ("d_b1", ctypes.c_void_p),
+                ("d_W2", ctypes.c_void_p), ("d_b2", ctypes.c_void_p)]
+
+
+class rs_mlp_grads(ctypes.Structure):
+    _fields_ = [("d_dW1", ctypes.c_void_p), ("d_db1", ctypes.c_void_p),
+                ("d_dW2", ctypes.c_void_p), ("d_db2", ctypes.c_void_p)]
+
+
 _lib = None
 _VP = ctypes.c_void_p
 
@@ -90,6 +101,11 @@ def lib():
         L.rs_project_bwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_gaussians),
                                      ctypes.POINTER(rs_projected), _VP, _VP, _VP, _VP, _VP, _VP,
                                      _VP, _VP]
+        L.rs_appearance_fwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.c_int32, _VP, _VP,
+                                        ctypes.POINTER(rs_mlp), _VP, _VP]
+        L.rs_appearance_bwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.c_int32, _VP, _VP,
+                                        ctypes.POINTER(rs_mlp), _VP, _VP, ctypes.POINTER(rs_mlp_grads), _VP]
+        L.rs_l1_loss_grad.argtypes = [ctypes.c_size_t, _VP, _VP, ctypes.c_float, _VP, _VP, _VP]
         for name in declared_symbols():
             getattr(L, name).restype = ctypes.c_char_p if name == "rs_error_string" else ctypes.c_int
         _lib = L
@@ -342,3 +358,92 @@ def rs_project_bwd(camera, gaussians: DeviceGaussians, proj: DeviceProjected, dL
         _ptr(dL_dmeans, torch.float32, 3 * n, "dL_dmeans"), _ptr(dL_dscales, torch.float32, 3 * n, "dL_dscales"),
         _ptr(dL_dquats, torch.float32, 4 * n, "dL_dquats"),
         _ptr(dL_dsh, torch.float32, 3 * K * n, "dL_dsh") if K else None, _stream(stream)))
+
+
+# ------------------------------------------------------------------ appearance MLP and L1 loss
+
+@dataclasses.dataclass
+class DeviceMLP:
+    """Appearance MLP weights as float32 CUDA tensors: W1 [hidden, latent_dim + 3], b1 [hidden],
+    W2 [3, hidden], b2 [3]."""
+    W1: torch.Tensor
+    b1: torch.Tensor
+    W2: torch.Tensor
+    b2: torch.Tensor
+
+    @property
+    def hidden(self) -> int:
+        return int(self.W1.shape[0])
+
+    @property
+    def latent_dim(self) -> int:
+        return int(self.W1.shape[1]) - 3
+
+    @staticmethod
+    def from_numpy(p, device="cuda"):
+        f = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+        return DeviceMLP(f(p["W1"]), f(p["b1"]), f(p["W2"]), f(p["b2"]))
+
+    def struct(self) -> rs_mlp:
+        m = rs_mlp()
+        H, L = self.hidden, self.latent_dim
+        m.latent_dim, m.hidden = L, H
+        m.d_W1 = _ptr(self.W1, torch.float32, H * (L + 3), "W1")
+        m.d_b1 = _ptr(self.b1, torch.float32, H, "b1")
+        m.d_W2 = _ptr(self.W2, torch.float32, 3 * H, "W2")
+        m.d_b2 = _ptr(self.b2, torch.float32, 3, "b2")
+        return m
+
+
+@dataclasses.dataclass
+class DeviceMLPGrads:
+    dW1: torch.Tensor
+    db1: torch.Tensor
+    dW2: torch.Tensor
+    db2: torch.Tensor
+
+    @staticmethod
+    def like(m: DeviceMLP):
+        return DeviceMLPGrads(torch.empty_like(m.W1), torch.empty_like(m.b1), torch.empty_like(m.W2),
+                              torch.empty_like(m.b2))
+
+    def struct(self) -> rs_mlp_grads:
+        g = rs_mlp_grads()
+        g.d_dW1 = _ptr(self.dW1, torch.float32, None, "dW1")
+        g.d_db1 = _ptr(self.db1, torch.float32, None, "db1")
+        g.d_dW2 = _ptr(self.dW2, torch.float32, None, "dW2")
+        g.d_db2 = _ptr(self.db2, torch.float32, None, "db2")
+        return g
+
+
+def rs_appearance_fwd(camera, means: torch.Tensor, latents: torch.Tensor, mlp: DeviceMLP,
+                      colors: torch.Tensor, stream=None):
+    n = int(latents.shape[1])
+    c, m = camera_struct(camera), mlp.struct()
+    _check("rs_appearance_fwd", lib().rs_appearance_fwd(
+        ctypes.byref(c), n, _ptr(means, torch.float32, 3 * n, "means"),
+        _ptr(latents, torch.float32, mlp.latent_dim * n, "latents"), ctypes.byref(m),
+        _ptr(colors, torch.float32, 3 * n, "colors"), _stream(stream)))
+
+
+def rs_appearance_bwd(camera, means: torch.Tensor, latents: torch.Tensor, mlp: DeviceMLP,
+                      dL_dcolors: torch.Tensor, dL_dlatents: torch.Tensor, grads: DeviceMLPGrads,
+                      stream=None):
+    n = int(latents.shape[1])
+    c, m, g = camera_struct(camera), mlp.struct(), grads.struct()
+    _check("rs_appearance_bwd", lib().rs_appearance_bwd(
+        ctypes.byref(c), n, _ptr(means, torch.float32, 3 * n, "means"),
+        _ptr(latents, torch.float32, mlp.latent_dim * n, "latents"), ctypes.byref(m),
+        _ptr(dL_dcolors, torch.float32, 3 * n, "dL_dcolors"),
+        _ptr(dL_dlatents, torch.float32, mlp.latent_dim * n, "dL_dlatents"), ctypes.byref(g), _stream(stream)))
+
+
+def rs_l1_loss_grad(image: torch.Tensor, target: torch.Tensor, scale: float, dL_dimage: torch.Tensor,
+                    loss: torch.Tensor | None = None, stream=None):
+    count = int(image.numel())
+    if int(target.numel()) != count:
+        raise ValueError("image and target differ in size")
+    _check("rs_l1_loss_grad", lib().rs_l1_loss_grad(
+        count, _ptr(image, torch.float32, count, "image"), _ptr(target, torch.float32, count, "target"),
+        ctypes.c_float(scale), _ptr(dL_dimage, torch.float32, count, "dL_dimage"),
+        _ptr(loss, torch.float32, 1, "loss"), _stream(stream)))

@@ -181,6 +181,57 @@ int rs_project_bwd(const rs_camera* camera, const rs_gaussians* gaussians,
                    const float* d_dL_dconic, const float* d_dL_dcolor, float* d_dL_dmeans,
                    float* d_dL_dscales, float* d_dL_dquats, float* d_dL_dsh, void* stream);
 
+/* Appearance MLP and L1 loss of the training-shaped step (rigel README "Appearance MLP"; the
+ * L1 term of its training loss).  rs_appearance_fwd produces the colours that rs_project reads
+ * when sh_degree is -1; rs_appearance_bwd takes the colours' gradient that rs_rasterize_bwd
+ * returns.  The pages give no device interface for these; this one follows the conventions
+ * above. */
+
+/* MLP weights, float32 device arrays: W1 [hidden][latent_dim + 3] and W2 [3][hidden], both
+ * row-major, b1 [hidden], b2 [3].  Supported sizes: hidden 32 or 64, 1 <= latent_dim <= 29
+ * (the page's MLP is sized for up to 29 latent dims and 64 hidden units). */
+typedef struct rs_mlp {
+    int32_t latent_dim, hidden;
+    const float* d_W1;
+    const float* d_b1;
+    const float* d_W2;
+    const float* d_b2;
+} rs_mlp;
+
+/* Weight gradients, same shapes as rs_mlp's arrays. */
+typedef struct rs_mlp_grads {
+    float* d_dW1;
+    float* d_db1;
+    float* d_dW2;
+    float* d_db2;
+} rs_mlp_grads;
+
+/* rigel README "Appearance MLP": for every Gaussian i, x = [latent_i ; (m_i - C) / |m_i - C|]
+ * with C = -R^T t the camera centre, h = relu(W1 x + b1), colour = sigmoid(W2 h + b2).
+ * Inputs: d_means [3][n], d_latents [latent_dim][n].  Output (overwritten): d_colors [3][n].
+ * The products run on the tensor cores in TF32 with split operands (three products per
+ * operand pair), which keeps float32 accuracy.  Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_appearance_fwd(const rs_camera* camera, int32_t n, const float* d_means,
+                      const float* d_latents, const rs_mlp* mlp, float* d_colors, void* stream);
+
+/* Backward of rs_appearance_fwd with the view direction held constant (rigel README "Appearance
+ * MLP": no gradient reaches the means through the MLP).  Input d_dL_dcolors [3][n].  Outputs:
+ * d_dL_dlatents [latent_dim][n] (overwritten) and the weight gradients summed over the n
+ * Gaussians (zeroed, then accumulated by the call; the accumulation order is not fixed).
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_appearance_bwd(const rs_camera* camera, int32_t n, const float* d_means,
+                      const float* d_latents, const rs_mlp* mlp, const float* d_dL_dcolors,
+                      float* d_dL_dlatents, const rs_mlp_grads* grads, void* stream);
+
+/* L1 loss between an image and its target over `count` floats:
+ * d_dL_dimage[i] = scale * sign(d_image[i] - d_target[i]) with sign(0) = 0 and, when d_loss is
+ * not NULL, *d_loss (one device float, overwritten) = scale * sum_i |d_image[i] - d_target[i]|
+ * (accumulation order not fixed).  With scale = 1 / (3 H W V) this is the gradient of the
+ * per-view mean absolute error averaged over V views (rigel README, training loss).
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_l1_loss_grad(size_t count, const float* d_image, const float* d_target, float scale,
+                    float* d_dL_dimage, float* d_loss, void* stream);
+
 /* Allocation-free variant of rs_bin.  The source pages have no counterpart: this entry point
  * exists for callers of this library that cannot allocate device memory -- for example a plug-in
  * whose host application owns and budgets all device memory, or a per-frame loop that must not

@@ -249,6 +249,22 @@ def appearance_bwd(cam, means, latents, W1, b1, W2, b2, dcolors):
     return out
 
 
+def l1_loss_grad(image, target, scale):
+    """L1 term of the training loss: (grad, loss) with grad = scale * sign(image - target) and
+    loss = scale * sum |image - target|."""
+    img = _d(image).reshape(-1)
+    tgt = _d(target).reshape(-1)
+    if img.size != tgt.size:
+        raise ValueError("image and target differ in size")
+    grad = np.zeros(img.size)
+    loss = ctypes.c_double(0.0)
+    rc = lib().orc_l1_loss_grad(ctypes.c_int64(img.size), _p(img), _p(tgt), ctypes.c_double(scale),
+                                _p(grad), ctypes.byref(loss))
+    if rc != 0:
+        raise ValueError(f"orc_l1_loss_grad returned {rc}")
+    return grad.reshape(np.shape(image)), float(loss.value)
+
+
 def render(cam, g, bg=(0.0, 0.0, 0.0), prec: int = 64):
     """Convenience: oracle project (decisions in `prec`) -> bin -> forward compositing."""
     P = project(cam, g, prec=prec)

@@ -892,4 +892,21 @@ int orc_appearance_bwd(const orc_camera* cam_in, int32_t n, int32_t L, int32_t H
     return 0;
 }
 
+
+// c8: the L1 term of rigel's training loss (README, training: "L1 + D-SSIM"), the absolute error
+// summed and scaled by `scale`, and its gradient, written from the definition: |d| and
+// d|d|/dd = sign d, with the subgradient 0 taken at d = 0.
+int orc_l1_loss_grad(int64_t count, const double* image, const double* target, double scale,
+                     double* grad, double* loss) {
+    if (count < 0) return -1;
+    double acc = 0.0;
+    for (int64_t i = 0; i < count; ++i) {
+        const double d = image[i] - target[i];
+        grad[i] = d > 0.0 ? scale : (d < 0.0 ? -scale : 0.0);
+        acc += d < 0.0 ? -d : d;
+    }
+    if (loss) *loss = scale * acc;
+    return 0;
+}
+
 }  // extern "C"

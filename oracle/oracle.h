@@ -118,6 +118,11 @@ int orc_appearance_bwd(const orc_camera* cam, int32_t n, int32_t L, int32_t H,
                        const double* dcolors, double* dlatents, double* dW1, double* db1,
                        double* dW2, double* db2);
 
+/* c8: L1 loss of the training step.  grad[i] = scale * sign(image[i] - target[i]) (sign(0) = 0),
+ * *loss = scale * sum_i |image[i] - target[i]|. */
+int orc_l1_loss_grad(int64_t count, const double* image, const double* target, double scale,
+                     double* grad, double* loss);
+
 #ifdef __cplusplus
 }
 #endif

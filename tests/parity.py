@@ -33,12 +33,8 @@ def u32(t):
     return t.cpu().numpy().view(np.uint32)
 
 
-def run_gpu(g, cam, bg=(0.0, 0.0, 0.0)):
-    """Forward through the C ABI; returns host copies plus the renderer for the backward."""
-    dg = rs.DeviceGaussians.from_numpy(g)
-    R = pipeline.Renderer(cam, g.n)
-    F = R.forward(dg, bg=bg)
-    torch.cuda.synchronize()
+def gpu_state(R, dg, F):
+    """Host copies of a forward's outputs, with the renderer and Gaussians for the backward."""
     P = F.proj
     return dict(renderer=R, dg=dg, n_entries=F.n_entries,
                 means2d=P.means2d.cpu().numpy(), depth=P.depth.cpu().numpy(),
@@ -48,6 +44,15 @@ def run_gpu(g, cam, bg=(0.0, 0.0, 0.0)):
                 point_list=u32(F.point_list[:F.n_entries]), ranges=u32(F.tile_ranges),
                 image=F.image.cpu().numpy(), final_T=F.final_T.cpu().numpy(),
                 n_contrib=u32(F.n_contrib))
+
+
+def run_gpu(g, cam, bg=(0.0, 0.0, 0.0)):
+    """Forward through the C ABI; returns host copies plus the renderer for the backward."""
+    dg = rs.DeviceGaussians.from_numpy(g)
+    R = pipeline.Renderer(cam, g.n)
+    F = R.forward(dg, bg=bg)
+    torch.cuda.synchronize()
+    return gpu_state(R, dg, F)
 
 
 def run_gpu_backward(G, dL):
@@ -62,9 +67,13 @@ def run_gpu_backward(G, dL):
     return G
 
 
-def allclose_report(name, got, ref, rtol, atol, mask=None, extra=None):
+def allclose_report(name, got, ref, rtol, atol, mask=None, extra=None, atol_of_max=0.0):
+    """|got - ref| <= atol + rtol |ref| (+ extra) elementwise; with atol_of_max the absolute part
+    is at least atol_of_max x max |ref| over the array."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
+    if atol_of_max and ref.size:
+        atol = max(atol, atol_of_max * float(np.abs(ref).max()))
     if extra is not None:
         extra = np.broadcast_to(np.asarray(extra, np.float64), ref.shape)
     if mask is not None:
@@ -136,7 +145,7 @@ def check_forward(cam, g, G, bg, tile_mask=None):
                 final_T_err=float(t_err), ambiguous_pixels=int((pm & (O["ambig"] != 0)).sum()))
 
 
-def check_raster_backward(cam, g, G, bg, fwd, dL, tile_mask=None):
+def check_raster_backward(cam, g, G, bg, fwd, dL, tile_mask=None, atol=GRAD_ATOL, atol_of_max=0.0):
     """Stage parity of the compositing backward: both sides walk the GPU's n_contrib, and the
     upstream gradient is zeroed at knife-edge pixels on both sides."""
     amb = fwd["O"]["ambig"] != 0
@@ -148,16 +157,16 @@ def check_raster_backward(cam, g, G, bg, fwd, dL, tile_mask=None):
                           tile_mask=tile_mask)
     res = {}
     for k in ("dmeans2d", "dconic", "dopacity", "dcolor"):
-        res[k] = allclose_report(k, G[k], O[k], GRAD_RTOL, GRAD_ATOL)
+        res[k] = allclose_report(k, G[k], O[k], GRAD_RTOL, atol, atol_of_max=atol_of_max)
     return O, res
 
 
-def check_project_backward(cam, g, G):
+def check_project_backward(cam, g, G, atol=GRAD_ATOL, atol_of_max=0.0):
     """Stage parity of the projection backward, fed the GPU's own raster gradients."""
     O = oracle.project_bwd(cam, g, G["radius"], G["dmeans2d"], G["dconic"], G["dcolor"])
     res = {}
     for k in ("dmeans", "dscales", "dquats"):
-        res[k] = allclose_report(k, G[k], O[k], GRAD_RTOL, GRAD_ATOL)
+        res[k] = allclose_report(k, G[k], O[k], GRAD_RTOL, atol, atol_of_max=atol_of_max)
     if G["dsh"] is not None:
-        res["dsh"] = allclose_report("dsh", G["dsh"], O["dsh"], GRAD_RTOL, GRAD_ATOL)
+        res["dsh"] = allclose_report("dsh", G["dsh"], O["dsh"], GRAD_RTOL, atol, atol_of_max=atol_of_max)
     return res

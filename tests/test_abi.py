@@ -80,3 +80,31 @@ def test_binding_refuses_cpu_tensors(L):
                            torch.zeros(3, 4), 0)
     with pytest.raises(TypeError):
         g.struct()
+
+
+def test_appearance_and_loss_validation(L):
+    cam = rs.camera_struct(scenes.procedural_camera(64, 48))
+    m = rs.rs_mlp()
+    m.latent_dim, m.hidden = 8, 64
+    m.d_W1 = m.d_b1 = m.d_W2 = m.d_b2 = ctypes.c_void_p(0x1000)
+    ok = ctypes.c_void_p(0x2000)
+    # unsupported widths and null weights are refused before any launch
+    for latent, hidden in ((8, 48), (0, 64), (30, 64), (8, 128)):
+        m.latent_dim, m.hidden = latent, hidden
+        assert L.rs_appearance_fwd(ctypes.byref(cam), 10, ok, ok, ctypes.byref(m), ok, None) == rs.RS_ERR_INVALID_ARG
+    m.latent_dim, m.hidden = 8, 64
+    m.d_W2 = None
+    assert L.rs_appearance_fwd(ctypes.byref(cam), 10, ok, ok, ctypes.byref(m), ok, None) == rs.RS_ERR_INVALID_ARG
+    m.d_W2 = ctypes.c_void_p(0x1000)
+    assert L.rs_appearance_fwd(ctypes.byref(cam), 10, None, ok, ctypes.byref(m), ok, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_appearance_fwd(ctypes.byref(cam), -1, ok, ok, ctypes.byref(m), ok, None) == rs.RS_ERR_INVALID_ARG
+    # n = 0 needs no buffers and launches nothing
+    assert L.rs_appearance_fwd(ctypes.byref(cam), 0, None, None, ctypes.byref(m), None, None) == rs.RS_OK
+    assert L.rs_appearance_bwd(ctypes.byref(cam), 10, ok, ok, ctypes.byref(m), ok, ok, None, None) == rs.RS_ERR_INVALID_ARG
+    gr = rs.rs_mlp_grads()
+    gr.d_dW1 = gr.d_db1 = gr.d_dW2 = ok
+    assert L.rs_appearance_bwd(ctypes.byref(cam), 10, ok, ok, ctypes.byref(m), ok, ok, ctypes.byref(gr),
+                               None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_l1_loss_grad(10, ok, ok, ctypes.c_float(float("nan")), ok, None, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_l1_loss_grad(10, None, ok, ctypes.c_float(1.0), ok, None, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_l1_loss_grad(10, ok, ok, ctypes.c_float(1.0), ok, ctypes.c_void_p(0x2001), None) == rs.RS_ERR_INVALID_ARG
