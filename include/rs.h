@@ -241,7 +241,7 @@ int rs_l1_loss_grad(size_t count, const float* d_image, const float* d_target, f
  * device image.  Every GPU that loads the library holds that array until the process exits.
  *  - Limit: the call returns RS_ERR_WORKSPACE, before any work, when
  *    rs_bin_workspace_size(n, camera, capacity) exceeds RS_BIN_NOALLOC_SCRATCH_BYTES
- *    (48 MiB: about 3.3 million entries for 160,000 Gaussians at 1920x1080).
+ *    (48 MiB: about 3.5 million entries for 160,000 Gaussians at 1920x1080).
  *  - Set-up: the first call on a device, with that device current, looks up the array's device
  *    address (cudaGetSymbolAddress) and keeps it for later calls; make that first call before
  *    any stream capture.  RS_ERR_CUDA if the lookup fails.
