@@ -62,7 +62,7 @@ B_BIN_PER_G = 8 + 4 * 16 + 8 + 40
 B_BIN_PER_ENTRY_FIXED, B_BIN_PER_ENTRY_PASS = 12, 16
 # DRAM bytes (read + write) of one k_raster_bwd launch on orbit view 1, from an ncu --set full
 # capture of the current kernel; must be re-taken (or set to None) whenever the kernel changes
-TRAFFIC_RASTER_BWD_BYTES = 58.290944e6 + 0.580352e6
+TRAFFIC_RASTER_BWD_BYTES = 58.293760e6 + 0.539136e6
 TRAFFIC_RASTER_BWD_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of k_raster_bwd, "
                              "160k scene, 1920x1080 orbit view 1")
 
@@ -84,6 +84,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-train", action="store_true",
+                    help="skip the training-shaped step's stage timings (reported beside the line)")
     return ap.parse_args()
 
 
@@ -287,12 +289,94 @@ def run_ours(args):
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(g, cams, rank, world, args, device)
+    if world == 1 and not args.no_train:
+        result["training_step"] = run_training_step(device)
     if world > 1:
         dist.barrier()
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# appearance MLP: HBM bytes per Gaussian (latents 8 + means 3 in, colours 3 out; the backward
+# also reads the colours' gradient and writes the latents' gradient)
+B_MLP_FWD_PER_G = 4 * (8 + 3 + 3)
+B_MLP_BWD_PER_G = 4 * (8 + 3 + 3 + 8)
+
+
+def run_training_step(device, steps: int = 5, warmup: int = 2):
+    """Stage times of the training-shaped step (250,000 Gaussians, 8 views of 400x400, MLP
+    11 -> 64 -> 3, L1 loss), CUDA events per stage, L2 written over before every view.  The
+    targets are this library's own renders of the Gaussians with their procedural colours (the
+    configuration's definition of ground truth); they are inputs to the timing only."""
+    import numpy as np
+    import torch
+
+    from gaussian_splatting_tile_gb300 import pipeline, rs, scenes
+
+    g, cams, p = scenes.training_scene()
+    dg = rs.DeviceGaussians.from_numpy(g, device)
+    mlp = rs.DeviceMLP.from_numpy(p, device)
+    lat = torch.from_numpy(p["latents"]).to(device)
+    tr = pipeline.Renderer(cams[0], g.n, device, capacity=4_000_000, keep_keys=False)
+    targets = []
+    for cam in cams:
+        tr.set_camera(cam)
+        targets.append(tr.forward(dg).image.clone())
+    del tr
+    step = pipeline.AppearanceStep(cams[0], dg, mlp, lat, device, capacity=4_000_000)
+    step.R.keep_keys = False
+    scale = 1.0 / (3 * cams[0].width * cams[0].height * len(cams))
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def one(v, ev=None):
+        cam = cams[v]
+        rec = (lambda k: ev[k].record(stream)) if ev else (lambda k: None)
+        step.R.set_camera(cam)
+        rec(0)
+        rs.rs_appearance_fwd(cam, dg.means, lat, mlp, step.colors)
+        rec(1)
+        F = step.R.forward(step.gc)
+        rec(2)
+        rs.rs_l1_loss_grad(F.image, targets[v], scale, step.dL_dimage, step.loss)
+        rec(3)
+        B = step.R.backward(step.gc, step.dL_dimage)
+        rec(4)
+        step.mlp_backward(B.dcolor)
+        rec(5)
+
+    for _ in range(warmup):
+        for v in range(len(cams)):
+            one(v)
+    torch.cuda.synchronize(device)
+    names = ["mlp_fwd", "render_fwd", "l1_loss", "render_bwd", "mlp_bwd"]
+    times = []
+    for _ in range(steps):
+        for v in range(len(cams)):
+            flush.fill_(float(v))
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            one(v, ev)
+            times.append(ev)
+    torch.cuda.synchronize(device)
+    st = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(5)] for e in times])
+    per_view = st.mean(axis=0)
+    hbm, src = measured_peaks()
+    n = g.n
+    mlp_fwd_s = per_view[0] * 1e-3
+    mlp_bwd_s = per_view[4] * 1e-3
+    return dict(workload=("250k Gaussians (sphere/helix/plane), 8 views of 400x400 per step, MLP 11->64->3 "
+                          "(split-TF32 tensor cores), L1 loss; targets are renders with the procedural colours"),
+                ms_per_step=float(st.sum(axis=1).mean() * len(cams)),
+                stage_ms_per_view=dict(zip(names, [float(x) for x in per_view])),
+                steps=steps, views_per_step=len(cams),
+                mlp_roofline=dict(bound="hbm", unit="GB/s", peak=hbm, peak_source=src,
+                                  fwd_achieved=n * B_MLP_FWD_PER_G / mlp_fwd_s / 1e9,
+                                  fwd_frac=n * B_MLP_FWD_PER_G / mlp_fwd_s / 1e9 / hbm,
+                                  bwd_achieved=n * B_MLP_BWD_PER_G / mlp_bwd_s / 1e9,
+                                  bwd_frac=n * B_MLP_BWD_PER_G / mlp_bwd_s / 1e9 / hbm,
+                                  bytes_per_gaussian=dict(fwd=B_MLP_FWD_PER_G, bwd=B_MLP_BWD_PER_G)))
 
 
 def roofline(res, Q, E, n, cam, blend_ratio):

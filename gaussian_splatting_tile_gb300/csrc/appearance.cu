@@ -95,29 +95,41 @@ __device__ void load_weights(const MlpArgs& a, WeightSmem<HID>& w) {
 }
 
 // x of Gaussians i0 .. i0 + 15 into s_x [16][kXStride]; rows past n and columns past D are zero.
+// The loads of a row are independent and unrolled (L < KS*8 - 2), so they are all in flight at
+// once.
 template <int KS>
 __device__ __forceinline__ void stage_x(const MlpArgs& a, int i0, float* s_x) {
     const int lane = threadIdx.x & 31;
     if (lane < kRows) {
         const int i = i0 + lane;
         float* row = s_x + lane * kXStride;
-        if (i < a.n) {
-            for (int k = 0; k < a.L; ++k) row[k] = a.latents[size_t(k) * a.n + i];
+        float v[KS * 8];
+        const bool in = i < a.n;
+#pragma unroll
+        for (int k = 0; k < KS * 8 - 3; ++k) v[k] = in && k < a.L ? a.latents[size_t(k) * a.n + i] : 0.f;
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+        if (in) {
             const CameraF& cam = a.cam;
             // camera centre C = -R^T t
             const float C0 = -(cam.R[0] * cam.t[0] + cam.R[3] * cam.t[1] + cam.R[6] * cam.t[2]);
             const float C1 = -(cam.R[1] * cam.t[0] + cam.R[4] * cam.t[1] + cam.R[7] * cam.t[2]);
             const float C2 = -(cam.R[2] * cam.t[0] + cam.R[5] * cam.t[1] + cam.R[8] * cam.t[2]);
-            const float d0 = a.means[i] - C0, d1 = a.means[size_t(a.n) + i] - C1,
-                        d2 = a.means[2 * size_t(a.n) + i] - C2;
+            d0 = a.means[i] - C0;
+            d1 = a.means[size_t(a.n) + i] - C1;
+            d2 = a.means[2 * size_t(a.n) + i] - C2;
             const float len = sqrtf(d0 * d0 + d1 * d1 + d2 * d2);
             const float il = len > 0.f ? 1.0f / len : 0.f;
-            row[a.L] = d0 * il;
-            row[a.L + 1] = d1 * il;
-            row[a.L + 2] = d2 * il;
-            for (int k = a.D; k < KS * 8; ++k) row[k] = 0.f;
-        } else {
-            for (int k = 0; k < KS * 8; ++k) row[k] = 0.f;
+            d0 *= il;
+            d1 *= il;
+            d2 *= il;
+        }
+#pragma unroll
+        for (int k = KS * 8 - 3; k < KS * 8; ++k) v[k] = 0.f;
+#pragma unroll
+        for (int k = 0; k < KS * 8; ++k) {
+            // the view direction sits right after the latents
+            const float dir = k == a.L ? d0 : k == a.L + 1 ? d1 : k == a.L + 2 ? d2 : 0.f;
+            row[k] = k < a.L ? v[k] : dir;
         }
     }
     __syncwarp();
@@ -253,21 +265,30 @@ __global__ void __launch_bounds__(kMlpThreads) k_mlp_bwd(MlpArgs a, const float*
     const int tiles = (a.n + kRows - 1) / kRows;
     for (int tile = blockIdx.x * kMlpWarps + (threadIdx.x >> 5); tile < tiles; tile += gridDim.x * kMlpWarps) {
         const int i0 = tile * kRows;
+        // dL/dcolour of this lane's slots (lane t = 0: channels 0, 1; t = 1: channel 2; slots
+        // 0, 2 for rows g, g + 8), loaded first so that the loads overlap the products
+        float dc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < 2) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = 2 * t + (k & 1), i = i0 + g + 8 * (k >> 1);
+                if (c < 3 && i < a.n) dc[k] = dcolors[size_t(c) * a.n + i];
+            }
+        }
         stage_x<KS>(a, i0, st.x);
         float h[HID / 8][4];
         layer1<HID, KS>(w, st.x, h);
         float z[4];
         layer2<HID>(w, h, z);
-        // dL/dz2 = dL/dcolour * s (1 - s), s = sigmoid(z2 + b2): lane t = 0 holds channels 0, 1
-        // and lane t = 1 channel 2 (slots 0, 2 for rows g, g + 8)
+        // dL/dz2 = dL/dcolour * s (1 - s), s = sigmoid(z2 + b2)
         float p[4] = {0.f, 0.f, 0.f, 0.f};
         if (t < 2) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int c = 2 * t + (k & 1), i = i0 + g + 8 * (k >> 1);
-                if (c < 3 && i < a.n) {
+                const int c = 2 * t + (k & 1);
+                if (c < 3) {
                     const float s = sigmoidf(z[k] + w.b2[c]);
-                    p[k] = dcolors[size_t(c) * a.n + i] * s * (1.f - s);
+                    p[k] = dc[k] * s * (1.f - s);
                 }
             }
         }
