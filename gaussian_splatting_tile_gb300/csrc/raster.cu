@@ -1,5 +1,6 @@
-// [3] forward compositing and [4] its backward: one 256-thread block per 16x16 tile, one pixel
-// per thread, the tile's depth-sorted list staged through shared memory 256 entries at a time.
+// [3] forward compositing and [4] its backward: one block per 16x16 tile (the forward 256
+// threads, one pixel each; the backward 128 threads, two pixels each), the tile's depth-sorted
+// list staged through shared memory 256 entries at a time.
 //
 // Forward: rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel" (cooperative
 // fetch, __syncthreads_count vote: the block leaves once all 256 pixels are saturated).
@@ -9,8 +10,9 @@
 // (shared-memory accumulators, one slot per staged entry) before one global atomic per entry,
 // component and tile -- the reduction rigel's README names as missing from its backward.
 //
-// Both kernels give each warp an 8x4 pixel rectangle and, after a batch is staged, let each warp
-// compact the entries whose alpha >= 1/255 box (from the record) meets its rectangle: the other
+// The forward gives each warp an 8x4 pixel rectangle, the backward an 8x8 square; after a batch
+// is staged, each warp compacts the entries whose alpha >= 1/255 box (from the record) meets its
+// rectangle: the other
 // entries would be examined and skipped at every pixel of the warp, so they are skipped without
 // being evaluated.  n_contrib is kept as a position in the list (one past the entry that stopped
 // the pixel, or the list length), which is exactly the count of examined entries.
@@ -29,7 +31,7 @@ constexpr unsigned kFull = 0xffffffffu;
 #define RS_FWD_MIN_BLOCKS 6
 #endif
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS 6
+#define RS_BWD_MIN_BLOCKS 8  // blocks of 128 threads
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -186,7 +188,45 @@ __device__ __forceinline__ int sum_slot(unsigned lane) {
 constexpr int kSums = 9;          // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2, gp, w G_rgb
 constexpr int kAccStride = kBatch + 1;  // padding keeps the nine slots of one entry in nine banks
 
-__global__ void __launch_bounds__(kTilePixels, RS_BWD_MIN_BLOCKS) k_raster_bwd(
+// The backward runs 128 threads per tile: warp w owns the 8x8 square at columns (w & 1) * 8 and
+// rows (w >> 1) * 8, and lane l the two pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4) of it.
+// Each warp-level reduction then covers 64 pixels, and the two pixels of a lane share their
+// column, so their nine sums fold before the shuffles.
+constexpr int kBwdThreads = 128;
+constexpr int kBwdWarps = kBwdThreads / 32;
+
+// Bit w is set when warp w's 8x8 square meets the entry's alpha >= 1/255 box.
+__device__ __forceinline__ uint32_t square_mask(const float4& p, const float4& q, int tx0, int ty0) {
+    if (!(p.w >= 0.f)) return 0u;
+    const float xl = p.x - p.w - float(tx0), xh = p.x + p.w - float(tx0);
+    const float yl = p.y - q.w - float(ty0), yh = p.y + q.w - float(ty0);
+    const bool c0 = xl <= 7.f && xh >= 0.f, c1 = xl <= 15.f && xh >= 8.f;
+    const bool r0 = yl <= 7.f && yh >= 0.f, r1 = yl <= 15.f && yh >= 8.f;
+    return (r0 && c0 ? 1u : 0u) | (r0 && c1 ? 2u : 0u) | (r1 && c0 ? 4u : 0u) | (r1 && c1 ? 8u : 0u);
+}
+
+// Per-pixel state of the reverse walk.
+struct BwdPixel {
+    float T, SG, G0, G1, G2;
+    uint32_t end;  // one past the last entry the pixel examined
+};
+
+// One entry at one pixel: updates the pixel's state; returns gp = dL/dpower (0 if clamped) and
+// w = alpha T_j, or false if the entry is skipped there.
+__device__ __forceinline__ bool bwd_step(BwdPixel& px, float alpha, float raw, const float4& c, float& gp,
+                                         float& w) {
+    const float one_m = 1.f - alpha;
+    const float Tj = __fdividef(px.T, one_m);
+    w = alpha * Tj;
+    const float cG = fmaf(c.x, px.G0, fmaf(c.y, px.G1, c.z * px.G2));
+    const float dalpha = Tj * (cG - px.SG);
+    px.SG = fmaf(alpha, cG, one_m * px.SG);
+    px.T = Tj;
+    gp = raw <= kAlphaMax ? alpha * dalpha : 0.f;  // not clamped: alpha = opacity * exp(power)
+    return true;
+}
+
+__global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     CameraF cam, int n, const Record* __restrict__ rec, const uint2* __restrict__ ranges,
     const uint32_t* __restrict__ list, float3 bg, const float* __restrict__ final_T,
     const uint32_t* __restrict__ n_contrib, const float* __restrict__ dL_dimage,
@@ -194,129 +234,136 @@ __global__ void __launch_bounds__(kTilePixels, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     float* __restrict__ dcol) {
     __shared__ float4 s_p[kBatch], s_q[kBatch], s_c[kBatch];
     __shared__ uint32_t s_g[kBatch];
-    __shared__ uint32_t s_mask[kBatch];
-    __shared__ uint8_t s_list[kWarps][kBatch];
+    __shared__ uint8_t s_mask[kBatch];
+    __shared__ uint8_t s_list[kBwdWarps][kBatch];
     __shared__ float s_acc[kSums * kAccStride];
-    __shared__ uint32_t s_max;
+    __shared__ uint32_t s_wmax[kBwdWarps];
     const int tile = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const unsigned lane = threadIdx.x & 31;
-    int tx0, ty0, px, py;
-    tile_pixel(cam, tile, tx0, ty0, px, py);
-    const bool inside = px < cam.W && py < cam.H;
+    const int tx0 = (tile % cam.TX) * kTile, ty0 = (tile / cam.TX) * kTile;
+    const int px = tx0 + (warp & 1) * 8 + int(lane & 7);
+    const int py0 = ty0 + (warp >> 1) * 8 + int(lane >> 3);
     const uint2 range = ranges[tile];
     const uint32_t len = range.y - range.x;
-    const size_t HW = size_t(cam.W) * cam.H, pix = inside ? size_t(py) * cam.W + px : 0;
-    // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the min()
-    // keeps inconsistent caller data inside the tile's list
-    const uint32_t my_n = inside ? min(n_contrib[pix], len) : 0u;
-    float T = inside ? final_T[pix] : 1.f;
-    const float G0 = inside ? dL_dimage[pix] : 0.f;
-    const float G1 = inside ? dL_dimage[HW + pix] : 0.f;
-    const float G2 = inside ? dL_dimage[2 * HW + pix] : 0.f;
-    // the colour behind an entry (per unit T) only enters the gradient through its dot product
-    // with dL/dC, so that scalar is carried instead of the colour
-    float SG = bg.x * G0 + bg.y * G1 + bg.z * G2;
-    if (threadIdx.x == 0) s_max = 0;
+    const size_t HW = size_t(cam.W) * cam.H;
+    BwdPixel P[2];
 #pragma unroll
-    for (int k = 0; k < kSums; ++k) s_acc[k * kAccStride + threadIdx.x] = 0.f;
+    for (int h = 0; h < 2; ++h) {
+        const int py = py0 + 4 * h;
+        const bool inside = px < cam.W && py < cam.H;
+        const size_t pix = inside ? size_t(py) * cam.W + px : 0;
+        // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the min()
+        // keeps inconsistent caller data inside the tile's list
+        P[h].end = range.x + (inside ? min(n_contrib[pix], len) : 0u);
+        P[h].T = inside ? final_T[pix] : 1.f;
+        P[h].G0 = inside ? dL_dimage[pix] : 0.f;
+        P[h].G1 = inside ? dL_dimage[HW + pix] : 0.f;
+        P[h].G2 = inside ? dL_dimage[2 * HW + pix] : 0.f;
+        // the colour behind an entry (per unit T) only enters the gradient through its dot
+        // product with dL/dC, so that scalar is carried instead of the colour
+        P[h].SG = bg.x * P[h].G0 + bg.y * P[h].G1 + bg.z * P[h].G2;
+    }
+    for (int i = threadIdx.x; i < kSums * kAccStride; i += kBwdThreads) s_acc[i] = 0.f;
+    const uint32_t warp_end = __reduce_max_sync(kFull, max(P[0].end, P[1].end));
+    if (lane == 0) s_wmax[warp] = warp_end;
     __syncthreads();
-    const uint32_t wmax = __reduce_max_sync(kFull, my_n);
-    if (lane == 0) atomicMax(&s_max, wmax);
-    __syncthreads();
-    const uint32_t my_end = range.x + my_n;
-    const uint32_t warp_end = range.x + wmax;
-    const uint32_t walk_end = range.x + s_max;
-    const float fx = float(px), fy = float(py);
+    uint32_t walk_end = s_wmax[0];
+#pragma unroll
+    for (int w = 1; w < kBwdWarps; ++w) walk_end = max(walk_end, s_wmax[w]);
+    const float fx = float(px), fy0 = float(py0), fy1 = float(py0 + 4);
     const uint32_t wbit = 1u << warp;
     const int slot = sum_slot(lane);
     uint8_t* my_list = s_list[warp];
     for (uint32_t batch_end = walk_end; batch_end > range.x;) {
         const uint32_t batch_start = batch_end - range.x > uint32_t(kBatch) ? batch_end - kBatch : range.x;
         const int cnt = int(batch_end - batch_start);
-        uint32_t m = 0u;
-        if (int(threadIdx.x) < cnt) {
-            const uint32_t g = list[batch_start + threadIdx.x];
-            const Record& r = rec[g];
-            s_g[threadIdx.x] = g;
-            s_p[threadIdx.x] = r.p;
-            s_q[threadIdx.x] = r.q;
-            s_c[threadIdx.x] = r.c;
-            m = warp_mask(r.p, r.q, tx0, ty0);
+#pragma unroll
+        for (int r = 0; r < kBatch / kBwdThreads; ++r) {
+            const int t = r * kBwdThreads + int(threadIdx.x);
+            uint32_t m = 0u;
+            if (t < cnt) {
+                const uint32_t g = list[batch_start + t];
+                const Record& rr = rec[g];
+                s_g[t] = g;
+                s_p[t] = rr.p;
+                s_q[t] = rr.q;
+                s_c[t] = rr.c;
+                m = square_mask(rr.p, rr.q, tx0, ty0);
+            }
+            s_mask[t] = uint8_t(m);
         }
-        s_mask[threadIdx.x] = m;
         __syncthreads();
         const int nl = compact_warp(my_list, [&](int j) {
             return (s_mask[j] & wbit) != 0u && batch_start + uint32_t(j) < warp_end;
         });
         for (int k = nl - 1; k >= 0; --k) {
             const int j = my_list[k];
-            float v[kSums];
-#pragma unroll
-            for (int t = 0; t < kSums; ++t) v[t] = 0.f;
-            bool act = false;
-            if (batch_start + uint32_t(j) < my_end) {
-                float dx, dy, G, raw;
-                const float alpha = entry_alpha(s_p[j], s_q[j], fx, fy, dx, dy, G, raw);
-                if (alpha >= kAlphaMin) {
-                    act = true;
-                    const float4 c = s_c[j];
-                    const float one_m = 1.f - alpha;
-                    const float Tj = __fdividef(T, one_m);
-                    const float w = alpha * Tj;
-                    v[6] = w * G0;
-                    v[7] = w * G1;
-                    v[8] = w * G2;
-                    const float cG = fmaf(c.x, G0, fmaf(c.y, G1, c.z * G2));
-                    const float dalpha = Tj * (cG - SG);
-                    SG = fmaf(alpha, cG, one_m * SG);
-                    T = Tj;
-                    if (raw <= kAlphaMax) {  // not clamped: alpha = opacity * exp(power)
-                        const float gp = alpha * dalpha;  // dL/dpower at this pixel
-                        v[0] = gp * dx;
-                        v[1] = gp * dy;
-                        v[2] = v[0] * dx;
-                        v[3] = v[0] * dy;
-                        v[4] = v[1] * dy;
-                        v[5] = gp;
-                    }
-                }
+            const uint32_t e = batch_start + uint32_t(j);
+            const float4 p = s_p[j], q = s_q[j];
+            float dx, dy0, dy1, G, raw0, raw1;
+            const float a0 = entry_alpha(p, q, fx, fy0, dx, dy0, G, raw0);
+            const float a1 = entry_alpha(p, q, fx, fy1, dx, dy1, G, raw1);
+            const bool act0 = e < P[0].end && a0 >= kAlphaMin;
+            const bool act1 = e < P[1].end && a1 >= kAlphaMin;
+            float gp0 = 0.f, gp1 = 0.f, w0 = 0.f, w1 = 0.f;
+            if (act0 || act1) {
+                const float4 c = s_c[j];
+                if (act0) bwd_step(P[0], a0, raw0, c, gp0, w0);
+                if (act1) bwd_step(P[1], a1, raw1, c, gp1, w1);
             }
-            if (__any_sync(kFull, act)) {
+            if (__any_sync(kFull, act0 || act1)) {
+                // the two pixels share dx: fold their sums, then reduce over the warp
+                const float sg = gp0 + gp1;
+                const float sgy = fmaf(gp1, dy1, gp0 * dy0);
+                float v[kSums];
+                v[0] = sg * dx;
+                v[1] = sgy;
+                v[2] = v[0] * dx;
+                v[3] = sgy * dx;
+                v[4] = fmaf(gp1 * dy1, dy1, (gp0 * dy0) * dy0);
+                v[5] = sg;
+                v[6] = fmaf(w1, P[1].G0, w0 * P[0].G0);
+                v[7] = fmaf(w1, P[1].G1, w0 * P[0].G1);
+                v[8] = fmaf(w1, P[1].G2, w0 * P[0].G2);
                 const float sum = butterfly9(v, lane);
                 if (slot >= 0) atomicAdd(&s_acc[slot * kAccStride + j], sum);
             }
         }
         __syncthreads();
-        if (int(threadIdx.x) < cnt) {
-            // per-entry tile sums -> gradients of the entry's Gaussian:
-            //   du = A sum(gp dx) + B sum(gp dy), dv = B sum(gp dx) + C sum(gp dy),
-            //   dA = -sum(gp dx^2)/2, dB = -sum(gp dx dy), dC = -sum(gp dy^2)/2,
-            //   dopacity = sum(gp)/opacity (gp = opacity exp(power) dL/dalpha), dcolour = sum(w G)
-            const int t = threadIdx.x;
-            float a[kSums];
-            bool any = false;
 #pragma unroll
-            for (int k = 0; k < kSums; ++k) {
-                a[k] = s_acc[k * kAccStride + t];
-                s_acc[k * kAccStride + t] = 0.f;
-                any |= a[k] != 0.f;
-            }
-            if (any) {
-                const uint32_t g = s_g[t];
-                const size_t N = size_t(n);
-                const float4 p = s_p[t], q = s_q[t];
-                constexpr float kLn2 = 0.6931471805599453f;
-                const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
-                atomicAdd(dm2 + g, fmaf(A, a[0], B * a[1]));
-                atomicAdd(dm2 + N + g, fmaf(B, a[0], C * a[1]));
-                atomicAdd(dcon + g, -0.5f * a[2]);
-                atomicAdd(dcon + N + g, -a[3]);
-                atomicAdd(dcon + 2 * N + g, -0.5f * a[4]);
-                atomicAdd(dop + g, a[5] / p.z);
-                atomicAdd(dcol + g, a[6]);
-                atomicAdd(dcol + N + g, a[7]);
-                atomicAdd(dcol + 2 * N + g, a[8]);
+        for (int r = 0; r < kBatch / kBwdThreads; ++r) {
+            const int t = r * kBwdThreads + int(threadIdx.x);
+            if (t < cnt) {
+                // per-entry tile sums -> gradients of the entry's Gaussian:
+                //   du = A sum(gp dx) + B sum(gp dy), dv = B sum(gp dx) + C sum(gp dy),
+                //   dA = -sum(gp dx^2)/2, dB = -sum(gp dx dy), dC = -sum(gp dy^2)/2,
+                //   dopacity = sum(gp)/opacity (gp = opacity exp(power) dL/dalpha),
+                //   dcolour = sum(w G)
+                float a[kSums];
+                bool any = false;
+#pragma unroll
+                for (int k = 0; k < kSums; ++k) {
+                    a[k] = s_acc[k * kAccStride + t];
+                    s_acc[k * kAccStride + t] = 0.f;
+                    any |= a[k] != 0.f;
+                }
+                if (any) {
+                    const uint32_t g = s_g[t];
+                    const size_t N = size_t(n);
+                    const float4 p = s_p[t], q = s_q[t];
+                    constexpr float kLn2 = 0.6931471805599453f;
+                    const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
+                    atomicAdd(dm2 + g, fmaf(A, a[0], B * a[1]));
+                    atomicAdd(dm2 + N + g, fmaf(B, a[0], C * a[1]));
+                    atomicAdd(dcon + g, -0.5f * a[2]);
+                    atomicAdd(dcon + N + g, -a[3]);
+                    atomicAdd(dcon + 2 * N + g, -0.5f * a[4]);
+                    atomicAdd(dop + g, a[5] / p.z);
+                    atomicAdd(dcol + g, a[6]);
+                    atomicAdd(dcol + N + g, a[7]);
+                    atomicAdd(dcol + 2 * N + g, a[8]);
+                }
             }
         }
         __syncthreads();
@@ -367,7 +414,7 @@ cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
                               const float* dL_dimage, float* dm2, float* dcon, float* dop,
                               float* dcol, cudaStream_t s) {
     const int tiles = cam.TX * cam.TY;
-    k_raster_bwd<<<tiles, kTilePixels, 0, s>>>(cam, n, rec, reinterpret_cast<const uint2*>(ranges),
+    k_raster_bwd<<<tiles, kBwdThreads, 0, s>>>(cam, n, rec, reinterpret_cast<const uint2*>(ranges),
                                                list, bg, final_T, n_contrib, dL_dimage, dm2, dcon,
                                                dop, dcol);
     return cudaGetLastError();
