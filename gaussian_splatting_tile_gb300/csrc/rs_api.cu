@@ -89,11 +89,17 @@ int rs_bin_workspace_size(int32_t n, const rs_camera* camera, size_t capacity, s
     return RS_OK;
 }
 
-int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
-           size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
-           uint32_t* d_point_list, uint32_t* d_tile_ranges, size_t* n_entries, void* stream) {
-    if (!camera_ok(camera) || !n_ok(n) || !n_entries || capacity > size_t(RS_MAX_ENTRIES))
-        return RS_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Validation and launches shared by rs_bin and rs_bin_async; on RS_OK the binning is enqueued
+// and *result_dev points at the workspace's {E (uint64), error (uint32), pad} block.
+int enqueue_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
+                size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
+                uint32_t* d_point_list, uint32_t* d_tile_ranges, cudaStream_t s,
+                const uint8_t** result_dev) {
+    if (!camera_ok(camera) || !n_ok(n) || capacity > size_t(RS_MAX_ENTRIES)) return RS_ERR_INVALID_ARG;
     if (!d_tile_ranges || !aligned(d_tile_ranges, 8)) return RS_ERR_INVALID_ARG;
     if (!d_workspace || !aligned(d_workspace, 256)) return RS_ERR_INVALID_ARG;
     if (n > 0 && !projected_ok(proj, false)) return RS_ERR_INVALID_ARG;
@@ -102,24 +108,52 @@ int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d
     const CameraF cam = rs::make_camera(*camera);
     const rs::BinPlan plan = rs::plan_bin(n, cam, capacity);
     if (workspace_bytes < plan.total_bytes) return RS_ERR_WORKSPACE;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     rs_projected empty{};
     const rs_projected& p = proj ? *proj : empty;
     cudaError_t e = rs::launch_bin(plan, cam, p, ws, d_keys_sorted, d_point_list, d_tile_ranges, s);
     if (e != cudaSuccess) return RS_ERR_CUDA;
+    *result_dev = ws + plan.off_result;
+    return RS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
+           size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
+           uint32_t* d_point_list, uint32_t* d_tile_ranges, size_t* n_entries, void* stream) {
+    if (!n_entries) return RS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint8_t* dev = nullptr;
+    const int rc = enqueue_bin(camera, proj, n, d_workspace, workspace_bytes, capacity, d_keys_sorted,
+                               d_point_list, d_tile_ranges, s, &dev);
+    if (rc != RS_OK) return rc;
     // the path's one device-to-host read: the entry count (and the sort's wait flag)
     struct {
         uint64_t E;
         uint32_t error, pad;
     } result{};
-    e = cudaMemcpyAsync(&result, ws + plan.off_result, sizeof(result), cudaMemcpyDeviceToHost, s);
+    cudaError_t e = cudaMemcpyAsync(&result, dev, sizeof(result), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return RS_ERR_CUDA;
     *n_entries = size_t(result.E);
     if (result.E > uint64_t(capacity)) return RS_ERR_CAPACITY;
     if (result.error != 0) return RS_ERR_DEVICE_TIMEOUT;
     return RS_OK;
+}
+
+int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
+                 size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
+                 uint32_t* d_point_list, uint32_t* d_tile_ranges, uint64_t* h_result, void* stream) {
+    if (!h_result || !aligned(h_result, 8)) return RS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint8_t* dev = nullptr;
+    const int rc = enqueue_bin(camera, proj, n, d_workspace, workspace_bytes, capacity, d_keys_sorted,
+                               d_point_list, d_tile_ranges, s, &dev);
+    if (rc != RS_OK) return rc;
+    return cuda_rc(cudaMemcpyAsync(h_result, dev, 2 * sizeof(uint64_t), cudaMemcpyDeviceToHost, s));
 }
 
 int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,

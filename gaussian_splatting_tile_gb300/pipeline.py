@@ -87,8 +87,12 @@ class Renderer:
         bgv = (ctypes.c_float * 3)(*[float(x) for x in bg])
         self._bgv = bgv
         vp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+        self._hres = ctypes.c_void_p(0)  # pinned (E, error) slot of the next rs_bin_async call
         calls = dict(
             project=rs.PreparedCall("rs_project", (cam, ctypes.byref(gs), ctypes.byref(ps))),
+            bin_async=rs.PreparedCall("rs_bin_async", (cam, ctypes.byref(ps), self.n, vp(self.workspace),
+                                                       self.workspace.numel(), self.capacity, vp(self.keys_sorted),
+                                                       vp(self.point_list), vp(self.tile_ranges), self._hres)),
             bin=rs.PreparedCall("rs_bin", (cam, ctypes.byref(ps), self.n, vp(self.workspace),
                                            self.workspace.numel(), self.capacity, vp(self.keys_sorted),
                                            vp(self.point_list), vp(self.tile_ranges), ctypes.byref(self._E))),
@@ -122,6 +126,22 @@ class Renderer:
                 self._alloc(int(self._E.value * 1.25) + 1024)
                 self._bound = None
 
+    def bin_async(self, result: torch.Tensor, stream=None):
+        """Enqueue the binning without waiting: (E, error flag) land in `result` (pinned int64
+        [2]) once the stream gets there.  If E turns out above the capacity, the frame rendered
+        the background: grow with `reserve(E)` and redo it."""
+        if result.is_cuda or result.dtype != torch.int64 or result.numel() < 2:
+            raise TypeError("result must be a pinned int64 host tensor with 2 elements")
+        calls = self._prepare(self._g, getattr(self, "bg", (0.0, 0.0, 0.0)))
+        self._hres.value = result.data_ptr()
+        calls["bin_async"].run(rs.stream_handle(stream))
+
+    def reserve(self, entries: int):
+        """Grow the entry buffers to hold at least `entries` entries."""
+        if entries > self.capacity:
+            self._alloc(int(entries * 1.25) + 1024)
+            self._bound = None
+
     def rasterize(self, bg=(0.0, 0.0, 0.0), stream=None):
         self.bg = tuple(bg)
         self._prepare(self._g, self.bg)["fwd"].run(rs.stream_handle(stream))
@@ -134,6 +154,28 @@ class Renderer:
         self.n_entries = E
         return Forward(self.proj, E, self.point_list, self.keys_sorted, self.tile_ranges,
                        self.image, self.final_T, self.n_contrib, self.bg)
+
+    def forward_async(self, g: rs.DeviceGaussians, result: torch.Tensor, bg=(0.0, 0.0, 0.0), stream=None):
+        """forward() with the sync-free binning: nothing waits for the entry count, which lands
+        in `result` (pinned int64 [2]: E, error flag).  After synchronising, check it with
+        `check_async(result)`; a frame whose E exceeded the capacity rendered the background."""
+        self.bg = tuple(bg)
+        self.project(g, stream)
+        self.bin_async(result, stream)
+        self.rasterize(bg, stream)
+
+    def check_async(self, result: torch.Tensor) -> int:
+        """E of a finished rs_bin_async; raises (after growing the buffers) on overflow or timeout."""
+        E, err = int(result[0]), int(result[1])
+        if err:
+            raise rs.RsError("rs_bin_async", rs.RS_ERR_DEVICE_TIMEOUT, rs.error_string(rs.RS_ERR_DEVICE_TIMEOUT))
+        if E > self.capacity:
+            self.reserve(E)
+            err = rs.RsError("rs_bin_async", rs.RS_ERR_CAPACITY, rs.error_string(rs.RS_ERR_CAPACITY))
+            err.n_entries = E
+            raise err
+        self.n_entries = E
+        return E
 
     def _grads(self, sh_degree: int):
         n, d = self.n, self.device

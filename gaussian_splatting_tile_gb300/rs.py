@@ -90,6 +90,8 @@ def lib():
         L.rs_bin.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
                              _VP, ctypes.c_size_t, ctypes.c_size_t, _VP, _VP, _VP,
                              ctypes.POINTER(ctypes.c_size_t), _VP]
+        L.rs_bin_async.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
+                                   _VP, ctypes.c_size_t, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP]
         L.rs_bin_noalloc.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
                                      ctypes.c_size_t, _VP, _VP, _VP, ctypes.POINTER(ctypes.c_size_t), _VP]
         L.rs_rasterize_fwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected),
@@ -290,6 +292,23 @@ def rs_bin(camera, proj: DeviceProjected, n: int, workspace: torch.Tensor, capac
         raise err
     _check("rs_bin", rc)
     return int(E.value)
+
+
+def rs_bin_async(camera, proj: DeviceProjected, n: int, workspace: torch.Tensor, capacity: int,
+                 keys_sorted, point_list: torch.Tensor, tile_ranges: torch.Tensor, result: torch.Tensor,
+                 stream=None):
+    """rs_bin without the host wait: enqueues the binning and a copy of (E, error flag) into
+    `result` (int64 [2], pinned host memory); read it after synchronising the stream."""
+    if result.is_cuda or result.dtype != torch.int64 or result.numel() < 2 or not result.is_contiguous():
+        raise TypeError("result must be a contiguous int64 host tensor with 2 elements (pinned)")
+    c = camera_struct(camera)
+    p = proj.struct()
+    _check("rs_bin_async", lib().rs_bin_async(
+        ctypes.byref(c), ctypes.byref(p), int(n), _ptr(workspace, torch.uint8, None, "workspace"),
+        int(workspace.numel()), int(capacity), _ptr(keys_sorted, torch.int64, capacity, "keys_sorted"),
+        _ptr(point_list, torch.int32, capacity, "point_list"),
+        _ptr(tile_ranges, torch.int32, 2 * ((camera.width + 15) // 16) * ((camera.height + 15) // 16), "tile_ranges"),
+        ctypes.c_void_p(result.data_ptr()), _stream(stream)))
 
 
 def rs_bin_noalloc(camera, proj: DeviceProjected, n: int, capacity: int, keys_sorted,

@@ -136,6 +136,22 @@ int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d
            size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
            uint32_t* d_point_list, uint32_t* d_tile_ranges, size_t* n_entries, void* stream);
 
+/* Binning without waiting for the entry count (the sync-free pipeline: the host keeps
+ * enqueueing the rest of the frame while the GPU bins).  Same arguments, work and outputs as
+ * rs_bin, except that the entry count is not waited for: the call enqueues, on `stream`, a copy
+ * of two uint64 words into h_result -- h_result[0] = E, h_result[1] = nonzero if a bounded wait
+ * of the sort's look-back gave up -- and returns.  Read h_result only after the stream has
+ * reached that point (cudaStreamSynchronize or an event recorded after the call); use pinned
+ * host memory (cudaHostAlloc), else the copy blocks the host.  When E > capacity no entry is
+ * written and every tile range is (0, 0), so later calls on these buffers render the
+ * background and stay within bounds; the caller must then grow the buffers and redo the frame.
+ * The device-side result is part of the workspace, so work enqueued later on the stream may
+ * reuse the workspace only after that copy (stream order guarantees it).
+ * Errors (returned at once): RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CUDA. */
+int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
+                 size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
+                 uint32_t* d_point_list, uint32_t* d_tile_ranges, uint64_t* h_result, void* stream);
+
 /* [3] Forward compositing, rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel".
  * One thread block per 16x16 tile; each pixel walks its tile's list front to back:
  * power = -1/2 (A dx^2 + C dy^2) - B dx dy with (dx, dy) = (x - u, y - v),

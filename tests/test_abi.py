@@ -108,3 +108,16 @@ def test_appearance_and_loss_validation(L):
     assert L.rs_l1_loss_grad(10, ok, ok, ctypes.c_float(float("nan")), ok, None, None) == rs.RS_ERR_INVALID_ARG
     assert L.rs_l1_loss_grad(10, None, ok, ctypes.c_float(1.0), ok, None, None) == rs.RS_ERR_INVALID_ARG
     assert L.rs_l1_loss_grad(10, ok, ok, ctypes.c_float(1.0), ok, ctypes.c_void_p(0x2001), None) == rs.RS_ERR_INVALID_ARG
+
+
+def test_bin_async_validation(L):
+    cam = rs.camera_struct(scenes.procedural_camera(64, 48))
+    ok = ctypes.c_void_p(0x2000)
+    ws = ctypes.c_void_p(0x1000)
+    # the pinned result pointer is required and must be 8-byte aligned; checked before any launch
+    assert L.rs_bin_async(ctypes.byref(cam), None, 0, ws, 1 << 20, 0, None, None, ok, None, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_bin_async(ctypes.byref(cam), None, 0, ws, 1 << 20, 0, None, None, ok,
+                          ctypes.c_void_p(0x3004), None) == rs.RS_ERR_INVALID_ARG
+    # the workspace size is validated on the host as for rs_bin
+    assert L.rs_bin_async(ctypes.byref(cam), None, 0, ws, 16, 0, None, None, ok, ctypes.c_void_p(0x3008),
+                          None) == rs.RS_ERR_WORKSPACE

@@ -148,6 +148,43 @@ def test_capacity_overflow_then_retry_matches():
     assert np.array_equal(ref["point_list"], P.u32(R.point_list[:E]))
 
 
+def test_bin_async_matches_rs_bin_and_reports_overflow():
+    """rs_bin_async (no host wait) gives rs_bin's outputs and reports (E, 0) in pinned memory; on
+    overflow it writes no entry, leaves every range empty (the frame renders the background) and
+    reports the count, and the redone frame matches."""
+    g = scenes.procedural_scene(seed=1, n_sphere=20_000, n_helix=5_000, n_plane=5_000)
+    cam = scenes.procedural_camera(320, 240)
+    ref = P.run_gpu(g, cam)
+    dg = rs.DeviceGaussians.from_numpy(g)
+    res = torch.full((2,), -1, dtype=torch.int64).pin_memory()
+    R = pipeline.Renderer(cam, g.n, capacity=ref["n_entries"] + 10)
+    R.forward_async(dg, res)
+    torch.cuda.synchronize()
+    assert R.check_async(res) == ref["n_entries"] and int(res[1]) == 0
+    E = ref["n_entries"]
+    assert np.array_equal(P.u32(R.point_list[:E]), ref["point_list"])
+    assert np.array_equal(R.keys_sorted[:E].cpu().numpy().view(np.uint64), ref["keys"])
+    assert np.array_equal(P.u32(R.tile_ranges), ref["ranges"])
+    assert np.array_equal(R.image.cpu().numpy(), ref["image"])
+    # overflow: nothing written, ranges empty, background image, count reported
+    small = pipeline.Renderer(cam, g.n, capacity=E // 2)
+    small.point_list.fill_(-7)
+    small.forward_async(dg, res, bg=(0.25, 0.5, 0.75))
+    torch.cuda.synchronize()
+    assert int(res[0]) == E
+    assert not small.tile_ranges.any()
+    assert (small.point_list == -7).all()
+    img = small.image.cpu().numpy()
+    assert np.allclose(img[0], 0.25) and np.allclose(img[1], 0.5) and np.allclose(img[2], 0.75)
+    with pytest.raises(rs.RsError) as e:
+        small.check_async(res)
+    assert e.value.code == rs.RS_ERR_CAPACITY and small.capacity >= E
+    small.forward_async(dg, res)
+    torch.cuda.synchronize()
+    assert small.check_async(res) == E
+    assert np.array_equal(P.u32(small.point_list[:E]), ref["point_list"])
+
+
 def test_forward_is_deterministic():
     g = scenes.procedural_scene(seed=3, n_sphere=20_000, n_helix=5_000, n_plane=5_000)
     cam = scenes.procedural_camera(320, 240)
