@@ -31,8 +31,15 @@ namespace {
 
 constexpr int kRsThreads = 256;
 constexpr int kRsWarps = kRsThreads / 32;
-constexpr int kDepthItems = 8;                          // depth sort: 2048 keys per block
-constexpr int kTileItems = 16;                          // tile sort: 4096 keys per block
+// keys per thread of the sort passes (a block holds 256 x that many keys)
+#ifndef RS_DEPTH_ITEMS
+#define RS_DEPTH_ITEMS 8
+#endif
+#ifndef RS_TILE_ITEMS
+#define RS_TILE_ITEMS 16
+#endif
+constexpr int kDepthItems = RS_DEPTH_ITEMS;             // depth sort: 2048 keys per block
+constexpr int kTileItems = RS_TILE_ITEMS;               // tile sort: 4096 keys per block
 constexpr int kDepthHistItems = 2;                      // depth digit counts: 512 keys per block
 constexpr unsigned kFull = 0xffffffffu;
 
