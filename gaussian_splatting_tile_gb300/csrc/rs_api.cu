@@ -244,4 +244,28 @@ int rs_l1_loss_grad(size_t count, const float* d_image, const float* d_target, f
                                  static_cast<cudaStream_t>(stream)));
 }
 
+int rs_adam_step(const rs_adam_segment* segs, int32_t n_segs, double beta1, double beta2, double eps,
+                 int32_t step, void* stream) {
+    if (!segs || n_segs < 0 || n_segs > RS_ADAM_MAX_SEGMENTS || step < 1) return RS_ERR_INVALID_ARG;
+    if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0) || !(eps > 0.0) || !isfinite(eps))
+        return RS_ERR_INVALID_ARG;
+    for (int i = 0; i < n_segs; ++i) {
+        const rs_adam_segment& g = segs[i];
+        if (g.activation < RS_ACT_IDENTITY || g.activation > RS_ACT_SIGMOID || !isfinite(g.lr)) return RS_ERR_INVALID_ARG;
+        if (g.count == 0) continue;
+        if (!dev_f(g.d_param) || !dev_f(g.d_grad) || !dev_f(g.d_m) || !dev_f(g.d_v)) return RS_ERR_INVALID_ARG;
+        if (g.d_activated && !aligned(g.d_activated, 4)) return RS_ERR_INVALID_ARG;
+    }
+    return cuda_rc(rs::launch_adam(segs, n_segs, beta1, beta2, eps, step, static_cast<cudaStream_t>(stream)));
+}
+
+int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_radius, float* d_accum,
+                     float* d_count, void* stream) {
+    if (!n_ok(n)) return RS_ERR_INVALID_ARG;
+    if (n > 0 && (!dev_f(d_dL_dmeans2d) || !dev_f(d_radius) || !dev_f(d_accum) || !dev_f(d_count)))
+        return RS_ERR_INVALID_ARG;
+    return cuda_rc(rs::launch_densify_stats(n, d_dL_dmeans2d, d_radius, d_accum, d_count,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -148,4 +148,10 @@ cudaError_t launch_appearance_bwd(const CameraF& cam, int n, const float* means,
 cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float scale, float* dimg,
                       float* loss, cudaStream_t s);
 
+// Fused Adam over parameter groups and the densification statistics.
+cudaError_t launch_adam(const rs_adam_segment* segs, int n, double beta1, double beta2, double eps, int step,
+                        cudaStream_t s);
+cudaError_t launch_densify_stats(int n, const float* dm2, const int* radius, float* accum, float* count,
+                                 cudaStream_t s);
+
 }  // namespace rs

@@ -63,6 +63,15 @@ class rs_mlp_grads(ctypes.Structure):
                 ("d_dW2", ctypes.c_void_p), ("d_db2", ctypes.c_void_p)]
 
 
+class rs_adam_segment(ctypes.Structure):
+    _fields_ = [("d_param", ctypes.c_void_p), ("d_grad", ctypes.c_void_p), ("d_m", ctypes.c_void_p),
+                ("d_v", ctypes.c_void_p), ("d_activated", ctypes.c_void_p), ("count", ctypes.c_size_t),
+                ("lr", ctypes.c_float), ("activation", ctypes.c_int32)]
+
+
+RS_ACT_IDENTITY, RS_ACT_EXP, RS_ACT_SIGMOID = 0, 1, 2
+RS_ADAM_MAX_SEGMENTS = 16
+
 _lib = None
 _VP = ctypes.c_void_p
 
@@ -108,6 +117,9 @@ def lib():
         L.rs_appearance_bwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.c_int32, _VP, _VP,
                                         ctypes.POINTER(rs_mlp), _VP, _VP, ctypes.POINTER(rs_mlp_grads), _VP]
         L.rs_l1_loss_grad.argtypes = [ctypes.c_size_t, _VP, _VP, ctypes.c_float, _VP, _VP, _VP]
+        L.rs_adam_step.argtypes = [ctypes.POINTER(rs_adam_segment), ctypes.c_int32, ctypes.c_double,
+                                   ctypes.c_double, ctypes.c_double, ctypes.c_int32, _VP]
+        L.rs_densify_stats.argtypes = [ctypes.c_int32, _VP, _VP, _VP, _VP, _VP]
         for name in declared_symbols():
             getattr(L, name).restype = ctypes.c_char_p if name == "rs_error_string" else ctypes.c_int
         _lib = L
@@ -466,3 +478,44 @@ def rs_l1_loss_grad(image: torch.Tensor, target: torch.Tensor, scale: float, dL_
         count, _ptr(image, torch.float32, count, "image"), _ptr(target, torch.float32, count, "target"),
         ctypes.c_float(scale), _ptr(dL_dimage, torch.float32, count, "dL_dimage"),
         _ptr(loss, torch.float32, 1, "loss"), _stream(stream)))
+
+
+# ------------------------------------------------------------------ optimiser
+
+@dataclasses.dataclass
+class AdamGroup:
+    """One parameter group of rs_adam_step: float32 CUDA tensors of equal size."""
+    param: torch.Tensor
+    grad: torch.Tensor
+    m: torch.Tensor
+    v: torch.Tensor
+    lr: float
+    activation: int = RS_ACT_IDENTITY
+    activated: torch.Tensor | None = None
+
+
+def rs_adam_step(groups, step: int, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-15,
+                 stream=None):
+    if len(groups) > RS_ADAM_MAX_SEGMENTS:
+        raise ValueError(f"at most {RS_ADAM_MAX_SEGMENTS} groups per call")
+    arr = (rs_adam_segment * max(1, len(groups)))()
+    for i, gr in enumerate(groups):
+        k = int(gr.param.numel())
+        arr[i].d_param = _ptr(gr.param, torch.float32, k, "param")
+        arr[i].d_grad = _ptr(gr.grad, torch.float32, k, "grad")
+        arr[i].d_m = _ptr(gr.m, torch.float32, k, "m")
+        arr[i].d_v = _ptr(gr.v, torch.float32, k, "v")
+        arr[i].d_activated = _ptr(gr.activated, torch.float32, k, "activated")
+        arr[i].count = k
+        arr[i].lr = float(gr.lr)
+        arr[i].activation = int(gr.activation)
+    _check("rs_adam_step", lib().rs_adam_step(arr, len(groups), float(beta1), float(beta2), float(eps), int(step),
+                                              _stream(stream)))
+
+
+def rs_densify_stats(dL_dmeans2d: torch.Tensor, radius: torch.Tensor, accum: torch.Tensor, count: torch.Tensor,
+                     stream=None):
+    n = int(radius.numel())
+    _check("rs_densify_stats", lib().rs_densify_stats(
+        n, _ptr(dL_dmeans2d, torch.float32, 2 * n, "dL_dmeans2d"), _ptr(radius, torch.int32, n, "radius"),
+        _ptr(accum, torch.float32, n, "accum"), _ptr(count, torch.float32, n, "count"), _stream(stream)))

@@ -248,6 +248,47 @@ int rs_appearance_bwd(const rs_camera* camera, int32_t n, const float* d_means,
 int rs_l1_loss_grad(size_t count, const float* d_image, const float* d_target, float scale,
                     float* d_dL_dimage, float* d_loss, void* stream);
 
+/* Optimiser step and densification statistics of the training loop (rigel README: the
+ * optimisation loop; "GaussianModel: activations, densify/prune"; per-group learning rates --
+ * its higher-order SH rate is a twentieth of the DC rate).  The pages give no device interface
+ * for these; this one follows the conventions above. */
+
+#define RS_ACT_IDENTITY 0   /* the parameter is used as it is                                */
+#define RS_ACT_EXP 1        /* the parameter is a log (e.g. log-scales): used as exp(param)   */
+#define RS_ACT_SIGMOID 2    /* the parameter is a logit (opacity): used as sigmoid(param)     */
+#define RS_ADAM_MAX_SEGMENTS 16
+
+/* One parameter group: `count` float32 device values updated in place with their Adam moments.
+ * d_grad is the gradient w.r.t. the value the renderer uses, act(param); the step applies the
+ * activation's derivative itself.  d_activated (may be NULL) receives act(param) after the step,
+ * e.g. the scales or opacities rs_project reads. */
+typedef struct rs_adam_segment {
+    float* d_param;
+    const float* d_grad;
+    float* d_m;
+    float* d_v;
+    float* d_activated;
+    size_t count;
+    float lr;
+    int32_t activation;   /* RS_ACT_* */
+} rs_adam_segment;
+
+/* Adam (Kingma & Ba) over up to RS_ADAM_MAX_SEGMENTS groups in one launch, step >= 1:
+ *   g = dL/dact * act'(param); m = b1 m + (1 - b1) g; v = b2 v + (1 - b2) g^2;
+ *   param -= lr * (m / (1 - b1^step)) / (sqrt(v / (1 - b2^step)) + eps).
+ * `segs` is a host array; segments must not overlap.  beta1, beta2 and eps are taken in double:
+ * 1 - beta is formed before rounding to float32 (0.999 has no float32 value close enough for
+ * 1 - 0.999 to keep more than 4 digits).  Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_adam_step(const rs_adam_segment* segs, int32_t n_segs, double beta1, double beta2, double eps,
+                 int32_t step, void* stream);
+
+/* Densification statistics (rigel README, "densify/prune" driven by the view-space gradient):
+ * for every Gaussian with radius > 0 in this view, d_accum[i] += |dL/dmeans2d_i| (Euclidean norm
+ * of d_dL_dmeans2d [2][n]) and d_count[i] += 1; others are left unchanged.  Errors:
+ * RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_radius, float* d_accum,
+                     float* d_count, void* stream);
+
 /* Allocation-free variant of rs_bin.  The source pages have no counterpart: this entry point
  * exists for callers of this library that cannot allocate device memory -- for example a plug-in
  * whose host application owns and budgets all device memory, or a per-frame loop that must not

@@ -265,6 +265,29 @@ def l1_loss_grad(image, target, scale):
     return grad.reshape(np.shape(image)), float(loss.value)
 
 
+def adam_step(param, grad, m, v, lr, activation=0, beta1=0.9, beta2=0.999, eps=1e-15, step=1):
+    """One Adam step on float64 copies; returns (param, m, v, activated)."""
+    p, g, mm, vv = (np.array(_d(a), copy=True).reshape(-1) for a in (param, grad, m, v))
+    act = np.zeros_like(p)
+    rc = lib().orc_adam_step(ctypes.c_int64(p.size), _p(p), _p(g), _p(mm), _p(vv), _p(act),
+                             ctypes.c_double(lr), ctypes.c_int32(activation), ctypes.c_double(beta1),
+                             ctypes.c_double(beta2), ctypes.c_double(eps), ctypes.c_int32(step))
+    if rc != 0:
+        raise ValueError(f"orc_adam_step returned {rc}")
+    return p, mm, vv, act
+
+
+def densify_stats(dmeans2d, radius, accum, count):
+    d2 = _d(dmeans2d)
+    n = d2.shape[1]
+    a, c = np.array(_d(accum), copy=True), np.array(_d(count), copy=True)
+    r = np.ascontiguousarray(radius, np.int32)
+    rc = lib().orc_densify_stats(ctypes.c_int32(n), _p(d2), _p(r), _p(a), _p(c))
+    if rc != 0:
+        raise ValueError(f"orc_densify_stats returned {rc}")
+    return a, c
+
+
 def render(cam, g, bg=(0.0, 0.0, 0.0), prec: int = 64):
     """Convenience: oracle project (decisions in `prec`) -> bin -> forward compositing."""
     P = project(cam, g, prec=prec)

@@ -909,4 +909,47 @@ int orc_l1_loss_grad(int64_t count, const double* image, const double* target, d
     return 0;
 }
 
+
+// c9: Adam (Kingma & Ba, "Adam: A Method for Stochastic Optimization", Algorithm 1) with the
+// bias corrections written as in the paper, one parameter at a time; the gradient of the raw
+// parameter is the given gradient times the activation's derivative (rigel README: parameters
+// are stored raw and activated in the model layer).
+int orc_adam_step(int64_t count, double* param, const double* grad, double* m, double* v,
+                  double* activated, double lr, int32_t activation, double beta1, double beta2,
+                  double eps, int32_t step) {
+    if (count < 0 || step < 1 || activation < 0 || activation > 2) return -1;
+    const double c1 = 1.0 - std::pow(beta1, step), c2 = 1.0 - std::pow(beta2, step);
+    for (int64_t i = 0; i < count; ++i) {
+        double g = grad[i];
+        if (activation == 1) g *= std::exp(param[i]);
+        if (activation == 2) {
+            const double a = 1.0 / (1.0 + std::exp(-param[i]));
+            g *= a * (1.0 - a);
+        }
+        m[i] = beta1 * m[i] + (1.0 - beta1) * g;
+        v[i] = beta2 * v[i] + (1.0 - beta2) * g * g;
+        const double mhat = m[i] / c1, vhat = v[i] / c2;
+        param[i] -= lr * mhat / (std::sqrt(vhat) + eps);
+        if (activated) {
+            activated[i] = activation == 1 ? std::exp(param[i])
+                         : activation == 2 ? 1.0 / (1.0 + std::exp(-param[i])) : param[i];
+        }
+    }
+    return 0;
+}
+
+// c10: the view-space gradient statistics that drive densification (rigel README,
+// "densify/prune"): norm of dL/dmeans2d accumulated over the views where the Gaussian is visible.
+int orc_densify_stats(int32_t n, const double* dmeans2d, const int32_t* radius, double* accum,
+                      double* count) {
+    if (n < 0) return -1;
+    for (int32_t i = 0; i < n; ++i) {
+        if (radius[i] <= 0) continue;
+        const double gx = dmeans2d[i], gy = dmeans2d[size_t(n) + i];
+        accum[i] += std::sqrt(gx * gx + gy * gy);
+        count[i] += 1.0;
+    }
+    return 0;
+}
+
 }  // extern "C"

@@ -123,6 +123,15 @@ int orc_appearance_bwd(const orc_camera* cam, int32_t n, int32_t L, int32_t H,
 int orc_l1_loss_grad(int64_t count, const double* image, const double* target, double scale,
                      double* grad, double* loss);
 
+/* c9: Adam step over one parameter group (in place), gradient given w.r.t. act(param);
+ * activation 0 identity, 1 exp, 2 sigmoid; activated (may be NULL) receives act(param). */
+int orc_adam_step(int64_t count, double* param, const double* grad, double* m, double* v,
+                  double* activated, double lr, int32_t activation, double beta1, double beta2,
+                  double eps, int32_t step);
+/* c10: densification statistics: accum[i] += |dmeans2d_i|, count[i] += 1 where radius[i] > 0. */
+int orc_densify_stats(int32_t n, const double* dmeans2d, const int32_t* radius, double* accum,
+                      double* count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -121,3 +121,27 @@ def test_bin_async_validation(L):
     # the workspace size is validated on the host as for rs_bin
     assert L.rs_bin_async(ctypes.byref(cam), None, 0, ws, 16, 0, None, None, ok, ctypes.c_void_p(0x3008),
                           None) == rs.RS_ERR_WORKSPACE
+
+
+def test_adam_and_densify_validation(L):
+    ok = ctypes.c_void_p(0x2000)
+    seg = (rs.rs_adam_segment * 2)()
+    for s in seg:
+        s.d_param = s.d_grad = s.d_m = s.d_v = ok
+        s.count, s.lr, s.activation = 10, 0.01, 0
+    f = ctypes.c_double
+    assert L.rs_adam_step(seg, 2, f(0.9), f(0.999), f(1e-15), 0, None) == rs.RS_ERR_INVALID_ARG  # step < 1
+    assert L.rs_adam_step(seg, 2, f(1.0), f(0.999), f(1e-15), 1, None) == rs.RS_ERR_INVALID_ARG  # beta1 = 1
+    assert L.rs_adam_step(seg, 2, f(0.9), f(0.999), f(0.0), 1, None) == rs.RS_ERR_INVALID_ARG    # eps = 0
+    assert L.rs_adam_step(seg, 17, f(0.9), f(0.999), f(1e-15), 1, None) == rs.RS_ERR_INVALID_ARG
+    seg[1].activation = 3
+    assert L.rs_adam_step(seg, 2, f(0.9), f(0.999), f(1e-15), 1, None) == rs.RS_ERR_INVALID_ARG
+    seg[1].activation = 1
+    seg[1].d_v = None
+    assert L.rs_adam_step(seg, 2, f(0.9), f(0.999), f(1e-15), 1, None) == rs.RS_ERR_INVALID_ARG
+    seg[1].count = 0  # empty groups need no buffers
+    seg[0].count = 0
+    assert L.rs_adam_step(seg, 2, f(0.9), f(0.999), f(1e-15), 1, None) == rs.RS_OK
+    assert L.rs_densify_stats(-1, ok, ok, ok, ok, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_densify_stats(5, None, ok, ok, ok, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_densify_stats(0, None, None, None, None, None) == rs.RS_OK
