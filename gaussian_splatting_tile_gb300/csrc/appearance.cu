@@ -502,4 +502,196 @@ cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float sc
     return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------- L1 + D-SSIM loss
+// 3DGS's photometric loss, which rigel trains with ("L1 + D-SSIM"):
+//   L = (1 - lambda) mean|I - T| + lambda (1 - mean SSIM(I, T)),
+// SSIM per channel and pixel with an 11x11 Gaussian window (sigma 1.5, the separable weights
+// normalised over the window, zeros outside the image), C1 = 0.01^2, C2 = 0.03^2:
+//   S = (2 mx my + C1)(2 sxy + C2) / ((mx^2 + my^2 + C1)(sx^2 + sy^2 + C2)),
+// with mx = G*I, sx^2 = G*I^2 - mx^2, sxy = G*(I T) - mx my.  Its gradient w.r.t. I is the window's
+// adjoint (the same symmetric window) applied to dS/dmx, dS/d(G*I^2), dS/d(G*IT):
+//   dS_sum/dI_q = (G*a)_q + 2 I_q (G*b)_q + T_q (G*c)_q,
+//   a = S (2my/A1 - 2my/A2 - 2mx/B1 + 2mx/B2), b = -S/B2, c = 2S/A2,
+// A1 = 2 mx my + C1, A2 = 2 sxy + C2, B1 = mx^2 + my^2 + C1, B2 = sx^2 + sy^2 + C2.
+// Two kernels over 16x16 output tiles with a 5-pixel halo staged in shared memory: the first
+// forms the five filtered maps (separably), S, the loss sums and a, b, c; the second filters
+// a, b, c and writes the gradient.
+namespace {
+
+constexpr int kSsimTile = 16;
+constexpr int kSsimR = 5;
+constexpr int kSsimP = kSsimTile + 2 * kSsimR;  // staged patch edge: 26
+
+struct SsimWindow {
+    float w[2 * kSsimR + 1];  // normalised 1-D Gaussian, sigma 1.5
+};
+
+__device__ __forceinline__ float patch_at(const float* __restrict__ img, int H, int W, int y, int x) {
+    return (y >= 0 && y < H && x >= 0 && x < W) ? img[size_t(y) * W + x] : 0.f;
+}
+
+__global__ void __launch_bounds__(256) k_ssim_fwd(SsimWindow win, int C, int H, int W,
+                                                  const float* __restrict__ img, const float* __restrict__ tgt,
+                                                  float* __restrict__ abc, float* __restrict__ sums) {
+    __shared__ float s_x[kSsimP][kSsimP], s_y[kSsimP][kSsimP];
+    __shared__ float s_h[5][kSsimP][kSsimTile];  // horizontally filtered x, y, xx, yy, xy
+    __shared__ float s_red[2][8];
+    const int TXn = (W + kSsimTile - 1) / kSsimTile;
+    const int tile = blockIdx.x, ch = blockIdx.y;
+    const int x0 = (tile % TXn) * kSsimTile - kSsimR, y0 = (tile / TXn) * kSsimTile - kSsimR;
+    const size_t plane = size_t(H) * W;
+    const float* X = img + ch * plane;
+    const float* Y = tgt + ch * plane;
+    for (int i = threadIdx.x; i < kSsimP * kSsimP; i += 256) {
+        const int py = i / kSsimP, px = i % kSsimP;
+        s_x[py][px] = patch_at(X, H, W, y0 + py, x0 + px);
+        s_y[py][px] = patch_at(Y, H, W, y0 + py, x0 + px);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kSsimP * kSsimTile; i += 256) {
+        const int py = i / kSsimTile, px = i % kSsimTile;
+        float h[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k <= 2 * kSsimR; ++k) {
+            const float w = win.w[k], a = s_x[py][px + k], b = s_y[py][px + k];
+            h[0] = fmaf(w, a, h[0]);
+            h[1] = fmaf(w, b, h[1]);
+            h[2] = fmaf(w, a * a, h[2]);
+            h[3] = fmaf(w, b * b, h[3]);
+            h[4] = fmaf(w, a * b, h[4]);
+        }
+#pragma unroll
+        for (int q = 0; q < 5; ++q) s_h[q][py][px] = h[q];
+    }
+    __syncthreads();
+    const int ty = threadIdx.x / kSsimTile, tx = threadIdx.x % kSsimTile;
+    const int gy = y0 + kSsimR + ty, gx = x0 + kSsimR + tx;
+    float ssim = 0.f, l1 = 0.f;
+    if (gy < H && gx < W) {
+        float v[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k <= 2 * kSsimR; ++k) {
+            const float w = win.w[k];
+#pragma unroll
+            for (int q = 0; q < 5; ++q) v[q] = fmaf(w, s_h[q][ty + k][tx], v[q]);
+        }
+        constexpr float C1 = 0.01f * 0.01f, C2 = 0.03f * 0.03f;
+        const float mx = v[0], my = v[1];
+        const float sxx = v[2] - mx * mx, syy = v[3] - my * my, sxy = v[4] - mx * my;
+        const float A1 = 2.f * mx * my + C1, A2 = 2.f * sxy + C2;
+        const float B1 = mx * mx + my * my + C1, B2 = sxx + syy + C2;
+        const float S = (A1 * A2) / (B1 * B2);
+        ssim = S;
+        l1 = fabsf(s_x[ty + kSsimR][tx + kSsimR] - s_y[ty + kSsimR][tx + kSsimR]);
+        const size_t o = ch * plane + size_t(gy) * W + gx;
+        const size_t N = size_t(C) * plane;
+        abc[o] = S * (2.f * my / A1 - 2.f * my / A2 - 2.f * mx / B1 + 2.f * mx / B2);
+        abc[N + o] = -S / B2;
+        abc[2 * N + o] = 2.f * S / A2;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ssim += __shfl_xor_sync(kFull, ssim, o);
+        l1 += __shfl_xor_sync(kFull, l1, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_red[0][threadIdx.x >> 5] = ssim;
+        s_red[1][threadIdx.x >> 5] = l1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = 0.f, b = 0.f;
+        for (int w = 0; w < 8; ++w) {
+            a += s_red[0][w];
+            b += s_red[1][w];
+        }
+        atomicAdd(sums, a);
+        atomicAdd(sums + 1, b);
+    }
+}
+
+// dL/dI = scale (1 - lambda) sign(I - T) / N - scale lambda / N (G*a + 2 I G*b + T G*c); the
+// loss scale ((1 - lambda) sum|I - T| + lambda (N - sum S)) / N goes to *loss.
+__global__ void __launch_bounds__(256) k_ssim_bwd(SsimWindow win, int C, int H, int W,
+                                                  const float* __restrict__ img, const float* __restrict__ tgt,
+                                                  const float* __restrict__ abc, float lambda, float scale,
+                                                  float* __restrict__ dimg) {
+    __shared__ float s_in[3][kSsimP][kSsimP];
+    __shared__ float s_h[3][kSsimP][kSsimTile];
+    const int TXn = (W + kSsimTile - 1) / kSsimTile;
+    const int tile = blockIdx.x, ch = blockIdx.y;
+    const int x0 = (tile % TXn) * kSsimTile - kSsimR, y0 = (tile / TXn) * kSsimTile - kSsimR;
+    const size_t plane = size_t(H) * W;
+    const size_t N = size_t(C) * plane;
+    for (int i = threadIdx.x; i < kSsimP * kSsimP; i += 256) {
+        const int py = i / kSsimP, px = i % kSsimP;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) s_in[q][py][px] = patch_at(abc + q * N + ch * plane, H, W, y0 + py, x0 + px);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kSsimP * kSsimTile; i += 256) {
+        const int py = i / kSsimTile, px = i % kSsimTile;
+        float h[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k <= 2 * kSsimR; ++k) {
+            const float w = win.w[k];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) h[q] = fmaf(w, s_in[q][py][px + k], h[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) s_h[q][py][px] = h[q];
+    }
+    __syncthreads();
+    const int ty = threadIdx.x / kSsimTile, tx = threadIdx.x % kSsimTile;
+    const int gy = y0 + kSsimR + ty, gx = x0 + kSsimR + tx;
+    if (gy >= H || gx >= W) return;
+    float g[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k <= 2 * kSsimR; ++k) {
+        const float w = win.w[k];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) g[q] = fmaf(w, s_h[q][ty + k][tx], g[q]);
+    }
+    const size_t o = ch * plane + size_t(gy) * W + gx;
+    const float x = img[o], y = tgt[o];
+    const float d = x - y;
+    const float sgn = d > 0.f ? 1.f : (d < 0.f ? -1.f : 0.f);
+    const float dS = fmaf(2.f * x, g[1], fmaf(y, g[2], g[0]));
+    const float inv = scale / float(N);
+    dimg[o] = inv * ((1.f - lambda) * sgn - lambda * dS);
+}
+
+__global__ void k_ssim_loss(const float* __restrict__ sums, size_t N, float lambda, float scale, float* loss) {
+    // sums[0] = sum S, sums[1] = sum |I - T|
+    *loss = scale * ((1.f - lambda) * sums[1] + lambda * (float(N) - sums[0])) / float(N);
+}
+
+}  // namespace
+
+size_t ssim_workspace_bytes(int C, int H, int W) {
+    return 3 * size_t(C) * H * W * sizeof(float) + 256;
+}
+
+cudaError_t launch_l1_dssim(int C, int H, int W, const float* img, const float* tgt, float lambda, float scale,
+                            float* dimg, float* loss, void* ws, cudaStream_t s) {
+    SsimWindow win;
+    double t[2 * kSsimR + 1], sum = 0.0;
+    for (int i = 0; i <= 2 * kSsimR; ++i) {
+        t[i] = std::exp(-double((i - kSsimR) * (i - kSsimR)) / (2.0 * 1.5 * 1.5));
+        sum += t[i];
+    }
+    for (int i = 0; i <= 2 * kSsimR; ++i) win.w[i] = float(t[i] / sum);
+    float* abc = static_cast<float*>(ws);
+    float* sums = reinterpret_cast<float*>(static_cast<char*>(ws) + 3 * size_t(C) * H * W * sizeof(float));
+    cudaError_t e = cudaMemsetAsync(sums, 0, 2 * sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((W + kSsimTile - 1) / kSsimTile) * ((H + kSsimTile - 1) / kSsimTile);
+    const dim3 grid{unsigned(tiles), unsigned(C), 1u};
+    k_ssim_fwd<<<grid, 256, 0, s>>>(win, C, H, W, img, tgt, abc, sums);
+    k_ssim_bwd<<<grid, 256, 0, s>>>(win, C, H, W, img, tgt, abc, lambda, scale, dimg);
+    if (loss) k_ssim_loss<<<1, 1, 0, s>>>(sums, size_t(C) * H * W, lambda, scale, loss);
+    return cudaGetLastError();
+}
+
 }  // namespace rs

@@ -268,4 +268,25 @@ int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_rad
                                             static_cast<cudaStream_t>(stream)));
 }
 
+int rs_l1_dssim_workspace_size(int32_t channels, int32_t height, int32_t width, size_t* bytes) {
+    if (channels < 1 || height < 1 || width < 1 || height > 32768 || width > 32768 || channels > 64 || !bytes)
+        return RS_ERR_INVALID_ARG;
+    *bytes = rs::ssim_workspace_bytes(channels, height, width);
+    return RS_OK;
+}
+
+int rs_l1_dssim_loss_grad(int32_t channels, int32_t height, int32_t width, const float* d_image,
+                          const float* d_target, float lambda, float scale, float* d_dL_dimage,
+                          float* d_loss, void* d_workspace, size_t workspace_bytes, void* stream) {
+    size_t need = 0;
+    if (rs_l1_dssim_workspace_size(channels, height, width, &need) != RS_OK) return RS_ERR_INVALID_ARG;
+    if (!(lambda >= 0.f && lambda <= 1.f) || !isfinite(scale)) return RS_ERR_INVALID_ARG;
+    if (!dev_f(d_image) || !dev_f(d_target) || !dev_f(d_dL_dimage)) return RS_ERR_INVALID_ARG;
+    if (d_loss && !aligned(d_loss, 4)) return RS_ERR_INVALID_ARG;
+    if (!d_workspace || !aligned(d_workspace, 16)) return RS_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return RS_ERR_WORKSPACE;
+    return cuda_rc(rs::launch_l1_dssim(channels, height, width, d_image, d_target, lambda, scale, d_dL_dimage,
+                                       d_loss, d_workspace, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

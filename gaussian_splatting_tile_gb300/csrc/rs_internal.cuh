@@ -147,6 +147,10 @@ cudaError_t launch_appearance_bwd(const CameraF& cam, int n, const float* means,
                                   const rs_mlp_grads& gr, cudaStream_t s);
 cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float scale, float* dimg,
                       float* loss, cudaStream_t s);
+// L1 + D-SSIM loss and gradient; the workspace holds 3 C H W floats and two sums.
+size_t ssim_workspace_bytes(int C, int H, int W);
+cudaError_t launch_l1_dssim(int C, int H, int W, const float* img, const float* tgt, float lambda, float scale,
+                            float* dimg, float* loss, void* ws, cudaStream_t s);
 
 // Fused Adam over parameter groups and the densification statistics.
 cudaError_t launch_adam(const rs_adam_segment* segs, int n, double beta1, double beta2, double eps, int step,

@@ -120,6 +120,10 @@ def lib():
         L.rs_adam_step.argtypes = [ctypes.POINTER(rs_adam_segment), ctypes.c_int32, ctypes.c_double,
                                    ctypes.c_double, ctypes.c_double, ctypes.c_int32, _VP]
         L.rs_densify_stats.argtypes = [ctypes.c_int32, _VP, _VP, _VP, _VP, _VP]
+        L.rs_l1_dssim_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+        L.rs_l1_dssim_loss_grad.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _VP, _VP, ctypes.c_float,
+                                            ctypes.c_float, _VP, _VP, _VP, ctypes.c_size_t, _VP]
         for name in declared_symbols():
             getattr(L, name).restype = ctypes.c_char_p if name == "rs_error_string" else ctypes.c_int
         _lib = L
@@ -519,3 +523,23 @@ def rs_densify_stats(dL_dmeans2d: torch.Tensor, radius: torch.Tensor, accum: tor
     _check("rs_densify_stats", lib().rs_densify_stats(
         n, _ptr(dL_dmeans2d, torch.float32, 2 * n, "dL_dmeans2d"), _ptr(radius, torch.int32, n, "radius"),
         _ptr(accum, torch.float32, n, "accum"), _ptr(count, torch.float32, n, "count"), _stream(stream)))
+
+
+def rs_l1_dssim_workspace_size(channels: int, height: int, width: int) -> int:
+    b = ctypes.c_size_t(0)
+    _check("rs_l1_dssim_workspace_size", lib().rs_l1_dssim_workspace_size(int(channels), int(height), int(width),
+                                                                          ctypes.byref(b)))
+    return int(b.value)
+
+
+def rs_l1_dssim_loss_grad(image: torch.Tensor, target: torch.Tensor, lam: float, scale: float,
+                          dL_dimage: torch.Tensor, loss: torch.Tensor | None, workspace: torch.Tensor, stream=None):
+    """image, target, dL_dimage: float32 CUDA [C, H, W]; workspace: uint8 CUDA tensor of at least
+    rs_l1_dssim_workspace_size bytes."""
+    C, H, W = (int(x) for x in image.shape)
+    n = C * H * W
+    _check("rs_l1_dssim_loss_grad", lib().rs_l1_dssim_loss_grad(
+        C, H, W, _ptr(image, torch.float32, n, "image"), _ptr(target, torch.float32, n, "target"),
+        ctypes.c_float(lam), ctypes.c_float(scale), _ptr(dL_dimage, torch.float32, n, "dL_dimage"),
+        _ptr(loss, torch.float32, 1, "loss"), _ptr(workspace, torch.uint8, None, "workspace"),
+        int(workspace.numel()), _stream(stream)))

@@ -248,6 +248,20 @@ int rs_appearance_bwd(const rs_camera* camera, int32_t n, const float* d_means,
 int rs_l1_loss_grad(size_t count, const float* d_image, const float* d_target, float scale,
                     float* d_dL_dimage, float* d_loss, void* stream);
 
+/* L1 + D-SSIM loss, the photometric loss rigel trains with (README: "L1 + D-SSIM"; the pages
+ * give no formula, so this is 3DGS's): over C channels of H x W images,
+ *   L = (1 - lambda) mean |I - T| + lambda (1 - mean SSIM(I, T)),
+ * SSIM per channel and pixel with an 11 x 11 Gaussian window (sigma 1.5, separable weights
+ * normalised over the window, zeros outside the image), C1 = 0.01^2, C2 = 0.03^2; means over all
+ * C H W values.  Writes d_dL_dimage = scale * dL/dI [C][H][W] and, when d_loss is not NULL,
+ * *d_loss = scale * L (one device float; accumulation order not fixed).  d_workspace: at least
+ * rs_l1_dssim_workspace_size bytes, 16-byte aligned, contents undefined on entry and exit.
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CUDA. */
+int rs_l1_dssim_workspace_size(int32_t channels, int32_t height, int32_t width, size_t* bytes);
+int rs_l1_dssim_loss_grad(int32_t channels, int32_t height, int32_t width, const float* d_image,
+                          const float* d_target, float lambda, float scale, float* d_dL_dimage,
+                          float* d_loss, void* d_workspace, size_t workspace_bytes, void* stream);
+
 /* Optimiser step and densification statistics of the training loop (rigel README: the
  * optimisation loop; "GaussianModel: activations, densify/prune"; per-group learning rates --
  * its higher-order SH rate is a twentieth of the DC rate).  The pages give no device interface

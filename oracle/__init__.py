@@ -288,6 +288,23 @@ def densify_stats(dmeans2d, radius, accum, count):
     return a, c
 
 
+def l1_dssim(image, target, lam=0.2, scale=1.0):
+    """L1 + D-SSIM over [C,H,W] images: (grad [C,H,W], loss, ssim map [C,H,W])."""
+    img = _d(image)
+    tgt = _d(target)
+    if img.ndim == 2:
+        img, tgt = img[None], tgt[None]
+    C, H, W = img.shape
+    grad = np.zeros_like(img)
+    smap = np.zeros_like(img)
+    loss = ctypes.c_double(0.0)
+    rc = lib().orc_l1_dssim(ctypes.c_int32(C), ctypes.c_int32(H), ctypes.c_int32(W), _p(img), _p(tgt),
+                            ctypes.c_double(lam), ctypes.c_double(scale), _p(grad), ctypes.byref(loss), _p(smap))
+    if rc != 0:
+        raise ValueError(f"orc_l1_dssim returned {rc}")
+    return grad, float(loss.value), smap
+
+
 def render(cam, g, bg=(0.0, 0.0, 0.0), prec: int = 64):
     """Convenience: oracle project (decisions in `prec`) -> bin -> forward compositing."""
     P = project(cam, g, prec=prec)

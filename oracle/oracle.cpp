@@ -952,4 +952,77 @@ int orc_densify_stats(int32_t n, const double* dmeans2d, const int32_t* radius, 
     return 0;
 }
 
+
+// c11: L1 + D-SSIM, the photometric loss rigel's training uses ("L1 + D-SSIM"; the pages give no
+// formula, so 3DGS's, after Wang et al., "Image quality assessment: from error visibility to
+// structural similarity"): local means, variances and covariance under a normalised 11 x 11
+// Gaussian window (sigma 1.5; pixels outside the image count as zero), SSIM per pixel, averaged.
+// The window is applied directly in 2-D.  The gradient follows the chain rule through the five
+// filtered maps: S depends on the pixel values only through mx = G*I, sxx' = G*I^2 and
+// sxy' = G*(I T), whose derivatives w.r.t. I_q are G(p - q), 2 I_q G(p - q) and T_q G(p - q).
+int orc_l1_dssim(int32_t C, int32_t H, int32_t W, const double* image, const double* target,
+                 double lambda, double scale, double* grad, double* loss, double* ssim) {
+    if (C < 1 || H < 1 || W < 1) return -1;
+    const int R = 5;
+    double G[11][11], sum = 0.0;
+    for (int i = 0; i < 11; ++i)
+        for (int j = 0; j < 11; ++j) {
+            G[i][j] = std::exp(-double((i - R) * (i - R) + (j - R) * (j - R)) / (2.0 * 1.5 * 1.5));
+            sum += G[i][j];
+        }
+    for (int i = 0; i < 11; ++i)
+        for (int j = 0; j < 11; ++j) G[i][j] /= sum;
+    const double C1 = 0.01 * 0.01, C2 = 0.03 * 0.03;
+    const size_t plane = size_t(H) * W, N = size_t(C) * plane;
+    std::vector<double> a(N), b(N), c(N);
+    double sum_s = 0.0, sum_l1 = 0.0;
+    for (int ch = 0; ch < C; ++ch) {
+        const double* X = image + ch * plane;
+        const double* Y = target + ch * plane;
+        for (int y = 0; y < H; ++y)
+            for (int x = 0; x < W; ++x) {
+                double mx = 0, my = 0, xx = 0, yy = 0, xy = 0;
+                for (int i = -R; i <= R; ++i)
+                    for (int j = -R; j <= R; ++j) {
+                        const int yy_ = y + i, xx_ = x + j;
+                        if (yy_ < 0 || yy_ >= H || xx_ < 0 || xx_ >= W) continue;
+                        const double w = G[i + R][j + R];
+                        const double u = X[size_t(yy_) * W + xx_], v = Y[size_t(yy_) * W + xx_];
+                        mx += w * u; my += w * v; xx += w * u * u; yy += w * v * v; xy += w * u * v;
+                    }
+                const double sx = xx - mx * mx, sy = yy - my * my, sxy = xy - mx * my;
+                const double A1 = 2 * mx * my + C1, A2 = 2 * sxy + C2;
+                const double B1 = mx * mx + my * my + C1, B2 = sx + sy + C2;
+                const double S = A1 * A2 / (B1 * B2);
+                const size_t o = ch * plane + size_t(y) * W + x;
+                if (ssim) ssim[o] = S;
+                sum_s += S;
+                sum_l1 += std::fabs(X[size_t(y) * W + x] - Y[size_t(y) * W + x]);
+                // dS/dmx, dS/d(G*I^2), dS/d(G*I T)
+                a[o] = S * (2 * my / A1 - 2 * my / A2 - 2 * mx / B1 + 2 * mx / B2);
+                b[o] = -S / B2;
+                c[o] = 2 * S / A2;
+            }
+    }
+    for (int ch = 0; ch < C; ++ch)
+        for (int y = 0; y < H; ++y)
+            for (int x = 0; x < W; ++x) {
+                const size_t q = ch * plane + size_t(y) * W + x;
+                const double u = image[q], v = target[q];
+                double dS = 0;
+                for (int i = -R; i <= R; ++i)
+                    for (int j = -R; j <= R; ++j) {
+                        const int py = y + i, px = x + j;  // pixel p whose window holds q
+                        if (py < 0 || py >= H || px < 0 || px >= W) continue;
+                        const size_t o = ch * plane + size_t(py) * W + px;
+                        dS += G[i + R][j + R] * (a[o] + 2 * u * b[o] + v * c[o]);
+                    }
+                const double d = u - v;
+                const double sgn = d > 0 ? 1.0 : (d < 0 ? -1.0 : 0.0);
+                grad[q] = scale * ((1 - lambda) * sgn - lambda * dS) / double(N);
+            }
+    if (loss) *loss = scale * ((1 - lambda) * sum_l1 + lambda * (double(N) - sum_s)) / double(N);
+    return 0;
+}
+
 }  // extern "C"

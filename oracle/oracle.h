@@ -132,6 +132,13 @@ int orc_adam_step(int64_t count, double* param, const double* grad, double* m, d
 int orc_densify_stats(int32_t n, const double* dmeans2d, const int32_t* radius, double* accum,
                       double* count);
 
+/* c11: L1 + D-SSIM loss (3DGS's photometric loss), C channels of H x W images:
+ * L = (1 - lambda) mean|I - T| + lambda (1 - mean SSIM), 11 x 11 Gaussian window (sigma 1.5,
+ * normalised), zeros outside the image, C1 = 0.01^2, C2 = 0.03^2.  grad = scale dL/dI,
+ * *loss = scale L; ssim (may be NULL) receives the per-pixel SSIM map. */
+int orc_l1_dssim(int32_t C, int32_t H, int32_t W, const double* image, const double* target,
+                 double lambda, double scale, double* grad, double* loss, double* ssim);
+
 #ifdef __cplusplus
 }
 #endif

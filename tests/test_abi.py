@@ -145,3 +145,14 @@ def test_adam_and_densify_validation(L):
     assert L.rs_densify_stats(-1, ok, ok, ok, ok, None) == rs.RS_ERR_INVALID_ARG
     assert L.rs_densify_stats(5, None, ok, ok, ok, None) == rs.RS_ERR_INVALID_ARG
     assert L.rs_densify_stats(0, None, None, None, None, None) == rs.RS_OK
+
+
+def test_l1_dssim_validation(L):
+    ok = ctypes.c_void_p(0x2000)
+    b = ctypes.c_size_t(0)
+    assert L.rs_l1_dssim_workspace_size(0, 4, 4, ctypes.byref(b)) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_l1_dssim_workspace_size(3, 4, 4, ctypes.byref(b)) == rs.RS_OK and b.value >= 3 * 3 * 16 * 4
+    f = ctypes.c_float
+    assert L.rs_l1_dssim_loss_grad(3, 4, 4, ok, ok, f(1.5), f(1.0), ok, None, ok, b.value, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_l1_dssim_loss_grad(3, 4, 4, ok, ok, f(0.2), f(1.0), ok, None, ok, 8, None) == rs.RS_ERR_WORKSPACE
+    assert L.rs_l1_dssim_loss_grad(3, 4, 4, ok, None, f(0.2), f(1.0), ok, None, ok, b.value, None) == rs.RS_ERR_INVALID_ARG

@@ -168,3 +168,27 @@ def test_training_shaped_step():
         for k in ("dW1", "db1", "dW2", "db2"):
             allclose_report(f"view {v} {k}", getattr(step.mlp_grads, k).cpu().numpy(), O[k], GRAD_RTOL, atol,
                             atol_of_max=frac)
+
+
+@pytest.mark.parametrize("shape,lam", [((3, 37, 53), 0.2), ((3, 400, 400), 0.2), ((1, 5, 3), 0.5), ((2, 16, 16), 1.0)])
+def test_l1_dssim_matches_oracle(shape, lam):
+    """L1 + D-SSIM: gradient |g - g_ref| <= 1e-3 |g_ref| + 1e-5 max|g_ref| (float32 window sums of
+    order one, the SSIM quotients and the 121-tap adjoint), loss rel 1e-5; two calls in a row on
+    the same workspace give the same result."""
+    rng = np.random.default_rng(sum(shape))
+    img = rng.uniform(0, 1, shape).astype(np.float32)
+    tgt = np.clip(img + 0.2 * rng.standard_normal(shape), 0, 1).astype(np.float32)
+    scale = 0.125
+    ws = torch.empty(rs.rs_l1_dssim_workspace_size(*shape), dtype=torch.uint8, device="cuda")
+    t = lambda a: torch.from_numpy(a).cuda()
+    out = []
+    for _ in range(2):
+        d = torch.full(shape, float("nan"), device="cuda")
+        loss = torch.full((1,), float("nan"), device="cuda")
+        rs.rs_l1_dssim_loss_grad(t(img), t(tgt), lam, scale, d, loss, ws)
+        torch.cuda.synchronize()
+        out.append((d.cpu().numpy(), float(loss.item())))
+    g_ref, l_ref, _ = oracle.l1_dssim(img, tgt, lam, scale)
+    for d, loss in out:
+        allclose_report("dL/dimage", d, g_ref, 1e-3, 1e-5 * float(np.abs(g_ref).max()))
+        assert abs(loss - l_ref) <= 1e-5 * abs(l_ref)
