@@ -443,15 +443,24 @@ __global__ void __launch_bounds__(kSlThreads) k_slices(CameraF cam, uint32_t n, 
     }
 }
 
-template <int RBITS>
+// Projected data the ellipse test reads (RS_TILE_TEST_ELLIPSE).
+struct EllipseSource {
+    const float* means2d;
+    const float* conic;
+    const float* alpha_k;
+    const int* radius;
+};
+
+template <int RBITS, bool ELL>
 __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n, Count count,
                                                        const uint32_t* __restrict__ perm, SliceOut sl,
                                                        int digit_bits, int passes, uint32_t* __restrict__ ghist,
                                                        uint32_t* __restrict__ tile_keys,
-                                                       uint32_t* __restrict__ vals) {
+                                                       uint32_t* __restrict__ vals, EllipseSource es) {
     constexpr int R = 1 << RBITS;
     __shared__ uint64_t s_start[kExpChunk + 1];
-    __shared__ uint2 s_rect[kExpChunk];
+    __shared__ uint2 s_rect[ELL ? 1 : kExpChunk];
+    __shared__ float s_e[ELL ? 7 : 1][ELL ? kExpChunk : 1];  // u, v, A, B, C, k, radius
     __shared__ uint32_t s_g[kExpChunk];
     __shared__ uint32_t s_h[3][R];
     const uint32_t E = count.get();
@@ -459,6 +468,7 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
     if (blockIdx.x >= chunks) return;
     for (int i = threadIdx.x; i < 3 * R; i += kExpThreads) (&s_h[0][0])[i] = 0u;
     const uint32_t lane = threadIdx.x & 31;
+    const uint32_t tiles_total = uint32_t(cam.TX) * uint32_t(cam.TY);
     for (uint32_t c = blockIdx.x; c < chunks; c += gridDim.x) {
         const uint32_t e0 = c * kExpChunk;
         // owners of the chunk's entries: depth positions i0 ..= i1.  Every Gaussian before the
@@ -472,8 +482,19 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
             const uint32_t i = i0 + uint32_t(j);
             s_start[j] = i < n ? sl.start[i] : uint64_t(0xffffffffffffffffull);
             if (j < w) {
-                s_rect[j] = sl.rect[i];
-                s_g[j] = perm[i];
+                const uint32_t g = perm[i];
+                s_g[j] = g;
+                if (ELL) {
+                    s_e[0][j] = es.means2d[g];
+                    s_e[1][j] = es.means2d[size_t(n) + g];
+                    s_e[2][j] = es.conic[g];
+                    s_e[3][j] = es.conic[size_t(n) + g];
+                    s_e[4][j] = es.conic[2 * size_t(n) + g];
+                    s_e[5][j] = es.alpha_k[g];
+                    s_e[6][j] = float(es.radius[g]);
+                } else {
+                    s_rect[j] = sl.rect[i];
+                }
             }
         }
         __syncthreads();
@@ -488,10 +509,32 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
                     const int mid = (lo + hi) >> 1;
                     if (s_start[mid] <= e) lo = mid; else hi = mid;
                 }
-                const uint2 r = s_rect[lo];
                 const uint32_t kk = uint32_t(uint64_t(e) - s_start[lo]);
-                const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
-                tile = ty * uint32_t(cam.TX) + tx;
+                if (ELL) {
+                    // the kk-th tile of the splat's rows of column runs
+                    EllipseTiles el;
+                    tile = tiles_total;  // unreachable for consistent inputs; k_ranges skips it
+                    const float u = s_e[0][lo], v = s_e[1][lo], r = s_e[6][lo];
+                    const int rect[4] = {span_bound(u, r, cam.TX, false), span_bound(u, r, cam.TX, true),
+                                         span_bound(v, r, cam.TY, false), span_bound(v, r, cam.TY, true)};
+                    if (ellipse_tiles_init(u, v, s_e[2][lo], s_e[3][lo], s_e[4][lo], s_e[5][lo], rect, cam.TY, el)) {
+                        uint32_t cum = 0u;
+                        for (int ty = el.ylo; ty <= el.yhi; ++ty) {
+                            int xlo, xhi;
+                            ellipse_row(el, ty, cam.TX, xlo, xhi);
+                            const uint32_t wd = xhi >= xlo ? uint32_t(xhi - xlo + 1) : 0u;
+                            if (kk < cum + wd) {
+                                tile = uint32_t(ty) * uint32_t(cam.TX) + uint32_t(xlo) + (kk - cum);
+                                break;
+                            }
+                            cum += wd;
+                        }
+                    }
+                } else {
+                    const uint2 r = s_rect[lo];
+                    const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
+                    tile = ty * uint32_t(cam.TX) + tx;
+                }
                 tile_keys[e] = tile;
                 vals[e] = s_g[lo];
             }
@@ -565,9 +608,13 @@ BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity) {
 
 template <int RBITS>
 void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* perm, const SliceOut& sl, int digit,
-                   int passes, uint32_t* ghist, uint32_t* tk, uint32_t* tv, cudaStream_t s) {
+                   int passes, uint32_t* ghist, uint32_t* tk, uint32_t* tv, const rs_projected& p, cudaStream_t s) {
     const unsigned blocks = unsigned(std::min<size_t>(sl.chunks, 152 * 8));
-    k_expand<RBITS><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
+    const EllipseSource es{p.d_means2d, p.d_conic, p.d_alpha_k, p.d_radius};
+    if (p.tile_test == RS_TILE_TEST_ELLIPSE)
+        k_expand<RBITS, true><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv, es);
+    else
+        k_expand<RBITS, false><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv, es);
 }
 
 cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_projected& p, uint8_t* ws,
@@ -629,10 +676,10 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
     const Count ce{0u, result, uint32_t(plan.capacity)};
     uint32_t* ghist_tile = reinterpret_cast<uint32_t*>(ws + plan.off_ghist_tile);
     switch (rbits) {
-        case 4: expand_launch<4>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
-        case 6: expand_launch<6>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
-        case 7: expand_launch<7>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
-        default: expand_launch<8>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], s); break;
+        case 4: expand_launch<4>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], p, s); break;
+        case 6: expand_launch<6>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], p, s); break;
+        case 7: expand_launch<7>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], p, s); break;
+        default: expand_launch<8>(cam, n, ce, perm, sl, digit, plan.tile_passes, ghist_tile, TK[cur], TV[cur], p, s); break;
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

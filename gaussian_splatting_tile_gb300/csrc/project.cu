@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
                                                  const float* __restrict__ sh,
                                                  const float* __restrict__ colors, float* means2d,
                                                  float* depth, float* conic, float* color,
-                                                 int* radius, uint32_t* tiles, Record* rec) {
+                                                 int* radius, uint32_t* tiles, Record* rec,
+                                                 int tile_test, float* alpha_k) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const size_t N = size_t(n);
@@ -235,15 +236,35 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
     const float s[3] = {__ldg(scales + i), __ldg(scales + N + i), __ldg(scales + 2 * N + i)};
     const float q[4] = {__ldg(quats + i), __ldg(quats + N + i), __ldg(quats + 2 * N + i),
                         __ldg(quats + 3 * N + i)};
+    const float o = __ldg(opacity + i);
     Geo G;
     geometry(cam, m, s, q, G);
-    if (!G.visible) {
+    uint32_t nt = 0;
+    float ak = 0.f;
+    if (G.visible) {
+        nt = uint32_t(G.rect[1] - G.rect[0]) * uint32_t(G.rect[3] - G.rect[2]);
+        if (tile_test == RS_TILE_TEST_ELLIPSE) {
+            // only the tiles the alpha >= 1/255 ellipse meets; none culls the splat
+            ak = alpha_k_of(o);
+            nt = 0;
+            EllipseTiles e;
+            if (ellipse_tiles_init(G.u, G.v, G.A, G.B, G.C, ak, G.rect, cam.TY, e)) {
+                for (int ty = e.ylo; ty <= e.yhi; ++ty) {
+                    int xlo, xhi;
+                    ellipse_row(e, ty, cam.TX, xlo, xhi);
+                    if (xhi >= xlo) nt += uint32_t(xhi - xlo + 1);
+                }
+            }
+        }
+    }
+    if (!G.visible || nt == 0) {
         means2d[i] = 0.f; means2d[N + i] = 0.f;
         depth[i] = 0.f;
         conic[i] = 0.f; conic[N + i] = 0.f; conic[2 * N + i] = 0.f;
         color[i] = 0.f; color[N + i] = 0.f; color[2 * N + i] = 0.f;
         radius[i] = 0;
         tiles[i] = 0;
+        if (alpha_k) alpha_k[i] = 0.f;
         return;
     }
     float rgb[3];
@@ -263,13 +284,13 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
             rgb[ch] = acc;
         }
     }
-    const float o = __ldg(opacity + i);
     means2d[i] = G.u; means2d[N + i] = G.v;
     depth[i] = G.p[2];
     conic[i] = G.A; conic[N + i] = G.B; conic[2 * N + i] = G.C;
     color[i] = rgb[0]; color[N + i] = rgb[1]; color[2 * N + i] = rgb[2];
     radius[i] = G.radius;
-    tiles[i] = uint32_t(G.rect[1] - G.rect[0]) * uint32_t(G.rect[3] - G.rect[2]);
+    tiles[i] = nt;
+    if (alpha_k) alpha_k[i] = ak;
     // Half-extents of the region where opacity * exp(power) >= 1/255, i.e. d^T Q d <= k with
     // k = 2 ln(255 o): the ellipse's bounding box is sqrt(k a) by sqrt(k c) (a, c the diagonal of
     // Sigma_2d = Q^-1).  Inflated by 0.1% in k and 0.01 px so that float rounding in the
@@ -467,7 +488,7 @@ cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_p
     k_project<D><<<blocks, threads, 0, s>>>(cam, g.n, g.d_means, g.d_scales, g.d_quats,         \
                                              g.d_opacity, g.d_sh, g.d_colors, o.d_means2d,      \
                                              o.d_depth, o.d_conic, o.d_color, o.d_radius,       \
-                                             o.d_tiles_touched, rec)
+                                             o.d_tiles_touched, rec, o.tile_test, o.d_alpha_k)
     switch (g.sh_degree) {
         case -1: RS_PROJECT(-1); break;
         case 0: RS_PROJECT(0); break;

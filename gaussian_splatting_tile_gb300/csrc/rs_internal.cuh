@@ -95,6 +95,74 @@ __device__ __forceinline__ int span_bound(float p, float r, int n_tiles, bool up
     return int(f);
 }
 
+// Tile coverage of the ellipse test (RS_TILE_TEST_ELLIPSE): the tiles of the radius square whose
+// pixel-centre squares [16 tx, 16 tx + 15] x [16 ty, 16 ty + 15] meet the ellipse d^T Q d <= k
+// (Q = (A, B; B, C) the conic, d = pixel - mean).  The ellipse is convex, so each tile row meets it in a run of
+// columns, found from the ellipse's x-extent over the row's band of y: the extreme point of the
+// left (right) boundary x = (-B dy -+ sqrt(A k - det dy^2)) / A, at dy = +-B sqrt(k / (det C))
+// with x = -+sqrt(C k / det), if it lies in the band, else the nearer band edge.  Widened by
+// 0.01 px.  Every operation is an explicitly rounded IEEE single-precision operation (no fused
+// multiply-add), so any implementation that performs the same operations takes the same integer
+// decisions.
+struct EllipseTiles {
+    float u, v, A, B, C, k;
+    float det, eyc, ex, dyl;  // A C - B^2, y half-extent, x half-extent, dy of the leftmost point
+    int ylo, yhi;             // tile rows, inclusive (none when ylo > yhi)
+    int xl, xh;               // the radius square's columns [xl, xh)
+};
+
+// rect = the radius square's tile span {xl, xh, yl, yh} (half-open): the test keeps a subset of
+// it, so the rendered footprint stays the square test's.
+__device__ __forceinline__ bool ellipse_tiles_init(float u, float v, float A, float B, float C, float k,
+                                                   const int (&rect)[4], int TY, EllipseTiles& e) {
+    e.u = u; e.v = v; e.A = A; e.B = B; e.C = C; e.k = k;
+    e.xl = rect[0];
+    e.xh = rect[1];
+    e.ylo = 0; e.yhi = -1;
+    if (!(k > 0.f) || !(A > 0.f) || !(C > 0.f)) return false;
+    e.det = __fsub_rn(__fmul_rn(A, C), __fmul_rn(B, B));
+    if (!(e.det > 0.f)) return false;
+    e.eyc = __fsqrt_rn(__fdiv_rn(__fmul_rn(A, k), e.det));
+    e.ex = __fsqrt_rn(__fdiv_rn(__fmul_rn(C, k), e.det));
+    e.dyl = __fmul_rn(B, __fsqrt_rn(__fdiv_rn(k, __fmul_rn(e.det, C))));
+    const float ey = __fadd_rn(e.eyc, 0.01f);
+    float lo = ceilf(__fdiv_rn(__fsub_rn(__fsub_rn(v, ey), 15.f), 16.f));
+    float hi = floorf(__fdiv_rn(__fadd_rn(v, ey), 16.f));
+    lo = fminf(fmaxf(lo, 0.f), float(TY));
+    hi = fmaxf(fminf(hi, float(TY - 1)), -1.f);
+    e.ylo = max(int(lo), rect[2]);
+    e.yhi = min(int(hi), rect[3] - 1);
+    return e.ylo <= e.yhi;
+}
+
+// x boundary of the ellipse at height dy: sign -1 left, +1 right.
+__device__ __forceinline__ float ellipse_x(const EllipseTiles& e, float dy, float sign) {
+    const float t = __fsub_rn(__fmul_rn(e.A, e.k), __fmul_rn(e.det, __fmul_rn(dy, dy)));
+    const float s = __fsqrt_rn(fmaxf(t, 0.f));
+    return __fdiv_rn(__fadd_rn(-__fmul_rn(e.B, dy), sign * s), e.A);
+}
+
+// Columns [xlo, xhi] (inclusive; none when xlo > xhi) of tile row ty.
+__device__ __forceinline__ void ellipse_row(const EllipseTiles& e, int ty, int TX, int& xlo, int& xhi) {
+    const float y0 = fminf(fmaxf(__fsub_rn(float(16 * ty), e.v), -e.eyc), e.eyc);
+    const float y1 = fminf(fmaxf(__fsub_rn(float(16 * ty + 15), e.v), -e.eyc), e.eyc);
+    const float xmin = (y0 <= e.dyl && e.dyl <= y1) ? -e.ex : fminf(ellipse_x(e, y0, -1.f), ellipse_x(e, y1, -1.f));
+    const float dyr = -e.dyl;
+    const float xmax = (y0 <= dyr && dyr <= y1) ? e.ex : fmaxf(ellipse_x(e, y0, 1.f), ellipse_x(e, y1, 1.f));
+    float lo = ceilf(__fdiv_rn(__fsub_rn(__fadd_rn(e.u, xmin), 15.01f), 16.f));
+    float hi = floorf(__fdiv_rn(__fadd_rn(__fadd_rn(e.u, xmax), 0.01f), 16.f));
+    lo = fminf(fmaxf(lo, 0.f), float(TX));
+    hi = fmaxf(fminf(hi, float(TX - 1)), -1.f);
+    xlo = max(int(lo), e.xl);
+    xhi = min(int(hi), e.xh - 1);
+}
+
+// k of the ellipse test for an opacity (0 when it can never reach alpha 1/255).
+__device__ __forceinline__ float alpha_k_of(float o) {
+    const float o255 = 255.f * o;
+    return o255 > 1.f ? 2.002f * logf(o255) : 0.f;
+}
+
 // Launchers (each returns the cudaError_t of its launches).
 cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_projected& out,
                            cudaStream_t s);

@@ -42,7 +42,7 @@ class Renderer:
     """Holds the buffers for one camera size and Gaussian count."""
 
     def __init__(self, camera, n: int, device="cuda", capacity: int | None = None,
-                 keep_keys: bool = True):
+                 keep_keys: bool = True, tile_test: int = rs.RS_TILE_TEST_SQUARE):
         self.camera = camera
         self.n = int(n)
         self.device = torch.device(device)
@@ -50,7 +50,7 @@ class Renderer:
         self.keep_keys = keep_keys
         self.cam_struct = rs.camera_struct(camera)
         self._bound = None
-        self.proj = rs.DeviceProjected.empty(self.n, self.device)
+        self.proj = rs.DeviceProjected.empty(self.n, self.device, tile_test)
         H, W = camera.height, camera.width
         self.image = torch.empty(3, H, W, dtype=torch.float32, device=self.device)
         self.final_T = torch.empty(H, W, dtype=torch.float32, device=self.device)

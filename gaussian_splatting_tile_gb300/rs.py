@@ -49,7 +49,11 @@ class rs_projected(ctypes.Structure):
     _fields_ = [("d_means2d", ctypes.c_void_p), ("d_depth", ctypes.c_void_p),
                 ("d_conic", ctypes.c_void_p), ("d_color", ctypes.c_void_p),
                 ("d_radius", ctypes.c_void_p), ("d_tiles_touched", ctypes.c_void_p),
-                ("d_records", ctypes.c_void_p)]
+                ("d_records", ctypes.c_void_p), ("d_alpha_k", ctypes.c_void_p),
+                ("tile_test", ctypes.c_int32)]
+
+
+RS_TILE_TEST_SQUARE, RS_TILE_TEST_ELLIPSE = 0, 1
 
 
 class rs_mlp(ctypes.Structure):
@@ -219,14 +223,17 @@ class DeviceProjected:
     radius: torch.Tensor
     tiles_touched: torch.Tensor
     records: torch.Tensor  # uint8 [N*48]
+    alpha_k: torch.Tensor | None = None  # [N], written and read in the ellipse tile test
+    tile_test: int = 0                   # RS_TILE_TEST_SQUARE or RS_TILE_TEST_ELLIPSE
 
     @staticmethod
-    def empty(n: int, device="cuda"):
+    def empty(n: int, device="cuda", tile_test: int = 0):
         f = lambda *s: torch.empty(*s, dtype=torch.float32, device=device)
         return DeviceProjected(f(2, n), f(n), f(3, n), f(3, n),
                                torch.empty(n, dtype=torch.int32, device=device),
                                torch.empty(n, dtype=torch.int32, device=device),
-                               torch.empty(max(n, 1) * RECORD_BYTES, dtype=torch.uint8, device=device))
+                               torch.empty(max(n, 1) * RECORD_BYTES, dtype=torch.uint8, device=device),
+                               f(max(n, 1)) if tile_test == RS_TILE_TEST_ELLIPSE else None, int(tile_test))
 
     def struct(self) -> rs_projected:
         n = int(self.depth.shape[0])
@@ -238,6 +245,9 @@ class DeviceProjected:
         s.d_radius = _ptr(self.radius, torch.int32, n, "radius")
         s.d_tiles_touched = _ptr(self.tiles_touched, None, n, "tiles_touched")
         s.d_records = _ptr(self.records, torch.uint8, n * RECORD_BYTES, "records")
+        s.tile_test = int(self.tile_test)
+        if self.tile_test == RS_TILE_TEST_ELLIPSE:
+            s.d_alpha_k = _ptr(self.alpha_k, torch.float32, n, "alpha_k")
         return s
 
 

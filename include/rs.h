@@ -93,7 +93,25 @@ typedef struct rs_projected {
     int32_t* d_radius;
     uint32_t* d_tiles_touched;
     void* d_records;
+    /* Which tiles a splat covers (read by rs_project and rs_bin; a zeroed struct means
+     * RS_TILE_TEST_SQUARE):
+     *  - RS_TILE_TEST_SQUARE: the tiles of its radius square, the pages' binning (rigel README
+     *    "Binning"; learn-gs "11 - Tiles", tile_spans).
+     *  - RS_TILE_TEST_ELLIPSE: only the tiles of that square whose pixel centres
+     *    [16 tx, 16 tx + 15] x [16 ty, 16 ty + 15] meet the ellipse where opacity exp(power)
+     *    >= 1/255, i.e.
+     *    d^T conic d <= k with k = 2.002 ln(255 opacity) (0.1% wider than exact, plus 0.01 px),
+     *    rows outer and columns inner as before.  The pages list this exact ellipse-tile test as
+     *    their next step; the skipped tiles hold only alpha < 1/255, so the image, final_T and
+     *    the gradients are those of the square test, with fewer entries; n_contrib counts only
+     *    the entries each pixel examined.  A splat meeting no tile is culled (radius 0).
+     *    rs_project writes d_alpha_k [n] (k, 0 when culled) and rs_bin reads it. */
+    float* d_alpha_k;
+    int32_t tile_test;
 } rs_projected;
+
+#define RS_TILE_TEST_SQUARE 0
+#define RS_TILE_TEST_ELLIPSE 1
 
 /* Human-readable text for a return code; never NULL. */
 const char* rs_error_string(int code);

@@ -63,6 +63,8 @@ def lib():
         _lib.orc_exclusive_scan_u32.restype = ctypes.c_uint64
         _lib.orc_bin_count.restype = ctypes.c_int64
         _lib.orc_bin.restype = ctypes.c_int64
+        _lib.orc_bin_ellipse.restype = ctypes.c_int64
+        _lib.orc_ellipse_tiles.restype = ctypes.c_int32
     return _lib
 
 
@@ -146,6 +148,44 @@ def bin(cam, means2d, depth, radius):
     assert E2 == E
     return dict(keys_sorted=keys[:E], point_list=pl[:E], ranges=ranges, tiles_touched=tt,
                 n_entries=int(E))
+
+
+def bin_ellipse(cam, means2d, depth, radius, conic, alpha_k):
+    """c2' (exact ellipse-tile test) from float32 projected data; same outputs as bin()."""
+    m2 = np.ascontiguousarray(means2d, np.float32)
+    dp = np.ascontiguousarray(depth, np.float32)
+    rd = np.ascontiguousarray(radius, np.int32)
+    cn = np.ascontiguousarray(conic, np.float32)
+    ak = np.ascontiguousarray(alpha_k, np.float32)
+    n = rd.shape[0]
+    c = _cam(cam)
+    n_tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
+    ranges = np.zeros((n_tiles, 2), np.uint32)
+    tt = np.zeros(n, np.uint32)
+    cap = 1 << 16
+    while True:
+        keys = np.zeros(cap, np.uint64)
+        pl = np.zeros(cap, np.uint32)
+        E = lib().orc_bin_ellipse(ctypes.byref(c), ctypes.c_int32(n), _p(m2), _p(dp), _p(rd), _p(cn), _p(ak),
+                                  ctypes.c_int64(cap), _p(keys), _p(pl), _p(ranges), _p(tt))
+        if E >= 0:
+            break
+        cap = int(tt.astype(np.int64).sum()) + 1
+    return dict(keys_sorted=keys[:E], point_list=pl[:E], ranges=ranges, tiles_touched=tt, n_entries=int(E))
+
+
+def ellipse_tiles(cam, u, v, A, B, C, k, radius, max_rows=4096):
+    """Rows and per-row column runs of the exact ellipse-tile test within the radius square:
+    list of (ty, xlo, xhi)."""
+    ylo = ctypes.c_int32(0)
+    xlo = np.zeros(max_rows, np.int32)
+    xhi = np.zeros(max_rows, np.int32)
+    c = _cam(cam)
+    f = ctypes.c_float
+    rows = lib().orc_ellipse_tiles(ctypes.byref(c), f(u), f(v), f(A), f(B), f(C), f(k), ctypes.c_int32(radius),
+                                   ctypes.byref(ylo),
+                                   _p(xlo), _p(xhi), ctypes.c_int32(max_rows))
+    return [(ylo.value + r, int(xlo[r]), int(xhi[r])) for r in range(min(rows, max_rows))]
 
 
 def raster_fwd(cam, means2d, conic, opacity, color, ranges, point_list, bg=(0.0, 0.0, 0.0),

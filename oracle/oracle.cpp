@@ -655,6 +655,70 @@ void view_dir(const Cam<double>& cam, const double* m, double* d) {
 
 }  // namespace
 
+// c2': the exact ellipse-tile test of the pages' "next" list, within the radius square (the
+// footprint the pages' binning renders).  The alpha >= 1/255 region of a splat is the ellipse
+// d^T Q d <= k (Q the conic (A, B; B, C), k = 2.002 ln(255 o) as given).
+// A tile row's band of pixel centres y in [16 ty, 16 ty + 15] meets it in an x-interval; the
+// leftmost point of the ellipse (x = -sqrt(C k / det) at dy = B sqrt(k / (det C))) bounds it
+// when it lies in the band, else the band edge nearer to it does, where the boundary is
+// x = (-B dy - sqrt(A k - det dy^2)) / A; likewise on the right.  Widened by 0.01 px.  Every step
+// is one IEEE single-precision operation (this file is built without contraction), the same
+// sequence as the kernels' test, so both take identical integer decisions.
+struct EllipseF {
+    float u, v, A, B, C, k, det, eyc, ex, dyl;
+    int ylo, yhi, xl, xh;
+};
+
+// rect: the radius square's tile span {xl, xh, yl, yh} (half-open); the test keeps a subset of it.
+static bool ellipse_init(float u, float v, float A, float B, float C, float k, const int* rect, int TY,
+                         EllipseF& e) {
+    e.u = u; e.v = v; e.A = A; e.B = B; e.C = C; e.k = k;
+    e.xl = rect[0];
+    e.xh = rect[1];
+    e.ylo = 0; e.yhi = -1;
+    if (!(k > 0.f) || !(A > 0.f) || !(C > 0.f)) return false;
+    const float ac = A * C, bb = B * B;
+    e.det = ac - bb;
+    if (!(e.det > 0.f)) return false;
+    const float ak = A * k, ck = C * k, dc = e.det * C;
+    e.eyc = std::sqrt(ak / e.det);
+    e.ex = std::sqrt(ck / e.det);
+    e.dyl = B * std::sqrt(k / dc);
+    const float ey = e.eyc + 0.01f;
+    const float vl = v - ey;
+    float lo = std::ceil((vl - 15.f) / 16.f);
+    float hi = std::floor((v + ey) / 16.f);
+    lo = std::fmin(std::fmax(lo, 0.f), float(TY));
+    hi = std::fmax(std::fmin(hi, float(TY - 1)), -1.f);
+    e.ylo = std::max(int(lo), rect[2]);
+    e.yhi = std::min(int(hi), rect[3] - 1);
+    return e.ylo <= e.yhi;
+}
+
+static float ellipse_x(const EllipseF& e, float dy, float sign) {
+    const float ak = e.A * e.k, dy2 = dy * dy, ddy = e.det * dy2;
+    const float t = ak - ddy;
+    const float sq = std::sqrt(std::fmax(t, 0.f));
+    const float bd = e.B * dy;
+    return (-bd + sign * sq) / e.A;
+}
+
+static void ellipse_row(const EllipseF& e, int ty, int TX, int& xlo, int& xhi) {
+    const float y0 = std::fmin(std::fmax(float(16 * ty) - e.v, -e.eyc), e.eyc);
+    const float y1 = std::fmin(std::fmax(float(16 * ty + 15) - e.v, -e.eyc), e.eyc);
+    const float xmin = (y0 <= e.dyl && e.dyl <= y1) ? -e.ex
+                                                     : std::fmin(ellipse_x(e, y0, -1.f), ellipse_x(e, y1, -1.f));
+    const float dyr = -e.dyl;
+    const float xmax = (y0 <= dyr && dyr <= y1) ? e.ex : std::fmax(ellipse_x(e, y0, 1.f), ellipse_x(e, y1, 1.f));
+    const float ul = e.u + xmin, ur = e.u + xmax;
+    float lo = std::ceil((ul - 15.01f) / 16.f);
+    float hi = std::floor((ur + 0.01f) / 16.f);
+    lo = std::fmin(std::fmax(lo, 0.f), float(TX));
+    hi = std::fmax(std::fmin(hi, float(TX - 1)), -1.f);
+    xlo = std::max(int(lo), e.xl);
+    xhi = std::min(int(hi), e.xh - 1);
+}
+
 extern "C" {
 
 int orc_project(int prec, const orc_camera* cam, int32_t n, const double* means,
@@ -1023,6 +1087,67 @@ int orc_l1_dssim(int32_t C, int32_t H, int32_t W, const double* image, const dou
             }
     if (loss) *loss = scale * ((1 - lambda) * sum_l1 + lambda * (double(N) - sum_s)) / double(N);
     return 0;
+}
+
+
+int32_t orc_ellipse_tiles(const orc_camera* cam, float u, float v, float A, float B, float C, float k,
+                          int32_t radius, int32_t* ylo, int32_t* xlo, int32_t* xhi, int32_t max_rows) {
+    const int TX = (cam->width + TILE - 1) / TILE, TY = (cam->height + TILE - 1) / TILE;
+    const float r = float(radius);
+    const int rect[4] = {span_lo<float>(u, r, TX), span_hi<float>(u, r, TX), span_lo<float>(v, r, TY),
+                         span_hi<float>(v, r, TY)};
+    EllipseF e;
+    if (radius <= 0 || !ellipse_init(u, v, A, B, C, k, rect, TY, e)) return 0;
+    const int rows = e.yhi - e.ylo + 1;
+    if (ylo) *ylo = e.ylo;
+    for (int r = 0; r < rows && r < max_rows; ++r) {
+        int a, b;
+        ellipse_row(e, e.ylo + r, TX, a, b);
+        xlo[r] = a;
+        xhi[r] = b;
+    }
+    return rows;
+}
+
+int64_t orc_bin_ellipse(const orc_camera* cam, int32_t n, const float* means2d, const float* depth,
+                        const int32_t* radius, const float* conic, const float* alpha_k,
+                        int64_t capacity, uint64_t* keys_sorted, uint32_t* point_list,
+                        uint32_t* ranges, uint32_t* tiles_touched) {
+    const int TX = (cam->width + TILE - 1) / TILE, TY = (cam->height + TILE - 1) / TILE;
+    std::vector<Entry> ent;
+    for (int32_t i = 0; i < n; ++i) {
+        uint32_t cnt = 0;
+        EllipseF e;
+        const float u = means2d[i], v = means2d[size_t(n) + i], r = float(radius[i]);
+        const int rect[4] = {span_lo<float>(u, r, TX), span_hi<float>(u, r, TX), span_lo<float>(v, r, TY),
+                             span_hi<float>(v, r, TY)};
+        if (radius[i] > 0 &&
+            ellipse_init(u, v, conic[i], conic[size_t(n) + i], conic[2 * size_t(n) + i], alpha_k[i], rect, TY, e)) {
+            uint32_t bits;
+            std::memcpy(&bits, &depth[i], 4);
+            for (int ty = e.ylo; ty <= e.yhi; ++ty) {
+                int xlo, xhi;
+                ellipse_row(e, ty, TX, xlo, xhi);
+                for (int tx = xlo; tx <= xhi; ++tx) {
+                    ++cnt;
+                    const uint64_t tile = uint64_t(ty) * uint64_t(TX) + uint64_t(tx);
+                    ent.push_back(Entry{(tile << 32) | uint64_t(bits), uint32_t(i)});
+                }
+            }
+        }
+        if (tiles_touched) tiles_touched[i] = cnt;
+    }
+    const int64_t E = int64_t(ent.size());
+    if (E > capacity) return -2;
+    std::stable_sort(ent.begin(), ent.end(), [](const Entry& a, const Entry& b) { return a.key < b.key; });
+    std::vector<uint64_t> ks(static_cast<size_t>(E));
+    for (int64_t q = 0; q < E; ++q) {
+        if (keys_sorted) keys_sorted[q] = ent[size_t(q)].key;
+        point_list[q] = ent[size_t(q)].value;
+        ks[size_t(q)] = ent[size_t(q)].key;
+    }
+    orc_tile_ranges(ks.data(), E, TX * TY, ranges);
+    return E;
 }
 
 }  // extern "C"

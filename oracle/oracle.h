@@ -139,6 +139,20 @@ int orc_densify_stats(int32_t n, const double* dmeans2d, const int32_t* radius, 
 int orc_l1_dssim(int32_t C, int32_t H, int32_t W, const double* image, const double* target,
                  double lambda, double scale, double* grad, double* loss, double* ssim);
 
+/* c2': binning with the exact ellipse-tile test (the pages' "next" step): per visible Gaussian
+ * only the tiles of its radius square whose pixel-centre squares meet the ellipse
+ * d^T conic d <= alpha_k, in float
+ * with the same operations as the kernels' test; otherwise as orc_bin.  The spans per row go to
+ * spans [n_rows_total] when not NULL (testing). */
+int64_t orc_bin_ellipse(const orc_camera* cam, int32_t n, const float* means2d, const float* depth,
+                        const int32_t* radius, const float* conic, const float* alpha_k,
+                        int64_t capacity, uint64_t* keys_sorted, uint32_t* point_list,
+                        uint32_t* ranges, uint32_t* tiles_touched);
+/* The rows [ylo, yhi] and per-row columns [xlo[r], xhi[r]] of one Gaussian's ellipse test (up to
+ * max_rows rows); returns the number of rows (0 when none). */
+int32_t orc_ellipse_tiles(const orc_camera* cam, float u, float v, float A, float B, float C, float k,
+                          int32_t radius, int32_t* ylo, int32_t* xlo, int32_t* xhi, int32_t max_rows);
+
 #ifdef __cplusplus
 }
 #endif

@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gaussian_splatting_tile_gb300 import pipeline, rs, scenes
 
 from . import parity as P
@@ -192,3 +193,53 @@ def test_forward_is_deterministic():
     b = P.run_gpu(g, cam)
     for k in ("means2d", "conic", "color", "keys", "point_list", "ranges", "image", "final_T", "n_contrib"):
         assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("which", ["tiny", "160k_1080p"])
+def test_ellipse_tile_test(which):
+    """RS_TILE_TEST_ELLIPSE: binning bit-exact against the oracle's ellipse binning on the same
+    projected data; the image and final_T bit-identical to the square test's (the dropped tiles
+    hold only alpha < 1/255); gradients equal to the square test's up to summation order; fewer
+    entries; n_contrib never larger."""
+    if which == "tiny":
+        g, cam = scenes.tiny_scene(seed=0)
+    else:
+        g = scenes.procedural_scene(seed=0)
+        cam = scenes.orbit_cameras(1920, 1080)[10]
+    dg = rs.DeviceGaussians.from_numpy(g)
+    dL = torch.from_numpy(scenes.image_grad(cam)).cuda()
+    out = {}
+    for mode in (rs.RS_TILE_TEST_SQUARE, rs.RS_TILE_TEST_ELLIPSE):
+        R = pipeline.Renderer(cam, g.n, tile_test=mode)
+        F = R.forward(dg)
+        B = R.backward(dg, dL)
+        torch.cuda.synchronize()
+        st = P.gpu_state(R, dg, F)
+        st.update({k: getattr(B, k).cpu().numpy() for k in ("dmeans2d", "dconic", "dopacity", "dcolor",
+                                                            "dmeans", "dscales", "dquats")})
+        if mode == rs.RS_TILE_TEST_ELLIPSE:
+            st["alpha_k"] = R.proj.alpha_k.cpu().numpy()
+        out[mode] = st
+    sq, el = out[rs.RS_TILE_TEST_SQUARE], out[rs.RS_TILE_TEST_ELLIPSE]
+    # binning against the oracle, on the GPU's projected data
+    Be = oracle.bin_ellipse(cam, el["means2d"], el["depth"], el["radius"], el["conic"], el["alpha_k"])
+    assert el["n_entries"] == Be["n_entries"]
+    assert np.array_equal(el["tiles_touched"], Be["tiles_touched"])
+    assert np.array_equal(el["keys"], Be["keys_sorted"])
+    assert np.array_equal(el["point_list"], Be["point_list"])
+    assert np.array_equal(el["ranges"].reshape(-1, 2), Be["ranges"])
+    assert el["n_entries"] < sq["n_entries"]
+    # projection: the ellipse test only culls; k = 2.002 ln(255 o)
+    vis = el["radius"] > 0
+    assert not (vis & (sq["radius"] == 0)).any()
+    for k in ("means2d", "depth", "conic", "color"):
+        assert np.array_equal(el[k][..., vis], sq[k][..., vis])
+    o = g.opacity.astype(np.float64)[vis]
+    P.allclose_report("alpha_k", el["alpha_k"][vis], 2.002 * np.log(255 * o), 1e-6, 1e-6)
+    # the same image, and gradients up to summation order
+    assert np.array_equal(el["image"], sq["image"]) and np.array_equal(el["final_T"], sq["final_T"])
+    assert (el["n_contrib"] <= sq["n_contrib"]).all()
+    # both are float32 sums over tiles in no fixed order; where those sums cancel, their rounding
+    # scales with the terms, not the result, so the absolute part is 1e-5 of the largest gradient
+    for k in ("dmeans2d", "dconic", "dopacity", "dcolor", "dmeans", "dscales", "dquats"):
+        P.allclose_report(k, el[k], sq[k], P.GRAD_RTOL, P.GRAD_ATOL, atol_of_max=1e-5)
