@@ -84,6 +84,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ellipse", action="store_true",
+                    help="skip the frame timing with the exact ellipse-tile binning (reported beside the line)")
     ap.add_argument("--no-adam", action="store_true",
                     help="skip the fused Adam step's timing (reported beside the line)")
     ap.add_argument("--no-train", action="store_true",
@@ -300,6 +302,8 @@ def run_ours(args):
         result["e2e"] = run_e2e(g, cams, rank, world, args, device)
     if world == 1 and not args.no_train:
         result["training_step"] = run_training_step(device)
+    if world == 1 and not args.no_ellipse:
+        result["ellipse_tile_test"] = run_ellipse(g, cams, device)
     if world == 1 and not args.no_adam:
         result["adam"] = run_adam(g, device)
         result["l1_dssim"] = run_l1_dssim(device)
@@ -389,6 +393,56 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
                                   bwd_achieved=n * B_MLP_BWD_PER_G / mlp_bwd_s / 1e9,
                                   bwd_frac=n * B_MLP_BWD_PER_G / mlp_bwd_s / 1e9 / hbm,
                                   bytes_per_gaussian=dict(fwd=B_MLP_FWD_PER_G, bwd=B_MLP_BWD_PER_G)))
+
+
+def run_ellipse(g, cams, device, steps: int = 30, warmup: int = 5):
+    """The same frames (forward + backward, sync-free binning, L2 written over before each) with
+    RS_TILE_TEST_ELLIPSE: only the tiles of each radius square that the alpha >= 1/255 ellipse
+    meets are binned.  The image is the same; the entry count and the work fall."""
+    import numpy as np
+    import torch
+
+    from gaussian_splatting_tile_gb300 import pipeline, rs, scenes
+
+    dg = rs.DeviceGaussians.from_numpy(g, device)
+    R = pipeline.Renderer(cams[0], g.n, device, capacity=4_000_000, keep_keys=False,
+                          tile_test=rs.RS_TILE_TEST_ELLIPSE)
+    dL = torch.from_numpy(scenes.image_grad(cams[0])).to(device)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for v in range(warmup):
+        R.set_camera(cams[v])
+        R.forward(dg)
+        R.backward(dg, dL)
+    res = torch.zeros(steps, 2, dtype=torch.int64).pin_memory()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    for i in range(steps):
+        flush.fill_(float(i))
+        e = ev[i]
+        R.set_camera(cams[(warmup + i) % len(cams)])
+        e[0].record(stream)
+        R.project(dg)
+        e[1].record(stream)
+        R.bin_async(res[i])
+        e[2].record(stream)
+        R.rasterize()
+        e[3].record(stream)
+        R._grads(dg.sh_degree)
+        R.rasterize_backward(dL)
+        e[4].record(stream)
+        R.project_backward(dg)
+        e[5].record(stream)
+    torch.cuda.synchronize(device)
+    ents = [int(x) for x in res[:, 0].tolist()]
+    if max(ents) > R.capacity or int(res[:, 1].abs().sum()) != 0:
+        raise RuntimeError("ellipse-test binning overflowed or timed out")
+    st = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(5)] for e in ev])
+    ms = float(st.sum(axis=1).mean())
+    return dict(ms_per_step=ms, entries_per_frame=float(np.mean(ents)),
+                stage_ms=dict(zip(["project", "bin", "rasterize_fwd", "rasterize_bwd", "project_bwd"],
+                                  [float(x) for x in st.mean(axis=0)])),
+                note="same views and image as the headline line; fewer (splat, tile) entries")
 
 
 def run_adam(g, device, steps: int = 20, warmup: int = 3):
