@@ -340,6 +340,8 @@ struct SliceOut {
     uint2* rect;          // [n] tile rectangle of each Gaussian (depth order)
     uint32_t* owner;      // [chunks] depth position owning entry 1024 c
     uint32_t chunks;      // ceil(capacity / 1024)
+    const float* ell;     // ellipse test only: the projection's words, [RS_ELLIPSE_WORDS][n] by
+                          // Gaussian (row 0 k, rows 1.. the per-splat setup)
 };
 
 __global__ void __launch_bounds__(kSlThreads) k_slices(CameraF cam, uint32_t n, const uint32_t* __restrict__ perm,
@@ -443,24 +445,34 @@ __global__ void __launch_bounds__(kSlThreads) k_slices(CameraF cam, uint32_t n, 
     }
 }
 
-// Projected data the ellipse test reads (RS_TILE_TEST_ELLIPSE).
-struct EllipseSource {
-    const float* means2d;
-    const float* conic;
-    const float* alpha_k;
-    const int* radius;
-};
+
+// The ellipse test's tile runs of a window's Gaussians, built once per chunk, one row per
+// thread: row r of window Gaussian j is table entry rowstart[j] + r, holding the window's
+// entries before that row (counted from the first Gaussian's slice start), the row's first tile
+// and j; an entry then finds its row with one binary search.  Chunks whose Gaussians have more
+// rows than the table holds walk the rows per entry.
+constexpr int kRowCap = 2048;
 
 template <int RBITS, bool ELL>
 __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n, Count count,
                                                        const uint32_t* __restrict__ perm, SliceOut sl,
                                                        int digit_bits, int passes, uint32_t* __restrict__ ghist,
                                                        uint32_t* __restrict__ tile_keys,
-                                                       uint32_t* __restrict__ vals, EllipseSource es) {
+                                                       uint32_t* __restrict__ vals) {
     constexpr int R = 1 << RBITS;
+    constexpr int ROWS = ELL ? kRowCap : 1;
     __shared__ uint64_t s_start[kExpChunk + 1];
     __shared__ uint2 s_rect[ELL ? 1 : kExpChunk];
-    __shared__ float s_e[ELL ? 7 : 1][ELL ? kExpChunk : 1];  // u, v, A, B, C, k, radius
+    __shared__ uint32_t s_rowstart[ELL ? kExpChunk + 1 : 1];
+    __shared__ uint32_t s_w[kExpThreads / 32];
+    // ellipse mode, dynamic: the window's tile rows (ylo | yhi << 16) [kExpChunk], then the row
+    // table: the window's entries before each row [ROWS], the row's first tile [ROWS] and its
+    // Gaussian [ROWS] (16 bits); the other ellipse words are read from the slice output
+    extern __shared__ __align__(16) float s_dyn[];
+    float* s_e = s_dyn;
+    uint32_t* s_rowcum = reinterpret_cast<uint32_t*>(s_dyn + (ELL ? kExpChunk : 0));
+    uint32_t* s_rowtile = s_rowcum + ROWS;
+    uint16_t* s_rowg = reinterpret_cast<uint16_t*>(s_rowtile + ROWS);  // window index of the row's Gaussian
     __shared__ uint32_t s_g[kExpChunk];
     __shared__ uint32_t s_h[3][R];
     const uint32_t E = count.get();
@@ -485,15 +497,77 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
                 const uint32_t g = perm[i];
                 s_g[j] = g;
                 if (ELL) {
-                    s_e[0][j] = es.means2d[g];
-                    s_e[1][j] = es.means2d[size_t(n) + g];
-                    s_e[2][j] = es.conic[g];
-                    s_e[3][j] = es.conic[size_t(n) + g];
-                    s_e[4][j] = es.conic[2 * size_t(n) + g];
-                    s_e[5][j] = es.alpha_k[g];
-                    s_e[6][j] = float(es.radius[g]);
+                    // rows ylo | yhi << 16; a Gaussian without entries has none
+                    const bool has = (i + 1 < n ? sl.start[i + 1] : uint64_t(E)) > sl.start[i];
+                    s_e[j] = has ? sl.ell[10 * size_t(n) + g] : __uint_as_float(0xffff0000u);
                 } else {
                     s_rect[j] = sl.rect[i];
+                }
+            }
+        }
+        bool table = false;
+        if (ELL) {
+            __syncthreads();
+            // rows of the window's Gaussians (thread t: Gaussians 4t .. 4t + 3), their prefix
+            uint32_t nr[kExpChunk / kExpThreads], sum = 0;
+#pragma unroll
+            for (int q = 0; q < kExpChunk / kExpThreads; ++q) {
+                const int j = int(threadIdx.x) * (kExpChunk / kExpThreads) + q;
+                nr[q] = 0u;
+                if (j < w) {
+                    const uint32_t y = __float_as_uint(s_e[j]);
+                    const int ylo = int(int16_t(y & 0xffff)), yhi = int(int16_t(y >> 16));
+                    nr[q] = yhi >= ylo ? uint32_t(yhi - ylo + 1) : 0u;
+                }
+                sum += nr[q];
+            }
+            uint32_t base = block_exclusive_scan_256(sum, s_w);
+#pragma unroll
+            for (int q = 0; q < kExpChunk / kExpThreads; ++q) {
+                const int j = int(threadIdx.x) * (kExpChunk / kExpThreads) + q;
+                if (j < w) s_rowstart[j] = base;
+                base += nr[q];
+            }
+            if (threadIdx.x == kExpThreads - 1) s_rowstart[w] = base;  // total rows
+            __syncthreads();
+            const uint32_t rows = s_rowstart[w];
+            table = rows <= uint32_t(kRowCap);
+            if (table) {
+                // one row per thread: its Gaussian (the last whose first row is at most o), its
+                // run of columns; widths into s_rowcum, then their prefix over the window
+                uint32_t wsum = 0;
+                constexpr int RPT = kRowCap / kExpThreads;  // rows per thread in the prefix
+                for (int o = int(threadIdx.x); o < int(rows); o += kExpThreads) {
+                    int a = 0, b = w;  // s_rowstart[a] <= o < s_rowstart[b]
+                    while (b - a > 1) {
+                        const int mid = (a + b) >> 1;
+                        if (s_rowstart[mid] <= uint32_t(o)) a = mid; else b = mid;
+                    }
+                    EllipseTiles el;
+                    ellipse_unpack(sl.ell + size_t(n) + s_g[a], int(n), el);
+                    const int ty = el.ylo + (o - int(s_rowstart[a]));
+                    int xlo, xhi;
+                    ellipse_row(el, ty, cam.TX, xlo, xhi);
+                    s_rowcum[o] = xhi >= xlo ? uint32_t(xhi - xlo + 1) : 0u;
+                    s_rowtile[o] = uint32_t(ty) * uint32_t(cam.TX) + uint32_t(max(xlo, 0));
+                    s_rowg[o] = uint16_t(a);
+                }
+                __syncthreads();
+                // exclusive prefix of the widths: thread t owns rows RPT t .. RPT t + RPT - 1
+                uint32_t loc[RPT];
+#pragma unroll
+                for (int q = 0; q < RPT; ++q) {
+                    const int o = int(threadIdx.x) * RPT + q;
+                    loc[q] = o < int(rows) ? s_rowcum[o] : 0u;
+                    wsum += loc[q];
+                }
+                uint32_t run = block_exclusive_scan_256(wsum, s_w);
+                __syncthreads();  // every row's width was read before it is overwritten
+#pragma unroll
+                for (int q = 0; q < RPT; ++q) {
+                    const int o = int(threadIdx.x) * RPT + q;
+                    if (o < int(rows)) s_rowcum[o] = run;
+                    run += loc[q];
                 }
             }
         }
@@ -503,21 +577,31 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
             const uint32_t e = e0 + k * kExpThreads + threadIdx.x;
             const bool valid = e < E;
             uint32_t tile = 0u;
-            if (valid) {
+            uint32_t gid = 0u;
+            if (valid && ELL && table) {
+                // the window's rows in entry order: the last row starting at or before e
+                const uint32_t off = uint32_t(uint64_t(e) - s_start[0]);
+                int a = 0, b = int(s_rowstart[w]);
+                while (b - a > 1) {
+                    const int mid = (a + b) >> 1;
+                    if (s_rowcum[mid] <= off) a = mid; else b = mid;
+                }
+                tile = s_rowtile[a] + (off - s_rowcum[a]);
+                gid = s_g[s_rowg[a]];
+            } else if (valid) {
                 int lo = 0, hi = w;  // s_start[lo] <= e < s_start[hi]
                 while (hi - lo > 1) {
                     const int mid = (lo + hi) >> 1;
                     if (s_start[mid] <= e) lo = mid; else hi = mid;
                 }
                 const uint32_t kk = uint32_t(uint64_t(e) - s_start[lo]);
+                gid = s_g[lo];
                 if (ELL) {
-                    // the kk-th tile of the splat's rows of column runs
-                    EllipseTiles el;
+                    // the kk-th tile of the splat's rows of column runs, walked row by row
                     tile = tiles_total;  // unreachable for consistent inputs; k_ranges skips it
-                    const float u = s_e[0][lo], v = s_e[1][lo], r = s_e[6][lo];
-                    const int rect[4] = {span_bound(u, r, cam.TX, false), span_bound(u, r, cam.TX, true),
-                                         span_bound(v, r, cam.TY, false), span_bound(v, r, cam.TY, true)};
-                    if (ellipse_tiles_init(u, v, s_e[2][lo], s_e[3][lo], s_e[4][lo], s_e[5][lo], rect, cam.TY, el)) {
+                    EllipseTiles el;
+                    ellipse_unpack(sl.ell + size_t(n) + s_g[lo], int(n), el);
+                    if (el.ylo <= el.yhi) {
                         uint32_t cum = 0u;
                         for (int ty = el.ylo; ty <= el.yhi; ++ty) {
                             int xlo, xhi;
@@ -535,8 +619,10 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
                     const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
                     tile = ty * uint32_t(cam.TX) + tx;
                 }
+            }
+            if (valid) {
                 tile_keys[e] = tile;
-                vals[e] = s_g[lo];
+                vals[e] = gid;
             }
             for (int p = 0; p < passes; ++p) {
                 const uint32_t d = valid ? (tile >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
@@ -610,11 +696,15 @@ template <int RBITS>
 void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* perm, const SliceOut& sl, int digit,
                    int passes, uint32_t* ghist, uint32_t* tk, uint32_t* tv, const rs_projected& p, cudaStream_t s) {
     const unsigned blocks = unsigned(std::min<size_t>(sl.chunks, 152 * 8));
-    const EllipseSource es{p.d_means2d, p.d_conic, p.d_alpha_k, p.d_radius};
-    if (p.tile_test == RS_TILE_TEST_ELLIPSE)
-        k_expand<RBITS, true><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv, es);
+    if (p.tile_test == RS_TILE_TEST_ELLIPSE) {
+        constexpr size_t smem = (kExpChunk + 2 * kRowCap) * sizeof(float) + kRowCap * sizeof(uint16_t);
+        if (cudaFuncSetAttribute(k_expand<RBITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess)
+            return;  // that error stays the last error, which launch_bin returns
+        k_expand<RBITS, true><<<blocks, kExpThreads, smem, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
+    }
     else
-        k_expand<RBITS, false><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv, es);
+        k_expand<RBITS, false><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
 }
 
 cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_projected& p, uint8_t* ws,
@@ -666,8 +756,10 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
     uint32_t* TK[2] = {tk, tk + plan.capacity};
     uint32_t* TV[2] = {point_list, reinterpret_cast<uint32_t*>(ws + plan.off_tvals)};
     int cur = plan.tile_passes % 2;  // the last pass lands in buffer 0 (the caller's list)
+    const bool ell = p.tile_test == RS_TILE_TEST_ELLIPSE;
     const SliceOut sl{reinterpret_cast<uint64_t*>(ws + plan.off_start), reinterpret_cast<uint2*>(ws + plan.off_rect),
-                      reinterpret_cast<uint32_t*>(ws + plan.off_owner), uint32_t(plan.chunks)};
+                      reinterpret_cast<uint32_t*>(ws + plan.off_owner), uint32_t(plan.chunks),
+                      ell ? p.d_ellipse : nullptr};
     k_slices<<<unsigned(plan.slice_blocks), kSlThreads, 0, s>>>(
         cam, n, perm, tiles_sorted, p.d_means2d, p.d_radius, counters + 7,
         reinterpret_cast<unsigned long long*>(ws + plan.off_status_slices), error, result, sl);

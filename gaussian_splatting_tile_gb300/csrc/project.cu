@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
                                                  const float* __restrict__ colors, float* means2d,
                                                  float* depth, float* conic, float* color,
                                                  int* radius, uint32_t* tiles, Record* rec,
-                                                 int tile_test, float* alpha_k) {
+                                                 int tile_test, float* ellipse) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const size_t N = size_t(n);
@@ -255,6 +255,13 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
                     if (xhi >= xlo) nt += uint32_t(xhi - xlo + 1);
                 }
             }
+            if (nt > 0) {
+                // the per-splat setup, for the binning's expansion
+                float w[kEllWords];
+                ellipse_pack(e, w);
+#pragma unroll
+                for (int q = 0; q < kEllWords; ++q) ellipse[(q + 1) * N + i] = w[q];
+            }
         }
     }
     if (!G.visible || nt == 0) {
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
         color[i] = 0.f; color[N + i] = 0.f; color[2 * N + i] = 0.f;
         radius[i] = 0;
         tiles[i] = 0;
-        if (alpha_k) alpha_k[i] = 0.f;
+        if (tile_test == RS_TILE_TEST_ELLIPSE) ellipse[i] = 0.f;
         return;
     }
     float rgb[3];
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
     color[i] = rgb[0]; color[N + i] = rgb[1]; color[2 * N + i] = rgb[2];
     radius[i] = G.radius;
     tiles[i] = nt;
-    if (alpha_k) alpha_k[i] = ak;
+    if (tile_test == RS_TILE_TEST_ELLIPSE) ellipse[i] = ak;
     // Half-extents of the region where opacity * exp(power) >= 1/255, i.e. d^T Q d <= k with
     // k = 2 ln(255 o): the ellipse's bounding box is sqrt(k a) by sqrt(k c) (a, c the diagonal of
     // Sigma_2d = Q^-1).  Inflated by 0.1% in k and 0.01 px so that float rounding in the
@@ -488,7 +495,7 @@ cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_p
     k_project<D><<<blocks, threads, 0, s>>>(cam, g.n, g.d_means, g.d_scales, g.d_quats,         \
                                              g.d_opacity, g.d_sh, g.d_colors, o.d_means2d,      \
                                              o.d_depth, o.d_conic, o.d_color, o.d_radius,       \
-                                             o.d_tiles_touched, rec, o.tile_test, o.d_alpha_k)
+                                             o.d_tiles_touched, rec, o.tile_test, o.d_ellipse)
     switch (g.sh_degree) {
         case -1: RS_PROJECT(-1); break;
         case 0: RS_PROJECT(0); break;

@@ -45,7 +45,7 @@ bool projected_ok(const rs_projected* p, bool need_records) {
         return false;
     if (need_records && !(p->d_records && aligned(p->d_records, 16))) return false;
     if (p->tile_test != RS_TILE_TEST_SQUARE && p->tile_test != RS_TILE_TEST_ELLIPSE) return false;
-    if (p->tile_test == RS_TILE_TEST_ELLIPSE && !dev_f(p->d_alpha_k)) return false;
+    if (p->tile_test == RS_TILE_TEST_ELLIPSE && !dev_f(p->d_ellipse)) return false;
     return true;
 }
 

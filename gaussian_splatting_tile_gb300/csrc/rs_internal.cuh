@@ -97,16 +97,18 @@ __device__ __forceinline__ int span_bound(float p, float r, int n_tiles, bool up
 
 // Tile coverage of the ellipse test (RS_TILE_TEST_ELLIPSE): the tiles of the radius square whose
 // pixel-centre squares [16 tx, 16 tx + 15] x [16 ty, 16 ty + 15] meet the ellipse d^T Q d <= k
-// (Q = (A, B; B, C) the conic, d = pixel - mean).  The ellipse is convex, so each tile row meets it in a run of
-// columns, found from the ellipse's x-extent over the row's band of y: the extreme point of the
-// left (right) boundary x = (-B dy -+ sqrt(A k - det dy^2)) / A, at dy = +-B sqrt(k / (det C))
-// with x = -+sqrt(C k / det), if it lies in the band, else the nearer band edge.  Widened by
-// 0.01 px.  Every operation is an explicitly rounded IEEE single-precision operation (no fused
-// multiply-add), so any implementation that performs the same operations takes the same integer
-// decisions.
+// (Q = (A, B; B, C) the conic, d = pixel - mean).  The ellipse is convex, so each tile row meets
+// it in a run of columns, found from the ellipse's x-extent over the row's band of y: the
+// extreme point of the left (right) boundary x = -(B/A) dy -+ sqrt(A k - det dy^2) / A, at
+// dy = +-B sqrt(k / (det C)) with x = -+sqrt(C k / det), if it lies in the band, else the nearer
+// band edge.  Widened by 0.01 px.  Every operation is an explicitly rounded IEEE single-precision
+// operation (no fused multiply-add; divisions and square roots correctly rounded), so any
+// implementation that performs the same operations takes the same integer decisions.  The
+// per-splat part (divisions included) is computed once; a row costs two square roots.
 struct EllipseTiles {
-    float u, v, A, B, C, k;
-    float det, eyc, ex, dyl;  // A C - B^2, y half-extent, x half-extent, dy of the leftmost point
+    float u, v;
+    float nb, inva, ak, det;  // B / A, 1 / A, A k, A C - B^2
+    float eyc, ex, dyl;       // y half-extent, x half-extent, dy of the leftmost point
     int ylo, yhi;             // tile rows, inclusive (none when ylo > yhi)
     int xl, xh;               // the radius square's columns [xl, xh)
 };
@@ -115,19 +117,22 @@ struct EllipseTiles {
 // it, so the rendered footprint stays the square test's.
 __device__ __forceinline__ bool ellipse_tiles_init(float u, float v, float A, float B, float C, float k,
                                                    const int (&rect)[4], int TY, EllipseTiles& e) {
-    e.u = u; e.v = v; e.A = A; e.B = B; e.C = C; e.k = k;
+    e.u = u; e.v = v;
     e.xl = rect[0];
     e.xh = rect[1];
     e.ylo = 0; e.yhi = -1;
     if (!(k > 0.f) || !(A > 0.f) || !(C > 0.f)) return false;
     e.det = __fsub_rn(__fmul_rn(A, C), __fmul_rn(B, B));
     if (!(e.det > 0.f)) return false;
-    e.eyc = __fsqrt_rn(__fdiv_rn(__fmul_rn(A, k), e.det));
+    e.inva = __fdiv_rn(1.f, A);
+    e.nb = __fmul_rn(B, e.inva);
+    e.ak = __fmul_rn(A, k);
+    e.eyc = __fsqrt_rn(__fdiv_rn(e.ak, e.det));
     e.ex = __fsqrt_rn(__fdiv_rn(__fmul_rn(C, k), e.det));
     e.dyl = __fmul_rn(B, __fsqrt_rn(__fdiv_rn(k, __fmul_rn(e.det, C))));
     const float ey = __fadd_rn(e.eyc, 0.01f);
-    float lo = ceilf(__fdiv_rn(__fsub_rn(__fsub_rn(v, ey), 15.f), 16.f));
-    float hi = floorf(__fdiv_rn(__fadd_rn(v, ey), 16.f));
+    float lo = ceilf(__fmul_rn(__fsub_rn(__fsub_rn(v, ey), 15.f), 0.0625f));
+    float hi = floorf(__fmul_rn(__fadd_rn(v, ey), 0.0625f));
     lo = fminf(fmaxf(lo, 0.f), float(TY));
     hi = fmaxf(fminf(hi, float(TY - 1)), -1.f);
     e.ylo = max(int(lo), rect[2]);
@@ -135,26 +140,41 @@ __device__ __forceinline__ bool ellipse_tiles_init(float u, float v, float A, fl
     return e.ylo <= e.yhi;
 }
 
-// x boundary of the ellipse at height dy: sign -1 left, +1 right.
-__device__ __forceinline__ float ellipse_x(const EllipseTiles& e, float dy, float sign) {
-    const float t = __fsub_rn(__fmul_rn(e.A, e.k), __fmul_rn(e.det, __fmul_rn(dy, dy)));
-    const float s = __fsqrt_rn(fmaxf(t, 0.f));
-    return __fdiv_rn(__fadd_rn(-__fmul_rn(e.B, dy), sign * s), e.A);
-}
-
 // Columns [xlo, xhi] (inclusive; none when xlo > xhi) of tile row ty.
 __device__ __forceinline__ void ellipse_row(const EllipseTiles& e, int ty, int TX, int& xlo, int& xhi) {
     const float y0 = fminf(fmaxf(__fsub_rn(float(16 * ty), e.v), -e.eyc), e.eyc);
     const float y1 = fminf(fmaxf(__fsub_rn(float(16 * ty + 15), e.v), -e.eyc), e.eyc);
-    const float xmin = (y0 <= e.dyl && e.dyl <= y1) ? -e.ex : fminf(ellipse_x(e, y0, -1.f), ellipse_x(e, y1, -1.f));
+    // boundary at the band edges: centre -(B/A) y, half-width sqrt(A k - det y^2) / A
+    const float c0 = -__fmul_rn(e.nb, y0), c1 = -__fmul_rn(e.nb, y1);
+    const float h0 = __fmul_rn(__fsqrt_rn(fmaxf(__fsub_rn(e.ak, __fmul_rn(e.det, __fmul_rn(y0, y0))), 0.f)), e.inva);
+    const float h1 = __fmul_rn(__fsqrt_rn(fmaxf(__fsub_rn(e.ak, __fmul_rn(e.det, __fmul_rn(y1, y1))), 0.f)), e.inva);
+    const float xmin = (y0 <= e.dyl && e.dyl <= y1) ? -e.ex : fminf(__fsub_rn(c0, h0), __fsub_rn(c1, h1));
     const float dyr = -e.dyl;
-    const float xmax = (y0 <= dyr && dyr <= y1) ? e.ex : fmaxf(ellipse_x(e, y0, 1.f), ellipse_x(e, y1, 1.f));
-    float lo = ceilf(__fdiv_rn(__fsub_rn(__fadd_rn(e.u, xmin), 15.01f), 16.f));
-    float hi = floorf(__fdiv_rn(__fadd_rn(__fadd_rn(e.u, xmax), 0.01f), 16.f));
+    const float xmax = (y0 <= dyr && dyr <= y1) ? e.ex : fmaxf(__fadd_rn(c0, h0), __fadd_rn(c1, h1));
+    float lo = ceilf(__fmul_rn(__fsub_rn(__fadd_rn(e.u, xmin), 15.01f), 0.0625f));
+    float hi = floorf(__fmul_rn(__fadd_rn(__fadd_rn(e.u, xmax), 0.01f), 0.0625f));
     lo = fminf(fmaxf(lo, 0.f), float(TX));
     hi = fmaxf(fminf(hi, float(TX - 1)), -1.f);
     xlo = max(int(lo), e.xl);
     xhi = min(int(hi), e.xh - 1);
+}
+
+// The per-splat part as 11 words (expansion staging): u, v, nb, inva, ak, det, eyc, ex, dyl,
+// ylo | yhi << 16, xl | xh << 16 (tile indices fit 16 bits: at most 2048 columns or rows).
+constexpr int kEllWords = 11;
+static_assert(kEllWords + 1 == RS_ELLIPSE_WORDS, "k, then the packed setup");
+__device__ __forceinline__ void ellipse_pack(const EllipseTiles& e, float (&w)[kEllWords]) {
+    w[0] = e.u; w[1] = e.v; w[2] = e.nb; w[3] = e.inva; w[4] = e.ak; w[5] = e.det;
+    w[6] = e.eyc; w[7] = e.ex; w[8] = e.dyl;
+    w[9] = __uint_as_float(uint32_t(e.ylo & 0xffff) | (uint32_t(e.yhi & 0xffff) << 16));
+    w[10] = __uint_as_float(uint32_t(e.xl & 0xffff) | (uint32_t(e.xh & 0xffff) << 16));
+}
+__device__ __forceinline__ void ellipse_unpack(const float* w, int stride, EllipseTiles& e) {
+    e.u = w[0]; e.v = w[stride]; e.nb = w[2 * stride]; e.inva = w[3 * stride]; e.ak = w[4 * stride];
+    e.det = w[5 * stride]; e.eyc = w[6 * stride]; e.ex = w[7 * stride]; e.dyl = w[8 * stride];
+    const uint32_t y = __float_as_uint(w[9 * stride]), x = __float_as_uint(w[10 * stride]);
+    e.ylo = int(int16_t(y & 0xffff)); e.yhi = int(int16_t(y >> 16));
+    e.xl = int(int16_t(x & 0xffff)); e.xh = int(int16_t(x >> 16));
 }
 
 // k of the ellipse test for an opacity (0 when it can never reach alpha 1/255).

@@ -49,11 +49,12 @@ class rs_projected(ctypes.Structure):
     _fields_ = [("d_means2d", ctypes.c_void_p), ("d_depth", ctypes.c_void_p),
                 ("d_conic", ctypes.c_void_p), ("d_color", ctypes.c_void_p),
                 ("d_radius", ctypes.c_void_p), ("d_tiles_touched", ctypes.c_void_p),
-                ("d_records", ctypes.c_void_p), ("d_alpha_k", ctypes.c_void_p),
+                ("d_records", ctypes.c_void_p), ("d_ellipse", ctypes.c_void_p),
                 ("tile_test", ctypes.c_int32)]
 
 
 RS_TILE_TEST_SQUARE, RS_TILE_TEST_ELLIPSE = 0, 1
+RS_ELLIPSE_WORDS = 12  # rows of the ellipse tile test's per-Gaussian words
 
 
 class rs_mlp(ctypes.Structure):
@@ -223,7 +224,8 @@ class DeviceProjected:
     radius: torch.Tensor
     tiles_touched: torch.Tensor
     records: torch.Tensor  # uint8 [N*48]
-    alpha_k: torch.Tensor | None = None  # [N], written and read in the ellipse tile test
+    ellipse: torch.Tensor | None = None  # [RS_ELLIPSE_WORDS, N], the ellipse tile test's words:
+                                         # row 0 its k, the rest its setup for the binning
     tile_test: int = 0                   # RS_TILE_TEST_SQUARE or RS_TILE_TEST_ELLIPSE
 
     @staticmethod
@@ -233,7 +235,13 @@ class DeviceProjected:
                                torch.empty(n, dtype=torch.int32, device=device),
                                torch.empty(n, dtype=torch.int32, device=device),
                                torch.empty(max(n, 1) * RECORD_BYTES, dtype=torch.uint8, device=device),
-                               f(max(n, 1)) if tile_test == RS_TILE_TEST_ELLIPSE else None, int(tile_test))
+                               f(RS_ELLIPSE_WORDS, max(n, 1)) if tile_test == RS_TILE_TEST_ELLIPSE else None,
+                               int(tile_test))
+
+    @property
+    def alpha_k(self) -> torch.Tensor | None:
+        """k of the alpha >= 1/255 ellipse, per Gaussian (0 when culled); ellipse test only."""
+        return None if self.ellipse is None else self.ellipse[0, : self.depth.shape[0]]
 
     def struct(self) -> rs_projected:
         n = int(self.depth.shape[0])
@@ -247,7 +255,10 @@ class DeviceProjected:
         s.d_records = _ptr(self.records, torch.uint8, n * RECORD_BYTES, "records")
         s.tile_test = int(self.tile_test)
         if self.tile_test == RS_TILE_TEST_ELLIPSE:
-            s.d_alpha_k = _ptr(self.alpha_k, torch.float32, n, "alpha_k")
+            if self.ellipse is None or self.ellipse.dtype != torch.float32 or not self.ellipse.is_contiguous() \
+                    or tuple(self.ellipse.shape) != (RS_ELLIPSE_WORDS, max(n, 1)):
+                raise ValueError(f"ellipse: want a contiguous float32 [{RS_ELLIPSE_WORDS}, {max(n, 1)}] tensor")
+            s.d_ellipse = ctypes.c_void_p(self.ellipse.data_ptr())
         return s
 
 

@@ -105,13 +105,15 @@ typedef struct rs_projected {
      *    their next step; the skipped tiles hold only alpha < 1/255, so the image, final_T and
      *    the gradients are those of the square test, with fewer entries; n_contrib counts only
      *    the entries each pixel examined.  A splat meeting no tile is culled (radius 0).
-     *    rs_project writes d_alpha_k [n] (k, 0 when culled) and rs_bin reads it. */
-    float* d_alpha_k;
+     *    rs_project writes d_ellipse [RS_ELLIPSE_WORDS][n]: row 0 is k (0 when culled), rows
+     *    1.. the test's per-splat setup that rs_bin reads (contents otherwise unspecified). */
+    float* d_ellipse;
     int32_t tile_test;
 } rs_projected;
 
 #define RS_TILE_TEST_SQUARE 0
 #define RS_TILE_TEST_ELLIPSE 1
+#define RS_ELLIPSE_WORDS 12
 
 /* Human-readable text for a return code; never NULL. */
 const char* rs_error_string(int code);

@@ -661,18 +661,19 @@ void view_dir(const Cam<double>& cam, const double* m, double* d) {
 // A tile row's band of pixel centres y in [16 ty, 16 ty + 15] meets it in an x-interval; the
 // leftmost point of the ellipse (x = -sqrt(C k / det) at dy = B sqrt(k / (det C))) bounds it
 // when it lies in the band, else the band edge nearer to it does, where the boundary is
-// x = (-B dy - sqrt(A k - det dy^2)) / A; likewise on the right.  Widened by 0.01 px.  Every step
-// is one IEEE single-precision operation (this file is built without contraction), the same
+// x = -(B/A) dy - sqrt(A k - det dy^2) / A (1/A, B/A and A k formed once per splat); likewise on
+// the right.  Widened by 0.01 px.  Every step is one IEEE single-precision operation (this file
+// is built without contraction; divisions and square roots are correctly rounded), the same
 // sequence as the kernels' test, so both take identical integer decisions.
 struct EllipseF {
-    float u, v, A, B, C, k, det, eyc, ex, dyl;
+    float u, v, nb, inva, ak, det, eyc, ex, dyl;
     int ylo, yhi, xl, xh;
 };
 
 // rect: the radius square's tile span {xl, xh, yl, yh} (half-open); the test keeps a subset of it.
 static bool ellipse_init(float u, float v, float A, float B, float C, float k, const int* rect, int TY,
                          EllipseF& e) {
-    e.u = u; e.v = v; e.A = A; e.B = B; e.C = C; e.k = k;
+    e.u = u; e.v = v;
     e.xl = rect[0];
     e.xh = rect[1];
     e.ylo = 0; e.yhi = -1;
@@ -680,14 +681,17 @@ static bool ellipse_init(float u, float v, float A, float B, float C, float k, c
     const float ac = A * C, bb = B * B;
     e.det = ac - bb;
     if (!(e.det > 0.f)) return false;
-    const float ak = A * k, ck = C * k, dc = e.det * C;
-    e.eyc = std::sqrt(ak / e.det);
+    e.inva = 1.f / A;
+    e.nb = B * e.inva;
+    e.ak = A * k;
+    const float ck = C * k, dc = e.det * C;
+    e.eyc = std::sqrt(e.ak / e.det);
     e.ex = std::sqrt(ck / e.det);
     e.dyl = B * std::sqrt(k / dc);
     const float ey = e.eyc + 0.01f;
     const float vl = v - ey;
-    float lo = std::ceil((vl - 15.f) / 16.f);
-    float hi = std::floor((v + ey) / 16.f);
+    float lo = std::ceil((vl - 15.f) * 0.0625f);
+    float hi = std::floor((v + ey) * 0.0625f);
     lo = std::fmin(std::fmax(lo, 0.f), float(TY));
     hi = std::fmax(std::fmin(hi, float(TY - 1)), -1.f);
     e.ylo = std::max(int(lo), rect[2]);
@@ -695,24 +699,24 @@ static bool ellipse_init(float u, float v, float A, float B, float C, float k, c
     return e.ylo <= e.yhi;
 }
 
-static float ellipse_x(const EllipseF& e, float dy, float sign) {
-    const float ak = e.A * e.k, dy2 = dy * dy, ddy = e.det * dy2;
-    const float t = ak - ddy;
-    const float sq = std::sqrt(std::fmax(t, 0.f));
-    const float bd = e.B * dy;
-    return (-bd + sign * sq) / e.A;
+// half-width of the ellipse at height dy: sqrt(A k - det dy^2) / A
+static float ellipse_half(const EllipseF& e, float dy) {
+    const float dy2 = dy * dy, ddy = e.det * dy2;
+    const float t = e.ak - ddy;
+    return std::sqrt(std::fmax(t, 0.f)) * e.inva;
 }
 
 static void ellipse_row(const EllipseF& e, int ty, int TX, int& xlo, int& xhi) {
     const float y0 = std::fmin(std::fmax(float(16 * ty) - e.v, -e.eyc), e.eyc);
     const float y1 = std::fmin(std::fmax(float(16 * ty + 15) - e.v, -e.eyc), e.eyc);
-    const float xmin = (y0 <= e.dyl && e.dyl <= y1) ? -e.ex
-                                                     : std::fmin(ellipse_x(e, y0, -1.f), ellipse_x(e, y1, -1.f));
+    const float c0 = -(e.nb * y0), c1 = -(e.nb * y1);
+    const float h0 = ellipse_half(e, y0), h1 = ellipse_half(e, y1);
+    const float xmin = (y0 <= e.dyl && e.dyl <= y1) ? -e.ex : std::fmin(c0 - h0, c1 - h1);
     const float dyr = -e.dyl;
-    const float xmax = (y0 <= dyr && dyr <= y1) ? e.ex : std::fmax(ellipse_x(e, y0, 1.f), ellipse_x(e, y1, 1.f));
+    const float xmax = (y0 <= dyr && dyr <= y1) ? e.ex : std::fmax(c0 + h0, c1 + h1);
     const float ul = e.u + xmin, ur = e.u + xmax;
-    float lo = std::ceil((ul - 15.01f) / 16.f);
-    float hi = std::floor((ur + 0.01f) / 16.f);
+    float lo = std::ceil((ul - 15.01f) * 0.0625f);
+    float hi = std::floor((ur + 0.01f) * 0.0625f);
     lo = std::fmin(std::fmax(lo, 0.f), float(TX));
     hi = std::fmax(std::fmin(hi, float(TX - 1)), -1.f);
     xlo = std::max(int(lo), e.xl);

@@ -21,6 +21,19 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_header_constants_match_the_binding():
+    """Every #define of include/rs.h that the binding mirrors has the same value there."""
+    import pathlib
+    import re
+    text = (pathlib.Path(__file__).resolve().parents[1] / "include" / "rs.h").read_text()
+    defs = {m.group(1): int(m.group(2)) for m in re.finditer(r"^#define (RS_\w+) \(?(-?\d+)\)?", text, re.M)}
+    mirrored = [k for k in defs if hasattr(rs, k)]
+    assert {"RS_OK", "RS_ERR_CAPACITY", "RS_TILE_TEST_SQUARE", "RS_TILE_TEST_ELLIPSE", "RS_ELLIPSE_WORDS",
+            "RS_ACT_EXP", "RS_ADAM_MAX_SEGMENTS"} <= set(mirrored)
+    for k in mirrored:
+        assert getattr(rs, k) == defs[k], k
+
+
 def test_error_strings(L):
     for code in (0, -1, -2, -3, -4, 7):
         assert rs.error_string(code)
