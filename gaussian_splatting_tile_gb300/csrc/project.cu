@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
     Record r;
     r.p = make_float4(G.u, G.v, o, ext_x);
     r.q = make_float4(-0.5f * kLog2e * G.A, -kLog2e * G.B, -0.5f * kLog2e * G.C, ext_y);
-    r.c = make_float4(rgb[0], rgb[1], rgb[2], 0.f);
+    r.c = make_float4(rgb[0], rgb[1], rgb[2], 1.0f / o);
     rec[i] = r;
 }
 

@@ -22,6 +22,8 @@ namespace rs {
 namespace {
 
 constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per thread
+constexpr uint32_t kChunk = RS_RASTER_CHUNK;  // backward task length and checkpoint spacing
+static_assert(kChunk == uint32_t(kBatch), "a forward batch ends at every chunk boundary");
 constexpr int kWarps = kTilePixels / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -31,7 +33,7 @@ constexpr unsigned kFull = 0xffffffffu;
 #define RS_FWD_MIN_BLOCKS 6
 #endif
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS 8  // blocks of 128 threads
+#define RS_BWD_MIN_BLOCKS 10  // blocks of 128 threads
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -88,7 +90,9 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
                                                            const uint32_t* __restrict__ list,
                                                            float3 bg, float* __restrict__ image,
                                                            float* __restrict__ final_T,
-                                                           uint32_t* __restrict__ n_contrib) {
+                                                           uint32_t* __restrict__ n_contrib,
+                                                           uint32_t* __restrict__ chunk_tile,
+                                                           float4* __restrict__ ckpt, uint32_t slots) {
     __shared__ float4 s_p[kBatch], s_q[kBatch], s_c[kBatch];
     __shared__ uint32_t s_mask[kBatch];
     __shared__ uint8_t s_list[kWarps][kBatch];
@@ -100,16 +104,30 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
     const uint2 range = ranges[tile];
     const float fx = float(px), fy = float(py);
     float T = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
+    float D0 = 0.f, D1 = 0.f, D2 = 0.f;  // colour added since the last chunk boundary
     uint32_t stop = range.y;  // one past the last entry this pixel examined
     bool done = !inside;
     const uint32_t wbit = 1u << warp;
     uint8_t* my_list = s_list[warp];
-    for (uint32_t base = range.x; base < range.y; base += kBatch) {
+    // the tile's list positions that are multiples of the chunk size are the backward's task
+    // starts: record which tile holds them
+    for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
+         c += kTilePixels)
+        chunk_tile[c] = uint32_t(tile);
+    const int lidx = (py - ty0) * kTile + (px - tx0);
+    // batches end at the chunk boundaries of the point list; at each boundary inside the list a
+    // pixel still going records T and the colour its previous stretch added
+    for (uint32_t base = range.x, bend; base < range.y; base = bend) {
+        bend = min(range.y, (base / kChunk + 1) * kChunk);
+        if (base != range.x && !done) {
+            if (base / kChunk < slots) ckpt[size_t(base / kChunk) * kTilePixels + lidx] = make_float4(D0, D1, D2, T);
+            D0 = D1 = D2 = 0.f;
+        }
         // every thread reaches this barrier; the block leaves once all 256 pixels are done
         if (__syncthreads_count(done) == kBatch) break;
         const uint32_t e = base + threadIdx.x;
         uint32_t m = 0u;
-        if (e < range.y) {
+        if (e < bend) {
             const Record& r = rec[list[e]];
             s_p[threadIdx.x] = r.p;
             s_q[threadIdx.x] = r.q;
@@ -131,6 +149,9 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
             C0 = fmaf(c.x, w, C0);
             C1 = fmaf(c.y, w, C1);
             C2 = fmaf(c.z, w, C2);
+            D0 = fmaf(c.x, w, D0);
+            D1 = fmaf(c.y, w, D1);
+            D2 = fmaf(c.z, w, D2);
             T = fmaf(-T, alpha, T);
             if (T < kTStop) {
                 done = true;
@@ -146,6 +167,21 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
         image[2 * HW + pix] = fmaf(T, bg.z, C2);
         final_T[pix] = T;
         n_contrib[pix] = stop - range.x;
+        // the backward resumes at each recorded boundary b with the colour behind it,
+        // sum over entries from b on of colour alpha T, plus T bg: summed back to front from the
+        // stretches' own sums (a difference of running totals would lose the small tail)
+        if (stop > range.x) {
+            float b0 = fmaf(T, bg.x, D0), b1 = fmaf(T, bg.y, D1), b2 = fmaf(T, bg.z, D2);
+            for (uint32_t b = ((stop - 1u) / kChunk) * kChunk; b > range.x; b -= kChunk) {
+                if (b / kChunk >= slots) continue;
+                float4& f = ckpt[size_t(b / kChunk) * kTilePixels + lidx];
+                const float4 d = f;
+                f = make_float4(b0, b1, b2, d.w);
+                b0 += d.x;
+                b1 += d.y;
+                b2 += d.z;
+            }
+        }
     }
 }
 
@@ -185,35 +221,41 @@ __device__ __forceinline__ int sum_slot(unsigned lane) {
     return v < 9 ? v : -1;
 }
 
-constexpr int kSums = 9;          // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2, gp, w G_rgb
-constexpr int kAccStride = kBatch + 1;  // padding keeps the nine slots of one entry in nine banks
+constexpr int kSums = 9;  // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2, gp, w G_rgb
 
-// The backward runs 128 threads per tile: warp w owns the 8x8 square at columns (w & 1) * 8 and
-// rows (w >> 1) * 8, and lane l the two pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4) of it.
-// Each warp-level reduction then covers 64 pixels, and the two pixels of a lane share their
-// column, so their nine sums fold before the shuffles.
+// The backward runs one block of 128 threads per task: the entries of one 256-entry chunk of the
+// point list, [256 c, 256 c + 256), which may hold the end of one tile's list and several short
+// lists after it (pieces).  A piece that stops at the chunk's end while its tile's list goes on
+// starts each pixel from the state the forward recorded there, so a long list is walked by as
+// many blocks as it has chunks.  Within a block the four warps are independent: warp w owns the
+// 8x8 square at columns (w & 1) * 8 and rows (w >> 1) * 8 of the piece's tile, and lane l the two
+// pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4) of it.  A warp walks each piece back to
+// front, 32 entries at a time: each lane loads one entry's record and tests the entry's
+// alpha >= 1/255 box against the square; the hits are staged in the warp's own shared-memory
+// slots and evaluated one after another by all 64 pixels.  The two pixels of a lane share their
+// column, so their nine sums fold before one reduce-scatter over the warp, and nine lanes each
+// add one of the sums to the Gaussian's gradient with a global atomic.  There is no block-wide
+// barrier.
 constexpr int kBwdThreads = 128;
 constexpr int kBwdWarps = kBwdThreads / 32;
 
-// Bit w is set when warp w's 8x8 square meets the entry's alpha >= 1/255 box.
-__device__ __forceinline__ uint32_t square_mask(const float4& p, const float4& q, int tx0, int ty0) {
-    if (!(p.w >= 0.f)) return 0u;
-    const float xl = p.x - p.w - float(tx0), xh = p.x + p.w - float(tx0);
-    const float yl = p.y - q.w - float(ty0), yh = p.y + q.w - float(ty0);
-    const bool c0 = xl <= 7.f && xh >= 0.f, c1 = xl <= 15.f && xh >= 8.f;
-    const bool r0 = yl <= 7.f && yh >= 0.f, r1 = yl <= 15.f && yh >= 8.f;
-    return (r0 && c0 ? 1u : 0u) | (r0 && c1 ? 2u : 0u) | (r1 && c0 ? 4u : 0u) | (r1 && c1 ? 8u : 0u);
+// True when the entry's alpha >= 1/255 box meets the 8x8 pixel square with corner (ox, oy).
+__device__ __forceinline__ bool square_hit(const float4& p, const float4& q, float ox, float oy) {
+    if (!(p.w >= 0.f)) return false;
+    const float xl = p.x - p.w - ox, xh = p.x + p.w - ox;
+    const float yl = p.y - q.w - oy, yh = p.y + q.w - oy;
+    return xl <= 7.f && xh >= 0.f && yl <= 7.f && yh >= 0.f;
 }
 
 // Per-pixel state of the reverse walk.
 struct BwdPixel {
     float T, SG, G0, G1, G2;
-    uint32_t end;  // one past the last entry the pixel examined
+    uint32_t end;  // one past the last entry of the piece the pixel examined
 };
 
 // One entry at one pixel: updates the pixel's state; returns gp = dL/dpower (0 if clamped) and
-// w = alpha T_j, or false if the entry is skipped there.
-__device__ __forceinline__ bool bwd_step(BwdPixel& px, float alpha, float raw, const float4& c, float& gp,
+// w = alpha T_j.
+__device__ __forceinline__ void bwd_step(BwdPixel& px, float alpha, float raw, const float4& c, float& gp,
                                          float& w) {
     const float one_m = 1.f - alpha;
     const float Tj = __fdividef(px.T, one_m);
@@ -223,151 +265,160 @@ __device__ __forceinline__ bool bwd_step(BwdPixel& px, float alpha, float raw, c
     px.SG = fmaf(alpha, cG, one_m * px.SG);
     px.T = Tj;
     gp = raw <= kAlphaMax ? alpha * dalpha : 0.f;  // not clamped: alpha = opacity * exp(power)
-    return true;
 }
 
 __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     CameraF cam, int n, const Record* __restrict__ rec, const uint2* __restrict__ ranges,
-    const uint32_t* __restrict__ list, float3 bg, const float* __restrict__ final_T,
-    const uint32_t* __restrict__ n_contrib, const float* __restrict__ dL_dimage,
-    float* __restrict__ dm2, float* __restrict__ dcon, float* __restrict__ dop,
-    float* __restrict__ dcol) {
-    __shared__ float4 s_p[kBatch], s_q[kBatch], s_c[kBatch];
-    __shared__ uint32_t s_g[kBatch];
-    __shared__ uint8_t s_mask[kBatch];
-    __shared__ uint8_t s_list[kBwdWarps][kBatch];
-    __shared__ float s_acc[kSums * kAccStride];
-    __shared__ uint32_t s_wmax[kBwdWarps];
-    const int tile = blockIdx.x;
+    const uint32_t* __restrict__ list, float3 bg,
+    const float* __restrict__ final_T, const uint32_t* __restrict__ n_contrib,
+    const uint32_t* __restrict__ chunk_tile, const float4* __restrict__ ckpt, uint32_t slots,
+    const float* __restrict__ dL_dimage, float* __restrict__ dm2, float* __restrict__ dcon,
+    float* __restrict__ dop, float* __restrict__ dcol) {
+    __shared__ float4 s_p[kBwdWarps][32], s_q[kBwdWarps][32], s_c[kBwdWarps][32];
+    __shared__ uint32_t s_g[kBwdWarps][32];
+    const uint32_t n_tiles = uint32_t(cam.TX) * uint32_t(cam.TY);
+    const uint32_t a0 = blockIdx.x * kChunk, a1 = a0 + kChunk;
+    // the tile holding position a0; a chunk past the end of the list has none
+    uint32_t tile = chunk_tile[blockIdx.x];
+    if (tile >= n_tiles) return;
+    uint2 range = ranges[tile];
+    if (!(range.x <= a0 && a0 < range.y)) return;
     const int warp = threadIdx.x >> 5;
     const unsigned lane = threadIdx.x & 31;
-    const int tx0 = (tile % cam.TX) * kTile, ty0 = (tile / cam.TX) * kTile;
-    const int px = tx0 + (warp & 1) * 8 + int(lane & 7);
-    const int py0 = ty0 + (warp >> 1) * 8 + int(lane >> 3);
-    const uint2 range = ranges[tile];
-    const uint32_t len = range.y - range.x;
     const size_t HW = size_t(cam.W) * cam.H;
-    BwdPixel P[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int py = py0 + 4 * h;
-        const bool inside = px < cam.W && py < cam.H;
-        const size_t pix = inside ? size_t(py) * cam.W + px : 0;
-        // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the min()
-        // keeps inconsistent caller data inside the tile's list
-        P[h].end = range.x + (inside ? min(n_contrib[pix], len) : 0u);
-        P[h].T = inside ? final_T[pix] : 1.f;
-        P[h].G0 = inside ? dL_dimage[pix] : 0.f;
-        P[h].G1 = inside ? dL_dimage[HW + pix] : 0.f;
-        P[h].G2 = inside ? dL_dimage[2 * HW + pix] : 0.f;
-        // the colour behind an entry (per unit T) only enters the gradient through its dot
-        // product with dL/dC, so that scalar is carried instead of the colour
-        P[h].SG = bg.x * P[h].G0 + bg.y * P[h].G1 + bg.z * P[h].G2;
-    }
-    for (int i = threadIdx.x; i < kSums * kAccStride; i += kBwdThreads) s_acc[i] = 0.f;
-    const uint32_t warp_end = __reduce_max_sync(kFull, max(P[0].end, P[1].end));
-    if (lane == 0) s_wmax[warp] = warp_end;
-    __syncthreads();
-    uint32_t walk_end = s_wmax[0];
-#pragma unroll
-    for (int w = 1; w < kBwdWarps; ++w) walk_end = max(walk_end, s_wmax[w]);
-    const float fx = float(px), fy0 = float(py0), fy1 = float(py0 + 4);
-    const uint32_t wbit = 1u << warp;
+    // the sum this lane holds after the reduce-scatter, and where it goes:
+    //   du = A sum(gp dx) + B sum(gp dy), dv = B sum(gp dx) + C sum(gp dy),
+    //   dA = -sum(gp dx^2)/2, dB = -sum(gp dx dy), dC = -sum(gp dy^2)/2,
+    //   dopacity = sum(gp)/opacity (gp = opacity exp(power) dL/dalpha), dcolour = sum(w G)
+    // (the record holds the conic scaled by -log2(e)/2 and -log2(e), and 1/opacity)
     const int slot = sum_slot(lane);
-    uint8_t* my_list = s_list[warp];
-    for (uint32_t batch_end = walk_end; batch_end > range.x;) {
-        const uint32_t batch_start = batch_end - range.x > uint32_t(kBatch) ? batch_end - kBatch : range.x;
-        const int cnt = int(batch_end - batch_start);
+    const size_t N = size_t(n);
+    float* const dst = slot == 0 ? dm2 : slot == 1 ? dm2 + N : slot == 2 ? dcon : slot == 3 ? dcon + N
+                     : slot == 4 ? dcon + 2 * N : slot == 5 ? dop : slot >= 6 ? dcol + size_t(slot - 6) * N : dm2;
+    const float kconst = slot == 2 || slot == 4 ? -0.5f : slot == 3 ? -1.f : 1.f;
+    constexpr float kLn2 = 0.6931471805599453f;
+    uint32_t pa = a0;
+    while (true) {
+        // the piece [pa, pb) of this tile's list
+        const uint32_t pb = min(range.y, a1);
+        const int tx0 = int(tile % uint32_t(cam.TX)) * kTile, ty0 = int(tile / uint32_t(cam.TX)) * kTile;
+        const int sx = tx0 + (warp & 1) * 8, sy = ty0 + (warp >> 1) * 8;
+        const int px = sx + int(lane & 7);
+        const int py0 = sy + int(lane >> 3);
+        const uint32_t len = range.y - range.x;
+        BwdPixel P[2];
 #pragma unroll
-        for (int r = 0; r < kBatch / kBwdThreads; ++r) {
-            const int t = r * kBwdThreads + int(threadIdx.x);
-            uint32_t m = 0u;
-            if (t < cnt) {
-                const uint32_t g = list[batch_start + t];
-                const Record& rr = rec[g];
-                s_g[t] = g;
-                s_p[t] = rr.p;
-                s_q[t] = rr.q;
-                s_c[t] = rr.c;
-                m = square_mask(rr.p, rr.q, tx0, ty0);
-            }
-            s_mask[t] = uint8_t(m);
-        }
-        __syncthreads();
-        const int nl = compact_warp(my_list, [&](int j) {
-            return (s_mask[j] & wbit) != 0u && batch_start + uint32_t(j) < warp_end;
-        });
-        for (int k = nl - 1; k >= 0; --k) {
-            const int j = my_list[k];
-            const uint32_t e = batch_start + uint32_t(j);
-            const float4 p = s_p[j], q = s_q[j];
-            float dx, dy0, dy1, G, raw0, raw1;
-            const float a0 = entry_alpha(p, q, fx, fy0, dx, dy0, G, raw0);
-            const float a1 = entry_alpha(p, q, fx, fy1, dx, dy1, G, raw1);
-            const bool act0 = e < P[0].end && a0 >= kAlphaMin;
-            const bool act1 = e < P[1].end && a1 >= kAlphaMin;
-            float gp0 = 0.f, gp1 = 0.f, w0 = 0.f, w1 = 0.f;
-            if (act0 || act1) {
-                const float4 c = s_c[j];
-                if (act0) bwd_step(P[0], a0, raw0, c, gp0, w0);
-                if (act1) bwd_step(P[1], a1, raw1, c, gp1, w1);
-            }
-            if (__any_sync(kFull, act0 || act1)) {
-                // the two pixels share dx: fold their sums, then reduce over the warp
-                const float sg = gp0 + gp1;
-                const float sgy = fmaf(gp1, dy1, gp0 * dy0);
-                float v[kSums];
-                v[0] = sg * dx;
-                v[1] = sgy;
-                v[2] = v[0] * dx;
-                v[3] = sgy * dx;
-                v[4] = fmaf(gp1 * dy1, dy1, (gp0 * dy0) * dy0);
-                v[5] = sg;
-                v[6] = fmaf(w1, P[1].G0, w0 * P[0].G0);
-                v[7] = fmaf(w1, P[1].G1, w0 * P[0].G1);
-                v[8] = fmaf(w1, P[1].G2, w0 * P[0].G2);
-                const float sum = butterfly9(v, lane);
-                if (slot >= 0) atomicAdd(&s_acc[slot * kAccStride + j], sum);
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < kBatch / kBwdThreads; ++r) {
-            const int t = r * kBwdThreads + int(threadIdx.x);
-            if (t < cnt) {
-                // per-entry tile sums -> gradients of the entry's Gaussian:
-                //   du = A sum(gp dx) + B sum(gp dy), dv = B sum(gp dx) + C sum(gp dy),
-                //   dA = -sum(gp dx^2)/2, dB = -sum(gp dx dy), dC = -sum(gp dy^2)/2,
-                //   dopacity = sum(gp)/opacity (gp = opacity exp(power) dL/dalpha),
-                //   dcolour = sum(w G)
-                float a[kSums];
-                bool any = false;
-#pragma unroll
-                for (int k = 0; k < kSums; ++k) {
-                    a[k] = s_acc[k * kAccStride + t];
-                    s_acc[k * kAccStride + t] = 0.f;
-                    any |= a[k] != 0.f;
-                }
-                if (any) {
-                    const uint32_t g = s_g[t];
-                    const size_t N = size_t(n);
-                    const float4 p = s_p[t], q = s_q[t];
-                    constexpr float kLn2 = 0.6931471805599453f;
-                    const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
-                    atomicAdd(dm2 + g, fmaf(A, a[0], B * a[1]));
-                    atomicAdd(dm2 + N + g, fmaf(B, a[0], C * a[1]));
-                    atomicAdd(dcon + g, -0.5f * a[2]);
-                    atomicAdd(dcon + N + g, -a[3]);
-                    atomicAdd(dcon + 2 * N + g, -0.5f * a[4]);
-                    atomicAdd(dop + g, a[5] / p.z);
-                    atomicAdd(dcol + g, a[6]);
-                    atomicAdd(dcol + N + g, a[7]);
-                    atomicAdd(dcol + 2 * N + g, a[8]);
+        for (int h = 0; h < 2; ++h) {
+            const int py = py0 + 4 * h;
+            const bool inside = px < cam.W && py < cam.H;
+            const size_t pix = inside ? size_t(py) * cam.W + px : 0;
+            // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the
+            // min() keeps inconsistent caller data inside the tile's list
+            const uint32_t end = range.x + (inside ? min(n_contrib[pix], len) : 0u);
+            P[h].end = min(end, pb);
+            P[h].G0 = P[h].G1 = P[h].G2 = 0.f;
+            P[h].T = 1.f;
+            P[h].SG = 0.f;
+            if (end > pa) {
+                P[h].G0 = dL_dimage[pix];
+                P[h].G1 = dL_dimage[HW + pix];
+                P[h].G2 = dL_dimage[2 * HW + pix];
+                const uint32_t ck = pb / kChunk;
+                if (end > pb && ck < slots) {
+                    // the pixel goes on past the chunk: resume from the forward's state at pb,
+                    // (colour behind pb, T); the colour behind per unit T enters as its dot
+                    // product with dL/dC
+                    const float4 f = ckpt[size_t(ck) * kTilePixels + (py - ty0) * kTile + (px - tx0)];
+                    P[h].T = f.w;
+                    P[h].SG = __fdividef(fmaf(P[h].G0, f.x, fmaf(P[h].G1, f.y, P[h].G2 * f.z)), f.w);
+                } else {
+                    // the colour behind an entry (per unit T) only enters the gradient through
+                    // its dot product with dL/dC, so that scalar is carried instead of the colour
+                    P[h].T = final_T[pix];
+                    P[h].SG = bg.x * P[h].G0 + bg.y * P[h].G1 + bg.z * P[h].G2;
                 }
             }
         }
-        __syncthreads();
-        batch_end = batch_start;
+        const uint32_t warp_end = __reduce_max_sync(kFull, max(P[0].end, P[1].end));
+        const float fx = float(px), fy0 = float(py0), fy1 = float(py0 + 4);
+        const float ox = float(sx), oy = float(sy);
+        for (uint32_t hi = warp_end; hi > pa;) {
+            const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
+            const uint32_t e = lo + lane;
+            bool hit = false;
+            if (e < hi) {
+                const uint32_t g = list[e];
+                const Record& r = rec[g];
+                const float4 p = r.p, q = r.q, c = r.c;
+                hit = square_hit(p, q, ox, oy);
+                if (hit) {
+                    s_p[warp][lane] = p;
+                    s_q[warp][lane] = q;
+                    s_c[warp][lane] = c;
+                    s_g[warp][lane] = g;
+                }
+            }
+            uint32_t m = __ballot_sync(kFull, hit);
+            __syncwarp();
+            while (m) {
+                const int j = 31 - __clz(m);
+                m ^= 1u << j;
+                const uint32_t ej = lo + uint32_t(j);
+                const float4 p = s_p[warp][j], q = s_q[warp][j];
+                float dx, dy0, dy1, G, raw0, raw1;
+                const float al0 = entry_alpha(p, q, fx, fy0, dx, dy0, G, raw0);
+                const float al1 = entry_alpha(p, q, fx, fy1, dx, dy1, G, raw1);
+                const bool act0 = ej < P[0].end && al0 >= kAlphaMin;
+                const bool act1 = ej < P[1].end && al1 >= kAlphaMin;
+                float gp0 = 0.f, gp1 = 0.f, w0 = 0.f, w1 = 0.f;
+                const float4 c = s_c[warp][j];
+                if (act0) bwd_step(P[0], al0, raw0, c, gp0, w0);
+                if (act1) bwd_step(P[1], al1, raw1, c, gp1, w1);
+                if (__any_sync(kFull, act0 || act1)) {
+                    // the two pixels share dx: fold their sums, then reduce over the warp
+                    const float sg = gp0 + gp1;
+                    const float sgy = fmaf(gp1, dy1, gp0 * dy0);
+                    float v[kSums];
+                    v[0] = sg * dx;
+                    v[1] = sgy;
+                    v[2] = v[0] * dx;
+                    v[3] = sgy * dx;
+                    v[4] = fmaf(gp1 * dy1, dy1, (gp0 * dy0) * dy0);
+                    v[5] = sg;
+                    v[6] = fmaf(w1, P[1].G0, w0 * P[0].G0);
+                    v[7] = fmaf(w1, P[1].G1, w0 * P[0].G1);
+                    v[8] = fmaf(w1, P[1].G2, w0 * P[0].G2);
+                    const float sum = butterfly9(v, lane);
+                    const float other = __shfl_xor_sync(kFull, sum, 2);  // slots 0 and 1: lanes 0 and 2
+                    if (slot >= 0) {
+                        const float B = -kLn2 * q.y;
+                        const float a = slot == 0 ? -2.f * kLn2 * q.x : slot == 1 ? -2.f * kLn2 * q.z
+                                      : slot == 5 ? c.w : kconst;
+                        atomicAdd(dst + s_g[warp][j], fmaf(a, sum, slot < 2 ? B * other : 0.f));
+                    }
+                }
+            }
+            __syncwarp();  // the slots are read before the next batch overwrites them
+            hi = lo;
+        }
+        if (pb >= a1) break;
+        // this tile's list ended inside the chunk: the next non-empty list starts at pb (unless
+        // pb is the end of the point list)
+        uint32_t next = n_tiles;
+        for (uint32_t u = tile + 1; u < n_tiles; u += 32) {
+            const uint32_t t = u + lane;
+            const uint2 r = t < n_tiles ? ranges[t] : make_uint2(0u, 0u);
+            const uint32_t b = __ballot_sync(kFull, r.y > r.x);
+            if (b) {
+                next = u + uint32_t(__ffs(b) - 1);
+                break;
+            }
+        }
+        if (next >= n_tiles) break;
+        tile = next;
+        range = ranges[tile];
+        if (range.x != pb) break;
+        pa = pb;
     }
 }
 
@@ -399,24 +450,48 @@ __global__ void k_zero4(ZeroSpans z) {
 
 }  // namespace
 
+size_t raster_workspace_bytes(size_t capacity) {
+    const size_t slots = capacity / kChunk + 1;
+    return ((slots * sizeof(uint32_t) + 255) & ~size_t(255)) + slots * kTilePixels * sizeof(float4);
+}
+
+namespace {
+struct RasterWs {
+    uint32_t* chunk_tile;
+    float4* ckpt;
+    uint32_t slots;
+};
+RasterWs raster_ws(void* ws, size_t capacity) {
+    const size_t slots = capacity / kChunk + 1;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    return RasterWs{reinterpret_cast<uint32_t*>(b),
+                    reinterpret_cast<float4*>(b + ((slots * sizeof(uint32_t) + 255) & ~size_t(255))),
+                    uint32_t(slots)};
+}
+}  // namespace
+
 cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
-                              const uint32_t* list, float3 bg, float* image, float* final_T,
-                              uint32_t* n_contrib, cudaStream_t s) {
+                              const uint32_t* list, size_t capacity, float3 bg, float* image, float* final_T,
+                              uint32_t* n_contrib, void* ws, cudaStream_t s) {
     const int tiles = cam.TX * cam.TY;
+    const RasterWs w = raster_ws(ws, capacity);
     k_raster_fwd<<<tiles, kTilePixels, 0, s>>>(cam, rec, reinterpret_cast<const uint2*>(ranges), list,
-                                               bg, image, final_T, n_contrib);
+                                               bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots);
     return cudaGetLastError();
 }
 
 cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
-                              const uint32_t* ranges, const uint32_t* list, float3 bg,
-                              const float* final_T, const uint32_t* n_contrib,
-                              const float* dL_dimage, float* dm2, float* dcon, float* dop,
-                              float* dcol, cudaStream_t s) {
-    const int tiles = cam.TX * cam.TY;
-    k_raster_bwd<<<tiles, kBwdThreads, 0, s>>>(cam, n, rec, reinterpret_cast<const uint2*>(ranges),
-                                               list, bg, final_T, n_contrib, dL_dimage, dm2, dcon,
-                                               dop, dcol);
+                              const uint32_t* ranges, const uint32_t* list, size_t capacity, float3 bg,
+                              const float* final_T, const uint32_t* n_contrib, const void* ws,
+                              const float* dL_dimage, float* dm2, float* dcon, float* dop, float* dcol,
+                              cudaStream_t s) {
+    const RasterWs w = raster_ws(const_cast<void*>(ws), capacity);
+    // one block per chunk of the capacity; chunks past the list's end return at once
+    const unsigned blocks = unsigned((capacity + kChunk - 1) / kChunk);
+    if (blocks == 0) return cudaSuccess;
+    k_raster_bwd<<<blocks, kBwdThreads, 0, s>>>(cam, n, rec, reinterpret_cast<const uint2*>(ranges), list, bg,
+                                                final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
+                                                dL_dimage, dm2, dcon, dop, dcol);
     return cudaGetLastError();
 }
 

@@ -158,10 +158,16 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
     return cuda_rc(cudaMemcpyAsync(h_result, dev, 2 * sizeof(uint64_t), cudaMemcpyDeviceToHost, s));
 }
 
+size_t rs_raster_workspace_size(size_t capacity) {
+    if (capacity > size_t(RS_MAX_ENTRIES)) return 0;
+    return rs::raster_workspace_bytes(capacity);
+}
+
 int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
-                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
-                     float* d_image, float* d_final_T, uint32_t* d_n_contrib, void* stream) {
-    if (!camera_ok(camera) || !n_ok(n) || !bg) return RS_ERR_INVALID_ARG;
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
+                     const float* bg, float* d_image, float* d_final_T, uint32_t* d_n_contrib,
+                     void* d_workspace, size_t workspace_bytes, void* stream) {
+    if (!camera_ok(camera) || !n_ok(n) || !bg || capacity > size_t(RS_MAX_ENTRIES)) return RS_ERR_INVALID_ARG;
     if (!dev_f(d_image) || !dev_f(d_final_T) || !dev_f(d_n_contrib)) return RS_ERR_INVALID_ARG;
     const CameraF cam = rs::make_camera(*camera);
     const float3 b = make_float3(bg[0], bg[1], bg[2]);
@@ -169,23 +175,28 @@ int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t 
     if (n == 0) return cuda_rc(rs::launch_fill_background(cam, b, d_image, d_final_T, d_n_contrib, s));
     if (!proj || !proj->d_records || !aligned(proj->d_records, 16)) return RS_ERR_INVALID_ARG;
     if (!d_tile_ranges || !aligned(d_tile_ranges, 8) || !dev_f(d_point_list)) return RS_ERR_INVALID_ARG;
+    if (!d_workspace || !aligned(d_workspace, 16)) return RS_ERR_INVALID_ARG;
+    if (workspace_bytes < rs::raster_workspace_bytes(capacity)) return RS_ERR_WORKSPACE;
     return cuda_rc(rs::launch_raster_fwd(cam, static_cast<const rs::Record*>(proj->d_records),
-                                         d_tile_ranges, d_point_list, b, d_image, d_final_T,
-                                         d_n_contrib, s));
+                                         d_tile_ranges, d_point_list, capacity, b, d_image, d_final_T,
+                                         d_n_contrib, d_workspace, s));
 }
 
 int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
-                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
-                     const float* d_final_T, const uint32_t* d_n_contrib,
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
+                     const float* bg, const float* d_final_T, const uint32_t* d_n_contrib,
+                     const void* d_workspace, size_t workspace_bytes,
                      const float* d_dL_dimage, float* d_dL_dmeans2d, float* d_dL_dconic,
                      float* d_dL_dopacity, float* d_dL_dcolor, void* stream) {
-    if (!camera_ok(camera) || !n_ok(n) || !bg) return RS_ERR_INVALID_ARG;
+    if (!camera_ok(camera) || !n_ok(n) || !bg || capacity > size_t(RS_MAX_ENTRIES)) return RS_ERR_INVALID_ARG;
     if (n == 0) return RS_OK;
     if (!proj || !proj->d_records || !aligned(proj->d_records, 16)) return RS_ERR_INVALID_ARG;
     if (!d_tile_ranges || !aligned(d_tile_ranges, 8) || !dev_f(d_point_list)) return RS_ERR_INVALID_ARG;
     if (!dev_f(d_final_T) || !dev_f(d_n_contrib) || !dev_f(d_dL_dimage)) return RS_ERR_INVALID_ARG;
     if (!dev_f(d_dL_dmeans2d) || !dev_f(d_dL_dconic) || !dev_f(d_dL_dopacity) || !dev_f(d_dL_dcolor))
         return RS_ERR_INVALID_ARG;
+    if (!d_workspace || !aligned(d_workspace, 16)) return RS_ERR_INVALID_ARG;
+    if (workspace_bytes < rs::raster_workspace_bytes(capacity)) return RS_ERR_WORKSPACE;
     const CameraF cam = rs::make_camera(*camera);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (rs::launch_zero_grads(d_dL_dmeans2d, d_dL_dconic, d_dL_dopacity, d_dL_dcolor, size_t(n), s) !=
@@ -193,9 +204,9 @@ int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t 
         return RS_ERR_CUDA;
     const float3 b = make_float3(bg[0], bg[1], bg[2]);
     return cuda_rc(rs::launch_raster_bwd(cam, n, static_cast<const rs::Record*>(proj->d_records),
-                                         d_tile_ranges, d_point_list, b, d_final_T, d_n_contrib,
-                                         d_dL_dimage, d_dL_dmeans2d, d_dL_dconic, d_dL_dopacity,
-                                         d_dL_dcolor, s));
+                                         d_tile_ranges, d_point_list, capacity, b, d_final_T,
+                                         d_n_contrib, d_workspace, d_dL_dimage, d_dL_dmeans2d, d_dL_dconic,
+                                         d_dL_dopacity, d_dL_dcolor, s));
 }
 
 int rs_project_bwd(const rs_camera* camera, const rs_gaussians* gaussians,

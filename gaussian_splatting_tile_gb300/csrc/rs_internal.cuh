@@ -30,7 +30,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 //   q = (qa, qb, qc, ext_y)       power in log2 units: power2 = qa dx^2 + qb dx dy + qc dy^2
 //                                 with qa = -A/2 log2(e), qb = -B log2(e), qc = -C/2 log2(e);
 //                                 half-height of the alpha >= 1/255 region
-//   c = (r, g, b, 0)              colour
+//   c = (r, g, b, 1/opacity)      colour; the reciprocal for the opacity gradient
 // Storing the log2-scaled quadratic lets the rasterisers evaluate exp(power) as one ex2 on the
 // multi-function unit; forward and backward read the same words, so both evaluate alpha with
 // bit-identical arithmetic.  The extents (negative: never reaches 1/255) let a warp skip entries
@@ -213,14 +213,16 @@ BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity);
 cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_projected& p, uint8_t* ws,
                        uint64_t* keys_out, uint32_t* point_list, uint32_t* tile_ranges, cudaStream_t s);
 
+// Compositing workspace: chunk -> tile map and the forward's per-pixel state at chunk boundaries.
+size_t raster_workspace_bytes(size_t capacity);
 cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
-                              const uint32_t* list, float3 bg, float* image, float* final_T,
-                              uint32_t* n_contrib, cudaStream_t s);
+                              const uint32_t* list, size_t capacity, float3 bg, float* image, float* final_T,
+                              uint32_t* n_contrib, void* ws, cudaStream_t s);
 cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
-                              const uint32_t* ranges, const uint32_t* list, float3 bg,
-                              const float* final_T, const uint32_t* n_contrib,
-                              const float* dL_dimage, float* dm2, float* dcon, float* dop,
-                              float* dcol, cudaStream_t s);
+                              const uint32_t* ranges, const uint32_t* list, size_t capacity, float3 bg,
+                              const float* final_T, const uint32_t* n_contrib, const void* ws,
+                              const float* dL_dimage, float* dm2, float* dcon, float* dop, float* dcol,
+                              cudaStream_t s);
 // Fill a background image (n = 0 or no entries): image = bg, final_T = 1, n_contrib = 0.
 cudaError_t launch_fill_background(const CameraF& cam, float3 bg, float* image, float* final_T,
                                    uint32_t* n_contrib, cudaStream_t s);

@@ -64,6 +64,8 @@ class Renderer:
         ws = rs.rs_bin_workspace_size(self.n, self.camera, self.capacity)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
         self.point_list = torch.empty(max(self.capacity, 1), dtype=torch.int32, device=self.device)
+        self.raster_ws = torch.empty(rs.rs_raster_workspace_size(self.capacity), dtype=torch.uint8,
+                                     device=self.device)
         self.keys_sorted = (torch.empty(max(self.capacity, 1), dtype=torch.int64, device=self.device)
                             if self.keep_keys else None)
 
@@ -97,12 +99,14 @@ class Renderer:
                                            self.workspace.numel(), self.capacity, vp(self.keys_sorted),
                                            vp(self.point_list), vp(self.tile_ranges), ctypes.byref(self._E))),
             fwd=rs.PreparedCall("rs_rasterize_fwd", (cam, ctypes.byref(ps), self.n, vp(self.tile_ranges),
-                                                     vp(self.point_list), bgv, vp(self.image),
-                                                     vp(self.final_T), vp(self.n_contrib))))
+                                                     vp(self.point_list), self.capacity, bgv, vp(self.image),
+                                                     vp(self.final_T), vp(self.n_contrib), vp(self.raster_ws),
+                                                     self.raster_ws.numel())))
         if self.grads is not None:
             gr = self.grads
             calls["rbwd_args"] = (cam, ctypes.byref(ps), self.n, vp(self.tile_ranges), vp(self.point_list),
-                                  bgv, vp(self.final_T), vp(self.n_contrib))
+                                  self.capacity, bgv, vp(self.final_T), vp(self.n_contrib),
+                                  vp(self.raster_ws), self.raster_ws.numel())
             calls["rbwd_out"] = (vp(gr.dmeans2d), vp(gr.dconic), vp(gr.dopacity), vp(gr.dcolor))
             calls["pbwd"] = rs.PreparedCall("rs_project_bwd", (
                 cam, ctypes.byref(gs), ctypes.byref(ps), vp(gr.dmeans2d), vp(gr.dconic), vp(gr.dcolor),

@@ -21,6 +21,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "rs.h")
 
 RS_OK, RS_ERR_INVALID_ARG, RS_ERR_CAPACITY, RS_ERR_WORKSPACE, RS_ERR_CUDA = 0, -1, -2, -3, -4
 RS_ERR_DEVICE_TIMEOUT = -5
+RS_TILE, RS_RECORD_BYTES, RS_MAX_GAUSSIANS, RS_MAX_ENTRIES = 16, 48, 1 << 26, (1 << 30) - 1
 RECORD_BYTES = 48
 TILE = 16
 
@@ -55,6 +56,7 @@ class rs_projected(ctypes.Structure):
 
 RS_TILE_TEST_SQUARE, RS_TILE_TEST_ELLIPSE = 0, 1
 RS_ELLIPSE_WORDS = 12  # rows of the ellipse tile test's per-Gaussian words
+RS_RASTER_CHUNK = 256  # entries per backward task; spacing of the forward's recorded states
 
 
 class rs_mlp(ctypes.Structure):
@@ -108,12 +110,14 @@ def lib():
                                    _VP, ctypes.c_size_t, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP]
         L.rs_bin_noalloc.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
                                      ctypes.c_size_t, _VP, _VP, _VP, ctypes.POINTER(ctypes.c_size_t), _VP]
+        L.rs_raster_workspace_size.argtypes = [ctypes.c_size_t]
+        L.rs_raster_workspace_size.restype = ctypes.c_size_t
         L.rs_rasterize_fwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected),
-                                       ctypes.c_int32, _VP, _VP, ctypes.POINTER(ctypes.c_float),
-                                       _VP, _VP, _VP, _VP]
+                                       ctypes.c_int32, _VP, _VP, ctypes.c_size_t, ctypes.POINTER(ctypes.c_float),
+                                       _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]
         L.rs_rasterize_bwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected),
-                                       ctypes.c_int32, _VP, _VP, ctypes.POINTER(ctypes.c_float),
-                                       _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
+                                       ctypes.c_int32, _VP, _VP, ctypes.c_size_t, ctypes.POINTER(ctypes.c_float),
+                                       _VP, _VP, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]
         L.rs_project_bwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_gaussians),
                                      ctypes.POINTER(rs_projected), _VP, _VP, _VP, _VP, _VP, _VP,
                                      _VP, _VP]
@@ -375,27 +379,36 @@ def _bg(bg):
     return arr
 
 
+def rs_raster_workspace_size(capacity: int) -> int:
+    """Bytes of the compositing workspace for a point list of `capacity` entries."""
+    return int(lib().rs_raster_workspace_size(int(capacity)))
+
+
 def rs_rasterize_fwd(camera, proj: DeviceProjected, n: int, tile_ranges, point_list, bg, image,
-                     final_T, n_contrib, stream=None):
+                     final_T, n_contrib, workspace, stream=None):
     c = camera_struct(camera)
     p = proj.struct()
     HW = camera.width * camera.height
     _check("rs_rasterize_fwd", lib().rs_rasterize_fwd(
         ctypes.byref(c), ctypes.byref(p), int(n), _ptr(tile_ranges, torch.int32, None, "tile_ranges"),
-        _ptr(point_list, torch.int32, None, "point_list"), _bg(bg), _ptr(image, torch.float32, 3 * HW, "image"),
-        _ptr(final_T, torch.float32, HW, "final_T"), _ptr(n_contrib, torch.int32, HW, "n_contrib"),
-        _stream(stream)))
+        _ptr(point_list, torch.int32, None, "point_list"), int(point_list.numel()), _bg(bg),
+        _ptr(image, torch.float32, 3 * HW, "image"), _ptr(final_T, torch.float32, HW, "final_T"),
+        _ptr(n_contrib, torch.int32, HW, "n_contrib"), _ptr(workspace, torch.uint8, None, "workspace"),
+        int(workspace.numel()), _stream(stream)))
 
 
 def rs_rasterize_bwd(camera, proj: DeviceProjected, n: int, tile_ranges, point_list, bg, final_T,
-                     n_contrib, dL_dimage, dL_dmeans2d, dL_dconic, dL_dopacity, dL_dcolor, stream=None):
+                     n_contrib, workspace, dL_dimage, dL_dmeans2d, dL_dconic, dL_dopacity, dL_dcolor,
+                     stream=None):
     c = camera_struct(camera)
     p = proj.struct()
     HW = camera.width * camera.height
     _check("rs_rasterize_bwd", lib().rs_rasterize_bwd(
         ctypes.byref(c), ctypes.byref(p), int(n), _ptr(tile_ranges, torch.int32, None, "tile_ranges"),
-        _ptr(point_list, torch.int32, None, "point_list"), _bg(bg), _ptr(final_T, torch.float32, HW, "final_T"),
-        _ptr(n_contrib, torch.int32, HW, "n_contrib"), _ptr(dL_dimage, torch.float32, 3 * HW, "dL_dimage"),
+        _ptr(point_list, torch.int32, None, "point_list"), int(point_list.numel()), _bg(bg),
+        _ptr(final_T, torch.float32, HW, "final_T"),
+        _ptr(n_contrib, torch.int32, HW, "n_contrib"), _ptr(workspace, torch.uint8, None, "workspace"),
+        int(workspace.numel()), _ptr(dL_dimage, torch.float32, 3 * HW, "dL_dimage"),
         _ptr(dL_dmeans2d, torch.float32, 2 * n, "dL_dmeans2d"), _ptr(dL_dconic, torch.float32, 3 * n, "dL_dconic"),
         _ptr(dL_dopacity, torch.float32, n, "dL_dopacity"), _ptr(dL_dcolor, torch.float32, 3 * n, "dL_dcolor"),
         _stream(stream)))

@@ -172,6 +172,14 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
                  size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,
                  uint32_t* d_point_list, uint32_t* d_tile_ranges, uint64_t* h_result, void* stream);
 
+/* Compositing workspace: the forward's per-pixel state at every RS_RASTER_CHUNK-th position of
+ * the point list that falls inside a tile's list, and which tile holds each such position; the
+ * backward reads both to walk every 256-entry stretch of the point list as a task of its own.
+ * Returns the bytes a point list of `capacity` entries needs; 0 if capacity > RS_MAX_ENTRIES.
+ * Host-only (no GPU work). */
+#define RS_RASTER_CHUNK 256
+size_t rs_raster_workspace_size(size_t capacity);
+
 /* [3] Forward compositing, rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel".
  * One thread block per 16x16 tile; each pixel walks its tile's list front to back:
  * power = -1/2 (A dx^2 + C dy^2) - B dx dy with (dx, dy) = (x - u, y - v),
@@ -179,26 +187,35 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
  * C += colour alpha T, T *= 1 - alpha; the pixel stops after the entry that brings T below 1e-4.
  * image = C + T bg.  n_contrib counts every entry the pixel examined (skipped ones and the one
  * that stopped it included).  bg: host float[3].
+ * capacity: the length of d_point_list (the capacity given to rs_bin).  d_workspace: at least
+ * rs_raster_workspace_size(capacity) bytes of device memory, 16-byte aligned, owned by the
+ * caller; the call fills it for rs_rasterize_bwd (no initial contents needed).
  * Outputs: d_image [3][H][W], d_final_T [H][W], d_n_contrib [H][W] uint32.
- * Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE (workspace too small), RS_ERR_CUDA. */
 int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
-                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
-                     float* d_image, float* d_final_T, uint32_t* d_n_contrib, void* stream);
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
+                     const float* bg, float* d_image, float* d_final_T, uint32_t* d_n_contrib,
+                     void* d_workspace, size_t workspace_bytes, void* stream);
 
 /* [4] Backward of the compositing, rigel README "Backward": each tile's list is walked back to
- * front from final_T, undoing the transmittance one step at a time (T_i = T_{i+1} / (1 - a_i))
- * and carrying the colour behind the current entry; entries past a pixel's n_contrib and
- * skipped entries (alpha < 1/255) give nothing; an entry whose opacity * exp(power) exceeds
- * 0.99 (clamped) passes no gradient to opacity, conic or mean ("Deliberate differences").
- * Per-pixel contributions are reduced across each warp and tile before they reach global memory.
- * Inputs: the forward's tile_ranges, point_list, final_T, n_contrib, bg (host float[3]) and
- * d_dL_dimage [3][H][W].  Outputs (zeroed, then accumulated by the call):
+ * front, undoing the transmittance one step at a time (T_i = T_{i+1} / (1 - a_i)) and carrying
+ * the colour behind the current entry; entries past a pixel's n_contrib and skipped entries
+ * (alpha < 1/255) give nothing; an entry whose opacity * exp(power) exceeds 0.99 (clamped)
+ * passes no gradient to opacity, conic or mean ("Deliberate differences").
+ * The walk is split at every RS_RASTER_CHUNK-th position of the point list: a stretch that ends
+ * inside a tile's list starts from the state the forward recorded there (T, and the colour
+ * behind that position) instead of from final_T, so long lists are walked in parallel.
+ * Per-pixel contributions are reduced across each warp before they reach global memory.
+ * Inputs: the forward's tile_ranges, point_list, capacity, final_T, n_contrib and workspace (as
+ * rs_rasterize_fwd left them), bg (host float[3]) and d_dL_dimage [3][H][W].
+ * Outputs (zeroed, then accumulated by the call):
  * d_dL_dmeans2d [2][n], d_dL_dconic [3][n], d_dL_dopacity [n], d_dL_dcolor [3][n].
  * The accumulation order is not fixed, so results may differ in the last bits between runs.
- * Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CUDA. */
 int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
-                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, const float* bg,
-                     const float* d_final_T, const uint32_t* d_n_contrib,
+                     const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
+                     const float* bg, const float* d_final_T, const uint32_t* d_n_contrib,
+                     const void* d_workspace, size_t workspace_bytes,
                      const float* d_dL_dimage, float* d_dL_dmeans2d, float* d_dL_dconic,
                      float* d_dL_dopacity, float* d_dL_dcolor, void* stream);
 

@@ -73,9 +73,10 @@ def test_invalid_arguments_rejected_before_any_launch(L):
     g.sh_degree = 0
     assert L.rs_project(ctypes.byref(cam), ctypes.byref(g), None, None) == rs.RS_ERR_INVALID_ARG
     bgv = (ctypes.c_float * 3)(0, 0, 0)
-    assert L.rs_rasterize_fwd(ctypes.byref(cam), None, 5, None, None, bgv, None, None, None, None) == rs.RS_ERR_INVALID_ARG
-    assert L.rs_rasterize_bwd(ctypes.byref(cam), None, 5, None, None, bgv, None, None, None, None, None, None,
-                              None, None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_rasterize_fwd(ctypes.byref(cam), None, 5, None, None, 0, bgv, None, None, None, None, 0,
+                              None) == rs.RS_ERR_INVALID_ARG
+    assert L.rs_rasterize_bwd(ctypes.byref(cam), None, 5, None, None, 0, bgv, None, None, None, 0, None,
+                              None, None, None, None, None) == rs.RS_ERR_INVALID_ARG
     E = ctypes.c_size_t(0)
     assert L.rs_bin(ctypes.byref(cam), None, 5, None, 0, 0, None, None, None, ctypes.byref(E), None) == rs.RS_ERR_INVALID_ARG
     # misaligned workspace
@@ -84,6 +85,35 @@ def test_invalid_arguments_rejected_before_any_launch(L):
     # workspace too small (validated on the host, before launches)
     assert L.rs_bin(ctypes.byref(cam), None, 0, ctypes.c_void_p(0x1000), 16, 0, None, None,
                     ctypes.c_void_p(0x2000), ctypes.byref(E), None) == rs.RS_ERR_WORKSPACE
+
+
+def test_raster_workspace_validation(L):
+    """The compositing workspace: one 256-pixel float4 state and one tile index per 256 entries
+    of capacity (plus one); too small or misaligned is refused before any launch."""
+    cam = rs.camera_struct(scenes.procedural_camera(64, 48))
+    chunk = rs.RS_RASTER_CHUNK
+    for cap in (0, 1, 255, 256, 4_000_000):
+        slots = cap // chunk + 1
+        assert rs.rs_raster_workspace_size(cap) >= slots * (chunk * 16 + 4)
+    assert rs.rs_raster_workspace_size(1_000_000) < rs.rs_raster_workspace_size(4_000_000)
+    assert L.rs_raster_workspace_size(rs.RS_MAX_ENTRIES + 1) == 0
+    p = rs.rs_projected()
+    p.d_records = 0x1000
+    bgv = (ctypes.c_float * 3)(0, 0, 0)
+    fake = lambda a: ctypes.c_void_p(a)
+    cap = 10_000
+    need = rs.rs_raster_workspace_size(cap)
+    fwd = lambda ws, nb, c=cap: L.rs_rasterize_fwd(ctypes.byref(cam), ctypes.byref(p), 5, fake(0x2000), fake(0x3000),
+                                                    c, bgv, fake(0x4000), fake(0x5000), fake(0x6000), ws, nb, None)
+    bwd = lambda ws, nb, c=cap: L.rs_rasterize_bwd(ctypes.byref(cam), ctypes.byref(p), 5, fake(0x2000),
+                                                    fake(0x3000), c, bgv, fake(0x5000), fake(0x6000),
+                                                    ws, nb, fake(0x7000), fake(0x8000), fake(0x9000),
+                                                    fake(0xa000), fake(0xb000), None)
+    for call in (fwd, bwd):
+        assert call(fake(0xc000), need - 1) == rs.RS_ERR_WORKSPACE
+        assert call(fake(0xc008), need) == rs.RS_ERR_INVALID_ARG
+        assert call(None, need) == rs.RS_ERR_INVALID_ARG
+        assert call(fake(0xc000), need, rs.RS_MAX_ENTRIES + 1) == rs.RS_ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors(L):
