@@ -173,14 +173,14 @@ def launches_per_step(n: int, E: int, n_tiles: int) -> int:
     """Kernels of this library one forward + backward launches (the D2H read is a copy).
 
     Binning: one clearing kernel; a digit histogram and four 8-bit passes over the Gaussians'
-    depth keys; the scan of their tile counts fused with the expansion into entries (which
+    depth keys; the scan of their tile counts (slices) and the expansion into entries (which
     also counts the tile-id digits); ceil(tile_bits / 8) passes over the entries' tile ids; the
-    tile ranges."""
+    tile ranges.  Forward: the tile order (longest lists first) and the compositing."""
     tile_bits = max(1, math.ceil(math.log2(n_tiles))) if n_tiles > 1 else 1
     tile_passes = math.ceil(tile_bits / 8)
     project = 1
-    binning = 1 + (1 + 4) + 1 + tile_passes + 1
-    fwd = 1
+    binning = 1 + (1 + 4) + 2 + tile_passes + 1
+    fwd = 2
     bwd = 1 + 1 + 1  # zero the gradients, compositing backward, projection backward
     return project + binning + fwd + bwd
 

@@ -33,7 +33,7 @@ constexpr unsigned kFull = 0xffffffffu;
 #define RS_FWD_MIN_BLOCKS 6
 #endif
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS 10  // blocks of 128 threads
+#define RS_BWD_MIN_BLOCKS 8  // blocks of 128 threads
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -85,41 +85,40 @@ __device__ __forceinline__ int compact_warp(uint8_t* list, Hit hit) {
     return n;
 }
 
-__global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
-                                                           const uint2* __restrict__ ranges,
-                                                           const uint32_t* __restrict__ list,
-                                                           float3 bg, float* __restrict__ image,
-                                                           float* __restrict__ final_T,
-                                                           uint32_t* __restrict__ n_contrib,
-                                                           uint32_t* __restrict__ chunk_tile,
-                                                           float4* __restrict__ ckpt, uint32_t slots) {
-    __shared__ float4 s_p[kBatch], s_q[kBatch], s_c[kBatch];
-    __shared__ uint32_t s_mask[kBatch];
-    __shared__ uint8_t s_list[kWarps][kBatch];
-    const int tile = blockIdx.x;
+// Shared staging of the forward: one batch of 256 entries.
+struct FwdSmem {
+    float4 p[kBatch], q[kBatch], c[kBatch];
+    uint32_t mask[kBatch];
+    uint8_t list[kWarps][kBatch];
+};
+
+// The forward of one tile.  SPLIT: the tile's list crosses a chunk boundary of the point list,
+// so each pixel also sums the colour of every stretch between boundaries and records its state
+// there for the backward; other tiles skip that work.
+template <bool SPLIT>
+__device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record* __restrict__ rec, uint32_t tile,
+                                                uint2 range,
+                                                const uint32_t* __restrict__ list, float3 bg,
+                                                float* __restrict__ image, float* __restrict__ final_T,
+                                                uint32_t* __restrict__ n_contrib, float4* __restrict__ ckpt,
+                                                uint32_t slots, FwdSmem& sm) {
     const int warp = threadIdx.x >> 5;
     int tx0, ty0, px, py;
-    tile_pixel(cam, tile, tx0, ty0, px, py);
+    tile_pixel(cam, int(tile), tx0, ty0, px, py);
     const bool inside = px < cam.W && py < cam.H;
-    const uint2 range = ranges[tile];
     const float fx = float(px), fy = float(py);
     float T = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
     float D0 = 0.f, D1 = 0.f, D2 = 0.f;  // colour added since the last chunk boundary
     uint32_t stop = range.y;  // one past the last entry this pixel examined
     bool done = !inside;
     const uint32_t wbit = 1u << warp;
-    uint8_t* my_list = s_list[warp];
-    // the tile's list positions that are multiples of the chunk size are the backward's task
-    // starts: record which tile holds them
-    for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
-         c += kTilePixels)
-        chunk_tile[c] = uint32_t(tile);
+    uint8_t* my_list = sm.list[warp];
     const int lidx = (py - ty0) * kTile + (px - tx0);
     // batches end at the chunk boundaries of the point list; at each boundary inside the list a
     // pixel still going records T and the colour its previous stretch added
     for (uint32_t base = range.x, bend; base < range.y; base = bend) {
         bend = min(range.y, (base / kChunk + 1) * kChunk);
-        if (base != range.x && !done) {
+        if (SPLIT && base != range.x && !done) {
             if (base / kChunk < slots) ckpt[size_t(base / kChunk) * kTilePixels + lidx] = make_float4(D0, D1, D2, T);
             D0 = D1 = D2 = 0.f;
         }
@@ -129,29 +128,31 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
         uint32_t m = 0u;
         if (e < bend) {
             const Record& r = rec[list[e]];
-            s_p[threadIdx.x] = r.p;
-            s_q[threadIdx.x] = r.q;
-            s_c[threadIdx.x] = r.c;
+            sm.p[threadIdx.x] = r.p;
+            sm.q[threadIdx.x] = r.q;
+            sm.c[threadIdx.x] = r.c;
             m = warp_mask(r.p, r.q, tx0, ty0);
         }
-        s_mask[threadIdx.x] = m;
+        sm.mask[threadIdx.x] = m;
         __syncthreads();
         if (__all_sync(kFull, done)) continue;
-        const int nl = compact_warp(my_list, [&](int j) { return (s_mask[j] & wbit) != 0u; });
+        const int nl = compact_warp(my_list, [&](int j) { return (sm.mask[j] & wbit) != 0u; });
         if (done) continue;
         for (int k = 0; k < nl; ++k) {
             const int j = my_list[k];
             float dx, dy, G, raw;
-            const float alpha = entry_alpha(s_p[j], s_q[j], fx, fy, dx, dy, G, raw);
+            const float alpha = entry_alpha(sm.p[j], sm.q[j], fx, fy, dx, dy, G, raw);
             if (alpha < kAlphaMin) continue;
-            const float4 c = s_c[j];
+            const float4 c = sm.c[j];
             const float w = alpha * T;
             C0 = fmaf(c.x, w, C0);
             C1 = fmaf(c.y, w, C1);
             C2 = fmaf(c.z, w, C2);
-            D0 = fmaf(c.x, w, D0);
-            D1 = fmaf(c.y, w, D1);
-            D2 = fmaf(c.z, w, D2);
+            if (SPLIT) {
+                D0 = fmaf(c.x, w, D0);
+                D1 = fmaf(c.y, w, D1);
+                D2 = fmaf(c.z, w, D2);
+            }
             T = fmaf(-T, alpha, T);
             if (T < kTStop) {
                 done = true;
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
         // the backward resumes at each recorded boundary b with the colour behind it,
         // sum over entries from b on of colour alpha T, plus T bg: summed back to front from the
         // stretches' own sums (a difference of running totals would lose the small tail)
-        if (stop > range.x) {
+        if (SPLIT && stop > range.x) {
             float b0 = fmaf(T, bg.x, D0), b1 = fmaf(T, bg.y, D1), b2 = fmaf(T, bg.z, D2);
             for (uint32_t b = ((stop - 1u) / kChunk) * kChunk; b > range.x; b -= kChunk) {
                 if (b / kChunk >= slots) continue;
@@ -183,6 +184,29 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
+                                                           const uint2* __restrict__ ranges,
+                                                           const uint32_t* __restrict__ list,
+                                                           float3 bg, float* __restrict__ image,
+                                                           float* __restrict__ final_T,
+                                                           uint32_t* __restrict__ n_contrib,
+                                                           uint32_t* __restrict__ chunk_tile,
+                                                           float4* __restrict__ ckpt, uint32_t slots,
+                                                           const uint32_t* __restrict__ order) {
+    __shared__ FwdSmem sm;
+    const uint32_t tile = order[blockIdx.x];
+    const uint2 range = ranges[tile];
+    // the tile's list positions that are multiples of the chunk size are the backward's task
+    // starts: record which tile holds them
+    for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
+         c += kTilePixels)
+        chunk_tile[c] = tile;
+    if (range.y > range.x && (range.y - 1u) / kChunk > range.x / kChunk)
+        raster_fwd_tile<true>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, sm);
+    else
+        raster_fwd_tile<false>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, sm);
 }
 
 // Reduce-scatter of nine per-lane values over the warp in five xor-shuffle steps (9 -> 5 -> 3
@@ -450,33 +474,77 @@ __global__ void k_zero4(ZeroSpans z) {
 
 }  // namespace
 
-size_t raster_workspace_bytes(size_t capacity) {
-    const size_t slots = capacity / kChunk + 1;
-    return ((slots * sizeof(uint32_t) + 255) & ~size_t(255)) + slots * kTilePixels * sizeof(float4);
-}
-
 namespace {
 struct RasterWs {
-    uint32_t* chunk_tile;
-    float4* ckpt;
+    uint32_t* chunk_tile;   // [slots] tile holding list position 256 c
+    float4* ckpt;           // [slots][256] the forward's state at position 256 c
+    uint32_t* order;        // [n_tiles] tiles in the forward's order
     uint32_t slots;
 };
-RasterWs raster_ws(void* ws, size_t capacity) {
+size_t align256z(size_t x) { return (x + 255) & ~size_t(255); }
+RasterWs raster_ws(void* ws, size_t capacity, size_t n_tiles, size_t* bytes = nullptr) {
     const size_t slots = capacity / kChunk + 1;
     uint8_t* b = static_cast<uint8_t*>(ws);
-    return RasterWs{reinterpret_cast<uint32_t*>(b),
-                    reinterpret_cast<float4*>(b + ((slots * sizeof(uint32_t) + 255) & ~size_t(255))),
-                    uint32_t(slots)};
+    size_t o = 0;
+    RasterWs w;
+    w.chunk_tile = reinterpret_cast<uint32_t*>(b + o);
+    o = align256z(o + slots * sizeof(uint32_t));
+    w.order = reinterpret_cast<uint32_t*>(b + o);
+    o = align256z(o + n_tiles * sizeof(uint32_t));
+    w.ckpt = reinterpret_cast<float4*>(b + o);
+    o += slots * kTilePixels * sizeof(float4);
+    w.slots = uint32_t(slots);
+    if (bytes) *bytes = o;
+    return w;
+}
+
+// Tiles in decreasing order of list length (by powers of two): the forward's blocks take tiles
+// in this order, so the longest lists start first and the short ones fill in around them (the
+// hardware hands out blocks in index order as earlier ones finish).
+constexpr int kOrderThreads = 1024;
+__global__ void __launch_bounds__(kOrderThreads) k_tile_order(const uint2* __restrict__ ranges, uint32_t n_tiles,
+                                                             uint32_t* __restrict__ order) {
+    __shared__ uint32_t s_cnt[33];
+    if (threadIdx.x < 33) s_cnt[threadIdx.x] = 0u;
+    __syncthreads();
+    for (uint32_t t = threadIdx.x; t < n_tiles; t += kOrderThreads) {
+        const uint2 r = ranges[t];
+        const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
+        atomicAdd(&s_cnt[__clz(len)], 1u);  // bucket 32 - bit length: longest first
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t run = 0u;
+        for (int b = 0; b < 33; ++b) {
+            const uint32_t c = s_cnt[b];
+            s_cnt[b] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (uint32_t t = threadIdx.x; t < n_tiles; t += kOrderThreads) {
+        const uint2 r = ranges[t];
+        const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
+        order[atomicAdd(&s_cnt[__clz(len)], 1u)] = t;
+    }
 }
 }  // namespace
+
+size_t raster_workspace_bytes(size_t capacity, size_t n_tiles) {
+    size_t bytes = 0;
+    raster_ws(nullptr, capacity, n_tiles, &bytes);
+    return bytes;
+}
 
 cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
                               const uint32_t* list, size_t capacity, float3 bg, float* image, float* final_T,
                               uint32_t* n_contrib, void* ws, cudaStream_t s) {
     const int tiles = cam.TX * cam.TY;
-    const RasterWs w = raster_ws(ws, capacity);
+    const RasterWs w = raster_ws(ws, capacity, size_t(tiles));
+    k_tile_order<<<1, kOrderThreads, 0, s>>>(reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order);
     k_raster_fwd<<<tiles, kTilePixels, 0, s>>>(cam, rec, reinterpret_cast<const uint2*>(ranges), list,
-                                               bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots);
+                                               bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
+                                               w.order);
     return cudaGetLastError();
 }
 
@@ -485,7 +553,7 @@ cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
                               const float* final_T, const uint32_t* n_contrib, const void* ws,
                               const float* dL_dimage, float* dm2, float* dcon, float* dop, float* dcol,
                               cudaStream_t s) {
-    const RasterWs w = raster_ws(const_cast<void*>(ws), capacity);
+    const RasterWs w = raster_ws(const_cast<void*>(ws), capacity, size_t(cam.TX) * cam.TY);
     // one block per chunk of the capacity; chunks past the list's end return at once
     const unsigned blocks = unsigned((capacity + kChunk - 1) / kChunk);
     if (blocks == 0) return cudaSuccess;

@@ -158,9 +158,10 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
     return cuda_rc(cudaMemcpyAsync(h_result, dev, 2 * sizeof(uint64_t), cudaMemcpyDeviceToHost, s));
 }
 
-size_t rs_raster_workspace_size(size_t capacity) {
-    if (capacity > size_t(RS_MAX_ENTRIES)) return 0;
-    return rs::raster_workspace_bytes(capacity);
+size_t rs_raster_workspace_size(const rs_camera* camera, size_t capacity) {
+    if (!camera_ok(camera) || capacity > size_t(RS_MAX_ENTRIES)) return 0;
+    const CameraF cam = rs::make_camera(*camera);
+    return rs::raster_workspace_bytes(capacity, size_t(cam.TX) * cam.TY);
 }
 
 int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
@@ -176,7 +177,7 @@ int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t 
     if (!proj || !proj->d_records || !aligned(proj->d_records, 16)) return RS_ERR_INVALID_ARG;
     if (!d_tile_ranges || !aligned(d_tile_ranges, 8) || !dev_f(d_point_list)) return RS_ERR_INVALID_ARG;
     if (!d_workspace || !aligned(d_workspace, 16)) return RS_ERR_INVALID_ARG;
-    if (workspace_bytes < rs::raster_workspace_bytes(capacity)) return RS_ERR_WORKSPACE;
+    if (workspace_bytes < rs::raster_workspace_bytes(capacity, size_t(cam.TX) * cam.TY)) return RS_ERR_WORKSPACE;
     return cuda_rc(rs::launch_raster_fwd(cam, static_cast<const rs::Record*>(proj->d_records),
                                          d_tile_ranges, d_point_list, capacity, b, d_image, d_final_T,
                                          d_n_contrib, d_workspace, s));
@@ -196,8 +197,8 @@ int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t 
     if (!dev_f(d_dL_dmeans2d) || !dev_f(d_dL_dconic) || !dev_f(d_dL_dopacity) || !dev_f(d_dL_dcolor))
         return RS_ERR_INVALID_ARG;
     if (!d_workspace || !aligned(d_workspace, 16)) return RS_ERR_INVALID_ARG;
-    if (workspace_bytes < rs::raster_workspace_bytes(capacity)) return RS_ERR_WORKSPACE;
     const CameraF cam = rs::make_camera(*camera);
+    if (workspace_bytes < rs::raster_workspace_bytes(capacity, size_t(cam.TX) * cam.TY)) return RS_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (rs::launch_zero_grads(d_dL_dmeans2d, d_dL_dconic, d_dL_dopacity, d_dL_dcolor, size_t(n), s) !=
         cudaSuccess)

@@ -214,7 +214,7 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
                        uint64_t* keys_out, uint32_t* point_list, uint32_t* tile_ranges, cudaStream_t s);
 
 // Compositing workspace: chunk -> tile map and the forward's per-pixel state at chunk boundaries.
-size_t raster_workspace_bytes(size_t capacity);
+size_t raster_workspace_bytes(size_t capacity, size_t n_tiles);
 cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
                               const uint32_t* list, size_t capacity, float3 bg, float* image, float* final_T,
                               uint32_t* n_contrib, void* ws, cudaStream_t s);

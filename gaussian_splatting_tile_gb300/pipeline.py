@@ -64,7 +64,7 @@ class Renderer:
         ws = rs.rs_bin_workspace_size(self.n, self.camera, self.capacity)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
         self.point_list = torch.empty(max(self.capacity, 1), dtype=torch.int32, device=self.device)
-        self.raster_ws = torch.empty(rs.rs_raster_workspace_size(self.capacity), dtype=torch.uint8,
+        self.raster_ws = torch.empty(rs.rs_raster_workspace_size(self.camera, self.capacity), dtype=torch.uint8,
                                      device=self.device)
         self.keys_sorted = (torch.empty(max(self.capacity, 1), dtype=torch.int64, device=self.device)
                             if self.keep_keys else None)

@@ -110,7 +110,7 @@ def lib():
                                    _VP, ctypes.c_size_t, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP]
         L.rs_bin_noalloc.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected), ctypes.c_int32,
                                      ctypes.c_size_t, _VP, _VP, _VP, ctypes.POINTER(ctypes.c_size_t), _VP]
-        L.rs_raster_workspace_size.argtypes = [ctypes.c_size_t]
+        L.rs_raster_workspace_size.argtypes = [ctypes.POINTER(rs_camera), ctypes.c_size_t]
         L.rs_raster_workspace_size.restype = ctypes.c_size_t
         L.rs_rasterize_fwd.argtypes = [ctypes.POINTER(rs_camera), ctypes.POINTER(rs_projected),
                                        ctypes.c_int32, _VP, _VP, ctypes.c_size_t, ctypes.POINTER(ctypes.c_float),
@@ -379,9 +379,13 @@ def _bg(bg):
     return arr
 
 
-def rs_raster_workspace_size(capacity: int) -> int:
+def rs_raster_workspace_size(camera, capacity: int) -> int:
     """Bytes of the compositing workspace for a point list of `capacity` entries."""
-    return int(lib().rs_raster_workspace_size(int(capacity)))
+    c = camera_struct(camera)
+    n = int(lib().rs_raster_workspace_size(ctypes.byref(c), int(capacity)))
+    if n == 0:
+        raise ValueError("invalid camera or capacity")
+    return n
 
 
 def rs_rasterize_fwd(camera, proj: DeviceProjected, n: int, tile_ranges, point_list, bg, image,

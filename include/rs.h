@@ -173,12 +173,13 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
                  uint32_t* d_point_list, uint32_t* d_tile_ranges, uint64_t* h_result, void* stream);
 
 /* Compositing workspace: the forward's per-pixel state at every RS_RASTER_CHUNK-th position of
- * the point list that falls inside a tile's list, and which tile holds each such position; the
- * backward reads both to walk every 256-entry stretch of the point list as a task of its own.
- * Returns the bytes a point list of `capacity` entries needs; 0 if capacity > RS_MAX_ENTRIES.
- * Host-only (no GPU work). */
+ * the point list that falls inside a tile's list, and which tile holds each such position (the
+ * backward reads both to walk every 256-entry stretch of the point list as a task of its own);
+ * and the order in which the forward takes the tiles (longest lists first).
+ * Returns the bytes a point list of `capacity` entries needs for this camera's tile grid; 0 for
+ * an invalid camera or capacity > RS_MAX_ENTRIES.  Host-only (no GPU work). */
 #define RS_RASTER_CHUNK 256
-size_t rs_raster_workspace_size(size_t capacity);
+size_t rs_raster_workspace_size(const rs_camera* camera, size_t capacity);
 
 /* [3] Forward compositing, rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel".
  * One thread block per 16x16 tile; each pixel walks its tile's list front to back:
@@ -188,8 +189,8 @@ size_t rs_raster_workspace_size(size_t capacity);
  * image = C + T bg.  n_contrib counts every entry the pixel examined (skipped ones and the one
  * that stopped it included).  bg: host float[3].
  * capacity: the length of d_point_list (the capacity given to rs_bin).  d_workspace: at least
- * rs_raster_workspace_size(capacity) bytes of device memory, 16-byte aligned, owned by the
- * caller; the call fills it for rs_rasterize_bwd (no initial contents needed).
+ * rs_raster_workspace_size(camera, capacity) bytes of device memory, 16-byte aligned, owned by
+ * the caller; the call fills it for rs_rasterize_bwd (no initial contents needed).
  * Outputs: d_image [3][H][W], d_final_T [H][W], d_n_contrib [H][W] uint32.
  * Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE (workspace too small), RS_ERR_CUDA. */
 int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,

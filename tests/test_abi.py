@@ -90,19 +90,23 @@ def test_invalid_arguments_rejected_before_any_launch(L):
 def test_raster_workspace_validation(L):
     """The compositing workspace: one 256-pixel float4 state and one tile index per 256 entries
     of capacity (plus one); too small or misaligned is refused before any launch."""
-    cam = rs.camera_struct(scenes.procedural_camera(64, 48))
+    camera = scenes.procedural_camera(64, 48)
+    cam = rs.camera_struct(camera)
     chunk = rs.RS_RASTER_CHUNK
     for cap in (0, 1, 255, 256, 4_000_000):
         slots = cap // chunk + 1
-        assert rs.rs_raster_workspace_size(cap) >= slots * (chunk * 16 + 4)
-    assert rs.rs_raster_workspace_size(1_000_000) < rs.rs_raster_workspace_size(4_000_000)
-    assert L.rs_raster_workspace_size(rs.RS_MAX_ENTRIES + 1) == 0
+        assert rs.rs_raster_workspace_size(camera, cap) >= slots * (chunk * 16 + 4) + 4 * 12
+    assert rs.rs_raster_workspace_size(camera, 1_000_000) < rs.rs_raster_workspace_size(camera, 4_000_000)
+    big = scenes.procedural_camera(1920, 1080)
+    assert rs.rs_raster_workspace_size(big, 1000) >= rs.rs_raster_workspace_size(camera, 1000) + 4 * (8160 - 12) - 256
+    assert L.rs_raster_workspace_size(ctypes.byref(cam), rs.RS_MAX_ENTRIES + 1) == 0
+    assert L.rs_raster_workspace_size(None, 10) == 0
     p = rs.rs_projected()
     p.d_records = 0x1000
     bgv = (ctypes.c_float * 3)(0, 0, 0)
     fake = lambda a: ctypes.c_void_p(a)
     cap = 10_000
-    need = rs.rs_raster_workspace_size(cap)
+    need = rs.rs_raster_workspace_size(camera, cap)
     fwd = lambda ws, nb, c=cap: L.rs_rasterize_fwd(ctypes.byref(cam), ctypes.byref(p), 5, fake(0x2000), fake(0x3000),
                                                     c, bgv, fake(0x4000), fake(0x5000), fake(0x6000), ws, nb, None)
     bwd = lambda ws, nb, c=cap: L.rs_rasterize_bwd(ctypes.byref(cam), ctypes.byref(p), 5, fake(0x2000),
