@@ -36,10 +36,16 @@ constexpr int kRsWarps = kRsThreads / 32;
 #define RS_DEPTH_ITEMS 8
 #endif
 #ifndef RS_TILE_ITEMS
-#define RS_TILE_ITEMS 16
+#define RS_TILE_ITEMS 20
 #endif
 constexpr int kDepthItems = RS_DEPTH_ITEMS;             // depth sort: 2048 keys per block
-constexpr int kTileItems = RS_TILE_ITEMS;               // tile sort: 4096 keys per block
+constexpr int kTileItems = RS_TILE_ITEMS;               // tile sort: 5120 keys per block
+// Tile-sort blocks resident per SM: two blocks of 5120 keys hold 1.56 M entries on the 152 SMs in
+// one wave (a pass whose blocks do not all fit waits a second block latency for the last ones).
+#ifndef RS_TILE_MIN_BLOCKS
+#define RS_TILE_MIN_BLOCKS 2
+#endif
+constexpr int kTileMinBlocks = RS_TILE_MIN_BLOCKS;
 constexpr int kDepthHistItems = 2;                      // depth digit counts: 512 keys per block
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -158,8 +164,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t a, uint32_
 // first put in that order in shared memory, so the global writes of one digit are consecutive.
 // With KEYS64 (last pass of the tile sort) the 64-bit keys (tile << 32) | float_bits(depth) are
 // written as well when `keys64` is given.
-template <int RBITS, int ITEMS, bool FROM_DEPTH, bool GATHER_TILES, bool KEYS64 = false>
-__global__ void __launch_bounds__(kRsThreads) k_sweep_pass(
+template <int RBITS, int ITEMS, bool FROM_DEPTH, bool GATHER_TILES, bool KEYS64 = false, int MINB = 1>
+__global__ void __launch_bounds__(kRsThreads, MINB) k_sweep_pass(
     const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, DepthKeySource src,
     Count count, int shift, int pass, SortCtl ctl, uint32_t* __restrict__ keys_out,
     uint32_t* __restrict__ vals_out, const uint32_t* __restrict__ tiles_in,
@@ -643,11 +649,11 @@ void tile_sort_launch(const uint32_t* kin, const uint32_t* vin, Count count, int
                       const float* depth, uint64_t* keys64, const SortCtl& ctl, unsigned blocks, uint32_t* kout,
                       uint32_t* vout, cudaStream_t s) {
     if (last && keys64)
-        k_sweep_pass<RBITS, kTileItems, false, false, true><<<blocks, kRsThreads, 0, s>>>(
+        k_sweep_pass<RBITS, kTileItems, false, false, true, kTileMinBlocks><<<blocks, kRsThreads, 0, s>>>(
             kin, vin, DepthKeySource{depth, nullptr}, count, pass * digit, pass, ctl, kout, vout, nullptr,
             nullptr, keys64);
     else
-        k_sweep_pass<RBITS, kTileItems, false, false><<<blocks, kRsThreads, 0, s>>>(
+        k_sweep_pass<RBITS, kTileItems, false, false, false, kTileMinBlocks><<<blocks, kRsThreads, 0, s>>>(
             kin, vin, DepthKeySource{}, count, pass * digit, pass, ctl, kout, vout, nullptr, nullptr, nullptr);
 }
 

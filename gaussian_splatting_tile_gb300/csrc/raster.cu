@@ -498,34 +498,71 @@ RasterWs raster_ws(void* ws, size_t capacity, size_t n_tiles, size_t* bytes = nu
     return w;
 }
 
-// Tiles in decreasing order of list length (by powers of two): the forward's blocks take tiles
-// in this order, so the longest lists start first and the short ones fill in around them (the
-// hardware hands out blocks in index order as earlier ones finish).
+// Tiles in decreasing order of list length, in six classes (>= 1024, 512, 256, 128, 32 entries,
+// shorter): the forward's blocks take tiles in this order, so the longest lists start first and
+// the short ones fill in around them (the hardware hands out blocks in index order as earlier
+// ones finish).  One block; a warp ranks its tiles per class with ballots, the warps' class
+// counts are scanned class-major, and every tile is written to its slot (deterministic).
 constexpr int kOrderThreads = 1024;
+constexpr int kOrderWarps = kOrderThreads / 32;
+constexpr int kOrderPer = 8;  // tiles per thread per round (8160 tiles at 1080p: one round)
+constexpr int kClasses = 6;  // fewer measured slower: 2 classes 0.156 ms, 3 0.140, 4 0.132, 6 0.133
+__device__ __forceinline__ int tile_class(uint2 r) {
+    const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
+    return len >= 1024u ? 0 : len >= 512u ? 1 : len >= 256u ? 2 : len >= 128u ? 3 : len >= 32u ? 4 : 5;
+}
+
 __global__ void __launch_bounds__(kOrderThreads) k_tile_order(const uint2* __restrict__ ranges, uint32_t n_tiles,
                                                              uint32_t* __restrict__ order) {
-    __shared__ uint32_t s_cnt[33];
-    if (threadIdx.x < 33) s_cnt[threadIdx.x] = 0u;
-    __syncthreads();
-    for (uint32_t t = threadIdx.x; t < n_tiles; t += kOrderThreads) {
-        const uint2 r = ranges[t];
-        const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
-        atomicAdd(&s_cnt[__clz(len)], 1u);  // bucket 32 - bit length: longest first
+    __shared__ uint32_t s_cnt[kClasses][kOrderWarps];
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5, lt = (1u << lane) - 1u;
+    // 1. per warp and class: the number of tiles
+    uint32_t cnt[kClasses] = {};
+    for (uint32_t base = 0; base < n_tiles; base += kOrderThreads * kOrderPer) {
+#pragma unroll
+        for (int k = 0; k < kOrderPer; ++k) {
+            const uint32_t t = base + k * kOrderThreads + threadIdx.x;
+            const int c = t < n_tiles ? tile_class(ranges[t]) : kClasses;
+#pragma unroll
+            for (int j = 0; j < kClasses; ++j) cnt[j] += __popc(__ballot_sync(kFull, c == j));
+        }
     }
+    if (lane == 0)
+#pragma unroll
+        for (int j = 0; j < kClasses; ++j) s_cnt[j][warp] = cnt[j];
     __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t run = 0u;
-        for (int b = 0; b < 33; ++b) {
-            const uint32_t c = s_cnt[b];
-            s_cnt[b] = run;
-            run += c;
+    // 2. exclusive scan in (class, warp) order by one warp
+    if (warp == 0) {
+        uint32_t carry = 0u;
+        for (int j = 0; j < kClasses; ++j) {
+            const uint32_t v = s_cnt[j][lane];
+            uint32_t x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, x, o);
+                if (lane >= uint32_t(o)) x += y;
+            }
+            s_cnt[j][lane] = carry + x - v;
+            carry += __shfl_sync(kFull, x, 31);
         }
     }
     __syncthreads();
-    for (uint32_t t = threadIdx.x; t < n_tiles; t += kOrderThreads) {
-        const uint2 r = ranges[t];
-        const uint32_t len = r.y > r.x ? r.y - r.x : 0u;
-        order[atomicAdd(&s_cnt[__clz(len)], 1u)] = t;
+    // 3. every tile to its slot: warp offset + earlier tiles of its class in the warp
+    uint32_t run[kClasses];
+#pragma unroll
+    for (int j = 0; j < kClasses; ++j) run[j] = s_cnt[j][warp];
+    for (uint32_t base = 0; base < n_tiles; base += kOrderThreads * kOrderPer) {
+#pragma unroll
+        for (int k = 0; k < kOrderPer; ++k) {
+            const uint32_t t = base + k * kOrderThreads + threadIdx.x;
+            const int c = t < n_tiles ? tile_class(ranges[t]) : kClasses;
+#pragma unroll
+            for (int j = 0; j < kClasses; ++j) {
+                const uint32_t m = __ballot_sync(kFull, c == j);
+                if (c == j) order[run[j] + uint32_t(__popc(m & lt))] = t;
+                run[j] += __popc(m);
+            }
+        }
     }
 }
 }  // namespace
