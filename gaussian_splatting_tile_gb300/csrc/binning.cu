@@ -100,7 +100,10 @@ __device__ __forceinline__ void rs_load(const uint32_t* __restrict__ keys, const
                                         const DepthKeySource& src, uint32_t i, uint32_t& key,
                                         uint32_t& val) {
     if (FROM_DEPTH) {
-        key = src.radius[i] > 0 ? __float_as_uint(src.depth[i]) : 0xffffffffu;
+        // both loads issued together (a depth load behind the radius test would wait for it)
+        const int r = src.radius[i];
+        const uint32_t d = __float_as_uint(src.depth[i]);
+        key = r > 0 ? d : 0xffffffffu;
         val = i;
     } else {
         key = keys[i];

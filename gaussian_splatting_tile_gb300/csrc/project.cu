@@ -10,6 +10,18 @@
 namespace rs {
 namespace {
 
+// One thread per Gaussian.  Blocks of 128 threads at 9 per SM (at most 56 registers): 160k
+// Gaussians then run in a single wave on the 152 SMs (at 256 threads and 64 registers, 4 blocks
+// per SM, 608 resident blocks left 17 of 625 for a second wave).
+#ifndef RS_PROJ_THREADS
+#define RS_PROJ_THREADS 128
+#endif
+#ifndef RS_PROJ_MIN_BLOCKS
+#define RS_PROJ_MIN_BLOCKS 9
+#endif
+constexpr int kProjThreads = RS_PROJ_THREADS;
+constexpr int kProjMinBlocks = RS_PROJ_MIN_BLOCKS;
+
 // Real SH normalisations of "3D Gaussian Splatting ビューワを作る" 2.2.3 (after Sloan's
 // "Stupid Spherical Harmonics (SH) Tricks", Appendix A2).
 constexpr float kY0 = 0.28209479177387814f;   // 1 / (2 sqrt(pi))
@@ -220,7 +232,7 @@ __device__ __forceinline__ void view_dir(const CameraF& cam, const float m[3], f
 }
 
 template <int DEG>
-__global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float* __restrict__ means,
+__global__ void __launch_bounds__(kProjThreads, kProjMinBlocks) k_project(CameraF cam, int n, const float* __restrict__ means,
                                                  const float* __restrict__ scales,
                                                  const float* __restrict__ quats,
                                                  const float* __restrict__ opacity,
@@ -318,7 +330,7 @@ __global__ void __launch_bounds__(256) k_project(CameraF cam, int n, const float
 }
 
 template <int DEG>
-__global__ void __launch_bounds__(256) k_project_bwd(
+__global__ void __launch_bounds__(kProjThreads, kProjMinBlocks) k_project_bwd(
     CameraF cam, int n, const float* __restrict__ means, const float* __restrict__ scales,
     const float* __restrict__ quats, const float* __restrict__ sh,
     const int* __restrict__ radius, const float* __restrict__ dm2,
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(256) k_project_bwd(
 cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_projected& o,
                            cudaStream_t s) {
     if (g.n == 0) return cudaSuccess;
-    const int threads = 256;
+    const int threads = kProjThreads;
     const int blocks = (g.n + threads - 1) / threads;
     Record* rec = reinterpret_cast<Record*>(o.d_records);
 #define RS_PROJECT(D)                                                                           \
@@ -512,7 +524,7 @@ cudaError_t launch_project_bwd(const CameraF& cam, const rs_gaussians& g, const 
                                float* dmeans, float* dscales, float* dquats, float* dsh,
                                cudaStream_t s) {
     if (g.n == 0) return cudaSuccess;
-    const int threads = 256;
+    const int threads = kProjThreads;
     const int blocks = (g.n + threads - 1) / threads;
 #define RS_PROJECT_BWD(D)                                                                      \
     k_project_bwd<D><<<blocks, threads, 0, s>>>(cam, g.n, g.d_means, g.d_scales, g.d_quats,    \
