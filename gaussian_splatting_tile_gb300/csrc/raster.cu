@@ -389,9 +389,8 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 m ^= 1u << j;
                 const uint32_t ej = lo + uint32_t(j);
                 const float4 p = s_p[warp][j], q = s_q[warp][j];
-                float dx, dy0, dy1, G, raw0, raw1;
-                const float al0 = entry_alpha(p, q, fx, fy0, dx, dy0, G, raw0);
-                const float al1 = entry_alpha(p, q, fx, fy1, dx, dy1, G, raw1);
+                float dx, dy0, dy1, al0, raw0, al1, raw1;
+                entry_alpha_col(p, q, fx, fy0, fy1, dx, dy0, dy1, al0, raw0, al1, raw1);
                 const bool act0 = ej < P[0].end && al0 >= kAlphaMin;
                 const bool act1 = ej < P[1].end && al1 >= kAlphaMin;
                 float gp0 = 0.f, gp1 = 0.f, w0 = 0.f, w1 = 0.f;

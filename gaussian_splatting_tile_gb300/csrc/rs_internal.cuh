@@ -74,14 +74,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // take identical skip, clamp and stop decisions (rigel README "Rasterization":
 // alpha = min(0.99, opacity exp(power)), power = -1/2 (A dx^2 + C dy^2) - B dx dy, here in log2
 // units).  Returns alpha; `G` = exp(power), `raw` = opacity * G before the clamp.
+// The quadratic is evaluated as dy (qc dy + qb dx) + (qa dx) dx, so that pixels sharing a column
+// (the backward's two pixels per lane) share the dx terms: entry_alpha_col gives each of them
+// exactly what entry_alpha gives.
 __device__ __forceinline__ float entry_alpha(const float4& p, const float4& q, float px, float py,
                                              float& dx, float& dy, float& G, float& raw) {
     dx = px - p.x;
     dy = py - p.y;
-    const float power2 = fmaf(dx, fmaf(q.x, dx, q.y * dy), (q.z * dy) * dy);
+    const float power2 = fmaf(dy, fmaf(q.z, dy, q.y * dx), (q.x * dx) * dx);
     G = ex2_approx(power2);
     raw = p.z * G;
     return fminf(kAlphaMax, raw);
+}
+
+// entry_alpha at (px, py0) and (px, py1), bit-identical to two calls.
+__device__ __forceinline__ void entry_alpha_col(const float4& p, const float4& q, float px, float py0, float py1,
+                                                float& dx, float& dy0, float& dy1, float& a0, float& raw0,
+                                                float& a1, float& raw1) {
+    dx = px - p.x;
+    dy0 = py0 - p.y;
+    dy1 = py1 - p.y;
+    const float bx = q.y * dx, axx = (q.x * dx) * dx;
+    raw0 = p.z * ex2_approx(fmaf(dy0, fmaf(q.z, dy0, bx), axx));
+    raw1 = p.z * ex2_approx(fmaf(dy1, fmaf(q.z, dy1, bx), axx));
+    a0 = fminf(kAlphaMax, raw0);
+    a1 = fminf(kAlphaMax, raw1);
 }
 
 // Tile span bound of a splat's bounding square (learn-gs "11 - Tiles", tile_spans):
