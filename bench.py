@@ -49,7 +49,7 @@ SMS, FP32_LANES, MUFU_LANES, MAX_MHZ = 152, 128, 16, 2070.0
 #            = 43 ops + 1 rcp.
 OPS_FWD_EXAMINED, OPS_FWD_BLEND = 10, 6
 OPS_BWD_EXAMINED, OPS_BWD_BLEND = 10, 43
-# bytes (algorithmic, moved once): see DESIGN.md "Roofline"
+# bytes (algorithmic, moved once)
 B_PROJECT_PER_G = 236 + 44          # SH degree 3 inputs + means2d/depth/conic/colour/radius/tiles
 B_PROJECT_BWD_PER_G = 504
 B_FWD_PER_ENTRY, B_FWD_PER_PIXEL = 40, 20
@@ -62,7 +62,7 @@ B_BIN_PER_G = 8 + 4 * 16 + 8 + 40
 B_BIN_PER_ENTRY_FIXED, B_BIN_PER_ENTRY_PASS = 12, 16
 # DRAM bytes (read + write) of one k_raster_bwd launch on orbit view 1, from an ncu --set full
 # capture of the current kernel; must be re-taken (or set to None) whenever the kernel changes
-TRAFFIC_RASTER_BWD_BYTES = 58.296576e6 + 0.474368e6
+TRAFFIC_RASTER_BWD_BYTES = 44.814080e6 + 0.104448e6
 TRAFFIC_RASTER_BWD_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of k_raster_bwd, "
                              "160k scene, 1920x1080 orbit view 1")
 
