@@ -259,3 +259,59 @@ class AppearanceStep:
     def view(self, camera, target, scale, bg=(0.0, 0.0, 0.0), stream=None):
         F = self.forward(camera, target, scale, bg, stream)
         return F, self.backward(stream=stream)
+
+
+class FrameGraph:
+    """One view's forward and backward captured as a single CUDA graph and replayed.
+
+    Every call of the frame is stream-ordered with no host wait (the binning's entry count is
+    copied to pinned host memory in stream order, `rs_bin_async`), so projection, binning,
+    compositing and both backward passes fit in one graph launch -- the sync-free, graph-captured
+    pipeline that "3D Gaussian Splatting ビューワを作る" (4.2-4.3, indirect dispatch) and the rigel
+    README ("Binning", the one device-to-host sync) point to.  The kernels take the camera by
+    value, so a graph belongs to one view (`FrameGraphs` keeps one per view).  A replay reads the
+    Gaussians and dL/dimage from the buffers given at capture and writes the renderer's buffers.
+    `check()` (after the stream has passed the replay) returns the entry count and raises when
+    it exceeded the capacity: that frame rendered the background, the renderer has grown and the
+    graph must be captured again."""
+
+    def __init__(self, R: Renderer, gs: rs.DeviceGaussians, dL_dimage: torch.Tensor, camera,
+                 bg=(0.0, 0.0, 0.0)):
+        self.R, self.camera, self.bg = R, camera, tuple(bg)
+        self.result = torch.zeros(2, dtype=torch.int64).pin_memory()
+        R.set_camera(camera)
+        R._grads(gs.sh_degree)
+        # one eager frame: builds the prepared calls and checks that the buffers are big enough
+        R.forward_async(gs, self.result, bg)
+        R.backward(gs, dL_dimage)
+        torch.cuda.current_stream(R.device).synchronize()
+        R.check_async(self.result)
+        self.capacity = R.capacity
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            R.forward_async(gs, self.result, bg)
+            R.backward(gs, dL_dimage)
+
+    def replay(self):
+        if self.R.capacity != self.capacity:
+            raise RuntimeError("the renderer's buffers changed since the capture")
+        self.graph.replay()
+
+    def check(self) -> int:
+        return self.R.check_async(self.result)
+
+
+class FrameGraphs:
+    """One `FrameGraph` per view of a fixed camera list, captured on first use."""
+
+    def __init__(self, R: Renderer, gs: rs.DeviceGaussians, dL_dimage: torch.Tensor, cameras,
+                 bg=(0.0, 0.0, 0.0)):
+        self.R, self.gs, self.dL, self.cameras, self.bg = R, gs, dL_dimage, list(cameras), tuple(bg)
+        self.graphs: dict[int, FrameGraph] = {}
+
+    def get(self, view: int) -> FrameGraph:
+        fg = self.graphs.get(view)
+        if fg is None or fg.capacity != self.R.capacity:
+            fg = FrameGraph(self.R, self.gs, self.dL, self.cameras[view], self.bg)
+            self.graphs[view] = fg
+        return fg
