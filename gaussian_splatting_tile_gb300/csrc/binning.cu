@@ -701,6 +701,11 @@ BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity) {
     return p;
 }
 
+__global__ void k_report(const uint64_t* __restrict__ result, uint64_t* __restrict__ host) {
+    host[0] = result[0];                                   // E
+    host[1] = uint64_t(reinterpret_cast<const uint32_t*>(result + 1)[0]);  // look-back timeout flag
+}
+
 template <int RBITS>
 void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* perm, const SliceOut& sl, int digit,
                    int passes, uint32_t* ghist, uint32_t* tk, uint32_t* tv, const rs_projected& p, cudaStream_t s) {
@@ -714,6 +719,11 @@ void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* per
     }
     else
         k_expand<RBITS, false><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
+}
+
+cudaError_t launch_report(const uint8_t* result_block, uint64_t* host, cudaStream_t s) {
+    k_report<<<1, 1, 0, s>>>(reinterpret_cast<const uint64_t*>(result_block), host);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_projected& p, uint8_t* ws,

@@ -155,6 +155,13 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
     const int rc = enqueue_bin(camera, proj, n, d_workspace, workspace_bytes, capacity, d_keys_sorted,
                                d_point_list, d_tile_ranges, s, &dev);
     if (rc != RS_OK) return rc;
+    // pinned host memory is in the device's address space under unified addressing: a one-thread
+    // kernel writes the two words there, so the frame has no copy (a copy would queue behind
+    // other transfers on the copy engine); memory that is not mapped gets a copy instead
+    void* mapped = nullptr;
+    if (cudaHostGetDevicePointer(&mapped, h_result, 0) == cudaSuccess && mapped)
+        return cuda_rc(rs::launch_report(dev, static_cast<uint64_t*>(mapped), s));
+    (void)cudaGetLastError();  // the failed lookup is not an error of this call
     return cuda_rc(cudaMemcpyAsync(h_result, dev, 2 * sizeof(uint64_t), cudaMemcpyDeviceToHost, s));
 }
 

@@ -231,6 +231,9 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
                        uint64_t* keys_out, uint32_t* point_list, uint32_t* tile_ranges, cudaStream_t s);
 
 // Compositing workspace: chunk -> tile map and the forward's per-pixel state at chunk boundaries.
+// Writes the binning's {E, error} (the workspace's result block) to `host` (a device-visible
+// pointer to pinned host memory) from a one-thread kernel.
+cudaError_t launch_report(const uint8_t* result_block, uint64_t* host, cudaStream_t s);
 size_t raster_workspace_bytes(size_t capacity, size_t n_tiles);
 cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
                               const uint32_t* list, size_t capacity, float3 bg, float* image, float* final_T,

@@ -315,3 +315,99 @@ class FrameGraphs:
             fg = FrameGraph(self.R, self.gs, self.dL, self.cameras[view], self.bg)
             self.graphs[view] = fg
         return fg
+
+
+class StreamedFrames:
+    """Forward + backward of a sequence of views whose Gaussian parameters and dL/dimage come
+    from pinned host memory and whose per-Gaussian gradients go back to pinned host memory, with
+    the copies of one frame overlapping the compute of its neighbours.
+
+    Two slots, each a renderer with its own device inputs, gradients and per-view frame graphs,
+    alternate between frames.  Frame k's host-to-device copies run on an input copy stream once
+    frame k - 2 (same slot) has finished reading its inputs; its graph replays on the compute
+    stream once those copies and frame k - 2's device-to-host copies are done; its gradients go
+    back on an output copy stream once it has finished.  So the two copy directions and the
+    compute proceed at once, and a step costs about the longest of the three.
+
+    `host_in`: pinned float32 tensors means [3,N], scales [3,N], quats [4,N], opacity [N] and
+    sh [3K,N] (or colors [3,N] with sh_degree -1); `host_dL`: pinned [3,H,W].  `host_out[slot]`
+    receives dmeans, dscales, dquats, dopacity, dsh (or dcolor) of that slot's frames."""
+
+    OUT = ("dmeans", "dscales", "dquats", "dopacity")
+
+    def __init__(self, cameras, host_in: dict, sh_degree: int, host_dL: torch.Tensor, device="cuda",
+                 capacity: int | None = None, bg=(0.0, 0.0, 0.0)):
+        self.device = torch.device(device)
+        self.cameras = list(cameras)
+        self.host_in, self.host_dL, self.sh_degree = host_in, host_dL, sh_degree
+        n = int(host_in["opacity"].shape[0])
+        self.out_names = self.OUT + (("dsh",) if sh_degree >= 0 else ("dcolor",))
+        self.slots = []
+        for _ in range(2):
+            R = Renderer(self.cameras[0], n, self.device, capacity=capacity, keep_keys=False)
+            dev = {k: torch.empty_like(v, device=self.device) for k, v in host_in.items()}
+            if sh_degree >= 0:
+                dg = rs.DeviceGaussians(dev["means"], dev["scales"], dev["quats"], dev["opacity"], dev["sh"],
+                                        sh_degree)
+            else:
+                dg = rs.DeviceGaussians(dev["means"], dev["scales"], dev["quats"], dev["opacity"], None, -1,
+                                        dev["colors"])
+            ddL = torch.empty_like(host_dL, device=self.device)
+            R._grads(sh_degree)
+            host_out = {k: torch.empty(tuple(getattr(R.grads, k).shape), dtype=torch.float32).pin_memory()
+                        for k in self.out_names}
+            ev = lambda: torch.cuda.Event()
+            self.slots.append(dict(R=R, dev=dev, dg=dg, ddL=ddL, host_out=host_out,
+                                   graphs=FrameGraphs(R, dg, ddL, self.cameras, bg), in_ready=ev(),
+                                   comp_done=ev(), out_done=ev(), frames=[]))
+        self.compute = torch.cuda.current_stream(self.device)
+        self.h2d = torch.cuda.Stream(self.device)
+        self.d2h = torch.cuda.Stream(self.device)
+        self.k = 0
+
+    @property
+    def host_out(self):
+        return [s["host_out"] for s in self.slots]
+
+    def prepare(self, views):
+        """Captures the frame graphs of `views` in both slots (each capture runs one frame)."""
+        for s in self.slots:
+            for v in sorted(set(views)):
+                self._copy_in(s)
+                self.compute.wait_event(s["in_ready"])
+                s["graphs"].get(v)
+        torch.cuda.synchronize(self.device)
+
+    def _copy_in(self, s):
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(s["comp_done"])  # the slot's previous frame has read its inputs
+            for k, v in self.host_in.items():
+                s["dev"][k].copy_(v, non_blocking=True)
+            s["ddL"].copy_(self.host_dL, non_blocking=True)
+            s["in_ready"].record(self.h2d)
+
+    def frame(self, view: int):
+        """Enqueues one frame of `view`; nothing waits on the host."""
+        s = self.slots[self.k % 2]
+        self.k += 1
+        fg = s["graphs"].get(view)  # captured already after prepare(); else captured here
+        self._copy_in(s)
+        self.compute.wait_event(s["in_ready"])
+        self.compute.wait_event(s["out_done"])  # the slot's previous gradients are on the host
+        fg.replay()
+        s["comp_done"].record(self.compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(s["comp_done"])
+            for k in self.out_names:
+                s["host_out"][k].copy_(getattr(s["R"].grads, k), non_blocking=True)
+            s["out_done"].record(self.d2h)
+        s["frames"].append(fg)
+
+    def finish(self) -> list[int]:
+        """Waits for every enqueued frame; returns their entry counts (raises on an overflow)."""
+        torch.cuda.synchronize(self.device)
+        counts = []
+        for s in self.slots:
+            counts += [fg.check() for fg in s["frames"]]
+            s["frames"].clear()
+        return counts

@@ -158,15 +158,16 @@ int rs_bin(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d
 
 /* Binning without waiting for the entry count (the sync-free pipeline: the host keeps
  * enqueueing the rest of the frame while the GPU bins).  Same arguments, work and outputs as
- * rs_bin, except that the entry count is not waited for: the call enqueues, on `stream`, a copy
- * of two uint64 words into h_result -- h_result[0] = E, h_result[1] = nonzero if a bounded wait
- * of the sort's look-back gave up -- and returns.  Read h_result only after the stream has
- * reached that point (cudaStreamSynchronize or an event recorded after the call); use pinned
- * host memory (cudaHostAlloc), else the copy blocks the host.  When E > capacity no entry is
- * written and every tile range is (0, 0), so later calls on these buffers render the
+ * rs_bin, except that the entry count is not waited for: the call enqueues, on `stream`, the
+ * writing of two uint64 words into h_result -- h_result[0] = E, h_result[1] = nonzero if a
+ * bounded wait of the sort's look-back gave up -- and returns.  h_result must be pinned host
+ * memory (cudaHostAlloc, cudaMallocHost, or registered with cudaHostRegister); where it is mapped
+ * into the device's address space (always under unified addressing) a one-thread kernel writes
+ * it, else a device-to-host copy does.  Read h_result only after the stream has reached that
+ * point (cudaStreamSynchronize or an event recorded after the call).  When E > capacity no entry
+ * is written and every tile range is (0, 0), so later calls on these buffers render the
  * background and stay within bounds; the caller must then grow the buffers and redo the frame.
- * The device-side result is part of the workspace, so work enqueued later on the stream may
- * reuse the workspace only after that copy (stream order guarantees it).
+ * Nothing in the call waits on the host, so it can be captured in a CUDA graph.
  * Errors (returned at once): RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CUDA. */
 int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, void* d_workspace,
                  size_t workspace_bytes, size_t capacity, uint64_t* d_keys_sorted,

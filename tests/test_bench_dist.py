@@ -57,7 +57,7 @@ def test_single_rank_is_identity():
 def test_launch_count_model():
     import bench
     # 160k Gaussians on 8160 tiles (13 tile bits): projection; clear, depth histogram + 4 passes,
-    # slices, expansion, 2 tile passes, ranges; tile order, compositing; zeroing, compositing
-    # backward, projection backward
+    # slices, expansion, 2 tile passes, ranges, E to the host; tile order, compositing; zeroing,
+    # compositing backward, projection backward
     n = bench.launches_per_step(160_000, 1_531_492, 120 * 68)
-    assert n == 1 + (1 + 5 + 2 + 2 + 1) + 2 + 3
+    assert n == 1 + (1 + 5 + 2 + 2 + 1 + 1) + 2 + 3
