@@ -190,6 +190,7 @@ __device__ __forceinline__ float sigmoidf(float z) { return 1.0f / (1.0f + expf(
 
 template <int HID, int KS>
 __global__ void __launch_bounds__(kMlpThreads) k_mlp_fwd(MlpArgs a, float* __restrict__ colors) {
+    RS_PDL_ENTER();
     extern __shared__ __align__(16) unsigned char smem[];
     WeightSmem<HID>& w = *reinterpret_cast<WeightSmem<HID>*>(smem);
     float* s_x = reinterpret_cast<float*>(smem + sizeof(WeightSmem<HID>)) +
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(kMlpThreads) k_mlp_bwd(MlpArgs a, const float*
                                                         float* __restrict__ dlatents, float* __restrict__ dW1,
                                                         float* __restrict__ db1, float* __restrict__ dW2,
                                                         float* __restrict__ db2) {
+    RS_PDL_ENTER();
     constexpr int HS = HID + 8;   // row stride of dz1 and h copies
     constexpr int Q = HID / 32;   // hidden units owned per lane: lane + 32 q
     extern __shared__ __align__(16) unsigned char smem[];
@@ -397,6 +399,7 @@ __global__ void __launch_bounds__(kMlpThreads) k_mlp_bwd(MlpArgs a, const float*
 }
 
 __global__ void k_zero_mlp_grads(float* dW1, int nW1, float* db1, int nb1, float* dW2, int nW2, float* db2) {
+    RS_PDL_ENTER();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nW1; i += gridDim.x * blockDim.x) dW1[i] = 0.f;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nb1; i += gridDim.x * blockDim.x) db1[i] = 0.f;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nW2; i += gridDim.x * blockDim.x) dW2[i] = 0.f;
@@ -407,6 +410,7 @@ __global__ void k_zero_mlp_grads(float* dW1, int nW1, float* db1, int nb1, float
 __global__ void __launch_bounds__(256) k_l1(size_t count, const float* __restrict__ img,
                                             const float* __restrict__ tgt, float scale,
                                             float* __restrict__ dimg, float* __restrict__ loss) {
+    RS_PDL_ENTER();
     __shared__ float s_w[8];
     float acc = 0.f;
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += size_t(gridDim.x) * blockDim.x) {
@@ -433,7 +437,7 @@ cudaError_t launch_fwd_t(const MlpArgs& a, float* colors, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int tiles = (a.n + kRows - 1) / kRows;
     const int blocks = std::min((tiles + kMlpWarps - 1) / kMlpWarps, 152 * 4);
-    k_mlp_fwd<HID, KS><<<blocks, kMlpThreads, smem, s>>>(a, colors);
+    pdl_launch(k_mlp_fwd<HID, KS>, blocks, kMlpThreads, smem, s, a, colors);
     return cudaGetLastError();
 }
 
@@ -442,11 +446,11 @@ cudaError_t launch_bwd_t(const MlpArgs& a, const float* dcol, float* dlat, const
     const size_t smem = sizeof(WeightSmem<HID>) + sizeof(BwdSums<HID>) + size_t(kMlpWarps) * sizeof(BwdWarpSmem<HID>);
     cudaError_t e = cudaFuncSetAttribute(k_mlp_bwd<HID, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    k_zero_mlp_grads<<<8, 256, 0, s>>>(gr.d_dW1, HID * a.D, gr.d_db1, HID, gr.d_dW2, 3 * HID, gr.d_db2);
+    pdl_launch(k_zero_mlp_grads, 8, 256, 0, s, gr.d_dW1, HID * a.D, gr.d_db1, HID, gr.d_dW2, 3 * HID, gr.d_db2);
     if (a.n == 0) return cudaGetLastError();
     const int tiles = (a.n + kRows - 1) / kRows;
     const int blocks = std::min((tiles + kMlpWarps - 1) / kMlpWarps, 152 * 2);
-    k_mlp_bwd<HID, KS><<<blocks, kMlpThreads, smem, s>>>(a, dcol, dlat, gr.d_dW1, gr.d_db1, gr.d_dW2, gr.d_db2);
+    pdl_launch(k_mlp_bwd<HID, KS>, blocks, kMlpThreads, smem, s, a, dcol, dlat, gr.d_dW1, gr.d_db1, gr.d_dW2, gr.d_db2);
     return cudaGetLastError();
 }
 
@@ -498,7 +502,7 @@ cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float sc
     }
     if (count == 0) return cudaSuccess;
     const unsigned blocks = unsigned(std::min<size_t>((count + 255) / 256, 152 * 8));
-    k_l1<<<blocks, 256, 0, s>>>(count, img, tgt, scale, dimg, loss);
+    pdl_launch(k_l1, blocks, 256, 0, s, count, img, tgt, scale, dimg, loss);
     return cudaGetLastError();
 }
 
@@ -534,6 +538,7 @@ __device__ __forceinline__ float patch_at(const float* __restrict__ img, int H, 
 __global__ void __launch_bounds__(256) k_ssim_fwd(SsimWindow win, int C, int H, int W,
                                                   const float* __restrict__ img, const float* __restrict__ tgt,
                                                   float* __restrict__ abc, float* __restrict__ sums) {
+    RS_PDL_ENTER();
     __shared__ float s_x[kSsimP][kSsimP], s_y[kSsimP][kSsimP];
     __shared__ float s_h[5][kSsimP][kSsimTile];  // horizontally filtered x, y, xx, yy, xy
     __shared__ float s_red[2][8];
@@ -617,6 +622,7 @@ __global__ void __launch_bounds__(256) k_ssim_bwd(SsimWindow win, int C, int H, 
                                                   const float* __restrict__ img, const float* __restrict__ tgt,
                                                   const float* __restrict__ abc, float lambda, float scale,
                                                   float* __restrict__ dimg) {
+    RS_PDL_ENTER();
     __shared__ float s_in[3][kSsimP][kSsimP];
     __shared__ float s_h[3][kSsimP][kSsimTile];
     const int TXn = (W + kSsimTile - 1) / kSsimTile;
@@ -663,6 +669,7 @@ __global__ void __launch_bounds__(256) k_ssim_bwd(SsimWindow win, int C, int H, 
 }
 
 __global__ void k_ssim_loss(const float* __restrict__ sums, size_t N, float lambda, float scale, float* loss) {
+    RS_PDL_ENTER();
     // sums[0] = sum S, sums[1] = sum |I - T|
     *loss = scale * ((1.f - lambda) * sums[1] + lambda * (float(N) - sums[0])) / float(N);
 }
@@ -688,9 +695,9 @@ cudaError_t launch_l1_dssim(int C, int H, int W, const float* img, const float* 
     if (e != cudaSuccess) return e;
     const int tiles = ((W + kSsimTile - 1) / kSsimTile) * ((H + kSsimTile - 1) / kSsimTile);
     const dim3 grid{unsigned(tiles), unsigned(C), 1u};
-    k_ssim_fwd<<<grid, 256, 0, s>>>(win, C, H, W, img, tgt, abc, sums);
-    k_ssim_bwd<<<grid, 256, 0, s>>>(win, C, H, W, img, tgt, abc, lambda, scale, dimg);
-    if (loss) k_ssim_loss<<<1, 1, 0, s>>>(sums, size_t(C) * H * W, lambda, scale, loss);
+    pdl_launch(k_ssim_fwd, grid, 256, 0, s, win, C, H, W, img, tgt, abc, sums);
+    pdl_launch(k_ssim_bwd, grid, 256, 0, s, win, C, H, W, img, tgt, abc, lambda, scale, dimg);
+    if (loss) pdl_launch(k_ssim_loss, 1, 1, 0, s, sums, size_t(C) * H * W, lambda, scale, loss);
     return cudaGetLastError();
 }
 

@@ -116,6 +116,7 @@ template <int RBITS, int ITEMS, int PASSES, bool FROM_DEPTH>
 __global__ void __launch_bounds__(kRsThreads) k_sweep_hist(const uint32_t* __restrict__ keys,
                                                           DepthKeySource src, Count count, int digit_bits,
                                                           uint32_t* __restrict__ ghist) {
+    RS_PDL_ENTER();
     constexpr int R = 1 << RBITS;
     __shared__ uint32_t s_h[PASSES][R];
     for (int i = threadIdx.x; i < PASSES * R; i += kRsThreads) (&s_h[0][0])[i] = 0u;
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kRsThreads, MINB) k_sweep_pass(
     Count count, int shift, int pass, SortCtl ctl, uint32_t* __restrict__ keys_out,
     uint32_t* __restrict__ vals_out, const uint32_t* __restrict__ tiles_in,
     uint32_t* __restrict__ tiles_out, uint64_t* __restrict__ keys64) {
+    RS_PDL_ENTER();
     constexpr int R = 1 << RBITS;
     constexpr uint32_t TILE = kRsThreads * ITEMS;
     __shared__ uint32_t s_cnt[kRsWarps][R];
@@ -299,6 +301,7 @@ __global__ void __launch_bounds__(kRsThreads, MINB) k_sweep_pass(
 // result block) in one launch.
 __global__ void k_clear(uint32_t* __restrict__ ranges, uint32_t range_words, uint32_t* __restrict__ ctl,
                         size_t ctl_words) {
+    RS_PDL_ENTER();
     const size_t stride = size_t(gridDim.x) * blockDim.x;
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < range_words; i += stride) ranges[i] = 0u;
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < ctl_words; i += stride) ctl[i] = 0u;
@@ -307,6 +310,7 @@ __global__ void k_clear(uint32_t* __restrict__ ranges, uint32_t range_words, uin
 // Ranges from the sorted tile ids.
 __global__ void k_ranges(const uint32_t* __restrict__ tiles, Count count, uint32_t n_tiles,
                          uint32_t* __restrict__ ranges) {
+    RS_PDL_ENTER();
     const uint32_t E = count.get();
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride) {
@@ -359,6 +363,7 @@ __global__ void __launch_bounds__(kSlThreads) k_slices(CameraF cam, uint32_t n, 
                                                       const int* __restrict__ radius, uint32_t* counter,
                                                       unsigned long long* status, uint32_t* error,
                                                       uint64_t* total_out, SliceOut out) {
+    RS_PDL_ENTER();
     __shared__ uint64_t s_w[kSlThreads / 32];
     __shared__ uint64_t s_prefix;
     __shared__ uint32_t s_blk;
@@ -468,6 +473,7 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
                                                        int digit_bits, int passes, uint32_t* __restrict__ ghist,
                                                        uint32_t* __restrict__ tile_keys,
                                                        uint32_t* __restrict__ vals) {
+    RS_PDL_ENTER();
     constexpr int R = 1 << RBITS;
     constexpr int ROWS = ELL ? kRowCap : 1;
     __shared__ uint64_t s_start[kExpChunk + 1];
@@ -652,11 +658,11 @@ void tile_sort_launch(const uint32_t* kin, const uint32_t* vin, Count count, int
                       const float* depth, uint64_t* keys64, const SortCtl& ctl, unsigned blocks, uint32_t* kout,
                       uint32_t* vout, cudaStream_t s) {
     if (last && keys64)
-        k_sweep_pass<RBITS, kTileItems, false, false, true, kTileMinBlocks><<<blocks, kRsThreads, 0, s>>>(
+        pdl_launch(k_sweep_pass<RBITS, kTileItems, false, false, true, kTileMinBlocks>, blocks, kRsThreads, 0, s,
             kin, vin, DepthKeySource{depth, nullptr}, count, pass * digit, pass, ctl, kout, vout, nullptr,
             nullptr, keys64);
     else
-        k_sweep_pass<RBITS, kTileItems, false, false, false, kTileMinBlocks><<<blocks, kRsThreads, 0, s>>>(
+        pdl_launch(k_sweep_pass<RBITS, kTileItems, false, false, false, kTileMinBlocks>, blocks, kRsThreads, 0, s,
             kin, vin, DepthKeySource{}, count, pass * digit, pass, ctl, kout, vout, nullptr, nullptr, nullptr);
 }
 
@@ -702,6 +708,7 @@ BinPlan plan_bin(int32_t n, const CameraF& cam, size_t capacity) {
 }
 
 __global__ void k_report(const uint64_t* __restrict__ result, uint64_t* __restrict__ host) {
+    RS_PDL_ENTER();
     host[0] = result[0];                                   // E
     host[1] = uint64_t(reinterpret_cast<const uint32_t*>(result + 1)[0]);  // look-back timeout flag
 }
@@ -715,14 +722,14 @@ void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* per
         if (cudaFuncSetAttribute(k_expand<RBITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
             cudaSuccess)
             return;  // that error stays the last error, which launch_bin returns
-        k_expand<RBITS, true><<<blocks, kExpThreads, smem, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
+        pdl_launch(k_expand<RBITS, true>, blocks, kExpThreads, smem, s, cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
     }
     else
-        k_expand<RBITS, false><<<blocks, kExpThreads, 0, s>>>(cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
+        pdl_launch(k_expand<RBITS, false>, blocks, kExpThreads, 0, s, cam, n, ce, perm, sl, digit, passes, ghist, tk, tv);
 }
 
 cudaError_t launch_report(const uint8_t* result_block, uint64_t* host, cudaStream_t s) {
-    k_report<<<1, 1, 0, s>>>(reinterpret_cast<const uint64_t*>(result_block), host);
+    pdl_launch(k_report, 1, 1, 0, s, reinterpret_cast<const uint64_t*>(result_block), host);
     return cudaGetLastError();
 }
 
@@ -732,7 +739,7 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
     {
         const size_t words = plan.ctl_bytes / 4 + 2u * uint32_t(plan.n_tiles);
         const unsigned blocks = unsigned(std::min<size_t>(ceil_div(words, 256), 152 * 8));
-        k_clear<<<blocks, 256, 0, s>>>(tile_ranges, 2u * uint32_t(plan.n_tiles), ctl_words, plan.ctl_bytes / 4);
+        pdl_launch(k_clear, blocks, 256, 0, s, tile_ranges, 2u * uint32_t(plan.n_tiles), ctl_words, plan.ctl_bytes / 4);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || plan.n == 0) return e;
@@ -753,15 +760,15 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
                        reinterpret_cast<uint32_t*>(ws + plan.off_status_depth), error,
                        uint32_t(plan.depth_tiles)};
     const unsigned dblocks = unsigned(plan.depth_tiles);
-    k_sweep_hist<8, kDepthHistItems, 4, true><<<unsigned(ceil_div(n, kRsThreads * kDepthHistItems)), kRsThreads, 0, s>>>(
+    pdl_launch(k_sweep_hist<8, kDepthHistItems, 4, true>, unsigned(ceil_div(n, kRsThreads * kDepthHistItems)), kRsThreads, 0, s,
         nullptr, src, cn, 8, dctl.ghist);
-    k_sweep_pass<8, kDepthItems, true, false><<<dblocks, kRsThreads, 0, s>>>(
+    pdl_launch(k_sweep_pass<8, kDepthItems, true, false>, dblocks, kRsThreads, 0, s,
         nullptr, nullptr, src, cn, 0, 0, dctl, DK[0], DV[0], nullptr, nullptr, nullptr);
-    k_sweep_pass<8, kDepthItems, false, false><<<dblocks, kRsThreads, 0, s>>>(
+    pdl_launch(k_sweep_pass<8, kDepthItems, false, false>, dblocks, kRsThreads, 0, s,
         DK[0], DV[0], src, cn, 8, 1, dctl, DK[1], DV[1], nullptr, nullptr, nullptr);
-    k_sweep_pass<8, kDepthItems, false, false><<<dblocks, kRsThreads, 0, s>>>(
+    pdl_launch(k_sweep_pass<8, kDepthItems, false, false>, dblocks, kRsThreads, 0, s,
         DK[1], DV[1], src, cn, 16, 2, dctl, DK[0], DV[0], nullptr, nullptr, nullptr);
-    k_sweep_pass<8, kDepthItems, false, true><<<dblocks, kRsThreads, 0, s>>>(
+    pdl_launch(k_sweep_pass<8, kDepthItems, false, true>, dblocks, kRsThreads, 0, s,
         DK[0], DV[0], src, cn, 24, 3, dctl, DK[1], DV[1], p.d_tiles_touched, tiles_sorted, nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -779,7 +786,7 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
     const SliceOut sl{reinterpret_cast<uint64_t*>(ws + plan.off_start), reinterpret_cast<uint2*>(ws + plan.off_rect),
                       reinterpret_cast<uint32_t*>(ws + plan.off_owner), uint32_t(plan.chunks),
                       ell ? p.d_ellipse : nullptr};
-    k_slices<<<unsigned(plan.slice_blocks), kSlThreads, 0, s>>>(
+    pdl_launch(k_slices, unsigned(plan.slice_blocks), kSlThreads, 0, s,
         cam, n, perm, tiles_sorted, p.d_means2d, p.d_radius, counters + 7,
         reinterpret_cast<unsigned long long*>(ws + plan.off_status_slices), error, result, sl);
     e = cudaGetLastError();
@@ -811,7 +818,7 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
     }
     {
         const unsigned rb = unsigned(std::min<size_t>(ceil_div(plan.capacity, 256), 152 * 16));
-        k_ranges<<<rb, 256, 0, s>>>(TK[0], ce, uint32_t(plan.n_tiles), tile_ranges);
+        pdl_launch(k_ranges, rb, 256, 0, s, TK[0], ce, uint32_t(plan.n_tiles), tile_ranges);
     }
     return cudaGetLastError();
 }

@@ -41,6 +41,7 @@ __device__ __forceinline__ float adam_one(const AdamTable& T, int act, float lr,
 }
 
 __global__ void __launch_bounds__(256) k_adam(AdamTable T) {
+    RS_PDL_ENTER();
     const size_t stride = size_t(gridDim.x) * blockDim.x;
     const size_t nq = T.qstart[T.n];
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nq; i += stride) {
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(256) k_adam(AdamTable T) {
 __global__ void __launch_bounds__(256) k_densify_stats(int n, const float* __restrict__ dm2,
                                                        const int* __restrict__ radius,
                                                        float* __restrict__ accum, float* __restrict__ count) {
+    RS_PDL_ENTER();
     const int stride = gridDim.x * blockDim.x;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         if (radius[i] > 0) {
@@ -116,7 +118,7 @@ cudaError_t launch_adam(const rs_adam_segment* segs, int n, double beta1, double
     const size_t total = std::max(T.qstart[n], T.tstart[n]);
     if (total == 0) return cudaSuccess;
     const unsigned blocks = unsigned(std::min<size_t>((total + 255) / 256, 152 * 16));
-    k_adam<<<blocks, 256, 0, s>>>(T);
+    pdl_launch(k_adam, blocks, 256, 0, s, T);
     return cudaGetLastError();
 }
 
@@ -124,7 +126,7 @@ cudaError_t launch_densify_stats(int n, const float* dm2, const int* radius, flo
                                  cudaStream_t s) {
     if (n == 0) return cudaSuccess;
     const unsigned blocks = unsigned(std::min((n + 255) / 256, 152 * 8));
-    k_densify_stats<<<blocks, 256, 0, s>>>(n, dm2, radius, accum, count);
+    pdl_launch(k_densify_stats, blocks, 256, 0, s, n, dm2, radius, accum, count);
     return cudaGetLastError();
 }
 

@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kProjThreads, kProjMinBlocks) k_project(Camera
                                                  float* depth, float* conic, float* color,
                                                  int* radius, uint32_t* tiles, Record* rec,
                                                  int tile_test, float* ellipse) {
+    RS_PDL_ENTER();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const size_t N = size_t(n);
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(kProjThreads, kProjMinBlocks) k_project_bwd(
     const int* __restrict__ radius, const float* __restrict__ dm2,
     const float* __restrict__ dcon, const float* __restrict__ dcol, float* dmeans,
     float* dscales, float* dquats, float* dsh) {
+    RS_PDL_ENTER();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const size_t N = size_t(n);
@@ -504,7 +506,7 @@ cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_p
     const int blocks = (g.n + threads - 1) / threads;
     Record* rec = reinterpret_cast<Record*>(o.d_records);
 #define RS_PROJECT(D)                                                                           \
-    k_project<D><<<blocks, threads, 0, s>>>(cam, g.n, g.d_means, g.d_scales, g.d_quats,         \
+    pdl_launch(k_project<D>, blocks, threads, 0, s, cam, g.n, g.d_means, g.d_scales, g.d_quats,         \
                                              g.d_opacity, g.d_sh, g.d_colors, o.d_means2d,      \
                                              o.d_depth, o.d_conic, o.d_color, o.d_radius,       \
                                              o.d_tiles_touched, rec, o.tile_test, o.d_ellipse)
@@ -527,7 +529,7 @@ cudaError_t launch_project_bwd(const CameraF& cam, const rs_gaussians& g, const 
     const int threads = kProjThreads;
     const int blocks = (g.n + threads - 1) / threads;
 #define RS_PROJECT_BWD(D)                                                                      \
-    k_project_bwd<D><<<blocks, threads, 0, s>>>(cam, g.n, g.d_means, g.d_scales, g.d_quats,    \
+    pdl_launch(k_project_bwd<D>, blocks, threads, 0, s, cam, g.n, g.d_means, g.d_scales, g.d_quats,    \
                                                  g.d_sh, p.d_radius, dm2, dcon, dcol, dmeans,  \
                                                  dscales, dquats, dsh)
     switch (g.sh_degree) {

@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
                                                            uint32_t* __restrict__ chunk_tile,
                                                            float4* __restrict__ ckpt, uint32_t slots,
                                                            const uint32_t* __restrict__ order) {
+    RS_PDL_ENTER();
     __shared__ FwdSmem sm;
     const uint32_t tile = order[blockIdx.x];
     const uint2 range = ranges[tile];
@@ -298,6 +299,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     const uint32_t* __restrict__ chunk_tile, const float4* __restrict__ ckpt, uint32_t slots,
     const float* __restrict__ dL_dimage, float* __restrict__ dm2, float* __restrict__ dcon,
     float* __restrict__ dop, float* __restrict__ dcol) {
+    RS_PDL_ENTER();
     __shared__ float4 s_p[kBwdWarps][32], s_q[kBwdWarps][32], s_c[kBwdWarps][32];
     __shared__ uint32_t s_g[kBwdWarps][32];
     const uint32_t n_tiles = uint32_t(cam.TX) * uint32_t(cam.TY);
@@ -447,6 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
 
 __global__ void k_fill_background(CameraF cam, float3 bg, float* image, float* final_T,
                                   uint32_t* n_contrib) {
+    RS_PDL_ENTER();
     const size_t HW = size_t(cam.W) * cam.H;
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < HW; i += size_t(gridDim.x) * blockDim.x) {
         image[i] = bg.x;
@@ -464,6 +467,7 @@ struct ZeroSpans {
 };
 
 __global__ void k_zero4(ZeroSpans z) {
+    RS_PDL_ENTER();
     const size_t stride = size_t(gridDim.x) * blockDim.x;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
@@ -513,6 +517,7 @@ __device__ __forceinline__ int tile_class(uint2 r) {
 
 __global__ void __launch_bounds__(kOrderThreads) k_tile_order(const uint2* __restrict__ ranges, uint32_t n_tiles,
                                                              uint32_t* __restrict__ order) {
+    RS_PDL_ENTER();
     __shared__ uint32_t s_cnt[kClasses][kOrderWarps];
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5, lt = (1u << lane) - 1u;
     // 1. per warp and class: the number of tiles
@@ -577,8 +582,8 @@ cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint3
                               uint32_t* n_contrib, void* ws, cudaStream_t s) {
     const int tiles = cam.TX * cam.TY;
     const RasterWs w = raster_ws(ws, capacity, size_t(tiles));
-    k_tile_order<<<1, kOrderThreads, 0, s>>>(reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order);
-    k_raster_fwd<<<tiles, kTilePixels, 0, s>>>(cam, rec, reinterpret_cast<const uint2*>(ranges), list,
+    pdl_launch(k_tile_order, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order);
+    pdl_launch(k_raster_fwd, tiles, kTilePixels, 0, s, cam, rec, reinterpret_cast<const uint2*>(ranges), list,
                                                bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
                                                w.order);
     return cudaGetLastError();
@@ -593,7 +598,7 @@ cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
     // one block per chunk of the capacity; chunks past the list's end return at once
     const unsigned blocks = unsigned((capacity + kChunk - 1) / kChunk);
     if (blocks == 0) return cudaSuccess;
-    k_raster_bwd<<<blocks, kBwdThreads, 0, s>>>(cam, n, rec, reinterpret_cast<const uint2*>(ranges), list, bg,
+    pdl_launch(k_raster_bwd, blocks, kBwdThreads, 0, s, cam, n, rec, reinterpret_cast<const uint2*>(ranges), list, bg,
                                                 final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
                                                 dL_dimage, dm2, dcon, dop, dcol);
     return cudaGetLastError();
@@ -603,7 +608,7 @@ cudaError_t launch_fill_background(const CameraF& cam, float3 bg, float* image, 
                                    uint32_t* n_contrib, cudaStream_t s) {
     const size_t HW = size_t(cam.W) * cam.H;
     const unsigned blocks = unsigned(std::min<size_t>((HW + 255) / 256, 152 * 16));
-    k_fill_background<<<blocks, 256, 0, s>>>(cam, bg, image, final_T, n_contrib);
+    pdl_launch(k_fill_background, blocks, 256, 0, s, cam, bg, image, final_T, n_contrib);
     return cudaGetLastError();
 }
 
@@ -612,7 +617,7 @@ cudaError_t launch_zero_grads(float* dm2, float* dcon, float* dop, float* dcol, 
     if (n == 0) return cudaSuccess;
     ZeroSpans z{{dm2, dcon, dop, dcol}, {2 * n, 3 * n, n, 3 * n}};
     const unsigned blocks = unsigned(std::min<size_t>((3 * n + 255) / 256, 152 * 8));
-    k_zero4<<<blocks, 256, 0, s>>>(z);
+    pdl_launch(k_zero4, blocks, 256, 0, s, z);
     return cudaGetLastError();
 }
 

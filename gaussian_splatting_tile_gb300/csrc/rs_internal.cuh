@@ -6,13 +6,43 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "rs.h"
 
 namespace rs {
 
+// Launches `kernel` on `s` with programmatic stream serialization (see RS_PDL_ENTER).
+template <typename... Params, typename... Args>
+inline cudaError_t pdl_launch(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Constants of the method (rigel README "Projection", "Rasterization"; learn-gs "11 - Tiles",
 // constants cell).
+// Programmatic dependent launch (Hopper and later): kernels of the frame are launched with
+// programmatic stream serialization, so a kernel's blocks are scheduled while its predecessor
+// drains.  Every kernel of the library begins with RS_PDL_ENTER(): it waits until the kernels
+// before it in the stream have completed and their writes are visible (so a kernel never reads
+// a predecessor's output early, and completion stays transitive along the stream), then lets
+// its own dependents be scheduled.  In a kernel launched without the attribute both are no-ops.
+#define RS_PDL_ENTER()                                              \
+    do {                                                            \
+        asm volatile("griddepcontrol.wait;" ::: "memory");          \
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); \
+    } while (0)
+
 constexpr int kTile = RS_TILE;
 constexpr int kTilePixels = kTile * kTile;
 constexpr float kDilation = 0.3f;      // EWA low-pass added to the 2D covariance diagonal
