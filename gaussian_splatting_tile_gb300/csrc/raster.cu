@@ -33,7 +33,7 @@ constexpr unsigned kFull = 0xffffffffu;
 #define RS_FWD_MIN_BLOCKS 6
 #endif
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS 8  // blocks of 128 threads
+#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : 8)  // resident backward blocks per SM
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -261,15 +261,24 @@ constexpr int kSums = 9;  // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2
 // column, so their nine sums fold before one reduce-scatter over the warp, and nine lanes each
 // add one of the sums to the Gaussian's gradient with a global atomic.  There is no block-wide
 // barrier.
-constexpr int kBwdThreads = 128;
-constexpr int kBwdWarps = kBwdThreads / 32;
+// Pixels per lane, stacked 4 rows apart in one column (2: warps of 8x8; 4: warps of 8x16, which
+// cut the warp-entries by a third but measured 0.293 -> 0.303 ms with more registers per lane).
+#ifndef RS_BWD_PX
+#define RS_BWD_PX 2
+#endif
+constexpr int kBwdPx = RS_BWD_PX;
+static_assert(kBwdPx == 2 || kBwdPx == 4, "two or four pixels per lane");
+constexpr int kSqH = 4 * kBwdPx;                 // rows of a warp's area (8 columns wide)
+constexpr int kBwdWarps = 2 * (kTile / kSqH);    // warps per tile
+constexpr int kBwdThreads = 32 * kBwdWarps;
 
-// True when the entry's alpha >= 1/255 box meets the 8x8 pixel square with corner (ox, oy).
+// True when the entry's alpha >= 1/255 box meets the warp's 8 x kSqH pixel area with corner
+// (ox, oy).
 __device__ __forceinline__ bool square_hit(const float4& p, const float4& q, float ox, float oy) {
     if (!(p.w >= 0.f)) return false;
     const float xl = p.x - p.w - ox, xh = p.x + p.w - ox;
     const float yl = p.y - q.w - oy, yh = p.y + q.w - oy;
-    return xl <= 7.f && xh >= 0.f && yl <= 7.f && yh >= 0.f;
+    return xl <= 7.f && xh >= 0.f && yl <= float(kSqH - 1) && yh >= 0.f;
 }
 
 // Per-pixel state of the reverse walk.
@@ -328,13 +337,13 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
         // the piece [pa, pb) of this tile's list
         const uint32_t pb = min(range.y, a1);
         const int tx0 = int(tile % uint32_t(cam.TX)) * kTile, ty0 = int(tile / uint32_t(cam.TX)) * kTile;
-        const int sx = tx0 + (warp & 1) * 8, sy = ty0 + (warp >> 1) * 8;
+        const int sx = tx0 + (warp & 1) * 8, sy = ty0 + (warp >> 1) * kSqH;
         const int px = sx + int(lane & 7);
         const int py0 = sy + int(lane >> 3);
         const uint32_t len = range.y - range.x;
-        BwdPixel P[2];
+        BwdPixel P[kBwdPx];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kBwdPx; ++h) {
             const int py = py0 + 4 * h;
             const bool inside = px < cam.W && py < cam.H;
             const size_t pix = inside ? size_t(py) * cam.W + px : 0;
@@ -365,8 +374,11 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 }
             }
         }
-        const uint32_t warp_end = __reduce_max_sync(kFull, max(P[0].end, P[1].end));
-        const float fx = float(px), fy0 = float(py0), fy1 = float(py0 + 4);
+        uint32_t lane_end = P[0].end;
+#pragma unroll
+        for (int h = 1; h < kBwdPx; ++h) lane_end = max(lane_end, P[h].end);
+        const uint32_t warp_end = __reduce_max_sync(kFull, lane_end);
+        const float fx = float(px), fy0 = float(py0);
         const float ox = float(sx), oy = float(sy);
         for (uint32_t hi = warp_end; hi > pa;) {
             const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
@@ -391,28 +403,48 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 m ^= 1u << j;
                 const uint32_t ej = lo + uint32_t(j);
                 const float4 p = s_p[warp][j], q = s_q[warp][j];
-                float dx, dy0, dy1, al0, raw0, al1, raw1;
-                entry_alpha_col(p, q, fx, fy0, fy1, dx, dy0, dy1, al0, raw0, al1, raw1);
-                const bool act0 = ej < P[0].end && al0 >= kAlphaMin;
-                const bool act1 = ej < P[1].end && al1 >= kAlphaMin;
-                float gp0 = 0.f, gp1 = 0.f, w0 = 0.f, w1 = 0.f;
+                // the lane's pixels share a column: dx and its terms are common (the same
+                // arithmetic as entry_alpha, pixel by pixel)
+                const float dx = fx - p.x;
+                const float bx = q.y * dx, axx = (q.x * dx) * dx;
+                float dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
+                bool any = false;
                 const float4 c = s_c[warp][j];
-                if (act0) bwd_step(P[0], al0, raw0, c, gp0, w0);
-                if (act1) bwd_step(P[1], al1, raw1, c, gp1, w1);
-                if (__any_sync(kFull, act0 || act1)) {
-                    // the two pixels share dx: fold their sums, then reduce over the warp
-                    const float sg = gp0 + gp1;
-                    const float sgy = fmaf(gp1, dy1, gp0 * dy0);
+#pragma unroll
+                for (int h = 0; h < kBwdPx; ++h) {
+                    dy[h] = (fy0 + float(4 * h)) - p.y;
+                    const float raw = p.z * ex2_approx(fmaf(dy[h], fmaf(q.z, dy[h], bx), axx));
+                    const float al = fminf(kAlphaMax, raw);
+                    const bool act = ej < P[h].end && al >= kAlphaMin;
+                    gp[h] = 0.f;
+                    w[h] = 0.f;
+                    if (act) bwd_step(P[h], al, raw, c, gp[h], w[h]);
+                    any |= act;
+                }
+                if (__any_sync(kFull, any)) {
+                    // the lane's pixels share dx: fold their sums, then reduce over the warp
+                    float sg = gp[0], sgy = gp[0] * dy[0], sgyy = (gp[0] * dy[0]) * dy[0];
+                    float c0 = w[0] * P[0].G0, c1 = w[0] * P[0].G1, c2 = w[0] * P[0].G2;
+#pragma unroll
+                    for (int h = 1; h < kBwdPx; ++h) {
+                        sg += gp[h];
+                        const float t = gp[h] * dy[h];
+                        sgy += t;
+                        sgyy = fmaf(t, dy[h], sgyy);
+                        c0 = fmaf(w[h], P[h].G0, c0);
+                        c1 = fmaf(w[h], P[h].G1, c1);
+                        c2 = fmaf(w[h], P[h].G2, c2);
+                    }
                     float v[kSums];
                     v[0] = sg * dx;
                     v[1] = sgy;
                     v[2] = v[0] * dx;
                     v[3] = sgy * dx;
-                    v[4] = fmaf(gp1 * dy1, dy1, (gp0 * dy0) * dy0);
+                    v[4] = sgyy;
                     v[5] = sg;
-                    v[6] = fmaf(w1, P[1].G0, w0 * P[0].G0);
-                    v[7] = fmaf(w1, P[1].G1, w0 * P[0].G1);
-                    v[8] = fmaf(w1, P[1].G2, w0 * P[0].G2);
+                    v[6] = c0;
+                    v[7] = c1;
+                    v[8] = c2;
                     const float sum = butterfly9(v, lane);
                     const float other = __shfl_xor_sync(kFull, sum, 2);  // slots 0 and 1: lanes 0 and 2
                     if (slot >= 0) {
