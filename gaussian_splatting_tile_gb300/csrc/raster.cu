@@ -25,26 +25,37 @@ constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per th
 constexpr uint32_t kChunk = RS_RASTER_CHUNK;  // backward task length and checkpoint spacing
 static_assert(kChunk == uint32_t(kBatch), "a forward batch ends at every chunk boundary");
 constexpr int kWarps = kTilePixels / 32;
+// The forward covers a tile with kFwdHalves blocks: 1 (256 threads, the whole 16x16 tile) or 2
+// (128 threads, a 16x8 half each, so a batch's barrier waits for 4 warps instead of 8; measured
+// 0.129 -> 0.132 ms: each half stages the whole list).
+#ifndef RS_FWD_HALVES
+#define RS_FWD_HALVES 1
+#endif
+constexpr int kFwdHalves = RS_FWD_HALVES;
+constexpr int kFwdThreads = kTilePixels / kFwdHalves;
+constexpr int kFwdWarps = kFwdThreads / 32;
+constexpr int kFwdRows = kTile / kFwdHalves;  // pixel rows of a block
 constexpr unsigned kFull = 0xffffffffu;
 
 // Resident blocks per SM the compositing kernels are compiled for (register budget per thread =
 // 65536 / (256 x blocks)).
 #ifndef RS_FWD_MIN_BLOCKS
-#define RS_FWD_MIN_BLOCKS 6
+#define RS_FWD_MIN_BLOCKS (6 * RS_FWD_HALVES)
 #endif
 #ifndef RS_BWD_MIN_BLOCKS
 #define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : 8)  // resident backward blocks per SM
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
-// (w >> 1) * 4 of the tile; lane l is pixel (l & 7, l >> 3) inside it.
-__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int& tx0, int& ty0, int& px,
+// (w >> 1) * 4 of the block's rows (from row0 of the tile); lane l is pixel (l & 7, l >> 3)
+// inside it.
+__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int row0, int& tx0, int& ty0, int& px,
                                            int& py) {
     tx0 = (tile % cam.TX) * kTile;
     ty0 = (tile / cam.TX) * kTile;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     px = tx0 + (warp & 1) * 8 + (lane & 7);
-    py = ty0 + (warp >> 1) * 4 + (lane >> 3);
+    py = ty0 + row0 + (warp >> 1) * 4 + (lane >> 3);
 }
 
 // Bit w is set when warp w's 8x4 pixel rectangle meets the entry's alpha >= 1/255 box
@@ -58,7 +69,7 @@ __device__ __forceinline__ uint32_t warp_mask(const float4& p, const float4& q, 
     const bool c1 = xl <= 15.f && xh >= 8.f;
     uint32_t m = 0u;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kFwdWarps / 2; ++r) {
         const bool row = yl <= float(4 * r + 3) && yh >= float(4 * r);
         m |= (row && c0 ? 1u : 0u) << (2 * r);
         m |= (row && c1 ? 1u : 0u) << (2 * r + 1);
@@ -89,7 +100,7 @@ __device__ __forceinline__ int compact_warp(uint8_t* list, Hit hit) {
 struct FwdSmem {
     float4 p[kBatch], q[kBatch], c[kBatch];
     uint32_t mask[kBatch];
-    uint8_t list[kWarps][kBatch];
+    uint8_t list[kFwdWarps][kBatch];
 };
 
 // The forward of one tile.  SPLIT: the tile's list crosses a chunk boundary of the point list,
@@ -103,8 +114,9 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
                                                 uint32_t* __restrict__ n_contrib, float4* __restrict__ ckpt,
                                                 uint32_t slots, FwdSmem& sm) {
     const int warp = threadIdx.x >> 5;
+    const int row0 = int(blockIdx.x % kFwdHalves) * kFwdRows;
     int tx0, ty0, px, py;
-    tile_pixel(cam, int(tile), tx0, ty0, px, py);
+    tile_pixel(cam, int(tile), row0, tx0, ty0, px, py);
     const bool inside = px < cam.W && py < cam.H;
     const float fx = float(px), fy = float(py);
     float T = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
@@ -122,18 +134,22 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
             if (base / kChunk < slots) ckpt[size_t(base / kChunk) * kTilePixels + lidx] = make_float4(D0, D1, D2, T);
             D0 = D1 = D2 = 0.f;
         }
-        // every thread reaches this barrier; the block leaves once all 256 pixels are done
-        if (__syncthreads_count(done) == kBatch) break;
-        const uint32_t e = base + threadIdx.x;
-        uint32_t m = 0u;
-        if (e < bend) {
-            const Record& r = rec[list[e]];
-            sm.p[threadIdx.x] = r.p;
-            sm.q[threadIdx.x] = r.q;
-            sm.c[threadIdx.x] = r.c;
-            m = warp_mask(r.p, r.q, tx0, ty0);
+        // every thread reaches this barrier; the block leaves once all its pixels are done
+        if (__syncthreads_count(done) == kFwdThreads) break;
+#pragma unroll
+        for (int k = 0; k < kFwdHalves; ++k) {
+            const int t = k * kFwdThreads + int(threadIdx.x);
+            const uint32_t e = base + uint32_t(t);
+            uint32_t m = 0u;
+            if (e < bend) {
+                const Record& r = rec[list[e]];
+                sm.p[t] = r.p;
+                sm.q[t] = r.q;
+                sm.c[t] = r.c;
+                m = warp_mask(r.p, r.q, tx0, ty0 + row0);
+            }
+            sm.mask[t] = m;
         }
-        sm.mask[threadIdx.x] = m;
         __syncthreads();
         if (__all_sync(kFull, done)) continue;
         const int nl = compact_warp(my_list, [&](int j) { return (sm.mask[j] & wbit) != 0u; });
@@ -186,7 +202,7 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
     }
 }
 
-__global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
+__global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
                                                            const uint2* __restrict__ ranges,
                                                            const uint32_t* __restrict__ list,
                                                            float3 bg, float* __restrict__ image,
@@ -197,13 +213,14 @@ __global__ void __launch_bounds__(kTilePixels, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
                                                            const uint32_t* __restrict__ order) {
     RS_PDL_ENTER();
     __shared__ FwdSmem sm;
-    const uint32_t tile = order[blockIdx.x];
+    const uint32_t tile = order[blockIdx.x / kFwdHalves];
     const uint2 range = ranges[tile];
     // the tile's list positions that are multiples of the chunk size are the backward's task
     // starts: record which tile holds them
-    for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
-         c += kTilePixels)
-        chunk_tile[c] = tile;
+    if (blockIdx.x % kFwdHalves == 0)
+        for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
+             c += kFwdThreads)
+            chunk_tile[c] = tile;
     if (range.y > range.x && (range.y - 1u) / kChunk > range.x / kChunk)
         raster_fwd_tile<true>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, sm);
     else
@@ -615,7 +632,7 @@ cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint3
     const int tiles = cam.TX * cam.TY;
     const RasterWs w = raster_ws(ws, capacity, size_t(tiles));
     pdl_launch(k_tile_order, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order);
-    pdl_launch(k_raster_fwd, tiles, kTilePixels, 0, s, cam, rec, reinterpret_cast<const uint2*>(ranges), list,
+    pdl_launch(k_raster_fwd, tiles * kFwdHalves, kFwdThreads, 0, s, cam, rec, reinterpret_cast<const uint2*>(ranges), list,
                                                bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
                                                w.order);
     return cudaGetLastError();
