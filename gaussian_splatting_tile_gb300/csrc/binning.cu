@@ -375,11 +375,27 @@ __global__ void __launch_bounds__(kSlThreads) k_slices(CameraF cam, uint32_t n, 
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t i0 = blk * kSlGauss + threadIdx.x * kSlItems;
     uint32_t cnt[kSlItems];
+    uint2 rect[kSlItems];
     uint64_t run = 0;
 #pragma unroll
     for (int k = 0; k < kSlItems; ++k) {
         cnt[k] = i0 + k < n ? tiles_sorted[i0 + k] : 0u;
         run += cnt[k];
+    }
+    // the tile rectangles (gathers through the depth order) before the look-back, so that their
+    // loads overlap it
+#pragma unroll
+    for (int k = 0; k < kSlItems; ++k) {
+        rect[k] = make_uint2(0u, 1u);
+        if (cnt[k]) {
+            const uint32_t g = perm[i0 + k];
+            const float u = means2d[g], v = means2d[size_t(n) + g];
+            const float rad = float(radius[g]);
+            const int xl = span_bound(u, rad, cam.TX, false), xh = span_bound(u, rad, cam.TX, true);
+            const int yl = span_bound(v, rad, cam.TY, false);
+            // >= 1 whenever tiles_touched > 0 came from the projection (same span arithmetic)
+            rect[k] = make_uint2(uint32_t(xl) | (uint32_t(yl) << 16), uint32_t(max(xh - xl, 1)));
+        }
     }
     uint64_t x = run;
 #pragma unroll
@@ -439,21 +455,13 @@ __global__ void __launch_bounds__(kSlThreads) k_slices(CameraF cam, uint32_t n, 
         const uint32_t i = i0 + k;
         if (i < n) {
             out.start[i] = start;
-            uint2 r = make_uint2(0u, 1u);
             if (cnt[k]) {
-                const uint32_t g = perm[i];
-                const float u = means2d[g], v = means2d[size_t(n) + g];
-                const float rad = float(radius[g]);
-                const int xl = span_bound(u, rad, cam.TX, false), xh = span_bound(u, rad, cam.TX, true);
-                const int yl = span_bound(v, rad, cam.TY, false);
-                // >= 1 whenever tiles_touched > 0 came from the projection (same span arithmetic)
-                r = make_uint2(uint32_t(xl) | (uint32_t(yl) << 16), uint32_t(max(xh - xl, 1)));
                 // chunks whose first entry falls in this slice
                 const uint64_t end = start + cnt[k];
                 for (uint64_t c = (start + kExpChunk - 1) / kExpChunk; c * kExpChunk < end && c < out.chunks; ++c)
                     out.owner[c] = i;
             }
-            out.rect[i] = r;
+            out.rect[i] = rect[k];
         }
         start += cnt[k];
     }
@@ -476,8 +484,13 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
     RS_PDL_ENTER();
     constexpr int R = 1 << RBITS;
     constexpr int ROWS = ELL ? kRowCap : 1;
-    __shared__ uint64_t s_start[kExpChunk + 1];
-    __shared__ uint2 s_rect[ELL ? 1 : kExpChunk];
+    // entries per block: 2048 for the square test (752 blocks of 5 per SM hold a 1080p frame's
+    // 1.54 M entries in one wave), 1024 with the ellipse test's row tables; the slice scan
+    // records the owner of every 1024th entry
+    constexpr int CH = ELL ? kExpChunk : 2 * kExpChunk;
+    constexpr int OWN = CH / kExpChunk;
+    __shared__ uint64_t s_start[CH + 1];
+    __shared__ uint2 s_rect[ELL ? 1 : CH];
     __shared__ uint32_t s_rowstart[ELL ? kExpChunk + 1 : 1];
     __shared__ uint32_t s_w[kExpThreads / 32];
     // ellipse mode, dynamic: the window's tile rows (ylo | yhi << 16) [kExpChunk], then the row
@@ -488,22 +501,22 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
     uint32_t* s_rowcum = reinterpret_cast<uint32_t*>(s_dyn + (ELL ? kExpChunk : 0));
     uint32_t* s_rowtile = s_rowcum + ROWS;
     uint16_t* s_rowg = reinterpret_cast<uint16_t*>(s_rowtile + ROWS);  // window index of the row's Gaussian
-    __shared__ uint32_t s_g[kExpChunk];
+    __shared__ uint32_t s_g[CH];
     __shared__ uint32_t s_h[3][R];
     const uint32_t E = count.get();
-    const uint32_t chunks = (E + kExpChunk - 1) / kExpChunk;
+    const uint32_t chunks = (E + CH - 1) / CH;
     if (blockIdx.x >= chunks) return;
     for (int i = threadIdx.x; i < 3 * R; i += kExpThreads) (&s_h[0][0])[i] = 0u;
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t tiles_total = uint32_t(cam.TX) * uint32_t(cam.TY);
     for (uint32_t c = blockIdx.x; c < chunks; c += gridDim.x) {
-        const uint32_t e0 = c * kExpChunk;
+        const uint32_t e0 = c * CH;
         // owners of the chunk's entries: depth positions i0 ..= i1.  Every Gaussian before the
         // culled tail of the depth order has at least one entry, so there are at most 1024 of
         // them; the slice after i1 starts past the chunk.
-        const uint32_t i0 = sl.owner[c];
-        const uint32_t i1 = c + 1 < chunks ? sl.owner[c + 1] : min(i0 + uint32_t(kExpChunk) - 1u, n - 1u);
-        const int w = int(min(i1 - i0 + 1u, uint32_t(kExpChunk)));
+        const uint32_t i0 = sl.owner[OWN * c];
+        const uint32_t i1 = c + 1 < chunks ? sl.owner[OWN * (c + 1)] : min(i0 + uint32_t(CH) - 1u, n - 1u);
+        const int w = int(min(i1 - i0 + 1u, uint32_t(CH)));
         __syncthreads();  // the previous chunk is done with the window
         for (int j = threadIdx.x; j <= w; j += kExpThreads) {
             const uint32_t i = i0 + uint32_t(j);
@@ -588,7 +601,7 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
         }
         __syncthreads();
 #pragma unroll
-        for (int k = 0; k < kExpChunk / kExpThreads; ++k) {
+        for (int k = 0; k < CH / kExpThreads; ++k) {
             const uint32_t e = e0 + k * kExpThreads + threadIdx.x;
             const bool valid = e < E;
             uint32_t tile = 0u;
@@ -716,7 +729,8 @@ __global__ void k_report(const uint64_t* __restrict__ result, uint64_t* __restri
 template <int RBITS>
 void expand_launch(const CameraF& cam, uint32_t n, Count ce, const uint32_t* perm, const SliceOut& sl, int digit,
                    int passes, uint32_t* ghist, uint32_t* tk, uint32_t* tv, const rs_projected& p, cudaStream_t s) {
-    const unsigned blocks = unsigned(std::min<size_t>(sl.chunks, 152 * 8));
+    const size_t per = p.tile_test == RS_TILE_TEST_ELLIPSE ? 1 : 2;  // 1024-entry chunks per block
+    const unsigned blocks = unsigned(std::min<size_t>((sl.chunks + per - 1) / per, 152 * 8));
     if (p.tile_test == RS_TILE_TEST_ELLIPSE) {
         constexpr size_t smem = (kExpChunk + 2 * kRowCap) * sizeof(float) + kRowCap * sizeof(uint16_t);
         if (cudaFuncSetAttribute(k_expand<RBITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
