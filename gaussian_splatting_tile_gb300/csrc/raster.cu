@@ -25,37 +25,28 @@ constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per th
 constexpr uint32_t kChunk = RS_RASTER_CHUNK;  // backward task length and checkpoint spacing
 static_assert(kChunk == uint32_t(kBatch), "a forward batch ends at every chunk boundary");
 constexpr int kWarps = kTilePixels / 32;
-// The forward covers a tile with kFwdHalves blocks: 1 (256 threads, the whole 16x16 tile) or 2
-// (128 threads, a 16x8 half each, so a batch's barrier waits for 4 warps instead of 8; measured
-// 0.129 -> 0.132 ms: each half stages the whole list).
-#ifndef RS_FWD_HALVES
-#define RS_FWD_HALVES 1
-#endif
-constexpr int kFwdHalves = RS_FWD_HALVES;
-constexpr int kFwdThreads = kTilePixels / kFwdHalves;
+constexpr int kFwdThreads = kTilePixels;  // the forward: one block of 256 threads per tile
 constexpr int kFwdWarps = kFwdThreads / 32;
-constexpr int kFwdRows = kTile / kFwdHalves;  // pixel rows of a block
 constexpr unsigned kFull = 0xffffffffu;
 
 // Resident blocks per SM the compositing kernels are compiled for (register budget per thread =
 // 65536 / (256 x blocks)).
 #ifndef RS_FWD_MIN_BLOCKS
-#define RS_FWD_MIN_BLOCKS (6 * RS_FWD_HALVES)
+#define RS_FWD_MIN_BLOCKS 6
 #endif
 #ifndef RS_BWD_MIN_BLOCKS
 #define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : 8)  // resident backward blocks per SM
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
-// (w >> 1) * 4 of the block's rows (from row0 of the tile); lane l is pixel (l & 7, l >> 3)
-// inside it.
-__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int row0, int& tx0, int& ty0, int& px,
+// (w >> 1) * 4 of the tile; lane l is pixel (l & 7, l >> 3) inside it.
+__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int& tx0, int& ty0, int& px,
                                            int& py) {
     tx0 = (tile % cam.TX) * kTile;
     ty0 = (tile / cam.TX) * kTile;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     px = tx0 + (warp & 1) * 8 + (lane & 7);
-    py = ty0 + row0 + (warp >> 1) * 4 + (lane >> 3);
+    py = ty0 + (warp >> 1) * 4 + (lane >> 3);
 }
 
 // Bit w is set when warp w's 8x4 pixel rectangle meets the entry's alpha >= 1/255 box
@@ -101,7 +92,16 @@ struct FwdSmem {
     float4 p[kBatch], q[kBatch], c[kBatch];
     uint32_t mask[kBatch];
     uint8_t list[kFwdWarps][kBatch];
+    uint8_t comp[kFwdWarps][kBatch];  // 1 where some pixel of the warp composited the entry
 };
+
+// Entry j of the staged batch: bit w set when warp w composited it at some pixel.
+__device__ __forceinline__ uint8_t comp_byte(const FwdSmem& sm, int j) {
+    uint32_t b = 0u;
+#pragma unroll
+    for (int w = 0; w < kFwdWarps; ++w) b |= uint32_t(sm.comp[w][j]) << w;
+    return uint8_t(b);
+}
 
 // The forward of one tile.  SPLIT: the tile's list crosses a chunk boundary of the point list,
 // so each pixel also sums the colour of every stretch between boundaries and records its state
@@ -112,11 +112,10 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
                                                 const uint32_t* __restrict__ list, float3 bg,
                                                 float* __restrict__ image, float* __restrict__ final_T,
                                                 uint32_t* __restrict__ n_contrib, float4* __restrict__ ckpt,
-                                                uint32_t slots, FwdSmem& sm) {
+                                                uint32_t slots, uint8_t* __restrict__ comp, FwdSmem& sm) {
     const int warp = threadIdx.x >> 5;
-    const int row0 = int(blockIdx.x % kFwdHalves) * kFwdRows;
     int tx0, ty0, px, py;
-    tile_pixel(cam, int(tile), row0, tx0, ty0, px, py);
+    tile_pixel(cam, int(tile), tx0, ty0, px, py);
     const bool inside = px < cam.W && py < cam.H;
     const float fx = float(px), fy = float(py);
     float T = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
@@ -128,6 +127,7 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
     const int lidx = (py - ty0) * kTile + (px - tx0);
     // batches end at the chunk boundaries of the point list; at each boundary inside the list a
     // pixel still going records T and the colour its previous stretch added
+    uint32_t pbase = 0u, pend = 0u;  // the previous batch, whose composited flags go out next
     for (uint32_t base = range.x, bend; base < range.y; base = bend) {
         bend = min(range.y, (base / kChunk + 1) * kChunk);
         if (SPLIT && base != range.x && !done) {
@@ -135,22 +135,27 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
             D0 = D1 = D2 = 0.f;
         }
         // every thread reaches this barrier; the block leaves once all its pixels are done
-        if (__syncthreads_count(done) == kFwdThreads) break;
-#pragma unroll
-        for (int k = 0; k < kFwdHalves; ++k) {
-            const int t = k * kFwdThreads + int(threadIdx.x);
-            const uint32_t e = base + uint32_t(t);
-            uint32_t m = 0u;
-            if (e < bend) {
-                const Record& r = rec[list[e]];
-                sm.p[t] = r.p;
-                sm.q[t] = r.q;
-                sm.c[t] = r.c;
-                m = warp_mask(r.p, r.q, tx0, ty0 + row0);
-            }
-            sm.mask[t] = m;
+        const int ndone = __syncthreads_count(done);
+        if (pbase + threadIdx.x < pend) comp[pbase + threadIdx.x] = comp_byte(sm, threadIdx.x);
+        pbase = base;
+        pend = 0u;
+        if (ndone == kFwdThreads) break;
+        pend = bend;
+        const uint32_t e = base + threadIdx.x;
+        uint32_t m = 0u;
+        if (e < bend) {
+            const Record& r = rec[list[e]];
+            sm.p[threadIdx.x] = r.p;
+            sm.q[threadIdx.x] = r.q;
+            sm.c[threadIdx.x] = r.c;
+            m = warp_mask(r.p, r.q, tx0, ty0);
         }
+        sm.mask[threadIdx.x] = m;
         __syncthreads();
+        // this warp's composited flags for the batch (the previous batch's were gathered before
+        // the barrier above)
+        reinterpret_cast<uint2*>(sm.comp[warp])[threadIdx.x & 31] = make_uint2(0u, 0u);
+        __syncwarp();
         if (__all_sync(kFull, done)) continue;
         const int nl = compact_warp(my_list, [&](int j) { return (sm.mask[j] & wbit) != 0u; });
         if (done) continue;
@@ -159,6 +164,7 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
             float dx, dy, G, raw;
             const float alpha = entry_alpha(sm.p[j], sm.q[j], fx, fy, dx, dy, G, raw);
             if (alpha < kAlphaMin) continue;
+            sm.comp[warp][j] = 1u;  // every lane that composites stores the same flag
             const float4 c = sm.c[j];
             const float w = alpha * T;
             C0 = fmaf(c.x, w, C0);
@@ -177,6 +183,8 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
             }
         }
     }
+    __syncthreads();
+    if (pbase + threadIdx.x < pend) comp[pbase + threadIdx.x] = comp_byte(sm, threadIdx.x);
     if (inside) {
         const size_t HW = size_t(cam.W) * cam.H, pix = size_t(py) * cam.W + px;
         image[pix] = fmaf(T, bg.x, C0);
@@ -210,21 +218,21 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
                                                            uint32_t* __restrict__ n_contrib,
                                                            uint32_t* __restrict__ chunk_tile,
                                                            float4* __restrict__ ckpt, uint32_t slots,
-                                                           const uint32_t* __restrict__ order) {
+                                                           const uint32_t* __restrict__ order,
+                                                           uint8_t* __restrict__ comp) {
     RS_PDL_ENTER();
     __shared__ FwdSmem sm;
-    const uint32_t tile = order[blockIdx.x / kFwdHalves];
+    const uint32_t tile = order[blockIdx.x];
     const uint2 range = ranges[tile];
     // the tile's list positions that are multiples of the chunk size are the backward's task
     // starts: record which tile holds them
-    if (blockIdx.x % kFwdHalves == 0)
-        for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
-             c += kFwdThreads)
-            chunk_tile[c] = tile;
+    for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
+         c += kFwdThreads)
+        chunk_tile[c] = tile;
     if (range.y > range.x && (range.y - 1u) / kChunk > range.x / kChunk)
-        raster_fwd_tile<true>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, sm);
+        raster_fwd_tile<true>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
     else
-        raster_fwd_tile<false>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, sm);
+        raster_fwd_tile<false>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
 }
 
 // Reduce-scatter of nine per-lane values over the warp in five xor-shuffle steps (9 -> 5 -> 3
@@ -323,8 +331,8 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     const uint32_t* __restrict__ list, float3 bg,
     const float* __restrict__ final_T, const uint32_t* __restrict__ n_contrib,
     const uint32_t* __restrict__ chunk_tile, const float4* __restrict__ ckpt, uint32_t slots,
-    const float* __restrict__ dL_dimage, float* __restrict__ dm2, float* __restrict__ dcon,
-    float* __restrict__ dop, float* __restrict__ dcol) {
+    const uint8_t* __restrict__ comp, const float* __restrict__ dL_dimage, float* __restrict__ dm2,
+    float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol) {
     RS_PDL_ENTER();
     __shared__ float4 s_p[kBwdWarps][32], s_q[kBwdWarps][32], s_c[kBwdWarps][32];
     __shared__ uint32_t s_g[kBwdWarps][32];
@@ -397,6 +405,11 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
         const uint32_t warp_end = __reduce_max_sync(kFull, lane_end);
         const float fx = float(px), fy0 = float(py0);
         const float ox = float(sx), oy = float(sy);
+        // the forward's warps (8x4 pixels) inside this warp's area: an entry none of them
+        // composited has no active pixel here
+        uint32_t fwarps = 0u;
+#pragma unroll
+        for (int r = 0; r < kSqH / 4; ++r) fwarps |= 1u << (((sy - ty0) / 4 + r) * 2 + (warp & 1));
         for (uint32_t hi = warp_end; hi > pa;) {
             const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
             const uint32_t e = lo + lane;
@@ -405,7 +418,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 const uint32_t g = list[e];
                 const Record& r = rec[g];
                 const float4 p = r.p, q = r.q, c = r.c;
-                hit = square_hit(p, q, ox, oy);
+                hit = (uint32_t(comp[e]) & fwarps) != 0u && square_hit(p, q, ox, oy);
                 if (hit) {
                     s_p[warp][lane] = p;
                     s_q[warp][lane] = q;
@@ -531,6 +544,7 @@ struct RasterWs {
     uint32_t* chunk_tile;   // [slots] tile holding list position 256 c
     float4* ckpt;           // [slots][256] the forward's state at position 256 c
     uint32_t* order;        // [n_tiles] tiles in the forward's order
+    uint8_t* comp;          // [capacity] per entry: the forward warps (8x4 pixels) that composited it
     uint32_t slots;
 };
 size_t align256z(size_t x) { return (x + 255) & ~size_t(255); }
@@ -544,7 +558,9 @@ RasterWs raster_ws(void* ws, size_t capacity, size_t n_tiles, size_t* bytes = nu
     w.order = reinterpret_cast<uint32_t*>(b + o);
     o = align256z(o + n_tiles * sizeof(uint32_t));
     w.ckpt = reinterpret_cast<float4*>(b + o);
-    o += slots * kTilePixels * sizeof(float4);
+    o = align256z(o + slots * kTilePixels * sizeof(float4));
+    w.comp = b + o;
+    o += capacity;
     w.slots = uint32_t(slots);
     if (bytes) *bytes = o;
     return w;
@@ -632,9 +648,9 @@ cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint3
     const int tiles = cam.TX * cam.TY;
     const RasterWs w = raster_ws(ws, capacity, size_t(tiles));
     pdl_launch(k_tile_order, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order);
-    pdl_launch(k_raster_fwd, tiles * kFwdHalves, kFwdThreads, 0, s, cam, rec, reinterpret_cast<const uint2*>(ranges), list,
+    pdl_launch(k_raster_fwd, tiles, kFwdThreads, 0, s, cam, rec, reinterpret_cast<const uint2*>(ranges), list,
                                                bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
-                                               w.order);
+                                               w.order, w.comp);
     return cudaGetLastError();
 }
 
@@ -648,7 +664,7 @@ cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
     const unsigned blocks = unsigned((capacity + kChunk - 1) / kChunk);
     if (blocks == 0) return cudaSuccess;
     pdl_launch(k_raster_bwd, blocks, kBwdThreads, 0, s, cam, n, rec, reinterpret_cast<const uint2*>(ranges), list, bg,
-                                                final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
+                                                final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots, w.comp,
                                                 dL_dimage, dm2, dcon, dop, dcol);
     return cudaGetLastError();
 }

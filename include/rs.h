@@ -176,6 +176,7 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
 /* Compositing workspace: the forward's per-pixel state at every RS_RASTER_CHUNK-th position of
  * the point list that falls inside a tile's list, and which tile holds each such position (the
  * backward reads both to walk every 256-entry stretch of the point list as a task of its own);
+ * per entry, which 8x4-pixel groups of its tile composited it (the backward skips the others);
  * and the order in which the forward takes the tiles (longest lists first).
  * Returns the bytes a point list of `capacity` entries needs for this camera's tile grid; 0 for
  * an invalid camera or capacity > RS_MAX_ENTRIES.  Host-only (no GPU work). */
