@@ -24,7 +24,6 @@ namespace {
 constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per thread
 constexpr uint32_t kChunk = RS_RASTER_CHUNK;  // backward task length and checkpoint spacing
 static_assert(kChunk == uint32_t(kBatch), "a forward batch ends at every chunk boundary");
-constexpr int kWarps = kTilePixels / 32;
 constexpr int kFwdThreads = kTilePixels;  // the forward: one block of 256 threads per tile
 constexpr int kFwdWarps = kFwdThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
@@ -297,15 +296,6 @@ constexpr int kSqH = 4 * kBwdPx;                 // rows of a warp's area (8 col
 constexpr int kBwdWarps = 2 * (kTile / kSqH);    // warps per tile
 constexpr int kBwdThreads = 32 * kBwdWarps;
 
-// True when the entry's alpha >= 1/255 box meets the warp's 8 x kSqH pixel area with corner
-// (ox, oy).
-__device__ __forceinline__ bool square_hit(const float4& p, const float4& q, float ox, float oy) {
-    if (!(p.w >= 0.f)) return false;
-    const float xl = p.x - p.w - ox, xh = p.x + p.w - ox;
-    const float yl = p.y - q.w - oy, yh = p.y + q.w - oy;
-    return xl <= 7.f && xh >= 0.f && yl <= float(kSqH - 1) && yh >= 0.f;
-}
-
 // Per-pixel state of the reverse walk.
 struct BwdPixel {
     float T, SG, G0, G1, G2;
@@ -404,7 +394,6 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
         for (int h = 1; h < kBwdPx; ++h) lane_end = max(lane_end, P[h].end);
         const uint32_t warp_end = __reduce_max_sync(kFull, lane_end);
         const float fx = float(px), fy0 = float(py0);
-        const float ox = float(sx), oy = float(sy);
         // the forward's warps (8x4 pixels) inside this warp's area: an entry none of them
         // composited has no active pixel here
         uint32_t fwarps = 0u;
@@ -415,11 +404,13 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
             const uint32_t e = lo + lane;
             bool hit = false;
             if (e < hi) {
+                // an entry some forward warp of this area composited (its alpha >= 1/255 box
+                // meets the area then too): only those records are loaded
                 const uint32_t g = list[e];
-                const Record& r = rec[g];
-                const float4 p = r.p, q = r.q, c = r.c;
-                hit = (uint32_t(comp[e]) & fwarps) != 0u && square_hit(p, q, ox, oy);
+                hit = (uint32_t(comp[e]) & fwarps) != 0u;
                 if (hit) {
+                    const Record& r = rec[g];
+                    const float4 p = r.p, q = r.q, c = r.c;
                     s_p[warp][lane] = p;
                     s_q[warp][lane] = q;
                     s_c[warp][lane] = c;
