@@ -193,6 +193,8 @@ __global__ void __launch_bounds__(kRsThreads, MINB) k_sweep_pass(
     const uint32_t lt = (1u << lane) - 1u;
     const uint32_t t = threadIdx.x;
     uint32_t* status = ctl.status + size_t(pass) * ctl.max_tiles * 256;
+    // the digit totals (complete since the histogram kernel), loaded now to overlap the ranking
+    const uint32_t gtotal = t < uint32_t(R) ? ctl.ghist[pass * 256 + t] : 0u;
     uint32_t run = 0u, lstart;
     {
         const uint32_t base = tile * TILE + warp * (32 * ITEMS);
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kRsThreads, MINB) k_sweep_pass(
             }
         }
     }
-    uint32_t excl = 0u, gtotal = 0u;
+    uint32_t excl = 0u;
     if (t < uint32_t(R)) {
         if (tile != 0) {
             // look back over up to kWindow predecessors at a time: the window's status words are
@@ -276,7 +278,6 @@ __global__ void __launch_bounds__(kRsThreads, MINB) k_sweep_pass(
             }
             st_relaxed(status + size_t(tile) * 256 + t, kFlagIncl | (excl + run));
         }
-        gtotal = ctl.ghist[pass * 256 + t];
     }
     const uint32_t dbase = block_exclusive_scan_256(t < uint32_t(R) ? gtotal : 0u, s_w);
     if (t < uint32_t(R)) s_delta[t] = dbase + excl - lstart;

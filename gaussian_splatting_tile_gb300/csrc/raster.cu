@@ -28,13 +28,20 @@ constexpr int kFwdThreads = kTilePixels;  // the forward: one block of 256 threa
 constexpr int kFwdWarps = kFwdThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
+// Backward: 1 takes the hit entries two at a time and, where both have composited pixels, reduces
+// their sums together (reduce18); 0 reduces entry by entry (butterfly9).
+#ifndef RS_BWD_PAIR
+#define RS_BWD_PAIR 1
+#endif
 // Resident blocks per SM the compositing kernels are compiled for (register budget per thread =
-// 65536 / (256 x blocks)).
+// 65536 / (threads per block x blocks)).
 #ifndef RS_FWD_MIN_BLOCKS
 #define RS_FWD_MIN_BLOCKS 6
 #endif
+// backward (128-thread blocks): 7 with paired entries (72 registers; 6: 0.257 ms, 8: 0.260,
+// 7: 0.251 on the 160k 1080p orbit), 8 without (64 registers)
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : 8)  // resident backward blocks per SM
+#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : RS_BWD_PAIR ? 7 : 8)
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -272,6 +279,60 @@ __device__ __forceinline__ int sum_slot(unsigned lane) {
 
 constexpr int kSums = 9;  // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2, gp, w G_rgb
 
+// Two entries' nine sums reduced together (18 -> 9 -> 5 -> 3 -> 2 -> 1): the first step hands
+// each half-warp one entry's vector, the rest is butterfly9's, and the last step splits the pair
+// instead of summing it twice.  Lane L then holds sum pair_slot(L) of the 18 (entry pair_slot / 9,
+// value pair_slot % 9): 20 shuffles for two entries where two butterfly9 calls take 24.
+__device__ __forceinline__ float reduce18(const float (&v)[9], const float (&u)[9], unsigned lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+    float a[9];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) a[k] = (b4 ? u[k] : v[k]) + __shfl_xor_sync(kFull, b4 ? v[k] : u[k], 16);
+    float b[5];
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const float lo = a[k], hi = k + 5 < 9 ? a[k + 5] : 0.f;
+        b[k] = (b3 ? hi : lo) + __shfl_xor_sync(kFull, b3 ? lo : hi, 8);
+    }
+    float c[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const float lo = b[k], hi = k + 3 < 5 ? b[k + 3] : 0.f;
+        c[k] = (b2 ? hi : lo) + __shfl_xor_sync(kFull, b2 ? lo : hi, 4);
+    }
+    float d[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float lo = c[k], hi = k + 2 < 3 ? c[k + 2] : 0.f;
+        d[k] = (b1 ? hi : lo) + __shfl_xor_sync(kFull, b1 ? lo : hi, 2);
+    }
+    return (b0 ? d[1] : d[0]) + __shfl_xor_sync(kFull, b0 ? d[0] : d[1], 1);
+}
+
+// Which of the 18 sums lane L holds after reduce18 (-1: padding).  Sums 0 and 1 (and 9 and 10)
+// sit on lanes 0 and 1 (16 and 17).
+__device__ __forceinline__ int pair_slot(unsigned lane) {
+    int n = 18, real = 18, i = 0;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        const int h = (n + 1) / 2;
+        if (lane & unsigned(m)) {
+            i += h;
+            real = max(real - h, 0);
+        } else {
+            real = min(real, h);
+        }
+        n = h;
+    }
+    return real >= 1 ? i : -1;
+}
+
+// The global array and the scale of gradient sum `slot` (0..8) of an entry.
+__device__ __forceinline__ float* sum_dst(int slot, size_t N, float* dm2, float* dcon, float* dop, float* dcol) {
+    return slot == 0 ? dm2 : slot == 1 ? dm2 + N : slot == 2 ? dcon : slot == 3 ? dcon + N
+         : slot == 4 ? dcon + 2 * N : slot == 5 ? dop : slot >= 6 ? dcol + size_t(slot - 6) * N : dm2;
+}
+
 // The backward runs one block of 128 threads per task: the entries of one 256-entry chunk of the
 // point list, [256 c, 256 c + 256), which may hold the end of one tile's list and several short
 // lists after it (pieces).  A piece that stops at the chunk's end while its tile's list goes on
@@ -279,17 +340,19 @@ constexpr int kSums = 9;  // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2
 // many blocks as it has chunks.  Within a block the four warps are independent: warp w owns the
 // 8x8 square at columns (w & 1) * 8 and rows (w >> 1) * 8 of the piece's tile, and lane l the two
 // pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4) of it.  A warp walks each piece back to
-// front, 32 entries at a time: each lane loads one entry's record and tests the entry's
-// alpha >= 1/255 box against the square; the hits are staged in the warp's own shared-memory
-// slots and evaluated one after another by all 64 pixels.  The two pixels of a lane share their
-// column, so their nine sums fold before one reduce-scatter over the warp, and nine lanes each
-// add one of the sums to the Gaussian's gradient with a global atomic.  There is no block-wide
-// barrier.
+// front, 32 entries at a time: each lane reads one entry's composited flags from the forward and,
+// where one of the two forward warps inside the square composited it (a hit), loads its record
+// into the warp's own shared-memory slots; the hits are evaluated one after another by all 64
+// pixels.  The two pixels of a lane share their
+// column, so their nine sums fold before a reduce-scatter over the warp (two consecutive hits'
+// sums in one, where both have composited pixels), and one lane per sum adds it to the
+// Gaussian's gradient with a global atomic.  There is no block-wide barrier.
 // Pixels per lane, stacked 4 rows apart in one column (2: warps of 8x8; 4: warps of 8x16, which
 // cut the warp-entries by a third but measured 0.293 -> 0.303 ms with more registers per lane).
 #ifndef RS_BWD_PX
 #define RS_BWD_PX 2
 #endif
+
 constexpr int kBwdPx = RS_BWD_PX;
 static_assert(kBwdPx == 2 || kBwdPx == 4, "two or four pixels per lane");
 constexpr int kSqH = 4 * kBwdPx;                 // rows of a warp's area (8 columns wide)
@@ -343,9 +406,16 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     // (the record holds the conic scaled by -log2(e)/2 and -log2(e), and 1/opacity)
     const int slot = sum_slot(lane);
     const size_t N = size_t(n);
-    float* const dst = slot == 0 ? dm2 : slot == 1 ? dm2 + N : slot == 2 ? dcon : slot == 3 ? dcon + N
-                     : slot == 4 ? dcon + 2 * N : slot == 5 ? dop : slot >= 6 ? dcol + size_t(slot - 6) * N : dm2;
+    float* const dst = sum_dst(slot, N, dm2, dcon, dop, dcol);
     const float kconst = slot == 2 || slot == 4 ? -0.5f : slot == 3 ? -1.f : 1.f;
+#if RS_BWD_PAIR
+    // the same for the sums of an entry pair (second entry: pair_slot >= 9)
+    const int pidx = pair_slot(lane);
+    const bool psecond = pidx >= 9;
+    const int pslot = pidx < 0 ? -1 : psecond ? pidx - 9 : pidx;
+    float* const pdst = sum_dst(pslot, N, dm2, dcon, dop, dcol);
+    const float pconst = pslot == 2 || pslot == 4 ? -0.5f : pslot == 3 ? -1.f : 1.f;
+#endif
     constexpr float kLn2 = 0.6931471805599453f;
     uint32_t pa = a0;
     while (true) {
@@ -419,16 +489,14 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
             }
             uint32_t m = __ballot_sync(kFull, hit);
             __syncwarp();
-            while (m) {
-                const int j = 31 - __clz(m);
-                m ^= 1u << j;
+            // entry j at the lane's pixels: updates their state, returns whether any composited
+            auto step = [&](int j, float& dx, float (&dy)[kBwdPx], float (&gp)[kBwdPx], float (&w)[kBwdPx]) {
                 const uint32_t ej = lo + uint32_t(j);
                 const float4 p = s_p[warp][j], q = s_q[warp][j];
                 // the lane's pixels share a column: dx and its terms are common (the same
                 // arithmetic as entry_alpha, pixel by pixel)
-                const float dx = fx - p.x;
+                dx = fx - p.x;
                 const float bx = q.y * dx, axx = (q.x * dx) * dx;
-                float dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
                 bool any = false;
                 const float4 c = s_c[warp][j];
 #pragma unroll
@@ -442,39 +510,84 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                     if (act) bwd_step(P[h], al, raw, c, gp[h], w[h]);
                     any |= act;
                 }
-                if (__any_sync(kFull, any)) {
-                    // the lane's pixels share dx: fold their sums, then reduce over the warp
-                    float sg = gp[0], sgy = gp[0] * dy[0], sgyy = (gp[0] * dy[0]) * dy[0];
-                    float c0 = w[0] * P[0].G0, c1 = w[0] * P[0].G1, c2 = w[0] * P[0].G2;
+                return any;
+            };
+            // the lane's pixels share dx: their sums fold before the reduction over the warp
+            auto fold = [&](float dx, const float (&dy)[kBwdPx], const float (&gp)[kBwdPx], const float (&w)[kBwdPx],
+                            float (&v)[kSums]) {
+                float sg = gp[0], sgy = gp[0] * dy[0], sgyy = (gp[0] * dy[0]) * dy[0];
+                float c0 = w[0] * P[0].G0, c1 = w[0] * P[0].G1, c2 = w[0] * P[0].G2;
 #pragma unroll
-                    for (int h = 1; h < kBwdPx; ++h) {
-                        sg += gp[h];
-                        const float t = gp[h] * dy[h];
-                        sgy += t;
-                        sgyy = fmaf(t, dy[h], sgyy);
-                        c0 = fmaf(w[h], P[h].G0, c0);
-                        c1 = fmaf(w[h], P[h].G1, c1);
-                        c2 = fmaf(w[h], P[h].G2, c2);
-                    }
-                    float v[kSums];
-                    v[0] = sg * dx;
-                    v[1] = sgy;
-                    v[2] = v[0] * dx;
-                    v[3] = sgy * dx;
-                    v[4] = sgyy;
-                    v[5] = sg;
-                    v[6] = c0;
-                    v[7] = c1;
-                    v[8] = c2;
-                    const float sum = butterfly9(v, lane);
-                    const float other = __shfl_xor_sync(kFull, sum, 2);  // slots 0 and 1: lanes 0 and 2
-                    if (slot >= 0) {
-                        const float B = -kLn2 * q.y;
-                        const float a = slot == 0 ? -2.f * kLn2 * q.x : slot == 1 ? -2.f * kLn2 * q.z
-                                      : slot == 5 ? c.w : kconst;
-                        atomicAdd(dst + s_g[warp][j], fmaf(a, sum, slot < 2 ? B * other : 0.f));
-                    }
+                for (int h = 1; h < kBwdPx; ++h) {
+                    sg += gp[h];
+                    const float t = gp[h] * dy[h];
+                    sgy += t;
+                    sgyy = fmaf(t, dy[h], sgyy);
+                    c0 = fmaf(w[h], P[h].G0, c0);
+                    c1 = fmaf(w[h], P[h].G1, c1);
+                    c2 = fmaf(w[h], P[h].G2, c2);
                 }
+                v[0] = sg * dx;
+                v[1] = sgy;
+                v[2] = v[0] * dx;
+                v[3] = sgy * dx;
+                v[4] = sgyy;
+                v[5] = sg;
+                v[6] = c0;
+                v[7] = c1;
+                v[8] = c2;
+            };
+            // one entry's sums over the warp, added to its Gaussian's gradient by nine lanes
+            auto reduce_one = [&](int j, float dx, const float (&dy)[kBwdPx], const float (&gp)[kBwdPx],
+                                  const float (&w)[kBwdPx]) {
+                float v[kSums];
+                fold(dx, dy, gp, w, v);
+                const float sum = butterfly9(v, lane);
+                const float other = __shfl_xor_sync(kFull, sum, 2);  // slots 0 and 1: lanes 0 and 2
+                if (slot >= 0) {
+                    const float4 q = s_q[warp][j];
+                    const float B = -kLn2 * q.y;
+                    const float a = slot == 0 ? -2.f * kLn2 * q.x : slot == 1 ? -2.f * kLn2 * q.z
+                                  : slot == 5 ? s_c[warp][j].w : kconst;
+                    atomicAdd(dst + s_g[warp][j], fmaf(a, sum, slot < 2 ? B * other : 0.f));
+                }
+            };
+            while (m) {
+                const int j = 31 - __clz(m);
+                m ^= 1u << j;
+                float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
+                const bool any = step(j, dx, dy, gp, w);
+#if RS_BWD_PAIR
+                if (m) {
+                    // the next hit (in front of j) as well, and both entries' sums in one reduction
+                    const int k = 31 - __clz(m);
+                    m ^= 1u << k;
+                    float dx2, dy2[kBwdPx], gp2[kBwdPx], w2[kBwdPx];
+                    const bool any2 = step(k, dx2, dy2, gp2, w2);
+                    const bool r1 = __any_sync(kFull, any), r2 = __any_sync(kFull, any2);
+                    if (r1 && r2) {
+                        float v[kSums], u[kSums];
+                        fold(dx, dy, gp, w, v);
+                        fold(dx2, dy2, gp2, w2, u);
+                        const float sum = reduce18(v, u, lane);
+                        const float other = __shfl_xor_sync(kFull, sum, 1);  // slots 0 and 1: lanes 2i, 2i + 1
+                        if (pslot >= 0) {
+                            const int jj = psecond ? k : j;
+                            const float4 q = s_q[warp][jj];
+                            const float B = -kLn2 * q.y;
+                            const float a = pslot == 0 ? -2.f * kLn2 * q.x : pslot == 1 ? -2.f * kLn2 * q.z
+                                          : pslot == 5 ? s_c[warp][jj].w : pconst;
+                            atomicAdd(pdst + s_g[warp][jj], fmaf(a, sum, pslot < 2 ? B * other : 0.f));
+                        }
+                    } else if (r1) {
+                        reduce_one(j, dx, dy, gp, w);
+                    } else if (r2) {
+                        reduce_one(k, dx2, dy2, gp2, w2);
+                    }
+                    continue;
+                }
+#endif
+                if (__any_sync(kFull, any)) reduce_one(j, dx, dy, gp, w);
             }
             __syncwarp();  // the slots are read before the next batch overwrites them
             hi = lo;
