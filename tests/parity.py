@@ -87,11 +87,15 @@ def allclose_report(name, got, ref, rtol, atol, mask=None, extra=None, atol_of_m
     return float(err.max()) if err.size else 0.0
 
 
-def check_projection(cam, g, G):
+def check_projection(cam, g, G, min_clear=0.995):
+    """min_clear: the share of Gaussians with no knife-edge decision the check insists on.  The
+    tile-span decisions compare (u +- r) / 16 with integers at a margin relative to u, so at the
+    same scene density their knife-edge share grows with the image's pixel coordinates (0.4% of
+    the Gaussians at 1080p, 0.8% at 3840 x 2160, 1.2% at 4608 x 4096)."""
     O64 = oracle.project(cam, g, prec=64, margin=MARGIN)
     O32 = oracle.project(cam, g, prec=32)
     clear = O64["ambig"] == 0
-    assert clear.mean() > 0.995
+    assert clear.mean() > min_clear
     # integer decisions: exact where not at a knife edge (taken in float, the kernel's precision)
     assert np.array_equal(G["radius"][clear], O32["radius"][clear])
     assert np.array_equal(G["tiles_touched"][clear], O32["tiles_touched"][clear])
