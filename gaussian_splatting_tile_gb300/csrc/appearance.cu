@@ -518,186 +518,306 @@ cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float sc
 //   dS_sum/dI_q = (G*a)_q + 2 I_q (G*b)_q + T_q (G*c)_q,
 //   a = S (2my/A1 - 2my/A2 - 2mx/B1 + 2mx/B2), b = -S/B2, c = 2S/A2,
 // A1 = 2 mx my + C1, A2 = 2 sxy + C2, B1 = mx^2 + my^2 + C1, B2 = sx^2 + sy^2 + C2.
-// Two kernels over 16x16 output tiles with a 5-pixel halo staged in shared memory: the first
-// forms the five filtered maps (separably), S, the loss sums and a, b, c; the second filters
-// a, b, c and writes the gradient.
+// Two kernels over 32x32 output tiles, each staging its 42x42 input patch (5-pixel halo, zeros
+// outside the image) in shared memory and filtering it separably: the first forms the five
+// filtered maps, S, a, b, c and the block's sums of S and |I - T|; the second filters a, b, c
+// and writes the gradient.  In both passes a thread computes four neighbouring outputs from one
+// run of 14 staged inputs (the horizontal pass along a row, the vertical pass down a column),
+// so every staged value is loaded once per four outputs instead of once per output.  The
+// blocks' sums land in per-block slots, summed in a fixed order by a third kernel.
 namespace {
 
-constexpr int kSsimTile = 16;
-constexpr int kSsimR = 5;
-constexpr int kSsimP = kSsimTile + 2 * kSsimR;  // staged patch edge: 26
+constexpr int kSsimTile = 32;                   // output tile edge
+constexpr int kSsimR = 5;                       // window radius
+constexpr int kSsimTaps = 2 * kSsimR + 1;
+constexpr int kSsimP = kSsimTile + 2 * kSsimR;  // staged patch rows: 42
+constexpr int kSsimLead = 3;                    // extra staged columns left of the window's reach
+constexpr int kSsimPS = 48;                     // staged columns (x0 - 3 .. x0 + 44): 16-byte groups
+constexpr int kSsimThreads = 256;
+constexpr int kSsimOut = 4;                     // outputs per thread and pass
+constexpr int kSsimGroups = kSsimTile / kSsimOut;  // column groups of a patch row: 8
 
 struct SsimWindow {
-    float w[2 * kSsimR + 1];  // normalised 1-D Gaussian, sigma 1.5
+    float w[kSsimTaps];  // normalised 1-D Gaussian, sigma 1.5
 };
 
-__device__ __forceinline__ float patch_at(const float* __restrict__ img, int H, int W, int y, int x) {
-    return (y >= 0 && y < H && x >= 0 && x < W) ? img[size_t(y) * W + x] : 0.f;
+// Stages the plane's rows y0 .. y0 + 41, columns xs .. xs + 47 (xs = x0 - 3, a multiple of 4;
+// zeros outside the H x W image) into dst[kSsimP][kSsimPS] with asynchronous copies (cp.async,
+// PTX ISA: bytes past the source size are filled with zeros), all in flight together; the
+// caller waits with ssim_stage_wait.  VEC: 16-byte copies of four columns (needs W and the
+// plane's address to be multiples of 4 floats and 16 bytes); otherwise 4-byte copies.
+template <bool VEC>
+__device__ __forceinline__ void ssim_stage(const float* __restrict__ plane, int H, int W, int y0, int xs,
+                                           float* dst) {
+    const unsigned base = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    if (VEC) {
+        constexpr int kG = kSsimPS / 4;  // 12 groups per row
+        for (int e = threadIdx.x; e < kSsimP * kG; e += kSsimThreads) {
+            const int r = e / kG, x = xs + 4 * (e - r * kG), y = y0 + r;
+            // a group starts at a multiple of 4, so it is wholly left of column 0 or not at all
+            const int n = (y >= 0 && y < H && x >= 0 && x < W) ? 4 * min(4, W - x) : 0;
+            const float* src = n ? plane + size_t(y) * W + x : plane;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(base + 16u * unsigned(e)), "l"(src),
+                         "r"(n) : "memory");
+        }
+    } else {
+        for (int e = threadIdx.x; e < kSsimP * kSsimPS; e += kSsimThreads) {
+            const int r = e / kSsimPS, x = xs + (e - r * kSsimPS), y = y0 + r;
+            const bool in = y >= 0 && y < H && x >= 0 && x < W;
+            const float* src = in ? plane + size_t(y) * W + x : plane;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(base + 4u * unsigned(e)), "l"(src),
+                         "r"(in ? 4 : 0) : "memory");
+        }
+    }
 }
 
-__global__ void __launch_bounds__(256) k_ssim_fwd(SsimWindow win, int C, int H, int W,
-                                                  const float* __restrict__ img, const float* __restrict__ tgt,
-                                                  float* __restrict__ abc, float* __restrict__ sums) {
+__device__ __forceinline__ void ssim_stage_wait() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+}
+
+// The staged values of patch row `row` that outputs 4 g .. 4 g + 3 of the horizontal pass read:
+// v[3 + o + k] is tap k of output 4 g + o (five 16-byte loads; v[0..2] and v[17..19] unused).
+__device__ __forceinline__ void ssim_row_run(const float* patch, int row, int g, float (&v)[20]) {
+    const float4* q = reinterpret_cast<const float4*>(patch + row * kSsimPS + g * kSsimOut);
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const float4 t = q[k];
+        v[4 * k] = t.x;
+        v[4 * k + 1] = t.y;
+        v[4 * k + 2] = t.z;
+        v[4 * k + 3] = t.w;
+    }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kSsimThreads) k_ssim_fwd(SsimWindow win, int H, int W,
+                                                           const float* __restrict__ img,
+                                                           const float* __restrict__ tgt, size_t N,
+                                                           float* __restrict__ abc, float2* __restrict__ partial) {
     RS_PDL_ENTER();
-    __shared__ float s_x[kSsimP][kSsimP], s_y[kSsimP][kSsimP];
-    __shared__ float s_h[5][kSsimP][kSsimTile];  // horizontally filtered x, y, xx, yy, xy
-    __shared__ float s_red[2][8];
-    const int TXn = (W + kSsimTile - 1) / kSsimTile;
-    const int tile = blockIdx.x, ch = blockIdx.y;
-    const int x0 = (tile % TXn) * kSsimTile - kSsimR, y0 = (tile / TXn) * kSsimTile - kSsimR;
+    __shared__ __align__(16) float s_x[kSsimP * kSsimPS], s_y[kSsimP * kSsimPS];
+    __shared__ __align__(16) float s_h[5][kSsimP][kSsimTile];  // horizontally filtered x, y, xx, yy, xy
+    __shared__ float s_red[2][kSsimThreads / 32];
+    const int ch = blockIdx.z;
+    const int x0 = blockIdx.x * kSsimTile - kSsimR, y0 = blockIdx.y * kSsimTile - kSsimR;
     const size_t plane = size_t(H) * W;
-    const float* X = img + ch * plane;
-    const float* Y = tgt + ch * plane;
-    for (int i = threadIdx.x; i < kSsimP * kSsimP; i += 256) {
-        const int py = i / kSsimP, px = i % kSsimP;
-        s_x[py][px] = patch_at(X, H, W, y0 + py, x0 + px);
-        s_y[py][px] = patch_at(Y, H, W, y0 + py, x0 + px);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < kSsimP * kSsimTile; i += 256) {
-        const int py = i / kSsimTile, px = i % kSsimTile;
-        float h[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    ssim_stage<VEC>(img + ch * plane, H, W, y0, x0 - kSsimLead, s_x);
+    ssim_stage<VEC>(tgt + ch * plane, H, W, y0, x0 - kSsimLead, s_y);
+    ssim_stage_wait();
+    // horizontal pass: task t = patch row t / 8, outputs 4 (t % 8) .. + 3 of that row
+    for (int t = threadIdx.x; t < kSsimP * kSsimGroups; t += kSsimThreads) {
+        const int row = t / kSsimGroups, g = t % kSsimGroups;
+        float a[20], b[20];
+        ssim_row_run(s_x, row, g, a);
+        ssim_row_run(s_y, row, g, b);
+        float h[5][kSsimOut];
 #pragma unroll
-        for (int k = 0; k <= 2 * kSsimR; ++k) {
-            const float w = win.w[k], a = s_x[py][px + k], b = s_y[py][px + k];
-            h[0] = fmaf(w, a, h[0]);
-            h[1] = fmaf(w, b, h[1]);
-            h[2] = fmaf(w, a * a, h[2]);
-            h[3] = fmaf(w, b * b, h[3]);
-            h[4] = fmaf(w, a * b, h[4]);
-        }
+        for (int o = 0; o < kSsimOut; ++o) h[0][o] = h[1][o] = h[2][o] = h[3][o] = h[4][o] = 0.f;
 #pragma unroll
-        for (int q = 0; q < 5; ++q) s_h[q][py][px] = h[q];
-    }
-    __syncthreads();
-    const int ty = threadIdx.x / kSsimTile, tx = threadIdx.x % kSsimTile;
-    const int gy = y0 + kSsimR + ty, gx = x0 + kSsimR + tx;
-    float ssim = 0.f, l1 = 0.f;
-    if (gy < H && gx < W) {
-        float v[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k <= 2 * kSsimR; ++k) {
+        for (int k = 0; k < kSsimTaps; ++k) {
             const float w = win.w[k];
 #pragma unroll
-            for (int q = 0; q < 5; ++q) v[q] = fmaf(w, s_h[q][ty + k][tx], v[q]);
+            for (int o = 0; o < kSsimOut; ++o) {
+                const float xa = a[kSsimLead + o + k], yb = b[kSsimLead + o + k];
+                h[0][o] = fmaf(w, xa, h[0][o]);
+                h[1][o] = fmaf(w, yb, h[1][o]);
+                h[2][o] = fmaf(w, xa * xa, h[2][o]);
+                h[3][o] = fmaf(w, yb * yb, h[3][o]);
+                h[4][o] = fmaf(w, xa * yb, h[4][o]);
+            }
         }
-        constexpr float C1 = 0.01f * 0.01f, C2 = 0.03f * 0.03f;
-        const float mx = v[0], my = v[1];
-        const float sxx = v[2] - mx * mx, syy = v[3] - my * my, sxy = v[4] - mx * my;
+#pragma unroll
+        for (int q = 0; q < 5; ++q)
+            *reinterpret_cast<float4*>(&s_h[q][row][g * kSsimOut]) = make_float4(h[q][0], h[q][1], h[q][2], h[q][3]);
+    }
+    __syncthreads();
+    // vertical pass: lane = output column, warp w = output rows 4 w .. 4 w + 3
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float v[5][kSsimOut];
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+        float col[kSsimOut + 2 * kSsimR];
+#pragma unroll
+        for (int i = 0; i < kSsimOut + 2 * kSsimR; ++i) col[i] = s_h[q][warp * kSsimOut + i][lane];
+#pragma unroll
+        for (int o = 0; o < kSsimOut; ++o) {
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < kSsimTaps; ++k) acc = fmaf(win.w[k], col[o + k], acc);
+            v[q][o] = acc;
+        }
+    }
+    constexpr float C1 = 0.01f * 0.01f, C2 = 0.03f * 0.03f;
+    const int gx = x0 + kSsimR + lane;
+    float ssim = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int o = 0; o < kSsimOut; ++o) {
+        const int ty = warp * kSsimOut + o, gy = y0 + kSsimR + ty;
+        if (gy >= H || gx >= W) continue;
+        const float mx = v[0][o], my = v[1][o];
+        const float sxx = v[2][o] - mx * mx, syy = v[3][o] - my * my, sxy = v[4][o] - mx * my;
         const float A1 = 2.f * mx * my + C1, A2 = 2.f * sxy + C2;
         const float B1 = mx * mx + my * my + C1, B2 = sxx + syy + C2;
-        const float S = (A1 * A2) / (B1 * B2);
-        ssim = S;
-        l1 = fabsf(s_x[ty + kSsimR][tx + kSsimR] - s_y[ty + kSsimR][tx + kSsimR]);
-        const size_t o = ch * plane + size_t(gy) * W + gx;
-        const size_t N = size_t(C) * plane;
-        abc[o] = S * (2.f * my / A1 - 2.f * my / A2 - 2.f * mx / B1 + 2.f * mx / B2);
-        abc[N + o] = -S / B2;
-        abc[2 * N + o] = 2.f * S / A2;
+        // two reciprocals serve every quotient: 1/A1 = A2 rA, 1/A2 = A1 rA, 1/B1 = B2 rB, 1/B2 = B1 rB
+        const float rA = __frcp_rn(A1 * A2), rB = __frcp_rn(B1 * B2);
+        const float S = (A1 * A2) * rB;
+        ssim += S;
+        const int cc = (ty + kSsimR) * kSsimPS + kSsimLead + kSsimR + lane;  // the output's own pixel
+        l1 += fabsf(s_x[cc] - s_y[cc]);
+        const size_t at = ch * plane + size_t(gy) * W + gx;
+        abc[at] = S * (2.f * my * (A2 - A1) * rA + 2.f * mx * (B1 - B2) * rB);
+        abc[N + at] = -S * B1 * rB;
+        abc[2 * N + at] = 2.f * S * A1 * rA;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         ssim += __shfl_xor_sync(kFull, ssim, o);
         l1 += __shfl_xor_sync(kFull, l1, o);
     }
-    if ((threadIdx.x & 31) == 0) {
-        s_red[0][threadIdx.x >> 5] = ssim;
-        s_red[1][threadIdx.x >> 5] = l1;
+    if (lane == 0) {
+        s_red[0][warp] = ssim;
+        s_red[1][warp] = l1;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        float a = 0.f, b = 0.f;
-        for (int w = 0; w < 8; ++w) {
-            a += s_red[0][w];
-            b += s_red[1][w];
+        float sa = 0.f, sb = 0.f;
+        for (int w = 0; w < kSsimThreads / 32; ++w) {
+            sa += s_red[0][w];
+            sb += s_red[1][w];
         }
-        atomicAdd(sums, a);
-        atomicAdd(sums + 1, b);
+        partial[(size_t(ch) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x] = make_float2(sa, sb);
     }
 }
 
-// dL/dI = scale (1 - lambda) sign(I - T) / N - scale lambda / N (G*a + 2 I G*b + T G*c); the
-// loss scale ((1 - lambda) sum|I - T| + lambda (N - sum S)) / N goes to *loss.
-__global__ void __launch_bounds__(256) k_ssim_bwd(SsimWindow win, int C, int H, int W,
-                                                  const float* __restrict__ img, const float* __restrict__ tgt,
-                                                  const float* __restrict__ abc, float lambda, float scale,
-                                                  float* __restrict__ dimg) {
+// dL/dI = scale (1 - lambda) sign(I - T) / N - scale lambda / N (G*a + 2 I G*b + T G*c).
+template <bool VEC>
+__global__ void __launch_bounds__(kSsimThreads) k_ssim_bwd(SsimWindow win, int H, int W,
+                                                           const float* __restrict__ img,
+                                                           const float* __restrict__ tgt, size_t N,
+                                                           const float* __restrict__ abc, float lambda, float scale,
+                                                           float* __restrict__ dimg) {
     RS_PDL_ENTER();
-    __shared__ float s_in[3][kSsimP][kSsimP];
-    __shared__ float s_h[3][kSsimP][kSsimTile];
-    const int TXn = (W + kSsimTile - 1) / kSsimTile;
-    const int tile = blockIdx.x, ch = blockIdx.y;
-    const int x0 = (tile % TXn) * kSsimTile - kSsimR, y0 = (tile / TXn) * kSsimTile - kSsimR;
+    __shared__ __align__(16) float s_in[3][kSsimP * kSsimPS];
+    __shared__ __align__(16) float s_h[3][kSsimP][kSsimTile];
+    const int ch = blockIdx.z;
+    const int x0 = blockIdx.x * kSsimTile - kSsimR, y0 = blockIdx.y * kSsimTile - kSsimR;
     const size_t plane = size_t(H) * W;
-    const size_t N = size_t(C) * plane;
-    for (int i = threadIdx.x; i < kSsimP * kSsimP; i += 256) {
-        const int py = i / kSsimP, px = i % kSsimP;
 #pragma unroll
-        for (int q = 0; q < 3; ++q) s_in[q][py][px] = patch_at(abc + q * N + ch * plane, H, W, y0 + py, x0 + px);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < kSsimP * kSsimTile; i += 256) {
-        const int py = i / kSsimTile, px = i % kSsimTile;
-        float h[3] = {0.f, 0.f, 0.f};
+    for (int q = 0; q < 3; ++q) ssim_stage<VEC>(abc + q * N + ch * plane, H, W, y0, x0 - kSsimLead, s_in[q]);
+    ssim_stage_wait();
+    for (int t = threadIdx.x; t < kSsimP * kSsimGroups; t += kSsimThreads) {
+        const int row = t / kSsimGroups, g = t % kSsimGroups;
 #pragma unroll
-        for (int k = 0; k <= 2 * kSsimR; ++k) {
-            const float w = win.w[k];
+        for (int q = 0; q < 3; ++q) {
+            float a[20];
+            ssim_row_run(s_in[q], row, g, a);
+            float h[kSsimOut] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < 3; ++q) h[q] = fmaf(w, s_in[q][py][px + k], h[q]);
+            for (int k = 0; k < kSsimTaps; ++k)
+#pragma unroll
+                for (int o = 0; o < kSsimOut; ++o) h[o] = fmaf(win.w[k], a[kSsimLead + o + k], h[o]);
+            *reinterpret_cast<float4*>(&s_h[q][row][g * kSsimOut]) = make_float4(h[0], h[1], h[2], h[3]);
         }
-#pragma unroll
-        for (int q = 0; q < 3; ++q) s_h[q][py][px] = h[q];
     }
     __syncthreads();
-    const int ty = threadIdx.x / kSsimTile, tx = threadIdx.x % kSsimTile;
-    const int gy = y0 + kSsimR + ty, gx = x0 + kSsimR + tx;
-    if (gy >= H || gx >= W) return;
-    float g[3] = {0.f, 0.f, 0.f};
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float gsum[3][kSsimOut];
 #pragma unroll
-    for (int k = 0; k <= 2 * kSsimR; ++k) {
-        const float w = win.w[k];
+    for (int q = 0; q < 3; ++q) {
+        float col[kSsimOut + 2 * kSsimR];
 #pragma unroll
-        for (int q = 0; q < 3; ++q) g[q] = fmaf(w, s_h[q][ty + k][tx], g[q]);
+        for (int i = 0; i < kSsimOut + 2 * kSsimR; ++i) col[i] = s_h[q][warp * kSsimOut + i][lane];
+#pragma unroll
+        for (int o = 0; o < kSsimOut; ++o) {
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < kSsimTaps; ++k) acc = fmaf(win.w[k], col[o + k], acc);
+            gsum[q][o] = acc;
+        }
     }
-    const size_t o = ch * plane + size_t(gy) * W + gx;
-    const float x = img[o], y = tgt[o];
-    const float d = x - y;
-    const float sgn = d > 0.f ? 1.f : (d < 0.f ? -1.f : 0.f);
-    const float dS = fmaf(2.f * x, g[1], fmaf(y, g[2], g[0]));
+    const int gx = x0 + kSsimR + lane;
     const float inv = scale / float(N);
-    dimg[o] = inv * ((1.f - lambda) * sgn - lambda * dS);
+#pragma unroll
+    for (int o = 0; o < kSsimOut; ++o) {
+        const int gy = y0 + kSsimR + warp * kSsimOut + o;
+        if (gy >= H || gx >= W) continue;
+        const size_t at = ch * plane + size_t(gy) * W + gx;
+        const float x = img[at], y = tgt[at];
+        const float d = x - y;
+        const float sgn = d > 0.f ? 1.f : (d < 0.f ? -1.f : 0.f);
+        const float dS = fmaf(2.f * x, gsum[1][o], fmaf(y, gsum[2][o], gsum[0][o]));
+        dimg[at] = inv * ((1.f - lambda) * sgn - lambda * dS);
+    }
 }
 
-__global__ void k_ssim_loss(const float* __restrict__ sums, size_t N, float lambda, float scale, float* loss) {
+// loss = scale ((1 - lambda) sum|I - T| + lambda (N - sum S)) / N from the blocks' sums, added in
+// a fixed order.
+__global__ void __launch_bounds__(1024) k_ssim_loss(const float2* __restrict__ partial, uint32_t count, size_t N,
+                                                    float lambda, float scale, float* loss) {
     RS_PDL_ENTER();
-    // sums[0] = sum S, sums[1] = sum |I - T|
-    *loss = scale * ((1.f - lambda) * sums[1] + lambda * (float(N) - sums[0])) / float(N);
+    __shared__ float s_a[32], s_b[32];
+    float a = 0.f, b = 0.f;
+    for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) {
+        const float2 p = partial[i];
+        a += p.x;
+        b += p.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(kFull, a, o);
+        b += __shfl_xor_sync(kFull, b, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_a[threadIdx.x >> 5] = a;
+        s_b[threadIdx.x >> 5] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float sa = 0.f, sb = 0.f;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) {
+            sa += s_a[w];
+            sb += s_b[w];
+        }
+        *loss = scale * ((1.f - lambda) * sb + lambda * (float(N) - sa)) / float(N);
+    }
+}
+
+size_t ssim_blocks(int C, int H, int W) {
+    return size_t((W + kSsimTile - 1) / kSsimTile) * size_t((H + kSsimTile - 1) / kSsimTile) * size_t(C);
 }
 
 }  // namespace
 
 size_t ssim_workspace_bytes(int C, int H, int W) {
-    return 3 * size_t(C) * H * W * sizeof(float) + 256;
+    const size_t maps = 3 * size_t(C) * H * W * sizeof(float);
+    return ((maps + 255) & ~size_t(255)) + ssim_blocks(C, H, W) * sizeof(float2) + 256;
 }
 
 cudaError_t launch_l1_dssim(int C, int H, int W, const float* img, const float* tgt, float lambda, float scale,
                             float* dimg, float* loss, void* ws, cudaStream_t s) {
     SsimWindow win;
-    double t[2 * kSsimR + 1], sum = 0.0;
-    for (int i = 0; i <= 2 * kSsimR; ++i) {
+    double t[kSsimTaps], sum = 0.0;
+    for (int i = 0; i < kSsimTaps; ++i) {
         t[i] = std::exp(-double((i - kSsimR) * (i - kSsimR)) / (2.0 * 1.5 * 1.5));
         sum += t[i];
     }
-    for (int i = 0; i <= 2 * kSsimR; ++i) win.w[i] = float(t[i] / sum);
+    for (int i = 0; i < kSsimTaps; ++i) win.w[i] = float(t[i] / sum);
+    const size_t N = size_t(C) * H * W;
     float* abc = static_cast<float*>(ws);
-    float* sums = reinterpret_cast<float*>(static_cast<char*>(ws) + 3 * size_t(C) * H * W * sizeof(float));
-    cudaError_t e = cudaMemsetAsync(sums, 0, 2 * sizeof(float), s);
-    if (e != cudaSuccess) return e;
-    const int tiles = ((W + kSsimTile - 1) / kSsimTile) * ((H + kSsimTile - 1) / kSsimTile);
-    const dim3 grid{unsigned(tiles), unsigned(C), 1u};
-    pdl_launch(k_ssim_fwd, grid, 256, 0, s, win, C, H, W, img, tgt, abc, sums);
-    pdl_launch(k_ssim_bwd, grid, 256, 0, s, win, C, H, W, img, tgt, abc, lambda, scale, dimg);
-    if (loss) pdl_launch(k_ssim_loss, 1, 1, 0, s, sums, size_t(C) * H * W, lambda, scale, loss);
+    float2* partial = reinterpret_cast<float2*>(static_cast<char*>(ws) + ((3 * N * sizeof(float) + 255) & ~size_t(255)));
+    const dim3 grid{unsigned((W + kSsimTile - 1) / kSsimTile), unsigned((H + kSsimTile - 1) / kSsimTile), unsigned(C)};
+    // 16-byte staging copies need every row of every plane to start on a 16-byte boundary
+    const bool vec = W % 4 == 0 && ((reinterpret_cast<uintptr_t>(img) | reinterpret_cast<uintptr_t>(tgt)) & 15u) == 0;
+    if (vec) {
+        pdl_launch(k_ssim_fwd<true>, grid, kSsimThreads, 0, s, win, H, W, img, tgt, N, abc, partial);
+        pdl_launch(k_ssim_bwd<true>, grid, kSsimThreads, 0, s, win, H, W, img, tgt, N, abc, lambda, scale, dimg);
+    } else {
+        pdl_launch(k_ssim_fwd<false>, grid, kSsimThreads, 0, s, win, H, W, img, tgt, N, abc, partial);
+        pdl_launch(k_ssim_bwd<false>, grid, kSsimThreads, 0, s, win, H, W, img, tgt, N, abc, lambda, scale, dimg);
+    }
+    if (loss)
+        pdl_launch(k_ssim_loss, 1, 1024, 0, s, partial, uint32_t(ssim_blocks(C, H, W)), N, lambda, scale, loss);
     return cudaGetLastError();
 }
 

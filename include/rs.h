@@ -294,7 +294,7 @@ int rs_l1_loss_grad(size_t count, const float* d_image, const float* d_target, f
  * SSIM per channel and pixel with an 11 x 11 Gaussian window (sigma 1.5, separable weights
  * normalised over the window, zeros outside the image), C1 = 0.01^2, C2 = 0.03^2; means over all
  * C H W values.  Writes d_dL_dimage = scale * dL/dI [C][H][W] and, when d_loss is not NULL,
- * *d_loss = scale * L (one device float; accumulation order not fixed).  d_workspace: at least
+ * *d_loss = scale * L (one device float, summed in a fixed order).  d_workspace: at least
  * rs_l1_dssim_workspace_size bytes, 16-byte aligned, contents undefined on entry and exit.
  * Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CUDA. */
 int rs_l1_dssim_workspace_size(int32_t channels, int32_t height, int32_t width, size_t* bytes);
