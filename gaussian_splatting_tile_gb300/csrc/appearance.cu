@@ -611,6 +611,16 @@ __global__ void __launch_bounds__(kSsimThreads) k_ssim_fwd(SsimWindow win, int H
         float a[20], b[20];
         ssim_row_run(s_x, row, g, a);
         ssim_row_run(s_y, row, g, b);
+        // the products once per staged value (14 of them), not once per tap and output
+        constexpr int kRun = kSsimOut + 2 * kSsimR;
+        float xx[kRun], yy[kRun], xy[kRun];
+#pragma unroll
+        for (int i = 0; i < kRun; ++i) {
+            const float xa = a[kSsimLead + i], yb = b[kSsimLead + i];
+            xx[i] = xa * xa;
+            yy[i] = yb * yb;
+            xy[i] = xa * yb;
+        }
         float h[5][kSsimOut];
 #pragma unroll
         for (int o = 0; o < kSsimOut; ++o) h[0][o] = h[1][o] = h[2][o] = h[3][o] = h[4][o] = 0.f;
@@ -619,12 +629,11 @@ __global__ void __launch_bounds__(kSsimThreads) k_ssim_fwd(SsimWindow win, int H
             const float w = win.w[k];
 #pragma unroll
             for (int o = 0; o < kSsimOut; ++o) {
-                const float xa = a[kSsimLead + o + k], yb = b[kSsimLead + o + k];
-                h[0][o] = fmaf(w, xa, h[0][o]);
-                h[1][o] = fmaf(w, yb, h[1][o]);
-                h[2][o] = fmaf(w, xa * xa, h[2][o]);
-                h[3][o] = fmaf(w, yb * yb, h[3][o]);
-                h[4][o] = fmaf(w, xa * yb, h[4][o]);
+                h[0][o] = fmaf(w, a[kSsimLead + o + k], h[0][o]);
+                h[1][o] = fmaf(w, b[kSsimLead + o + k], h[1][o]);
+                h[2][o] = fmaf(w, xx[o + k], h[2][o]);
+                h[3][o] = fmaf(w, yy[o + k], h[3][o]);
+                h[4][o] = fmaf(w, xy[o + k], h[4][o]);
             }
         }
 #pragma unroll
@@ -705,6 +714,18 @@ __global__ void __launch_bounds__(kSsimThreads) k_ssim_bwd(SsimWindow win, int H
     const size_t plane = size_t(H) * W;
 #pragma unroll
     for (int q = 0; q < 3; ++q) ssim_stage<VEC>(abc + q * N + ch * plane, H, W, y0, x0 - kSsimLead, s_in[q]);
+    // the thread's own outputs' image and target values, loaded now to arrive during the filtering
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gx = x0 + kSsimR + lane;
+    float px[kSsimOut], py[kSsimOut];
+#pragma unroll
+    for (int o = 0; o < kSsimOut; ++o) {
+        const int gy = y0 + kSsimR + warp * kSsimOut + o;
+        const bool in = gy < H && gx < W;
+        const size_t at = ch * plane + size_t(in ? gy : 0) * W + (in ? gx : 0);
+        px[o] = in ? img[at] : 0.f;
+        py[o] = in ? tgt[at] : 0.f;
+    }
     ssim_stage_wait();
     for (int t = threadIdx.x; t < kSsimP * kSsimGroups; t += kSsimThreads) {
         const int row = t / kSsimGroups, g = t % kSsimGroups;
@@ -721,7 +742,6 @@ __global__ void __launch_bounds__(kSsimThreads) k_ssim_bwd(SsimWindow win, int H
         }
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float gsum[3][kSsimOut];
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
@@ -736,14 +756,13 @@ __global__ void __launch_bounds__(kSsimThreads) k_ssim_bwd(SsimWindow win, int H
             gsum[q][o] = acc;
         }
     }
-    const int gx = x0 + kSsimR + lane;
     const float inv = scale / float(N);
 #pragma unroll
     for (int o = 0; o < kSsimOut; ++o) {
         const int gy = y0 + kSsimR + warp * kSsimOut + o;
         if (gy >= H || gx >= W) continue;
         const size_t at = ch * plane + size_t(gy) * W + gx;
-        const float x = img[at], y = tgt[at];
+        const float x = px[o], y = py[o];
         const float d = x - y;
         const float sgn = d > 0.f ? 1.f : (d < 0.f ? -1.f : 0.f);
         const float dS = fmaf(2.f * x, gsum[1][o], fmaf(y, gsum[2][o], gsum[0][o]));
