@@ -2,14 +2,18 @@
 //
 // Per Gaussian and view: x = [latent ; unit view direction], h = relu(W1 x + b1),
 // colour = sigmoid(W2 h + b2).  The page runs one thread per Gaussian with the weights in shared
-// memory.  Here a warp takes 16 Gaussians at a time and runs both layers as mma.sync m16n8k8
-// TF32 products on the tensor cores with split operands: a = a_hi + a_lo with both parts TF32,
-// and a.b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi, which keeps float32 accuracy.  The first layer's
-// accumulator fragment is the second layer's A operand without any data movement: in k-chunk kc
-// of the second product, fragment columns t and t + 4 stand for hidden units kc*8 + 2t and
-// kc*8 + 2t + 1, which are the two accumulator columns lane (g, t) already holds.
+// memory.  All products keep float32 accuracy with split TF32 operands: a = a_hi + a_lo with both
+// parts TF32, and a.b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi.
 //
-// The backward recomputes both layers, forms dL/dz2 and dL/dz1 in registers, gets dL/dx with a
+// The forward runs the first layer on the fifth-generation tensor cores (tcgen05.mma, 128
+// Gaussians x HID per CTA, the accumulator in tensor memory) and the thin second layer (three
+// outputs) in float32 on the CUDA cores while reading the accumulator back.
+//
+// The backward takes 16 Gaussians per warp and runs its products as mma.sync m16n8k8 TF32: it
+// recomputes both layers (the first layer's accumulator fragment is the second layer's A
+// operand without any data movement: in k-chunk kc of the second product, fragment columns t
+// and t + 4 stand for hidden units kc*8 + 2t and kc*8 + 2t + 1, which are the two accumulator
+// columns lane (g, t) already holds), forms dL/dz2 and dL/dz1 in registers, gets dL/dx with a
 // third product (same renumbering), and accumulates the weight gradients from per-warp
 // shared-memory copies of dL/dz1, h and x, each lane owning whole hidden units; a block adds its
 // warps' sums in shared memory and flushes them with one global atomic per weight per block (the
@@ -188,38 +192,252 @@ __device__ __forceinline__ void layer2(const WeightSmem<HID>& w, const float (&h
 
 __device__ __forceinline__ float sigmoidf(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+// ---------------------------------------------------------------- forward on the tensor cores (tcgen05)
+// A CTA of 128 threads takes 128 Gaussians at a time (thread r = row r = TMEM lane r).  Layer 1,
+// Z = X W1^T [128 x HID] (X's columns: the view direction, then the latents; W1's columns staged
+// in the same order), runs as tcgen05.mma kind::tf32 (M = 128, N = HID, K = 8 per
+// instruction) with split operands, Z = Xh W1h + Xh W1l + Xl W1h (the three products that keep
+// float32 accuracy), accumulated in tensor memory.  X and W1 sit in shared memory in the
+// no-swizzle K-major layout of the PTX ISA's tcgen05 matrix descriptors: 8-row x 16-byte core
+// matrices of 128 contiguous bytes, the next core matrix along K 128 bytes on (leading byte
+// offset), the next 8-row group 2 KS x 128 bytes on (stride byte offset).  Each warp then reads
+// its 32 rows of Z from tensor memory (tcgen05.ld 32x32b), adds b1, applies relu and forms the
+// three outputs of the thin second layer (N = 3) in float32 before the sigmoid.
+__device__ unsigned int g_tc_error;  // set when a bounded tensor-core wait gave up
+
+constexpr int kTcRows = 128;
+constexpr uint32_t kTcWaitLimit = 1u << 22;  // mbarrier polls before a wait is given up
+
 template <int HID, int KS>
-__global__ void __launch_bounds__(kMlpThreads) k_mlp_fwd(MlpArgs a, float* __restrict__ colors) {
-    RS_PDL_ENTER();
-    extern __shared__ __align__(16) unsigned char smem[];
-    WeightSmem<HID>& w = *reinterpret_cast<WeightSmem<HID>*>(smem);
-    float* s_x = reinterpret_cast<float*>(smem + sizeof(WeightSmem<HID>)) +
-                 (threadIdx.x >> 5) * (kRows * kXStride);
-    load_weights<HID>(a, w);
-    __syncthreads();
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int tiles = (a.n + kRows - 1) / kRows;
-    for (int tile = blockIdx.x * kMlpWarps + (threadIdx.x >> 5); tile < tiles; tile += gridDim.x * kMlpWarps) {
-        const int i0 = tile * kRows;
-        stage_x<KS>(a, i0, s_x);
-        float h[HID / 8][4];
-        layer1<HID, KS>(w, s_x, h);
-        float z[4];
-        layer2<HID>(w, h, z);
-        // lane t = 0 holds channels 0, 1 and lane t = 1 channel 2, for rows g and g + 8
-        if (t < 2) {
+struct TcFwdSmem {
+    static constexpr int kCore = 128;                       // bytes per core matrix
+    static constexpr int kACores = (kTcRows / 8) * 2 * KS;  // X: 16 row groups x 2 KS core columns
+    static constexpr int kBCores = (HID / 8) * 2 * KS;      // W1: HID / 8 row groups
+    alignas(1024) uint8_t a_hi[kACores * kCore], a_lo[kACores * kCore];
+    alignas(128) uint8_t b_hi[kBCores * kCore], b_lo[kBCores * kCore];
+    alignas(16) float w2[3][HID];
+    alignas(16) float b1[HID];
+    float b2[4];
+    alignas(8) uint64_t mbar;
+    uint32_t tmem;
+};
+
+// Byte offset of element (row, k) in a K-major no-swizzle operand with 2 KS core columns.
+template <int KS>
+__device__ __forceinline__ int tc_kmajor_offset(int row, int k) {
+    return ((row >> 3) * (2 * KS) + (k >> 2)) * 128 + (row & 7) * 16 + (k & 3) * 4;
+}
+
+// tcgen05 shared-memory matrix descriptor (PTX ISA "Matrix Descriptors"): start address, leading
+// and stride byte offsets (all >> 4), the fixed 0b001 at bits 46-48, no swizzle.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(lbo >> 4) << 16) | (uint64_t(sbo >> 4) << 32) |
+           (uint64_t(1) << 46);
+}
+
+// Instruction descriptor of kind::tf32 (PTX ISA "Instruction descriptor"): D float32 (bits 4-5 = 1),
+// A and B TF32 (bits 7-9 and 10-12 = 2), both K-major, N >> 3 at bits 17-22, M >> 4 at 24-28.
+template <int N>
+__host__ __device__ constexpr uint32_t tc_idesc_tf32() {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(kTcRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u));
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+    for (uint32_t i = 0; i < kTcWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(mbar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// 32 consecutive tensor-memory columns of the warp's 32 lanes (tcgen05.ld 32x32b.x32): lane t
+// gets row (lane base + t), columns taddr .. taddr + 31.
+template <int COLS>
+__device__ __forceinline__ void tc_ld_rows(uint32_t taddr, float (&v)[COLS]);
+
+template <>
+__device__ __forceinline__ void tc_ld_rows<32>(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int i = i0 + g + 8 * half;
-                if (i < a.n) {
-                    const int c0 = 2 * t;
-                    colors[size_t(c0) * a.n + i] = sigmoidf(z[2 * half] + w.b2[c0]);
-                    if (t == 0) colors[size_t(1) * a.n + i] = sigmoidf(z[2 * half + 1] + w.b2[1]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int HID, int KS>
+__global__ void __launch_bounds__(kTcRows) k_mlp_fwd_tc(MlpArgs a, float* __restrict__ colors) {
+    RS_PDL_ENTER();
+    using Smem = TcFwdSmem<HID, KS>;
+    extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
+    // the operands' 1 KB alignment, whatever the dynamic region's base (1 KB of slack is allocated)
+    const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(tc_smem_raw));
+    Smem& sm = *reinterpret_cast<Smem*>(tc_smem_raw + ((1024u - (raw & 1023u)) & 1023u));
+    const int r = threadIdx.x, warp = r >> 5;
+    constexpr int K = KS * 8;
+    // W1 as TF32 heads and tails in the K-major layout, its columns in X's order (the view
+    // direction first, then the latents; zeros past D), W2 and the biases
+    for (int e = r; e < HID * K; e += kTcRows) {
+        const int j = e / K, k = e % K;
+        const int src = k < 3 ? a.L + k : k - 3;
+        const float v = k < a.D ? a.W1[j * a.D + src] : 0.f;
+        uint32_t h, l;
+        split(v, h, l);
+        const int o = tc_kmajor_offset<KS>(j, k);
+        *reinterpret_cast<uint32_t*>(sm.b_hi + o) = h;
+        *reinterpret_cast<uint32_t*>(sm.b_lo + o) = l;
+    }
+    for (int e = r; e < 3 * HID; e += kTcRows) sm.w2[e / HID][e % HID] = a.W2[e];
+    for (int e = r; e < HID; e += kTcRows) sm.b1[e] = a.b1[e];
+    if (r < 3) sm.b2[r] = a.b2[r];
+    const uint32_t mbar = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.mbar));
+    if (r == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mbar) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 0) {
+        const uint32_t slot = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.tmem));
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(slot), "r"(HID)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    const uint32_t tmem = sm.tmem;
+    const uint32_t a_hi = static_cast<uint32_t>(__cvta_generic_to_shared(sm.a_hi));
+    const uint32_t a_lo = static_cast<uint32_t>(__cvta_generic_to_shared(sm.a_lo));
+    const uint32_t b_hi = static_cast<uint32_t>(__cvta_generic_to_shared(sm.b_hi));
+    const uint32_t b_lo = static_cast<uint32_t>(__cvta_generic_to_shared(sm.b_lo));
+    constexpr uint32_t kSbo = 2 * KS * 128;
+    constexpr uint32_t idesc = tc_idesc_tf32<HID>();
+    // camera centre C = -R^T t
+    const CameraF& cam = a.cam;
+    const float C0 = -(cam.R[0] * cam.t[0] + cam.R[3] * cam.t[1] + cam.R[6] * cam.t[2]);
+    const float C1 = -(cam.R[1] * cam.t[0] + cam.R[4] * cam.t[1] + cam.R[7] * cam.t[2]);
+    const float C2 = -(cam.R[2] * cam.t[0] + cam.R[5] * cam.t[1] + cam.R[8] * cam.t[2]);
+    const int tiles = (a.n + kTcRows - 1) / kTcRows;
+    uint32_t phase = 0;
+    bool failed = false;
+    // this thread's row of X for a tile: the unit view direction, then the latents (zeros past D);
+    // the next tile's row is loaded while the current tile's products and epilogue run
+    float x[K - 3], d[3];
+    auto load_row = [&](int tile) {
+        const int i = tile * kTcRows + r;
+        const bool in = tile < tiles && i < a.n;
+#pragma unroll
+        for (int k = 0; k < K - 3; ++k) x[k] = in && k < a.L ? a.latents[size_t(k) * a.n + i] : 0.f;
+        d[0] = in ? a.means[i] - C0 : 0.f;
+        d[1] = in ? a.means[size_t(a.n) + i] - C1 : 0.f;
+        d[2] = in ? a.means[2 * size_t(a.n) + i] - C2 : 0.f;
+    };
+    load_row(blockIdx.x);
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int i = tile * kTcRows + r;
+        const bool in = i < a.n;
+        {
+            const float len = sqrtf(d[0] * d[0] + d[1] * d[1] + d[2] * d[2]);
+            const float il = len > 0.f ? 1.0f / len : 0.f;
+            const float dn[3] = {d[0] * il, d[1] * il, d[2] * il};
+#pragma unroll
+            for (int k = 0; k < K; k += 4) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int kk = k + q;
+                    split(kk < 3 ? dn[kk] : x[kk - 3], h[q], l[q]);
                 }
+                const int o = tc_kmajor_offset<KS>(r, k);
+                *reinterpret_cast<uint4*>(sm.a_hi + o) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(sm.a_lo + o) = make_uint4(l[0], l[1], l[2], l[3]);
             }
         }
-        __syncwarp();  // s_x is rewritten by the next tile
+        // the operands are visible to the tensor cores, and every warp is done reading the
+        // previous tile's tensor memory
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+        if (r == 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const uint32_t off = uint32_t(ks) * 2u * 128u;  // two core columns per K = 8 step
+                const uint64_t ah = tc_desc(a_hi + off, 128, kSbo), al = tc_desc(a_lo + off, 128, kSbo);
+                const uint64_t bh = tc_desc(b_hi + off, 128, kSbo), bl = tc_desc(b_lo + off, 128, kSbo);
+                tc_mma_tf32(tmem, ah, bh, idesc, ks > 0);
+                tc_mma_tf32(tmem, ah, bl, idesc, true);
+                tc_mma_tf32(tmem, al, bh, idesc, true);
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+                         : "memory");
+        }
+        load_row(tile + int(gridDim.x));
+        // the products are done (or every thread gives up together: the warp-wide loads and the
+        // barriers below need the whole CTA)
+        const bool ok = __syncthreads_and(mbar_wait(mbar, phase));
+        phase ^= 1u;
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+        if (!ok) {
+            // give up on this CTA: flag it, and let the output show it
+            atomicOr(&g_tc_error, 1u);
+            failed = true;
+            if (in)
+                for (int c = 0; c < 3; ++c) colors[size_t(c) * a.n + i] = __int_as_float(0x7fc00000);
+            break;
+        }
+        // relu(Z + b1) and the second layer, 32 hidden units at a time
+        float o0 = sm.b2[0], o1 = sm.b2[1], o2 = sm.b2[2];
+#pragma unroll
+        for (int half = 0; half < HID / 32; ++half) {
+            float z[32];
+            tc_ld_rows<32>(tmem + (uint32_t(warp * 32) << 16) + uint32_t(32 * half), z);
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+                const int j = 32 * half + jj;
+                const float4 bb = *reinterpret_cast<const float4*>(&sm.b1[j]);
+                const float4 u0 = *reinterpret_cast<const float4*>(&sm.w2[0][j]);
+                const float4 u1 = *reinterpret_cast<const float4*>(&sm.w2[1][j]);
+                const float4 u2 = *reinterpret_cast<const float4*>(&sm.w2[2][j]);
+                const float h0 = fmaxf(z[jj] + bb.x, 0.f), h1 = fmaxf(z[jj + 1] + bb.y, 0.f);
+                const float h2 = fmaxf(z[jj + 2] + bb.z, 0.f), h3 = fmaxf(z[jj + 3] + bb.w, 0.f);
+                o0 = fmaf(u0.x, h0, o0); o0 = fmaf(u0.y, h1, o0); o0 = fmaf(u0.z, h2, o0); o0 = fmaf(u0.w, h3, o0);
+                o1 = fmaf(u1.x, h0, o1); o1 = fmaf(u1.y, h1, o1); o1 = fmaf(u1.z, h2, o1); o1 = fmaf(u1.w, h3, o1);
+                o2 = fmaf(u2.x, h0, o2); o2 = fmaf(u2.y, h1, o2); o2 = fmaf(u2.z, h2, o2); o2 = fmaf(u2.w, h3, o2);
+            }
+        }
+        if (in) {
+            colors[i] = sigmoidf(o0);
+            colors[size_t(a.n) + i] = sigmoidf(o1);
+            colors[2 * size_t(a.n) + i] = sigmoidf(o2);
+        }
     }
+    // tensor memory goes back once no warp reads it and no product is in flight
+    if (failed) (void)mbar_wait(mbar, phase ^ 1u);
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(HID) : "memory");
 }
 
 // Per-warp staging of the backward and the block's gradient sums.
@@ -432,12 +650,13 @@ __global__ void __launch_bounds__(256) k_l1(size_t count, const float* __restric
 
 template <int HID, int KS>
 cudaError_t launch_fwd_t(const MlpArgs& a, float* colors, cudaStream_t s) {
-    const size_t smem = sizeof(WeightSmem<HID>) + size_t(kMlpWarps) * kRows * kXStride * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_mlp_fwd<HID, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    const size_t smem = sizeof(TcFwdSmem<HID, KS>) + 1024;  // + room to align the base to 1 KB
+    cudaError_t e = cudaFuncSetAttribute(k_mlp_fwd_tc<HID, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    const int tiles = (a.n + kRows - 1) / kRows;
-    const int blocks = std::min((tiles + kMlpWarps - 1) / kMlpWarps, 152 * 4);
-    pdl_launch(k_mlp_fwd<HID, KS>, blocks, kMlpThreads, smem, s, a, colors);
+    const int tiles = (a.n + kTcRows - 1) / kTcRows;
+    // at most 512 / HID CTAs can hold tensor memory on an SM at once
+    const int blocks = std::min(tiles, 152 * std::min(8, 512 / HID));
+    pdl_launch(k_mlp_fwd_tc<HID, KS>, blocks, kTcRows, smem, s, a, colors);
     return cudaGetLastError();
 }
 
@@ -492,6 +711,15 @@ cudaError_t launch_appearance_bwd(const CameraF& cam, int n, const float* means,
                                   const rs_mlp_grads& gr, cudaStream_t s) {
     const MlpArgs a = make_args(cam, n, means, latents, m);
     return m.hidden == 32 ? bwd_ks<32>(a, dcolors, dlatents, gr, s) : bwd_ks<64>(a, dcolors, dlatents, gr, s);
+}
+
+int take_device_error() {
+    unsigned int v = 0u;
+    if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v)) != cudaSuccess) return -1;
+    if (v == 0u) return 0;
+    const unsigned int zero = 0u;
+    if (cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    return 1;
 }
 
 cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float scale, float* dimg,

@@ -289,6 +289,11 @@ int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_rad
                                             static_cast<cudaStream_t>(stream)));
 }
 
+int rs_device_error(void) {
+    const int r = rs::take_device_error();
+    return r < 0 ? RS_ERR_CUDA : r > 0 ? RS_ERR_DEVICE_TIMEOUT : RS_OK;
+}
+
 int rs_l1_dssim_workspace_size(int32_t channels, int32_t height, int32_t width, size_t* bytes) {
     if (channels < 1 || height < 1 || width < 1 || height > 32768 || width > 32768 || channels > 64 || !bytes)
         return RS_ERR_INVALID_ARG;

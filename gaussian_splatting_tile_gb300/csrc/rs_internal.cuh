@@ -288,6 +288,9 @@ cudaError_t launch_appearance_bwd(const CameraF& cam, int n, const float* means,
 cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float scale, float* dimg,
                       float* loss, cudaStream_t s);
 // L1 + D-SSIM loss and gradient; the workspace holds 3 C H W floats and two sums.
+// 1 if a tensor-core wait gave up since the last call (the flag is cleared), 0 if not, -1 on a
+// CUDA error.
+int take_device_error();
 size_t ssim_workspace_bytes(int C, int H, int W);
 cudaError_t launch_l1_dssim(int C, int H, int W, const float* img, const float* tgt, float lambda, float scale,
                             float* dimg, float* loss, void* ws, cudaStream_t s);

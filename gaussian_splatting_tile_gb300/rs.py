@@ -83,10 +83,18 @@ _lib = None
 _VP = ctypes.c_void_p
 
 
+def declared_signatures(header: str = HEADER):
+    """(return type, name) of the entry points include/rs.h declares."""
+    text = open(header).read()
+    return sorted(set(re.findall(r"^\s*(int|const char\*|size_t)\s+(rs_\w+)\s*\(", text, re.M)))
+
+
 def declared_symbols(header: str = HEADER):
     """Names of the entry points include/rs.h declares."""
-    text = open(header).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*|size_t)\s+(rs_\w+)\s*\(", text, re.M)))
+    return sorted({name for _, name in declared_signatures(header)})
+
+
+_RESTYPES = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char*": ctypes.c_char_p}
 
 
 def lib():
@@ -133,8 +141,9 @@ def lib():
                                                  ctypes.POINTER(ctypes.c_size_t)]
         L.rs_l1_dssim_loss_grad.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _VP, _VP, ctypes.c_float,
                                             ctypes.c_float, _VP, _VP, _VP, ctypes.c_size_t, _VP]
-        for name in declared_symbols():
-            getattr(L, name).restype = ctypes.c_char_p if name == "rs_error_string" else ctypes.c_int
+        L.rs_device_error.argtypes = []
+        for ret, name in declared_signatures():
+            getattr(L, name).restype = _RESTYPES[ret]
         _lib = L
     return _lib
 
@@ -497,6 +506,12 @@ def rs_appearance_fwd(camera, means: torch.Tensor, latents: torch.Tensor, mlp: D
         ctypes.byref(c), n, _ptr(means, torch.float32, 3 * n, "means"),
         _ptr(latents, torch.float32, mlp.latent_dim * n, "latents"), ctypes.byref(m),
         _ptr(colors, torch.float32, 3 * n, "colors"), _stream(stream)))
+
+
+def rs_device_error() -> int:
+    """RS_ERR_DEVICE_TIMEOUT if a tensor-core wait gave up since the last call (the flag is
+    cleared), else RS_OK; synchronises the device."""
+    return int(lib().rs_device_error())
 
 
 def rs_appearance_bwd(camera, means: torch.Tensor, latents: torch.Tensor, mlp: DeviceMLP,

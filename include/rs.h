@@ -266,7 +266,9 @@ typedef struct rs_mlp_grads {
  * with C = -R^T t the camera centre, h = relu(W1 x + b1), colour = sigmoid(W2 h + b2).
  * Inputs: d_means [3][n], d_latents [latent_dim][n].  Output (overwritten): d_colors [3][n].
  * The products run on the tensor cores in TF32 with split operands (three products per
- * operand pair), which keeps float32 accuracy.  Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+ * operand pair), which keeps float32 accuracy.  Each CTA waits for its tensor-core products
+ * with a bounded wait; one that gives up writes NaN colours for its Gaussians and raises the
+ * flag rs_device_error reports.  Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
 int rs_appearance_fwd(const rs_camera* camera, int32_t n, const float* d_means,
                       const float* d_latents, const rs_mlp* mlp, float* d_colors, void* stream);
 
@@ -278,6 +280,11 @@ int rs_appearance_fwd(const rs_camera* camera, int32_t n, const float* d_means,
 int rs_appearance_bwd(const rs_camera* camera, int32_t n, const float* d_means,
                       const float* d_latents, const rs_mlp* mlp, const float* d_dL_dcolors,
                       float* d_dL_dlatents, const rs_mlp_grads* grads, void* stream);
+
+/* Reads and clears the device flag raised by a kernel whose bounded wait on the tensor cores gave
+ * up: RS_ERR_DEVICE_TIMEOUT if it was raised since the last call, else RS_OK (RS_ERR_CUDA if
+ * the flag cannot be read).  Synchronises the device. */
+int rs_device_error(void);
 
 /* L1 loss between an image and its target over `count` floats:
  * d_dL_dimage[i] = scale * sign(d_image[i] - d_target[i]) with sign(0) = 0 and, when d_loss is

@@ -97,6 +97,9 @@ def test_raster_workspace_validation(L):
         slots = cap // chunk + 1
         assert rs.rs_raster_workspace_size(camera, cap) >= slots * (chunk * 16 + 4) + 4 * 12
     assert rs.rs_raster_workspace_size(camera, 1_000_000) < rs.rs_raster_workspace_size(camera, 4_000_000)
+    # sizes past 2^31 bytes come back whole (the binding takes the header's size_t return type)
+    assert L.rs_raster_workspace_size.restype is ctypes.c_size_t
+    assert rs.rs_raster_workspace_size(camera, rs.RS_MAX_ENTRIES) >= (rs.RS_MAX_ENTRIES // chunk) * chunk * 16 > 2**31
     big = scenes.procedural_camera(1920, 1080)
     assert rs.rs_raster_workspace_size(big, 1000) >= rs.rs_raster_workspace_size(camera, 1000) + 4 * (8160 - 12) - 256
     assert L.rs_raster_workspace_size(ctypes.byref(cam), rs.RS_MAX_ENTRIES + 1) == 0

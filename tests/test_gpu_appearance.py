@@ -89,6 +89,37 @@ def test_mlp_matches_oracle(n, L, H, seed):
         allclose_report(k, getattr(grads, k).cpu().numpy(), O[k], GRAD_RTOL, GRAD_ATOL)
 
 
+@pytest.mark.parametrize("H", [64, 32])
+def test_mlp_many_tiles_per_block(H):
+    # 300k Gaussians: more 128-row tiles than the forward launches blocks, so each block walks
+    # several tiles (tensor memory and the completion barrier are reused across them)
+    n, L = 300_000, 8
+    rng = np.random.default_rng(11 + H)
+    cam = scenes.procedural_camera(64, 48, azimuth=0.7)
+    means = rng.uniform(-1.5, 1.5, (3, n)).astype(np.float32)
+    latents = rng.standard_normal((L, n)).astype(np.float32)
+    p = mlp_params(rng, L, H)
+    dcol = rng.standard_normal((3, n)).astype(np.float32)
+    dcol[:, relu_knife_edges(cam, means, latents, p["W1"], p["b1"])] = 0.0
+    mlp = rs.DeviceMLP.from_numpy(p)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    colors = torch.full((3, n), float("nan"), device="cuda")
+    rs.rs_appearance_fwd(cam, t(means), t(latents), mlp, colors)
+    dlat = torch.full((L, n), float("nan"), device="cuda")
+    grads = rs.DeviceMLPGrads.like(mlp)
+    rs.rs_appearance_bwd(cam, t(means), t(latents), mlp, t(dcol), dlat, grads)
+    torch.cuda.synchronize()
+    ref = oracle.appearance_fwd(cam, means, latents, p["W1"], p["b1"], p["W2"], p["b2"])
+    allclose_report("colors", colors.cpu().numpy(), ref, 1e-4, 1e-5)
+    O = oracle.appearance_bwd(cam, means, latents, p["W1"], p["b1"], p["W2"], p["b2"], dcol)
+    allclose_report("dlatents", dlat.cpu().numpy(), O["dlatents"], GRAD_RTOL, GRAD_ATOL)
+    # weight gradients are sums over 300k Gaussians: the absolute part scales with the largest sum
+    for k in ("dW1", "db1", "dW2", "db2"):
+        allclose_report(k, getattr(grads, k).cpu().numpy(), O[k], GRAD_RTOL, GRAD_ATOL, atol_of_max=1e-5)
+    # no block gave up waiting for its tensor-core products
+    assert rs.rs_device_error() == rs.RS_OK
+
+
 def test_mlp_empty():
     cam = scenes.procedural_camera(64, 48)
     p = mlp_params(np.random.default_rng(5), 8, 64)
