@@ -74,6 +74,43 @@ __device__ __forceinline__ uint32_t warp_mask(const float4& p, const float4& q, 
     return m;
 }
 
+// The warps of mask m (from warp_mask) whose 8x4 rectangle the entry's alpha >= 1/255 ellipse can
+// reach: the largest exponent over the rectangle (pixel centres relaxed to the continuous
+// rectangle, so nothing that passes is dropped) is compared with log2(1 / (255 opacity)), less a
+// margin that covers the rounding of both this test and the compositing's own evaluation.  The
+// exponent is concave, so outside its peak its largest value on a rectangle lies on the edge(s)
+// facing the peak; on an edge it is a parabola whose vertex is clamped to the edge.
+#ifndef RS_FWD_EXACT_MASK
+#define RS_FWD_EXACT_MASK 1
+#endif
+__device__ __forceinline__ float edge_peak(float qa, float qb, float qc, float fixed, float lo, float hi, float r2a) {
+    // max over t in [lo, hi] of qa t^2 + qb fixed t + qc fixed^2 (qa < 0); r2a = 1 / (2 qa)
+    const float t = fminf(fmaxf(-qb * fixed * r2a, lo), hi);
+    return fmaf(t, fmaf(qa, t, qb * fixed), (qc * fixed) * fixed);
+}
+
+__device__ __forceinline__ uint32_t warp_mask_exact(uint32_t m, const float4& p, const float4& q, const float4& c,
+                                                    int tx0, int ty0) {
+    constexpr float kLog2_255 = 7.994353436858858f;
+    constexpr float kMargin = 0.02f;  // log2 units: 1.4% of alpha
+    const float thr = __log2f(c.w) - kLog2_255 - kMargin;  // c.w = 1 / opacity
+    const float rx = __frcp_rn(2.f * q.x), rz = __frcp_rn(2.f * q.z);
+    uint32_t keep = 0u;
+    for (uint32_t mm = m; mm;) {
+        const int r = __ffs(mm) - 1;
+        mm &= mm - 1u;
+        const float X0 = float(tx0 + (r & 1) * 8) - p.x, X1 = X0 + 7.f;   // dx range
+        const float Y0 = float(ty0 + (r >> 1) * 4) - p.y, Y1 = Y0 + 3.f;  // dy range
+        float best = -INFINITY;
+        const bool inx = X0 <= 0.f && X1 >= 0.f, iny = Y0 <= 0.f && Y1 >= 0.f;
+        if (inx && iny) best = 0.f;
+        if (!inx) best = fmaxf(best, edge_peak(q.z, q.y, q.x, X0 > 0.f ? X0 : X1, Y0, Y1, rz));
+        if (!iny) best = fmaxf(best, edge_peak(q.x, q.y, q.z, Y0 > 0.f ? Y0 : Y1, X0, X1, rx));
+        if (best >= thr) keep |= 1u << r;
+    }
+    return keep;
+}
+
 // Compacts, in order, the staged entries j (< 256) for which `hit` holds into `list`; returns
 // the count.  Warp-cooperative: every lane of the warp must call it.
 template <typename Hit>
@@ -155,6 +192,9 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
             sm.q[threadIdx.x] = r.q;
             sm.c[threadIdx.x] = r.c;
             m = warp_mask(r.p, r.q, tx0, ty0);
+#if RS_FWD_EXACT_MASK
+            if (m) m = warp_mask_exact(m, r.p, r.q, r.c, tx0, ty0);
+#endif
         }
         sm.mask[threadIdx.x] = m;
         __syncthreads();
