@@ -322,12 +322,14 @@ class StreamedFrames:
     from pinned host memory and whose per-Gaussian gradients go back to pinned host memory, with
     the copies of one frame overlapping the compute of its neighbours.
 
-    Two slots, each a renderer with its own device inputs, gradients and per-view frame graphs,
-    alternate between frames.  Frame k's host-to-device copies run on an input copy stream once
-    frame k - 2 (same slot) has finished reading its inputs; its graph replays on the compute
-    stream once those copies and frame k - 2's device-to-host copies are done; its gradients go
-    back on an output copy stream once it has finished.  So the two copy directions and the
-    compute proceed at once, and a step costs about the longest of the three.
+    `slots` slots (at least two), each a renderer with its own device inputs, gradients,
+    per-view frame graphs and compute stream, take the frames in turn.  Frame k's host-to-device
+    copies run on an input copy stream once frame k - slots (same slot) has finished reading its
+    inputs; its graph replays on its slot's compute stream once those copies and frame
+    k - slots' device-to-host copies are done; its gradients go back on an output copy stream
+    once it has finished.  So the two copy directions and the compute of neighbouring frames
+    proceed at once (one frame's latency-bound binning overlaps another's compositing), and a
+    step costs about the longest of them.
 
     `host_in`: pinned float32 tensors means [3,N], scales [3,N], quats [4,N], opacity [N] and
     sh [3K,N] (or colors [3,N] with sh_degree -1); `host_dL`: pinned [3,H,W].  `host_out[slot]`
@@ -336,14 +338,15 @@ class StreamedFrames:
     OUT = ("dmeans", "dscales", "dquats", "dopacity")
 
     def __init__(self, cameras, host_in: dict, sh_degree: int, host_dL: torch.Tensor, device="cuda",
-                 capacity: int | None = None, bg=(0.0, 0.0, 0.0)):
+                 capacity: int | None = None, bg=(0.0, 0.0, 0.0), slots: int = 2):
         self.device = torch.device(device)
         self.cameras = list(cameras)
         self.host_in, self.host_dL, self.sh_degree = host_in, host_dL, sh_degree
         n = int(host_in["opacity"].shape[0])
         self.out_names = self.OUT + (("dsh",) if sh_degree >= 0 else ("dcolor",))
         self.slots = []
-        for _ in range(2):
+        self.n_slots = max(2, int(slots))
+        for _ in range(self.n_slots):
             R = Renderer(self.cameras[0], n, self.device, capacity=capacity, keep_keys=False)
             dev = {k: torch.empty_like(v, device=self.device) for k, v in host_in.items()}
             if sh_degree >= 0:
@@ -360,7 +363,7 @@ class StreamedFrames:
             self.slots.append(dict(R=R, dev=dev, dg=dg, ddL=ddL, host_out=host_out,
                                    graphs=FrameGraphs(R, dg, ddL, self.cameras, bg), in_ready=ev(),
                                    comp_done=ev(), out_done=ev(), frames=[]))
-        self.compute = torch.cuda.current_stream(self.device)
+        self.compute = [torch.cuda.Stream(self.device) for _ in self.slots]
         self.h2d = torch.cuda.Stream(self.device)
         self.d2h = torch.cuda.Stream(self.device)
         self.k = 0
@@ -371,10 +374,11 @@ class StreamedFrames:
 
     def prepare(self, views):
         """Captures the frame graphs of `views` in both slots (each capture runs one frame)."""
+        cur = torch.cuda.current_stream(self.device)
         for s in self.slots:
             for v in sorted(set(views)):
                 self._copy_in(s)
-                self.compute.wait_event(s["in_ready"])
+                cur.wait_event(s["in_ready"])
                 s["graphs"].get(v)
         torch.cuda.synchronize(self.device)
 
@@ -388,14 +392,16 @@ class StreamedFrames:
 
     def frame(self, view: int):
         """Enqueues one frame of `view`; nothing waits on the host."""
-        s = self.slots[self.k % 2]
+        slot = self.k % self.n_slots
+        s, cs = self.slots[slot], self.compute[slot]
         self.k += 1
         fg = s["graphs"].get(view)  # captured already after prepare(); else captured here
         self._copy_in(s)
-        self.compute.wait_event(s["in_ready"])
-        self.compute.wait_event(s["out_done"])  # the slot's previous gradients are on the host
-        fg.replay()
-        s["comp_done"].record(self.compute)
+        cs.wait_event(s["in_ready"])
+        cs.wait_event(s["out_done"])  # the slot's previous gradients are on the host
+        with torch.cuda.stream(cs):
+            fg.replay()
+        s["comp_done"].record(cs)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(s["comp_done"])
             for k in self.out_names:

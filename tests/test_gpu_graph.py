@@ -67,18 +67,19 @@ def test_frame_graph_replays_the_eager_frame():
     assert not torch.equal(ref2["image"], ref[2]["image"])
 
 
-def test_streamed_frames_match_eager_frames():
-    """pipeline.StreamedFrames (host inputs, host gradients, copies overlapping compute): the
-    gradients that reach pinned host memory equal the eager frame's, for the last frame of each
-    of its two slots; the entry counts match."""
+@pytest.mark.parametrize("slots", [2, 4])
+def test_streamed_frames_match_eager_frames(slots):
+    """pipeline.StreamedFrames (host inputs, host gradients, copies and the slots' compute
+    overlapping): the gradients that reach pinned host memory equal the eager frame's, for the
+    last frame of every slot; the entry counts match."""
     g = scenes.procedural_scene(seed=2, n_sphere=15_000, n_helix=4_000, n_plane=4_000)
     cams = [scenes.procedural_camera(320, 240, azimuth=a) for a in (0.3, 1.9, 3.4)]
     dL = scenes.image_grad(cams[0])
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).pin_memory()
     host = dict(means=pin(g.means), scales=pin(g.scales), quats=pin(g.quats), opacity=pin(g.opacity),
                 sh=pin(g.sh))
-    S = pipeline.StreamedFrames(cams, host, g.sh_degree, pin(dL))
-    views = [0, 1, 2, 1, 0, 2]
+    S = pipeline.StreamedFrames(cams, host, g.sh_degree, pin(dL), slots=slots)
+    views = [0, 1, 2, 1, 0, 2, 2, 0, 1]
     S.prepare(views)
     for v in views:
         S.frame(v)
@@ -87,7 +88,8 @@ def test_streamed_frames_match_eager_frames():
     R = pipeline.Renderer(cams[0], g.n)
     ref = {v: eager(R, dg, torch.from_numpy(dL).cuda(), cams[v]) for v in set(views)}
     assert all(c > 0 for c in counts) and len(counts) == len(views)
-    for slot, last in ((0, views[-2]), (1, views[-1])):  # frames alternate slots 0, 1, 0, ...
+    for slot in range(slots):  # frame k runs in slot k % slots
+        last = views[max(k for k in range(len(views)) if k % slots == slot)]
         out = S.host_out[slot]
         for k in ("dmeans", "dscales", "dquats", "dopacity", "dsh"):
             x, y = out[k].double(), ref[last][k].cpu().double()
