@@ -413,10 +413,11 @@ __device__ __forceinline__ void bwd_step(BwdPixel& px, float alpha, float raw, c
     const float Tj = __fdividef(px.T, one_m);
     w = alpha * Tj;
     const float cG = fmaf(c.x, px.G0, fmaf(c.y, px.G1, c.z * px.G2));
-    const float dalpha = Tj * (cG - px.SG);
-    px.SG = fmaf(alpha, cG, one_m * px.SG);
+    // dL/dalpha = Tj (cG - SG), and the entry's own colour joins SG: SG + alpha (cG - SG)
+    const float d = cG - px.SG;
+    px.SG = fmaf(alpha, d, px.SG);
     px.T = Tj;
-    gp = raw <= kAlphaMax ? alpha * dalpha : 0.f;  // not clamped: alpha = opacity * exp(power)
+    gp = raw <= kAlphaMax ? w * d : 0.f;  // alpha dL/dalpha; not clamped: alpha = opacity exp(power)
 }
 
 __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
