@@ -435,6 +435,11 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
+    # the entry count of every view lands in pinned memory in stream order (rs_bin_async) and is
+    # checked after the steps: no host wait inside a view
+    results = torch.zeros((warmup + steps) * len(cams), 2, dtype=torch.int64).pin_memory()
+    used = [0]
+
     def one(v, ev=None):
         cam = cams[v]
         rec = (lambda k: ev[k].record(stream)) if ev else (lambda k: None)
@@ -442,9 +447,11 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
         rec(0)
         rs.rs_appearance_fwd(cam, dg.means, lat, mlp, step.colors)
         rec(1)
-        F = step.R.forward(step.gc)
+        res = results[used[0]]
+        used[0] += 1
+        step.R.forward_async(step.gc, res)
         rec(2)
-        rs.rs_l1_loss_grad(F.image, targets[v], scale, step.dL_dimage, step.loss)
+        rs.rs_l1_loss_grad(step.R.image, targets[v], scale, step.dL_dimage, step.loss)
         rec(3)
         B = step.R.backward(step.gc, step.dL_dimage)
         rec(4)
@@ -464,6 +471,8 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
             one(v, ev)
             times.append(ev)
     torch.cuda.synchronize(device)
+    for k in range(used[0]):
+        step.R.check_async(results[k])  # raises if a view overflowed the capacity or timed out
     st = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(5)] for e in times])
     per_view = st.mean(axis=0)
     hbm, src = measured_peaks()
