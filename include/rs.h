@@ -361,8 +361,13 @@ int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_rad
  *    rs_bin_workspace_size(n, camera, capacity) exceeds RS_BIN_NOALLOC_SCRATCH_BYTES
  *    (48 MiB: about 3.5 million entries for 160,000 Gaussians at 1920x1080).
  *  - Set-up: the first call on a device, with that device current, looks up the array's device
- *    address (cudaGetSymbolAddress) and keeps it for later calls; make that first call before
- *    any stream capture.  RS_ERR_CUDA if the lookup fails.
+ *    address (cudaGetSymbolAddress) and keeps it for later calls.  Under the CUDA runtime's lazy
+ *    module loading (its default) that lookup is also what loads the array onto the device, so
+ *    this first call may allocate device memory and synchronise: make it once, as a warm-up,
+ *    outside any region where allocation is not allowed and before any stream capture.  If the
+ *    lookup fails the call returns RS_ERR_CUDA and the next call tries again.
+ *  - On RS_ERR_CUDA the call waits for `stream` before returning, so no work of the call still
+ *    uses the array when it returns.
  *  - Sharing: all calls use the same array and it keeps the last call's contents; nothing in it
  *    needs to start at zero.  Calls whose work overlaps on the GPU (other streams, other host
  *    threads on the same device) race on the array: serialise them.

@@ -150,8 +150,14 @@ def bin(cam, means2d, depth, radius):
                 n_entries=int(E))
 
 
-def bin_ellipse(cam, means2d, depth, radius, conic, alpha_k):
-    """c2' (exact ellipse-tile test) from float32 projected data; same outputs as bin()."""
+ELLIPSE_WIDEN = 0.02     # px: the square widened on every side for the "dropped for certain" test
+ELLIPSE_MARGIN = 1e-5    # relative margin on k
+
+
+def bin_ellipse(cam, means2d, depth, radius, conic, alpha_k, widen=ELLIPSE_WIDEN, margin=ELLIPSE_MARGIN):
+    """c2' (ellipse-tile test, from its definition in double precision) from float32 projected data.
+    Same outputs as bin(), plus the knife-edge decisions: `ambiguous` [M, 2] uint32 rows of
+    (Gaussian index, tile id) where either outcome is correct, and `ambiguous_gaussian` [n] bool."""
     m2 = np.ascontiguousarray(means2d, np.float32)
     dp = np.ascontiguousarray(depth, np.float32)
     rd = np.ascontiguousarray(radius, np.int32)
@@ -162,30 +168,45 @@ def bin_ellipse(cam, means2d, depth, radius, conic, alpha_k):
     n_tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
     ranges = np.zeros((n_tiles, 2), np.uint32)
     tt = np.zeros(n, np.uint32)
-    cap = 1 << 16
+    ag = np.zeros(n, np.uint8)
+    cap, acap = 1 << 16, 1 << 12
+    na = ctypes.c_int64(0)
     while True:
         keys = np.zeros(cap, np.uint64)
         pl = np.zeros(cap, np.uint32)
+        pairs = np.zeros((acap, 2), np.uint32)
         E = lib().orc_bin_ellipse(ctypes.byref(c), ctypes.c_int32(n), _p(m2), _p(dp), _p(rd), _p(cn), _p(ak),
-                                  ctypes.c_int64(cap), _p(keys), _p(pl), _p(ranges), _p(tt))
+                                  ctypes.c_double(widen), ctypes.c_double(margin), ctypes.c_int64(cap),
+                                  _p(keys), _p(pl), _p(ranges), _p(tt), _p(ag), ctypes.c_int64(acap),
+                                  _p(pairs), ctypes.byref(na))
         if E >= 0:
             break
-        cap = int(tt.astype(np.int64).sum()) + 1
-    return dict(keys_sorted=keys[:E], point_list=pl[:E], ranges=ranges, tiles_touched=tt, n_entries=int(E))
+        cap = max(cap, int(tt.astype(np.int64).sum()) + 1)
+        acap = max(acap, na.value + 1)
+    return dict(keys_sorted=keys[:E], point_list=pl[:E], ranges=ranges, tiles_touched=tt, n_entries=int(E),
+                ambiguous=pairs[:na.value].copy(), ambiguous_gaussian=ag.astype(bool))
 
 
-def ellipse_tiles(cam, u, v, A, B, C, k, radius, max_rows=4096):
-    """Rows and per-row column runs of the exact ellipse-tile test within the radius square:
-    list of (ty, xlo, xhi)."""
-    ylo = ctypes.c_int32(0)
-    xlo = np.zeros(max_rows, np.int32)
-    xhi = np.zeros(max_rows, np.int32)
+def ellipse_tiles(cam, u, v, A, B, C, k, radius, widen=ELLIPSE_WIDEN, margin=ELLIPSE_MARGIN):
+    """Decisions of the ellipse-tile test over one Gaussian's radius square: (rect, codes) with
+    rect = (xl, xh, yl, yh) half-open and codes [yh - yl, xh - xl] uint8, bit 0 kept, bit 1 knife edge."""
     c = _cam(cam)
+    rect = np.zeros(4, np.int32)
+    TX, TY = (cam.width + 15) // 16, (cam.height + 15) // 16
+    codes = np.zeros(TX * TY, np.uint8)
     f = ctypes.c_float
-    rows = lib().orc_ellipse_tiles(ctypes.byref(c), f(u), f(v), f(A), f(B), f(C), f(k), ctypes.c_int32(radius),
-                                   ctypes.byref(ylo),
-                                   _p(xlo), _p(xhi), ctypes.c_int32(max_rows))
-    return [(ylo.value + r, int(xlo[r]), int(xhi[r])) for r in range(min(rows, max_rows))]
+    cnt = lib().orc_ellipse_tiles(ctypes.byref(c), f(u), f(v), f(A), f(B), f(C), f(k), ctypes.c_int32(radius),
+                                  ctypes.c_double(widen), ctypes.c_double(margin), _p(rect), _p(codes),
+                                  ctypes.c_int64(codes.size))
+    assert cnt >= 0
+    xl, xh, yl, yh = (int(x) for x in rect)
+    return (xl, xh, yl, yh), codes[:cnt].reshape(yh - yl, xh - xl)
+
+
+def quad_min_rect(A, B, C, x0, x1, y0, y1):
+    lib().orc_quad_min_rect.restype = ctypes.c_double
+    d = ctypes.c_double
+    return lib().orc_quad_min_rect(d(A), d(B), d(C), d(x0), d(x1), d(y0), d(y1))
 
 
 def raster_fwd(cam, means2d, conic, opacity, color, ranges, point_list, bg=(0.0, 0.0, 0.0),

@@ -655,72 +655,52 @@ void view_dir(const Cam<double>& cam, const double* m, double* d) {
 
 }  // namespace
 
-// c2': the exact ellipse-tile test of the pages' "next" list, within the radius square (the
-// footprint the pages' binning renders).  The alpha >= 1/255 region of a splat is the ellipse
-// d^T Q d <= k (Q the conic (A, B; B, C), k = 2.002 ln(255 o) as given).
-// A tile row's band of pixel centres y in [16 ty, 16 ty + 15] meets it in an x-interval; the
-// leftmost point of the ellipse (x = -sqrt(C k / det) at dy = B sqrt(k / (det C))) bounds it
-// when it lies in the band, else the band edge nearer to it does, where the boundary is
-// x = -(B/A) dy - sqrt(A k - det dy^2) / A (1/A, B/A and A k formed once per splat); likewise on
-// the right.  Widened by 0.01 px.  Every step is one IEEE single-precision operation (this file
-// is built without contraction; divisions and square roots are correctly rounded), the same
-// sequence as the kernels' test, so both take identical integer decisions.
-struct EllipseF {
-    float u, v, nb, inva, ak, det, eyc, ex, dyl;
-    int ylo, yhi, xl, xh;
-};
+// c2': the ellipse-tile test of the pages' "next" list ([viewer] 2.3.4, footnote 3, names a
+// tighter test than the bounding square; the reading taken here is the exact one), stated from
+// its definition in double precision.
+// The region where a splat can reach alpha >= 1/255 is the ellipse q(d) = d^T Q d <= k, with Q
+// the conic ((A, B), (B, C)), d = pixel - mean and k = 2.002 ln(255 o) as given (0.1% wider than
+// the exact 2 ln(255 o)).  A tile of the splat's radius square is kept when its pixel-centre
+// square [16 tx, 16 tx + 15] x [16 ty, 16 ty + 15] holds a point of that region, i.e. when the
+// minimum of q over the square is at most k.
 
-// rect: the radius square's tile span {xl, xh, yl, yh} (half-open); the test keeps a subset of it.
-static bool ellipse_init(float u, float v, float A, float B, float C, float k, const int* rect, int TY,
-                         EllipseF& e) {
-    e.u = u; e.v = v;
-    e.xl = rect[0];
-    e.xh = rect[1];
-    e.ylo = 0; e.yhi = -1;
-    if (!(k > 0.f) || !(A > 0.f) || !(C > 0.f)) return false;
-    const float ac = A * C, bb = B * B;
-    e.det = ac - bb;
-    if (!(e.det > 0.f)) return false;
-    e.inva = 1.f / A;
-    e.nb = B * e.inva;
-    e.ak = A * k;
-    const float ck = C * k, dc = e.det * C;
-    e.eyc = std::sqrt(e.ak / e.det);
-    e.ex = std::sqrt(ck / e.det);
-    e.dyl = B * std::sqrt(k / dc);
-    const float ey = e.eyc + 0.01f;
-    const float vl = v - ey;
-    float lo = std::ceil((vl - 15.f) * 0.0625f);
-    float hi = std::floor((v + ey) * 0.0625f);
-    lo = std::fmin(std::fmax(lo, 0.f), float(TY));
-    hi = std::fmax(std::fmin(hi, float(TY - 1)), -1.f);
-    e.ylo = std::max(int(lo), rect[2]);
-    e.yhi = std::min(int(hi), rect[3] - 1);
-    return e.ylo <= e.yhi;
+// Minimum of the positive-definite quadratic q(x, y) = A x^2 + 2 B x y + C y^2 over the
+// rectangle [x0, x1] x [y0, y1].  If the rectangle holds the origin (q's minimum) it is 0.
+// Otherwise the convex q attains its minimum over the rectangle on the boundary; along an edge
+// it is a one-variable parabola, smallest at its vertex or, when the vertex is off the edge, at
+// the nearer end.
+static double quad_min_rect(double A, double B, double C, double x0, double x1, double y0, double y1) {
+    if (x0 <= 0.0 && 0.0 <= x1 && y0 <= 0.0 && 0.0 <= y1) return 0.0;
+    auto q = [&](double x, double y) { return A * x * x + 2.0 * B * x * y + C * y * y; };
+    double best = HUGE_VAL;
+    for (double x : {x0, x1}) {  // vertical edge: C y^2 + 2 B x y + A x^2, vertex y = -B x / C
+        const double y = std::min(std::max(-B * x / C, y0), y1);
+        best = std::min(best, q(x, y));
+    }
+    for (double y : {y0, y1}) {  // horizontal edge: vertex x = -B y / A
+        const double x = std::min(std::max(-B * y / A, x0), x1);
+        best = std::min(best, q(x, y));
+    }
+    return best;
 }
 
-// half-width of the ellipse at height dy: sqrt(A k - det dy^2) / A
-static float ellipse_half(const EllipseF& e, float dy) {
-    const float dy2 = dy * dy, ddy = e.det * dy2;
-    const float t = e.ak - ddy;
-    return std::sqrt(std::fmax(t, 0.f)) * e.inva;
-}
-
-static void ellipse_row(const EllipseF& e, int ty, int TX, int& xlo, int& xhi) {
-    const float y0 = std::fmin(std::fmax(float(16 * ty) - e.v, -e.eyc), e.eyc);
-    const float y1 = std::fmin(std::fmax(float(16 * ty + 15) - e.v, -e.eyc), e.eyc);
-    const float c0 = -(e.nb * y0), c1 = -(e.nb * y1);
-    const float h0 = ellipse_half(e, y0), h1 = ellipse_half(e, y1);
-    const float xmin = (y0 <= e.dyl && e.dyl <= y1) ? -e.ex : std::fmin(c0 - h0, c1 - h1);
-    const float dyr = -e.dyl;
-    const float xmax = (y0 <= dyr && dyr <= y1) ? e.ex : std::fmax(c0 + h0, c1 + h1);
-    const float ul = e.u + xmin, ur = e.u + xmax;
-    float lo = std::ceil((ul - 15.01f) * 0.0625f);
-    float hi = std::floor((ur + 0.01f) * 0.0625f);
-    lo = std::fmin(std::fmax(lo, 0.f), float(TX));
-    hi = std::fmax(std::fmin(hi, float(TX - 1)), -1.f);
-    xlo = std::max(int(lo), e.xl);
-    xhi = std::min(int(hi), e.xh - 1);
+// The decision for tile (tx, ty) and whether it is a knife edge.  The test is exact only up to
+// rounding in any implementation, so a decision is flagged as ambiguous -- either outcome
+// correct -- when it is not clear at a margin: kept for certain needs the minimum over the
+// square at most k (1 - margin); dropped for certain needs the minimum over the square widened
+// by `widen` pixels on every side above k (1 + margin).
+constexpr uint8_t ELL_KEEP = 1, ELL_AMBIG = 2;
+static uint8_t ellipse_tile_decision(double u, double v, double A, double B, double C, double k, int tx, int ty,
+                              double widen, double margin) {
+    if (!(k > 0.0) || !(A > 0.0) || !(C > 0.0) || !(A * C - B * B > 0.0)) return 0;
+    const double x0 = TILE * tx - u, x1 = TILE * tx + (TILE - 1) - u;
+    const double y0 = TILE * ty - v, y1 = TILE * ty + (TILE - 1) - v;
+    const double m = quad_min_rect(A, B, C, x0, x1, y0, y1);
+    const double mw = quad_min_rect(A, B, C, x0 - widen, x1 + widen, y0 - widen, y1 + widen);
+    const bool keep = m <= k;
+    const bool sure_keep = m <= k * (1.0 - margin);
+    const bool sure_drop = mw > k * (1.0 + margin);
+    return uint8_t((keep ? ELL_KEEP : 0) | (!sure_keep && !sure_drop ? ELL_AMBIG : 0));
 }
 
 extern "C" {
@@ -1095,54 +1075,67 @@ int orc_l1_dssim(int32_t C, int32_t H, int32_t W, const double* image, const dou
 
 
 int32_t orc_ellipse_tiles(const orc_camera* cam, float u, float v, float A, float B, float C, float k,
-                          int32_t radius, int32_t* ylo, int32_t* xlo, int32_t* xhi, int32_t max_rows) {
+                          int32_t radius, double widen, double margin, int32_t* rect, uint8_t* codes,
+                          int64_t max_codes) {
     const int TX = (cam->width + TILE - 1) / TILE, TY = (cam->height + TILE - 1) / TILE;
     const float r = float(radius);
-    const int rect[4] = {span_lo<float>(u, r, TX), span_hi<float>(u, r, TX), span_lo<float>(v, r, TY),
-                         span_hi<float>(v, r, TY)};
-    EllipseF e;
-    if (radius <= 0 || !ellipse_init(u, v, A, B, C, k, rect, TY, e)) return 0;
-    const int rows = e.yhi - e.ylo + 1;
-    if (ylo) *ylo = e.ylo;
-    for (int r = 0; r < rows && r < max_rows; ++r) {
-        int a, b;
-        ellipse_row(e, e.ylo + r, TX, a, b);
-        xlo[r] = a;
-        xhi[r] = b;
-    }
-    return rows;
+    rect[0] = span_lo<float>(u, r, TX);
+    rect[1] = span_hi<float>(u, r, TX);
+    rect[2] = span_lo<float>(v, r, TY);
+    rect[3] = span_hi<float>(v, r, TY);
+    if (radius <= 0) rect[1] = rect[0], rect[3] = rect[2];
+    const int64_t cols = rect[1] - rect[0], rows = rect[3] - rect[2];
+    if (cols * rows > max_codes) return -1;
+    for (int ty = rect[2]; ty < rect[3]; ++ty)
+        for (int tx = rect[0]; tx < rect[1]; ++tx)
+            codes[(ty - rect[2]) * cols + (tx - rect[0])] =
+                ellipse_tile_decision(u, v, A, B, C, k, tx, ty, widen, margin);
+    return int32_t(cols * rows);
 }
 
 int64_t orc_bin_ellipse(const orc_camera* cam, int32_t n, const float* means2d, const float* depth,
-                        const int32_t* radius, const float* conic, const float* alpha_k,
-                        int64_t capacity, uint64_t* keys_sorted, uint32_t* point_list,
-                        uint32_t* ranges, uint32_t* tiles_touched) {
+                        const int32_t* radius, const float* conic, const float* alpha_k, double widen,
+                        double margin, int64_t capacity, uint64_t* keys_sorted, uint32_t* point_list,
+                        uint32_t* ranges, uint32_t* tiles_touched, uint8_t* ambig_gauss,
+                        int64_t ambig_capacity, uint32_t* ambig_pairs, int64_t* n_ambig) {
     const int TX = (cam->width + TILE - 1) / TILE, TY = (cam->height + TILE - 1) / TILE;
     std::vector<Entry> ent;
+    int64_t na = 0;
     for (int32_t i = 0; i < n; ++i) {
         uint32_t cnt = 0;
-        EllipseF e;
-        const float u = means2d[i], v = means2d[size_t(n) + i], r = float(radius[i]);
-        const int rect[4] = {span_lo<float>(u, r, TX), span_hi<float>(u, r, TX), span_lo<float>(v, r, TY),
-                             span_hi<float>(v, r, TY)};
-        if (radius[i] > 0 &&
-            ellipse_init(u, v, conic[i], conic[size_t(n) + i], conic[2 * size_t(n) + i], alpha_k[i], rect, TY, e)) {
+        uint8_t amb = 0;
+        if (radius[i] > 0) {
+            const float u = means2d[i], v = means2d[size_t(n) + i], r = float(radius[i]);
+            const int xl = span_lo<float>(u, r, TX), xh = span_hi<float>(u, r, TX);
+            const int yl = span_lo<float>(v, r, TY), yh = span_hi<float>(v, r, TY);
             uint32_t bits;
             std::memcpy(&bits, &depth[i], 4);
-            for (int ty = e.ylo; ty <= e.yhi; ++ty) {
-                int xlo, xhi;
-                ellipse_row(e, ty, TX, xlo, xhi);
-                for (int tx = xlo; tx <= xhi; ++tx) {
-                    ++cnt;
+            for (int ty = yl; ty < yh; ++ty)
+                for (int tx = xl; tx < xh; ++tx) {
+                    const uint8_t d = ellipse_tile_decision(u, v, conic[i], conic[size_t(n) + i],
+                                                            conic[2 * size_t(n) + i], alpha_k[i], tx, ty,
+                                                            widen, margin);
                     const uint64_t tile = uint64_t(ty) * uint64_t(TX) + uint64_t(tx);
-                    ent.push_back(Entry{(tile << 32) | uint64_t(bits), uint32_t(i)});
+                    if (d & ELL_AMBIG) {
+                        amb = 1;
+                        if (na < ambig_capacity) {
+                            ambig_pairs[2 * na] = uint32_t(i);
+                            ambig_pairs[2 * na + 1] = uint32_t(tile);
+                        }
+                        ++na;
+                    }
+                    if (d & ELL_KEEP) {
+                        ++cnt;
+                        ent.push_back(Entry{(tile << 32) | uint64_t(bits), uint32_t(i)});
+                    }
                 }
-            }
         }
         if (tiles_touched) tiles_touched[i] = cnt;
+        if (ambig_gauss) ambig_gauss[i] = amb;
     }
+    *n_ambig = na;
     const int64_t E = int64_t(ent.size());
-    if (E > capacity) return -2;
+    if (E > capacity || na > ambig_capacity) return -2;
     std::stable_sort(ent.begin(), ent.end(), [](const Entry& a, const Entry& b) { return a.key < b.key; });
     std::vector<uint64_t> ks(static_cast<size_t>(E));
     for (int64_t q = 0; q < E; ++q) {
@@ -1152,6 +1145,10 @@ int64_t orc_bin_ellipse(const orc_camera* cam, int32_t n, const float* means2d, 
     }
     orc_tile_ranges(ks.data(), E, TX * TY, ranges);
     return E;
+}
+
+double orc_quad_min_rect(double A, double B, double C, double x0, double x1, double y0, double y1) {
+    return quad_min_rect(A, B, C, x0, x1, y0, y1);
 }
 
 }  // extern "C"

@@ -139,19 +139,28 @@ int orc_densify_stats(int32_t n, const double* dmeans2d, const int32_t* radius, 
 int orc_l1_dssim(int32_t C, int32_t H, int32_t W, const double* image, const double* target,
                  double lambda, double scale, double* grad, double* loss, double* ssim);
 
-/* c2': binning with the exact ellipse-tile test (the pages' "next" step): per visible Gaussian
- * only the tiles of its radius square whose pixel-centre squares meet the ellipse
- * d^T conic d <= alpha_k, in float
- * with the same operations as the kernels' test; otherwise as orc_bin.  The spans per row go to
- * spans [n_rows_total] when not NULL (testing). */
+/* c2': binning with the ellipse-tile test (the pages' "next" step), from its definition in
+ * double precision: per visible Gaussian (radius > 0) only the tiles of its radius square whose
+ * pixel-centre square [16 tx, 16 tx + 15] x [16 ty, 16 ty + 15] holds a point with
+ * d^T conic d <= alpha_k; otherwise as orc_bin.  A decision is a knife edge (either outcome
+ * correct) unless the minimum over the square is at most k (1 - margin) or the minimum over the
+ * square widened by `widen` px exceeds k (1 + margin); such (Gaussian, tile) pairs go to
+ * ambig_pairs [2 * ambig_capacity] as (index, tile id), their count to *n_ambig, and
+ * ambig_gauss [n] (may be NULL) marks Gaussians with any.  Returns E, or -2 when E > capacity or
+ * the pairs exceed ambig_capacity (the counts are still written). */
 int64_t orc_bin_ellipse(const orc_camera* cam, int32_t n, const float* means2d, const float* depth,
-                        const int32_t* radius, const float* conic, const float* alpha_k,
-                        int64_t capacity, uint64_t* keys_sorted, uint32_t* point_list,
-                        uint32_t* ranges, uint32_t* tiles_touched);
-/* The rows [ylo, yhi] and per-row columns [xlo[r], xhi[r]] of one Gaussian's ellipse test (up to
- * max_rows rows); returns the number of rows (0 when none). */
+                        const int32_t* radius, const float* conic, const float* alpha_k, double widen,
+                        double margin, int64_t capacity, uint64_t* keys_sorted, uint32_t* point_list,
+                        uint32_t* ranges, uint32_t* tiles_touched, uint8_t* ambig_gauss,
+                        int64_t ambig_capacity, uint32_t* ambig_pairs, int64_t* n_ambig);
+/* The decisions of one Gaussian over its radius square: rect = {xl, xh, yl, yh} (half-open),
+ * codes [(yh - yl) * (xh - xl)] row-major, bit 0 kept, bit 1 knife edge.  Returns the number of
+ * codes, or -1 when they exceed max_codes. */
 int32_t orc_ellipse_tiles(const orc_camera* cam, float u, float v, float A, float B, float C, float k,
-                          int32_t radius, int32_t* ylo, int32_t* xlo, int32_t* xhi, int32_t max_rows);
+                          int32_t radius, double widen, double margin, int32_t* rect, uint8_t* codes,
+                          int64_t max_codes);
+/* Minimum of A x^2 + 2 B x y + C y^2 (positive definite) over [x0, x1] x [y0, y1]. */
+double orc_quad_min_rect(double A, double B, double C, double x0, double x1, double y0, double y1);
 
 #ifdef __cplusplus
 }

@@ -213,12 +213,44 @@ def test_forward_is_deterministic():
         assert np.array_equal(a[k], b[k]), k
 
 
+def pair_codes(idx, tile):
+    return (np.asarray(idx, np.uint64) << np.uint64(32)) | np.asarray(tile, np.uint64)
+
+
+def check_ellipse_binning(cam, g, sq, el):
+    """The GPU's ellipse binning against the oracle's, which states the test from its definition
+    in double precision: keys, point lists and counts equal on every (Gaussian, tile) decision
+    that is not a knife edge (at knife edges either outcome is correct, and those pairs are left
+    out of the comparison on both sides).  The oracle reads the square test's projection (the
+    radius square and the values of every Gaussian, including those the GPU's ellipse test culled)
+    and the GPU's k where the GPU kept the Gaussian (else k from its definition, in float32)."""
+    o = g.opacity.astype(np.float64)
+    k_def = np.where(255 * o > 1, 2.002 * np.log(np.maximum(255 * o, 1.0)), 0.0).astype(np.float32)
+    k = np.where(el["radius"] > 0, el["alpha_k"], k_def).astype(np.float32)
+    Be = oracle.bin_ellipse(cam, sq["means2d"], sq["depth"], sq["radius"], sq["conic"], k)
+    amb = pair_codes(Be["ambiguous"][:, 0], Be["ambiguous"][:, 1])
+    gpu_pairs = pair_codes(el["point_list"], el["keys"] >> np.uint64(32))
+    orc_pairs = pair_codes(Be["point_list"], Be["keys_sorted"] >> np.uint64(32))
+    keep_g, keep_o = ~np.isin(gpu_pairs, amb), ~np.isin(orc_pairs, amb)
+    assert np.array_equal(el["keys"][keep_g], Be["keys_sorted"][keep_o])
+    assert np.array_equal(el["point_list"][keep_g], Be["point_list"][keep_o])
+    clear = ~Be["ambiguous_gaussian"]
+    assert np.array_equal(el["tiles_touched"][clear], Be["tiles_touched"][clear])
+    assert np.array_equal(el["radius"][clear] > 0, Be["tiles_touched"][clear] > 0)
+    # the GPU's ranges are those of its own sorted keys
+    assert np.array_equal(el["ranges"].reshape(-1, 2), oracle.tile_ranges(el["keys"], cam.n_tiles))
+    if amb.size == 0:
+        assert np.array_equal(el["ranges"].reshape(-1, 2), Be["ranges"])
+    assert amb.size <= 0.01 * max(1, Be["n_entries"])
+    return Be
+
+
 @pytest.mark.parametrize("which", ["tiny", "160k_1080p"])
 def test_ellipse_tile_test(which):
-    """RS_TILE_TEST_ELLIPSE: binning bit-exact against the oracle's ellipse binning on the same
-    projected data; the image and final_T bit-identical to the square test's (the dropped tiles
-    hold only alpha < 1/255); gradients equal to the square test's up to summation order; fewer
-    entries; n_contrib never larger."""
+    """RS_TILE_TEST_ELLIPSE: binning equal to the oracle's ellipse binning on the same projected
+    data, decision by decision off knife edges; the image and final_T bit-identical to the square
+    test's (the dropped tiles hold only alpha < 1/255); gradients equal to the square test's up to
+    summation order; fewer entries; n_contrib never larger."""
     if which == "tiny":
         g, cam = scenes.tiny_scene(seed=0)
     else:
@@ -239,13 +271,7 @@ def test_ellipse_tile_test(which):
             st["alpha_k"] = R.proj.alpha_k.cpu().numpy()
         out[mode] = st
     sq, el = out[rs.RS_TILE_TEST_SQUARE], out[rs.RS_TILE_TEST_ELLIPSE]
-    # binning against the oracle, on the GPU's projected data
-    Be = oracle.bin_ellipse(cam, el["means2d"], el["depth"], el["radius"], el["conic"], el["alpha_k"])
-    assert el["n_entries"] == Be["n_entries"]
-    assert np.array_equal(el["tiles_touched"], Be["tiles_touched"])
-    assert np.array_equal(el["keys"], Be["keys_sorted"])
-    assert np.array_equal(el["point_list"], Be["point_list"])
-    assert np.array_equal(el["ranges"].reshape(-1, 2), Be["ranges"])
+    check_ellipse_binning(cam, g, sq, el)
     assert el["n_entries"] < sq["n_entries"]
     # projection: the ellipse test only culls; k = 2.002 ln(255 o)
     vis = el["radius"] > 0

@@ -1,29 +1,29 @@
-"""Pins of the oracle's exact ellipse-tile test (c2', the pages' next binning step), CPU only.
+"""Pins of the oracle's ellipse-tile test (c2', the pages' next binning step), CPU only.
 
-For random splats the tiles the test keeps are compared with brute force in double precision:
-every tile holding a pixel centre with d^T Q d <= k must be kept (the test is conservative),
-and every kept tile must come within 0.02 px (the widening) of the ellipse with k x (1 + 1e-6)
-(the test is tight); with a finite radius the kept tiles lie inside the radius square.  The
-binning built on it keeps the (tile, depth) order of the square test's entries restricted to the
-kept tiles."""
+The oracle keeps a tile of a splat's radius square when the minimum of q(d) = d^T Q d over the
+tile's pixel-centre square is at most k.  It is pinned against things that do not share its
+arithmetic:
+  - its rectangle minimum against scipy's bounded least squares (q = |L^T d|^2 with Q = L L^T, a
+    library routine) and against the closed form of an axis-aligned ellipse;
+  - its decisions against brute force over the integer pixel centres (every tile holding a pixel
+    centre inside the ellipse is kept), against the ellipse's closed-form bounding box (no tile
+    outside it is kept), and, tile by tile, against the bounded least-squares minimum;
+  - its binning: the square binning's per-tile lists with entries removed, order kept."""
 import numpy as np
+from scipy.optimize import lsq_linear
 
 import oracle
 from gaussian_splatting_tile_gb300 import scenes
 
 
-def brute_min_over_rect(A, B, C, x0, x1, y0, y1):
-    """min of A x^2 + 2 B x y + C y^2 over the rectangle [x0, x1] x [y0, y1] (double)."""
-    if x0 <= 0 <= x1 and y0 <= 0 <= y1:
-        return 0.0
-    best = np.inf
-    for X in (x0, x1):
-        y = np.clip(-B * X / C, y0, y1)
-        best = min(best, A * X * X + 2 * B * X * y + C * y * y)
-    for Y in (y0, y1):
-        x = np.clip(-B * Y / A, x0, x1)
-        best = min(best, A * x * x + 2 * B * x * Y + C * Y * Y)
-    return best
+def lsq_min(A, B, C, x0, x1, y0, y1):
+    """min of A x^2 + 2 B x y + C y^2 over a rectangle by bounded least squares."""
+    Lc = np.linalg.cholesky(np.array([[A, B], [B, C]], np.float64))  # Q = Lc Lc^T
+    if x0 == x1 and y0 == y1:
+        d = np.array([x0, y0])
+        return float(d @ np.array([[A, B], [B, C]]) @ d)
+    r = lsq_linear(Lc.T, np.zeros(2), bounds=([x0, y0], [x1, y1]), method="bvls", tol=1e-14)
+    return 2.0 * r.cost
 
 
 def random_splats(rng, count, cam):
@@ -39,29 +39,84 @@ def random_splats(rng, count, cam):
         yield np.float32(u), np.float32(v), Q[0, 0], Q[0, 1], Q[1, 1], k
 
 
-def test_conservative_and_tight_against_brute_force():
+def test_rectangle_minimum_against_bounded_least_squares():
+    rng = np.random.default_rng(1)
+    for _ in range(3000):
+        M = rng.normal(size=(2, 2))
+        Q = M @ M.T + 0.05 * np.eye(2)
+        A, B, C = Q[0, 0], Q[0, 1], Q[1, 1]
+        x0, y0 = rng.uniform(-30, 30, 2)
+        x1, y1 = x0 + rng.uniform(0, 20), y0 + rng.uniform(0, 20)
+        got = oracle.quad_min_rect(A, B, C, x0, x1, y0, y1)
+        ref = lsq_min(A, B, C, x0, x1, y0, y1)
+        assert abs(got - ref) <= 1e-9 * max(1.0, ref), (A, B, C, x0, x1, y0, y1, got, ref)
+
+
+def test_rectangle_minimum_closed_form_axis_aligned():
+    # B = 0: the minimum is A dist(0, [x0, x1])^2 + C dist(0, [y0, y1])^2
+    dist = lambda a, b: 0.0 if a <= 0 <= b else min(abs(a), abs(b))
+    rng = np.random.default_rng(2)
+    for _ in range(500):
+        A, C = rng.uniform(0.01, 3, 2)
+        x0, y0 = rng.uniform(-30, 30, 2)
+        x1, y1 = x0 + rng.uniform(0, 20), y0 + rng.uniform(0, 20)
+        ref = A * dist(x0, x1) ** 2 + C * dist(y0, y1) ** 2
+        assert abs(oracle.quad_min_rect(A, 0.0, C, x0, x1, y0, y1) - ref) <= 1e-12 * max(1, ref)
+    # a hand case: unit circle scaled by 1/sigma^2 = 1/25 at (8, 8); tile (1, 0) starts at x = 16,
+    # 8 px away: q = 64 / 25 = 2.56, kept for k = 2.56 (1 + 2e-5) and dropped for k = 2.56 (1 - 2e-5)
+    cam = scenes.procedural_camera(64, 64)
+    for k, kept in ((2.56 * (1 + 2e-5), 1), (2.56 * (1 - 2e-5), 0)):
+        rect, codes = oracle.ellipse_tiles(cam, 8.0, 8.0, 0.04, 0.0, 0.04, k, 1 << 20, widen=0.0)
+        xl, xh, yl, yh = rect
+        assert codes[0 - yl, 1 - xl] & 1 == kept and codes[0 - yl, 1 - xl] & 2 == 0
+
+
+def test_decisions_against_pixel_centres_bounding_box_and_least_squares():
     rng = np.random.default_rng(0)
     cam = scenes.procedural_camera(200, 136)
     TX, TY = (cam.width + 15) // 16, (cam.height + 15) // 16
-    for u, v, A, B, C, k in random_splats(rng, 400, cam):
-        rows = oracle.ellipse_tiles(cam, u, v, A, B, C, k, 1 << 20)  # the square does not bind
-        kept = {(ty, tx) for ty, lo, hi in rows for tx in range(lo, hi + 1)}
-        r = int(rng.integers(3, 40))
-        sq = lambda p, n: (int(np.clip(np.floor((p - r) / 16), 0, n)), int(np.clip(np.floor((p + r) / 16) + 1, 0, n)))
-        (xl, xh), (yl, yh) = sq(float(u), TX), sq(float(v), TY)
-        kept_r = {(ty, tx) for ty, lo, hi in oracle.ellipse_tiles(cam, u, v, A, B, C, k, r) for tx in range(lo, hi + 1)}
-        assert kept_r == {(ty, tx) for ty, tx in kept if yl <= ty < yh and xl <= tx < xh}
+    px, py = np.meshgrid(np.arange(16 * TX, dtype=np.float64), np.arange(16 * TY, dtype=np.float64))
+    n_amb = n_dec = 0
+    for u, v, A, B, C, k in random_splats(rng, 250, cam):
+        rect, codes = oracle.ellipse_tiles(cam, u, v, A, B, C, k, 1 << 20)  # the square does not bind
+        assert rect == (0, TX, 0, TY)
+        kept, amb = (codes & 1) != 0, (codes & 2) != 0
+        n_amb += int(amb.sum())
+        n_dec += codes.size
         Ad, Bd, Cd, kd = float(A), float(B), float(C), float(k)
+        # every tile holding a pixel centre inside the ellipse is kept
+        dx, dy = px - float(u), py - float(v)
+        inside = (Ad * dx * dx + 2 * Bd * dx * dy + Cd * dy * dy) <= kd * (1 - 1e-5)
+        hit = inside.reshape(TY, 16, TX, 16).any(axis=(1, 3))
+        assert not (hit & ~kept & ~amb).any()
+        # nothing outside the ellipse's bounding box |dx| <= sqrt(k C / det), |dy| <= sqrt(k A / det)
+        det = Ad * Cd - Bd * Bd
+        ex, ey = (np.sqrt(kd * Cd / det), np.sqrt(kd * Ad / det)) if kd > 0 else (-1.0, -1.0)
         for ty in range(TY):
             for tx in range(TX):
                 x0, x1 = 16 * tx - float(u), 16 * tx + 15 - float(u)
                 y0, y1 = 16 * ty - float(v), 16 * ty + 15 - float(v)
-                m = brute_min_over_rect(Ad, Bd, Cd, x0, x1, y0, y1)
-                if kd > 0 and m <= kd * (1 - 1e-6):
-                    assert (ty, tx) in kept, (u, v, A, B, C, k, ty, tx)
-                if (ty, tx) in kept:
-                    mw = brute_min_over_rect(Ad, Bd, Cd, x0 - 0.02, x1 + 0.02, y0 - 0.02, y1 + 0.02)
-                    assert mw <= kd * (1 + 1e-6), (u, v, A, B, C, k, ty, tx, mw)
+                if x1 < -ex - 1e-9 or x0 > ex + 1e-9 or y1 < -ey - 1e-9 or y0 > ey + 1e-9:
+                    assert not kept[ty, tx]
+                    continue
+                if amb[ty, tx]:
+                    continue
+                m = lsq_min(Ad, Bd, Cd, x0, x1, y0, y1)
+                assert kept[ty, tx] == (m <= kd), (u, v, A, B, C, k, ty, tx, m)
+    assert n_amb <= 0.01 * n_dec
+
+
+def test_radius_square_bounds_the_kept_tiles():
+    rng = np.random.default_rng(3)
+    cam = scenes.procedural_camera(200, 136)
+    TX, TY = (cam.width + 15) // 16, (cam.height + 15) // 16
+    for u, v, A, B, C, k in random_splats(rng, 200, cam):
+        (_, _, _, _), full = oracle.ellipse_tiles(cam, u, v, A, B, C, k, 1 << 20)
+        r = int(rng.integers(3, 40))
+        (xl, xh, yl, yh), sub = oracle.ellipse_tiles(cam, u, v, A, B, C, k, r)
+        assert (xl, xh) == (int(np.clip(np.floor((u - r) / 16), 0, TX)), int(np.clip(np.floor((u + r) / 16) + 1, 0, TX)))
+        assert (yl, yh) == (int(np.clip(np.floor((v - r) / 16), 0, TY)), int(np.clip(np.floor((v + r) / 16) + 1, 0, TY)))
+        assert np.array_equal(sub, full[yl:yh, xl:xh])
 
 
 def test_binning_is_the_square_binning_restricted_to_kept_tiles():
@@ -82,7 +137,13 @@ def test_binning_is_the_square_binning_restricted_to_kept_tiles():
         el = list(Be["point_list"][e0:e1])
         it = iter(sq)
         assert all(x in it for x in el)  # subsequence
-    # and each Gaussian's count is the number of tiles the test keeps for it
-    for i in np.flatnonzero(rd > 0)[:200]:
-        rows = oracle.ellipse_tiles(cam, m2[0, i], m2[1, i], con[0, i], con[1, i], con[2, i], k[i], rd[i])
-        assert Be["tiles_touched"][i] == sum(max(0, hi - lo + 1) for _, lo, hi in rows)
+    # each Gaussian's count is the number of tiles the test keeps for it, and its knife edges are
+    # the ones listed
+    amb = {(int(i), int(t)) for i, t in Be["ambiguous"]}
+    for i in np.flatnonzero(rd > 0)[:300]:
+        (xl, xh, yl, yh), codes = oracle.ellipse_tiles(cam, m2[0, i], m2[1, i], con[0, i], con[1, i], con[2, i],
+                                                       k[i], rd[i])
+        assert Be["tiles_touched"][i] == int((codes & 1).sum())
+        listed = {t for j, t in amb if j == i}
+        assert listed == {(yl + a) * cam.tiles_x + xl + b for a, b in zip(*np.nonzero(codes & 2))}
+        assert Be["ambiguous_gaussian"][i] == bool(listed)

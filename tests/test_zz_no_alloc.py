@@ -32,10 +32,14 @@ def _bin_both(g, cam, capacity):
 def test_noalloc_matches_rs_bin_on_two_calls_in_a_row():
     build_lib.build()
     assert torch.cuda.is_available()
-    cases = [scenes.tiny_scene(seed=0),
+    tiny = scenes.tiny_scene(seed=0)
+    cases = [tiny,
              (scenes.procedural_scene(seed=1, n_sphere=40_000, n_helix=10_000, n_plane=10_000),
-              scenes.procedural_camera(640, 480, azimuth=0.7))]
-    for g, cam in cases:  # two calls in a row, different sizes: the scratch is reused
+              scenes.procedural_camera(640, 480, azimuth=0.7)),
+             tiny]
+    # calls in a row on one shared array: small, larger, then small again over the larger call's
+    # leftovers
+    for g, cam in cases:
         E_ref, ref, E, got = _bin_both(g, cam, capacity=1_000_000)
         assert E == E_ref > 0
         for a, b in zip(ref, got):
@@ -47,13 +51,21 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     build_lib.build()
     g, cam = scenes.tiny_scene(seed=0)
     R = pipeline.Renderer(cam, g.n, capacity=4096)
+    R.project(rs.DeviceGaussians.from_numpy(g))
+    R.keys_sorted.fill_(-3)
+    R.point_list.fill_(-5)
+    R.tile_ranges.fill_(-7)
+    torch.cuda.synchronize()
     too_many = 8_000_000  # about 160 MB of sort buffers, beyond the 48 MiB array
     import ctypes
     c = rs.camera_struct(cam)
     p = R.proj.struct()
-    E = ctypes.c_size_t(0)
+    E = ctypes.c_size_t(12345)
     rc = rs.lib().rs_bin_noalloc(ctypes.byref(c), ctypes.byref(p), g.n, too_many,
                                  ctypes.c_void_p(R.keys_sorted.data_ptr()),
                                  ctypes.c_void_p(R.point_list.data_ptr()),
                                  ctypes.c_void_p(R.tile_ranges.data_ptr()), ctypes.byref(E), None)
+    torch.cuda.synchronize()
     assert rc == rs.RS_ERR_WORKSPACE
+    assert E.value == 12345
+    assert (R.keys_sorted == -3).all() and (R.point_list == -5).all() and (R.tile_ranges == -7).all()
