@@ -76,6 +76,14 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def workload_config():
+    """The headline workload, the same for both arms."""
+    return dict(workload="160k Gaussians (sphere shell 100k + helix 30k + checkered plane 30k), SH degree 3, "
+                         "1920x1080, 60-view orbit at radius 4.3, 50-degree vertical FOV; fwd+bwd per view",
+                n_gaussians=160_000, width=WIDTH, height=HEIGHT, views=VIEWS,
+                l2="inputs resident; a 256 MB buffer is written before every timed group of views (not timed)")
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -92,6 +100,9 @@ def parse():
                     help="skip the fused Adam step's timing (reported beside the line)")
     ap.add_argument("--no-train", action="store_true",
                     help="skip the training-shaped step's stage timings (reported beside the line)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration timings (tiny, 720x720, 1280x720 and 1920x1080 orbits, 1M)")
+    ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -188,6 +199,235 @@ def launches_per_step(n: int, E: int, n_tiles: int) -> int:
     return project + binning + fwd + bwd
 
 
+# ------------------------------------------------------------------ measured compute peaks
+
+def measure_peaks(device, reps: int = 3):
+    """Rates of the instructions the compositing kernels are bound by, measured on this GPU at the
+    clock it runs at (include/rs_peaks.h): FP32 fused multiply-adds (lane ops/s), the MUFU ex2
+    (lane ops/s) and scattered red.global.add.f32 to an L2-resident buffer (ops/s), best of
+    `reps` launches of about 50-100 ms each, after one warm-up launch; clocks sampled meanwhile."""
+    import ctypes
+
+    import torch
+
+    from gaussian_splatting_tile_gb300 import rs
+
+    L = rs.lib()
+    L.rs_device_sm_count.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+    for f in (L.rs_peak_ffma, L.rs_peak_ex2):
+        f.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+    L.rs_peak_red.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_uint32,
+                              ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+    sm = ctypes.c_int32(0)
+    if L.rs_device_sm_count(ctypes.byref(sm)) != 0:
+        raise RuntimeError("rs_device_sm_count failed")
+    blocks = sm.value * 8  # 2048 resident threads per SM
+    sink = torch.zeros(blocks * 256, dtype=torch.float32, device=device)
+    n_red = 160_000 * 9  # the compositing backward's per-Gaussian sums at 160k Gaussians (5.8 MB)
+    target = torch.zeros(n_red, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    h = ctypes.c_void_p(stream.cuda_stream)
+
+    def best(fn, *args):
+        out = ctypes.c_double(0.0)
+        rate = 0.0
+        for r in range(reps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc = fn(*args, ctypes.byref(out), h)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            if rc != 0:
+                raise RuntimeError(f"{fn.__name__} returned {rc}")
+            if r:
+                rate = max(rate, out.value / (a.elapsed_time(b) * 1e-3))
+        return rate
+
+    clocks = ClockSampler(device.index or 0)
+    clocks.start()
+    ffma = best(L.rs_peak_ffma, blocks, 40_000, ctypes.c_void_p(sink.data_ptr()))
+    ex2 = best(L.rs_peak_ex2, blocks, 5_000, ctypes.c_void_p(sink.data_ptr()))
+    red = best(L.rs_peak_red, blocks, 4_000, ctypes.c_void_p(target.data_ptr()), n_red)
+    clk = clocks.stop()
+    mhz = clk["sm_mhz"] or MAX_MHZ
+    return dict(sms=sm.value, fp32_lane_ops_per_s=ffma, mufu_ex2_per_s=ex2, red_f32_per_s=red,
+                sm_mhz=clk["sm_mhz"], clock_reasons=clk["reasons"],
+                nominal_at_clock=dict(fp32_lane_ops_per_s=sm.value * FP32_LANES * mhz * 1e6,
+                                      mufu_ex2_per_s=sm.value * MUFU_LANES * mhz * 1e6),
+                how="rs_peak_ffma / rs_peak_ex2 / rs_peak_red: 8 blocks of 256 threads per SM, 8 independent "
+                    "chains per thread (red: scattered words of a 5.8 MB buffer), best of 3 timed launches")
+
+
+# ------------------------------------------------------------------ the configurations of the workload
+
+def config_scenes(name):
+    """(gaussians, cameras, description) of one configuration of the workload."""
+    from gaussian_splatting_tile_gb300 import scenes
+    if name == "C1":
+        g, cam = scenes.tiny_scene(seed=0)
+        return g, [cam], "tiny: 2,000 Gaussians, SH degree 0, 128x128, f = 150, camera at distance 4"
+    if name == "C2":
+        return (scenes.procedural_scene(seed=0), [scenes.procedural_camera(720, 720, focal=700.0)],
+                "160k procedural scene, SH degree 3, 720x720, f = 700, radius 4.3, elevation 0.5 rad")
+    if name == "C3a":
+        return (scenes.procedural_scene(seed=0), scenes.orbit_cameras(1280, 720, VIEWS),
+                "160k procedural scene, SH degree 3, 1280x720, 50-degree vertical FOV, 60-view orbit")
+    if name == "C3b":
+        return (scenes.procedural_scene(seed=0), scenes.orbit_cameras(WIDTH, HEIGHT, VIEWS),
+                "160k procedural scene, SH degree 3, 1920x1080, 50-degree vertical FOV, 60-view orbit")
+    if name == "C4":
+        g, cam = scenes.stress_scene(seed=0)
+        return g, [cam], "stress: 1,000,000 Gaussians in a 6x6x6 cube, SH degree 3, 1920x1080 from distance 5"
+    raise KeyError(name)
+
+
+CONFIG_NAMES = ("C1", "C2", "C3a", "C3b", "C4")
+
+
+def time_config(name, device, flush, reps_single: int = 10):
+    """One configuration on the GPU: every view (60 for the orbits) launched call by call with CUDA
+    events between the five stages (sync-free binning), then replayed one view at a time as one
+    CUDA graph per view with events around each replay; L2 written over before every timed frame.
+    Returns per-view fwd / bwd / fwd+bwd times, entries and examined entries (Q = sum n_contrib)."""
+    import numpy as np
+    import torch
+
+    from gaussian_splatting_tile_gb300 import pipeline, rs, scenes
+
+    g, cams, desc = config_scenes(name)
+    views = len(cams)
+    if views == 1:  # a single view is timed reps_single times (medians over the repeats)
+        cams = cams * reps_single
+    dg = rs.DeviceGaussians.from_numpy(g, device)
+    dL = torch.from_numpy(scenes.image_grad(cams[0])).to(device)
+    R = pipeline.Renderer(cams[0], g.n, device, keep_keys=False)
+    stream = torch.cuda.current_stream(device)
+    Q, E_eager = [], []
+    for cam in cams:  # sizes the buffers (rs_bin grows them), warms up, counts Q
+        R.set_camera(cam)
+        R.forward(dg)
+        Q.append(float(R.n_contrib.to(torch.int64).sum().item()))
+        E_eager.append(R.n_entries)
+    R.backward(dg, dL)  # the last view's forward is still in the buffers
+    res = torch.zeros(len(cams), 2, dtype=torch.int64).pin_memory()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in cams]
+    torch.cuda.synchronize(device)
+    for i, cam in enumerate(cams):
+        flush.fill_(float(i))
+        e = ev[i]
+        R.set_camera(cam)
+        e[0].record(stream)
+        R.project(dg)
+        e[1].record(stream)
+        R.bin_async(res[i])
+        e[2].record(stream)
+        R.rasterize()
+        e[3].record(stream)
+        R._grads(dg.sh_degree)
+        R.rasterize_backward(dL)
+        e[4].record(stream)
+        R.project_backward(dg)
+        e[5].record(stream)
+    torch.cuda.synchronize(device)
+    ents = [int(x) for x in res[:, 0].tolist()]
+    if ents != E_eager or int(res[:, 1].abs().sum()):
+        raise RuntimeError(f"{name}: sync-free binning disagrees with rs_bin or timed out")
+    st = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(5)] for e in ev])
+    graphs = pipeline.FrameGraphs(R, dg, dL, cams[:views])
+    for v in range(views):
+        graphs.get(v).replay()
+    torch.cuda.synchronize(device)
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
+    counts = []
+    for v in range(len(cams)):
+        flush.fill_(float(v))
+        gev[v][0].record(stream)
+        fg = graphs.get(v % views)
+        fg.replay()
+        gev[v][1].record(stream)
+        if views == 1:
+            torch.cuda.synchronize(device)
+            counts.append(fg.check())
+    torch.cuda.synchronize(device)
+    if views > 1:
+        counts = [graphs.get(v).check() for v in range(views)]
+    if counts != ents:
+        raise RuntimeError(f"{name}: graph replays disagree with the call-by-call frames")
+    lat = np.array([a.elapsed_time(b) for a, b in gev])
+    fb = st.sum(axis=1)
+    E = np.array(ents, np.float64)
+    out = dict(workload=desc, n_gaussians=g.n, width=cams[0].width, height=cams[0].height, views=views,
+               timed_frames=len(cams),
+               entries=dict(mean=float(E.mean()), min=int(E.min()), max=int(E.max())),
+               examined_Q=dict(mean=float(np.mean(Q)), min=float(np.min(Q)), max=float(np.max(Q))),
+               call_by_call_ms=dict(fwd=float(np.median(st[:, 0:3].sum(axis=1))),
+                                    bwd=float(np.median(st[:, 3:5].sum(axis=1))),
+                                    fwd_bwd=float(np.median(fb)),
+                                    stages=dict(zip(["project", "bin", "rasterize_fwd", "rasterize_bwd", "project_bwd"],
+                                                    [float(x) for x in np.median(st, axis=0)]))),
+               graph_ms_per_frame=dict(median=float(np.median(lat)), min=float(lat.min()), max=float(lat.max())),
+               entries_per_s_graph=float(E.sum() / (lat.sum() * 1e-3)),
+               entries_per_s_call_by_call=float(E.sum() / (fb.sum() * 1e-3)))
+    out["_stage_means"] = dict(zip(["project", "bin", "rasterize_fwd", "rasterize_bwd", "project_bwd"],
+                                   [float(x) for x in st.mean(axis=0)]))
+    out["_cam"] = cams[0]
+    del graphs, R
+    torch.cuda.synchronize(device)
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle timings (worker process)
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return None
+
+
+def pin_to_one_core():
+    """Pins this process to one core (the last one it may run on); returns that core."""
+    cores = sorted(os.sched_getaffinity(0))
+    os.sched_setaffinity(0, {cores[-1]})
+    return cores[-1]
+
+
+def oracle_worker(names):
+    """Times the oracle (single thread, pinned to one core) on one view of each named
+    configuration, stage by stage; prints one JSON object.  Runs as its own process so that it
+    overlaps the GPU timing without sharing the GPU process's cores."""
+    core = pin_to_one_core()
+    out = dict(core=core, cpu_model=cpu_model(), host_cpus=os.cpu_count(), configs={})
+    for name in names:
+        g, cams, _ = config_scenes(name)
+        frame_s, E, ratio, d = oracle_frame(g, cams[0])
+        out["configs"][name] = dict(frame_s=frame_s, entries=E, blend_ratio=ratio, stage_s=d,
+                                    entries_per_s=E / frame_s)
+    print(json.dumps(out), flush=True)
+
+
+def start_oracle_worker(names):
+    """Starts the oracle timings in a fresh Python process (no fork of this CUDA process)."""
+    return subprocess.Popen([sys.executable, os.path.abspath(__file__), "--oracle-worker", ",".join(names)],
+                            stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, cwd=ROOT)
+
+
+def finish_oracle_worker(proc, timeout=900):
+    try:
+        out, err = proc.communicate(timeout=timeout)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+        out, err = proc.communicate()
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    if proc.returncode != 0 or not lines:
+        raise RuntimeError(f"oracle worker failed ({proc.returncode}): {err[-2000:]}")
+    return json.loads(lines[-1])
+
+
 # ------------------------------------------------------------------ our implementation
 
 def run_ours(args):
@@ -198,6 +438,11 @@ def run_ours(args):
     from gaussian_splatting_tile_gb300 import pipeline, rs, scenes
 
     rank, world, local_rank = dist_env()
+    # the oracle's timings run in a process of their own, pinned to one core, started before this
+    # process touches the GPU; they overlap the GPU timing and are collected at the end
+    worker = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        worker = start_oracle_worker(CONFIG_NAMES if not args.no_configs else ("C3b",))
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     if world > 1 and not dist.is_initialized():
@@ -353,24 +598,19 @@ def run_ours(args):
                   warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True,
                   scaling="weak", vs_baseline=value / T4_ENTRIES_PER_S, dtype="f32",
                   data="synthetic (seeded procedural scene; no dataset)",
-                  config=dict(workload="160k Gaussians (sphere shell 100k + helix 30k + checkered plane "
-                                       "30k), SH degree 3, 1920x1080, 60-view orbit at radius 4.3, "
-                                       "50-degree vertical FOV; fwd+bwd per view",
-                              n_gaussians=g.n, width=WIDTH, height=HEIGHT, views=VIEWS,
-                              l2="256 MB buffer written before every timed group of views in flight "
-                                 "(not timed)",
-                              views_in_flight=M,
+                  config=workload_config(),
+                  timing=dict(views_in_flight=M,
                               binning="rs_bin_async: the entry count is copied to pinned host memory in "
                                       "stream order and checked after the timed steps (no host wait "
                                       "inside the frame)",
-                              timing="headline: the timed views views_in_flight at a time, each on its "
-                                     "own stream with its own renderer, every view one CUDA graph replay "
-                                     "captured before the timed region (every kernel runs at every replay); "
-                                     "CUDA events around each group; ms_per_step = summed group time / "
-                                     "views. "
-                                     "latency_ms_per_frame: the same graphs one view at a time on one "
-                                     "stream; stage_ms/fwd_ms/bwd_ms: the same frames launched call by "
-                                     "call with CUDA events between the stages (eager_ms_per_step)"),
+                              how="headline: the timed views views_in_flight at a time, each on its "
+                                  "own stream with its own renderer, every view one CUDA graph replay "
+                                  "captured before the timed region (every kernel runs at every replay); "
+                                  "CUDA events around each group; ms_per_step = summed group time / "
+                                  "views. "
+                                  "latency_ms_per_frame: the same graphs one view at a time on one "
+                                  "stream; stage_ms/fwd_ms/bwd_ms: the same frames launched call by "
+                                  "call with CUDA events between the stages (eager_ms_per_step)"),
                   fwd_ms=fwd_ms, bwd_ms=bwd_ms, wall_ms_timed_region=wall_ms,
                   stage_ms=dict(zip(["project", "bin", "rasterize_fwd", "rasterize_bwd", "project_bwd"],
                                     [float(x) for x in stage.mean(axis=0)])),
@@ -380,11 +620,12 @@ def run_ours(args):
                               reasons=sorted(set(clk_p["reasons"]) | set(clk_g["reasons"]) | set(clk["reasons"]))),
                   gpu_launches=sum(launches_per_step(g.n, E, cams[0].n_tiles) for E in entries))
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(g, cams[views[0]])
-        result["cpu_baseline"] = cpu
-    blend_ratio = result.get("cpu_baseline", {}).get("blend_ratio")
-    result["roofline"], result["roofline_step"] = roofline(result, Q, E_mean, g.n, cams[0], blend_ratio)
+    peaks = measure_peaks(device)
+    result["peaks"] = {k: v for k, v in peaks.items()}
+    configs = {}
+    if world == 1 and not args.no_configs:
+        for name in CONFIG_NAMES:
+            configs[name] = time_config(name, device, flush)
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(g, cams, rank, world, args, device)
@@ -395,6 +636,43 @@ def run_ours(args):
     if world == 1 and not args.no_adam:
         result["adam"] = run_adam(g, device)
         result["l1_dssim"] = run_l1_dssim(device)
+
+    oracle_t = finish_oracle_worker(worker) if worker is not None else None
+    blend_ratio = None
+    if oracle_t is not None:
+        c = oracle_t["configs"]["C3b"]
+        blend_ratio = c["blend_ratio"]
+        result["cpu_baseline"] = dict(
+            value=c["entries_per_s"], unit=UNIT, cores=1, kind="oracle",
+            sample="one full 1920x1080 view (orbit view 0, all tiles) of the 160k scene: projection, binning, "
+                   "compositing forward and backward, projection backward; single thread, float64, "
+                   "pinned to one core (in its own process, while the GPU timings ran)",
+            ms_per_frame=c["frame_s"] * 1e3, blend_ratio=c["blend_ratio"],
+            stage_s=c["stage_s"], cpu_model=oracle_t["cpu_model"], host_cpus=oracle_t["host_cpus"])
+    result["roofline"], result["roofline_step"] = roofline(result["stage_ms"], result["ms_per_step"], Q, E_mean,
+                                                           g.n, cams[0], blend_ratio, peaks)
+    if configs:
+        out = {}
+        for name, c in configs.items():
+            cam = c.pop("_cam")
+            st = c.pop("_stage_means")
+            o = oracle_t["configs"].get(name) if oracle_t else None
+            ratio = o["blend_ratio"] if o else None
+            gq = c["examined_Q"]["mean"]
+            dom, step = roofline(st, sum(st.values()), gq, c["entries"]["mean"], c["n_gaussians"], cam, ratio, peaks,
+                                 sh_degree=0 if name == "C1" else 3)
+            c["roofline"] = dict(step_frac_call_by_call=step["frac"], roofline_ms=step["roofline_ms"],
+                                 per_stage_frac=step["per_stage_frac"], rasterize_bwd_frac=dom["frac"],
+                                 composited_fraction=ratio)
+            if o:
+                c["oracle"] = dict(ms_per_frame=o["frame_s"] * 1e3, entries_per_s=o["entries_per_s"],
+                                   stage_s=o["stage_s"], view="first view of the configuration, all tiles",
+                                   cores=1)
+            out[name] = c
+        result["configs"] = out
+        if oracle_t:
+            result["oracle_host"] = dict(cpu_model=oracle_t["cpu_model"], host_cpus=oracle_t["host_cpus"],
+                                         pinned_core=oracle_t["core"])
     if world > 1:
         dist.barrier()
     if rank == 0:
@@ -623,40 +901,54 @@ def run_l1_dssim(device, steps: int = 20, warmup: int = 3):
                 roofline=dict(bound="hbm", unit="GB/s", achieved=gbs, peak=hbm, frac=gbs / hbm, peak_source=src))
 
 
-def roofline(res, Q, E, n, cam, blend_ratio):
-    """Dominant kernel (compositing backward) against the FP32 pipe, and the whole step against
-    the sum of per-stage roofline times."""
-    hbm_gbs, src = measured_peaks()
-    fp32 = SMS * FP32_LANES * MAX_MHZ * 1e6   # lane ops/s
-    mufu = SMS * MUFU_LANES * MAX_MHZ * 1e6
-    bw = hbm_gbs * 1e9
+def stage_roofline(Q, E, n, cam, blend_ratio, peaks, sh_degree=3):
+    """Per-stage roofline times (s) of one frame: max of algorithmic bytes / HBM bandwidth, FP32
+    lane ops / the measured FFMA rate and ex2 / the measured MUFU rate (the counts above)."""
+    hbm_gbs, _ = measured_peaks()
+    fp32, mufu, bw = peaks["fp32_lane_ops_per_s"], peaks["mufu_ex2_per_s"], hbm_gbs * 1e9
+    K = (sh_degree + 1) ** 2 if sh_degree >= 0 else 0
+    colour_in = 12 * K if K else 12
+    b_proj = 44 + colour_in + 44                  # means, scales, quats, opacity, colour source in; outputs
+    b_proj_bwd = (44 + colour_in + 32 + 4) + (40 + (12 * K if K else 0))
     r = blend_ratio if blend_ratio is not None else 0.0
     Qb = Q * r
     HW = cam.width * cam.height
-    ops_bwd = Q * OPS_BWD_EXAMINED + Qb * OPS_BWD_BLEND
-    t_bwd = res["stage_ms"]["rasterize_bwd"] * 1e-3
-    dominant = dict(kernel="rasterize_bwd (k_zero4 + k_raster_bwd)", bound="alu",
-                    achieved=ops_bwd / t_bwd / 1e12, peak=fp32 / 1e12, unit="Tops/s",
-                    frac=(ops_bwd / t_bwd) / fp32, traffic=TRAFFIC_RASTER_BWD_BYTES,
-                    traffic_source=TRAFFIC_RASTER_BWD_SOURCE,
-                    peak_source=f"152 SMs x 128 FP32 lanes x {MAX_MHZ:.0f} MHz (max SM clock)",
-                    ops_per_launch=ops_bwd, composited_fraction=r,
-                    composited_fraction_source="oracle on the timed view" if blend_ratio is not None else "unknown: counted as 0")
     t = {}
-    t["project"] = max(n * B_PROJECT_PER_G / bw, n * OPS_PROJECT_PER_G / fp32)
+    t["project"] = max(n * b_proj / bw, n * OPS_PROJECT_PER_G / fp32)
     tile_passes = math.ceil(max(1, math.ceil(math.log2(cam.n_tiles))) / 8)
     t["bin"] = (n * B_BIN_PER_G + E * (B_BIN_PER_ENTRY_FIXED + B_BIN_PER_ENTRY_PASS * tile_passes)
                 + cam.n_tiles * 8) / bw
     t["rasterize_fwd"] = max((E * B_FWD_PER_ENTRY + HW * B_FWD_PER_PIXEL) / bw,
                              (Q * OPS_FWD_EXAMINED + Qb * OPS_FWD_BLEND) / fp32, Q / mufu)
+    ops_bwd = Q * OPS_BWD_EXAMINED + Qb * OPS_BWD_BLEND
     t["rasterize_bwd"] = max((E * B_BWD_PER_ENTRY + HW * B_BWD_PER_PIXEL + n * B_BWD_PER_G) / bw,
                              ops_bwd / fp32, (Q + Qb) / mufu)
-    t["project_bwd"] = max(n * B_PROJECT_BWD_PER_G / bw, n * OPS_PROJECT_BWD_PER_G / fp32)
+    t["project_bwd"] = max(n * b_proj_bwd / bw, n * OPS_PROJECT_BWD_PER_G / fp32)
+    return t, ops_bwd
+
+
+def roofline(stage_ms, ms_per_step, Q, E, n, cam, blend_ratio, peaks, sh_degree=3):
+    """Dominant kernel (compositing backward) against the measured FP32 rate, and the whole step
+    against the sum of per-stage roofline times."""
+    hbm_gbs, src = measured_peaks()
+    t, ops_bwd = stage_roofline(Q, E, n, cam, blend_ratio, peaks, sh_degree)
+    fp32 = peaks["fp32_lane_ops_per_s"]
+    t_bwd = stage_ms["rasterize_bwd"] * 1e-3
+    peak_src = (f"measured: rs_peak_ffma, {peaks['sms']} SMs at {peaks['sm_mhz']} MHz sampled "
+                f"(nominal at that clock {peaks['nominal_at_clock']['fp32_lane_ops_per_s'] / 1e12:.1f} Tops/s)")
+    dominant = dict(kernel="rasterize_bwd (k_zero4 + k_raster_bwd)", bound="alu",
+                    achieved=ops_bwd / t_bwd / 1e12, peak=fp32 / 1e12, unit="Tops/s",
+                    frac=(ops_bwd / t_bwd) / fp32, traffic=TRAFFIC_RASTER_BWD_BYTES,
+                    traffic_source=TRAFFIC_RASTER_BWD_SOURCE, peak_source=peak_src,
+                    ops_per_launch=ops_bwd, composited_fraction=blend_ratio,
+                    composited_fraction_source="oracle on the timed view" if blend_ratio is not None
+                    else "unknown: counted as 0")
     t_roof = sum(t.values())
-    measured = res["ms_per_step"] * 1e-3
-    step = dict(roofline_ms=t_roof * 1e3, measured_ms=res["ms_per_step"], frac=t_roof / measured,
+    step = dict(roofline_ms=t_roof * 1e3, measured_ms=ms_per_step, frac=t_roof / (ms_per_step * 1e-3),
                 per_stage_roofline_ms={k: v * 1e3 for k, v in t.items()},
-                hbm_gbs=hbm_gbs, hbm_source=src, fp32_tops=fp32 / 1e12, mufu_tops=mufu / 1e12)
+                per_stage_frac={k: t[k] / (stage_ms[k] * 1e-3) for k in t if stage_ms.get(k)},
+                hbm_gbs=hbm_gbs, hbm_source=src, fp32_tops=fp32 / 1e12,
+                mufu_tops=peaks["mufu_ex2_per_s"] / 1e12, peaks_source="measured (rs_peaks.h)")
     return dominant, step
 
 
@@ -704,10 +996,10 @@ def run_e2e(g, cams, rank, world, args, device):
 
 # ------------------------------------------------------------------ CPU oracle (baseline)
 
-def oracle_frame(g, cam, tile_fraction: float = 1.0, seed: int = 0):
-    """The oracle as it stands (single-threaded C++), one view: projection, binning, then
-    compositing forward and backward over a fraction of the tiles, projection backward.
-    Returns (seconds scaled to a full frame, entries, composited/examined ratio, detail)."""
+def oracle_frame(g, cam):
+    """The oracle as it stands (single-threaded C++, float64), one full view: projection,
+    binning, compositing forward and backward over every tile, projection backward.
+    Returns (seconds, entries, composited/examined ratio, per-stage seconds)."""
     import numpy as np
 
     import oracle
@@ -718,76 +1010,63 @@ def oracle_frame(g, cam, tile_fraction: float = 1.0, seed: int = 0):
     t1 = time.perf_counter()
     B = oracle.bin(cam, P["means2d"].astype(np.float32), P["depth"].astype(np.float32), P["radius"])
     t2 = time.perf_counter()
-    tm = None
-    sample_entries = B["n_entries"]
-    if tile_fraction < 1.0:
-        rng = np.random.default_rng(seed)
-        tm = np.zeros(cam.n_tiles, np.uint8)
-        tm[rng.choice(cam.n_tiles, max(1, int(tile_fraction * cam.n_tiles)), replace=False)] = 1
-        r = B["ranges"].astype(np.int64)
-        sample_entries = int((r[:, 1] - r[:, 0])[tm.astype(bool)].sum())
-    F = oracle.raster_fwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"],
-                          B["point_list"], tile_mask=tm)
+    F = oracle.raster_fwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"], B["point_list"])
     t3 = time.perf_counter()
     O = oracle.raster_bwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"],
-                          B["point_list"], F["n_contrib"], scenes.image_grad(cam), tile_mask=tm)
+                          B["point_list"], F["n_contrib"], scenes.image_grad(cam))
     t4 = time.perf_counter()
     oracle.project_bwd(cam, g, P["radius"], O["dmeans2d"], O["dconic"], O["dcolor"])
     t5 = time.perf_counter()
-    scale = B["n_entries"] / max(sample_entries, 1)
-    frame_s = (t1 - t0) + (t2 - t1) + (t3 - t2 + t4 - t3) * scale + (t5 - t4)
     ratio = float(F["n_blend"].sum()) / max(float(F["n_contrib"].sum()), 1.0)
-    return frame_s, B["n_entries"], ratio, dict(project=t1 - t0, bin=t2 - t1, rasterize_fwd=t3 - t2,
-                                                rasterize_bwd=t4 - t3, project_bwd=t5 - t4,
-                                                sampled_entries=sample_entries)
-
-
-def cpu_baseline(g, cam):
-    frame_s, E, ratio, d = oracle_frame(g, cam, 1.0)
-    return dict(value=E / frame_s, unit=UNIT, cores=1, kind="oracle",
-                sample="one full 1920x1080 view (all tiles) of the 160k scene: projection, binning, "
-                       "compositing forward and backward, projection backward, single thread, float64",
-                ms_per_frame=frame_s * 1e3, blend_ratio=ratio,
-                stage_s={k: v for k, v in d.items() if k != "sampled_entries"},
-                host_cpus=os.cpu_count())
+    return t5 - t0, B["n_entries"], ratio, dict(project=t1 - t0, bin=t2 - t1, rasterize_fwd=t3 - t2,
+                                                rasterize_bwd=t4 - t3, project_bwd=t5 - t4)
 
 
 def run_reference(args):
-    """The oracle as the reference arm: every step is one view at a bounded sample (a quarter of
-    the tiles for the compositing passes, the whole view for projection and binning)."""
+    """The oracle as the reference arm, on the headline's workload: every step is one full view
+    of the orbit (projection, binning, compositing forward and backward over every tile,
+    projection backward), single-threaded and pinned to one core; W untimed steps, then K timed
+    steps, each timed in full (no sampling, no scaling)."""
     rank, world, _ = dist_env()
     if world > 1 and rank != 0:
         return
     from gaussian_splatting_tile_gb300 import scenes
+    core = pin_to_one_core()
     g = scenes.procedural_scene(seed=0)
     cams = scenes.orbit_cameras(WIDTH, HEIGHT, VIEWS)
     for v in assign_views(0, 1, args.warmup):
-        oracle_frame(g, cams[v], 0.25, seed=v)
+        oracle_frame(g, cams[v])
     tot_s, tot_e = 0.0, 0
+    stage = {}
     t0 = time.perf_counter()
     for v in assign_views(0, 1, args.steps, offset=args.warmup):
-        s, E, _, _ = oracle_frame(g, cams[v], 0.25, seed=v)
-        tot_s += s
+        s_, E, _, d = oracle_frame(g, cams[v])
+        tot_s += s_
         tot_e += E
+        for k, x in d.items():
+            stage[k] = stage.get(k, 0.0) + x
     wall = time.perf_counter() - t0
     value = tot_e / tot_s
     res = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
                warmup=args.warmup, ms_per_step=tot_s / args.steps * 1e3, higher_is_better=True,
                scaling="weak", vs_baseline=value / T4_ENTRIES_PER_S, dtype="f64",
                data="synthetic (seeded procedural scene; no dataset)", impl="reference",
-               config=dict(workload="160k Gaussians, SH degree 3, 1920x1080, 60-view orbit; fwd+bwd per view",
-                           n_gaussians=g.n, width=WIDTH, height=HEIGHT, views=VIEWS),
+               config=workload_config(),
                cpu_baseline=dict(value=value, unit=UNIT, cores=1, kind="oracle",
-                                 sample="per step one view: projection and binning in full, compositing "
-                                        "forward/backward on 25% of the tiles scaled by entries"),
+                                 sample="every step one full view of the orbit, all tiles: projection, "
+                                        "binning, compositing forward and backward, projection backward",
+                                 cpu_model=cpu_model(), pinned_core=core),
                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0),
-               wall_s=wall)
+               stage_s_per_step={k: x / args.steps for k, x in stage.items()},
+               wall_s_timed=wall)
     print(json.dumps(res), flush=True)
 
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.oracle_worker:
+        oracle_worker(args.oracle_worker.split(","))
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -41,7 +41,7 @@ def _stale(target, deps):
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    headers.append(os.path.join(INCLUDE, "rs.h"))
+    headers += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     flags = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
              *ARCH, *extra_flags]
     objs, jobs = [], []

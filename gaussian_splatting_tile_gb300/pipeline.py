@@ -60,6 +60,7 @@ class Renderer:
         self.grads = None
 
     def _alloc(self, capacity: int):
+        self._fwd_valid = False  # new entry buffers: a forward must run before any backward
         self.capacity = int(capacity)
         ws = rs.rs_bin_workspace_size(self.n, self.camera, self.capacity)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
@@ -149,6 +150,7 @@ class Renderer:
     def rasterize(self, bg=(0.0, 0.0, 0.0), stream=None):
         self.bg = tuple(bg)
         self._prepare(self._g, self.bg)["fwd"].run(rs.stream_handle(stream))
+        self._fwd_valid = True
 
     def forward(self, g: rs.DeviceGaussians, bg=(0.0, 0.0, 0.0), stream=None) -> Forward:
         self.bg = tuple(bg)
@@ -197,6 +199,8 @@ class Renderer:
         if not (dL_dimage.is_cuda and dL_dimage.dtype == torch.float32 and dL_dimage.is_contiguous()
                 and dL_dimage.numel() >= 3 * self.camera.width * self.camera.height):
             raise ValueError("dL_dimage must be a contiguous float32 CUDA tensor [3, H, W]")
+        if not self._fwd_valid:
+            raise RuntimeError("the entry buffers changed since the last forward: run the forward again")
         calls = self._prepare(self._g, self.bg)
         fn = rs.PreparedCall("rs_rasterize_bwd", calls["rbwd_args"] + (ctypes.c_void_p(dL_dimage.data_ptr()),)
                              + calls["rbwd_out"])

@@ -8,6 +8,7 @@ GPU is unavailable, the calls raise.
 from __future__ import annotations
 
 import ctypes
+import glob
 import dataclasses
 import os
 import re
@@ -83,14 +84,15 @@ _lib = None
 _VP = ctypes.c_void_p
 
 
-def declared_signatures(header: str = HEADER):
-    """(return type, name) of the entry points include/rs.h declares."""
-    text = open(header).read()
+def declared_signatures(header: str | None = None):
+    """(return type, name) of the entry points the headers under include/ declare (or `header`)."""
+    headers = [header] if header else sorted(glob.glob(os.path.join(os.path.dirname(HEADER), "*.h")))
+    text = "".join(open(h).read() for h in headers)
     return sorted(set(re.findall(r"^\s*(int|const char\*|size_t)\s+(rs_\w+)\s*\(", text, re.M)))
 
 
-def declared_symbols(header: str = HEADER):
-    """Names of the entry points include/rs.h declares."""
+def declared_symbols(header: str | None = None):
+    """Names of the entry points the headers under include/ declare (or `header`)."""
     return sorted({name for _, name in declared_signatures(header)})
 
 

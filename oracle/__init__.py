@@ -237,10 +237,13 @@ def raster_fwd(cam, means2d, conic, opacity, color, ranges, point_list, bg=(0.0,
 
 def raster_bwd(cam, means2d, conic, opacity, color, ranges, point_list, n_contrib, dL_dimage,
                bg=(0.0, 0.0, 0.0), tile_mask=None):
-    """c4 in double.  Returns dmeans2d [2,N], dconic [3,N], dopacity [N], dcolor [3,N]."""
+    """c4 in double.  Returns dmeans2d [2,N], dconic [3,N], dopacity [N], dcolor [3,N], and
+    `abs_<name>` of the same shapes: per output, the sum of the magnitudes of the terms it adds up
+    (the scale of a float computation's rounding error in that sum)."""
     n = int(np.asarray(opacity).shape[0])
     out = dict(dmeans2d=np.zeros((2, n)), dconic=np.zeros((3, n)), dopacity=np.zeros(n),
                dcolor=np.zeros((3, n)))
+    absum = np.zeros((9, n))
     c = _cam(cam)
     a = [_d(means2d), _d(conic), _d(opacity), _d(color)]
     rg = np.ascontiguousarray(ranges, np.uint32)
@@ -254,9 +257,10 @@ def raster_bwd(cam, means2d, conic, opacity, color, ranges, point_list, n_contri
     rc = lib().orc_raster_bwd(ctypes.byref(c), ctypes.c_int32(n), _p(a[0]), _p(a[1]), _p(a[2]),
                               _p(a[3]), _p(rg), _p(pl), _p(b), _p(nc), _p(gi), _p(tm),
                               _p(out["dmeans2d"]), _p(out["dconic"]), _p(out["dopacity"]),
-                              _p(out["dcolor"]))
+                              _p(out["dcolor"]), _p(absum))
     if rc != 0:
         raise ValueError(f"orc_raster_bwd returned {rc}")
+    out.update(abs_dmeans2d=absum[0:2], abs_dconic=absum[2:5], abs_dopacity=absum[5], abs_dcolor=absum[6:9])
     return out
 
 

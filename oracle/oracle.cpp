@@ -436,7 +436,7 @@ int raster_bwd(const orc_camera* cam, int32_t n, const double* means2d, const do
                const double* opacity, const double* color, const uint32_t* ranges,
                const uint32_t* list, const double* bg, const uint32_t* n_contrib,
                const double* dL_dimage, const uint8_t* tile_mask, double* dmeans2d,
-               double* dconic, double* dopacity, double* dcolor) {
+               double* dconic, double* dopacity, double* dcolor, double* absum) {
     const int W = cam->width, H = cam->height;
     const int TX = (W + TILE - 1) / TILE, TY = (H + TILE - 1) / TILE;
     const size_t HW = size_t(W) * size_t(H);
@@ -475,11 +475,13 @@ int raster_bwd(const orc_camera* cam, int32_t n, const double* means2d, const do
                     for (size_t k = seq.size(); k-- > 0;) {
                         const Reached& r = seq[k];
                         const uint32_t g = r.g;
-                        double dalpha = 0;
+                        double dalpha = 0, dalpha_mag = 0;
                         for (int ch = 0; ch < 3; ++ch) {
                             const double c = color[size_t(ch) * n + g];
                             dcolor[size_t(ch) * n + g] += r.alpha * r.T * dLdC[ch];
                             dalpha += dLdC[ch] * (c * r.T - S[ch] / (1.0 - r.alpha));
+                            dalpha_mag += std::fabs(dLdC[ch]) * (std::fabs(c * r.T) + std::fabs(S[ch] / (1.0 - r.alpha)));
+                            if (absum) absum[(6 + size_t(ch)) * n + g] += std::fabs(r.alpha * r.T * dLdC[ch]);
                         }
                         for (int ch = 0; ch < 3; ++ch) S[ch] += color[size_t(ch) * n + g] * r.alpha * r.T;
                         if (r.raw > 0.99) continue;  // clamped: alpha is the constant 0.99
@@ -493,6 +495,17 @@ int raster_bwd(const orc_camera* cam, int32_t n, const double* means2d, const do
                         // dpower/du = -dpower/d(dx) = A dx + B dy
                         dmeans2d[g] += gp * (A * r.dx + B * r.dy);
                         dmeans2d[size_t(n) + g] += gp * (Cc * r.dy + B * r.dx);
+                        if (absum) {
+                            // magnitudes of what the sums above add (with dL/dalpha's own terms
+                            // taken in absolute value): the scale of their rounding error
+                            const double gm = opacity[g] * r.G * dalpha_mag;
+                            absum[2 * size_t(n) + g] += 0.5 * r.dx * r.dx * gm;
+                            absum[3 * size_t(n) + g] += std::fabs(r.dx * r.dy) * gm;
+                            absum[4 * size_t(n) + g] += 0.5 * r.dy * r.dy * gm;
+                            absum[g] += gm * (std::fabs(A * r.dx) + std::fabs(B * r.dy));
+                            absum[size_t(n) + g] += gm * (std::fabs(Cc * r.dy) + std::fabs(B * r.dx));
+                            absum[5 * size_t(n) + g] += r.G * dalpha_mag;
+                        }
                     }
                 }
         }
@@ -822,10 +835,10 @@ int orc_raster_bwd(const orc_camera* cam, int32_t n, const double* means2d,
                    const uint32_t* ranges, const uint32_t* point_list, const double* bg,
                    const uint32_t* n_contrib, const double* dL_dimage,
                    const uint8_t* tile_mask, double* dmeans2d, double* dconic,
-                   double* dopacity, double* dcolor) {
+                   double* dopacity, double* dcolor, double* absum) {
     if (!cam || n < 0) return -1;
     return raster_bwd(cam, n, means2d, conic, opacity, color, ranges, point_list, bg, n_contrib,
-                      dL_dimage, tile_mask, dmeans2d, dconic, dopacity, dcolor);
+                      dL_dimage, tile_mask, dmeans2d, dconic, dopacity, dcolor, absum);
 }
 
 int orc_project_bwd(const orc_camera* cam_in, int32_t n, const double* means,

@@ -91,13 +91,16 @@ int orc_raster_fwd(int prec, const orc_camera* cam, int32_t n, const double* mea
                    uint32_t* n_contrib, double margin, uint8_t* ambig, uint32_t* n_blend);
 
 /* c4: backward of the compositing, in double.  Walk length per pixel is n_contrib (as given).
- * Gradients are accumulated into zero-initialised outputs by this call. */
+ * Gradients are accumulated into zero-initialised outputs by this call.  absum (may be NULL;
+ * zero-initialised, [9][n]: rows dmeans2d 0-1, dconic 2-4, dopacity 5, dcolor 6-8) receives for
+ * every output the sum of the magnitudes of the terms it adds up, with dL/dalpha's own terms in
+ * absolute value: the scale of the rounding error of any float computation of these sums. */
 int orc_raster_bwd(const orc_camera* cam, int32_t n, const double* means2d,
                    const double* conic, const double* opacity, const double* color,
                    const uint32_t* ranges, const uint32_t* point_list, const double* bg,
                    const uint32_t* n_contrib, const double* dL_dimage,
                    const uint8_t* tile_mask, double* dmeans2d, double* dconic,
-                   double* dopacity, double* dcolor);
+                   double* dopacity, double* dcolor, double* absum);
 
 /* c5: backward of the projection and colour, in double.  Culled Gaussians (radius 0) get zero
  * gradients.  dsh may be NULL when sh_degree < 0 (then dcolor is the colours' gradient). */

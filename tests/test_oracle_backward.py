@@ -5,6 +5,7 @@ quaternion-gradient invariant dq . q = 0, and the off-axis clamp branch.  CPU on
 import numpy as np
 import pytest
 
+import oracle
 from gaussian_splatting_tile_gb300 import scenes
 
 
@@ -219,3 +220,24 @@ def test_appearance_mlp(orc):
             Lm = Lf()
             flat[idx] = old
             assert (Lp - Lm) / (2 * h) == pytest.approx(an[name].reshape(-1)[idx], rel=1e-6, abs=1e-8)
+
+
+def test_magnitude_sums_bound_the_gradients():
+    """The compositing backward's magnitude sums (the rounding scale of the gradient sums) are at
+    least the gradients' magnitudes (triangle inequality) and vanish where nothing was added."""
+    g, cam = scenes.tiny_scene(seed=3, n=300)
+    P = oracle.project(cam, g)
+    B = oracle.bin(cam, P["means2d"].astype(np.float32), P["depth"].astype(np.float32), P["radius"])
+    F = oracle.raster_fwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"], B["point_list"])
+    O = oracle.raster_bwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"], B["point_list"],
+                          F["n_contrib"], scenes.image_grad(cam))
+    for k in ("dmeans2d", "dconic", "dopacity", "dcolor"):
+        assert (O["abs_" + k] >= np.abs(O[k]) * (1 - 1e-12)).all(), k
+        assert (O["abs_" + k] > 0).any()
+    absent = np.ones(g.n, bool)
+    absent[B["point_list"]] = False  # in no tile's list: nothing is added for them
+    absent[:5] = True
+    P["means2d"][:, :5] = -1e4  # five Gaussians moved far off the image keep their list entries
+    O2 = oracle.raster_bwd(cam, P["means2d"], P["conic"], g.opacity, P["color"], B["ranges"], B["point_list"],
+                           F["n_contrib"], scenes.image_grad(cam))
+    assert not O2["abs_dconic"][:, absent].any() and not O2["abs_dcolor"][:, absent].any()
