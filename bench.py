@@ -635,6 +635,7 @@ def run_ours(args):
         result["ellipse_tile_test"] = run_ellipse(g, cams, device)
     if world == 1 and not args.no_adam:
         result["adam"] = run_adam(g, device)
+        result["densify"] = run_densify(g, device)
         result["l1_dssim"] = run_l1_dssim(device)
 
     oracle_t = finish_oracle_worker(worker) if worker is not None else None
@@ -753,13 +754,52 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
         step.R.check_async(results[k])  # raises if a view overflowed the capacity or timed out
     st = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(5)] for e in times])
     per_view = st.mean(axis=0)
+    del step
+
+    # the step as a whole: its views in flight, each view one CUDA graph (MLP colours, render, L1
+    # loss, render backward, MLP backward) replayed on a stream of its own with buffers of its own
+    # (every view writes its own gradients); CUDA events on the main stream around each step, which
+    # every view's stream joins; L2 written over before every step (not timed)
+    V = len(cams)
+    per = [pipeline.AppearanceStep(cams[0], dg, mlp, lat, device, capacity=4_000_000) for _ in range(V)]
+    graphs = [pipeline.AppearanceGraph(per[v], cams[v], targets[v], scale) for v in range(V)]
+    sides = [torch.cuda.Stream(device) for _ in range(V)]
+
+    def step_in_flight():
+        for side, gr in zip(sides, graphs):
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                gr.replay()
+        for side in sides:
+            stream.wait_stream(side)
+
+    for _ in range(warmup):
+        step_in_flight()
+    torch.cuda.synchronize(device)
+    sev = []
+    for k in range(steps):
+        flush.fill_(float(k))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step_in_flight()
+        b.record(stream)
+        sev.append((a, b))
+    torch.cuda.synchronize(device)
+    for gr in graphs:
+        gr.check()  # raises if a view overflowed the capacity or timed out
+    inflight_ms = float(np.mean([a.elapsed_time(b) for a, b in sev]))
+    del graphs, per
+
     hbm, src = measured_peaks()
     n = g.n
     mlp_fwd_s = per_view[0] * 1e-3
     mlp_bwd_s = per_view[4] * 1e-3
     return dict(workload=("250k Gaussians (sphere/helix/plane), 8 views of 400x400 per step, MLP 11->64->3 "
                           "(split-TF32 tensor cores), L1 loss; targets are renders with the procedural colours"),
-                ms_per_step=float(st.sum(axis=1).mean() * len(cams)),
+                ms_per_step=inflight_ms,
+                ms_per_step_how=("the step's 8 views in flight, each one CUDA graph on its own stream with its "
+                                 "own buffers; CUDA events around each step"),
+                ms_per_step_call_by_call=float(st.sum(axis=1).mean() * len(cams)),
                 stage_ms_per_view=dict(zip(names, [float(x) for x in per_view])),
                 steps=steps, views_per_step=len(cams),
                 mlp_roofline=dict(bound="hbm", unit="GB/s", peak=hbm, peak_source=src,
@@ -861,6 +901,65 @@ def run_adam(g, device, steps: int = 20, warmup: int = 3):
     return dict(workload=f"{n} Gaussians x 59 parameters in 6 groups (exp and sigmoid activations fused)",
                 ms_per_step=ms, elements=elems, bytes_per_step=nbytes,
                 roofline=dict(bound="hbm", unit="GB/s", achieved=gbs, peak=hbm, frac=gbs / hbm, peak_source=src))
+
+
+def run_densify(g, device, steps: int = 10, warmup: int = 2):
+    """Densification of the 160k scene (clone / split / prune over its 59 parameter rows, each with
+    two Adam moments): rs_densify_plan (classification, scan, the count read back) then
+    rs_densify_apply, CUDA events, L2 written over before every call.  About 6% of the Gaussians
+    grow (half cloned, half split) and 2% are pruned.  HBM roofline: the plan reads 24 B and writes
+    1 B per Gaussian; the apply reads 708 B per Gaussian (59 rows x param, m, v) and writes 708 B
+    per output Gaussian."""
+    import numpy as np
+    import torch
+
+    from gaussian_splatting_tile_gb300 import rs
+
+    n = g.n
+    rng = np.random.default_rng(0)
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+    accum = f(np.where(rng.random(n) < 0.06, 1e-3, 1e-5))
+    count = f(np.ones(n))
+    log_scales = f(np.log(g.scales) + np.where(rng.random((1, n)) < 0.5, 2.5, 0.0))
+    logits = f(np.where(rng.random(n) < 0.02, -8.0, 2.0))
+    quats, means = f(g.quats), f(g.means)
+    sh = f(g.sh)
+    noise = f(rng.standard_normal((2, 3, n)))
+    ws = torch.empty(rs.rs_densify_workspace_size(n), dtype=torch.uint8, device=device)
+    rule = dict(grad_threshold=2e-4, dense_scale=0.05, min_opacity=0.005, max_scale=0.0)
+    counts = rs.rs_densify_plan(accum, count, log_scales, logits, workspace=ws, **rule)
+    n_out = counts["n_out"]
+    groups = []
+    for p, kind in ((means, rs.RS_DENSIFY_MEANS), (log_scales, rs.RS_DENSIFY_LOG_SCALES), (quats, 0),
+                    (logits[None], 0), (sh, 0)):
+        rows = p.numel() // n
+        z = lambda r: torch.zeros(r, n, device=device)
+        o = lambda r: torch.empty(r, n_out, device=device)
+        groups.append(rs.DensifyGroup(p.contiguous(), o(rows), z(rows), z(rows), o(rows), o(rows), kind))
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    t_plan, t_apply = [], []
+    for k in range(warmup + steps):
+        flush.fill_(float(k))
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        c = rs.rs_densify_plan(accum, count, log_scales, logits, workspace=ws, **rule)
+        e[1].record(stream)
+        rs.rs_densify_apply(n, ws, quats, log_scales, noise, groups, c["n_out"])
+        e[2].record(stream)
+        torch.cuda.synchronize(device)
+        if k >= warmup:
+            t_plan.append(e[0].elapsed_time(e[1]))
+            t_apply.append(e[1].elapsed_time(e[2]))
+    hbm, src = measured_peaks()
+    ms_plan, ms_apply = float(np.median(t_plan)), float(np.median(t_apply))
+    b_apply = 708 * n + 708 * n_out + n
+    gbs = b_apply / (ms_apply * 1e-3) / 1e9
+    return dict(workload=f"{n} Gaussians, 59 parameter rows with Adam moments; 6% grow, 2% pruned",
+                counts=counts, ms_plan=ms_plan, ms_apply=ms_apply,
+                note="the plan includes its one device-to-host read of the counts",
+                roofline=dict(kernel="k_densify_apply", bound="hbm", unit="GB/s", achieved=gbs, peak=hbm,
+                              frac=gbs / hbm, peak_source=src, bytes=b_apply))
 
 
 def run_l1_dssim(device, steps: int = 20, warmup: int = 3):

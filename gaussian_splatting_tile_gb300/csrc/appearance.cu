@@ -9,27 +9,19 @@
 // Gaussians x HID per CTA, the accumulator in tensor memory) and the thin second layer (three
 // outputs) in float32 on the CUDA cores while reading the accumulator back.
 //
-// The backward takes 16 Gaussians per warp and runs its products as mma.sync m16n8k8 TF32: it
-// recomputes both layers (the first layer's accumulator fragment is the second layer's A
-// operand without any data movement: in k-chunk kc of the second product, fragment columns t
-// and t + 4 stand for hidden units kc*8 + 2t and kc*8 + 2t + 1, which are the two accumulator
-// columns lane (g, t) already holds), forms dL/dz2 and dL/dz1 in registers, gets dL/dx with a
-// third product (same renumbering), and accumulates the weight gradients from per-warp
-// shared-memory copies of dL/dz1, h and x, each lane owning whole hidden units; a block adds its
-// warps' sums in shared memory and flushes them with one global atomic per weight per block (the
-// reduction pattern the page describes for its MLP backward).  View directions are constants:
-// no gradient reaches the means.
+// The backward runs on the tensor cores too (tcgen05.mma into tensor memory): per 128-Gaussian
+// tile it recomputes the first layer, forms dL/dz2, dL/dz1 and dL/dlatent in float32 on the CUDA
+// cores (two threads per Gaussian, one per half of the hidden units), and gets every weight
+// gradient from one product per tile, [dZ1 | H]^T [X | dZ2 | 1], accumulated in tensor memory over
+// all of a CTA's tiles and flushed with one global atomic per weight per CTA (the reduction
+// pattern the page describes for its MLP backward).  View directions are constants: no gradient
+// reaches the means.
 #include "rs_internal.cuh"
 
 namespace rs {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kMlpWarps = 4;
-constexpr int kMlpThreads = kMlpWarps * 32;
-constexpr int kRows = 16;              // Gaussians per warp tile (the mma M dimension)
-constexpr int kInMax = 32;             // padded input width: latent_dim + 3 <= 32
-constexpr int kXStride = kInMax + 4;   // row stride of x and W1 copies: conflict-free fragments
 
 __device__ __forceinline__ uint32_t tf32_of(float x) {
     uint32_t r;
@@ -43,22 +35,6 @@ __device__ __forceinline__ void split(float x, uint32_t& hi, uint32_t& lo) {
     lo = tf32_of(x - __uint_as_float(hi));
 }
 
-__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// d += a.b in split TF32 (three products)
-__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
-                                     uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
-    mma8(d, ah, bh0, bh1);
-    mma8(d, ah, bl0, bl1);
-    mma8(d, al, bh0, bh1);
-}
-
 struct MlpArgs {
     CameraF cam;
     int n, L, D;                       // Gaussians, latent width, input width L + 3
@@ -69,126 +45,6 @@ struct MlpArgs {
     const float* W2;
     const float* b2;
 };
-
-// Weights in shared memory: W1 [HID][kXStride] (columns past D zero) and W2 [3][HID + 8] as TF32
-// heads and tails, W2 in float32 for the backward's dL/dh, and the biases.
-template <int HID>
-struct WeightSmem {
-    uint32_t w1h[HID * kXStride], w1l[HID * kXStride];
-    uint32_t w2h[3 * (HID + 8)], w2l[3 * (HID + 8)];
-    float w2f[3 * HID];
-    float b1[HID];
-    float b2[4];
-};
-
-template <int HID>
-__device__ void load_weights(const MlpArgs& a, WeightSmem<HID>& w) {
-    for (int i = threadIdx.x; i < HID * kInMax; i += blockDim.x) {
-        const int h = i / kInMax, k = i % kInMax;
-        const float v = k < a.D ? a.W1[h * a.D + k] : 0.f;
-        split(v, w.w1h[h * kXStride + k], w.w1l[h * kXStride + k]);
-    }
-    for (int i = threadIdx.x; i < 3 * HID; i += blockDim.x) {
-        const int c = i / HID, h = i % HID;
-        const float v = a.W2[i];
-        split(v, w.w2h[c * (HID + 8) + h], w.w2l[c * (HID + 8) + h]);
-        w.w2f[i] = v;
-    }
-    for (int i = threadIdx.x; i < HID; i += blockDim.x) w.b1[i] = a.b1[i];
-    if (threadIdx.x < 3) w.b2[threadIdx.x] = a.b2[threadIdx.x];
-}
-
-// x of Gaussians i0 .. i0 + 15 into s_x [16][kXStride]; rows past n and columns past D are zero.
-// The loads of a row are independent and unrolled (L < KS*8 - 2), so they are all in flight at
-// once.
-template <int KS>
-__device__ __forceinline__ void stage_x(const MlpArgs& a, int i0, float* s_x) {
-    const int lane = threadIdx.x & 31;
-    if (lane < kRows) {
-        const int i = i0 + lane;
-        float* row = s_x + lane * kXStride;
-        float v[KS * 8];
-        const bool in = i < a.n;
-#pragma unroll
-        for (int k = 0; k < KS * 8 - 3; ++k) v[k] = in && k < a.L ? a.latents[size_t(k) * a.n + i] : 0.f;
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-        if (in) {
-            const CameraF& cam = a.cam;
-            // camera centre C = -R^T t
-            const float C0 = -(cam.R[0] * cam.t[0] + cam.R[3] * cam.t[1] + cam.R[6] * cam.t[2]);
-            const float C1 = -(cam.R[1] * cam.t[0] + cam.R[4] * cam.t[1] + cam.R[7] * cam.t[2]);
-            const float C2 = -(cam.R[2] * cam.t[0] + cam.R[5] * cam.t[1] + cam.R[8] * cam.t[2]);
-            d0 = a.means[i] - C0;
-            d1 = a.means[size_t(a.n) + i] - C1;
-            d2 = a.means[2 * size_t(a.n) + i] - C2;
-            const float len = sqrtf(d0 * d0 + d1 * d1 + d2 * d2);
-            const float il = len > 0.f ? 1.0f / len : 0.f;
-            d0 *= il;
-            d1 *= il;
-            d2 *= il;
-        }
-#pragma unroll
-        for (int k = KS * 8 - 3; k < KS * 8; ++k) v[k] = 0.f;
-#pragma unroll
-        for (int k = 0; k < KS * 8; ++k) {
-            // the view direction sits right after the latents
-            const float dir = k == a.L ? d0 : k == a.L + 1 ? d1 : k == a.L + 2 ? d2 : 0.f;
-            row[k] = k < a.L ? v[k] : dir;
-        }
-    }
-    __syncwarp();
-}
-
-// First layer: acc[nt] = W1 x + b1 for hidden units nt*8 + (2t, 2t + 1) of rows g, g + 8,
-// then relu (h > 0 exactly where z > 0).
-template <int HID, int KS>
-__device__ __forceinline__ void layer1(const WeightSmem<HID>& w, const float* s_x, float (&acc)[HID / 8][4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < HID / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-        uint32_t ah[4], al[4];
-        split(s_x[g * kXStride + ks * 8 + t], ah[0], al[0]);
-        split(s_x[(g + 8) * kXStride + ks * 8 + t], ah[1], al[1]);
-        split(s_x[g * kXStride + ks * 8 + t + 4], ah[2], al[2]);
-        split(s_x[(g + 8) * kXStride + ks * 8 + t + 4], ah[3], al[3]);
-#pragma unroll
-        for (int nt = 0; nt < HID / 8; ++nt) {
-            const int o = (nt * 8 + g) * kXStride + ks * 8 + t;
-            mma3(acc[nt], ah, al, w.w1h[o], w.w1h[o + 4], w.w1l[o], w.w1l[o + 4]);
-        }
-    }
-#pragma unroll
-    for (int nt = 0; nt < HID / 8; ++nt) {
-        const float c0 = w.b1[nt * 8 + 2 * t], c1 = w.b1[nt * 8 + 2 * t + 1];
-        acc[nt][0] = fmaxf(acc[nt][0] + c0, 0.f);
-        acc[nt][1] = fmaxf(acc[nt][1] + c1, 0.f);
-        acc[nt][2] = fmaxf(acc[nt][2] + c0, 0.f);
-        acc[nt][3] = fmaxf(acc[nt][3] + c1, 0.f);
-    }
-}
-
-// Second layer without bias: out = (rows g, g + 8) x (columns 2t, 2t + 1) of W2 h; columns 0..2
-// are the colour channels.
-template <int HID>
-__device__ __forceinline__ void layer2(const WeightSmem<HID>& w, const float (&h)[HID / 8][4], float (&out)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    out[0] = out[1] = out[2] = out[3] = 0.f;
-    const int gc = g < 3 ? g : 0;
-#pragma unroll
-    for (int kc = 0; kc < HID / 8; ++kc) {
-        uint32_t ah[4], al[4];
-        split(h[kc][0], ah[0], al[0]);
-        split(h[kc][2], ah[1], al[1]);
-        split(h[kc][1], ah[2], al[2]);
-        split(h[kc][3], ah[3], al[3]);
-        const int o = gc * (HID + 8) + kc * 8 + 2 * t;
-        const uint32_t bh0 = g < 3 ? w.w2h[o] : 0u, bh1 = g < 3 ? w.w2h[o + 1] : 0u;
-        const uint32_t bl0 = g < 3 ? w.w2l[o] : 0u, bl1 = g < 3 ? w.w2l[o + 1] : 0u;
-        mma3(out, ah, al, bh0, bh1, bl0, bl1);
-    }
-}
 
 __device__ __forceinline__ float sigmoidf(float z) { return 1.0f / (1.0f + expf(-z)); }
 
@@ -440,180 +296,512 @@ __global__ void __launch_bounds__(kTcRows) k_mlp_fwd_tc(MlpArgs a, float* __rest
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(HID) : "memory");
 }
 
-// Per-warp staging of the backward and the block's gradient sums.
-template <int HID>
-struct BwdWarpSmem {
-    float x[kRows * kXStride];
-    float dz1[kRows * (HID + 8)];
-    float h[kRows * (HID + 8)];
-    float dz2[kRows * 4];
-};
-template <int HID>
-struct BwdSums {
-    float dW1[HID * kInMax];
-    float db1[HID];
-    float dW2[3 * HID];
-    float db2[4];
-};
+// ---------------------------------------------------------------- backward on the tensor cores (tcgen05)
+// A CTA of 128 threads takes 128 Gaussians at a time (thread r = row r = TMEM lane r):
+//  1. Z1 = X W1^T on the tensor cores, as in the forward (tensor memory columns [0, HID)).
+//  2. Thread r reads its row of Z1 back and forms, in float32 on the CUDA cores,
+//     h = relu(z1 + b1), z2 = W2 h + b2, s = sigmoid(z2), dz2 = dL/dcolour s (1 - s),
+//     dz1 = (W2^T dz2) where z1 > 0, and dL/dlatent = W1^T dz1 (the latent columns of W1).
+//  3. The tile's weight gradients are one product on the tensor cores,
+//     G = [dZ1 | H]^T [X | dZ2 | 1] (M = 128: rows h of dZ1^T, then rows 64 + h of H^T; N = NW:
+//     the columns of X, then dz2 (3), then ones; K = the tile's 128 Gaussians), accumulated in
+//     tensor memory columns [HID, HID + NW) over all of the CTA's tiles.  Its blocks give
+//     dW1 = dZ1^T X, db1 = dZ1^T 1 and dW2^T = H^T dZ2; the others are not used.
+//  4. At the end every weight's CTA sum goes to global memory with one atomic (the reduction the
+//     page describes for its MLP backward, per CTA), and db2 with a block reduction.
+// Both operands of the product are the transposes of what the threads hold (row r of the tile),
+// stored K-major without swizzle: thread r writes column r.  In the core-matrix layout the bank
+// of element (m, r) is (m mod 8) * 4 + (r mod 4), so a warp writing one row m for its 32 Gaussians
+// would hit 4 banks; instead lane L writes, at step j, row 8 g + ((L / 4 + j) mod 8) of each group
+// g of eight rows -- 32 distinct banks -- after rotating its eight values of the group by L / 4.
+template <int KS>
+constexpr int tc_bwd_nw() { return ((8 * KS + 4 + 15) / 16) * 16; }
 
 template <int HID, int KS>
-__global__ void __launch_bounds__(kMlpThreads) k_mlp_bwd(MlpArgs a, const float* __restrict__ dcolors,
-                                                        float* __restrict__ dlatents, float* __restrict__ dW1,
-                                                        float* __restrict__ db1, float* __restrict__ dW2,
-                                                        float* __restrict__ db2) {
-    RS_PDL_ENTER();
-    constexpr int HS = HID + 8;   // row stride of dz1 and h copies
-    constexpr int Q = HID / 32;   // hidden units owned per lane: lane + 32 q
-    extern __shared__ __align__(16) unsigned char smem[];
-    WeightSmem<HID>& w = *reinterpret_cast<WeightSmem<HID>*>(smem);
-    BwdSums<HID>& sums = *reinterpret_cast<BwdSums<HID>*>(smem + sizeof(WeightSmem<HID>));
-    BwdWarpSmem<HID>& st = reinterpret_cast<BwdWarpSmem<HID>*>(
-        smem + sizeof(WeightSmem<HID>) + sizeof(BwdSums<HID>))[threadIdx.x >> 5];
-    load_weights<HID>(a, w);
-    for (int i = threadIdx.x; i < int(sizeof(BwdSums<HID>) / 4); i += blockDim.x)
-        reinterpret_cast<float*>(&sums)[i] = 0.f;
-    __syncthreads();
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    float gw1[Q][KS * 8], gb1[Q], gw2[Q][3], gb2 = 0.f;
+struct TcBwdSmem {
+    static constexpr int NW = tc_bwd_nw<KS>();
+    static constexpr int kCore = 128;
+    static constexpr int kXCores = (kTcRows / 8) * 2 * KS;   // X [128 x 8 KS]
+    static constexpr int kWCores = (HID / 8) * 2 * KS;       // W1 [HID x 8 KS]
+    static constexpr int kGCores = (kTcRows / 8) * 32;       // [dZ1 | H]^T [128 x 128 Gaussians]
+    static constexpr int kRCores = (NW / 8) * 32;            // [X | dZ2 | 1]^T [NW x 128 Gaussians]
+    alignas(1024) uint8_t x_hi[kXCores * kCore], x_lo[kXCores * kCore];
+    alignas(128) uint8_t w_hi[kWCores * kCore], w_lo[kWCores * kCore];
+    alignas(128) uint8_t g_hi[kGCores * kCore], g_lo[kGCores * kCore];
+    alignas(128) uint8_t r_hi[kRCores * kCore], r_lo[kRCores * kCore];
+    // W1 in float32, row-major [HID][8 KS], for dL/dx where it fits (else W1 = head + tail)
+    static constexpr bool kW1f = KS <= 3;
+    alignas(16) float w1f[kW1f ? HID * 8 * KS : 4];
+    alignas(16) float w2[3][HID];
+    alignas(16) float b1[HID];
+    float b2[4];
+    float db2[4][4];
+    alignas(8) uint64_t mbar_z, mbar_g;
+    uint32_t tmem;
+};
+
+// Byte offset of element (row, k) of a K-major no-swizzle operand whose K extent is KC core
+// columns (4 elements each).
+template <int KC>
+__device__ __forceinline__ int tc_offset(int row, int k) {
+    return ((row >> 3) * KC + (k >> 2)) * 128 + (row & 7) * 16 + (k & 3) * 4;
+}
+
+// v rotated by s (0..7) positions: out[i] = v[(i + s) mod 8], in three select stages.
+__device__ __forceinline__ void rotate8(float (&v)[8], int s) {
+    float t[8];
+    if (s & 1) {
 #pragma unroll
-    for (int q = 0; q < Q; ++q) {
+        for (int i = 0; i < 8; ++i) t[i] = v[(i + 1) & 7];
 #pragma unroll
-        for (int j = 0; j < KS * 8; ++j) gw1[q][j] = 0.f;
-        gb1[q] = 0.f;
-        gw2[q][0] = gw2[q][1] = gw2[q][2] = 0.f;
+        for (int i = 0; i < 8; ++i) v[i] = t[i];
     }
-    const int tiles = (a.n + kRows - 1) / kRows;
-    for (int tile = blockIdx.x * kMlpWarps + (threadIdx.x >> 5); tile < tiles; tile += gridDim.x * kMlpWarps) {
-        const int i0 = tile * kRows;
-        // dL/dcolour of this lane's slots (lane t = 0: channels 0, 1; t = 1: channel 2; slots
-        // 0, 2 for rows g, g + 8), loaded first so that the loads overlap the products
-        float dc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (t < 2) {
+    if (s & 2) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int c = 2 * t + (k & 1), i = i0 + g + 8 * (k >> 1);
-                if (c < 3 && i < a.n) dc[k] = dcolors[size_t(c) * a.n + i];
+        for (int i = 0; i < 8; ++i) t[i] = v[(i + 2) & 7];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = t[i];
+    }
+    if (s & 4) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = v[(i + 4) & 7];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = t[i];
+    }
+}
+
+// tcgen05.ld 32x32b.x8 without the wait: the registers are valid only after tc_ld_wait.
+__device__ __forceinline__ void tc_ld8_async(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+// Waits for this thread's tensor-memory loads; the registers pass through an empty asm so that
+// no use of them is scheduled before the wait.
+__device__ __forceinline__ void tc_ld_wait(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <>
+__device__ __forceinline__ void tc_ld_rows<16>(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Split into a TF32 head (x with its low 13 mantissa bits cleared) and the exact remainder; the
+// tensor cores read a TF32 operand from the top 19 bits of its word, so the remainder's own low
+// bits are dropped there: the pair still carries x to about 2^-21.
+__device__ __forceinline__ void split_trunc(float x, uint32_t& hi, uint32_t& lo) {
+    hi = __float_as_uint(x) & 0xffffe000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+// Column k (this thread's Gaussian) of rows 8 grp .. 8 grp + 7 of a transposed operand with 32
+// core columns of K, as TF32 heads and tails (truncating split), written in the conflict-free
+// rotated order.
+__device__ __forceinline__ void store_col8_t(uint8_t* hi, uint8_t* lo, int grp, int k, float (&v)[8], int lane) {
+    const int s = lane >> 2;
+    rotate8(v, s);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t h, l;
+        split_trunc(v[j], h, l);
+        const int o = tc_offset<32>(8 * grp + ((s + j) & 7), k);
+        *reinterpret_cast<uint32_t*>(hi + o) = h;
+        *reinterpret_cast<uint32_t*>(lo + o) = l;
+    }
+}
+
+constexpr int kTcBwdThreads = 2 * kTcRows;  // two threads per Gaussian row: one per half of the hidden units
+
+// tcgen05.st 32x32b.x32: 32 consecutive tensor-memory columns of this warp's 32 lanes.
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+        "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+        "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+        "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+template <int HID, int KS>
+__global__ void __launch_bounds__(kTcBwdThreads) k_mlp_bwd_tc(MlpArgs a, const float* __restrict__ dcolors,
+                                                               float* __restrict__ dlatents, float* __restrict__ dW1,
+                                                               float* __restrict__ db1, float* __restrict__ dW2,
+                                                               float* __restrict__ db2) {
+    RS_PDL_ENTER();
+    using Smem = TcBwdSmem<HID, KS>;
+    constexpr int NW = Smem::NW;
+    constexpr int K = KS * 8;
+    constexpr int kOnes = K + 3;       // the column of ones in [X | dZ2 | 1]
+    constexpr int HH = HID / 2;        // hidden units per half
+    extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
+    const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(tc_smem_raw));
+    Smem& sm = *reinterpret_cast<Smem*>(tc_smem_raw + ((1024u - (raw & 1023u)) & 1023u));
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int r = t & (kTcRows - 1);   // this thread's row (Gaussian) of the tile = tensor-memory lane
+    const int half = t >> 7;           // which half of the hidden units: [half HH, half HH + HH)
+    // W1 (split, K-major, columns in X's order: the view direction, then the latents), W2, biases;
+    // the transposed weight-gradient operand starts at zero (rows past HID in either half are
+    // never written)
+    for (int e = t; e < HID * K; e += kTcBwdThreads) {
+        const int j = e / K, k = e % K;
+        const int src = k < 3 ? a.L + k : k - 3;
+        const float v = k < a.D ? a.W1[j * a.D + src] : 0.f;
+        uint32_t h, l;
+        split(v, h, l);
+        const int o = tc_offset<2 * KS>(j, k);
+        *reinterpret_cast<uint32_t*>(sm.w_hi + o) = h;
+        *reinterpret_cast<uint32_t*>(sm.w_lo + o) = l;
+        if constexpr (Smem::kW1f) sm.w1f[j * K + k] = v;
+    }
+    for (int e = t; e < int(sizeof(sm.g_hi) / 16); e += kTcBwdThreads) {
+        reinterpret_cast<uint4*>(sm.g_hi)[e] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sm.g_lo)[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int e = t; e < 3 * HID; e += kTcBwdThreads) sm.w2[e / HID][e % HID] = a.W2[e];
+    for (int e = t; e < HID; e += kTcBwdThreads) sm.b1[e] = a.b1[e];
+    if (t < 3) sm.b2[t] = a.b2[t];
+    const uint32_t mbar_z = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.mbar_z));
+    const uint32_t mbar_g = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.mbar_g));
+    if (t == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mbar_z) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mbar_g) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    // tensor memory: Z1 [0, HID), G [HID, HID + NW), the second half's partial dL/dx
+    // [HID + NW, HID + NW + 32)
+    constexpr uint32_t kTmemCols = 256;
+    constexpr uint32_t kDlCol = HID + NW;
+    static_assert(kDlCol + 32 <= kTmemCols, "tensor memory");
+    if (warp == 0) {
+        const uint32_t slot = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.tmem));
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(slot),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    const uint32_t tmem = sm.tmem;
+    const uint32_t trow = tmem + (uint32_t((warp & 3) * 32) << 16);  // this warp's 32 lanes
+    const uint32_t x_hi = static_cast<uint32_t>(__cvta_generic_to_shared(sm.x_hi));
+    const uint32_t x_lo = static_cast<uint32_t>(__cvta_generic_to_shared(sm.x_lo));
+    const uint32_t w_hi = static_cast<uint32_t>(__cvta_generic_to_shared(sm.w_hi));
+    const uint32_t w_lo = static_cast<uint32_t>(__cvta_generic_to_shared(sm.w_lo));
+    const uint32_t g_hi = static_cast<uint32_t>(__cvta_generic_to_shared(sm.g_hi));
+    const uint32_t g_lo = static_cast<uint32_t>(__cvta_generic_to_shared(sm.g_lo));
+    const uint32_t r_hi = static_cast<uint32_t>(__cvta_generic_to_shared(sm.r_hi));
+    const uint32_t r_lo = static_cast<uint32_t>(__cvta_generic_to_shared(sm.r_lo));
+    constexpr uint32_t kSboX = 2 * KS * 128, kSboG = 32 * 128;
+    constexpr uint32_t idesc_z = tc_idesc_tf32<HID>(), idesc_g = tc_idesc_tf32<NW>();
+    const CameraF& cam = a.cam;
+    const float C0 = -(cam.R[0] * cam.t[0] + cam.R[3] * cam.t[1] + cam.R[6] * cam.t[2]);
+    const float C1 = -(cam.R[1] * cam.t[0] + cam.R[4] * cam.t[1] + cam.R[7] * cam.t[2]);
+    const float C2 = -(cam.R[2] * cam.t[0] + cam.R[5] * cam.t[1] + cam.R[8] * cam.t[2]);
+    const int tiles = (a.n + kTcRows - 1) / kTcRows;
+    uint32_t phase_z = 0, phase_g = 0;
+    bool failed = false, g_pending = false;
+    float db2_acc[3] = {0.f, 0.f, 0.f};
+    // the first half loads this row's latents and view direction; both load dL/dcolour
+    float x[K - 3], d[3], dc[3];
+    auto load_row = [&](int tile) {
+        const int i = tile * kTcRows + r;
+        const bool in = tile < tiles && i < a.n;
+        if (half == 0) {
+#pragma unroll
+            for (int k = 0; k < K - 3; ++k) x[k] = in && k < a.L ? a.latents[size_t(k) * a.n + i] : 0.f;
+            d[0] = in ? a.means[i] - C0 : 0.f;
+            d[1] = in ? a.means[size_t(a.n) + i] - C1 : 0.f;
+            d[2] = in ? a.means[2 * size_t(a.n) + i] - C2 : 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 3; ++c) dc[c] = in ? dcolors[size_t(c) * a.n + i] : 0.f;
+    };
+    load_row(blockIdx.x);
+    int done = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++done) {
+        const int i = tile * kTcRows + r;
+        const bool in = i < a.n;
+        float xr[K];  // (first half) this row of X: the unit view direction, the latents, zeros
+        if (half == 0) {
+            const float len = sqrtf(d[0] * d[0] + d[1] * d[1] + d[2] * d[2]);
+            const float il = len > 0.f ? 1.0f / len : 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k) xr[k] = k < 3 ? d[k] * il : x[k - 3];
+#pragma unroll
+            for (int k = 0; k < K; k += 4) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) split_trunc(xr[k + q], h[q], l[q]);
+                const int o = tc_offset<2 * KS>(r, k);
+                *reinterpret_cast<uint4*>(sm.x_hi + o) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(sm.x_lo + o) = make_uint4(l[0], l[1], l[2], l[3]);
             }
         }
-        stage_x<KS>(a, i0, st.x);
-        float h[HID / 8][4];
-        layer1<HID, KS>(w, st.x, h);
-        float z[4];
-        layer2<HID>(w, h, z);
-        // dL/dz2 = dL/dcolour * s (1 - s), s = sigmoid(z2 + b2)
-        float p[4] = {0.f, 0.f, 0.f, 0.f};
-        if (t < 2) {
+        const float g0 = dc[0], g1 = dc[1], g2 = dc[2];
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+        if (t == 0) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int c = 2 * t + (k & 1);
-                if (c < 3) {
-                    const float s = sigmoidf(z[k] + w.b2[c]);
-                    p[k] = dc[k] * s * (1.f - s);
+            for (int ks = 0; ks < KS; ++ks) {
+                const uint32_t off = uint32_t(ks) * 256u;
+                const uint64_t ah = tc_desc(x_hi + off, 128, kSboX), al = tc_desc(x_lo + off, 128, kSboX);
+                const uint64_t bh = tc_desc(w_hi + off, 128, kSboX), bl = tc_desc(w_lo + off, 128, kSboX);
+                tc_mma_tf32(tmem, ah, bh, idesc_z, ks > 0);
+                tc_mma_tf32(tmem, ah, bl, idesc_z, true);
+                tc_mma_tf32(tmem, al, bh, idesc_z, true);
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar_z)
+                         : "memory");
+        }
+        load_row(tile + int(gridDim.x));
+        bool ok = mbar_wait(mbar_z, phase_z);
+        phase_z ^= 1u;
+        // the previous tile's weight-gradient product has read its operands before they are
+        // rewritten below
+        if (g_pending) {
+            ok = mbar_wait(mbar_g, phase_g) && ok;
+            phase_g ^= 1u;
+            g_pending = false;
+        }
+        ok = __syncthreads_and(ok);
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+        if (!ok) {
+            atomicOr(&g_tc_error, 1u);
+            failed = true;
+            break;
+        }
+        // this half's share of the second layer from its columns of Z1, exchanged with the other
+        // half's through shared memory
+        float z2[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < HH / 16; ++c) {
+            float z[16];
+            tc_ld_rows<16>(trow + uint32_t(half * HH + 16 * c), z);
+#pragma unroll
+            for (int q = 0; q < 16; q += 4) {
+                const int u = half * HH + 16 * c + q;
+                const float4 bb = *reinterpret_cast<const float4*>(&sm.b1[u]);
+                const float4 u0 = *reinterpret_cast<const float4*>(&sm.w2[0][u]);
+                const float4 u1 = *reinterpret_cast<const float4*>(&sm.w2[1][u]);
+                const float4 u2 = *reinterpret_cast<const float4*>(&sm.w2[2][u]);
+                const float h0 = fmaxf(z[q] + bb.x, 0.f), h1 = fmaxf(z[q + 1] + bb.y, 0.f);
+                const float h2 = fmaxf(z[q + 2] + bb.z, 0.f), h3 = fmaxf(z[q + 3] + bb.w, 0.f);
+                z2[0] = fmaf(u0.x, h0, fmaf(u0.y, h1, fmaf(u0.z, h2, fmaf(u0.w, h3, z2[0]))));
+                z2[1] = fmaf(u1.x, h0, fmaf(u1.y, h1, fmaf(u1.z, h2, fmaf(u1.w, h3, z2[1]))));
+                z2[2] = fmaf(u2.x, h0, fmaf(u2.y, h1, fmaf(u2.z, h2, fmaf(u2.w, h3, z2[2]))));
+            }
+        }
+        // the exchange goes through the X operand's buffer: the product that read it is done,
+        // and the next tile's X is written only after the barrier before the next product
+        float* const zx = reinterpret_cast<float*>(sm.x_hi);
+        static_assert(sizeof(sm.x_hi) >= 2 * kTcRows * 3 * sizeof(float), "exchange space");
+        zx[(half * kTcRows + r) * 3 + 0] = z2[0];
+        zx[(half * kTcRows + r) * 3 + 1] = z2[1];
+        zx[(half * kTcRows + r) * 3 + 2] = z2[2];
+        __syncthreads();
+        float dz2[3];
+        const float gc[3] = {g0, g1, g2};
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+            const float zz = zx[r * 3 + c] + zx[(kTcRows + r) * 3 + c] + sm.b2[c];
+            const float sg = sigmoidf(zz);
+            dz2[c] = gc[c] * sg * (1.f - sg);
+            if (half == 0) db2_acc[c] += dz2[c];
+        }
+        // this half's hidden units, eight at a time: h, dz1 = (W2^T dz2) where z1 > 0, their
+        // columns of the transposed operand, and its share of dL/dx = W1^T dz1 (latent columns)
+        float dl[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dl[k] = 0.f;
+        uint32_t zc[8], zn[8];
+        tc_ld8_async(trow + uint32_t(half * HH), zc);
+        tc_ld_wait(zc);
+#pragma unroll 1
+        for (int gq = 0; gq < HH / 8; ++gq) {
+            const int grp = half * (HH / 8) + gq;
+            if (gq + 1 < HH / 8) tc_ld8_async(trow + uint32_t(8 * (grp + 1)), zn);
+            float vd[8], vh[8];
+#pragma unroll
+            for (int q = 0; q < 8; q += 4) {
+                const int u = 8 * grp + q;
+                const float4 bb = *reinterpret_cast<const float4*>(&sm.b1[u]);
+                const float4 u0 = *reinterpret_cast<const float4*>(&sm.w2[0][u]);
+                const float4 u1 = *reinterpret_cast<const float4*>(&sm.w2[1][u]);
+                const float4 u2 = *reinterpret_cast<const float4*>(&sm.w2[2][u]);
+                const float b4[4] = {bb.x, bb.y, bb.z, bb.w};
+                const float a0[4] = {u0.x, u0.y, u0.z, u0.w}, a1[4] = {u1.x, u1.y, u1.z, u1.w};
+                const float a2[4] = {u2.x, u2.y, u2.z, u2.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float zz = __uint_as_float(zc[q + e]) + b4[e];
+                    const float tt = fmaf(a0[e], dz2[0], fmaf(a1[e], dz2[1], a2[e] * dz2[2]));
+                    vd[q + e] = zz > 0.f ? tt : 0.f;
+                    vh[q + e] = fmaxf(zz, 0.f);
                 }
             }
-        }
-        // every lane needs dL/dz2 of rows g and g + 8
-        const float d00 = __shfl_sync(kFull, p[0], 4 * g), d01 = __shfl_sync(kFull, p[1], 4 * g);
-        const float d10 = __shfl_sync(kFull, p[2], 4 * g), d11 = __shfl_sync(kFull, p[3], 4 * g);
-        const float d02 = __shfl_sync(kFull, p[0], 4 * g + 1), d12 = __shfl_sync(kFull, p[2], 4 * g + 1);
-        // dL/dz1 = (W2^T dL/dz2) where z1 > 0, in the accumulator layout of h
-        float dz[HID / 8][4];
 #pragma unroll
-        for (int nt = 0; nt < HID / 8; ++nt) {
-            const int u0 = nt * 8 + 2 * t, u1 = u0 + 1;
-            const float w00 = w.w2f[u0], w10 = w.w2f[HID + u0], w20 = w.w2f[2 * HID + u0];
-            const float w01 = w.w2f[u1], w11 = w.w2f[HID + u1], w21 = w.w2f[2 * HID + u1];
-            dz[nt][0] = h[nt][0] > 0.f ? fmaf(d00, w00, fmaf(d01, w10, d02 * w20)) : 0.f;
-            dz[nt][1] = h[nt][1] > 0.f ? fmaf(d00, w01, fmaf(d01, w11, d02 * w21)) : 0.f;
-            dz[nt][2] = h[nt][2] > 0.f ? fmaf(d10, w00, fmaf(d11, w10, d12 * w20)) : 0.f;
-            dz[nt][3] = h[nt][3] > 0.f ? fmaf(d10, w01, fmaf(d11, w11, d12 * w21)) : 0.f;
-        }
-        // dL/dx = W1^T dL/dz1: A = dz1 (hidden units renumbered as in layer 2), B = W1
-        float dx[KS][4];
+            for (int q = 0; q < 8; ++q) {
+                const int u = 8 * grp + q;
 #pragma unroll
-        for (int nt = 0; nt < KS; ++nt) dx[nt][0] = dx[nt][1] = dx[nt][2] = dx[nt][3] = 0.f;
+                for (int k = 0; k < K; k += 4) {
+                    float w4[4];
+                    if constexpr (Smem::kW1f) {
+                        const float4 f = *reinterpret_cast<const float4*>(&sm.w1f[u * K + k]);
+                        w4[0] = f.x; w4[1] = f.y; w4[2] = f.z; w4[3] = f.w;
+                    } else {
+                        const int o = tc_offset<2 * KS>(u, k);
+                        const uint4 wh = *reinterpret_cast<const uint4*>(sm.w_hi + o);
+                        const uint4 wl = *reinterpret_cast<const uint4*>(sm.w_lo + o);
+                        w4[0] = __uint_as_float(wh.x) + __uint_as_float(wl.x);
+                        w4[1] = __uint_as_float(wh.y) + __uint_as_float(wl.y);
+                        w4[2] = __uint_as_float(wh.z) + __uint_as_float(wl.z);
+                        w4[3] = __uint_as_float(wh.w) + __uint_as_float(wl.w);
+                    }
 #pragma unroll
-        for (int kc = 0; kc < HID / 8; ++kc) {
-            uint32_t ah[4], al[4];
-            split(dz[kc][0], ah[0], al[0]);
-            split(dz[kc][2], ah[1], al[1]);
-            split(dz[kc][1], ah[2], al[2]);
-            split(dz[kc][3], ah[3], al[3]);
+                    for (int e = 0; e < 4; ++e)
+                        if (k + e >= 3) dl[k + e - 3] = fmaf(vd[q], w4[e], dl[k + e - 3]);
+                }
+            }
+            store_col8_t(sm.g_hi, sm.g_lo, grp, r, vd, lane);
+            store_col8_t(sm.g_hi, sm.g_lo, 8 + grp, r, vh, lane);
+            if (gq + 1 < HH / 8) {
+                tc_ld_wait(zn);
 #pragma unroll
-            for (int nt = 0; nt < KS; ++nt) {
-                const int o = (kc * 8 + 2 * t) * kXStride + nt * 8 + g;
-                mma3(dx[nt], ah, al, w.w1h[o], w.w1h[o + kXStride], w.w1l[o], w.w1l[o + kXStride]);
+                for (int q = 0; q < 8; ++q) zc[q] = zn[q];
             }
         }
+        // the transposed [X | dZ2 | 1]^T: the first half writes X's columns, the second dz2,
+        // ones (zero past the tile's Gaussians) and zeros; the second half also hands its share
+        // of dL/dx to the first through tensor memory
+        if (half == 0) {
 #pragma unroll
-        for (int nt = 0; nt < KS; ++nt) {
+            for (int gq = 0; gq < K / 8; ++gq) {
+                float v[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int j = nt * 8 + 2 * t + (k & 1), i = i0 + g + 8 * (k >> 1);
-                if (j < a.L && i < a.n) dlatents[size_t(j) * a.n + i] = dx[nt][k];
+                for (int q = 0; q < 8; ++q) v[q] = xr[8 * gq + q];
+                store_col8_t(sm.r_hi, sm.r_lo, gq, r, v, lane);
             }
-        }
-        // stage dz1, h, dz2 for the weight gradients
+        } else {
 #pragma unroll
-        for (int nt = 0; nt < HID / 8; ++nt) {
-            const int u0 = nt * 8 + 2 * t;
-            *reinterpret_cast<float2*>(&st.dz1[g * HS + u0]) = make_float2(dz[nt][0], dz[nt][1]);
-            *reinterpret_cast<float2*>(&st.dz1[(g + 8) * HS + u0]) = make_float2(dz[nt][2], dz[nt][3]);
-            *reinterpret_cast<float2*>(&st.h[g * HS + u0]) = make_float2(h[nt][0], h[nt][1]);
-            *reinterpret_cast<float2*>(&st.h[(g + 8) * HS + u0]) = make_float2(h[nt][2], h[nt][3]);
+            for (int gq = K / 8; gq < NW / 8; ++gq) {
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c = 8 * gq + q;
+                    v[q] = c < K + 3 ? dz2[c - K] : (c == kOnes && in) ? 1.f : 0.f;
+                }
+                store_col8_t(sm.r_hi, sm.r_lo, gq, r, v, lane);
+            }
+            tc_st32(trow + kDlCol, dl);
         }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
         if (t == 0) {
-            st.dz2[g * 4] = d00;
-            st.dz2[g * 4 + 1] = d01;
-            st.dz2[g * 4 + 2] = d02;
-            st.dz2[(g + 8) * 4] = d10;
-            st.dz2[(g + 8) * 4 + 1] = d11;
-            st.dz2[(g + 8) * 4 + 2] = d12;
-        }
-        __syncwarp();
-        // lane owns hidden units lane + 32 q: dW1 rows, db1, dW2 columns; lanes 0..2 db2
-#pragma unroll 4
-        for (int r = 0; r < kRows; ++r) {
-            const float* xr = st.x + r * kXStride;
-            const float e0 = st.dz2[r * 4], e1 = st.dz2[r * 4 + 1], e2 = st.dz2[r * 4 + 2];
 #pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                const int u = lane + 32 * q;
-                const float dzv = st.dz1[r * HS + u], hv = st.h[r * HS + u];
-                gb1[q] += dzv;
-#pragma unroll
-                for (int j = 0; j < KS * 8; ++j) gw1[q][j] = fmaf(dzv, xr[j], gw1[q][j]);
-                gw2[q][0] = fmaf(e0, hv, gw2[q][0]);
-                gw2[q][1] = fmaf(e1, hv, gw2[q][1]);
-                gw2[q][2] = fmaf(e2, hv, gw2[q][2]);
+            for (int ks = 0; ks < kTcRows / 8; ++ks) {
+                const uint32_t off = uint32_t(ks) * 256u;
+                const uint64_t ah = tc_desc(g_hi + off, 128, kSboG), al = tc_desc(g_lo + off, 128, kSboG);
+                const uint64_t bh = tc_desc(r_hi + off, 128, kSboG), bl = tc_desc(r_lo + off, 128, kSboG);
+                tc_mma_tf32(tmem + uint32_t(HID), ah, bh, idesc_g, done > 0 || ks > 0);
+                tc_mma_tf32(tmem + uint32_t(HID), ah, bl, idesc_g, true);
+                tc_mma_tf32(tmem + uint32_t(HID), al, bh, idesc_g, true);
             }
-            gb2 += lane == 0 ? e0 : lane == 1 ? e1 : lane == 2 ? e2 : 0.f;
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar_g)
+                         : "memory");
         }
-        __syncwarp();  // the staging is rewritten by the next tile
+        g_pending = true;
+        if (half == 0) {
+            float o[32];
+            tc_ld_rows<32>(trow + kDlCol, o);
+            if (in) {
+#pragma unroll
+                for (int k = 0; k < K - 3; ++k)
+                    if (k < a.L) dlatents[size_t(k) * a.n + i] = dl[k] + o[k];
+            }
+        }
     }
-    // block sums, then one global atomic per weight per block
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int u = lane + 32 * q;
-#pragma unroll
-        for (int j = 0; j < KS * 8; ++j)
-            if (j < a.D) atomicAdd(&sums.dW1[u * kInMax + j], gw1[q][j]);
-        atomicAdd(&sums.db1[u], gb1[q]);
-#pragma unroll
-        for (int c = 0; c < 3; ++c) atomicAdd(&sums.dW2[c * HID + u], gw2[q][c]);
+    // the accumulated weight gradients, once the last product is done
+    bool have = done > 0 && !failed;
+    if (g_pending) {
+        const bool ok = __syncthreads_and(mbar_wait(mbar_g, phase_g));
+        phase_g ^= 1u;
+        if (!ok) {
+            atomicOr(&g_tc_error, 1u);
+            failed = true;
+            have = false;
+        }
     }
-    if (lane < 3) atomicAdd(&sums.db2[lane], gb2);
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    if (have && half == 0) {
+        // thread r holds row r of G: r < 64 is hidden unit r of dZ1^T (dW1 row r, db1 from the
+        // ones column), r >= 64 hidden unit r - 64 of H^T (dW2 column r - 64 from the dz2 columns)
+        float gr[NW];
+#pragma unroll
+        for (int c = 0; c < NW; c += 16) {
+            float tv[16];
+            tc_ld_rows<16>(trow + uint32_t(HID + c), tv);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) gr[c + q] = tv[q];
+        }
+        if (r < HID) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                if (k < a.D) {
+                    const int src = k < 3 ? a.L + k : k - 3;
+                    atomicAdd(dW1 + r * a.D + src, gr[k]);
+                }
+            }
+            atomicAdd(db1 + r, gr[kOnes]);
+        } else if (r >= 64 && r < 64 + HID) {
+#pragma unroll
+            for (int c = 0; c < 3; ++c) atomicAdd(dW2 + c * HID + (r - 64), gr[K + c]);
+        }
+    }
+    // db2: the block's sum of dz2 (the first half's rows)
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        float v = db2_acc[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+        if (lane == 0 && warp < 4) sm.db2[warp][c] = v;
+    }
+    // tensor memory goes back once no product is in flight and no warp reads it
+    if (failed) {
+        (void)mbar_wait(mbar_z, phase_z);
+        (void)mbar_wait(mbar_g, phase_g);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
     __syncthreads();
-    for (int i = threadIdx.x; i < HID * a.D; i += blockDim.x) {
-        const int u = i / a.D, j = i % a.D;
-        const float v = sums.dW1[u * kInMax + j];
-        if (v != 0.f) atomicAdd(dW1 + i, v);
-    }
-    for (int i = threadIdx.x; i < HID; i += blockDim.x)
-        if (sums.db1[i] != 0.f) atomicAdd(db1 + i, sums.db1[i]);
-    for (int i = threadIdx.x; i < 3 * HID; i += blockDim.x)
-        if (sums.dW2[i] != 0.f) atomicAdd(dW2 + i, sums.dW2[i]);
-    if (threadIdx.x < 3 && sums.db2[threadIdx.x] != 0.f) atomicAdd(db2 + threadIdx.x, sums.db2[threadIdx.x]);
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    if (t < 3 && done > 0 && !failed) atomicAdd(db2 + t, sm.db2[0][t] + sm.db2[1][t] + sm.db2[2][t] + sm.db2[3][t]);
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
 __global__ void k_zero_mlp_grads(float* dW1, int nW1, float* db1, int nb1, float* dW2, int nW2, float* db2) {
@@ -662,14 +850,17 @@ cudaError_t launch_fwd_t(const MlpArgs& a, float* colors, cudaStream_t s) {
 
 template <int HID, int KS>
 cudaError_t launch_bwd_t(const MlpArgs& a, const float* dcol, float* dlat, const rs_mlp_grads& gr, cudaStream_t s) {
-    const size_t smem = sizeof(WeightSmem<HID>) + sizeof(BwdSums<HID>) + size_t(kMlpWarps) * sizeof(BwdWarpSmem<HID>);
-    cudaError_t e = cudaFuncSetAttribute(k_mlp_bwd<HID, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    const size_t smem = sizeof(TcBwdSmem<HID, KS>) + 1024;  // + room to align the base to 1 KB
+    static_assert(sizeof(TcBwdSmem<HID, KS>) + 1024 <= 232448, "shared memory per CTA");
+    cudaError_t e = cudaFuncSetAttribute(k_mlp_bwd_tc<HID, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     pdl_launch(k_zero_mlp_grads, 8, 256, 0, s, gr.d_dW1, HID * a.D, gr.d_db1, HID, gr.d_dW2, 3 * HID, gr.d_db2);
     if (a.n == 0) return cudaGetLastError();
-    const int tiles = (a.n + kRows - 1) / kRows;
-    const int blocks = std::min((tiles + kMlpWarps - 1) / kMlpWarps, 152 * 2);
-    pdl_launch(k_mlp_bwd<HID, KS>, blocks, kMlpThreads, smem, s, a, dcol, dlat, gr.d_dW1, gr.d_db1, gr.d_dW2, gr.d_db2);
+    const int tiles = (a.n + kTcRows - 1) / kTcRows;
+    // one CTA per SM (the shared memory of one), each holding 256 columns of tensor memory
+    const int blocks = std::min(tiles, 152);
+    pdl_launch(k_mlp_bwd_tc<HID, KS>, blocks, kTcBwdThreads, smem, s, a, dcol, dlat, gr.d_dW1, gr.d_db1, gr.d_dW2,
+               gr.d_db2);
     return cudaGetLastError();
 }
 

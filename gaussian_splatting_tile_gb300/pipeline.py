@@ -249,6 +249,15 @@ class AppearanceStep:
         rs.rs_l1_loss_grad(F.image, target, scale, self.dL_dimage, self.loss, stream)
         return F
 
+    def forward_async(self, camera, target: torch.Tensor, scale: float, result: torch.Tensor, bg=(0.0, 0.0, 0.0),
+                      stream=None):
+        """forward() with the sync-free binning (Renderer.forward_async): nothing waits on the
+        host; check the entry count in `result` with self.R.check_async after the stream."""
+        self.R.set_camera(camera)
+        rs.rs_appearance_fwd(camera, self.g.means, self.latents, self.mlp, self.colors, stream)
+        self.R.forward_async(self.gc, result, bg=bg, stream=stream)
+        rs.rs_l1_loss_grad(self.R.image, target, scale, self.dL_dimage, self.loss, stream)
+
     def backward(self, dL_dimage: torch.Tensor | None = None, stream=None) -> Backward:
         """Compositing and projection backward from dL/dimage (default: the L1 gradient), then
         the MLP backward (into self.dL_dlatents and self.mlp_grads)."""
@@ -263,6 +272,36 @@ class AppearanceStep:
     def view(self, camera, target, scale, bg=(0.0, 0.0, 0.0), stream=None):
         F = self.forward(camera, target, scale, bg, stream)
         return F, self.backward(stream=stream)
+
+
+class AppearanceGraph:
+    """One view of the training-shaped step (MLP colours, render, L1 loss, render backward, MLP
+    backward) captured as a single CUDA graph, like FrameGraph: the camera is fixed, the
+    latents, weights, Gaussians and target are read from their buffers at every replay, and
+    `check()` (after the stream has passed the replay) returns the entry count."""
+
+    def __init__(self, step: AppearanceStep, camera, target: torch.Tensor, scale: float, bg=(0.0, 0.0, 0.0)):
+        self.step, self.camera = step, camera
+        self.result = torch.zeros(2, dtype=torch.int64).pin_memory()
+        R = step.R
+        R._grads(-1)
+        step.forward_async(camera, target, scale, self.result, bg)
+        step.backward()
+        torch.cuda.current_stream(R.device).synchronize()
+        R.check_async(self.result)
+        self.capacity = R.capacity
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            step.forward_async(camera, target, scale, self.result, bg)
+            step.backward()
+
+    def replay(self):
+        if self.step.R.capacity != self.capacity:
+            raise RuntimeError("the renderer's buffers changed since the capture")
+        self.graph.replay()
+
+    def check(self) -> int:
+        return self.step.R.check_async(self.result)
 
 
 class FrameGraph:

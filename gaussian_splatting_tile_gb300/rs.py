@@ -139,6 +139,11 @@ def lib():
         L.rs_adam_step.argtypes = [ctypes.POINTER(rs_adam_segment), ctypes.c_int32, ctypes.c_double,
                                    ctypes.c_double, ctypes.c_double, ctypes.c_int32, _VP]
         L.rs_densify_stats.argtypes = [ctypes.c_int32, _VP, _VP, _VP, _VP, _VP]
+        L.rs_densify_workspace_size.argtypes = [ctypes.c_int32]
+        L.rs_densify_plan.argtypes = [ctypes.c_int32, _VP, _VP, _VP, _VP, ctypes.POINTER(rs_densify_rule), _VP,
+                                      ctypes.c_size_t, _VP, ctypes.POINTER(ctypes.c_int32), _VP]
+        L.rs_densify_apply.argtypes = [ctypes.c_int32, _VP, ctypes.c_size_t, _VP, _VP, _VP,
+                                       ctypes.POINTER(rs_densify_group), ctypes.c_int32, ctypes.c_int32, _VP]
         L.rs_l1_dssim_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                  ctypes.POINTER(ctypes.c_size_t)]
         L.rs_l1_dssim_loss_grad.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _VP, _VP, ctypes.c_float,
@@ -578,6 +583,74 @@ def rs_densify_stats(dL_dmeans2d: torch.Tensor, radius: torch.Tensor, accum: tor
     _check("rs_densify_stats", lib().rs_densify_stats(
         n, _ptr(dL_dmeans2d, torch.float32, 2 * n, "dL_dmeans2d"), _ptr(radius, torch.int32, n, "radius"),
         _ptr(accum, torch.float32, n, "accum"), _ptr(count, torch.float32, n, "count"), _stream(stream)))
+
+
+RS_DENSIFY_COPY, RS_DENSIFY_MEANS, RS_DENSIFY_LOG_SCALES, RS_DENSIFY_MAX_GROUPS = 0, 1, 2, 8
+
+
+class rs_densify_rule(ctypes.Structure):
+    _fields_ = [("grad_threshold", ctypes.c_float), ("dense_scale", ctypes.c_float),
+                ("min_opacity", ctypes.c_float), ("max_scale", ctypes.c_float)]
+
+
+class rs_densify_group(ctypes.Structure):
+    _fields_ = [("d_param", _VP), ("d_m", _VP), ("d_v", _VP), ("d_param_out", _VP), ("d_m_out", _VP),
+                ("d_v_out", _VP), ("rows", ctypes.c_int32), ("kind", ctypes.c_int32)]
+
+
+@dataclasses.dataclass
+class DensifyGroup:
+    """One parameter array [rows, n] of rs_densify_apply with its Adam moments (m, v may be None);
+    the outputs [rows, n_out] (m_out, v_out may be None)."""
+    param: torch.Tensor
+    param_out: torch.Tensor
+    m: torch.Tensor | None = None
+    v: torch.Tensor | None = None
+    m_out: torch.Tensor | None = None
+    v_out: torch.Tensor | None = None
+    kind: int = RS_DENSIFY_COPY
+
+
+def rs_densify_workspace_size(n: int) -> int:
+    return int(lib().rs_densify_workspace_size(int(n)))
+
+
+def rs_densify_plan(accum, count, log_scales, opacity_logits, grad_threshold: float, dense_scale: float,
+                    min_opacity: float, max_scale: float, workspace: torch.Tensor, action: torch.Tensor | None = None,
+                    stream=None) -> dict:
+    """Classification and counts of rs_densify_plan (float32 CUDA tensors; workspace uint8 CUDA of at
+    least rs_densify_workspace_size(n) bytes; action: optional uint8 CUDA [n])."""
+    n = int(accum.numel())
+    rule = rs_densify_rule(float(grad_threshold), float(dense_scale), float(min_opacity), float(max_scale))
+    counts = (ctypes.c_int32 * 5)()
+    _check("rs_densify_plan", lib().rs_densify_plan(
+        n, _ptr(accum, torch.float32, n, "accum"), _ptr(count, torch.float32, n, "count"),
+        _ptr(log_scales, torch.float32, 3 * n, "log_scales"), _ptr(opacity_logits, torch.float32, n, "opacity_logits"),
+        ctypes.byref(rule), _ptr(workspace, torch.uint8, rs_densify_workspace_size(n), "workspace"),
+        ctypes.c_size_t(workspace.numel()), _ptr(action, torch.uint8, n, "action"), counts, _stream(stream)))
+    return dict(zip(("n_out", "kept", "cloned", "split", "removed"), (int(x) for x in counts)))
+
+
+def rs_densify_apply(n: int, workspace: torch.Tensor, quats, log_scales, noise, groups, n_out: int, stream=None):
+    """Moves every group (list of DensifyGroup) to its densified outputs; noise: float32 CUDA [2, 3, n]."""
+    if len(groups) > RS_DENSIFY_MAX_GROUPS:
+        raise ValueError(f"at most {RS_DENSIFY_MAX_GROUPS} groups per call")
+    arr = (rs_densify_group * max(1, len(groups)))()
+    for k, gr in enumerate(groups):
+        rows = int(gr.param.numel()) // max(n, 1)
+        arr[k].d_param = _ptr(gr.param, torch.float32, rows * n, "param")
+        arr[k].d_m = _ptr(gr.m, torch.float32, rows * n, "m")
+        arr[k].d_v = _ptr(gr.v, torch.float32, rows * n, "v")
+        arr[k].d_param_out = _ptr(gr.param_out, torch.float32, rows * n_out, "param_out")
+        arr[k].d_m_out = _ptr(gr.m_out, torch.float32, rows * n_out, "m_out")
+        arr[k].d_v_out = _ptr(gr.v_out, torch.float32, rows * n_out, "v_out")
+        arr[k].rows = rows
+        arr[k].kind = int(gr.kind)
+    _check("rs_densify_apply", lib().rs_densify_apply(
+        int(n), _ptr(workspace, torch.uint8, rs_densify_workspace_size(n), "workspace"),
+        ctypes.c_size_t(workspace.numel()), _ptr(quats, torch.float32, 4 * n, "quats"),
+        _ptr(log_scales, torch.float32, 3 * n, "log_scales"), _ptr(noise, torch.float32, 6 * n, "noise"),
+        arr, len(groups), int(n_out), _stream(stream)))
 
 
 def rs_l1_dssim_workspace_size(channels: int, height: int, width: int) -> int:

@@ -350,6 +350,78 @@ int rs_adam_step(const rs_adam_segment* segs, int32_t n_segs, double beta1, doub
 int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_radius, float* d_accum,
                      float* d_count, void* stream);
 
+/* Densification: clone, split and prune (rigel README: "GaussianModel: activations,
+ * densify/prune"; its training log reports clone / split / prune counts per densification, and
+ * densification and pruning must leave every parameter and its Adam moments the same length).
+ * The pages do not state the criteria; these are 3D Gaussian Splatting's adaptive density control.
+ * Per Gaussian i, with g_i = accum_i / count_i the mean view-space gradient norm (rs_densify_stats;
+ * no growth when count_i = 0) and s_max the largest of exp(log-scales):
+ *   - g_i >= grad_threshold and s_max <= dense_scale: cloned (kept, plus an identical copy);
+ *   - g_i >= grad_threshold and s_max > dense_scale: split into two children at
+ *     mean + R(q) (s * z_c) (R the rotation of the normalised quaternion, s = exp(log-scales),
+ *     z_c the caller's standard normal draws) with log-scales log(s / 1.6), the rest copied; the
+ *     parent is removed;
+ *   - otherwise kept;
+ * and then every Gaussian the step would produce whose opacity sigmoid(logit) is below
+ * min_opacity, or whose largest scale exceeds max_scale (when max_scale > 0), is removed (split
+ * children are tested with their own scales).  The comparisons run on the stored values:
+ * max log-scale against ln(dense_scale) and ln(max_scale), the logit against
+ * logit(min_opacity), accum against grad_threshold * count, in float32.
+ * Output order: the kept originals in index order, then the clones in the order of their sources,
+ * then every split Gaussian's first child in index order, then the second children.  Clones and
+ * children start with zero Adam moments; kept Gaussians keep theirs. */
+#define RS_DENSIFY_COPY 0        /* copied to every output of the Gaussian                       */
+#define RS_DENSIFY_MEANS 1       /* [3][n] means: split children are moved by R(q) (s * z_c)      */
+#define RS_DENSIFY_LOG_SCALES 2  /* [3][n] log-scales: split children get log(s / 1.6)           */
+#define RS_DENSIFY_MAX_GROUPS 8
+
+typedef struct rs_densify_rule {
+    float grad_threshold;   /* on accum / count (3DGS: 0.0002)                                  */
+    float dense_scale;      /* > 0: clone at most this largest scale, split above it             */
+    float min_opacity;      /* in [0, 1): prune below this opacity (3DGS: 0.005)                 */
+    float max_scale;        /* prune above this largest scale; <= 0: no size test                */
+} rs_densify_rule;
+
+/* One parameter array [rows][n] and its Adam moments (d_m, d_v may be NULL: no moments), moved
+ * to [rows][n_out] outputs (d_m_out, d_v_out may be NULL).  kind RS_DENSIFY_MEANS and
+ * RS_DENSIFY_LOG_SCALES need rows = 3. */
+typedef struct rs_densify_group {
+    const float* d_param;
+    const float* d_m;
+    const float* d_v;
+    float* d_param_out;
+    float* d_m_out;
+    float* d_v_out;
+    int32_t rows;
+    int32_t kind;           /* RS_DENSIFY_* */
+} rs_densify_group;
+
+/* Workspace bytes of rs_densify_plan / rs_densify_apply for n Gaussians (0 if n is invalid). */
+size_t rs_densify_workspace_size(int32_t n);
+
+/* Classifies every Gaussian and counts the outputs; reads the counts back to the host (one
+ * stream-ordered copy and a synchronisation of `stream`: the caller allocates the outputs with
+ * them).  Inputs: d_accum [n], d_count [n] (rs_densify_stats), d_log_scales [3][n],
+ * d_opacity_logits [n].  counts (host int32[5]): n_out, originals kept (cloned ones included),
+ * clones, Gaussians split, Gaussians removed.  d_action (device uint8 [n], may be NULL) receives
+ * each Gaussian's fate: 0 removed, 1 kept, 2 kept and cloned, 3 split.  d_workspace:
+ * rs_densify_workspace_size(n) bytes, 256-byte aligned; it keeps the classification for
+ * rs_densify_apply.  Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CAPACITY (n_out above
+ * RS_MAX_GAUSSIANS; counts are still written), RS_ERR_CUDA. */
+int rs_densify_plan(int32_t n, const float* d_accum, const float* d_count, const float* d_log_scales,
+                    const float* d_opacity_logits, const rs_densify_rule* rule, void* d_workspace,
+                    size_t workspace_bytes, uint8_t* d_action, int32_t* counts, void* stream);
+
+/* Writes the densified arrays of up to RS_DENSIFY_MAX_GROUPS groups in one launch, from the
+ * classification rs_densify_plan left in d_workspace (same n, same inputs).  d_quats [4][n] and
+ * d_log_scales [3][n] are the Gaussians' current quaternions and log-scales (the split offsets),
+ * d_noise [2][3][n] standard normal draws (child c, component k of Gaussian i at
+ * (c * 3 + k) * n + i).  n_out: counts[0] of the plan; outputs are [rows][n_out] and must not
+ * overlap the inputs.  Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CUDA. */
+int rs_densify_apply(int32_t n, const void* d_workspace, size_t workspace_bytes, const float* d_quats,
+                     const float* d_log_scales, const float* d_noise, const rs_densify_group* groups,
+                     int32_t n_groups, int32_t n_out, void* stream);
+
 /* Allocation-free variant of rs_bin.  The source pages have no counterpart: this entry point
  * exists for callers of this library that cannot allocate device memory -- for example a plug-in
  * whose host application owns and budgets all device memory, or a per-frame loop that must not

@@ -65,6 +65,7 @@ def lib():
         _lib.orc_bin.restype = ctypes.c_int64
         _lib.orc_bin_ellipse.restype = ctypes.c_int64
         _lib.orc_ellipse_tiles.restype = ctypes.c_int32
+        _lib.orc_densify_group.restype = ctypes.c_int32
     return _lib
 
 
@@ -368,6 +369,47 @@ def l1_dssim(image, target, lam=0.2, scale=1.0):
     if rc != 0:
         raise ValueError(f"orc_l1_dssim returned {rc}")
     return grad, float(loss.value), smap
+
+
+def densify_classify(accum, count, log_scales, logits, grad_threshold, dense_scale, min_opacity, max_scale=0.0):
+    """c12 decisions: (action [n] int32: 0 removed, 1 kept, 2 kept and cloned, 3 split;
+    ambiguous [n] bool; counts dict n_out, kept, cloned, split, removed)."""
+    a = _d(accum)
+    n = a.shape[0]
+    action = np.zeros(n, np.int32)
+    amb = np.zeros(n, np.uint8)
+    counts = np.zeros(5, np.int32)
+    rc = lib().orc_densify_classify(ctypes.c_int32(n), _p(a), _p(_d(count)), _p(_d(log_scales)), _p(_d(logits)),
+                                    ctypes.c_double(grad_threshold), ctypes.c_double(dense_scale),
+                                    ctypes.c_double(min_opacity), ctypes.c_double(max_scale), _p(action), _p(amb),
+                                    _p(counts))
+    if rc != 0:
+        raise ValueError(f"orc_densify_classify returned {rc}")
+    return action, amb.astype(bool), dict(zip(("n_out", "kept", "cloned", "split", "removed"), (int(x) for x in counts)))
+
+
+def densify_group(action, param, m=None, v=None, kind=0, quats=None, log_scales=None, noise=None):
+    """c12 for one parameter group [rows][n]: (param_out, m_out, v_out) of [rows][n_out]."""
+    act = np.ascontiguousarray(action, np.int32)
+    n = act.shape[0]
+    P = _d(param).reshape(-1, n)
+    rows = P.shape[0]
+    n_out = int(((act == 1) | (act == 2)).sum() + (act == 2).sum() + 2 * (act == 3).sum())
+    po = np.zeros((rows, max(n_out, 1)))
+    mo = np.zeros((rows, max(n_out, 1))) if m is not None else None
+    vo = np.zeros((rows, max(n_out, 1))) if v is not None else None
+    M = None if m is None else _d(m).reshape(rows, n)
+    V = None if v is None else _d(v).reshape(rows, n)
+    q = None if quats is None else _d(quats)
+    ls = None if log_scales is None else _d(log_scales)
+    z = None if noise is None else _d(noise)
+    if kind == 1 and (q is None or ls is None or z is None):
+        raise ValueError("means need quats, log_scales and noise")
+    wrote = lib().orc_densify_group(ctypes.c_int32(n), _p(act), ctypes.c_int32(rows), ctypes.c_int32(kind), _p(P),
+                                    _p(M), _p(V), _p(q), _p(ls), _p(z), ctypes.c_int32(n_out), _p(po), _p(mo), _p(vo))
+    assert wrote == n_out
+    cut = lambda x: None if x is None else x[:, :n_out]
+    return cut(po), cut(mo), cut(vo)
 
 
 def render(cam, g, bg=(0.0, 0.0, 0.0), prec: int = 64):

@@ -1160,6 +1160,102 @@ int64_t orc_bin_ellipse(const orc_camera* cam, int32_t n, const float* means2d, 
     return E;
 }
 
+// c12: densification ([rigel] "GaussianModel: activations, densify/prune"; the training log's
+// clone / split / prune counts).  The pages name the operations only; the criteria are those of
+// 3D Gaussian Splatting's adaptive density control, decided here in double precision.  A
+// decision within a relative 1e-5 of its threshold is flagged (either outcome is correct there).
+int orc_densify_classify(int32_t n, const double* accum, const double* count, const double* log_scales,
+                         const double* logits, double grad_threshold, double dense_scale, double min_opacity,
+                         double max_scale, int32_t* action, uint8_t* ambig, int32_t* counts) {
+    if (n < 0) return -1;
+    const double ln_dense = std::log(dense_scale);
+    const double logit_min = min_opacity > 0 ? std::log(min_opacity / (1.0 - min_opacity)) : -HUGE_VAL;
+    const double ln_max = max_scale > 0 ? std::log(max_scale) : HUGE_VAL;
+    const double ln_split = std::log(1.6);  // split children carry s / 1.6
+    auto near = [](double x, double thr) {
+        return std::isfinite(thr) && std::fabs(x - thr) <= 1e-5 * std::max(1.0, std::fabs(thr));
+    };
+    int32_t kept = 0, cloned = 0, split = 0, removed = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const size_t N = size_t(n);
+        const double ls = std::max(std::max(log_scales[i], log_scales[N + i]), log_scales[2 * N + i]);
+        // the mean view-space gradient norm reaches the threshold (no views: no growth)
+        const bool grow = count[i] > 0 && accum[i] / count[i] >= grad_threshold;
+        const bool dense = ls <= ln_dense;
+        const bool faint = logits[i] < logit_min;
+        uint8_t amb = 0;
+        if (count[i] > 0 && std::fabs(accum[i] - grad_threshold * count[i]) <= 1e-5 * grad_threshold * count[i]) amb = 1;
+        if (near(logits[i], logit_min)) amb = 1;
+        int32_t a;
+        if (grow) amb |= near(ls, ln_dense);
+        if (grow && !dense) {
+            amb |= near(ls - ln_split, ln_max);
+            a = (faint || ls - ln_split > ln_max) ? 0 : 3;
+        } else {
+            amb |= near(ls, ln_max);
+            a = (faint || ls > ln_max) ? 0 : grow ? 2 : 1;
+        }
+        action[i] = a;
+        if (ambig) ambig[i] = amb;
+        kept += a == 1 || a == 2;
+        cloned += a == 2;
+        split += a == 3;
+        removed += a == 0;
+    }
+    counts[0] = kept + cloned + 2 * split;
+    counts[1] = kept;
+    counts[2] = cloned;
+    counts[3] = split;
+    counts[4] = removed;
+    return 0;
+}
+
+// One parameter group [rows][n] after densification with the given actions (0 removed, 1 kept,
+// 2 kept and cloned, 3 split), in the stated order: kept originals, clones, first children,
+// second children.  kind 1: means (children at mean + R(q) (s * z_c)); kind 2: log-scales
+// (children log(s / 1.6)); kind 0: copied.  m and v (may be NULL) follow the kept originals;
+// clones and children start at zero.  Returns the number of Gaussians written.
+int32_t orc_densify_group(int32_t n, const int32_t* action, int32_t rows, int32_t kind, const double* param,
+                          const double* m, const double* v, const double* quats, const double* log_scales,
+                          const double* noise, int32_t n_out, double* param_out, double* m_out, double* v_out) {
+    const size_t N = size_t(n), NO = size_t(n_out);
+    int32_t o = 0;
+    auto put = [&](int32_t i, const double* value, bool fresh) {
+        for (int r = 0; r < rows; ++r) {
+            if (o < n_out) {
+                param_out[r * NO + o] = value ? value[r] : param[r * N + i];
+                if (m_out) m_out[r * NO + o] = fresh || !m ? 0.0 : m[r * N + i];
+                if (v_out) v_out[r * NO + o] = fresh || !v ? 0.0 : v[r * N + i];
+            }
+        }
+        ++o;
+    };
+    for (int32_t i = 0; i < n; ++i)
+        if (action[i] == 1 || action[i] == 2) put(i, nullptr, false);
+    for (int32_t i = 0; i < n; ++i)
+        if (action[i] == 2) put(i, nullptr, true);
+    for (int c = 0; c < 2; ++c)
+        for (int32_t i = 0; i < n; ++i) {
+            if (action[i] != 3) continue;
+            double value[64];
+            for (int r = 0; r < rows && r < 64; ++r) value[r] = param[r * N + i];
+            if (kind == 1) {
+                // a sample of N(mean, Sigma_3d): Sigma_3d = R S S^T R^T, so mean + R (s * z)
+                const double qn = std::sqrt(quats[i] * quats[i] + quats[N + i] * quats[N + i] +
+                                            quats[2 * N + i] * quats[2 * N + i] + quats[3 * N + i] * quats[3 * N + i]);
+                double Rq[9];
+                quat_to_rotmat<double>(quats[i] / qn, quats[N + i] / qn, quats[2 * N + i] / qn, quats[3 * N + i] / qn, Rq);
+                double sz[3];
+                for (int k = 0; k < 3; ++k) sz[k] = std::exp(log_scales[k * N + i]) * noise[(size_t(c) * 3 + k) * N + i];
+                for (int r = 0; r < 3; ++r) value[r] += Rq[r * 3 + 0] * sz[0] + Rq[r * 3 + 1] * sz[1] + Rq[r * 3 + 2] * sz[2];
+            } else if (kind == 2) {
+                for (int r = 0; r < 3; ++r) value[r] -= std::log(1.6);
+            }
+            put(i, value, true);
+        }
+    return o;
+}
+
 double orc_quad_min_rect(double A, double B, double C, double x0, double x1, double y0, double y1) {
     return quad_min_rect(A, B, C, x0, x1, y0, y1);
 }

@@ -162,6 +162,18 @@ int64_t orc_bin_ellipse(const orc_camera* cam, int32_t n, const float* means2d, 
 int32_t orc_ellipse_tiles(const orc_camera* cam, float u, float v, float A, float B, float C, float k,
                           int32_t radius, double widen, double margin, int32_t* rect, uint8_t* codes,
                           int64_t max_codes);
+/* c12: densification, decisions in double (3DGS's adaptive density control): action [n] (0 removed,
+ * 1 kept, 2 kept and cloned, 3 split), ambig [n] (may be NULL) marks decisions within a relative
+ * 1e-5 of a threshold, counts [5] = n_out, kept, cloned, split, removed. */
+int orc_densify_classify(int32_t n, const double* accum, const double* count, const double* log_scales,
+                         const double* logits, double grad_threshold, double dense_scale, double min_opacity,
+                         double max_scale, int32_t* action, uint8_t* ambig, int32_t* counts);
+/* One parameter group [rows][n] (rows <= 64) after densification with `action`; kind 0 copy,
+ * 1 means (split children at mean + R(q) (s * z_c), noise [2][3][n]), 2 log-scales (children
+ * log(s / 1.6)).  Returns the number of Gaussians written to the [rows][n_out] outputs. */
+int32_t orc_densify_group(int32_t n, const int32_t* action, int32_t rows, int32_t kind, const double* param,
+                          const double* m, const double* v, const double* quats, const double* log_scales,
+                          const double* noise, int32_t n_out, double* param_out, double* m_out, double* v_out);
 /* Minimum of A x^2 + 2 B x y + C y^2 (positive definite) over [x0, x1] x [y0, y1]. */
 double orc_quad_min_rect(double A, double B, double C, double x0, double x1, double y0, double y1);
 

@@ -71,3 +71,69 @@ def test_densify_stats_match_oracle():
     a_ref, c_ref = oracle.densify_stats(dm2, radius, acc0, cnt0)
     assert np.allclose(acc.cpu().numpy(), a_ref, rtol=1e-6, atol=1e-7)
     assert np.array_equal(cnt.cpu().numpy(), c_ref.astype(np.float32))
+
+
+def densify_inputs(n, seed):
+    rng = np.random.default_rng(seed)
+    f = lambda a: np.ascontiguousarray(a, np.float32)
+    return dict(accum=f(rng.exponential(3e-4, n)), count=f(rng.integers(0, 5, n)),
+                log_scales=f(rng.uniform(np.log(1e-3), np.log(0.8), (3, n))), logits=f(rng.normal(0, 3, n)),
+                quats=f(rng.standard_normal((4, n))), means=f(rng.standard_normal((3, n))),
+                sh=f(rng.standard_normal((48, n))), noise=f(rng.standard_normal((2, 3, n))),
+                m=[f(rng.standard_normal((r, n))) for r in (3, 3, 4, 1, 48)],
+                v=[f(rng.exponential(1.0, (r, n))) for r in (3, 3, 4, 1, 48)])
+
+
+@pytest.mark.parametrize("n", [100_003, 1])
+def test_densify_matches_oracle(n):
+    """rs_densify_plan + rs_densify_apply over five parameter groups (means, log-scales,
+    quaternions, opacity logits, 48 SH coefficients) with their Adam moments, against the oracle:
+    the same fate for every Gaussian whose decisions are not knife edges (at knife edges the GPU's
+    fate is given to the oracle: either is correct); every array and its moments of one length;
+    copies and moments bit for bit; split children's means within float32 rounding of R(q) (s * z)
+    and log-scales within one float32 step of log(s / 1.6)."""
+    TAU, DENSE, MIN_OP, MAX_SC = 2e-4, 0.05, 0.005, 0.5
+    h = densify_inputs(n, seed=3)
+    d = {k: torch.from_numpy(v).cuda() for k, v in h.items() if k not in ("m", "v")}
+    dm = [torch.from_numpy(x).cuda() for x in h["m"]]
+    dv = [torch.from_numpy(x).cuda() for x in h["v"]]
+    ws = torch.empty(rs.rs_densify_workspace_size(n), dtype=torch.uint8, device="cuda")
+    act = torch.full((n,), 255, dtype=torch.uint8, device="cuda")
+    counts = rs.rs_densify_plan(d["accum"], d["count"], d["log_scales"], d["logits"], TAU, DENSE, MIN_OP, MAX_SC, ws,
+                                act)
+    oa, amb, oc = oracle.densify_classify(h["accum"], h["count"], h["log_scales"], h["logits"], TAU, DENSE, MIN_OP,
+                                          MAX_SC)
+    ga = act.cpu().numpy().astype(np.int32)
+    assert np.array_equal(ga[~amb], oa[~amb])
+    assert amb.mean() < 1e-3
+    action = np.where(amb, ga, oa).astype(np.int32)
+    n_out = counts["n_out"]
+    assert n_out == int(((action == 1) | (action == 2)).sum() + (action == 2).sum() + 2 * (action == 3).sum())
+    if not amb.any():
+        assert counts == oc
+    params = [(d["means"], rs.RS_DENSIFY_MEANS), (d["log_scales"], rs.RS_DENSIFY_LOG_SCALES),
+              (d["quats"], rs.RS_DENSIFY_COPY), (d["logits"], rs.RS_DENSIFY_COPY), (d["sh"], rs.RS_DENSIFY_COPY)]
+    groups = []
+    for (p, kind), m, v in zip(params, dm, dv):
+        rows = p.numel() // n
+        o = lambda: torch.full((rows, max(n_out, 1)), float("nan"), device="cuda")
+        groups.append(rs.DensifyGroup(p.contiguous(), o(), m, v, o(), o(), kind))
+    rs.rs_densify_apply(n, ws, d["quats"], d["log_scales"], d["noise"], groups, n_out)
+    torch.cuda.synchronize()
+    host_params = [h["means"], h["log_scales"], h["quats"], h["logits"][None], h["sh"]]
+    for k, (gr, p, m, v) in enumerate(zip(groups, host_params, h["m"], h["v"])):
+        po, mo, vo = oracle.densify_group(action, p, m, v, kind=gr.kind, quats=h["quats"],
+                                          log_scales=h["log_scales"], noise=h["noise"])
+        gp, gm, gv = (x.cpu().numpy()[:, :n_out].astype(np.float64) for x in (gr.param_out, gr.m_out, gr.v_out))
+        assert gp.shape == po.shape == gm.shape == gv.shape  # one length for every array and its moments
+        assert np.array_equal(gm, mo) and np.array_equal(gv, vo), k
+        new = np.zeros(n_out, bool)
+        new[int(((action == 1) | (action == 2)).sum()):] = True
+        split_part = np.zeros(n_out, bool)
+        split_part[n_out - 2 * int((action == 3).sum()):] = True
+        if gr.kind == rs.RS_DENSIFY_COPY:
+            assert np.array_equal(gp, po), k
+        else:
+            assert np.array_equal(gp[:, ~split_part], po[:, ~split_part]), k
+            tol = 1e-6 * (np.abs(po[:, split_part]) + 1.0)
+            assert (np.abs(gp[:, split_part] - po[:, split_part]) <= tol).all(), k
