@@ -1,7 +1,9 @@
-// [1] projection and [5] projection backward: one thread per Gaussian.
+// [1] projection and [5] projection backward.
 //
-// Loads are planar (one coalesced 4-byte row per component), so a warp reads 128 contiguous
-// bytes per row; the kernel is bound by those bytes (about 236 per Gaussian at SH degree 3).
+// Loads are planar (one coalesced row per component).  The projection of the radius-square
+// binning takes RS_PROJ_VEC Gaussians per thread with 8- or 16-byte loads and stores of every row
+// when the rows are aligned for them (k_project_vec), else one per thread with 4-byte accesses
+// (k_project); it is bound by those bytes (about 236 per Gaussian read at SH degree 3).
 // Forward: rigel README "Projection"; "3D Gaussian Splatting ビューワを作る" 2.1-2.3;
 // learn-gs "11 - Tiles" tile_spans.  Backward: rigel README "Backward" and "Deliberate
 // differences from the reference implementation".
@@ -19,6 +21,10 @@ namespace {
 #ifndef RS_PROJ_MIN_BLOCKS
 #define RS_PROJ_MIN_BLOCKS 9
 #endif
+// Gaussians per thread of the vectorised projection (2: 8-byte accesses, 4: 16-byte accesses).
+#ifndef RS_PROJ_VEC
+#define RS_PROJ_VEC 2
+#endif
 constexpr int kProjThreads = RS_PROJ_THREADS;
 constexpr int kProjMinBlocks = RS_PROJ_MIN_BLOCKS;
 
@@ -35,29 +41,34 @@ constexpr float kY3c = 0.4570457994644658f;   // sqrt(21 / (2 pi)) / 4
 constexpr float kY3d = 0.3731763325901154f;   // sqrt(7 / pi) / 4
 constexpr float kY3e = 1.445305721320277f;    // sqrt(105 / pi) / 4
 
+// Every product and sum below is an explicitly rounded single-precision operation (no contraction
+// left to the compiler), so the two projection kernels give bit-identical colours.
+__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
+
 template <int DEG>
 __device__ __forceinline__ void sh_basis(float x, float y, float z, float* Y) {
     Y[0] = kY0;
     if (DEG >= 1) {
-        Y[1] = -kY1 * y;
-        Y[2] = kY1 * z;
-        Y[3] = -kY1 * x;
+        Y[1] = mul_rn(-kY1, y);
+        Y[2] = mul_rn(kY1, z);
+        Y[3] = mul_rn(-kY1, x);
     }
     if (DEG >= 2) {
-        const float xx = x * x, yy = y * y, zz = z * z;
-        Y[4] = kY2a * x * y;
-        Y[5] = -kY2a * y * z;
-        Y[6] = kY2b * (2.f * zz - xx - yy);
-        Y[7] = -kY2a * z * x;
-        Y[8] = kY2c * (xx - yy);
+        const float xx = mul_rn(x, x), yy = mul_rn(y, y), zz = mul_rn(z, z);
+        Y[4] = mul_rn(mul_rn(kY2a, x), y);
+        Y[5] = mul_rn(mul_rn(-kY2a, y), z);
+        Y[6] = mul_rn(kY2b, sub_rn(sub_rn(2.f * zz, xx), yy));
+        Y[7] = mul_rn(mul_rn(-kY2a, z), x);
+        Y[8] = mul_rn(kY2c, sub_rn(xx, yy));
         if (DEG >= 3) {
-            Y[9] = -kY3a * (3.f * xx - yy) * y;
-            Y[10] = kY3b * x * y * z;
-            Y[11] = -kY3c * (4.f * zz - xx - yy) * y;
-            Y[12] = kY3d * z * (2.f * zz - 3.f * xx - 3.f * yy);
-            Y[13] = -kY3c * x * (4.f * zz - xx - yy);
-            Y[14] = kY3e * (xx - yy) * z;
-            Y[15] = -kY3a * x * (xx - 3.f * yy);
+            Y[9] = mul_rn(mul_rn(-kY3a, sub_rn(3.f * xx, yy)), y);
+            Y[10] = mul_rn(mul_rn(mul_rn(kY3b, x), y), z);
+            Y[11] = mul_rn(mul_rn(-kY3c, sub_rn(sub_rn(4.f * zz, xx), yy)), y);
+            Y[12] = mul_rn(mul_rn(kY3d, z), sub_rn(sub_rn(2.f * zz, 3.f * xx), 3.f * yy));
+            Y[13] = mul_rn(mul_rn(-kY3c, x), sub_rn(sub_rn(4.f * zz, xx), yy));
+            Y[14] = mul_rn(mul_rn(kY3e, sub_rn(xx, yy)), z);
+            Y[15] = mul_rn(mul_rn(-kY3a, x), sub_rn(xx, 3.f * yy));
         }
     }
 }
@@ -220,15 +231,15 @@ __device__ __forceinline__ void geometry(const CameraF& cam, const float m[3], c
     G.visible = true;
 }
 
+// Unit direction from the camera centre -R^T t to the mean, with explicit operations (as sh_basis).
 __device__ __forceinline__ void view_dir(const CameraF& cam, const float m[3], float d[3], float& len) {
-    // camera centre -R^T t
-    const float C0 = -(cam.R[0] * cam.t[0] + cam.R[3] * cam.t[1] + cam.R[6] * cam.t[2]);
-    const float C1 = -(cam.R[1] * cam.t[0] + cam.R[4] * cam.t[1] + cam.R[7] * cam.t[2]);
-    const float C2 = -(cam.R[2] * cam.t[0] + cam.R[5] * cam.t[1] + cam.R[8] * cam.t[2]);
-    d[0] = m[0] - C0; d[1] = m[1] - C1; d[2] = m[2] - C2;
-    len = sqrtf(d[0] * d[0] + d[1] * d[1] + d[2] * d[2]);
-    const float il = len > 0.f ? 1.0f / len : 0.f;
-    d[0] *= il; d[1] *= il; d[2] *= il;
+    const float C0 = -fmaf(cam.R[6], cam.t[2], fmaf(cam.R[3], cam.t[1], mul_rn(cam.R[0], cam.t[0])));
+    const float C1 = -fmaf(cam.R[7], cam.t[2], fmaf(cam.R[4], cam.t[1], mul_rn(cam.R[1], cam.t[0])));
+    const float C2 = -fmaf(cam.R[8], cam.t[2], fmaf(cam.R[5], cam.t[1], mul_rn(cam.R[2], cam.t[0])));
+    d[0] = sub_rn(m[0], C0); d[1] = sub_rn(m[1], C1); d[2] = sub_rn(m[2], C2);
+    len = __fsqrt_rn(fmaf(d[2], d[2], fmaf(d[1], d[1], mul_rn(d[0], d[0]))));
+    const float il = len > 0.f ? __fdiv_rn(1.0f, len) : 0.f;
+    d[0] = mul_rn(d[0], il); d[1] = mul_rn(d[1], il); d[2] = mul_rn(d[2], il);
 }
 
 template <int DEG>
@@ -328,6 +339,157 @@ __global__ void __launch_bounds__(kProjThreads, kProjMinBlocks) k_project(Camera
     r.q = make_float4(-0.5f * kLog2e * G.A, -kLog2e * G.B, -0.5f * kLog2e * G.C, ext_y);
     r.c = make_float4(rgb[0], rgb[1], rgb[2], 1.0f / o);
     rec[i] = r;
+}
+
+// The projection of V (2 or 4) consecutive Gaussians per thread with 8- or 16-byte loads and
+// stores of every planar row (a warp moves 256 or 512 contiguous bytes per row and instruction):
+// the same per-Gaussian arithmetic as k_project (geometry, SH colour, record), for the
+// radius-square tile test, when n is a multiple of V and every row is 4V-byte aligned.  The SH rows
+// are read once any of the V is visible.
+template <int V>
+struct VecF;
+template <>
+struct VecF<2> {
+    float v[2];
+    __device__ __forceinline__ static VecF load(const float* p) {
+        const float2 t = __ldg(reinterpret_cast<const float2*>(p));
+        return VecF{{t.x, t.y}};
+    }
+    __device__ __forceinline__ static void store(float* p, const float (&a)[2]) {
+        *reinterpret_cast<float2*>(p) = make_float2(a[0], a[1]);
+    }
+    __device__ __forceinline__ static void store_i(int* p, const int (&a)[2]) {
+        *reinterpret_cast<int2*>(p) = make_int2(a[0], a[1]);
+    }
+    __device__ __forceinline__ static void store_u(uint32_t* p, const uint32_t (&a)[2]) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(a[0], a[1]);
+    }
+};
+template <>
+struct VecF<4> {
+    float v[4];
+    __device__ __forceinline__ static VecF load(const float* p) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(p));
+        return VecF{{t.x, t.y, t.z, t.w}};
+    }
+    __device__ __forceinline__ static void store(float* p, const float (&a)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(a[0], a[1], a[2], a[3]);
+    }
+    __device__ __forceinline__ static void store_i(int* p, const int (&a)[4]) {
+        *reinterpret_cast<int4*>(p) = make_int4(a[0], a[1], a[2], a[3]);
+    }
+    __device__ __forceinline__ static void store_u(uint32_t* p, const uint32_t (&a)[4]) {
+        *reinterpret_cast<uint4*>(p) = make_uint4(a[0], a[1], a[2], a[3]);
+    }
+};
+
+template <int DEG, int V>
+__global__ void __launch_bounds__(kProjThreads) k_project_vec(CameraF cam, int n, const float* __restrict__ means,
+                                                             const float* __restrict__ scales,
+                                                             const float* __restrict__ quats,
+                                                             const float* __restrict__ opacity,
+                                                             const float* __restrict__ sh,
+                                                             const float* __restrict__ colors, float* means2d,
+                                                             float* depth, float* conic, float* color, int* radius,
+                                                             uint32_t* tiles, Record* rec) {
+    RS_PDL_ENTER();
+    using L = VecF<V>;
+    const int i0 = V * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i0 >= n) return;
+    const size_t N = size_t(n);
+    auto row = [&](const float* base, size_t r) { return L::load(base + r * N + size_t(i0)); };
+    const L M0 = row(means, 0), M1 = row(means, 1), M2 = row(means, 2);
+    const L S0 = row(scales, 0), S1 = row(scales, 1), S2 = row(scales, 2);
+    const L Q0 = row(quats, 0), Q1 = row(quats, 1), Q2 = row(quats, 2), Q3 = row(quats, 3);
+    const L O = row(opacity, 0);
+    float u[V], v[V], z[V], cA[V], cB[V], cC[V], ex[V], ey[V], dir[V][3];
+    int rad[V];
+    uint32_t nt[V];
+    bool vis[V], any = false;
+#pragma unroll
+    for (int g = 0; g < V; ++g) {
+        const float m[3] = {M0.v[g], M1.v[g], M2.v[g]};
+        const float sc[3] = {S0.v[g], S1.v[g], S2.v[g]};
+        const float q[4] = {Q0.v[g], Q1.v[g], Q2.v[g], Q3.v[g]};
+        Geo G;
+        geometry(cam, m, sc, q, G);
+        vis[g] = G.visible;
+        any |= G.visible;
+        u[g] = G.visible ? G.u : 0.f;
+        v[g] = G.visible ? G.v : 0.f;
+        z[g] = G.visible ? G.p[2] : 0.f;
+        cA[g] = G.visible ? G.A : 0.f;
+        cB[g] = G.visible ? G.B : 0.f;
+        cC[g] = G.visible ? G.C : 0.f;
+        rad[g] = G.visible ? G.radius : 0;
+        nt[g] = G.visible ? uint32_t(G.rect[1] - G.rect[0]) * uint32_t(G.rect[3] - G.rect[2]) : 0u;
+        // the alpha >= 1/255 box (as k_project)
+        const float o255 = 255.f * O.v[g];
+        ex[g] = -1.f;
+        ey[g] = -1.f;
+        if (G.visible && o255 > 1.f) {
+            const float k = 2.002f * logf(o255);
+            ex[g] = sqrtf(k * G.a) + 0.01f;
+            ey[g] = sqrtf(k * G.c) + 0.01f;
+        }
+        float len;
+        view_dir(cam, m, dir[g], len);
+    }
+    float rgb[V][3];
+#pragma unroll
+    for (int g = 0; g < V; ++g) rgb[g][0] = rgb[g][1] = rgb[g][2] = 0.f;
+    if (any) {
+        if (DEG < 0) {
+#pragma unroll
+            for (int ch = 0; ch < 3; ++ch) {
+                const L c = row(colors, ch);
+#pragma unroll
+                for (int g = 0; g < V; ++g) rgb[g][ch] = c.v[g];
+            }
+        } else {
+            constexpr int K = (DEG + 1) * (DEG + 1);
+            float Y[V][16];
+#pragma unroll
+            for (int g = 0; g < V; ++g) sh_basis<(DEG < 0 ? 0 : DEG)>(dir[g][0], dir[g][1], dir[g][2], Y[g]);
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+#pragma unroll
+                for (int ch = 0; ch < 3; ++ch) {
+                    const L c = row(sh, size_t(k * 3 + ch));
+#pragma unroll
+                    for (int g = 0; g < V; ++g) rgb[g][ch] = fmaf(c.v[g], Y[g][k], rgb[g][ch]);
+                }
+            }
+        }
+    }
+    float c0[V], c1[V], c2[V];
+#pragma unroll
+    for (int g = 0; g < V; ++g) {
+        c0[g] = vis[g] ? rgb[g][0] : 0.f;
+        c1[g] = vis[g] ? rgb[g][1] : 0.f;
+        c2[g] = vis[g] ? rgb[g][2] : 0.f;
+    }
+    L::store(means2d + i0, u);
+    L::store(means2d + N + i0, v);
+    L::store(depth + i0, z);
+    L::store(conic + i0, cA);
+    L::store(conic + N + i0, cB);
+    L::store(conic + 2 * N + i0, cC);
+    L::store(color + i0, c0);
+    L::store(color + N + i0, c1);
+    L::store(color + 2 * N + i0, c2);
+    L::store_i(radius + i0, rad);
+    L::store_u(tiles + i0, nt);
+#pragma unroll
+    for (int g = 0; g < V; ++g) {
+        if (!vis[g]) continue;
+        const float o = O.v[g];
+        Record r;
+        r.p = make_float4(u[g], v[g], o, ex[g]);
+        r.q = make_float4(-0.5f * kLog2e * cA[g], -kLog2e * cB[g], -0.5f * kLog2e * cC[g], ey[g]);
+        r.c = make_float4(c0[g], c1[g], c2[g], 1.0f / o);
+        rec[i0 + g] = r;
+    }
 }
 
 template <int DEG>
@@ -503,8 +665,31 @@ cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_p
                            cudaStream_t s) {
     if (g.n == 0) return cudaSuccess;
     const int threads = kProjThreads;
-    const int blocks = (g.n + threads - 1) / threads;
     Record* rec = reinterpret_cast<Record*>(o.d_records);
+    // RS_PROJ_VEC Gaussians per thread (2 or 4) when the rows allow it, else one
+    constexpr int V = RS_PROJ_VEC;
+    auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & uintptr_t(4 * V - 1)) == 0; };
+    const bool vec = o.tile_test == RS_TILE_TEST_SQUARE && g.n % V == 0 && al(g.d_means) && al(g.d_scales) &&
+                     al(g.d_quats) && al(g.d_opacity) && al(g.sh_degree >= 0 ? g.d_sh : g.d_colors) &&
+                     al(o.d_means2d) && al(o.d_depth) && al(o.d_conic) && al(o.d_color) && al(o.d_radius) &&
+                     al(o.d_tiles_touched);
+    if (vec) {
+        const int blocks_v = (g.n / V + threads - 1) / threads;
+#define RS_PROJECT_VEC(D)                                                                          \
+    pdl_launch(k_project_vec<D, V>, blocks_v, threads, 0, s, cam, g.n, g.d_means, g.d_scales, g.d_quats,  \
+               g.d_opacity, g.d_sh, g.d_colors, o.d_means2d, o.d_depth, o.d_conic, o.d_color, o.d_radius, \
+               o.d_tiles_touched, rec)
+        switch (g.sh_degree) {
+            case -1: RS_PROJECT_VEC(-1); break;
+            case 0: RS_PROJECT_VEC(0); break;
+            case 1: RS_PROJECT_VEC(1); break;
+            case 2: RS_PROJECT_VEC(2); break;
+            default: RS_PROJECT_VEC(3); break;
+        }
+#undef RS_PROJECT_VEC
+        return cudaGetLastError();
+    }
+    const int blocks = (g.n + threads - 1) / threads;
 #define RS_PROJECT(D)                                                                           \
     pdl_launch(k_project<D>, blocks, threads, 0, s, cam, g.n, g.d_means, g.d_scales, g.d_quats,         \
                                              g.d_opacity, g.d_sh, g.d_colors, o.d_means2d,      \
