@@ -39,16 +39,23 @@ WIDTH, HEIGHT, VIEWS = 1920, 1080, 60
 # GB300: 152 SMs, 128 FP32 lanes and 16 MUFU lanes per SM, 2070 MHz maximum SM clock.
 SMS, FP32_LANES, MUFU_LANES, MAX_MHZ = 152, 128, 16, 2070.0
 
-# Algorithmic work per unit (counted from the method's formulas, rigel README "Rasterization"
-# and "Backward"; one FP32 instruction = one op, FMA included):
-#   forward, per examined entry: dx, dy (2), quadratic form (5), o*G (1), min (1), skip test (1)
-#            = 10 ops + 1 ex2; per composited entry: a*T (1), colour (3), T update (1), stop test (1)
-#   backward, per examined entry: the same 10 ops + 1 ex2; per composited entry: 1-a (1),
-#            T/(1-a) (1 + 1 rcp), a*T (1), colour grads (3), dL/da (7), colour behind (6),
-#            clamp test (1), dL/do (1), dL/dpower (1), conic (6), mean (6), per-pixel sums (9)
-#            = 43 ops + 1 rcp.
+# Algorithmic work per unit, counted from the oracle's statement of the method (rigel README
+# "Rasterization" and "Backward"): one FP32 instruction = one op, a multiply-add fused into one FMA,
+# per-Gaussian constants (the conic scaled by -1/2 and -1, the opacity) computed once per Gaussian.
+#   examined entry (forward and backward alike): dx, dy (2); the power as a quadratic in dx, dy
+#     with the precomputed coefficients (5); opacity * exp (1); min with 0.99 (1); the 1/255 skip
+#     test (1) = 10 ops + 1 exp.
+#   composited entry, forward: alpha T (1); C += c alpha T per channel (3); T (1 - alpha) as
+#     T - alpha T (1); the T < 1e-4 stop test (1) = 6 ops.
+#   composited entry, backward (the oracle's per-channel recurrence): 1 - alpha (1) and
+#     T_j = T / (1 - alpha) (1 + 1 reciprocal); dL/dc_ch += alpha T_j G_ch: alpha T_j (1) + 3 FMA;
+#     dL/dalpha += G_ch (c_ch T_j - S_ch / (1 - alpha)) per channel: 2 products, 1 difference,
+#     1 FMA (12); S_ch += c_ch alpha T_j (3); the clamp test (1); dL/do += G dL/dalpha (1);
+#     g = (o G) dL/dalpha (1); dA += -dx^2 g / 2, dB += -dx dy g, dC += -dy^2 g / 2 (h = -g/2,
+#     h dx, h dy, 2 h dx, then three FMA = 7); du += g (A dx + B dy), dv += g (C dy + B dx)
+#     (3 each, 6) = 37 ops + 1 reciprocal.
 OPS_FWD_EXAMINED, OPS_FWD_BLEND = 10, 6
-OPS_BWD_EXAMINED, OPS_BWD_BLEND = 10, 43
+OPS_BWD_EXAMINED, OPS_BWD_BLEND = 10, 37
 # bytes (algorithmic, moved once)
 B_PROJECT_PER_G = 236 + 44          # SH degree 3 inputs + means2d/depth/conic/colour/radius/tiles
 B_PROJECT_BWD_PER_G = 504
