@@ -109,6 +109,8 @@ def parse():
                     help="skip the training-shaped step's stage timings (reported beside the line)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration timings (tiny, 720x720, 1280x720 and 1920x1080 orbits, 1M)")
+    ap.add_argument("--configs", default=",".join(CONFIG_NAMES),
+                    help="which configurations to time (comma-separated names, default all)")
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -449,7 +451,8 @@ def run_ours(args):
     # process touches the GPU; they overlap the GPU timing and are collected at the end
     worker = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        worker = start_oracle_worker(CONFIG_NAMES if not args.no_configs else ("C3b",))
+        worker = start_oracle_worker(tuple(dict.fromkeys(
+            ["C3b"] + ([c for c in args.configs.split(",") if c] if not args.no_configs else []))))
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     if world > 1 and not dist.is_initialized():
@@ -631,7 +634,9 @@ def run_ours(args):
     result["peaks"] = {k: v for k, v in peaks.items()}
     configs = {}
     if world == 1 and not args.no_configs:
-        for name in CONFIG_NAMES:
+        for name in [c for c in args.configs.split(",") if c]:
+            if name not in CONFIG_NAMES:
+                raise SystemExit(f"unknown configuration {name!r} (have {', '.join(CONFIG_NAMES)})")
             configs[name] = time_config(name, device, flush)
 
     if not args.no_e2e:

@@ -58,7 +58,10 @@ constexpr uint32_t kFlagIncl = 2u << 30;   // status word: count of this and eve
 constexpr uint32_t kFlagMask = 3u << 30;
 constexpr uint32_t kCountMask = (1u << 30) - 1u;
 constexpr int kMaxSpins = 1 << 20;         // bound on one look-back wait (then give up, flag it)
-constexpr int kWindow = 32;                // predecessors whose status words are read together
+#ifndef RS_LOOKBACK_WINDOW
+#define RS_LOOKBACK_WINDOW 32
+#endif
+constexpr int kWindow = RS_LOOKBACK_WINDOW;  // predecessors whose status words are read together
 
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
     uint32_t v;
@@ -601,13 +604,36 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
             }
         }
         __syncthreads();
+        // the square test: warp v takes the chunk's entries [v CH/8, (v + 1) CH/8) 32 at a time
+        // (lane l on entry 32 k + l of its run, so the stores stay consecutive); a lane finds the
+        // owner of its first entry by binary search and then walks it forward past the few
+        // Gaussians whose slices start between its successive entries.  The ellipse path keeps the
+        // interleaved order (entry k 256 + t) of its row tables.
+        const uint32_t run0 = ELL ? e0 + threadIdx.x : e0 + (threadIdx.x >> 5) * uint32_t(CH / (kExpThreads / 32)) + lane;
+        int owner = -1;
 #pragma unroll
         for (int k = 0; k < CH / kExpThreads; ++k) {
-            const uint32_t e = e0 + k * kExpThreads + threadIdx.x;
+            const uint32_t e = ELL ? run0 + uint32_t(k * kExpThreads) : run0 + uint32_t(32 * k);
             const bool valid = e < E;
             uint32_t tile = 0u;
             uint32_t gid = 0u;
-            if (valid && ELL && table) {
+            if (valid && !ELL) {
+                if (owner < 0) {
+                    int lo = 0, hi = w;  // s_start[lo] <= e < s_start[hi]
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (s_start[mid] <= e) lo = mid; else hi = mid;
+                    }
+                    owner = lo;
+                } else {
+                    while (s_start[owner + 1] <= e) ++owner;  // s_start[w] lies past the chunk
+                }
+                const uint32_t kk = uint32_t(uint64_t(e) - s_start[owner]);
+                gid = s_g[owner];
+                const uint2 r = s_rect[owner];
+                const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
+                tile = ty * uint32_t(cam.TX) + tx;
+            } else if (valid && ELL && table) {
                 // the window's rows in entry order: the last row starting at or before e
                 const uint32_t off = uint32_t(uint64_t(e) - s_start[0]);
                 int a = 0, b = int(s_rowstart[w]);
