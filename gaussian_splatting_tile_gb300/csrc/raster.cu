@@ -28,8 +28,8 @@ constexpr int kFwdThreads = kTilePixels;  // the forward: one block of 256 threa
 constexpr int kFwdWarps = kFwdThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Backward: 1 takes the hit entries two at a time and, where both have composited pixels, reduces
-// their sums together (reduce18); 0 reduces entry by entry (butterfly9).
+// Backward: 1 takes the hit entries two at a time and reduces their sums together (reduce18); 0
+// reduces entry by entry (butterfly9).
 #ifndef RS_BWD_PAIR
 #define RS_BWD_PAIR 1
 #endif
@@ -38,10 +38,10 @@ constexpr unsigned kFull = 0xffffffffu;
 #ifndef RS_FWD_MIN_BLOCKS
 #define RS_FWD_MIN_BLOCKS 6
 #endif
-// backward (128-thread blocks): 7 with paired entries (72 registers; 6: 0.257 ms, 8: 0.260,
-// 7: 0.251 on the 160k 1080p orbit), 8 without (64 registers)
+// backward (128-thread blocks): 8 (62 registers with paired entries; 7 lets it take 72 and
+// measured 0.243 against 0.233 ms on the 160k 1080p orbit)
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : RS_BWD_PAIR ? 7 : 8)
+#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : 8)
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -385,7 +385,7 @@ __device__ __forceinline__ float* sum_dst(int slot, size_t N, float* dm2, float*
 // into the warp's own shared-memory slots; the hits are evaluated one after another by all 64
 // pixels.  The two pixels of a lane share their
 // column, so their nine sums fold before a reduce-scatter over the warp (two consecutive hits'
-// sums in one, where both have composited pixels), and one lane per sum adds it to the
+// sums in one), and one lane per sum adds it to the
 // Gaussian's gradient with a global atomic.  There is no block-wide barrier.
 // Pixels per lane, stacked 4 rows apart in one column (2: warps of 8x8; 4: warps of 8x16, which
 // cut the warp-entries by a third but measured 0.293 -> 0.303 ms with more registers per lane).
@@ -406,16 +406,18 @@ struct BwdPixel {
 };
 
 // One entry at one pixel: updates the pixel's state; returns gp = dL/dpower (0 if clamped) and
-// w = alpha T_j.
-__device__ __forceinline__ void bwd_step(BwdPixel& px, float alpha, float raw, const float4& c, float& gp,
-                                         float& w) {
-    const float one_m = 1.f - alpha;
-    const float Tj = __fdividef(px.T, one_m);
-    w = alpha * Tj;
+// w = alpha T_j.  Branch-free: a pixel the entry does not reach (act false) takes alpha as 0, so
+// SG + 0 d = SG and w = gp = 0, and keeps T through the select; an active pixel gets exactly the
+// arithmetic of the recurrence.
+__device__ __forceinline__ void bwd_step(BwdPixel& px, bool act, float alpha, float raw, const float4& c,
+                                         float& gp, float& w) {
+    const float a = act ? alpha : 0.f;
+    const float Tj = act ? px.T * rcp_approx(1.f - alpha) : px.T;
+    w = a * Tj;
     const float cG = fmaf(c.x, px.G0, fmaf(c.y, px.G1, c.z * px.G2));
     // dL/dalpha = Tj (cG - SG), and the entry's own colour joins SG: SG + alpha (cG - SG)
     const float d = cG - px.SG;
-    px.SG = fmaf(alpha, d, px.SG);
+    px.SG = fmaf(a, d, px.SG);
     px.T = Tj;
     gp = raw <= kAlphaMax ? w * d : 0.f;  // alpha dL/dalpha; not clamped: alpha = opacity exp(power)
 }
@@ -430,6 +432,9 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     RS_PDL_ENTER();
     __shared__ float4 s_p[kBwdWarps][32], s_q[kBwdWarps][32], s_c[kBwdWarps][32];
     __shared__ uint32_t s_g[kBwdWarps][32];
+    // per staged entry, the factors of its sums in the gradient: (dA-row and dC-row factors of
+    // du and dv, 1 / opacity, the B factor), see the comment on `slot` below
+    __shared__ float4 s_k[kBwdWarps][32];
     const uint32_t n_tiles = uint32_t(cam.TX) * uint32_t(cam.TY);
     const uint32_t a0 = blockIdx.x * kChunk, a1 = a0 + kChunk;
     // the tile holding position a0; a chunk past the end of the list has none
@@ -526,11 +531,12 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                     s_q[warp][lane] = q;
                     s_c[warp][lane] = c;
                     s_g[warp][lane] = g;
+                    s_k[warp][lane] = make_float4(-2.f * kLn2 * q.x, -2.f * kLn2 * q.z, c.w, -kLn2 * q.y);
                 }
             }
             uint32_t m = __ballot_sync(kFull, hit);
             __syncwarp();
-            // entry j at the lane's pixels: updates their state, returns whether any composited
+            // entry j at the lane's pixels: updates their state
             auto step = [&](int j, float& dx, float (&dy)[kBwdPx], float (&gp)[kBwdPx], float (&w)[kBwdPx]) {
                 const uint32_t ej = lo + uint32_t(j);
                 const float4 p = s_p[warp][j], q = s_q[warp][j];
@@ -538,20 +544,14 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 // arithmetic as entry_alpha, pixel by pixel)
                 dx = fx - p.x;
                 const float bx = q.y * dx, axx = (q.x * dx) * dx;
-                bool any = false;
                 const float4 c = s_c[warp][j];
 #pragma unroll
                 for (int h = 0; h < kBwdPx; ++h) {
                     dy[h] = (fy0 + float(4 * h)) - p.y;
                     const float raw = p.z * ex2_approx(fmaf(dy[h], fmaf(q.z, dy[h], bx), axx));
                     const float al = fminf(kAlphaMax, raw);
-                    const bool act = ej < P[h].end && al >= kAlphaMin;
-                    gp[h] = 0.f;
-                    w[h] = 0.f;
-                    if (act) bwd_step(P[h], al, raw, c, gp[h], w[h]);
-                    any |= act;
+                    bwd_step(P[h], ej < P[h].end && al >= kAlphaMin, al, raw, c, gp[h], w[h]);
                 }
-                return any;
             };
             // the lane's pixels share dx: their sums fold before the reduction over the warp
             auto fold = [&](float dx, const float (&dy)[kBwdPx], const float (&gp)[kBwdPx], const float (&w)[kBwdPx],
@@ -586,49 +586,40 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 const float sum = butterfly9(v, lane);
                 const float other = __shfl_xor_sync(kFull, sum, 2);  // slots 0 and 1: lanes 0 and 2
                 if (slot >= 0) {
-                    const float4 q = s_q[warp][j];
-                    const float B = -kLn2 * q.y;
-                    const float a = slot == 0 ? -2.f * kLn2 * q.x : slot == 1 ? -2.f * kLn2 * q.z
-                                  : slot == 5 ? s_c[warp][j].w : kconst;
-                    atomicAdd(dst + s_g[warp][j], fmaf(a, sum, slot < 2 ? B * other : 0.f));
+                    const float4 f = s_k[warp][j];
+                    const float a = slot == 0 ? f.x : slot == 1 ? f.y : slot == 5 ? f.z : kconst;
+                    atomicAdd(dst + s_g[warp][j], fmaf(a, sum, slot < 2 ? f.w * other : 0.f));
                 }
             };
+            // every hit has a composited pixel in this area (the forward's flags), so each one's sums
+            // go out without a vote; the hits are taken two at a time (back to front), their 18 sums
+            // in one reduction, an odd last one alone
             while (m) {
                 const int j = 31 - __clz(m);
                 m ^= 1u << j;
                 float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
-                const bool any = step(j, dx, dy, gp, w);
+                step(j, dx, dy, gp, w);
 #if RS_BWD_PAIR
                 if (m) {
-                    // the next hit (in front of j) as well, and both entries' sums in one reduction
                     const int k = 31 - __clz(m);
                     m ^= 1u << k;
                     float dx2, dy2[kBwdPx], gp2[kBwdPx], w2[kBwdPx];
-                    const bool any2 = step(k, dx2, dy2, gp2, w2);
-                    const bool r1 = __any_sync(kFull, any), r2 = __any_sync(kFull, any2);
-                    if (r1 && r2) {
-                        float v[kSums], u[kSums];
-                        fold(dx, dy, gp, w, v);
-                        fold(dx2, dy2, gp2, w2, u);
-                        const float sum = reduce18(v, u, lane);
-                        const float other = __shfl_xor_sync(kFull, sum, 1);  // slots 0 and 1: lanes 2i, 2i + 1
-                        if (pslot >= 0) {
-                            const int jj = psecond ? k : j;
-                            const float4 q = s_q[warp][jj];
-                            const float B = -kLn2 * q.y;
-                            const float a = pslot == 0 ? -2.f * kLn2 * q.x : pslot == 1 ? -2.f * kLn2 * q.z
-                                          : pslot == 5 ? s_c[warp][jj].w : pconst;
-                            atomicAdd(pdst + s_g[warp][jj], fmaf(a, sum, pslot < 2 ? B * other : 0.f));
-                        }
-                    } else if (r1) {
-                        reduce_one(j, dx, dy, gp, w);
-                    } else if (r2) {
-                        reduce_one(k, dx2, dy2, gp2, w2);
+                    step(k, dx2, dy2, gp2, w2);
+                    float v[kSums], u[kSums];
+                    fold(dx, dy, gp, w, v);
+                    fold(dx2, dy2, gp2, w2, u);
+                    const float sum = reduce18(v, u, lane);
+                    const float other = __shfl_xor_sync(kFull, sum, 1);  // slots 0 and 1: lanes 2i, 2i + 1
+                    if (pslot >= 0) {
+                        const int jj = psecond ? k : j;
+                        const float4 f = s_k[warp][jj];
+                        const float a = pslot == 0 ? f.x : pslot == 1 ? f.y : pslot == 5 ? f.z : pconst;
+                        atomicAdd(pdst + s_g[warp][jj], fmaf(a, sum, pslot < 2 ? f.w * other : 0.f));
                     }
                     continue;
                 }
 #endif
-                if (__any_sync(kFull, any)) reduce_one(j, dx, dy, gp, w);
+                reduce_one(j, dx, dy, gp, w);
             }
             __syncwarp();  // the slots are read before the next batch overwrites them
             hi = lo;

@@ -100,6 +100,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// 1 / x by the approximate reciprocal instruction (PTX rcp.approx.ftz.f32: relative error below
+// 2^-23 for normal x; the compositing backward's divisor 1 - alpha lies in [0.01, 1]).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // alpha of one list entry at pixel (px, py), shared by the forward and the backward so both
 // take identical skip, clamp and stop decisions (rigel README "Rasterization":
 // alpha = min(0.99, opacity exp(power)), power = -1/2 (A dx^2 + C dy^2) - B dx dy, here in log2
