@@ -94,7 +94,7 @@ __device__ __forceinline__ uint32_t warp_mask_exact(uint32_t m, const float4& p,
     constexpr float kLog2_255 = 7.994353436858858f;
     constexpr float kMargin = 0.02f;  // log2 units: 1.4% of alpha
     const float thr = __log2f(c.w) - kLog2_255 - kMargin;  // c.w = 1 / opacity
-    const float rx = __frcp_rn(2.f * q.x), rz = __frcp_rn(2.f * q.z);
+    const float rx = rcp_approx(2.f * q.x), rz = rcp_approx(2.f * q.z);
     uint32_t keep = 0u;
     for (uint32_t mm = m; mm;) {
         const int r = __ffs(mm) - 1;
@@ -205,11 +205,8 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
         if (__all_sync(kFull, done)) continue;
         const int nl = compact_warp(my_list, [&](int j) { return (sm.mask[j] & wbit) != 0u; });
         if (done) continue;
-        for (int k = 0; k < nl; ++k) {
-            const int j = my_list[k];
-            float dx, dy, G, raw;
-            const float alpha = entry_alpha(sm.p[j], sm.q[j], fx, fy, dx, dy, G, raw);
-            if (alpha < kAlphaMin) continue;
+        // entry j composited at this pixel; returns true when the pixel is done
+        auto blend = [&](int j, float alpha) {
             sm.comp[warp][j] = 1u;  // every lane that composites stores the same flag
             const float4 c = sm.c[j];
             const float w = alpha * T;
@@ -225,8 +222,26 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
             if (T < kTStop) {
                 done = true;
                 stop = base + uint32_t(j) + 1u;
-                break;
             }
+            return done;
+        };
+        // two entries per step: one list load, and the second alpha evaluated while the first
+        // blends (the blends stay in list order)
+        int k = 0;
+        for (; k + 1 < nl; k += 2) {
+            const uint32_t jj = *reinterpret_cast<const uint16_t*>(my_list + k);
+            const int j0 = int(jj & 0xffu), j1 = int(jj >> 8);
+            float dx, dy, G, raw;
+            const float a0 = entry_alpha(sm.p[j0], sm.q[j0], fx, fy, dx, dy, G, raw);
+            const float a1 = entry_alpha(sm.p[j1], sm.q[j1], fx, fy, dx, dy, G, raw);
+            if (a0 >= kAlphaMin && blend(j0, a0)) break;
+            if (a1 >= kAlphaMin && blend(j1, a1)) break;
+        }
+        if (k < nl && !done) {
+            const int j = my_list[k];
+            float dx, dy, G, raw;
+            const float a = entry_alpha(sm.p[j], sm.q[j], fx, fy, dx, dy, G, raw);
+            if (a >= kAlphaMin) blend(j, a);
         }
     }
     __syncthreads();
