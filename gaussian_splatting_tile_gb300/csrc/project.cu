@@ -1,12 +1,16 @@
 // [1] projection and [5] projection backward.
 //
 // Loads are planar (one coalesced row per component).  The projection of the radius-square
-// binning takes RS_PROJ_VEC Gaussians per thread with 8- or 16-byte loads and stores of every row
-// when the rows are aligned for them (k_project_vec), else one per thread with 4-byte accesses
-// (k_project); it is bound by those bytes (about 236 per Gaussian read at SH degree 3).
+// binning stages each tile's input rows in shared memory by bulk copies when n is a multiple of 4
+// and the rows are 16-byte aligned (k_project_staged), else takes RS_PROJ_VEC Gaussians per thread
+// with 8- or 16-byte loads and stores of every row when the rows allow it (k_project_vec), else
+// one per thread with 4-byte accesses (k_project); its input is about 236 bytes per Gaussian at SH
+// degree 3.
 // Forward: rigel README "Projection"; "3D Gaussian Splatting ビューワを作る" 2.1-2.3;
 // learn-gs "11 - Tiles" tile_spans.  Backward: rigel README "Backward" and "Deliberate
 // differences from the reference implementation".
+#include <algorithm>
+
 #include "rs_internal.cuh"
 
 namespace rs {
@@ -20,6 +24,11 @@ namespace {
 #endif
 #ifndef RS_PROJ_MIN_BLOCKS
 #define RS_PROJ_MIN_BLOCKS 9
+#endif
+// 1: the square-test projection stages its input rows in shared memory with bulk copies
+// (k_project_staged) when n and the rows allow it.
+#ifndef RS_PROJ_STAGED
+#define RS_PROJ_STAGED 1
 #endif
 // Gaussians per thread of the vectorised projection (2: 8-byte accesses, 4: 16-byte accesses).
 #ifndef RS_PROJ_VEC
@@ -492,6 +501,215 @@ __global__ void __launch_bounds__(kProjThreads) k_project_vec(CameraF cam, int n
     }
 }
 
+// ---------------------------------------------------------------- staged projection
+// The projection with every planar input row of a tile of Gaussians copied to shared memory
+// by bulk asynchronous copies (PTX cp.async.bulk, completion counted in bytes on an mbarrier),
+// one thread per Gaussian: the 11 geometry rows on one barrier, the colour rows (48 SH rows at
+// degree 3) on a second, so the geometry starts while the colour rows are still in flight.  A
+// persistent grid walks the tiles (with two buffers the next tile's rows are requested before the
+// current one is computed), so the input streams in bulk instead of in two dependent round trips
+// per thread.  Same arithmetic as k_project, Gaussian by Gaussian.
+// Taken when n is a multiple of 4 and every input row is 16-byte aligned (the copies' rule).
+// Tiles of 64 Gaussians, one buffer, 14 CTAs per SM (15 KB each at degree 3) measured 12.3 us per
+// 160k-Gaussian launch under ncu, against 14.3 (128, two buffers, 3 CTAs), 13.1 (128, one, 7)
+// and 14.5 (64, two, 7): the per-Gaussian arithmetic needs the warps more than the copies need a
+// second buffer.
+#ifndef RS_PROJ_STAGE_THREADS
+#define RS_PROJ_STAGE_THREADS 64
+#endif
+#ifndef RS_PROJ_STAGE_BUFS
+#define RS_PROJ_STAGE_BUFS 1
+#endif
+#ifndef RS_PROJ_STAGE_BLOCKS
+#define RS_PROJ_STAGE_BLOCKS 14
+#endif
+constexpr int kStgThreads = RS_PROJ_STAGE_THREADS;   // Gaussians per tile, one per thread
+constexpr int kStgBufs = RS_PROJ_STAGE_BUFS;         // 2: the next tile's rows requested ahead
+constexpr int kStgBlocksPerSM = RS_PROJ_STAGE_BLOCKS;
+static_assert(kStgBufs == 1 || kStgBufs == 2, "one or two buffers");
+constexpr int kStgGeoRows = 11;  // means 3, scales 3, quats 4, opacity 1
+constexpr uint32_t kStgWaitLimit = 1u << 22;
+
+template <int DEG>
+__host__ __device__ constexpr int stg_rows() {
+    return kStgGeoRows + (DEG < 0 ? 3 : 3 * (DEG + 1) * (DEG + 1));
+}
+
+__device__ unsigned int g_proj_error;  // set when a bounded wait on a staged copy gave up
+
+__device__ __forceinline__ void stg_mbar_init(uint32_t mbar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ void stg_expect(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void stg_copy(uint32_t dst, const float* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+__device__ __forceinline__ bool stg_wait(uint32_t mbar, uint32_t parity) {
+    for (uint32_t i = 0; i < kStgWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(mbar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+template <int DEG>
+__global__ void __launch_bounds__(kStgThreads) k_project_staged(CameraF cam, int n, const float* __restrict__ means,
+                                                              const float* __restrict__ scales,
+                                                              const float* __restrict__ quats,
+                                                              const float* __restrict__ opacity,
+                                                              const float* __restrict__ sh,
+                                                              const float* __restrict__ colors, float* means2d,
+                                                              float* depth, float* conic, float* color, int* radius,
+                                                              uint32_t* tiles, Record* rec) {
+    RS_PDL_ENTER();
+    constexpr int R = stg_rows<DEG>();
+    constexpr int T = kStgThreads;
+    extern __shared__ __align__(128) float s_rows[];  // [kStgBufs buffers][R rows][T Gaussians]
+    __shared__ __align__(8) uint64_t s_mbar[2][2];     // [buffer][geometry rows, colour rows]
+    const int t = threadIdx.x;
+    const size_t N = size_t(n);
+    const int n_tiles = (n + T - 1) / T;
+    if (t == 0) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            stg_mbar_init(uint32_t(__cvta_generic_to_shared(&s_mbar[b][0])));
+            stg_mbar_init(uint32_t(__cvta_generic_to_shared(&s_mbar[b][1])));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // thread 0: request tile `tile`'s rows into buffer b
+    auto issue = [&](int tile, int b) {
+        const size_t base = size_t(tile) * T;
+        const uint32_t bytes = uint32_t(min(size_t(T), N - base)) * 4u;
+        const uint32_t dst = uint32_t(__cvta_generic_to_shared(s_rows + size_t(b) * R * T));
+        const uint32_t mg = uint32_t(__cvta_generic_to_shared(&s_mbar[b][0]));
+        const uint32_t mc = uint32_t(__cvta_generic_to_shared(&s_mbar[b][1]));
+        stg_expect(mg, kStgGeoRows * bytes);
+        stg_expect(mc, (R - kStgGeoRows) * bytes);
+        auto row = [&](int r) { return dst + uint32_t(r * T * 4); };
+#pragma unroll
+        for (int r = 0; r < 3; ++r) stg_copy(row(r), means + size_t(r) * N + base, bytes, mg);
+#pragma unroll
+        for (int r = 0; r < 3; ++r) stg_copy(row(3 + r), scales + size_t(r) * N + base, bytes, mg);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) stg_copy(row(6 + r), quats + size_t(r) * N + base, bytes, mg);
+        stg_copy(row(10), opacity + base, bytes, mg);
+        const float* crow = DEG < 0 ? colors : sh;
+        for (int r = 0; r < R - kStgGeoRows; ++r) stg_copy(row(kStgGeoRows + r), crow + size_t(r) * N + base, bytes, mc);
+    };
+    int k = 0;
+    if (t == 0 && int(blockIdx.x) < n_tiles) issue(blockIdx.x, 0);
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++k) {
+        const int b = kStgBufs == 2 ? (k & 1) : 0;
+        const uint32_t par = uint32_t(kStgBufs == 2 ? (k >> 1) : k) & 1u;
+        const uint32_t mg = uint32_t(__cvta_generic_to_shared(&s_mbar[b][0]));
+        const uint32_t mc = uint32_t(__cvta_generic_to_shared(&s_mbar[b][1]));
+        const int next = tile + int(gridDim.x);
+        if (kStgBufs == 2 && t == 0 && next < n_tiles) {
+            // buffer b ^ 1 was last read in the previous step, which ended with a barrier
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(next, b ^ 1);
+        }
+        const float* S = s_rows + size_t(b) * R * T;
+        const int i = tile * T + t;
+        const bool live = i < n;
+        bool ok = __syncthreads_and(stg_wait(mg, par));
+        if (!ok) {
+            // give up: flag it, let this CTA's copies in flight land (bounded), leave
+            if (t == 0) {
+                atomicOr(&g_proj_error, 1u);
+                (void)stg_wait(mc, par);
+                if (kStgBufs == 2 && next < n_tiles) {
+                    (void)stg_wait(uint32_t(__cvta_generic_to_shared(&s_mbar[b ^ 1][0])), uint32_t((k + 1) >> 1) & 1u);
+                    (void)stg_wait(uint32_t(__cvta_generic_to_shared(&s_mbar[b ^ 1][1])), uint32_t((k + 1) >> 1) & 1u);
+                }
+            }
+            return;
+        }
+        const float m[3] = {S[0 * T + t], S[1 * T + t], S[2 * T + t]};
+        const float sc[3] = {S[3 * T + t], S[4 * T + t], S[5 * T + t]};
+        const float q[4] = {S[6 * T + t], S[7 * T + t], S[8 * T + t], S[9 * T + t]};
+        const float o = S[10 * T + t];
+        Geo G;
+        geometry(cam, m, sc, q, G);
+        const bool vis = live && G.visible;
+        float d[3], len;
+        view_dir(cam, m, d, len);
+        ok = __syncthreads_and(stg_wait(mc, par));
+        if (!ok) {
+            if (t == 0) {
+                atomicOr(&g_proj_error, 1u);
+                if (kStgBufs == 2 && next < n_tiles) {
+                    (void)stg_wait(uint32_t(__cvta_generic_to_shared(&s_mbar[b ^ 1][0])), uint32_t((k + 1) >> 1) & 1u);
+                    (void)stg_wait(uint32_t(__cvta_generic_to_shared(&s_mbar[b ^ 1][1])), uint32_t((k + 1) >> 1) & 1u);
+                }
+            }
+            return;
+        }
+        float rgb[3] = {0.f, 0.f, 0.f};
+        if (vis) {
+            if (DEG < 0) {
+#pragma unroll
+                for (int ch = 0; ch < 3; ++ch) rgb[ch] = S[(kStgGeoRows + ch) * T + t];
+            } else {
+                constexpr int K = (DEG + 1) * (DEG + 1);
+                float Y[16];
+                sh_basis<(DEG < 0 ? 0 : DEG)>(d[0], d[1], d[2], Y);
+#pragma unroll
+                for (int ch = 0; ch < 3; ++ch) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < K; ++kk) acc = fmaf(S[(kStgGeoRows + kk * 3 + ch) * T + t], Y[kk], acc);
+                    rgb[ch] = acc;
+                }
+            }
+        }
+        if (live) {
+            means2d[i] = vis ? G.u : 0.f;
+            means2d[N + i] = vis ? G.v : 0.f;
+            depth[i] = vis ? G.p[2] : 0.f;
+            conic[i] = vis ? G.A : 0.f;
+            conic[N + i] = vis ? G.B : 0.f;
+            conic[2 * N + i] = vis ? G.C : 0.f;
+            color[i] = rgb[0];
+            color[N + i] = rgb[1];
+            color[2 * N + i] = rgb[2];
+            radius[i] = vis ? G.radius : 0;
+            tiles[i] = vis ? uint32_t(G.rect[1] - G.rect[0]) * uint32_t(G.rect[3] - G.rect[2]) : 0u;
+        }
+        if (vis) {
+            // the alpha >= 1/255 box, as k_project
+            float ext_x = -1.f, ext_y = -1.f;
+            const float o255 = 255.f * o;
+            if (o255 > 1.f) {
+                const float kk = 2.002f * logf(o255);
+                ext_x = sqrtf(kk * G.a) + 0.01f;
+                ext_y = sqrtf(kk * G.c) + 0.01f;
+            }
+            Record r;
+            r.p = make_float4(G.u, G.v, o, ext_x);
+            r.q = make_float4(-0.5f * kLog2e * G.A, -kLog2e * G.B, -0.5f * kLog2e * G.C, ext_y);
+            r.c = make_float4(rgb[0], rgb[1], rgb[2], 1.0f / o);
+            rec[i] = r;
+        }
+        __syncthreads();  // buffer b is read before it is requested again
+        if (kStgBufs == 1 && t == 0 && next < n_tiles) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(next, 0);
+        }
+    }
+}
+
 template <int DEG>
 __global__ void __launch_bounds__(kProjThreads, kProjMinBlocks) k_project_bwd(
     CameraF cam, int n, const float* __restrict__ means, const float* __restrict__ scales,
@@ -661,11 +879,50 @@ __global__ void __launch_bounds__(kProjThreads, kProjMinBlocks) k_project_bwd(
 
 }  // namespace
 
+int take_projection_error() {
+    unsigned int v = 0u;
+    if (cudaMemcpyFromSymbol(&v, g_proj_error, sizeof(v)) != cudaSuccess) return -1;
+    if (v == 0u) return 0;
+    const unsigned int zero = 0u;
+    if (cudaMemcpyToSymbol(g_proj_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    return 1;
+}
+
 cudaError_t launch_project(const CameraF& cam, const rs_gaussians& g, const rs_projected& o,
                            cudaStream_t s) {
     if (g.n == 0) return cudaSuccess;
     const int threads = kProjThreads;
     Record* rec = reinterpret_cast<Record*>(o.d_records);
+#if RS_PROJ_STAGED
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & uintptr_t(15)) == 0; };
+    if (o.tile_test == RS_TILE_TEST_SQUARE && g.n % 4 == 0 && al16(g.d_means) && al16(g.d_scales) &&
+        al16(g.d_quats) && al16(g.d_opacity) && al16(g.sh_degree >= 0 ? g.d_sh : g.d_colors)) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const int n_tiles = (g.n + kStgThreads - 1) / kStgThreads;
+        const int blocks = std::min(n_tiles, std::max(1, sms) * kStgBlocksPerSM);
+#define RS_PROJECT_STAGED(D)                                                                               \
+    {                                                                                                      \
+        const size_t smem = size_t(kStgBufs) * stg_rows<D>() * kStgThreads * sizeof(float);               \
+        e = cudaFuncSetAttribute(k_project_staged<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)); \
+        if (e != cudaSuccess) return e;                                                                    \
+        pdl_launch(k_project_staged<D>, blocks, kStgThreads, smem, s, cam, g.n, g.d_means, g.d_scales,     \
+                   g.d_quats, g.d_opacity, g.d_sh, g.d_colors, o.d_means2d, o.d_depth, o.d_conic, o.d_color, \
+                   o.d_radius, o.d_tiles_touched, rec);                                                    \
+    }
+        switch (g.sh_degree) {
+            case -1: RS_PROJECT_STAGED(-1); break;
+            case 0: RS_PROJECT_STAGED(0); break;
+            case 1: RS_PROJECT_STAGED(1); break;
+            case 2: RS_PROJECT_STAGED(2); break;
+            default: RS_PROJECT_STAGED(3); break;
+        }
+#undef RS_PROJECT_STAGED
+        return cudaGetLastError();
+    }
+#endif
     // RS_PROJ_VEC Gaussians per thread (2 or 4) when the rows allow it, else one
     constexpr int V = RS_PROJ_VEC;
     auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & uintptr_t(4 * V - 1)) == 0; };

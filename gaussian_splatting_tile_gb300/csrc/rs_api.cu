@@ -290,8 +290,8 @@ int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_rad
 }
 
 int rs_device_error(void) {
-    const int r = rs::take_device_error();
-    return r < 0 ? RS_ERR_CUDA : r > 0 ? RS_ERR_DEVICE_TIMEOUT : RS_OK;
+    const int a = rs::take_device_error(), b = rs::take_projection_error();
+    return a < 0 || b < 0 ? RS_ERR_CUDA : a > 0 || b > 0 ? RS_ERR_DEVICE_TIMEOUT : RS_OK;
 }
 
 int rs_l1_dssim_workspace_size(int32_t channels, int32_t height, int32_t width, size_t* bytes) {

@@ -299,6 +299,8 @@ cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float sc
 // 1 if a tensor-core wait gave up since the last call (the flag is cleared), 0 if not, -1 on a
 // CUDA error.
 int take_device_error();
+// The same for the projection's bounded waits on its staged copies.
+int take_projection_error();
 size_t ssim_workspace_bytes(int C, int H, int W);
 cudaError_t launch_l1_dssim(int C, int H, int W, const float* img, const float* tgt, float lambda, float scale,
                             float* dimg, float* loss, void* ws, cudaStream_t s);

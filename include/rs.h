@@ -127,7 +127,11 @@ const char* rs_error_string(int code);
  * lambda_max = mid + sqrt(max(0.1, mid^2 - det)); span = [floor((u-r)/16), floor((u+r)/16)+1)
  * clamped to the tile grid (same in y); culled when the span is empty.  Colour: degree-K real
  * SH (viewer 2.2.3) at the unit direction from the camera centre -R^T t to the mean, no offset
- * or clamp; or the given colours.  Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
+ * or clamp; or the given colours.  With the square test, n a multiple of 4 and every input row
+ * 16-byte aligned, the input rows are staged through shared memory by bulk asynchronous copies
+ * with a bounded wait; a CTA whose wait gives up leaves its Gaussians' outputs unwritten and
+ * raises the flag rs_device_error reports (the results are the same on every path).
+ * Errors: RS_ERR_INVALID_ARG, RS_ERR_CUDA. */
 int rs_project(const rs_camera* camera, const rs_gaussians* gaussians, const rs_projected* out,
                void* stream);
 
@@ -281,9 +285,9 @@ int rs_appearance_bwd(const rs_camera* camera, int32_t n, const float* d_means,
                       const float* d_latents, const rs_mlp* mlp, const float* d_dL_dcolors,
                       float* d_dL_dlatents, const rs_mlp_grads* grads, void* stream);
 
-/* Reads and clears the device flag raised by a kernel whose bounded wait on the tensor cores gave
- * up: RS_ERR_DEVICE_TIMEOUT if it was raised since the last call, else RS_OK (RS_ERR_CUDA if
- * the flag cannot be read).  Synchronises the device. */
+/* Reads and clears the device flags raised by a kernel whose bounded wait gave up (on the tensor
+ * cores, or on the projection's staged copies): RS_ERR_DEVICE_TIMEOUT if one was raised since the
+ * last call, else RS_OK (RS_ERR_CUDA if a flag cannot be read).  Synchronises the device. */
 int rs_device_error(void);
 
 /* L1 loss between an image and its target over `count` floats:

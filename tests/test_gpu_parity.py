@@ -290,26 +290,35 @@ def test_ellipse_tile_test(which):
 
 
 @pytest.mark.parametrize("degree", [-1, 3])
-def test_vectorised_projection_equals_the_scalar_one(degree):
-    """rs_project takes four Gaussians per thread with 16-byte loads when n is a multiple of 4 and
-    the rows are 16-byte aligned, else one per thread: both run the same per-Gaussian arithmetic,
-    so the first 4000 Gaussians of an n = 4001 scene (scalar) project bit for bit as the n = 4000
-    scene (vectorised)."""
+def test_staged_and_vectorised_projections_equal_the_scalar_one(degree):
+    """rs_project has three paths with the same per-Gaussian arithmetic: input rows staged in
+    shared memory by bulk copies (n a multiple of 4, rows 16-byte aligned), two Gaussians per
+    thread with 8-byte loads (n even), one per thread otherwise.  The first 4000 Gaussians of an
+    n = 4001 scene (scalar) and of an n = 4002 scene (vectorised) project bit for bit as the
+    n = 4000 scene (staged, with a ragged last tile of 32 Gaussians)."""
     g = scenes.procedural_scene(seed=8, n_sphere=2500, n_helix=750, n_plane=751)
     if degree == -1:
         g.colors = np.ascontiguousarray(np.random.default_rng(1).uniform(0, 1, (3, g.n)), np.float32)
         g.sh, g.sh_degree = None, -1
     assert g.n == 4001
-    cut = scenes.Gaussians(np.ascontiguousarray(g.means[:, :4000]), np.ascontiguousarray(g.scales[:, :4000]),
-                           np.ascontiguousarray(g.quats[:, :4000]), np.ascontiguousarray(g.opacity[:4000]),
-                           None if g.sh is None else np.ascontiguousarray(g.sh[:, :4000]), g.sh_degree,
-                           None if g.colors is None else np.ascontiguousarray(g.colors[:, :4000]))
+
+    def first(m, extra=0):
+        idx = np.r_[np.arange(m), np.full(extra, m - 1)]
+        pick = lambda a: None if a is None else np.ascontiguousarray(a[..., idx])
+        return scenes.Gaussians(pick(g.means), pick(g.scales), pick(g.quats), pick(g.opacity), pick(g.sh),
+                                g.sh_degree, pick(g.colors))
+
     cam = scenes.procedural_camera(320, 240, azimuth=0.9)
-    a, b = P.run_gpu(g, cam), P.run_gpu(cut, cam)
-    for k in ("means2d", "depth", "conic", "color"):
-        assert np.array_equal(a[k][..., :4000], b[k]), k
-    assert np.array_equal(a["radius"][:4000], b["radius"]) and np.array_equal(a["tiles_touched"][:4000], b["tiles_touched"])
-    ra = a["renderer"].proj.records.cpu().numpy().view(np.float32).reshape(-1, 12)[:4000]
+    runs = {"scalar": P.run_gpu(g, cam), "vectorised": P.run_gpu(first(4001, 1), cam),
+            "staged": P.run_gpu(first(4000), cam)}
+    b = runs["staged"]
     rb = b["renderer"].proj.records.cpu().numpy().view(np.float32).reshape(-1, 12)
     vis = b["radius"] > 0
-    assert np.array_equal(ra[vis], rb[vis])
+    for name in ("scalar", "vectorised"):
+        a = runs[name]
+        for k in ("means2d", "depth", "conic", "color"):
+            assert np.array_equal(a[k][..., :4000], b[k]), (name, k)
+        assert np.array_equal(a["radius"][:4000], b["radius"]), name
+        assert np.array_equal(a["tiles_touched"][:4000], b["tiles_touched"]), name
+        ra = a["renderer"].proj.records.cpu().numpy().view(np.float32).reshape(-1, 12)[:4000]
+        assert np.array_equal(ra[vis], rb[vis]), name
