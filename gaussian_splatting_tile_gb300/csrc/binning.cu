@@ -63,6 +63,30 @@ constexpr int kMaxSpins = 1 << 20;         // bound on one look-back wait (then 
 #endif
 constexpr int kWindow = RS_LOOKBACK_WINDOW;  // predecessors whose status words are read together
 
+// Lanes of the warp holding the same value d as this lane, for 0 <= d <= R = 2^RBITS (R marks
+// "no key").  1: one ballot per bit of d (RBITS + 1 ballots and selects); 0: the match
+// instruction.  Both give the same mask; the match instruction's latency bounded the ranking and
+// digit-counting loops (at 10 M entries a tile-id pass took 129 us with it, 98 us with ballots;
+// the expansion 102 and 92 us).
+#ifndef RS_RANK_BALLOT
+#define RS_RANK_BALLOT 1
+#endif
+template <int RBITS>
+__device__ __forceinline__ uint32_t same_digit_lanes(uint32_t d) {
+#if RS_RANK_BALLOT
+    uint32_t m = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b <= RBITS; ++b) {
+        const bool bit = (d >> b) & 1u;
+        const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+        m &= bit ? bal : ~bal;
+    }
+    return m;
+#else
+    return __match_any_sync(0xffffffffu, d);
+#endif
+}
+
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -136,7 +160,7 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_hist(const uint32_t* __res
 #pragma unroll
         for (int p = 0; p < PASSES; ++p) {
             const uint32_t d = i < n ? (key >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
-            const uint32_t peers = __match_any_sync(kFull, d);
+            const uint32_t peers = same_digit_lanes<RBITS>(d);
             if (d < uint32_t(R) && lane == uint32_t(__ffs(peers) - 1)) atomicAdd(&s_h[p][d], uint32_t(__popc(peers)));
         }
     }
@@ -165,7 +189,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t a, uint32_
 
 // One stable pass over the digit at `shift`.  A block owns ITEMS x 256 consecutive keys of its
 // tile; warp w owns the w-th contiguous 32 x ITEMS of them and walks them 32 at a time in index
-// order, ranking equal digits with match masks and per-warp running counts.  A key goes to
+// order, ranking equal digits with masks of the lanes that hold them and per-warp running counts.  A key goes to
 // (keys of smaller digits) + (same digit in earlier tiles, from the look-back)
 // + (same digit in earlier warps of the tile) + (its rank in its warp).  The tile's keys are
 // first put in that order in shared memory, so the global writes of one digit are consecutive.
@@ -212,7 +236,7 @@ __global__ void __launch_bounds__(kRsThreads, MINB) k_sweep_pass(
         }
 #pragma unroll
         for (int k = 0; k < ITEMS; ++k) {
-            const uint32_t peers = __match_any_sync(kFull, d[k]);
+            const uint32_t peers = same_digit_lanes<RBITS>(d[k]);
             const uint32_t leader = uint32_t(__ffs(peers) - 1);
             const bool lead = lane == leader && d[k] < uint32_t(R);
             uint32_t before = lead ? s_cnt[warp][d[k]] : 0u;
@@ -681,7 +705,7 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
             }
             for (int p = 0; p < passes; ++p) {
                 const uint32_t d = valid ? (tile >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
-                const uint32_t peers = __match_any_sync(kFull, d);
+                const uint32_t peers = same_digit_lanes<RBITS>(d);
                 if (d < uint32_t(R) && lane == uint32_t(__ffs(peers) - 1)) atomicAdd(&s_h[p][d], uint32_t(__popc(peers)));
             }
         }
