@@ -21,6 +21,10 @@
 namespace rs {
 namespace {
 
+// Raised when a compositing kernel meets a point-list entry >= n or a tile range past the list's
+// capacity (caller data): the entry or the tile is skipped instead of read out of bounds.
+__device__ unsigned int g_raster_check;
+
 constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per thread
 constexpr uint32_t kChunk = RS_RASTER_CHUNK;  // backward task length and checkpoint spacing
 static_assert(kChunk == uint32_t(kBatch), "a forward batch ends at every chunk boundary");
@@ -150,8 +154,8 @@ __device__ __forceinline__ uint8_t comp_byte(const FwdSmem& sm, int j) {
 // so each pixel also sums the colour of every stretch between boundaries and records its state
 // there for the backward; other tiles skip that work.
 template <bool SPLIT>
-__device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record* __restrict__ rec, uint32_t tile,
-                                                uint2 range,
+__device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, const Record* __restrict__ rec,
+                                                uint32_t tile, uint2 range,
                                                 const uint32_t* __restrict__ list, float3 bg,
                                                 float* __restrict__ image, float* __restrict__ final_T,
                                                 uint32_t* __restrict__ n_contrib, float4* __restrict__ ckpt,
@@ -187,14 +191,19 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
         const uint32_t e = base + threadIdx.x;
         uint32_t m = 0u;
         if (e < bend) {
-            const Record& r = rec[list[e]];
-            sm.p[threadIdx.x] = r.p;
-            sm.q[threadIdx.x] = r.q;
-            sm.c[threadIdx.x] = r.c;
-            m = warp_mask(r.p, r.q, tx0, ty0);
+            const uint32_t g = list[e];
+            if (g >= n) {
+                atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
+            } else {
+                const Record& r = rec[g];
+                sm.p[threadIdx.x] = r.p;
+                sm.q[threadIdx.x] = r.q;
+                sm.c[threadIdx.x] = r.c;
+                m = warp_mask(r.p, r.q, tx0, ty0);
 #if RS_FWD_EXACT_MASK
-            if (m) m = warp_mask_exact(m, r.p, r.q, r.c, tx0, ty0);
+                if (m) m = warp_mask_exact(m, r.p, r.q, r.c, tx0, ty0);
 #endif
+            }
         }
         sm.mask[threadIdx.x] = m;
         __syncthreads();
@@ -271,7 +280,8 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, const Record
     }
 }
 
-__global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(CameraF cam, const Record* __restrict__ rec,
+__global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(CameraF cam, uint32_t n, uint32_t cap,
+                                                           const Record* __restrict__ rec,
                                                            const uint2* __restrict__ ranges,
                                                            const uint32_t* __restrict__ list,
                                                            float3 bg, float* __restrict__ image,
@@ -284,16 +294,21 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
     RS_PDL_ENTER();
     __shared__ FwdSmem sm;
     const uint32_t tile = order[blockIdx.x];
-    const uint2 range = ranges[tile];
+    uint2 range = ranges[tile];
+    if (range.y > cap || range.x > range.y) {
+        // caller data out of range: the tile is drawn empty
+        if (threadIdx.x == 0) atomicOr(&g_raster_check, 1u);
+        range = make_uint2(0u, 0u);
+    }
     // the tile's list positions that are multiples of the chunk size are the backward's task
     // starts: record which tile holds them
     for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
          c += kFwdThreads)
         chunk_tile[c] = tile;
     if (range.y > range.x && (range.y - 1u) / kChunk > range.x / kChunk)
-        raster_fwd_tile<true>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
+        raster_fwd_tile<true>(cam, n, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
     else
-        raster_fwd_tile<false>(cam, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
+        raster_fwd_tile<false>(cam, n, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
 }
 
 // Reduce-scatter of nine per-lane values over the warp in five xor-shuffle steps (9 -> 5 -> 3
@@ -442,7 +457,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     const uint32_t* __restrict__ list, float3 bg,
     const float* __restrict__ final_T, const uint32_t* __restrict__ n_contrib,
     const uint32_t* __restrict__ chunk_tile, const float4* __restrict__ ckpt, uint32_t slots,
-    const uint8_t* __restrict__ comp, const float* __restrict__ dL_dimage, float* __restrict__ dm2,
+    const uint8_t* __restrict__ comp, uint32_t cap, const float* __restrict__ dL_dimage, float* __restrict__ dm2,
     float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol) {
     RS_PDL_ENTER();
     __shared__ float4 s_p[kBwdWarps][32], s_q[kBwdWarps][32], s_c[kBwdWarps][32];
@@ -457,6 +472,11 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     if (tile >= n_tiles) return;
     uint2 range = ranges[tile];
     if (!(range.x <= a0 && a0 < range.y)) return;
+    if (range.y > cap) {
+        // caller data out of range (the forward drew this tile empty)
+        if (threadIdx.x == 0) atomicOr(&g_raster_check, 1u);
+        return;
+    }
     const int warp = threadIdx.x >> 5;
     const unsigned lane = threadIdx.x & 31;
     const size_t HW = size_t(cam.W) * cam.H;
@@ -539,6 +559,10 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 // meets the area then too): only those records are loaded
                 const uint32_t g = list[e];
                 hit = (uint32_t(comp[e]) & fwarps) != 0u;
+                if (hit && g >= uint32_t(n)) {
+                    atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
+                    hit = false;
+                }
                 if (hit) {
                     const Record& r = rec[g];
                     const float4 p = r.p, q = r.q, c = r.c;
@@ -655,7 +679,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
         if (next >= n_tiles) break;
         tile = next;
         range = ranges[tile];
-        if (range.x != pb) break;
+        if (range.x != pb || range.y > cap) break;
         pa = pb;
     }
 }
@@ -787,19 +811,29 @@ __global__ void __launch_bounds__(kOrderThreads) k_tile_order(const uint2* __res
 }
 }  // namespace
 
+int take_raster_check() {
+    unsigned int v = 0u;
+    if (cudaMemcpyFromSymbol(&v, g_raster_check, sizeof(v)) != cudaSuccess) return -1;
+    if (v == 0u) return 0;
+    const unsigned int zero = 0u;
+    if (cudaMemcpyToSymbol(g_raster_check, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    return 1;
+}
+
 size_t raster_workspace_bytes(size_t capacity, size_t n_tiles) {
     size_t bytes = 0;
     raster_ws(nullptr, capacity, n_tiles, &bytes);
     return bytes;
 }
 
-cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
+cudaError_t launch_raster_fwd(const CameraF& cam, int32_t n, const Record* rec, const uint32_t* ranges,
                               const uint32_t* list, size_t capacity, float3 bg, float* image, float* final_T,
                               uint32_t* n_contrib, void* ws, cudaStream_t s) {
     const int tiles = cam.TX * cam.TY;
     const RasterWs w = raster_ws(ws, capacity, size_t(tiles));
     pdl_launch(k_tile_order, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order);
-    pdl_launch(k_raster_fwd, tiles, kFwdThreads, 0, s, cam, rec, reinterpret_cast<const uint2*>(ranges), list,
+    pdl_launch(k_raster_fwd, tiles, kFwdThreads, 0, s, cam, uint32_t(n), uint32_t(capacity), rec,
+               reinterpret_cast<const uint2*>(ranges), list,
                                                bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
                                                w.order, w.comp);
     return cudaGetLastError();
@@ -816,7 +850,7 @@ cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
     if (blocks == 0) return cudaSuccess;
     pdl_launch(k_raster_bwd, blocks, kBwdThreads, 0, s, cam, n, rec, reinterpret_cast<const uint2*>(ranges), list, bg,
                                                 final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots, w.comp,
-                                                dL_dimage, dm2, dcon, dop, dcol);
+                                                uint32_t(capacity), dL_dimage, dm2, dcon, dop, dcol);
     return cudaGetLastError();
 }
 

@@ -70,6 +70,8 @@ const char* rs_error_string(int code) {
         case RS_ERR_WORKSPACE: return "workspace smaller than rs_bin_workspace_size reports";
         case RS_ERR_CUDA: return "CUDA runtime error";
         case RS_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up; the outputs are not valid";
+        case RS_ERR_DEVICE_CHECK:
+            return "a kernel found an index in the caller's data out of range and skipped it; the outputs are not valid";
         default: return "unknown error code";
     }
 }
@@ -185,7 +187,7 @@ int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t 
     if (!d_tile_ranges || !aligned(d_tile_ranges, 8) || !dev_f(d_point_list)) return RS_ERR_INVALID_ARG;
     if (!d_workspace || !aligned(d_workspace, 16)) return RS_ERR_INVALID_ARG;
     if (workspace_bytes < rs::raster_workspace_bytes(capacity, size_t(cam.TX) * cam.TY)) return RS_ERR_WORKSPACE;
-    return cuda_rc(rs::launch_raster_fwd(cam, static_cast<const rs::Record*>(proj->d_records),
+    return cuda_rc(rs::launch_raster_fwd(cam, n, static_cast<const rs::Record*>(proj->d_records),
                                          d_tile_ranges, d_point_list, capacity, b, d_image, d_final_T,
                                          d_n_contrib, d_workspace, s));
 }
@@ -290,8 +292,9 @@ int rs_densify_stats(int32_t n, const float* d_dL_dmeans2d, const int32_t* d_rad
 }
 
 int rs_device_error(void) {
-    const int a = rs::take_device_error(), b = rs::take_projection_error();
-    return a < 0 || b < 0 ? RS_ERR_CUDA : a > 0 || b > 0 ? RS_ERR_DEVICE_TIMEOUT : RS_OK;
+    const int a = rs::take_device_error(), b = rs::take_projection_error(), c = rs::take_raster_check();
+    if (a < 0 || b < 0 || c < 0) return RS_ERR_CUDA;
+    return c > 0 ? RS_ERR_DEVICE_CHECK : a > 0 || b > 0 ? RS_ERR_DEVICE_TIMEOUT : RS_OK;
 }
 
 int rs_l1_dssim_workspace_size(int32_t channels, int32_t height, int32_t width, size_t* bytes) {

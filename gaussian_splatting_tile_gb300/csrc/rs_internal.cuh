@@ -273,7 +273,7 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
 // pointer to pinned host memory) from a one-thread kernel.
 cudaError_t launch_report(const uint8_t* result_block, uint64_t* host, cudaStream_t s);
 size_t raster_workspace_bytes(size_t capacity, size_t n_tiles);
-cudaError_t launch_raster_fwd(const CameraF& cam, const Record* rec, const uint32_t* ranges,
+cudaError_t launch_raster_fwd(const CameraF& cam, int32_t n, const Record* rec, const uint32_t* ranges,
                               const uint32_t* list, size_t capacity, float3 bg, float* image, float* final_T,
                               uint32_t* n_contrib, void* ws, cudaStream_t s);
 cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
@@ -301,6 +301,9 @@ cudaError_t launch_l1(size_t count, const float* img, const float* tgt, float sc
 int take_device_error();
 // The same for the projection's bounded waits on its staged copies.
 int take_projection_error();
+// 1 if a compositing kernel found a point-list entry >= n or a tile range past the capacity since
+// the last call (the flag is cleared), 0 if not, -1 on a CUDA error.
+int take_raster_check();
 size_t ssim_workspace_bytes(int C, int H, int W);
 cudaError_t launch_l1_dssim(int C, int H, int W, const float* img, const float* tgt, float lambda, float scale,
                             float* dimg, float* loss, void* ws, cudaStream_t s);

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "librs.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "rs.h")
 
 RS_OK, RS_ERR_INVALID_ARG, RS_ERR_CAPACITY, RS_ERR_WORKSPACE, RS_ERR_CUDA = 0, -1, -2, -3, -4
-RS_ERR_DEVICE_TIMEOUT = -5
+RS_ERR_DEVICE_TIMEOUT, RS_ERR_DEVICE_CHECK = -5, -6
 RS_TILE, RS_RECORD_BYTES, RS_MAX_GAUSSIANS, RS_MAX_ENTRIES = 16, 48, 1 << 26, (1 << 30) - 1
 RECORD_BYTES = 48
 TILE = 16
@@ -516,8 +516,9 @@ def rs_appearance_fwd(camera, means: torch.Tensor, latents: torch.Tensor, mlp: D
 
 
 def rs_device_error() -> int:
-    """RS_ERR_DEVICE_TIMEOUT if a tensor-core wait gave up since the last call (the flag is
-    cleared), else RS_OK; synchronises the device."""
+    """RS_ERR_DEVICE_CHECK if a compositing kernel skipped caller data out of range (a point-list
+    entry >= n, a tile range past the capacity), RS_ERR_DEVICE_TIMEOUT if a bounded wait gave up,
+    since the last call (the flags are cleared), else RS_OK; synchronises the device."""
     return int(lib().rs_device_error())
 
 

@@ -42,6 +42,7 @@ extern "C" {
 #define RS_ERR_WORKSPACE (-3)       /* workspace smaller than rs_bin_workspace_size reports   */
 #define RS_ERR_CUDA (-4)            /* a CUDA runtime call or launch failed                   */
 #define RS_ERR_DEVICE_TIMEOUT (-5)  /* a bounded wait inside a kernel gave up (outputs invalid) */
+#define RS_ERR_DEVICE_CHECK (-6)    /* a kernel found caller data out of range and skipped it  */
 
 #define RS_TILE 16                  /* tile edge in pixels (rigel "Binning")                    */
 #define RS_RECORD_BYTES 48          /* packed per-Gaussian record written by rs_project         */
@@ -198,6 +199,9 @@ size_t rs_raster_workspace_size(const rs_camera* camera, size_t capacity);
  * rs_raster_workspace_size(camera, capacity) bytes of device memory, 16-byte aligned, owned by
  * the caller; the call fills it for rs_rasterize_bwd (no initial contents needed).
  * Outputs: d_image [3][H][W], d_final_T [H][W], d_n_contrib [H][W] uint32.
+ * The kernel checks the caller's list: an entry >= n is skipped (examined, never composited) and
+ * a tile whose range ends past capacity (or starts after its end) is drawn empty; either raises
+ * the flag rs_device_error reports as RS_ERR_DEVICE_CHECK.  Nothing is read outside the buffers.
  * Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE (workspace too small), RS_ERR_CUDA. */
 int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
                      const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
@@ -218,6 +222,8 @@ int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t 
  * Outputs (zeroed, then accumulated by the call):
  * d_dL_dmeans2d [2][n], d_dL_dconic [3][n], d_dL_dopacity [n], d_dL_dcolor [3][n].
  * The accumulation order is not fixed, so results may differ in the last bits between runs.
+ * The same checks as rs_rasterize_fwd: entries >= n and tiles whose range ends past capacity are
+ * skipped and raise the flag rs_device_error reports as RS_ERR_DEVICE_CHECK.
  * Errors: RS_ERR_INVALID_ARG, RS_ERR_WORKSPACE, RS_ERR_CUDA. */
 int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
                      const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
@@ -285,9 +291,10 @@ int rs_appearance_bwd(const rs_camera* camera, int32_t n, const float* d_means,
                       const float* d_latents, const rs_mlp* mlp, const float* d_dL_dcolors,
                       float* d_dL_dlatents, const rs_mlp_grads* grads, void* stream);
 
-/* Reads and clears the device flags raised by a kernel whose bounded wait gave up (on the tensor
- * cores, or on the projection's staged copies): RS_ERR_DEVICE_TIMEOUT if one was raised since the
- * last call, else RS_OK (RS_ERR_CUDA if a flag cannot be read).  Synchronises the device. */
+/* Reads and clears the device flags: RS_ERR_DEVICE_CHECK if a compositing kernel skipped caller
+ * data out of range (see rs_rasterize_fwd), else RS_ERR_DEVICE_TIMEOUT if a kernel's bounded wait
+ * gave up (on the tensor cores, or on the projection's staged copies), since the last call; else
+ * RS_OK (RS_ERR_CUDA if a flag cannot be read).  Synchronises the device. */
 int rs_device_error(void);
 
 /* L1 loss between an image and its target over `count` floats:

@@ -35,9 +35,11 @@ def test_header_constants_match_the_binding():
 
 
 def test_error_strings(L):
-    for code in (0, -1, -2, -3, -4, 7):
+    for code in (0, -1, -2, -3, -4, -5, -6, 7):
         assert rs.error_string(code)
     assert "capacity" in rs.error_string(rs.RS_ERR_CAPACITY)
+    assert "out of range" in rs.error_string(rs.RS_ERR_DEVICE_CHECK)
+    assert rs.error_string(rs.RS_ERR_DEVICE_CHECK) != rs.error_string(7)
 
 
 def test_workspace_size_grows_with_capacity(L):
