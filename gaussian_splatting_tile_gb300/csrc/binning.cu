@@ -87,6 +87,20 @@ __device__ __forceinline__ uint32_t same_digit_lanes(uint32_t d) {
 #endif
 }
 
+// Adds this lane's digit d to the histogram h (d == R: no key): the whole warp in one atomic when
+// every lane holds the same digit (the high digits of neighbouring keys), else one shared-memory
+// atomic per lane (the hardware serialises lanes that meet on one counter).  Counting needs no
+// ranks, so this replaces the equal-digit masks in the histogram loops.
+template <int R>
+__device__ __forceinline__ void count_digit(uint32_t* h, uint32_t d) {
+    const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+    if (__all_sync(0xffffffffu, d == d0)) {
+        if ((threadIdx.x & 31) == 0 && d0 < uint32_t(R)) atomicAdd(&h[d0], 32u);
+    } else if (d < uint32_t(R)) {
+        atomicAdd(&h[d], 1u);
+    }
+}
+
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -159,9 +173,7 @@ __global__ void __launch_bounds__(kRsThreads) k_sweep_hist(const uint32_t* __res
         if (i < n) rs_load<FROM_DEPTH>(keys, nullptr, src, i, key, val);
 #pragma unroll
         for (int p = 0; p < PASSES; ++p) {
-            const uint32_t d = i < n ? (key >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
-            const uint32_t peers = same_digit_lanes<RBITS>(d);
-            if (d < uint32_t(R) && lane == uint32_t(__ffs(peers) - 1)) atomicAdd(&s_h[p][d], uint32_t(__popc(peers)));
+            count_digit<R>(s_h[p], i < n ? (key >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R));
         }
     }
     __syncthreads();
@@ -704,9 +716,7 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
                 vals[e] = gid;
             }
             for (int p = 0; p < passes; ++p) {
-                const uint32_t d = valid ? (tile >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R);
-                const uint32_t peers = same_digit_lanes<RBITS>(d);
-                if (d < uint32_t(R) && lane == uint32_t(__ffs(peers) - 1)) atomicAdd(&s_h[p][d], uint32_t(__popc(peers)));
+                count_digit<R>(s_h[p], valid ? (tile >> (p * digit_bits)) & uint32_t(R - 1) : uint32_t(R));
             }
         }
     }
