@@ -101,6 +101,25 @@ __device__ __forceinline__ void count_digit(uint32_t* h, uint32_t d) {
     }
 }
 
+// q = n / d and r = n % d for 1 <= d and n < 2^24 (an entry's index within its Gaussian's tile
+// rectangle, which is below the tile count, and the rectangle's width): the quotient estimated
+// in float with the approximate reciprocal is within one of the exact one for these sizes, and
+// comparing n - q d with 0 and d corrects it.
+__device__ __forceinline__ void div_small(uint32_t n, uint32_t d, uint32_t& q, uint32_t& r) {
+    uint32_t qe = __float2uint_rz(__uint2float_rn(n) * rcp_approx(__uint2float_rn(d)));
+    int32_t rr = int32_t(n) - int32_t(qe * d);
+    while (rr < 0) {
+        --qe;
+        rr += int32_t(d);
+    }
+    while (rr >= int32_t(d)) {
+        ++qe;
+        rr -= int32_t(d);
+    }
+    q = qe;
+    r = uint32_t(rr);
+}
+
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -667,8 +686,9 @@ __global__ void __launch_bounds__(kExpThreads) k_expand(CameraF cam, uint32_t n,
                 const uint32_t kk = uint32_t(uint64_t(e) - s_start[owner]);
                 gid = s_g[owner];
                 const uint2 r = s_rect[owner];
-                const uint32_t ty = (r.x >> 16) + kk / r.y, tx = (r.x & 0xffffu) + kk % r.y;
-                tile = ty * uint32_t(cam.TX) + tx;
+                uint32_t q, rem;
+                div_small(kk, r.y, q, rem);
+                tile = ((r.x >> 16) + q) * uint32_t(cam.TX) + (r.x & 0xffffu) + rem;
             } else if (valid && ELL && table) {
                 // the window's rows in entry order: the last row starting at or before e
                 const uint32_t off = uint32_t(uint64_t(e) - s_start[0]);
