@@ -370,13 +370,33 @@ __global__ void k_clear(uint32_t* __restrict__ ranges, uint32_t range_words, uin
 __global__ void k_ranges(const uint32_t* __restrict__ tiles, Count count, uint32_t n_tiles,
                          uint32_t* __restrict__ ranges) {
     RS_PDL_ENTER();
+    constexpr uint32_t kNone = 0xffffffffu;  // never a tile id
     const uint32_t E = count.get();
+    const uint32_t quads = (E + 3u) / 4u;
     const uint32_t stride = gridDim.x * blockDim.x;
-    for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride) {
-        const uint32_t tile = tiles[e];
-        if (tile >= n_tiles) continue;  // unreachable for ids made by the expansion; keeps writes in bounds
-        if (e == 0 || tiles[e - 1] != tile) ranges[2 * size_t(tile)] = e;
-        if (e == E - 1 || tiles[e + 1] != tile) ranges[2 * size_t(tile) + 1] = e + 1;
+    // four consecutive entries per thread (one 16-byte load) and their two neighbours
+    for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += stride) {
+        const uint32_t e0 = 4u * q;
+        uint32_t t[6];  // tiles[e0 - 1 .. e0 + 4], kNone outside [0, E)
+        if (e0 + 4u <= E) {
+            const uint4 v = *reinterpret_cast<const uint4*>(tiles + e0);
+            t[1] = v.x;
+            t[2] = v.y;
+            t[3] = v.z;
+            t[4] = v.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) t[1 + j] = e0 + uint32_t(j) < E ? tiles[e0 + j] : kNone;
+        }
+        t[0] = e0 > 0u ? tiles[e0 - 1u] : kNone;
+        t[5] = e0 + 4u < E ? tiles[e0 + 4u] : kNone;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t e = e0 + uint32_t(j), tile = t[1 + j];
+            if (e >= E || tile >= n_tiles) continue;  // ids made by the expansion are always below n_tiles
+            if (t[j] != tile) ranges[2 * size_t(tile)] = e;
+            if (t[j + 2] != tile) ranges[2 * size_t(tile) + 1] = e + 1u;
+        }
     }
 }
 
@@ -912,7 +932,7 @@ cudaError_t launch_bin(const BinPlan& plan, const CameraF& cam, const rs_project
         cur ^= 1;
     }
     {
-        const unsigned rb = unsigned(std::min<size_t>(ceil_div(plan.capacity, 256), 152 * 16));
+        const unsigned rb = unsigned(std::min<size_t>(ceil_div(plan.capacity, 1024), 152 * 16));
         pdl_launch(k_ranges, rb, 256, 0, s, TK[0], ce, uint32_t(plan.n_tiles), tile_ranges);
     }
     return cudaGetLastError();
