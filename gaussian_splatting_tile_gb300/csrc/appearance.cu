@@ -637,6 +637,7 @@ __global__ void __launch_bounds__(kTcBwdThreads) k_mlp_bwd_tc(MlpArgs a, const f
         float dl[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) dl[k] = 0.f;
+        const int kd = (a.D + 3) & ~3;  // the inputs' columns, rounded up to groups of four
         uint32_t zc[8], zn[8];
         tc_ld8_async(trow + uint32_t(half * HH), zc);
         tc_ld_wait(zc);
@@ -663,11 +664,13 @@ __global__ void __launch_bounds__(kTcBwdThreads) k_mlp_bwd_tc(MlpArgs a, const f
                     vh[q + e] = fmaxf(zz, 0.f);
                 }
             }
+            // column groups of four past the inputs hold zero weights: skipped (uniform branch)
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int u = 8 * grp + q;
+            for (int k = 0; k < K; k += 4) {
+                if (k >= kd) break;
 #pragma unroll
-                for (int k = 0; k < K; k += 4) {
+                for (int q = 0; q < 8; ++q) {
+                    const int u = 8 * grp + q;
                     float w4[4];
                     if constexpr (Smem::kW1f) {
                         const float4 f = *reinterpret_cast<const float4*>(&sm.w1f[u * K + k]);
