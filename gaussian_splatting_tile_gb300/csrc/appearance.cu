@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kTcBwdThreads) k_mlp_bwd_tc(MlpArgs a, const f
         asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
         __syncthreads();
         asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-        if (t == 0) {
+        if (t == kTcRows) {  // a thread of the second half, which stages no X
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const uint32_t off = uint32_t(ks) * 256u;
@@ -725,7 +725,10 @@ __global__ void __launch_bounds__(kTcBwdThreads) k_mlp_bwd_tc(MlpArgs a, const f
         asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
         __syncthreads();
         asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-        if (t == 0) {
+        // issued (48 instructions) by a thread of the second half, which has nothing left to do in
+        // this tile, not by a thread of the first, which still writes dL/dlatent and then stages
+        // the next X
+        if (t == kTcRows) {
 #pragma unroll
             for (int ks = 0; ks < kTcRows / 8; ++ks) {
                 const uint32_t off = uint32_t(ks) * 256u;
