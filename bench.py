@@ -702,9 +702,10 @@ B_MLP_BWD_PER_G = 4 * (8 + 3 + 3 + 8)
 
 def run_training_step(device, steps: int = 5, warmup: int = 2):
     """Stage times of the training-shaped step (250,000 Gaussians, 8 views of 400x400, MLP
-    11 -> 64 -> 3, L1 loss), CUDA events per stage, L2 written over before every view.  The
-    targets are this library's own renders of the Gaussians with their procedural colours (the
-    configuration's definition of ground truth); they are inputs to the timing only."""
+    11 -> 64 -> 3, L1 loss), CUDA events per stage, L2 written over before every view; the MLP
+    kernels also timed alone (L2 written over, events around the one call) for their roofline.
+    The targets are this library's own renders of the Gaussians with their procedural colours
+    (the configuration's definition of ground truth); they are inputs to the timing only."""
     import numpy as np
     import torch
 
@@ -766,6 +767,26 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
         step.R.check_async(results[k])  # raises if a view overflowed the capacity or timed out
     st = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(5)] for e in times])
     per_view = st.mean(axis=0)
+    # the MLP kernels on their own for the roofline: L2 written over, then CUDA events around the
+    # one call (the fill keeps the GPU busy while the call is enqueued, so no host gap is timed,
+    # unlike the per-view stages above, whose MLP backward follows several host calls)
+    dcol = torch.empty(3, g.n, dtype=torch.float32, device=device)
+    dcol.normal_(0.0, 1e-3)
+    iso = []
+    for _ in range(steps):
+        for v in range(len(cams)):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            flush.fill_(float(v))
+            ev[0].record(stream)
+            rs.rs_appearance_fwd(cams[v], dg.means, lat, mlp, step.colors)
+            ev[1].record(stream)
+            flush.fill_(float(v) + 0.5)
+            ev[2].record(stream)
+            step.mlp_backward(dcol)
+            ev[3].record(stream)
+            iso.append(ev)
+    torch.cuda.synchronize(device)
+    mlp_iso = np.array([[e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3])] for e in iso]).mean(axis=0)
     del step
 
     # the step as a whole: its views in flight, each view one CUDA graph (MLP colours, render, L1
@@ -804,8 +825,8 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
 
     hbm, src = measured_peaks()
     n = g.n
-    mlp_fwd_s = per_view[0] * 1e-3
-    mlp_bwd_s = per_view[4] * 1e-3
+    mlp_fwd_s = mlp_iso[0] * 1e-3
+    mlp_bwd_s = mlp_iso[1] * 1e-3
     return dict(workload=("250k Gaussians (sphere/helix/plane), 8 views of 400x400 per step, MLP 11->64->3 "
                           "(split-TF32 tensor cores), L1 loss; targets are renders with the procedural colours"),
                 ms_per_step=inflight_ms,
@@ -813,6 +834,8 @@ def run_training_step(device, steps: int = 5, warmup: int = 2):
                                  "own buffers; CUDA events around each step"),
                 ms_per_step_call_by_call=float(st.sum(axis=1).mean() * len(cams)),
                 stage_ms_per_view=dict(zip(names, [float(x) for x in per_view])),
+                mlp_ms_isolated=dict(fwd=float(mlp_iso[0]), bwd=float(mlp_iso[1]),
+                                     how="L2 written over, then CUDA events around the one call"),
                 steps=steps, views_per_step=len(cams),
                 mlp_roofline=dict(bound="hbm", unit="GB/s", peak=hbm, peak_source=src,
                                   fwd_achieved=n * B_MLP_FWD_PER_G / mlp_fwd_s / 1e9,
