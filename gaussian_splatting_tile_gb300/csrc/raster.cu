@@ -6,16 +6,17 @@
 // fetch, __syncthreads_count vote: the block leaves once all 256 pixels are saturated).
 // Backward: rigel README "Backward": walk each tile back to front from final_T and n_contrib,
 // T_i = T_{i+1} / (1 - a_i), the colour behind carried as a running blend; per-pixel
-// contributions are summed over the warp (a shuffle reduce-scatter) and over the tile
-// (shared-memory accumulators, one slot per staged entry) before one global atomic per entry,
-// component and tile -- the reduction rigel's README names as missing from its backward.
+// contributions are summed over a warp's 64 pixels (buffered in shared memory and summed by four
+// lanes per entry) before one global atomic per entry, component and warp -- the reduction
+// rigel's README names as missing from its backward.
 //
-// The forward gives each warp an 8x4 pixel rectangle, the backward an 8x8 square; after a batch
-// is staged, each warp compacts the entries whose alpha >= 1/255 box (from the record) meets its
-// rectangle: the other
-// entries would be examined and skipped at every pixel of the warp, so they are skipped without
-// being evaluated.  n_contrib is kept as a position in the list (one past the entry that stopped
-// the pixel, or the list length), which is exactly the count of examined entries.
+// The forward gives each warp an 8x4 pixel rectangle, the backward an 8x8 square.  The forward
+// skips, per warp, the staged entries whose alpha >= 1/255 region cannot reach its rectangle, and
+// records which warps composited each entry; the backward evaluates an entry only in the squares
+// where the forward composited it.  Skipping such an entry is exactly what evaluating it and
+// failing the threshold at every pixel would do.  n_contrib is kept as a position in the list (one
+// past the entry that stopped the pixel, or the list length), which is exactly the count of
+// examined entries.
 #include "rs_internal.cuh"
 
 namespace rs {
@@ -32,8 +33,15 @@ constexpr int kFwdThreads = kTilePixels;  // the forward: one block of 256 threa
 constexpr int kFwdWarps = kFwdThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Backward: 1 takes the hit entries two at a time and reduces their sums together (reduce18); 0
-// reduces entry by entry (butterfly9).
+// Backward: how an entry's sums over the warp's pixels are formed.  1 (deferred): every hit's
+// per-pixel dL/dpower and alpha T_j go to a shared-memory buffer, and once eight hits are in it
+// (or the batch ends) four lanes per hit sum them; 0: each hit's nine sums are reduced over the
+// warp at once with shuffles.
+#ifndef RS_BWD_DEFER
+#define RS_BWD_DEFER 1
+#endif
+// Shuffle form only: 1 takes the hit entries two at a time and reduces their sums together
+// (reduce18); 0 reduces entry by entry (butterfly9).
 #ifndef RS_BWD_PAIR
 #define RS_BWD_PAIR 1
 #endif
@@ -42,10 +50,11 @@ constexpr unsigned kFull = 0xffffffffu;
 #ifndef RS_FWD_MIN_BLOCKS
 #define RS_FWD_MIN_BLOCKS 6
 #endif
-// backward (128-thread blocks): 8 (62 registers with paired entries; 7 lets it take 72 and
-// measured 0.243 against 0.233 ms on the 160k 1080p orbit)
+// backward (128-thread blocks): 7 with the deferred sums (72 registers: 0.192 ms on the 160k
+// 1080p orbit view, 0.202 at 8 blocks and 64 registers, 0.193 at 6); 8 with the shuffle sums (62
+// registers: 0.233 against 0.243 ms at 7)
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : 8)
+#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : RS_BWD_DEFER ? 7 : 8)
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -413,10 +422,13 @@ __device__ __forceinline__ float* sum_dst(int slot, size_t N, float* dm2, float*
 // front, 32 entries at a time: each lane reads one entry's composited flags from the forward and,
 // where one of the two forward warps inside the square composited it (a hit), loads its record
 // into the warp's own shared-memory slots; the hits are evaluated one after another by all 64
-// pixels.  The two pixels of a lane share their
-// column, so their nine sums fold before a reduce-scatter over the warp (two consecutive hits'
-// sums in one), and one lane per sum adds it to the
-// Gaussian's gradient with a global atomic.  There is no block-wide barrier.
+// pixels.  Each hit's nine sums over the square (dL/dpower times 1, dx, dy, dx^2, dx dy, dy^2,
+// and alpha T_j times dL/dC) are formed one of two ways: deferred (the default), the per-pixel
+// dL/dpower and alpha T_j go to a shared-memory buffer of eight hits, and when it is full or the
+// batch ends four lanes per hit add up its 64 pixels as moments, turn them into the Gaussian's
+// gradient values and reduce-scatter those between them; or by shuffles, the two pixels of a
+// lane folding their sums before a reduce-scatter over the whole warp.  Either way one lane per
+// value adds it to the Gaussian's gradient with a global atomic.  There is no block-wide barrier.
 // Pixels per lane, stacked 4 rows apart in one column (2: warps of 8x8; 4: warps of 8x16, which
 // cut the warp-entries by a third but measured 0.293 -> 0.303 ms with more registers per lane).
 #ifndef RS_BWD_PX
@@ -425,9 +437,15 @@ __device__ __forceinline__ float* sum_dst(int slot, size_t N, float* dm2, float*
 
 constexpr int kBwdPx = RS_BWD_PX;
 static_assert(kBwdPx == 2 || kBwdPx == 4, "two or four pixels per lane");
+static_assert(!RS_BWD_DEFER || kBwdPx == 2, "the deferred sums take two pixels per lane");
 constexpr int kSqH = 4 * kBwdPx;                 // rows of a warp's area (8 columns wide)
 constexpr int kBwdWarps = 2 * (kTile / kSqH);    // warps per tile
 constexpr int kBwdThreads = 32 * kBwdWarps;
+// Deferred sums: hits buffered per warp before they are summed, and the buffer's row stride in
+// float4 (33: the four lanes of a hit read lane slots 8r + i of rows h = 0..7 in one step, and
+// the odd stride puts the eight rows on distinct banks).
+constexpr int kHitBuf = 8;
+constexpr int kHitStride = 33;
 
 // Per-pixel state of the reverse walk.
 struct BwdPixel {
@@ -461,10 +479,20 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol) {
     RS_PDL_ENTER();
     __shared__ float4 s_p[kBwdWarps][32], s_q[kBwdWarps][32], s_c[kBwdWarps][32];
+#if RS_BWD_DEFER
+    // per buffered hit h and lane L: (dL/dpower, alpha T_j) at the lane's two pixels
+    __shared__ float4 s_buf[kBwdWarps][kHitBuf][kHitStride];
+    // dL/dC at lane L's two pixels: (G0, G1, G2 of the first, G0 of the second), (G1, G2 of it)
+    __shared__ float4 s_ga[kBwdWarps][32];
+    __shared__ float2 s_gb[kBwdWarps][32];
+    // staged slot of the batch's r-th hit (back to front)
+    __shared__ uint8_t s_r2j[kBwdWarps][32];
+#else
     __shared__ uint32_t s_g[kBwdWarps][32];
     // per staged entry, the factors of its sums in the gradient: (dA-row and dC-row factors of
     // du and dv, 1 / opacity, the B factor), see the comment on `slot` below
     __shared__ float4 s_k[kBwdWarps][32];
+#endif
     const uint32_t n_tiles = uint32_t(cam.TX) * uint32_t(cam.TY);
     const uint32_t a0 = blockIdx.x * kChunk, a1 = a0 + kChunk;
     // the tile holding position a0; a chunk past the end of the list has none
@@ -480,13 +508,22 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     const int warp = threadIdx.x >> 5;
     const unsigned lane = threadIdx.x & 31;
     const size_t HW = size_t(cam.W) * cam.H;
+    const size_t N = size_t(n);
+    constexpr float kLn2 = 0.6931471805599453f;
+#if RS_BWD_DEFER
+    // Summing buffered hits, lane L serves hit L & 7 and the lane slots 8r .. 8r + 7 (pixel rows r
+    // and r + 4 of the square, columns 0..7), r = L >> 3; after the reduce-scatter over the hit's
+    // four lanes it holds the gradient values below and adds them to:
+    //   r = 0: dmeans2d.x, dconic.C, dcolor.b     r = 1: dmeans2d.y, dopacity
+    //   r = 2: dconic.A, dcolor.r                  r = 3: dconic.B, dcolor.g
+    const int sr = int(lane >> 3), sh = int(lane & 7);
+#else
     // the sum this lane holds after the reduce-scatter, and where it goes:
     //   du = A sum(gp dx) + B sum(gp dy), dv = B sum(gp dx) + C sum(gp dy),
     //   dA = -sum(gp dx^2)/2, dB = -sum(gp dx dy), dC = -sum(gp dy^2)/2,
     //   dopacity = sum(gp)/opacity (gp = opacity exp(power) dL/dalpha), dcolour = sum(w G)
     // (the record holds the conic scaled by -log2(e)/2 and -log2(e), and 1/opacity)
     const int slot = sum_slot(lane);
-    const size_t N = size_t(n);
     float* const dst = sum_dst(slot, N, dm2, dcon, dop, dcol);
     const float kconst = slot == 2 || slot == 4 ? -0.5f : slot == 3 ? -1.f : 1.f;
 #if RS_BWD_PAIR
@@ -497,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
     float* const pdst = sum_dst(pslot, N, dm2, dcon, dop, dcol);
     const float pconst = pslot == 2 || pslot == 4 ? -0.5f : pslot == 3 ? -1.f : 1.f;
 #endif
-    constexpr float kLn2 = 0.6931471805599453f;
+#endif
     uint32_t pa = a0;
     while (true) {
         // the piece [pa, pb) of this tile's list
@@ -540,6 +577,12 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 }
             }
         }
+#if RS_BWD_DEFER
+        // the sums of the buffered hits read every lane's dL/dC (the previous piece's last read of
+        // these ended with a warp barrier)
+        s_ga[warp][lane] = make_float4(P[0].G0, P[0].G1, P[0].G2, P[1].G0);
+        s_gb[warp][lane] = make_float2(P[1].G1, P[1].G2);
+#endif
         uint32_t lane_end = P[0].end;
 #pragma unroll
         for (int h = 1; h < kBwdPx; ++h) lane_end = max(lane_end, P[h].end);
@@ -566,14 +609,23 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                 if (hit) {
                     const Record& r = rec[g];
                     const float4 p = r.p, q = r.q, c = r.c;
+#if RS_BWD_DEFER
+                    // the backward does not use the extent in p.w: it carries the Gaussian's index
+                    s_p[warp][lane] = make_float4(p.x, p.y, p.z, __uint_as_float(g));
+#else
                     s_p[warp][lane] = p;
-                    s_q[warp][lane] = q;
-                    s_c[warp][lane] = c;
                     s_g[warp][lane] = g;
                     s_k[warp][lane] = make_float4(-2.f * kLn2 * q.x, -2.f * kLn2 * q.z, c.w, -kLn2 * q.y);
+#endif
+                    s_q[warp][lane] = q;
+                    s_c[warp][lane] = c;
                 }
             }
             uint32_t m = __ballot_sync(kFull, hit);
+#if RS_BWD_DEFER
+            // the hits are taken back to front: the r-th is the one with r hits above it
+            if (hit) s_r2j[warp][__popc(m & (0xfffffffeu << lane))] = uint8_t(lane);
+#endif
             __syncwarp();
             // entry j at the lane's pixels: updates their state
             auto step = [&](int j, float& dx, float (&dy)[kBwdPx], float (&gp)[kBwdPx], float (&w)[kBwdPx]) {
@@ -592,6 +644,85 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
                     bwd_step(P[h], ej < P[h].end && al >= kAlphaMin, al, raw, c, gp[h], w[h]);
                 }
             };
+#if RS_BWD_DEFER
+            // The buffered hits' sums.  Lane (hit sh, row sr) adds up its eight lane slots as
+            // moments about the square's middle column (dx = bx + i - 3.5 at column i, dy = by0 or
+            // by1 on its two pixel rows), turns them into the hit's gradient values, and the
+            // hit's four lanes reduce-scatter those (xor 16, then xor 8) before the atomics.
+            auto flush = [&](int cnt, int r0) {
+                __syncwarp();
+                const float4* b = s_buf[warp][sh] + 8 * sr;
+                const float4* ga = s_ga[warp] + 8 * sr;
+                const float2* gb = s_gb[warp] + 8 * sr;
+                float S0 = 0.f, S1 = 0.f, X0 = 0.f, X1 = 0.f, XX = 0.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float xi = float(i) - 3.5f;
+                    const float4 v = b[i];  // (gp, gp', w, w') at the slot's two pixels
+                    const float4 g4 = ga[i];
+                    const float2 g2 = gb[i];
+                    S0 += v.x;
+                    S1 += v.y;
+                    X0 = fmaf(v.x, xi, X0);
+                    X1 = fmaf(v.y, xi, X1);
+                    XX = fmaf(v.x + v.y, xi * xi, XX);
+                    C0 = fmaf(v.z, g4.x, fmaf(v.w, g4.w, C0));
+                    C1 = fmaf(v.z, g4.y, fmaf(v.w, g2.x, C1));
+                    C2 = fmaf(v.z, g4.z, fmaf(v.w, g2.y, C2));
+                }
+                // lanes past the buffered count compute on stale slots and add nothing
+                const int j = s_r2j[warp][(r0 + sh) & 31] & 31;
+                const float4 p = s_p[warp][j], q = s_q[warp][j];
+                const float iop = s_c[warp][j].w;
+                const float bx = (float(sx) + 3.5f) - p.x;
+                const float by0 = float(sy + sr) - p.y, by1 = float(sy + sr + 4) - p.y;
+                const float S = S0 + S1, X = X0 + X1;
+                const float Sdx = fmaf(bx, S, X);          // sum gp dx
+                const float Sdx2 = fmaf(bx, Sdx + X, XX);  // sum gp dx^2
+                const float u0 = by0 * S0, u1 = by1 * S1;
+                const float Sdy = u0 + u1;                 // sum gp dy
+                const float Sdy2 = fmaf(by0, u0, by1 * u1);  // sum gp dy^2
+                const float Sdxdy = fmaf(by0, fmaf(bx, S0, X0), by1 * fmaf(bx, S1, X1));
+                // the conic from the record's log2-scaled quadratic: A = -2 ln2 qa, B = -ln2 qb, ...
+                const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
+                // (du, dv, dA, dB, dC, dopacity, dcolour): split into the values rows 0 and 1 keep
+                // (du, dv, dC, dopacity, db) and those rows 2 and 3 keep (dA, dB, dr, dg)
+                const float lo[5] = {fmaf(A, Sdx, B * Sdy), fmaf(C, Sdy, B * Sdx), -0.5f * Sdy2, iop * S, C2};
+                const float hi[5] = {-0.5f * Sdx2, -Sdxdy, C0, C1, 0.f};
+                const bool r1 = sr & 2, r0b = sr & 1;
+                float a[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) a[k] = (r1 ? hi[k] : lo[k]) + __shfl_xor_sync(kFull, r1 ? lo[k] : hi[k], 16);
+                const float v0 = (r0b ? a[1] : a[0]) + __shfl_xor_sync(kFull, r0b ? a[0] : a[1], 8);
+                const float v1 = (r0b ? a[3] : a[2]) + __shfl_xor_sync(kFull, r0b ? a[2] : a[3], 8);
+                const float v2 = (r0b ? 0.f : a[4]) + __shfl_xor_sync(kFull, r0b ? a[4] : 0.f, 8);
+                if (sh < cnt) {
+                    const size_t gi = __float_as_uint(p.w);
+                    float* const dst0 = sr == 0 ? dm2 : sr == 1 ? dm2 + N : sr == 2 ? dcon : dcon + N;
+                    float* const dst1 = sr == 0 ? dcon + 2 * N : sr == 1 ? dop : sr == 2 ? dcol : dcol + N;
+                    atomicAdd(dst0 + gi, v0);
+                    atomicAdd(dst1 + gi, v1);
+                    if (sr == 0) atomicAdd(dcol + 2 * N + gi, v2);
+                }
+                __syncwarp();  // the buffer is read before the next hits overwrite it
+            };
+            // every hit has a composited pixel in this area (the forward's flags); back to front,
+            // each hit's per-pixel values go to the buffer, which is summed when full and at the
+            // batch's end
+            int cnt = 0, r0 = 0;
+            while (m) {
+                const int j = 31 - __clz(m);
+                m ^= 1u << j;
+                float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
+                step(j, dx, dy, gp, w);
+                s_buf[warp][cnt][lane] = make_float4(gp[0], gp[1], w[0], w[1]);
+                if (++cnt == kHitBuf || m == 0u) {
+                    flush(cnt, r0);
+                    r0 += cnt;
+                    cnt = 0;
+                }
+            }
+#else
             // the lane's pixels share dx: their sums fold before the reduction over the warp
             auto fold = [&](float dx, const float (&dy)[kBwdPx], const float (&gp)[kBwdPx], const float (&w)[kBwdPx],
                             float (&v)[kSums]) {
@@ -660,6 +791,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
 #endif
                 reduce_one(j, dx, dy, gp, w);
             }
+#endif
             __syncwarp();  // the slots are read before the next batch overwrites them
             hi = lo;
         }
