@@ -33,28 +33,15 @@ constexpr int kFwdThreads = kTilePixels;  // the forward: one block of 256 threa
 constexpr int kFwdWarps = kFwdThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Backward: how an entry's sums over the warp's pixels are formed.  1 (deferred): every hit's
-// per-pixel dL/dpower and alpha T_j go to a shared-memory buffer, and once eight hits are in it
-// (or the batch ends) four lanes per hit sum them; 0: each hit's nine sums are reduced over the
-// warp at once with shuffles.
-#ifndef RS_BWD_DEFER
-#define RS_BWD_DEFER 1
-#endif
-// Shuffle form only: 1 takes the hit entries two at a time and reduces their sums together
-// (reduce18); 0 reduces entry by entry (butterfly9).
-#ifndef RS_BWD_PAIR
-#define RS_BWD_PAIR 1
-#endif
 // Resident blocks per SM the compositing kernels are compiled for (register budget per thread =
 // 65536 / (threads per block x blocks)).
 #ifndef RS_FWD_MIN_BLOCKS
 #define RS_FWD_MIN_BLOCKS 6
 #endif
-// backward (128-thread blocks): 7 with the deferred sums (72 registers: 0.192 ms on the 160k
-// 1080p orbit view, 0.202 at 8 blocks and 64 registers, 0.193 at 6); 8 with the shuffle sums (62
-// registers: 0.233 against 0.243 ms at 7)
+// backward, in groups of four one-warp blocks (one tile's squares): 7 (72 registers; 6 and 5
+// measured the same on the 160k 1080p orbit view, 8 at 64 registers slower)
 #ifndef RS_BWD_MIN_BLOCKS
-#define RS_BWD_MIN_BLOCKS (RS_BWD_PX == 4 ? 12 : RS_BWD_DEFER ? 7 : 8)
+#define RS_BWD_MIN_BLOCKS 7
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
@@ -320,130 +307,34 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
         raster_fwd_tile<false>(cam, n, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
 }
 
-// Reduce-scatter of nine per-lane values over the warp in five xor-shuffle steps (9 -> 5 -> 3
-// -> 2 -> 1 -> 1), each lane sending the half of its vector that its partner keeps.  Afterwards
-// lane L holds the warp's sum of value sum_slot(L) (lanes L and L^1 hold the same sum): 46
-// instructions instead of 9 x 5 shuffle-add pairs.
-__device__ __forceinline__ float butterfly9(const float (&v)[9], unsigned lane) {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-    float a[5];
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-        const float lo = v[k], hi = k + 5 < 9 ? v[k + 5] : 0.f;
-        a[k] = (b4 ? hi : lo) + __shfl_xor_sync(kFull, b4 ? lo : hi, 16);
-    }
-    float b[3];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        const float lo = a[k], hi = k + 3 < 5 ? a[k + 3] : 0.f;
-        b[k] = (b3 ? hi : lo) + __shfl_xor_sync(kFull, b3 ? lo : hi, 8);
-    }
-    float c[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const float lo = b[k], hi = k + 2 < 3 ? b[k + 2] : 0.f;
-        c[k] = (b2 ? hi : lo) + __shfl_xor_sync(kFull, b2 ? lo : hi, 4);
-    }
-    float d = (b1 ? c[1] : c[0]) + __shfl_xor_sync(kFull, b1 ? c[0] : c[1], 2);
-    return d + __shfl_xor_sync(kFull, d, 1);
-}
-
-// Which of the nine sums lane L holds after butterfly9 (-1: padding or the odd twin).
-__device__ __forceinline__ int sum_slot(unsigned lane) {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-    if ((lane & 1) || (b2 && b1) || (b3 && b2) || (b4 && b3 && b1)) return -1;
-    const int v = 5 * b4 + 3 * b3 + 2 * b2 + b1;
-    return v < 9 ? v : -1;
-}
-
-constexpr int kSums = 9;  // per entry: gp dx, gp dy, gp dx^2, gp dx dy, gp dy^2, gp, w G_rgb
-
-// Two entries' nine sums reduced together (18 -> 9 -> 5 -> 3 -> 2 -> 1): the first step hands
-// each half-warp one entry's vector, the rest is butterfly9's, and the last step splits the pair
-// instead of summing it twice.  Lane L then holds sum pair_slot(L) of the 18 (entry pair_slot / 9,
-// value pair_slot % 9): 20 shuffles for two entries where two butterfly9 calls take 24.
-__device__ __forceinline__ float reduce18(const float (&v)[9], const float (&u)[9], unsigned lane) {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
-    float a[9];
-#pragma unroll
-    for (int k = 0; k < 9; ++k) a[k] = (b4 ? u[k] : v[k]) + __shfl_xor_sync(kFull, b4 ? v[k] : u[k], 16);
-    float b[5];
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-        const float lo = a[k], hi = k + 5 < 9 ? a[k + 5] : 0.f;
-        b[k] = (b3 ? hi : lo) + __shfl_xor_sync(kFull, b3 ? lo : hi, 8);
-    }
-    float c[3];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        const float lo = b[k], hi = k + 3 < 5 ? b[k + 3] : 0.f;
-        c[k] = (b2 ? hi : lo) + __shfl_xor_sync(kFull, b2 ? lo : hi, 4);
-    }
-    float d[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const float lo = c[k], hi = k + 2 < 3 ? c[k + 2] : 0.f;
-        d[k] = (b1 ? hi : lo) + __shfl_xor_sync(kFull, b1 ? lo : hi, 2);
-    }
-    return (b0 ? d[1] : d[0]) + __shfl_xor_sync(kFull, b0 ? d[0] : d[1], 1);
-}
-
-// Which of the 18 sums lane L holds after reduce18 (-1: padding).  Sums 0 and 1 (and 9 and 10)
-// sit on lanes 0 and 1 (16 and 17).
-__device__ __forceinline__ int pair_slot(unsigned lane) {
-    int n = 18, real = 18, i = 0;
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        const int h = (n + 1) / 2;
-        if (lane & unsigned(m)) {
-            i += h;
-            real = max(real - h, 0);
-        } else {
-            real = min(real, h);
-        }
-        n = h;
-    }
-    return real >= 1 ? i : -1;
-}
-
-// The global array and the scale of gradient sum `slot` (0..8) of an entry.
-__device__ __forceinline__ float* sum_dst(int slot, size_t N, float* dm2, float* dcon, float* dop, float* dcol) {
-    return slot == 0 ? dm2 : slot == 1 ? dm2 + N : slot == 2 ? dcon : slot == 3 ? dcon + N
-         : slot == 4 ? dcon + 2 * N : slot == 5 ? dop : slot >= 6 ? dcol + size_t(slot - 6) * N : dm2;
-}
-
-// The backward runs one block of 128 threads per task: the entries of one 256-entry chunk of the
-// point list, [256 c, 256 c + 256), which may hold the end of one tile's list and several short
-// lists after it (pieces).  A piece that stops at the chunk's end while its tile's list goes on
-// starts each pixel from the state the forward recorded there, so a long list is walked by as
-// many blocks as it has chunks.  Within a block the four warps are independent: warp w owns the
-// 8x8 square at columns (w & 1) * 8 and rows (w >> 1) * 8 of the piece's tile, and lane l the two
-// pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4) of it.  A warp walks each piece back to
-// front, 32 entries at a time: each lane reads one entry's composited flags from the forward and,
-// where one of the two forward warps inside the square composited it (a hit), loads its record
-// into the warp's own shared-memory slots; the hits are evaluated one after another by all 64
-// pixels.  Each hit's nine sums over the square (dL/dpower times 1, dx, dy, dx^2, dx dy, dy^2,
-// and alpha T_j times dL/dC) are formed one of two ways: deferred (the default), the per-pixel
-// dL/dpower and alpha T_j go to a shared-memory buffer of eight hits, and when it is full or the
-// batch ends four lanes per hit add up its 64 pixels as moments, turn them into the Gaussian's
-// gradient values and reduce-scatter those between them; or by shuffles, the two pixels of a
-// lane folding their sums before a reduce-scatter over the whole warp.  Either way one lane per
-// value adds it to the Gaussian's gradient with a global atomic.  There is no block-wide barrier.
-// Pixels per lane, stacked 4 rows apart in one column (2: warps of 8x8; 4: warps of 8x16, which
-// cut the warp-entries by a third but measured 0.293 -> 0.303 ms with more registers per lane).
-#ifndef RS_BWD_PX
-#define RS_BWD_PX 2
-#endif
-
-constexpr int kBwdPx = RS_BWD_PX;
-static_assert(kBwdPx == 2 || kBwdPx == 4, "two or four pixels per lane");
-static_assert(!RS_BWD_DEFER || kBwdPx == 2, "the deferred sums take two pixels per lane");
-constexpr int kSqH = 4 * kBwdPx;                 // rows of a warp's area (8 columns wide)
-constexpr int kBwdWarps = 2 * (kTile / kSqH);    // warps per tile
-constexpr int kBwdThreads = 32 * kBwdWarps;
-// Deferred sums: hits buffered per warp before they are summed, and the buffer's row stride in
-// float4 (33: the four lanes of a hit read lane slots 8r + i of rows h = 0..7 in one step, and
-// the odd stride puts the eight rows on distinct banks).
+// The backward's unit of work is one 8x8 square of one 256-entry chunk of the point list,
+// [256 c, 256 c + 256), which may hold the end of one tile's list and several short lists after
+// it (pieces).  A piece that stops at the chunk's end while its tile's list goes on starts each
+// pixel from the state the forward recorded there, so a long list is walked by as many warps per
+// square as it has chunks.  Each block is one warp, persistent: it takes work items (chunk,
+// square) from a counter until the list ends.  Square s covers columns (s & 1) * 8 and rows
+// (s >> 1) * 8 of the piece's tile, and lane l the two pixels (l & 7, l >> 3) and
+// (l & 7, (l >> 3) + 4) of it.  A warp walks each piece back to front, 32 entries at a time: each
+// lane reads one entry's composited flags from the forward and, where one of the two forward
+// warps inside the square composited it (a hit), loads its record into the warp's shared-memory
+// slots; the hits are evaluated one after another by all 64 pixels.  Each hit's nine sums over
+// the square (dL/dpower times 1, dx, dy, dx^2, dx dy, dy^2, and alpha T_j times dL/dC) are
+// deferred: the per-pixel dL/dpower and alpha T_j go to a shared-memory buffer of eight hits, and
+// when it is full or the batch ends four lanes per hit add up its 64 pixels as moments, turn them
+// into the Gaussian's gradient values and reduce-scatter those between them; one lane per value
+// adds it to the Gaussian's gradient with a global atomic.  There are no block-wide barriers.
+// Measured and not kept (160k 1080p orbit view): the nine sums of each hit (or of two hits at
+// once) reduced over the whole warp with shuffles (0.220 ms against 0.192 for the deferred sums);
+// four pixels per lane on 8x16 areas; four-warp blocks, one per chunk (0.195 against 0.177 ms for
+// one-warp persistent blocks: a block's warps finish at different times and its slot waits for
+// the last).
+constexpr int kBwdPx = 2;                        // pixels per lane, 4 rows apart in one column
+constexpr int kSqH = 4 * kBwdPx;                 // rows of a square (8 columns wide)
+constexpr int kBwdWarps = 2 * (kTile / kSqH);    // squares per tile
+constexpr int kBwdThreads = 32;                  // one warp per block
+// Hits buffered per warp before they are summed, and the buffer's row stride in float4 (33: the
+// four lanes of a hit read lane slots 8r + i of rows h = 0..7 in one step, and the odd stride
+// puts the eight rows on distinct banks).
 constexpr int kHitBuf = 8;
 constexpr int kHitStride = 33;
 
@@ -470,349 +361,259 @@ __device__ __forceinline__ void bwd_step(BwdPixel& px, bool act, float alpha, fl
     gp = raw <= kAlphaMax ? w * d : 0.f;  // alpha dL/dalpha; not clamped: alpha = opacity exp(power)
 }
 
-__global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS) k_raster_bwd(
+__global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_raster_bwd(
     CameraF cam, int n, const Record* __restrict__ rec, const uint2* __restrict__ ranges,
     const uint32_t* __restrict__ list, float3 bg,
     const float* __restrict__ final_T, const uint32_t* __restrict__ n_contrib,
     const uint32_t* __restrict__ chunk_tile, const float4* __restrict__ ckpt, uint32_t slots,
     const uint8_t* __restrict__ comp, uint32_t cap, const float* __restrict__ dL_dimage, float* __restrict__ dm2,
-    float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol) {
+    float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol, uint32_t* __restrict__ work) {
     RS_PDL_ENTER();
-    __shared__ float4 s_p[kBwdWarps][32], s_q[kBwdWarps][32], s_c[kBwdWarps][32];
-#if RS_BWD_DEFER
+    __shared__ float4 s_p[32], s_q[32], s_c[32];
     // per buffered hit h and lane L: (dL/dpower, alpha T_j) at the lane's two pixels
-    __shared__ float4 s_buf[kBwdWarps][kHitBuf][kHitStride];
+    __shared__ float4 s_buf[kHitBuf][kHitStride];
     // dL/dC at lane L's two pixels: (G0, G1, G2 of the first, G0 of the second), (G1, G2 of it)
-    __shared__ float4 s_ga[kBwdWarps][32];
-    __shared__ float2 s_gb[kBwdWarps][32];
+    __shared__ float4 s_ga[32];
+    __shared__ float2 s_gb[32];
     // staged slot of the batch's r-th hit (back to front)
-    __shared__ uint8_t s_r2j[kBwdWarps][32];
-#else
-    __shared__ uint32_t s_g[kBwdWarps][32];
-    // per staged entry, the factors of its sums in the gradient: (dA-row and dC-row factors of
-    // du and dv, 1 / opacity, the B factor), see the comment on `slot` below
-    __shared__ float4 s_k[kBwdWarps][32];
-#endif
+    __shared__ uint8_t s_r2j[32];
     const uint32_t n_tiles = uint32_t(cam.TX) * uint32_t(cam.TY);
-    const uint32_t a0 = blockIdx.x * kChunk, a1 = a0 + kChunk;
-    // the tile holding position a0; a chunk past the end of the list has none
-    uint32_t tile = chunk_tile[blockIdx.x];
-    if (tile >= n_tiles) return;
-    uint2 range = ranges[tile];
-    if (!(range.x <= a0 && a0 < range.y)) return;
-    if (range.y > cap) {
-        // caller data out of range (the forward drew this tile empty)
-        if (threadIdx.x == 0) atomicOr(&g_raster_check, 1u);
-        return;
-    }
-    const int warp = threadIdx.x >> 5;
-    const unsigned lane = threadIdx.x & 31;
+    const unsigned lane = threadIdx.x;
     const size_t HW = size_t(cam.W) * cam.H;
     const size_t N = size_t(n);
     constexpr float kLn2 = 0.6931471805599453f;
-#if RS_BWD_DEFER
     // Summing buffered hits, lane L serves hit L & 7 and the lane slots 8r .. 8r + 7 (pixel rows r
     // and r + 4 of the square, columns 0..7), r = L >> 3; after the reduce-scatter over the hit's
     // four lanes it holds the gradient values below and adds them to:
     //   r = 0: dmeans2d.x, dconic.C, dcolor.b     r = 1: dmeans2d.y, dopacity
     //   r = 2: dconic.A, dcolor.r                  r = 3: dconic.B, dcolor.g
     const int sr = int(lane >> 3), sh = int(lane & 7);
-#else
-    // the sum this lane holds after the reduce-scatter, and where it goes:
-    //   du = A sum(gp dx) + B sum(gp dy), dv = B sum(gp dx) + C sum(gp dy),
-    //   dA = -sum(gp dx^2)/2, dB = -sum(gp dx dy), dC = -sum(gp dy^2)/2,
-    //   dopacity = sum(gp)/opacity (gp = opacity exp(power) dL/dalpha), dcolour = sum(w G)
-    // (the record holds the conic scaled by -log2(e)/2 and -log2(e), and 1/opacity)
-    const int slot = sum_slot(lane);
-    float* const dst = sum_dst(slot, N, dm2, dcon, dop, dcol);
-    const float kconst = slot == 2 || slot == 4 ? -0.5f : slot == 3 ? -1.f : 1.f;
-#if RS_BWD_PAIR
-    // the same for the sums of an entry pair (second entry: pair_slot >= 9)
-    const int pidx = pair_slot(lane);
-    const bool psecond = pidx >= 9;
-    const int pslot = pidx < 0 ? -1 : psecond ? pidx - 9 : pidx;
-    float* const pdst = sum_dst(pslot, N, dm2, dcon, dop, dcol);
-    const float pconst = pslot == 2 || pslot == 4 ? -0.5f : pslot == 3 ? -1.f : 1.f;
-#endif
-#endif
-    uint32_t pa = a0;
-    while (true) {
-        // the piece [pa, pb) of this tile's list
-        const uint32_t pb = min(range.y, a1);
-        const int tx0 = int(tile % uint32_t(cam.TX)) * kTile, ty0 = int(tile / uint32_t(cam.TX)) * kTile;
-        const int sx = tx0 + (warp & 1) * 8, sy = ty0 + (warp >> 1) * kSqH;
-        const int px = sx + int(lane & 7);
-        const int py0 = sy + int(lane >> 3);
-        const uint32_t len = range.y - range.x;
-        BwdPixel P[kBwdPx];
-#pragma unroll
-        for (int h = 0; h < kBwdPx; ++h) {
-            const int py = py0 + 4 * h;
-            const bool inside = px < cam.W && py < cam.H;
-            const size_t pix = inside ? size_t(py) * cam.W + px : 0;
-            // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the
-            // min() keeps inconsistent caller data inside the tile's list
-            const uint32_t end = range.x + (inside ? min(n_contrib[pix], len) : 0u);
-            P[h].end = min(end, pb);
-            P[h].G0 = P[h].G1 = P[h].G2 = 0.f;
-            P[h].T = 1.f;
-            P[h].SG = 0.f;
-            if (end > pa) {
-                P[h].G0 = dL_dimage[pix];
-                P[h].G1 = dL_dimage[HW + pix];
-                P[h].G2 = dL_dimage[2 * HW + pix];
-                const uint32_t ck = pb / kChunk;
-                if (end > pb && ck < slots) {
-                    // the pixel goes on past the chunk: resume from the forward's state at pb,
-                    // (colour behind pb, T); the colour behind per unit T enters as its dot
-                    // product with dL/dC
-                    const float4 f = ckpt[size_t(ck) * kTilePixels + (py - ty0) * kTile + (px - tx0)];
-                    P[h].T = f.w;
-                    P[h].SG = __fdividef(fmaf(P[h].G0, f.x, fmaf(P[h].G1, f.y, P[h].G2 * f.z)), f.w);
-                } else {
-                    // the colour behind an entry (per unit T) only enters the gradient through
-                    // its dot product with dL/dC, so that scalar is carried instead of the colour
-                    P[h].T = final_T[pix];
-                    P[h].SG = bg.x * P[h].G0 + bg.y * P[h].G1 + bg.z * P[h].G2;
-                }
-            }
+    // Persistent warps: warp w starts with (chunk, square) item w and, each time it finishes one,
+    // takes the next in increasing order from work[0] (offset by the grid's warp count) until it
+    // meets a chunk past the list's end; every later item is past it too.  An item is claimed only
+    // when a warp is free for it (claimed ahead, it would wait behind the claimant's current item
+    // while other warps idle at the end: 0.200 against 0.177 ms).  The last warp to leave resets
+    // the counter.
+    const uint32_t n_warps = gridDim.x;
+    uint32_t item = blockIdx.x;
+    for (;; item = __shfl_sync(kFull, lane == 0 ? n_warps + atomicAdd(work, 1u) : 0u, 0)) {
+        const uint32_t chunk = item / uint32_t(kBwdWarps);
+        const int sq = int(item % uint32_t(kBwdWarps));
+        if (chunk >= slots) break;
+        const uint32_t a0 = chunk * kChunk, a1 = a0 + kChunk;
+        // the tile holding position a0; a chunk past the end of the list has none
+        uint32_t tile = chunk_tile[chunk];
+        if (tile >= n_tiles) break;
+        uint2 range = ranges[tile];
+        if (!(range.x <= a0 && a0 < range.y)) break;
+        if (range.y > cap) {
+            // caller data out of range (the forward drew this tile empty)
+            if (lane == 0) atomicOr(&g_raster_check, 1u);
+            continue;
         }
-#if RS_BWD_DEFER
-        // the sums of the buffered hits read every lane's dL/dC (the previous piece's last read of
-        // these ended with a warp barrier)
-        s_ga[warp][lane] = make_float4(P[0].G0, P[0].G1, P[0].G2, P[1].G0);
-        s_gb[warp][lane] = make_float2(P[1].G1, P[1].G2);
-#endif
-        uint32_t lane_end = P[0].end;
-#pragma unroll
-        for (int h = 1; h < kBwdPx; ++h) lane_end = max(lane_end, P[h].end);
-        const uint32_t warp_end = __reduce_max_sync(kFull, lane_end);
-        const float fx = float(px), fy0 = float(py0);
-        // the forward's warps (8x4 pixels) inside this warp's area: an entry none of them
-        // composited has no active pixel here
-        uint32_t fwarps = 0u;
-#pragma unroll
-        for (int r = 0; r < kSqH / 4; ++r) fwarps |= 1u << (((sy - ty0) / 4 + r) * 2 + (warp & 1));
-        for (uint32_t hi = warp_end; hi > pa;) {
-            const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
-            const uint32_t e = lo + lane;
-            bool hit = false;
-            if (e < hi) {
-                // an entry some forward warp of this area composited (its alpha >= 1/255 box
-                // meets the area then too): only those records are loaded
-                const uint32_t g = list[e];
-                hit = (uint32_t(comp[e]) & fwarps) != 0u;
-                if (hit && g >= uint32_t(n)) {
-                    atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
-                    hit = false;
-                }
-                if (hit) {
-                    const Record& r = rec[g];
-                    const float4 p = r.p, q = r.q, c = r.c;
-#if RS_BWD_DEFER
-                    // the backward does not use the extent in p.w: it carries the Gaussian's index
-                    s_p[warp][lane] = make_float4(p.x, p.y, p.z, __uint_as_float(g));
-#else
-                    s_p[warp][lane] = p;
-                    s_g[warp][lane] = g;
-                    s_k[warp][lane] = make_float4(-2.f * kLn2 * q.x, -2.f * kLn2 * q.z, c.w, -kLn2 * q.y);
-#endif
-                    s_q[warp][lane] = q;
-                    s_c[warp][lane] = c;
-                }
-            }
-            uint32_t m = __ballot_sync(kFull, hit);
-#if RS_BWD_DEFER
-            // the hits are taken back to front: the r-th is the one with r hits above it
-            if (hit) s_r2j[warp][__popc(m & (0xfffffffeu << lane))] = uint8_t(lane);
-#endif
-            __syncwarp();
-            // entry j at the lane's pixels: updates their state
-            auto step = [&](int j, float& dx, float (&dy)[kBwdPx], float (&gp)[kBwdPx], float (&w)[kBwdPx]) {
-                const uint32_t ej = lo + uint32_t(j);
-                const float4 p = s_p[warp][j], q = s_q[warp][j];
-                // the lane's pixels share a column: dx and its terms are common (the same
-                // arithmetic as entry_alpha, pixel by pixel)
-                dx = fx - p.x;
-                const float bx = q.y * dx, axx = (q.x * dx) * dx;
-                const float4 c = s_c[warp][j];
-#pragma unroll
-                for (int h = 0; h < kBwdPx; ++h) {
-                    dy[h] = (fy0 + float(4 * h)) - p.y;
-                    const float raw = p.z * ex2_approx(fmaf(dy[h], fmaf(q.z, dy[h], bx), axx));
-                    const float al = fminf(kAlphaMax, raw);
-                    bwd_step(P[h], ej < P[h].end && al >= kAlphaMin, al, raw, c, gp[h], w[h]);
-                }
-            };
-#if RS_BWD_DEFER
-            // The buffered hits' sums.  Lane (hit sh, row sr) adds up its eight lane slots as
-            // moments about the square's middle column (dx = bx + i - 3.5 at column i, dy = by0 or
-            // by1 on its two pixel rows), turns them into the hit's gradient values, and the
-            // hit's four lanes reduce-scatter those (xor 16, then xor 8) before the atomics.
-            auto flush = [&](int cnt, int r0) {
-                __syncwarp();
-                const float4* b = s_buf[warp][sh] + 8 * sr;
-                const float4* ga = s_ga[warp] + 8 * sr;
-                const float2* gb = s_gb[warp] + 8 * sr;
-                float S0 = 0.f, S1 = 0.f, X0 = 0.f, X1 = 0.f, XX = 0.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float xi = float(i) - 3.5f;
-                    const float4 v = b[i];  // (gp, gp', w, w') at the slot's two pixels
-                    const float4 g4 = ga[i];
-                    const float2 g2 = gb[i];
-                    S0 += v.x;
-                    S1 += v.y;
-                    X0 = fmaf(v.x, xi, X0);
-                    X1 = fmaf(v.y, xi, X1);
-                    XX = fmaf(v.x + v.y, xi * xi, XX);
-                    C0 = fmaf(v.z, g4.x, fmaf(v.w, g4.w, C0));
-                    C1 = fmaf(v.z, g4.y, fmaf(v.w, g2.x, C1));
-                    C2 = fmaf(v.z, g4.z, fmaf(v.w, g2.y, C2));
-                }
-                // lanes past the buffered count compute on stale slots and add nothing
-                const int j = s_r2j[warp][(r0 + sh) & 31] & 31;
-                const float4 p = s_p[warp][j], q = s_q[warp][j];
-                const float iop = s_c[warp][j].w;
-                const float bx = (float(sx) + 3.5f) - p.x;
-                const float by0 = float(sy + sr) - p.y, by1 = float(sy + sr + 4) - p.y;
-                const float S = S0 + S1, X = X0 + X1;
-                const float Sdx = fmaf(bx, S, X);          // sum gp dx
-                const float Sdx2 = fmaf(bx, Sdx + X, XX);  // sum gp dx^2
-                const float u0 = by0 * S0, u1 = by1 * S1;
-                const float Sdy = u0 + u1;                 // sum gp dy
-                const float Sdy2 = fmaf(by0, u0, by1 * u1);  // sum gp dy^2
-                const float Sdxdy = fmaf(by0, fmaf(bx, S0, X0), by1 * fmaf(bx, S1, X1));
-                // the conic from the record's log2-scaled quadratic: A = -2 ln2 qa, B = -ln2 qb, ...
-                const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
-                // (du, dv, dA, dB, dC, dopacity, dcolour): split into the values rows 0 and 1 keep
-                // (du, dv, dC, dopacity, db) and those rows 2 and 3 keep (dA, dB, dr, dg)
-                const float lo[5] = {fmaf(A, Sdx, B * Sdy), fmaf(C, Sdy, B * Sdx), -0.5f * Sdy2, iop * S, C2};
-                const float hi[5] = {-0.5f * Sdx2, -Sdxdy, C0, C1, 0.f};
-                const bool r1 = sr & 2, r0b = sr & 1;
-                float a[5];
-#pragma unroll
-                for (int k = 0; k < 5; ++k) a[k] = (r1 ? hi[k] : lo[k]) + __shfl_xor_sync(kFull, r1 ? lo[k] : hi[k], 16);
-                const float v0 = (r0b ? a[1] : a[0]) + __shfl_xor_sync(kFull, r0b ? a[0] : a[1], 8);
-                const float v1 = (r0b ? a[3] : a[2]) + __shfl_xor_sync(kFull, r0b ? a[2] : a[3], 8);
-                const float v2 = (r0b ? 0.f : a[4]) + __shfl_xor_sync(kFull, r0b ? a[4] : 0.f, 8);
-                if (sh < cnt) {
-                    const size_t gi = __float_as_uint(p.w);
-                    float* const dst0 = sr == 0 ? dm2 : sr == 1 ? dm2 + N : sr == 2 ? dcon : dcon + N;
-                    float* const dst1 = sr == 0 ? dcon + 2 * N : sr == 1 ? dop : sr == 2 ? dcol : dcol + N;
-                    atomicAdd(dst0 + gi, v0);
-                    atomicAdd(dst1 + gi, v1);
-                    if (sr == 0) atomicAdd(dcol + 2 * N + gi, v2);
-                }
-                __syncwarp();  // the buffer is read before the next hits overwrite it
-            };
-            // every hit has a composited pixel in this area (the forward's flags); back to front,
-            // each hit's per-pixel values go to the buffer, which is summed when full and at the
-            // batch's end
-            int cnt = 0, r0 = 0;
-            while (m) {
-                const int j = 31 - __clz(m);
-                m ^= 1u << j;
-                float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
-                step(j, dx, dy, gp, w);
-                s_buf[warp][cnt][lane] = make_float4(gp[0], gp[1], w[0], w[1]);
-                if (++cnt == kHitBuf || m == 0u) {
-                    flush(cnt, r0);
-                    r0 += cnt;
-                    cnt = 0;
-                }
-            }
-#else
-            // the lane's pixels share dx: their sums fold before the reduction over the warp
-            auto fold = [&](float dx, const float (&dy)[kBwdPx], const float (&gp)[kBwdPx], const float (&w)[kBwdPx],
-                            float (&v)[kSums]) {
-                float sg = gp[0], sgy = gp[0] * dy[0], sgyy = (gp[0] * dy[0]) * dy[0];
-                float c0 = w[0] * P[0].G0, c1 = w[0] * P[0].G1, c2 = w[0] * P[0].G2;
-#pragma unroll
-                for (int h = 1; h < kBwdPx; ++h) {
-                    sg += gp[h];
-                    const float t = gp[h] * dy[h];
-                    sgy += t;
-                    sgyy = fmaf(t, dy[h], sgyy);
-                    c0 = fmaf(w[h], P[h].G0, c0);
-                    c1 = fmaf(w[h], P[h].G1, c1);
-                    c2 = fmaf(w[h], P[h].G2, c2);
-                }
-                v[0] = sg * dx;
-                v[1] = sgy;
-                v[2] = v[0] * dx;
-                v[3] = sgy * dx;
-                v[4] = sgyy;
-                v[5] = sg;
-                v[6] = c0;
-                v[7] = c1;
-                v[8] = c2;
-            };
-            // one entry's sums over the warp, added to its Gaussian's gradient by nine lanes
-            auto reduce_one = [&](int j, float dx, const float (&dy)[kBwdPx], const float (&gp)[kBwdPx],
-                                  const float (&w)[kBwdPx]) {
-                float v[kSums];
-                fold(dx, dy, gp, w, v);
-                const float sum = butterfly9(v, lane);
-                const float other = __shfl_xor_sync(kFull, sum, 2);  // slots 0 and 1: lanes 0 and 2
-                if (slot >= 0) {
-                    const float4 f = s_k[warp][j];
-                    const float a = slot == 0 ? f.x : slot == 1 ? f.y : slot == 5 ? f.z : kconst;
-                    atomicAdd(dst + s_g[warp][j], fmaf(a, sum, slot < 2 ? f.w * other : 0.f));
-                }
-            };
-            // every hit has a composited pixel in this area (the forward's flags), so each one's sums
-            // go out without a vote; the hits are taken two at a time (back to front), their 18 sums
-            // in one reduction, an odd last one alone
-            while (m) {
-                const int j = 31 - __clz(m);
-                m ^= 1u << j;
-                float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
-                step(j, dx, dy, gp, w);
-#if RS_BWD_PAIR
-                if (m) {
-                    const int k = 31 - __clz(m);
-                    m ^= 1u << k;
-                    float dx2, dy2[kBwdPx], gp2[kBwdPx], w2[kBwdPx];
-                    step(k, dx2, dy2, gp2, w2);
-                    float v[kSums], u[kSums];
-                    fold(dx, dy, gp, w, v);
-                    fold(dx2, dy2, gp2, w2, u);
-                    const float sum = reduce18(v, u, lane);
-                    const float other = __shfl_xor_sync(kFull, sum, 1);  // slots 0 and 1: lanes 2i, 2i + 1
-                    if (pslot >= 0) {
-                        const int jj = psecond ? k : j;
-                        const float4 f = s_k[warp][jj];
-                        const float a = pslot == 0 ? f.x : pslot == 1 ? f.y : pslot == 5 ? f.z : pconst;
-                        atomicAdd(pdst + s_g[warp][jj], fmaf(a, sum, pslot < 2 ? f.w * other : 0.f));
+        uint32_t pa = a0;
+        while (true) {
+            // the piece [pa, pb) of this tile's list
+            const uint32_t pb = min(range.y, a1);
+            const int tx0 = int(tile % uint32_t(cam.TX)) * kTile, ty0 = int(tile / uint32_t(cam.TX)) * kTile;
+            const int sx = tx0 + (sq & 1) * 8, sy = ty0 + (sq >> 1) * kSqH;
+            const int px = sx + int(lane & 7);
+            const int py0 = sy + int(lane >> 3);
+            const uint32_t len = range.y - range.x;
+            BwdPixel P[kBwdPx];
+    #pragma unroll
+            for (int h = 0; h < kBwdPx; ++h) {
+                const int py = py0 + 4 * h;
+                const bool inside = px < cam.W && py < cam.H;
+                const size_t pix = inside ? size_t(py) * cam.W + px : 0;
+                // n_contrib never exceeds the list length when it comes from rs_rasterize_fwd; the
+                // min() keeps inconsistent caller data inside the tile's list
+                const uint32_t end = range.x + (inside ? min(n_contrib[pix], len) : 0u);
+                P[h].end = min(end, pb);
+                P[h].G0 = P[h].G1 = P[h].G2 = 0.f;
+                P[h].T = 1.f;
+                P[h].SG = 0.f;
+                if (end > pa) {
+                    P[h].G0 = dL_dimage[pix];
+                    P[h].G1 = dL_dimage[HW + pix];
+                    P[h].G2 = dL_dimage[2 * HW + pix];
+                    const uint32_t ck = pb / kChunk;
+                    if (end > pb && ck < slots) {
+                        // the pixel goes on past the chunk: resume from the forward's state at pb,
+                        // (colour behind pb, T); the colour behind per unit T enters as its dot
+                        // product with dL/dC
+                        const float4 f = ckpt[size_t(ck) * kTilePixels + (py - ty0) * kTile + (px - tx0)];
+                        P[h].T = f.w;
+                        P[h].SG = __fdividef(fmaf(P[h].G0, f.x, fmaf(P[h].G1, f.y, P[h].G2 * f.z)), f.w);
+                    } else {
+                        // the colour behind an entry (per unit T) only enters the gradient through
+                        // its dot product with dL/dC, so that scalar is carried instead of the colour
+                        P[h].T = final_T[pix];
+                        P[h].SG = bg.x * P[h].G0 + bg.y * P[h].G1 + bg.z * P[h].G2;
                     }
-                    continue;
                 }
-#endif
-                reduce_one(j, dx, dy, gp, w);
             }
-#endif
-            __syncwarp();  // the slots are read before the next batch overwrites them
-            hi = lo;
-        }
-        if (pb >= a1) break;
-        // this tile's list ended inside the chunk: the next non-empty list starts at pb (unless
-        // pb is the end of the point list)
-        uint32_t next = n_tiles;
-        for (uint32_t u = tile + 1; u < n_tiles; u += 32) {
-            const uint32_t t = u + lane;
-            const uint2 r = t < n_tiles ? ranges[t] : make_uint2(0u, 0u);
-            const uint32_t b = __ballot_sync(kFull, r.y > r.x);
-            if (b) {
-                next = u + uint32_t(__ffs(b) - 1);
-                break;
+            // the sums of the buffered hits read every lane's dL/dC (the previous piece's last read of
+            // these ended with a warp barrier)
+            s_ga[lane] = make_float4(P[0].G0, P[0].G1, P[0].G2, P[1].G0);
+            s_gb[lane] = make_float2(P[1].G1, P[1].G2);
+            uint32_t lane_end = P[0].end;
+    #pragma unroll
+            for (int h = 1; h < kBwdPx; ++h) lane_end = max(lane_end, P[h].end);
+            const uint32_t warp_end = __reduce_max_sync(kFull, lane_end);
+            const float fx = float(px), fy0 = float(py0);
+            // the forward's warps (8x4 pixels) inside this warp's area: an entry none of them
+            // composited has no active pixel here
+            uint32_t fwarps = 0u;
+    #pragma unroll
+            for (int r = 0; r < kSqH / 4; ++r) fwarps |= 1u << (((sy - ty0) / 4 + r) * 2 + (sq & 1));
+            for (uint32_t hi = warp_end; hi > pa;) {
+                const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
+                const uint32_t e = lo + lane;
+                bool hit = false;
+                if (e < hi) {
+                    // an entry some forward warp of this area composited (its alpha >= 1/255 box
+                    // meets the area then too): only those records are loaded
+                    const uint32_t g = list[e];
+                    hit = (uint32_t(comp[e]) & fwarps) != 0u;
+                    if (hit && g >= uint32_t(n)) {
+                        atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
+                        hit = false;
+                    }
+                    if (hit) {
+                        const Record& r = rec[g];
+                        const float4 p = r.p, q = r.q, c = r.c;
+                        // the backward does not use the extent in p.w: it carries the Gaussian's index
+                        s_p[lane] = make_float4(p.x, p.y, p.z, __uint_as_float(g));
+                        s_q[lane] = q;
+                        s_c[lane] = c;
+                    }
+                }
+                uint32_t m = __ballot_sync(kFull, hit);
+                // the hits are taken back to front: the r-th is the one with r hits above it
+                if (hit) s_r2j[__popc(m & (0xfffffffeu << lane))] = uint8_t(lane);
+                __syncwarp();
+                // entry j at the lane's pixels: updates their state
+                auto step = [&](int j, float& dx, float (&dy)[kBwdPx], float (&gp)[kBwdPx], float (&w)[kBwdPx]) {
+                    const uint32_t ej = lo + uint32_t(j);
+                    const float4 p = s_p[j], q = s_q[j];
+                    // the lane's pixels share a column: dx and its terms are common (the same
+                    // arithmetic as entry_alpha, pixel by pixel)
+                    dx = fx - p.x;
+                    const float bx = q.y * dx, axx = (q.x * dx) * dx;
+                    const float4 c = s_c[j];
+    #pragma unroll
+                    for (int h = 0; h < kBwdPx; ++h) {
+                        dy[h] = (fy0 + float(4 * h)) - p.y;
+                        const float raw = p.z * ex2_approx(fmaf(dy[h], fmaf(q.z, dy[h], bx), axx));
+                        const float al = fminf(kAlphaMax, raw);
+                        bwd_step(P[h], ej < P[h].end && al >= kAlphaMin, al, raw, c, gp[h], w[h]);
+                    }
+                };
+                // The buffered hits' sums.  Lane (hit sh, row sr) adds up its eight lane slots as
+                // moments about the square's middle column (dx = bx + i - 3.5 at column i, dy = by0 or
+                // by1 on its two pixel rows), turns them into the hit's gradient values, and the
+                // hit's four lanes reduce-scatter those (xor 16, then xor 8) before the atomics.
+                auto flush = [&](int cnt, int r0) {
+                    __syncwarp();
+                    const float4* b = s_buf[sh] + 8 * sr;
+                    const float4* ga = s_ga + 8 * sr;
+                    const float2* gb = s_gb + 8 * sr;
+                    float S0 = 0.f, S1 = 0.f, X0 = 0.f, X1 = 0.f, XX = 0.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float xi = float(i) - 3.5f;
+                        const float4 v = b[i];  // (gp, gp', w, w') at the slot's two pixels
+                        const float4 g4 = ga[i];
+                        const float2 g2 = gb[i];
+                        S0 += v.x;
+                        S1 += v.y;
+                        X0 = fmaf(v.x, xi, X0);
+                        X1 = fmaf(v.y, xi, X1);
+                        XX = fmaf(v.x + v.y, xi * xi, XX);
+                        C0 = fmaf(v.z, g4.x, fmaf(v.w, g4.w, C0));
+                        C1 = fmaf(v.z, g4.y, fmaf(v.w, g2.x, C1));
+                        C2 = fmaf(v.z, g4.z, fmaf(v.w, g2.y, C2));
+                    }
+                    // lanes past the buffered count compute on stale slots and add nothing
+                    const int j = s_r2j[(r0 + sh) & 31] & 31;
+                    const float4 p = s_p[j], q = s_q[j];
+                    const float iop = s_c[j].w;
+                    const float bx = (float(sx) + 3.5f) - p.x;
+                    const float by0 = float(sy + sr) - p.y, by1 = float(sy + sr + 4) - p.y;
+                    const float S = S0 + S1, X = X0 + X1;
+                    const float Sdx = fmaf(bx, S, X);          // sum gp dx
+                    const float Sdx2 = fmaf(bx, Sdx + X, XX);  // sum gp dx^2
+                    const float u0 = by0 * S0, u1 = by1 * S1;
+                    const float Sdy = u0 + u1;                 // sum gp dy
+                    const float Sdy2 = fmaf(by0, u0, by1 * u1);  // sum gp dy^2
+                    const float Sdxdy = fmaf(by0, fmaf(bx, S0, X0), by1 * fmaf(bx, S1, X1));
+                    // the conic from the record's log2-scaled quadratic: A = -2 ln2 qa, B = -ln2 qb, ...
+                    const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
+                    // (du, dv, dA, dB, dC, dopacity, dcolour): split into the values rows 0 and 1 keep
+                    // (du, dv, dC, dopacity, db) and those rows 2 and 3 keep (dA, dB, dr, dg)
+                    const float lo[5] = {fmaf(A, Sdx, B * Sdy), fmaf(C, Sdy, B * Sdx), -0.5f * Sdy2, iop * S, C2};
+                    const float hi[5] = {-0.5f * Sdx2, -Sdxdy, C0, C1, 0.f};
+                    const bool r1 = sr & 2, r0b = sr & 1;
+                    float a[5];
+    #pragma unroll
+                    for (int k = 0; k < 5; ++k)
+                        a[k] = (r1 ? hi[k] : lo[k]) + __shfl_xor_sync(kFull, r1 ? lo[k] : hi[k], 16);
+                    const float v0 = (r0b ? a[1] : a[0]) + __shfl_xor_sync(kFull, r0b ? a[0] : a[1], 8);
+                    const float v1 = (r0b ? a[3] : a[2]) + __shfl_xor_sync(kFull, r0b ? a[2] : a[3], 8);
+                    const float v2 = (r0b ? 0.f : a[4]) + __shfl_xor_sync(kFull, r0b ? a[4] : 0.f, 8);
+                    if (sh < cnt) {
+                        const size_t gi = __float_as_uint(p.w);
+                        float* const dst0 = sr == 0 ? dm2 : sr == 1 ? dm2 + N : sr == 2 ? dcon : dcon + N;
+                        float* const dst1 = sr == 0 ? dcon + 2 * N : sr == 1 ? dop : sr == 2 ? dcol : dcol + N;
+                        atomicAdd(dst0 + gi, v0);
+                        atomicAdd(dst1 + gi, v1);
+                        if (sr == 0) atomicAdd(dcol + 2 * N + gi, v2);
+                    }
+                    __syncwarp();  // the buffer is read before the next hits overwrite it
+                };
+                // every hit has a composited pixel in this area (the forward's flags); back to front,
+                // each hit's per-pixel values go to the buffer, which is summed when full and at the
+                // batch's end
+                int cnt = 0, r0 = 0;
+                while (m) {
+                    const int j = 31 - __clz(m);
+                    m ^= 1u << j;
+                    float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
+                    step(j, dx, dy, gp, w);
+                    s_buf[cnt][lane] = make_float4(gp[0], gp[1], w[0], w[1]);
+                    if (++cnt == kHitBuf || m == 0u) {
+                        flush(cnt, r0);
+                        r0 += cnt;
+                        cnt = 0;
+                    }
+                }
+                __syncwarp();  // the slots are read before the next batch overwrites them
+                hi = lo;
             }
+            if (pb >= a1) break;
+            // this tile's list ended inside the chunk: the next non-empty list starts at pb (unless
+            // pb is the end of the point list)
+            uint32_t nt = n_tiles;
+            for (uint32_t u = tile + 1; u < n_tiles; u += 32) {
+                const uint32_t t = u + lane;
+                const uint2 r = t < n_tiles ? ranges[t] : make_uint2(0u, 0u);
+                const uint32_t b = __ballot_sync(kFull, r.y > r.x);
+                if (b) {
+                    nt = u + uint32_t(__ffs(b) - 1);
+                    break;
+                }
+            }
+            if (nt >= n_tiles) break;
+            tile = nt;
+            range = ranges[tile];
+            if (range.x != pb || range.y > cap) break;
+            pa = pb;
         }
-        if (next >= n_tiles) break;
-        tile = next;
-        range = ranges[tile];
-        if (range.x != pb || range.y > cap) break;
-        pa = pb;
+    }
+    if (lane == 0 && atomicAdd(work + 1, 1u) == n_warps - 1u) {
+        work[0] = 0u;
+        work[1] = 0u;
     }
 }
 
@@ -852,6 +653,7 @@ struct RasterWs {
     float4* ckpt;           // [slots][256] the forward's state at position 256 c
     uint32_t* order;        // [n_tiles] tiles in the forward's order
     uint8_t* comp;          // [capacity] per entry: the forward warps (8x4 pixels) that composited it
+    uint32_t* work;         // [2] the backward's next work item and count of finished warps
     uint32_t slots;
 };
 size_t align256z(size_t x) { return (x + 255) & ~size_t(255); }
@@ -867,7 +669,9 @@ RasterWs raster_ws(void* ws, size_t capacity, size_t n_tiles, size_t* bytes = nu
     w.ckpt = reinterpret_cast<float4*>(b + o);
     o = align256z(o + slots * kTilePixels * sizeof(float4));
     w.comp = b + o;
-    o += capacity;
+    o = align256z(o + capacity);
+    w.work = reinterpret_cast<uint32_t*>(b + o);
+    o += 2 * sizeof(uint32_t);
     w.slots = uint32_t(slots);
     if (bytes) *bytes = o;
     return w;
@@ -888,8 +692,14 @@ __device__ __forceinline__ int tile_class(uint2 r) {
 }
 
 __global__ void __launch_bounds__(kOrderThreads) k_tile_order(const uint2* __restrict__ ranges, uint32_t n_tiles,
-                                                             uint32_t* __restrict__ order) {
+                                                             uint32_t* __restrict__ order,
+                                                             uint32_t* __restrict__ work) {
     RS_PDL_ENTER();
+    // the backward's work counter starts at zero after every forward (each backward leaves it there)
+    if (threadIdx.x == 0) {
+        work[0] = 0u;
+        work[1] = 0u;
+    }
     __shared__ uint32_t s_cnt[kClasses][kOrderWarps];
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5, lt = (1u << lane) - 1u;
     // 1. per warp and class: the number of tiles
@@ -963,7 +773,8 @@ cudaError_t launch_raster_fwd(const CameraF& cam, int32_t n, const Record* rec, 
                               uint32_t* n_contrib, void* ws, cudaStream_t s) {
     const int tiles = cam.TX * cam.TY;
     const RasterWs w = raster_ws(ws, capacity, size_t(tiles));
-    pdl_launch(k_tile_order, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order);
+    pdl_launch(k_tile_order, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order,
+               w.work);
     pdl_launch(k_raster_fwd, tiles, kFwdThreads, 0, s, cam, uint32_t(n), uint32_t(capacity), rec,
                reinterpret_cast<const uint2*>(ranges), list,
                                                bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
@@ -973,16 +784,23 @@ cudaError_t launch_raster_fwd(const CameraF& cam, int32_t n, const Record* rec, 
 
 cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
                               const uint32_t* ranges, const uint32_t* list, size_t capacity, float3 bg,
-                              const float* final_T, const uint32_t* n_contrib, const void* ws,
+                              const float* final_T, const uint32_t* n_contrib, void* ws,
                               const float* dL_dimage, float* dm2, float* dcon, float* dop, float* dcol,
                               cudaStream_t s) {
-    const RasterWs w = raster_ws(const_cast<void*>(ws), capacity, size_t(cam.TX) * cam.TY);
-    // one block per chunk of the capacity; chunks past the list's end return at once
-    const unsigned blocks = unsigned((capacity + kChunk - 1) / kChunk);
-    if (blocks == 0) return cudaSuccess;
-    pdl_launch(k_raster_bwd, blocks, kBwdThreads, 0, s, cam, n, rec, reinterpret_cast<const uint2*>(ranges), list, bg,
-                                                final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots, w.comp,
-                                                uint32_t(capacity), dL_dimage, dm2, dcon, dop, dcol);
+    const RasterWs w = raster_ws(ws, capacity, size_t(cam.TX) * cam.TY);
+    // one-warp blocks, as many as fit on the GPU at once (at most one per item of the capacity),
+    // each taking (chunk, square) items until the list ends
+    const size_t chunks = (capacity + kChunk - 1) / kChunk;
+    if (chunks == 0) return cudaSuccess;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_raster_bwd, kBwdThreads, 0);
+    if (e != cudaSuccess) return e;
+    const size_t blocks = std::min(chunks * size_t(kBwdWarps), size_t(std::max(sms, 1)) * size_t(std::max(per_sm, 1)));
+    pdl_launch(k_raster_bwd, unsigned(blocks), kBwdThreads, 0, s, cam, n, rec, reinterpret_cast<const uint2*>(ranges),
+               list, bg, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots, w.comp, uint32_t(capacity), dL_dimage,
+               dm2, dcon, dop, dcol, w.work);
     return cudaGetLastError();
 }
 

@@ -195,7 +195,7 @@ int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t 
 int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
                      const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
                      const float* bg, const float* d_final_T, const uint32_t* d_n_contrib,
-                     const void* d_workspace, size_t workspace_bytes,
+                     void* d_workspace, size_t workspace_bytes,
                      const float* d_dL_dimage, float* d_dL_dmeans2d, float* d_dL_dconic,
                      float* d_dL_dopacity, float* d_dL_dcolor, void* stream) {
     if (!camera_ok(camera) || !n_ok(n) || !bg || capacity > size_t(RS_MAX_ENTRIES)) return RS_ERR_INVALID_ARG;

@@ -278,7 +278,7 @@ cudaError_t launch_raster_fwd(const CameraF& cam, int32_t n, const Record* rec, 
                               uint32_t* n_contrib, void* ws, cudaStream_t s);
 cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
                               const uint32_t* ranges, const uint32_t* list, size_t capacity, float3 bg,
-                              const float* final_T, const uint32_t* n_contrib, const void* ws,
+                              const float* final_T, const uint32_t* n_contrib, void* ws,
                               const float* dL_dimage, float* dm2, float* dcon, float* dop, float* dcol,
                               cudaStream_t s);
 // Fill a background image (n = 0 or no entries): image = bg, final_T = 1, n_contrib = 0.

@@ -182,7 +182,8 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
  * the point list that falls inside a tile's list, and which tile holds each such position (the
  * backward reads both to walk every 256-entry stretch of the point list as a task of its own);
  * per entry, which 8x4-pixel groups of its tile composited it (the backward skips the others);
- * and the order in which the forward takes the tiles (longest lists first).
+ * the order in which the forward takes the tiles (longest lists first); and the backward's work
+ * counter.
  * Returns the bytes a point list of `capacity` entries needs for this camera's tile grid; 0 for
  * an invalid camera or capacity > RS_MAX_ENTRIES.  Host-only (no GPU work). */
 #define RS_RASTER_CHUNK 256
@@ -216,9 +217,12 @@ int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t 
  * The walk is split at every RS_RASTER_CHUNK-th position of the point list: a stretch that ends
  * inside a tile's list starts from the state the forward recorded there (T, and the colour
  * behind that position) instead of from final_T, so long lists are walked in parallel.
- * Per-pixel contributions are reduced across each warp before they reach global memory.
+ * Per-pixel contributions are reduced across each 8x8 pixel square before they reach global
+ * memory.
  * Inputs: the forward's tile_ranges, point_list, capacity, final_T, n_contrib and workspace (as
- * rs_rasterize_fwd left them), bg (host float[3]) and d_dL_dimage [3][H][W].
+ * rs_rasterize_fwd left them), bg (host float[3]) and d_dL_dimage [3][H][W].  The call hands out
+ * its work through a counter of 8 bytes in the workspace, which the forward sets to zero and the
+ * call leaves at zero: two rs_rasterize_bwd calls must not use one workspace at the same time.
  * Outputs (zeroed, then accumulated by the call):
  * d_dL_dmeans2d [2][n], d_dL_dconic [3][n], d_dL_dopacity [n], d_dL_dcolor [3][n].
  * The accumulation order is not fixed, so results may differ in the last bits between runs.
@@ -228,7 +232,7 @@ int rs_rasterize_fwd(const rs_camera* camera, const rs_projected* proj, int32_t 
 int rs_rasterize_bwd(const rs_camera* camera, const rs_projected* proj, int32_t n,
                      const uint32_t* d_tile_ranges, const uint32_t* d_point_list, size_t capacity,
                      const float* bg, const float* d_final_T, const uint32_t* d_n_contrib,
-                     const void* d_workspace, size_t workspace_bytes,
+                     void* d_workspace, size_t workspace_bytes,
                      const float* d_dL_dimage, float* d_dL_dmeans2d, float* d_dL_dconic,
                      float* d_dL_dopacity, float* d_dL_dcolor, void* stream);
 

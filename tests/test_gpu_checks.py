@@ -92,3 +92,23 @@ def test_range_past_the_capacity_draws_the_tile_empty_and_is_reported():
     rs.rs_rasterize_bwd(cam, R.proj, n, ranges, R.point_list, (0.0, 0.0, 0.0), fT, nc, R.raster_ws, dL, *gr)
     assert rs.rs_device_error() in (rs.RS_ERR_DEVICE_CHECK, rs.RS_OK)
     assert all(torch.isfinite(x).all() for x in gr)
+
+
+def test_backward_twice_on_one_forward():
+    # the backward hands out its work through a counter in the workspace that the forward zeroes;
+    # the call leaves it at zero, so a second backward on the same forward state covers every
+    # chunk again (the gradients agree up to the order of the atomic additions)
+    g, cam, dg, R = rendered(seed=2)
+    dL = torch.from_numpy(scenes.image_grad(cam)).to(R.image.device)
+    n = g.n
+    runs = []
+    for _ in range(3):
+        gr = [torch.empty(k * n, dtype=torch.float32, device=R.image.device) for k in (2, 3, 1, 3)]
+        rs.rs_rasterize_bwd(cam, R.proj, n, R.tile_ranges, R.point_list, (0.0, 0.0, 0.0), R.final_T, R.n_contrib,
+                            R.raster_ws, dL, *gr)
+        torch.cuda.synchronize()
+        assert rs.rs_device_error() == rs.RS_OK
+        runs.append(gr)
+    for a, b in zip(runs[0], runs[2]):
+        assert torch.count_nonzero(a) > 0
+        assert torch.allclose(a, b, rtol=1e-4, atol=1e-6 * float(a.abs().max()))
