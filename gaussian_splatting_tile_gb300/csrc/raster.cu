@@ -331,7 +331,10 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
 // one-warp persistent blocks: a block's warps finish at different times and its slot waits for
 // the last); the two pixels' arithmetic and the buffer sums in paired fp32 instructions (f32x2:
 // 9% fewer instructions, but issue fell from 74% to 65% of cycles and the kernel took 187 against
-// 176 us; the buffer sums alone: 6% fewer, the same time).
+// 176 us; the buffer sums alone: 6% fewer, the same time); the items taken heaviest first (a
+// kernel between forward and backward filing each item in one of seven classes by the count of
+// its composited entries: 0.182 against 0.178 ms, the heavy items of the dense regions running all
+// at once).
 constexpr int kBwdPx = 2;                        // pixels per lane, 4 rows apart in one column
 constexpr int kSqH = 4 * kBwdPx;                 // rows of a square (8 columns wide)
 constexpr int kBwdWarps = 2 * (kTile / kSqH);    // squares per tile
