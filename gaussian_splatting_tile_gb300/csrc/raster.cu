@@ -26,17 +26,27 @@ namespace {
 // capacity (caller data): the entry or the tile is skipped instead of read out of bounds.
 __device__ unsigned int g_raster_check;
 
-constexpr int kBatch = kTilePixels;  // 256 entries staged per round, one per thread
+constexpr int kBatch = kTilePixels;  // 256 entries staged per round
 constexpr uint32_t kChunk = RS_RASTER_CHUNK;  // backward task length and checkpoint spacing
 static_assert(kChunk == uint32_t(kBatch), "a forward batch ends at every chunk boundary");
-constexpr int kFwdThreads = kTilePixels;  // the forward: one block of 256 threads per tile
+// The forward's block: 1, half a tile (16x8 pixels, 128 threads, two blocks per tile, each
+// staging the tile's batches for its own four warps); 0, the whole tile (256 threads).  A batch
+// waits at the block barrier for its slowest warp; with four warps instead of eight the slowest
+// one carries 1.34 instead of 1.64 times the mean work (counted with the oracle on the 160k
+// 1080p view): 0.131 -> 0.128 ms, issue 75% -> 79% of cycles for 1% more instructions.
+#ifndef RS_FWD_HALF
+#define RS_FWD_HALF 1
+#endif
+constexpr int kFwdHalves = RS_FWD_HALF ? 2 : 1;
+constexpr int kFwdThreads = kTilePixels / kFwdHalves;
 constexpr int kFwdWarps = kFwdThreads / 32;
+constexpr int kFwdRows = kTile / kFwdHalves;  // pixel rows of a forward block
 constexpr unsigned kFull = 0xffffffffu;
 
 // Resident blocks per SM the compositing kernels are compiled for (register budget per thread =
 // 65536 / (threads per block x blocks)).
 #ifndef RS_FWD_MIN_BLOCKS
-#define RS_FWD_MIN_BLOCKS 6
+#define RS_FWD_MIN_BLOCKS (RS_FWD_HALF ? 12 : 6)
 #endif
 // backward, in groups of four one-warp blocks (one tile's squares): 7 (72 registers; 6 and 5
 // measured the same on the 160k 1080p orbit view, 8 at 64 registers slower)
@@ -45,14 +55,16 @@ constexpr unsigned kFull = 0xffffffffu;
 #endif
 
 // Pixel of this thread: warp w owns the 8x4 sub-rectangle at columns (w & 1) * 8 and rows
-// (w >> 1) * 4 of the tile; lane l is pixel (l & 7, l >> 3) inside it.
-__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int& tx0, int& ty0, int& px,
-                                           int& py) {
+// (w >> 1) * 4 of the block's region, which starts at row ry0 = ty0 + kFwdRows * half of the
+// tile; lane l is pixel (l & 7, l >> 3) inside it.
+__device__ __forceinline__ void tile_pixel(const CameraF& cam, int tile, int half, int& tx0, int& ty0, int& ry0,
+                                           int& px, int& py) {
     tx0 = (tile % cam.TX) * kTile;
     ty0 = (tile / cam.TX) * kTile;
+    ry0 = ty0 + kFwdRows * half;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     px = tx0 + (warp & 1) * 8 + (lane & 7);
-    py = ty0 + (warp >> 1) * 4 + (lane >> 3);
+    py = ry0 + (warp >> 1) * 4 + (lane >> 3);
 }
 
 // Bit w is set when warp w's 8x4 pixel rectangle meets the entry's alpha >= 1/255 box
@@ -157,10 +169,10 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, 
                                                 const uint32_t* __restrict__ list, float3 bg,
                                                 float* __restrict__ image, float* __restrict__ final_T,
                                                 uint32_t* __restrict__ n_contrib, float4* __restrict__ ckpt,
-                                                uint32_t slots, uint8_t* __restrict__ comp, FwdSmem& sm) {
+                                                uint32_t slots, uint8_t* __restrict__ comp, int half, FwdSmem& sm) {
     const int warp = threadIdx.x >> 5;
-    int tx0, ty0, px, py;
-    tile_pixel(cam, int(tile), tx0, ty0, px, py);
+    int tx0, ty0, ry0, px, py;
+    tile_pixel(cam, int(tile), half, tx0, ty0, ry0, px, py);
     const bool inside = px < cam.W && py < cam.H;
     const float fx = float(px), fy = float(py);
     float T = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
@@ -181,29 +193,34 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, 
         }
         // every thread reaches this barrier; the block leaves once all its pixels are done
         const int ndone = __syncthreads_count(done);
-        if (pbase + threadIdx.x < pend) comp[pbase + threadIdx.x] = comp_byte(sm, threadIdx.x);
+#pragma unroll
+        for (int t = threadIdx.x; t < kBatch; t += kFwdThreads)
+            if (pbase + uint32_t(t) < pend) comp[pbase + t] = comp_byte(sm, t);
         pbase = base;
         pend = 0u;
         if (ndone == kFwdThreads) break;
         pend = bend;
-        const uint32_t e = base + threadIdx.x;
-        uint32_t m = 0u;
-        if (e < bend) {
-            const uint32_t g = list[e];
-            if (g >= n) {
-                atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
-            } else {
-                const Record& r = rec[g];
-                sm.p[threadIdx.x] = r.p;
-                sm.q[threadIdx.x] = r.q;
-                sm.c[threadIdx.x] = r.c;
-                m = warp_mask(r.p, r.q, tx0, ty0);
+#pragma unroll
+        for (int t = threadIdx.x; t < kBatch; t += kFwdThreads) {
+            const uint32_t e = base + uint32_t(t);
+            uint32_t m = 0u;
+            if (e < bend) {
+                const uint32_t g = list[e];
+                if (g >= n) {
+                    atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
+                } else {
+                    const Record& r = rec[g];
+                    sm.p[t] = r.p;
+                    sm.q[t] = r.q;
+                    sm.c[t] = r.c;
+                    m = warp_mask(r.p, r.q, tx0, ry0);
 #if RS_FWD_EXACT_MASK
-                if (m) m = warp_mask_exact(m, r.p, r.q, r.c, tx0, ty0);
+                    if (m) m = warp_mask_exact(m, r.p, r.q, r.c, tx0, ry0);
 #endif
+                }
             }
+            sm.mask[t] = m;
         }
-        sm.mask[threadIdx.x] = m;
         __syncthreads();
         // this warp's composited flags for the batch (the previous batch's were gathered before
         // the barrier above)
@@ -252,7 +269,9 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, 
         }
     }
     __syncthreads();
-    if (pbase + threadIdx.x < pend) comp[pbase + threadIdx.x] = comp_byte(sm, threadIdx.x);
+#pragma unroll
+    for (int t = threadIdx.x; t < kBatch; t += kFwdThreads)
+        if (pbase + uint32_t(t) < pend) comp[pbase + t] = comp_byte(sm, t);
     if (inside) {
         const size_t HW = size_t(cam.W) * cam.H, pix = size_t(py) * cam.W + px;
         image[pix] = fmaf(T, bg.x, C0);
@@ -288,10 +307,14 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
                                                            uint32_t* __restrict__ chunk_tile,
                                                            float4* __restrict__ ckpt, uint32_t slots,
                                                            const uint32_t* __restrict__ order,
-                                                           uint8_t* __restrict__ comp) {
+                                                           uint8_t* __restrict__ comp, size_t comp_stride) {
     RS_PDL_ENTER();
     __shared__ FwdSmem sm;
-    const uint32_t tile = order[blockIdx.x];
+    // blocks take the tiles in order, a tile's halves one after the other; half h writes its
+    // composited flags to its own array (comp + h comp_stride)
+    const uint32_t tile = order[blockIdx.x / uint32_t(kFwdHalves)];
+    const int half = int(blockIdx.x % uint32_t(kFwdHalves));
+    comp += size_t(half) * comp_stride;
     uint2 range = ranges[tile];
     if (range.y > cap || range.x > range.y) {
         // caller data out of range: the tile is drawn empty
@@ -300,13 +323,16 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
     }
     // the tile's list positions that are multiples of the chunk size are the backward's task
     // starts: record which tile holds them
-    for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x; c < (range.y + kChunk - 1) / kChunk && c < slots;
-         c += kFwdThreads)
-        chunk_tile[c] = tile;
+    if (half == 0)
+        for (uint32_t c = (range.x + kChunk - 1) / kChunk + threadIdx.x;
+             c < (range.y + kChunk - 1) / kChunk && c < slots; c += kFwdThreads)
+            chunk_tile[c] = tile;
     if (range.y > range.x && (range.y - 1u) / kChunk > range.x / kChunk)
-        raster_fwd_tile<true>(cam, n, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
+        raster_fwd_tile<true>(cam, n, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, half,
+                              sm);
     else
-        raster_fwd_tile<false>(cam, n, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, sm);
+        raster_fwd_tile<false>(cam, n, rec, tile, range, list, bg, image, final_T, n_contrib, ckpt, slots, comp, half,
+                               sm);
 }
 
 // The backward's unit of work is one 8x8 square of one 256-entry chunk of the point list,
@@ -373,8 +399,9 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
     const uint32_t* __restrict__ list, float3 bg,
     const float* __restrict__ final_T, const uint32_t* __restrict__ n_contrib,
     const uint32_t* __restrict__ chunk_tile, const float4* __restrict__ ckpt, uint32_t slots,
-    const uint8_t* __restrict__ comp, uint32_t cap, const float* __restrict__ dL_dimage, float* __restrict__ dm2,
-    float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol, uint32_t* __restrict__ work) {
+    const uint8_t* __restrict__ comp, size_t comp_stride, uint32_t cap, const float* __restrict__ dL_dimage,
+    float* __restrict__ dm2, float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol,
+    uint32_t* __restrict__ work) {
     RS_PDL_ENTER();
     __shared__ float4 s_p[32], s_q[32], s_c[32];
     // per buffered hit h and lane L: (dL/dpower, alpha T_j) at the lane's two pixels
@@ -428,7 +455,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
             const int py0 = sy + int(lane >> 3);
             const uint32_t len = range.y - range.x;
             BwdPixel P[kBwdPx];
-    #pragma unroll
+#pragma unroll
             for (int h = 0; h < kBwdPx; ++h) {
                 const int py = py0 + 4 * h;
                 const bool inside = px < cam.W && py < cam.H;
@@ -465,15 +492,18 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
             s_ga[lane] = make_float4(P[0].G0, P[0].G1, P[0].G2, P[1].G0);
             s_gb[lane] = make_float2(P[1].G1, P[1].G2);
             uint32_t lane_end = P[0].end;
-    #pragma unroll
+#pragma unroll
             for (int h = 1; h < kBwdPx; ++h) lane_end = max(lane_end, P[h].end);
             const uint32_t warp_end = __reduce_max_sync(kFull, lane_end);
             const float fx = float(px), fy0 = float(py0);
-            // the forward's warps (8x4 pixels) inside this warp's area: an entry none of them
-            // composited has no active pixel here
+            // the forward's warps (8x4 pixels) inside this warp's area, numbered within the forward
+            // block's region (the square's half of the tile with half-tile blocks): an entry none
+            // of them composited has no active pixel here
+            const int fr0 = (sy - ty0) / 4 - (RS_FWD_HALF ? 2 * (sq >> 1) : 0);
+            const uint8_t* const compq = comp + (RS_FWD_HALF ? size_t(sq >> 1) * comp_stride : size_t(0));
             uint32_t fwarps = 0u;
-    #pragma unroll
-            for (int r = 0; r < kSqH / 4; ++r) fwarps |= 1u << (((sy - ty0) / 4 + r) * 2 + (sq & 1));
+#pragma unroll
+            for (int r = 0; r < kSqH / 4; ++r) fwarps |= 1u << ((fr0 + r) * 2 + (sq & 1));
             for (uint32_t hi = warp_end; hi > pa;) {
                 const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
                 const uint32_t e = lo + lane;
@@ -482,7 +512,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                     // an entry some forward warp of this area composited (its alpha >= 1/255 box
                     // meets the area then too): only those records are loaded
                     const uint32_t g = list[e];
-                    hit = (uint32_t(comp[e]) & fwarps) != 0u;
+                    hit = (uint32_t(compq[e]) & fwarps) != 0u;
                     if (hit && g >= uint32_t(n)) {
                         atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
                         hit = false;
@@ -509,7 +539,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                     dx = fx - p.x;
                     const float bx = q.y * dx, axx = (q.x * dx) * dx;
                     const float4 c = s_c[j];
-    #pragma unroll
+#pragma unroll
                     for (int h = 0; h < kBwdPx; ++h) {
                         dy[h] = (fy0 + float(4 * h)) - p.y;
                         const float raw = p.z * ex2_approx(fmaf(dy[h], fmaf(q.z, dy[h], bx), axx));
@@ -527,7 +557,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                     const float4* ga = s_ga + 8 * sr;
                     const float2* gb = s_gb + 8 * sr;
                     float S0 = 0.f, S1 = 0.f, X0 = 0.f, X1 = 0.f, XX = 0.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float xi = float(i) - 3.5f;
                         const float4 v = b[i];  // (gp, gp', w, w') at the slot's two pixels
@@ -563,7 +593,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                     const float hi[5] = {-0.5f * Sdx2, -Sdxdy, C0, C1, 0.f};
                     const bool r1 = sr & 2, r0b = sr & 1;
                     float a[5];
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < 5; ++k)
                         a[k] = (r1 ? hi[k] : lo[k]) + __shfl_xor_sync(kFull, r1 ? lo[k] : hi[k], 16);
                     const float v0 = (r0b ? a[1] : a[0]) + __shfl_xor_sync(kFull, r0b ? a[0] : a[1], 8);
@@ -659,7 +689,8 @@ struct RasterWs {
     uint32_t* chunk_tile;   // [slots] tile holding list position 256 c
     float4* ckpt;           // [slots][256] the forward's state at position 256 c
     uint32_t* order;        // [n_tiles] tiles in the forward's order
-    uint8_t* comp;          // [capacity] per entry: the forward warps (8x4 pixels) that composited it
+    uint8_t* comp;          // [halves][comp_stride] per entry: the forward warps (8x4 pixels) that composited it
+    size_t comp_stride;     // the capacity rounded up to 256
     uint32_t* work;         // [2] the backward's next work item and count of finished warps
     uint32_t slots;
 };
@@ -676,7 +707,8 @@ RasterWs raster_ws(void* ws, size_t capacity, size_t n_tiles, size_t* bytes = nu
     w.ckpt = reinterpret_cast<float4*>(b + o);
     o = align256z(o + slots * kTilePixels * sizeof(float4));
     w.comp = b + o;
-    o = align256z(o + capacity);
+    w.comp_stride = align256z(capacity);
+    o += size_t(kFwdHalves) * w.comp_stride;
     w.work = reinterpret_cast<uint32_t*>(b + o);
     o += 2 * sizeof(uint32_t);
     w.slots = uint32_t(slots);
@@ -782,10 +814,9 @@ cudaError_t launch_raster_fwd(const CameraF& cam, int32_t n, const Record* rec, 
     const RasterWs w = raster_ws(ws, capacity, size_t(tiles));
     pdl_launch(k_tile_order, 1, kOrderThreads, 0, s, reinterpret_cast<const uint2*>(ranges), uint32_t(tiles), w.order,
                w.work);
-    pdl_launch(k_raster_fwd, tiles, kFwdThreads, 0, s, cam, uint32_t(n), uint32_t(capacity), rec,
-               reinterpret_cast<const uint2*>(ranges), list,
-                                               bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots,
-                                               w.order, w.comp);
+    pdl_launch(k_raster_fwd, unsigned(tiles * kFwdHalves), kFwdThreads, 0, s, cam, uint32_t(n), uint32_t(capacity),
+               rec, reinterpret_cast<const uint2*>(ranges), list, bg, image, final_T, n_contrib, w.chunk_tile, w.ckpt,
+               w.slots, w.order, w.comp, w.comp_stride);
     return cudaGetLastError();
 }
 
@@ -806,8 +837,8 @@ cudaError_t launch_raster_bwd(const CameraF& cam, int32_t n, const Record* rec,
     if (e != cudaSuccess) return e;
     const size_t blocks = std::min(chunks * size_t(kBwdWarps), size_t(std::max(sms, 1)) * size_t(std::max(per_sm, 1)));
     pdl_launch(k_raster_bwd, unsigned(blocks), kBwdThreads, 0, s, cam, n, rec, reinterpret_cast<const uint2*>(ranges),
-               list, bg, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots, w.comp, uint32_t(capacity), dL_dimage,
-               dm2, dcon, dop, dcol, w.work);
+               list, bg, final_T, n_contrib, w.chunk_tile, w.ckpt, w.slots, w.comp, w.comp_stride,
+               uint32_t(capacity), dL_dimage, dm2, dcon, dop, dcol, w.work);
     return cudaGetLastError();
 }
 
