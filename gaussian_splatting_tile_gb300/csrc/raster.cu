@@ -409,8 +409,6 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
     // dL/dC at lane L's two pixels: (G0, G1, G2 of the first, G0 of the second), (G1, G2 of it)
     __shared__ float4 s_ga[32];
     __shared__ float2 s_gb[32];
-    // staged slot of the batch's r-th hit (back to front)
-    __shared__ uint8_t s_r2j[32];
     const uint32_t n_tiles = uint32_t(cam.TX) * uint32_t(cam.TY);
     const unsigned lane = threadIdx.x;
     const size_t HW = size_t(cam.W) * cam.H;
@@ -508,32 +506,36 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                 const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
                 const uint32_t e = lo + lane;
                 bool hit = false;
+                uint32_t g = 0u;
                 if (e < hi) {
                     // an entry some forward warp of this area composited (its alpha >= 1/255 box
                     // meets the area then too): only those records are loaded
-                    const uint32_t g = list[e];
+                    g = list[e];
                     hit = (uint32_t(compq[e]) & fwarps) != 0u;
                     if (hit && g >= uint32_t(n)) {
                         atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
                         hit = false;
                     }
-                    if (hit) {
-                        const Record& r = rec[g];
-                        const float4 p = r.p, q = r.q, c = r.c;
-                        // the backward does not use the extent in p.w: it carries the Gaussian's index
-                        s_p[lane] = make_float4(p.x, p.y, p.z, __uint_as_float(g));
-                        s_q[lane] = q;
-                        s_c[lane] = c;
-                    }
                 }
-                uint32_t m = __ballot_sync(kFull, hit);
-                // the hits are taken back to front: the r-th is the one with r hits above it
-                if (hit) s_r2j[__popc(m & (0xfffffffeu << lane))] = uint8_t(lane);
+                const uint32_t m = __ballot_sync(kFull, hit);
+                const int nh = __popc(m);
+                if (hit) {
+                    // the hits are taken back to front and staged in that order: slot r holds the
+                    // hit with r hits above it, so that a buffer's hits sit in consecutive slots
+                    const int r = __popc(m & (0xfffffffeu << lane));
+                    const Record& rc = rec[g];
+                    const float4 p = rc.p, q = rc.q, c = rc.c;
+                    // the backward uses neither extent: p.w carries the Gaussian's index, q.w the
+                    // entry's list position
+                    s_p[r] = make_float4(p.x, p.y, p.z, __uint_as_float(g));
+                    s_q[r] = make_float4(q.x, q.y, q.z, __uint_as_float(e));
+                    s_c[r] = c;
+                }
                 __syncwarp();
-                // entry j at the lane's pixels: updates their state
+                // the hit in slot j at the lane's pixels: updates their state
                 auto step = [&](int j, float& dx, float (&dy)[kBwdPx], float (&gp)[kBwdPx], float (&w)[kBwdPx]) {
-                    const uint32_t ej = lo + uint32_t(j);
                     const float4 p = s_p[j], q = s_q[j];
+                    const uint32_t ej = __float_as_uint(q.w);
                     // the lane's pixels share a column: dx and its terms are common (the same
                     // arithmetic as entry_alpha, pixel by pixel)
                     dx = fx - p.x;
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                         C2 = fmaf(v.z, g4.z, fmaf(v.w, g2.y, C2));
                     }
                     // lanes past the buffered count compute on stale slots and add nothing
-                    const int j = s_r2j[(r0 + sh) & 31] & 31;
+                    const int j = (r0 + sh) & 31;
                     const float4 p = s_p[j], q = s_q[j];
                     const float iop = s_c[j].w;
                     const float bx = (float(sx) + 3.5f) - p.x;
@@ -613,13 +615,11 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                 // each hit's per-pixel values go to the buffer, which is summed when full and at the
                 // batch's end
                 int cnt = 0, r0 = 0;
-                while (m) {
-                    const int j = 31 - __clz(m);
-                    m ^= 1u << j;
+                for (int j = 0; j < nh; ++j) {
                     float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
                     step(j, dx, dy, gp, w);
                     s_buf[cnt][lane] = make_float4(gp[0], gp[1], w[0], w[1]);
-                    if (++cnt == kHitBuf || m == 0u) {
+                    if (++cnt == kHitBuf || j == nh - 1) {
                         flush(cnt, r0);
                         r0 += cnt;
                         cnt = 0;
