@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
 // slots; the hits are evaluated one after another by all 64 pixels.  Each hit's nine sums over
 // the square (dL/dpower times 1, dx, dy, dx^2, dx dy, dy^2, and alpha T_j times dL/dC) are
 // deferred: the per-pixel dL/dpower and alpha T_j go to a shared-memory buffer of eight hits, and
-// when it is full or the batch ends four lanes per hit add up its 64 pixels as moments, turn them
+// when it is full or the piece ends four lanes per hit add up its 64 pixels as moments, turn them
 // into the Gaussian's gradient values and reduce-scatter those between them; one lane per value
 // adds it to the Gaussian's gradient with a global atomic.  There are no block-wide barriers.
 // Measured and not kept (160k 1080p orbit view): the nine sums of each hit (or of two hits at
@@ -370,6 +370,7 @@ constexpr int kBwdThreads = 32;                  // one warp per block
 // puts the eight rows on distinct banks).
 constexpr int kHitBuf = 8;
 constexpr int kHitStride = 33;
+constexpr int kSlots = 32 + kHitBuf;  // record slots of the staged hits
 
 // Per-pixel state of the reverse walk.
 struct BwdPixel {
@@ -403,7 +404,8 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
     float* __restrict__ dm2, float* __restrict__ dcon, float* __restrict__ dop, float* __restrict__ dcol,
     uint32_t* __restrict__ work) {
     RS_PDL_ENTER();
-    __shared__ float4 s_p[32], s_q[32], s_c[32];
+    // staged hits: up to kHitBuf - 1 carried over from the previous batch, then this batch's
+    __shared__ float4 s_p[kSlots], s_q[kSlots], s_c[kSlots];
     // per buffered hit h and lane L: (dL/dpower, alpha T_j) at the lane's two pixels
     __shared__ float4 s_buf[kHitBuf][kHitStride];
     // dL/dC at lane L's two pixels: (G0, G1, G2 of the first, G0 of the second), (G1, G2 of it)
@@ -502,9 +504,91 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
             uint32_t fwarps = 0u;
 #pragma unroll
             for (int r = 0; r < kSqH / 4; ++r) fwarps |= 1u << ((fr0 + r) * 2 + (sq & 1));
+            // The buffered hits' sums.  Lane (hit sh, row sr) adds up its eight lane slots as
+            // moments about the square's middle column (dx = bx + i - 3.5 at column i, dy = by0 or
+            // by1 on its two pixel rows), turns them into the hit's gradient values, and the
+            // hit's four lanes reduce-scatter those (xor 16, then xor 8) before the atomics.
+            auto flush = [&](int cnt, int r0) {
+                __syncwarp();
+                const float4* b = s_buf[sh] + 8 * sr;
+                const float4* ga = s_ga + 8 * sr;
+                const float2* gb = s_gb + 8 * sr;
+                float S0 = 0.f, S1 = 0.f, X0 = 0.f, X1 = 0.f, XX = 0.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float xi = float(i) - 3.5f;
+                    const float4 v = b[i];  // (gp, gp', w, w') at the slot's two pixels
+                    const float4 g4 = ga[i];
+                    const float2 g2 = gb[i];
+                    S0 += v.x;
+                    S1 += v.y;
+                    X0 = fmaf(v.x, xi, X0);
+                    X1 = fmaf(v.y, xi, X1);
+                    XX = fmaf(v.x + v.y, xi * xi, XX);
+                    C0 = fmaf(v.z, g4.x, fmaf(v.w, g4.w, C0));
+                    C1 = fmaf(v.z, g4.y, fmaf(v.w, g2.x, C1));
+                    C2 = fmaf(v.z, g4.z, fmaf(v.w, g2.y, C2));
+                }
+                // lanes past the buffered count compute on stale slots and add nothing
+                const int j = min(r0 + sh, kSlots - 1);
+                const float4 p = s_p[j], q = s_q[j];
+                const float iop = s_c[j].w;
+                const float bx = (float(sx) + 3.5f) - p.x;
+                const float by0 = float(sy + sr) - p.y, by1 = float(sy + sr + 4) - p.y;
+                const float S = S0 + S1, X = X0 + X1;
+                const float Sdx = fmaf(bx, S, X);          // sum gp dx
+                const float Sdx2 = fmaf(bx, Sdx + X, XX);  // sum gp dx^2
+                const float u0 = by0 * S0, u1 = by1 * S1;
+                const float Sdy = u0 + u1;                 // sum gp dy
+                const float Sdy2 = fmaf(by0, u0, by1 * u1);  // sum gp dy^2
+                const float Sdxdy = fmaf(by0, fmaf(bx, S0, X0), by1 * fmaf(bx, S1, X1));
+                // the conic from the record's log2-scaled quadratic: A = -2 ln2 qa, B = -ln2 qb, ...
+                const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
+                // (du, dv, dA, dB, dC, dopacity, dcolour): split into the values rows 0 and 1 keep
+                // (du, dv, dC, dopacity, db) and those rows 2 and 3 keep (dA, dB, dr, dg)
+                const float lo[5] = {fmaf(A, Sdx, B * Sdy), fmaf(C, Sdy, B * Sdx), -0.5f * Sdy2, iop * S, C2};
+                const float hi[5] = {-0.5f * Sdx2, -Sdxdy, C0, C1, 0.f};
+                const bool r1 = sr & 2, r0b = sr & 1;
+                float a[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k)
+                    a[k] = (r1 ? hi[k] : lo[k]) + __shfl_xor_sync(kFull, r1 ? lo[k] : hi[k], 16);
+                const float v0 = (r0b ? a[1] : a[0]) + __shfl_xor_sync(kFull, r0b ? a[0] : a[1], 8);
+                const float v1 = (r0b ? a[3] : a[2]) + __shfl_xor_sync(kFull, r0b ? a[2] : a[3], 8);
+                const float v2 = (r0b ? 0.f : a[4]) + __shfl_xor_sync(kFull, r0b ? a[4] : 0.f, 8);
+                if (sh < cnt) {
+                    const size_t gi = __float_as_uint(p.w);
+                    float* const dst0 = sr == 0 ? dm2 : sr == 1 ? dm2 + N : sr == 2 ? dcon : dcon + N;
+                    float* const dst1 = sr == 0 ? dcon + 2 * N : sr == 1 ? dop : sr == 2 ? dcol : dcol + N;
+                    atomicAdd(dst0 + gi, v0);
+                    atomicAdd(dst1 + gi, v1);
+                    if (sr == 0) atomicAdd(dcol + 2 * N + gi, v2);
+                }
+                __syncwarp();  // the buffer is read before the next hits overwrite it
+            };
+            // the buffered hits: slots r0 .. r0 + cnt - 1, buffer rows 0 .. cnt - 1; a buffer not
+            // yet full at a batch's end is carried into the next batch
+            int cnt = 0, r0 = 0;
             for (uint32_t hi = warp_end; hi > pa;) {
                 const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
                 const uint32_t e = lo + lane;
+                if (r0 > 0 && cnt > 0) {
+                    // the carried hits move to the front slots (r0 >= kHitBuf > cnt: no overlap)
+                    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c = a;
+                    if (int(lane) < cnt) {
+                        a = s_p[r0 + lane];
+                        b = s_q[r0 + lane];
+                        c = s_c[r0 + lane];
+                    }
+                    __syncwarp();
+                    if (int(lane) < cnt) {
+                        s_p[lane] = a;
+                        s_q[lane] = b;
+                        s_c[lane] = c;
+                    }
+                    __syncwarp();
+                }
+                r0 = 0;
                 bool hit = false;
                 uint32_t g = 0u;
                 if (e < hi) {
@@ -520,9 +604,10 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                 const uint32_t m = __ballot_sync(kFull, hit);
                 const int nh = __popc(m);
                 if (hit) {
-                    // the hits are taken back to front and staged in that order: slot r holds the
-                    // hit with r hits above it, so that a buffer's hits sit in consecutive slots
-                    const int r = __popc(m & (0xfffffffeu << lane));
+                    // the hits are taken back to front and staged in that order after the carried
+                    // ones: slot cnt + r holds the hit with r hits above it, so that a buffer's hits
+                    // sit in consecutive slots
+                    const int r = cnt + __popc(m & (0xfffffffeu << lane));
                     const Record& rc = rec[g];
                     const float4 p = rc.p, q = rc.q, c = rc.c;
                     // the backward uses neither extent: p.w carries the Gaussian's index, q.w the
@@ -549,77 +634,14 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                         bwd_step(P[h], ej < P[h].end && al >= kAlphaMin, al, raw, c, gp[h], w[h]);
                     }
                 };
-                // The buffered hits' sums.  Lane (hit sh, row sr) adds up its eight lane slots as
-                // moments about the square's middle column (dx = bx + i - 3.5 at column i, dy = by0 or
-                // by1 on its two pixel rows), turns them into the hit's gradient values, and the
-                // hit's four lanes reduce-scatter those (xor 16, then xor 8) before the atomics.
-                auto flush = [&](int cnt, int r0) {
-                    __syncwarp();
-                    const float4* b = s_buf[sh] + 8 * sr;
-                    const float4* ga = s_ga + 8 * sr;
-                    const float2* gb = s_gb + 8 * sr;
-                    float S0 = 0.f, S1 = 0.f, X0 = 0.f, X1 = 0.f, XX = 0.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float xi = float(i) - 3.5f;
-                        const float4 v = b[i];  // (gp, gp', w, w') at the slot's two pixels
-                        const float4 g4 = ga[i];
-                        const float2 g2 = gb[i];
-                        S0 += v.x;
-                        S1 += v.y;
-                        X0 = fmaf(v.x, xi, X0);
-                        X1 = fmaf(v.y, xi, X1);
-                        XX = fmaf(v.x + v.y, xi * xi, XX);
-                        C0 = fmaf(v.z, g4.x, fmaf(v.w, g4.w, C0));
-                        C1 = fmaf(v.z, g4.y, fmaf(v.w, g2.x, C1));
-                        C2 = fmaf(v.z, g4.z, fmaf(v.w, g2.y, C2));
-                    }
-                    // lanes past the buffered count compute on stale slots and add nothing
-                    const int j = (r0 + sh) & 31;
-                    const float4 p = s_p[j], q = s_q[j];
-                    const float iop = s_c[j].w;
-                    const float bx = (float(sx) + 3.5f) - p.x;
-                    const float by0 = float(sy + sr) - p.y, by1 = float(sy + sr + 4) - p.y;
-                    const float S = S0 + S1, X = X0 + X1;
-                    const float Sdx = fmaf(bx, S, X);          // sum gp dx
-                    const float Sdx2 = fmaf(bx, Sdx + X, XX);  // sum gp dx^2
-                    const float u0 = by0 * S0, u1 = by1 * S1;
-                    const float Sdy = u0 + u1;                 // sum gp dy
-                    const float Sdy2 = fmaf(by0, u0, by1 * u1);  // sum gp dy^2
-                    const float Sdxdy = fmaf(by0, fmaf(bx, S0, X0), by1 * fmaf(bx, S1, X1));
-                    // the conic from the record's log2-scaled quadratic: A = -2 ln2 qa, B = -ln2 qb, ...
-                    const float A = -2.f * kLn2 * q.x, B = -kLn2 * q.y, C = -2.f * kLn2 * q.z;
-                    // (du, dv, dA, dB, dC, dopacity, dcolour): split into the values rows 0 and 1 keep
-                    // (du, dv, dC, dopacity, db) and those rows 2 and 3 keep (dA, dB, dr, dg)
-                    const float lo[5] = {fmaf(A, Sdx, B * Sdy), fmaf(C, Sdy, B * Sdx), -0.5f * Sdy2, iop * S, C2};
-                    const float hi[5] = {-0.5f * Sdx2, -Sdxdy, C0, C1, 0.f};
-                    const bool r1 = sr & 2, r0b = sr & 1;
-                    float a[5];
-#pragma unroll
-                    for (int k = 0; k < 5; ++k)
-                        a[k] = (r1 ? hi[k] : lo[k]) + __shfl_xor_sync(kFull, r1 ? lo[k] : hi[k], 16);
-                    const float v0 = (r0b ? a[1] : a[0]) + __shfl_xor_sync(kFull, r0b ? a[0] : a[1], 8);
-                    const float v1 = (r0b ? a[3] : a[2]) + __shfl_xor_sync(kFull, r0b ? a[2] : a[3], 8);
-                    const float v2 = (r0b ? 0.f : a[4]) + __shfl_xor_sync(kFull, r0b ? a[4] : 0.f, 8);
-                    if (sh < cnt) {
-                        const size_t gi = __float_as_uint(p.w);
-                        float* const dst0 = sr == 0 ? dm2 : sr == 1 ? dm2 + N : sr == 2 ? dcon : dcon + N;
-                        float* const dst1 = sr == 0 ? dcon + 2 * N : sr == 1 ? dop : sr == 2 ? dcol : dcol + N;
-                        atomicAdd(dst0 + gi, v0);
-                        atomicAdd(dst1 + gi, v1);
-                        if (sr == 0) atomicAdd(dcol + 2 * N + gi, v2);
-                    }
-                    __syncwarp();  // the buffer is read before the next hits overwrite it
-                };
                 // every hit has a composited pixel in this area (the forward's flags); back to front,
-                // each hit's per-pixel values go to the buffer, which is summed when full and at the
-                // batch's end
-                int cnt = 0, r0 = 0;
+                // each hit's per-pixel values go to the buffer, which is summed when full (a partial
+                // buffer is carried to the next batch, and summed at the piece's end)
                 for (int j = 0; j < nh; ++j) {
                     float dx, dy[kBwdPx], gp[kBwdPx], w[kBwdPx];
-                    step(j, dx, dy, gp, w);
+                    step(r0 + cnt, dx, dy, gp, w);
                     s_buf[cnt][lane] = make_float4(gp[0], gp[1], w[0], w[1]);
-                    if (++cnt == kHitBuf || j == nh - 1) {
+                    if (++cnt == kHitBuf) {
                         flush(cnt, r0);
                         r0 += cnt;
                         cnt = 0;
@@ -628,6 +650,8 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                 __syncwarp();  // the slots are read before the next batch overwrites them
                 hi = lo;
             }
+            // the piece's last hits (their sums use this piece's pixels)
+            if (cnt > 0) flush(cnt, r0);
             if (pb >= a1) break;
             // this tile's list ended inside the chunk: the next non-empty list starts at pb (unless
             // pb is the end of the point list)
