@@ -569,9 +569,27 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
             // the buffered hits: slots r0 .. r0 + cnt - 1, buffer rows 0 .. cnt - 1; a buffer not
             // yet full at a batch's end is carried into the next batch
             int cnt = 0, r0 = 0;
+            // each batch's list entries and composited flags are loaded one batch ahead
+            uint32_t g_next = 0u, f_next = 0u;
+            if (warp_end > pa) {
+                const uint32_t lo1 = warp_end - pa > 32u ? warp_end - 32u : pa;
+                if (lo1 + lane < warp_end) {
+                    g_next = list[lo1 + lane];
+                    f_next = compq[lo1 + lane];
+                }
+            }
             for (uint32_t hi = warp_end; hi > pa;) {
                 const uint32_t lo = hi - pa > 32u ? hi - 32u : pa;
                 const uint32_t e = lo + lane;
+                const uint32_t g_cur = g_next, f_cur = f_next;
+                g_next = f_next = 0u;
+                if (lo > pa) {
+                    const uint32_t lo2 = lo - pa > 32u ? lo - 32u : pa;
+                    if (lo2 + lane < lo) {
+                        g_next = list[lo2 + lane];
+                        f_next = compq[lo2 + lane];
+                    }
+                }
                 if (r0 > 0 && cnt > 0) {
                     // the carried hits move to the front slots (r0 >= kHitBuf > cnt: no overlap)
                     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c = a;
@@ -594,8 +612,8 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                 if (e < hi) {
                     // an entry some forward warp of this area composited (its alpha >= 1/255 box
                     // meets the area then too): only those records are loaded
-                    g = list[e];
-                    hit = (uint32_t(compq[e]) & fwarps) != 0u;
+                    g = g_cur;
+                    hit = (f_cur & fwarps) != 0u;
                     if (hit && g >= uint32_t(n)) {
                         atomicOr(&g_raster_check, 1u);  // caller data out of range: the entry is skipped
                         hit = false;
