@@ -443,7 +443,9 @@ int rs_densify_apply(int32_t n, const void* d_workspace, size_t workspace_bytes,
  * call cudaMalloc because an allocation synchronises the device and has unbounded latency.
  * Arguments, outputs and errors are those of rs_bin, except that there is no workspace: the
  * scratch is a fixed array of RS_BIN_NOALLOC_SCRATCH_BYTES bytes that is part of the library's
- * device image.  Every GPU that loads the library holds that array until the process exits.
+ * device image.  A GPU holds that array from the moment the array's module is loaded on it (with
+ * the runtime's lazy module loading, at the first rs_bin_noalloc call on that GPU, see Set-up)
+ * until the process exits.
  *  - Limit: the call returns RS_ERR_WORKSPACE, before any work, when
  *    rs_bin_workspace_size(n, camera, capacity) exceeds RS_BIN_NOALLOC_SCRATCH_BYTES
  *    (48 MiB: about 3.5 million entries for 160,000 Gaussians at 1920x1080).
