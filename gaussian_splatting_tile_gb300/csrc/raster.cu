@@ -1,6 +1,7 @@
-// [3] forward compositing and [4] its backward: one block per 16x16 tile (the forward 256
-// threads, one pixel each; the backward 128 threads, two pixels each), the tile's depth-sorted
-// list staged through shared memory 256 entries at a time.
+// [3] forward compositing and [4] its backward.  The forward runs one block of 128 threads per
+// half of a 16x16 tile, one pixel per thread, the tile's depth-sorted list staged through shared
+// memory 256 entries at a time; the backward runs persistent one-warp blocks, each taking 8x8
+// squares of 256-entry chunks of the point list, two pixels per lane.
 //
 // Forward: rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel" (cooperative
 // fetch, __syncthreads_count vote: the block leaves once all 256 pixels are saturated).

@@ -190,7 +190,8 @@ int rs_bin_async(const rs_camera* camera, const rs_projected* proj, int32_t n, v
 size_t rs_raster_workspace_size(const rs_camera* camera, size_t capacity);
 
 /* [3] Forward compositing, rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel".
- * One thread block per 16x16 tile; each pixel walks its tile's list front to back:
+ * One thread block per half of a 16x16 tile (16x8 pixels); each pixel walks its tile's list
+ * front to back:
  * power = -1/2 (A dx^2 + C dy^2) - B dx dy with (dx, dy) = (x - u, y - v),
  * alpha = min(0.99, opacity exp(power)); entries with alpha < 1/255 are skipped;
  * C += colour alpha T, T *= 1 - alpha; the pixel stops after the entry that brings T below 1e-4.
