@@ -4,7 +4,7 @@
 // squares of 256-entry chunks of the point list, two pixels per lane.
 //
 // Forward: rigel README "Rasterization"; learn-gs "11 - Tiles", "The kernel" (cooperative
-// fetch, __syncthreads_count vote: the block leaves once all 256 pixels are saturated).
+// fetch, __syncthreads_count vote: the block leaves once all its pixels are saturated).
 // Backward: rigel README "Backward": walk each tile back to front from final_T and n_contrib,
 // T_i = T_{i+1} / (1 - a_i), the colour behind carried as a running blend; per-pixel
 // contributions are summed over a warp's 64 pixels (buffered in shared memory and summed by four
