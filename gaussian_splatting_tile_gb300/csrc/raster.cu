@@ -18,6 +18,8 @@
 // failing the threshold at every pixel would do.  n_contrib is kept as a position in the list (one
 // past the entry that stopped the pixel, or the list length), which is exactly the count of
 // examined entries.
+#include <type_traits>
+
 #include "rs_internal.cuh"
 
 namespace rs {
@@ -382,7 +384,9 @@ struct BwdPixel {
 // One entry at one pixel: updates the pixel's state; returns gp = dL/dpower (0 if clamped) and
 // w = alpha T_j.  Branch-free: a pixel the entry does not reach (act false) takes alpha as 0, so
 // SG + 0 d = SG and w = gp = 0, and keeps T through the select; an active pixel gets exactly the
-// arithmetic of the recurrence.
+// arithmetic of the recurrence.  CLAMP false: the caller knows raw < kAlphaMax (see
+// kNoClampOpacity), so no clamp test.
+template <bool CLAMP>
 __device__ __forceinline__ void bwd_step(BwdPixel& px, bool act, float alpha, float raw, const float4& c,
                                          float& gp, float& w) {
     const float a = act ? alpha : 0.f;
@@ -393,8 +397,15 @@ __device__ __forceinline__ void bwd_step(BwdPixel& px, bool act, float alpha, fl
     const float d = cG - px.SG;
     px.SG = fmaf(a, d, px.SG);
     px.T = Tj;
-    gp = raw <= kAlphaMax ? w * d : 0.f;  // alpha dL/dalpha; not clamped: alpha = opacity exp(power)
+    // alpha dL/dalpha where not clamped (alpha = opacity exp(power))
+    gp = !CLAMP || raw <= kAlphaMax ? w * d : 0.f;
 }
+
+// An entry of opacity at most this cannot reach the 0.99 clamp at any pixel: opacity exp(power)
+// with power <= 0 stays below it even when rounding leaves the evaluated exponent slightly
+// positive (by less than log2(0.99 / 0.98) = 0.0146), so min(0.99, raw) = raw there, as in the
+// forward, and the clamp test can be skipped.
+constexpr float kNoClampOpacity = 0.98f;
 
 __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_raster_bwd(
     CameraF cam, int n, const Record* __restrict__ rec, const uint2* __restrict__ ranges,
@@ -645,13 +656,19 @@ __global__ void __launch_bounds__(kBwdThreads, RS_BWD_MIN_BLOCKS * kBwdWarps) k_
                     dx = fx - p.x;
                     const float bx = q.y * dx, axx = (q.x * dx) * dx;
                     const float4 c = s_c[j];
+                    auto pixels = [&](auto clamp) {
 #pragma unroll
-                    for (int h = 0; h < kBwdPx; ++h) {
-                        dy[h] = (fy0 + float(4 * h)) - p.y;
-                        const float raw = p.z * ex2_approx(fmaf(dy[h], fmaf(q.z, dy[h], bx), axx));
-                        const float al = fminf(kAlphaMax, raw);
-                        bwd_step(P[h], ej < P[h].end && al >= kAlphaMin, al, raw, c, gp[h], w[h]);
-                    }
+                        for (int h = 0; h < kBwdPx; ++h) {
+                            dy[h] = (fy0 + float(4 * h)) - p.y;
+                            const float raw = p.z * ex2_approx(fmaf(dy[h], fmaf(q.z, dy[h], bx), axx));
+                            const float al = decltype(clamp)::value ? fminf(kAlphaMax, raw) : raw;
+                            bwd_step<decltype(clamp)::value>(P[h], ej < P[h].end && al >= kAlphaMin, al, raw, c,
+                                                             gp[h], w[h]);
+                        }
+                    };
+                    // the branch is the same for the whole warp (one entry)
+                    if (p.z <= kNoClampOpacity) pixels(std::false_type{});
+                    else pixels(std::true_type{});
                 };
                 // every hit has a composited pixel in this area (the forward's flags); back to front,
                 // each hit's per-pixel values go to the buffer, which is summed when full (a partial
