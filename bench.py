@@ -69,7 +69,7 @@ B_BIN_PER_G = 8 + 4 * 16 + 8 + 40
 B_BIN_PER_ENTRY_FIXED, B_BIN_PER_ENTRY_PASS = 12, 16
 # DRAM bytes (read + write) of one k_raster_bwd launch on orbit view 1, from an ncu --set full
 # capture of the current kernel; must be re-taken (or set to None) whenever the kernel changes
-TRAFFIC_RASTER_BWD_BYTES = 46.210304e6 + 0.267776e6
+TRAFFIC_RASTER_BWD_BYTES = 46.209792e6 + 0.306688e6
 TRAFFIC_RASTER_BWD_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of k_raster_bwd, "
                              "160k scene, 1920x1080 orbit view 1")
 
