@@ -180,7 +180,7 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, 
     const bool inside = px < cam.W && py < cam.H;
     const float fx = float(px), fy = float(py);
     float T = 1.f, C0 = 0.f, C1 = 0.f, C2 = 0.f;
-    float D0 = 0.f, D1 = 0.f, D2 = 0.f;  // colour added since the last chunk boundary
+    float D0 = 0.f, D1 = 0.f, D2 = 0.f;  // colour added since the last chunk boundary (SPLIT)
     uint32_t stop = range.y;  // one past the last entry this pixel examined
     bool done = !inside;
     const uint32_t wbit = 1u << warp;
@@ -193,6 +193,10 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, 
         bend = min(range.y, (base / kChunk + 1) * kChunk);
         if (SPLIT && base != range.x && !done) {
             if (base / kChunk < slots) ckpt[size_t(base / kChunk) * kTilePixels + lidx] = make_float4(D0, D1, D2, T);
+            // the finished stretch joins the colour in front
+            C0 += D0;
+            C1 += D1;
+            C2 += D2;
             D0 = D1 = D2 = 0.f;
         }
         // every thread reaches this barrier; the block leaves once all its pixels are done
@@ -238,13 +242,16 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, 
             sm.comp[warp][j] = 1u;  // every lane that composites stores the same flag
             const float4 c = sm.c[j];
             const float w = alpha * T;
-            C0 = fmaf(c.x, w, C0);
-            C1 = fmaf(c.y, w, C1);
-            C2 = fmaf(c.z, w, C2);
+            // a tile whose list crosses chunk boundaries sums the current stretch only (it joins
+            // the colour in front at the stretch's end)
             if (SPLIT) {
                 D0 = fmaf(c.x, w, D0);
                 D1 = fmaf(c.y, w, D1);
                 D2 = fmaf(c.z, w, D2);
+            } else {
+                C0 = fmaf(c.x, w, C0);
+                C1 = fmaf(c.y, w, C1);
+                C2 = fmaf(c.z, w, C2);
             }
             T = fmaf(-T, alpha, T);
             if (T < kTStop) {
@@ -278,9 +285,10 @@ __device__ __forceinline__ void raster_fwd_tile(const CameraF& cam, uint32_t n, 
         if (pbase + uint32_t(t) < pend) comp[pbase + t] = comp_byte(sm, t);
     if (inside) {
         const size_t HW = size_t(cam.W) * cam.H, pix = size_t(py) * cam.W + px;
-        image[pix] = fmaf(T, bg.x, C0);
-        image[HW + pix] = fmaf(T, bg.y, C1);
-        image[2 * HW + pix] = fmaf(T, bg.z, C2);
+        // (D is the last stretch's colour with SPLIT, else 0)
+        image[pix] = fmaf(T, bg.x, C0 + D0);
+        image[HW + pix] = fmaf(T, bg.y, C1 + D1);
+        image[2 * HW + pix] = fmaf(T, bg.z, C2 + D2);
         final_T[pix] = T;
         n_contrib[pix] = stop - range.x;
         // the backward resumes at each recorded boundary b with the colour behind it,

@@ -280,8 +280,11 @@ def test_ellipse_tile_test(which):
         assert np.array_equal(el[k][..., vis], sq[k][..., vis])
     o = g.opacity.astype(np.float64)[vis]
     P.allclose_report("alpha_k", el["alpha_k"][vis], 2.002 * np.log(255 * o), 1e-6, 1e-6)
-    # the same image, and gradients up to summation order
-    assert np.array_equal(el["image"], sq["image"]) and np.array_equal(el["final_T"], sq["final_T"])
+    # the same transmittance, the same colour up to the rounding of its sums (a tile whose list
+    # crosses 256-entry chunk boundaries sums its colour per stretch between them, and the
+    # stretches fall at other entries when the lists differ), and gradients up to summation order
+    assert np.array_equal(el["final_T"], sq["final_T"])
+    P.allclose_report("image", el["image"], sq["image"], 1e-6, 1e-6)
     assert (el["n_contrib"] <= sq["n_contrib"]).all()
     # both are float32 sums over tiles in no fixed order; where those sums cancel, their rounding
     # scales with the terms, not the result, so the absolute part is 1e-5 of the largest gradient
