@@ -368,7 +368,9 @@ __global__ void __launch_bounds__(kFwdThreads, RS_FWD_MIN_BLOCKS) k_raster_fwd(C
 // four pixels per lane on 8x16 areas; four-warp blocks, one per chunk (0.195 against 0.177 ms for
 // one-warp persistent blocks: a block's warps finish at different times and its slot waits for
 // the last); a third form of the step for entries below every pixel's end (no end test: 126.2
-// against 125.0 M instructions, no faster); the two pixels' arithmetic and the buffer sums in
+// against 125.0 M instructions, no faster); a piece's pixel inputs (n_contrib, dL/dC, final_T
+// and the checkpoint) all loaded at once instead of after n_contrib (0.159 -> 0.161 ms); the two
+// pixels' arithmetic and the buffer sums in
 // paired fp32 instructions (f32x2:
 // 9% fewer instructions, but issue fell from 74% to 65% of cycles and the kernel took 187 against
 // 176 us; the buffer sums alone: 6% fewer, the same time); the items taken heaviest first (a
